@@ -1,0 +1,17 @@
+"""FP64 CPU oracle for normalised causal linear attention (test infrastructure).
+
+Only the tests, the smoke check and the benchmark's CPU-baseline leg import this
+package.  The product library never links, loads or calls it, and this package
+imports nothing from the product.
+"""
+from .oracle import (  # noqa: F401
+    PHI_ELU1,
+    PHI_IDENTITY,
+    PHI_RELU1,
+    build,
+    chunkwise,
+    dense,
+    num_cpus,
+    scan,
+    variant,
+)

@@ -1,0 +1,102 @@
+"""Seeded synthetic inputs for the linear-attention path.
+
+This module only draws random numbers and lays them out; it contains none of
+the method's arithmetic.  Both the CUDA path (tests, benchmark) and the CPU
+oracle (tests) are fed from it, so that both sides see identical bits.
+
+Recipe: torch CPU generator seeded per workload; normal draws in FP32 (FP64
+for the tiny FP64 workload), scaled, then rounded once to the workload dtype.
+Gates are alpha = sigmoid(g), g ~ N(mu, sigma), computed in FP64 and rounded to
+FP32; the gate is an input of the method, given per head and per token.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass, replace
+
+import torch
+
+
+@dataclass(frozen=True)
+class Workload:
+    name: str
+    B: int
+    H: int
+    T: int
+    r: int = 128
+    dv: int = 128
+    dtype: torch.dtype = torch.bfloat16
+    scale: float = 1.0          # standard deviation of q, k, v
+    gated: bool = False         # alpha = sigmoid(N(gate_mu, gate_sigma)) per head and token
+    gate_mu: float = 3.0
+    gate_sigma: float = 1.0
+    chunk: int = 64
+    eps: float = 1e-6
+    seed: int = 0
+    decode: bool = False        # one token per request on a pre-existing state
+    draw_fp64: bool = False     # draw in FP64 before rounding to ``dtype``
+
+    @property
+    def token_heads(self) -> int:
+        return self.B * self.H * self.T
+
+    def with_(self, **kw) -> "Workload":
+        return replace(self, **kw)
+
+
+# The five workloads of the method's measurement plan, seeds 0..4 in this order.
+TINY = Workload("tiny B1 H1 T64 r=dv=16 fp64->fp32", B=1, H=1, T=64, r=16, dv=16,
+                dtype=torch.float32, draw_fp64=True, seed=0)
+UNGATED = Workload("prefill B4 H16 T4096 d128 bf16 C64", B=4, H=16, T=4096, seed=1)
+GATED = Workload("gated prefill B2 H16 T16384 d128 bf16 alpha=sigmoid(N(3,1))", B=2, H=16,
+                 T=16384, gated=True, seed=2)
+DECODE = Workload("decode B256 H16 r=dv=128 bf16 qkv, fp32 state", B=256, H=16, T=1,
+                  decode=True, seed=3)
+LONG = Workload("long prefill B1 H32 T65536 d128 bf16 sigma=2 C64", B=1, H=32, T=65536,
+                scale=2.0, seed=4)
+WORKLOADS = {"tiny": TINY, "ungated": UNGATED, "gated": GATED, "decode": DECODE, "long": LONG}
+
+
+def prefill_inputs(w: Workload, device="cpu", with_state: bool = False, seed: int | None = None):
+    """q, k [B,H,T,r], v [B,H,T,dv] in ``w.dtype``; alpha [B,H,T] FP32 or None;
+    S0 [B,H,r,dv], z0 [B,H,r] FP32 (only when ``with_state``, else None).
+    The carried-in state, when asked for, is the one of a decode request:
+    S0 ~ N(0,1)*0.1 and z0 ~ U(1,100)."""
+    g = torch.Generator().manual_seed(w.seed if seed is None else seed)
+    draw_dtype = torch.float64 if w.draw_fp64 else torch.float32
+    shape_qk = (w.B, w.H, w.T, w.r)
+    shape_v = (w.B, w.H, w.T, w.dv)
+    q = (torch.randn(shape_qk, generator=g, dtype=draw_dtype) * w.scale).to(w.dtype)
+    k = (torch.randn(shape_qk, generator=g, dtype=draw_dtype) * w.scale).to(w.dtype)
+    v = (torch.randn(shape_v, generator=g, dtype=draw_dtype) * w.scale).to(w.dtype)
+    alpha = None
+    if w.gated:
+        gl = torch.randn((w.B, w.H, w.T), generator=g, dtype=torch.float64) * w.gate_sigma + w.gate_mu
+        alpha = torch.sigmoid(gl).to(torch.float32)
+    S0 = z0 = None
+    if with_state:
+        S0 = torch.randn((w.B, w.H, w.r, w.dv), generator=g, dtype=torch.float32) * 0.1
+        z0 = torch.rand((w.B, w.H, w.r), generator=g, dtype=torch.float32) * 99.0 + 1.0
+    out = dict(q=q, k=k, v=v, alpha=alpha, S0=S0, z0=z0)
+    if device != "cpu":
+        out = {n: (t.to(device) if t is not None else None) for n, t in out.items()}
+    return out
+
+
+def decode_inputs(w: Workload, device="cpu", seed: int | None = None):
+    """One token per request: q, k [B,H,1,r], v [B,H,1,dv] in ``w.dtype``;
+    pre-existing state S [B,H,r,dv] ~ N(0,1)*0.1 and z [B,H,r] ~ U(1,100), FP32;
+    alpha [B,H] FP32 when gated, else None."""
+    g = torch.Generator().manual_seed(w.seed if seed is None else seed)
+    q = torch.randn((w.B, w.H, 1, w.r), generator=g, dtype=torch.float32).mul(w.scale).to(w.dtype)
+    k = torch.randn((w.B, w.H, 1, w.r), generator=g, dtype=torch.float32).mul(w.scale).to(w.dtype)
+    v = torch.randn((w.B, w.H, 1, w.dv), generator=g, dtype=torch.float32).mul(w.scale).to(w.dtype)
+    S = torch.randn((w.B, w.H, w.r, w.dv), generator=g, dtype=torch.float32) * 0.1
+    z = torch.rand((w.B, w.H, w.r), generator=g, dtype=torch.float32) * 99.0 + 1.0
+    alpha = None
+    if w.gated:
+        gl = torch.randn((w.B, w.H), generator=g, dtype=torch.float64) * w.gate_sigma + w.gate_mu
+        alpha = torch.sigmoid(gl).to(torch.float32)
+    out = dict(q=q, k=k, v=v, alpha=alpha, S=S, z=z)
+    if device != "cpu":
+        out = {n: (t.to(device) if t is not None else None) for n, t in out.items()}
+    return out
