@@ -1,0 +1,153 @@
+/*
+ * linattn.h -- C ABI of the GB300 (sm_103a) library for normalised causal
+ * linear attention with a positive feature map and a recurrent S/z state.
+ *
+ * The method (sources cited by page title and section):
+ *   [LA] "Linear attention：把历史写进状态" (hs-black.github.io/posts/linear-attention)
+ *   [LC] "45. Linear Attention and Recurrent State | 线性注意力与递推状态" (datawhalechina, ch. 45)
+ *
+ *   phi(x)  = ELU(x) + 1  (x + 1 for x > 0, e^x otherwise)        [LA] "关键改写：让求和先发生"
+ *   S_t     = alpha_t S_{t-1} + phi(k_t) v_t^T                     [LA] "公式里的每个维度",
+ *   z_t     = alpha_t z_{t-1} + phi(k_t)                                "加一个门：让旧记忆逐渐淡出"
+ *   y_t     = phi(q_t)^T S_t / (phi(q_t)^T z_t + eps)              [LA] "ε 是数值保护"
+ * The state is updated before it is read, so y_t sees token t ([LA]
+ * "每来一个 token，更新两个累加器"; [LC] TODO 3).  alpha_t == 1 is the ungated
+ * form.  Prefill evaluates the recurrence chunk by chunk ([LA] "一个 chunk 的输出由
+ * 两部分组成"); decode applies one step of it to a stored state ([LA]
+ * "训练时，状态更新也能按块并行": the token recurrence suits decode).
+ *
+ * Conventions shared by every entry point:
+ *  - Pointers marked "device" are CUDA device (or managed) memory owned by the
+ *    caller; all arrays are dense, row-major and contiguous.  The library keeps
+ *    no pointer after a call returns and allocates no device memory.
+ *  - Work is enqueued on `stream` (a cudaStream_t; NULL is the legacy default
+ *    stream).  No call synchronises except la_last_device_status.
+ *  - Errors are return codes.  Argument errors are detected on the host before
+ *    anything is enqueued, and leave every output untouched.  LA_ERR_CUDA
+ *    reports a failed launch or an earlier asynchronous CUDA error; kernels that
+ *    give up waiting on an on-chip barrier record LA_ERR_TIMEOUT in a device
+ *    status word that la_last_device_status reads.
+ *  - Element types: q, k, v and y share `dtype` (BF16 or FP32).  States S, z and
+ *    gates alpha are always FP32.  Arithmetic is FP32 with FP32 accumulation;
+ *    on the BF16 path the features phi(q), phi(k) and the in-chunk score matrix
+ *    enter the tensor cores as BF16.
+ */
+#ifndef LINATTN_H
+#define LINATTN_H
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t. */
+typedef struct CUstream_st *la_stream_t;
+
+typedef enum {
+    LA_OK = 0,
+    LA_ERR_NULL = 1,        /* a required pointer is NULL                                      */
+    LA_ERR_SHAPE = 2,       /* a size is < 1, out of range, or sizes disagree                    */
+    LA_ERR_DTYPE = 3,       /* unknown element type                                            */
+    LA_ERR_ALIGN = 4,       /* a pointer is not aligned as the chosen kernel requires           */
+    LA_ERR_UNSUPPORTED = 5, /* a valid request that this build does not implement              */
+    LA_ERR_CUDA = 6,        /* a CUDA runtime call or launch failed                            */
+    LA_ERR_TIMEOUT = 7,     /* a kernel gave up waiting on an on-chip barrier                   */
+    LA_ERR_WORKSPACE = 8    /* workspace smaller than la_prefill_workspace_bytes, or NULL      */
+} la_status;
+
+typedef enum { LA_DTYPE_BF16 = 0, LA_DTYPE_FP32 = 1 } la_dtype;
+
+/*
+ * la_state_init -- S = 0, z = 0 (the empty history; [LA] "每来一个 token，更新两个累加器":
+ * the state starts from S0 = 0, z0 = 0; [LC] the zero-initialised state and normaliser).
+ *   S  device, FP32 [B,H,r,dv]  (row i = feature index, column j = value index)
+ *   z  device, FP32 [B,H,r]
+ * Requires B, H, r, dv >= 1.  Errors: LA_ERR_NULL, LA_ERR_SHAPE, LA_ERR_CUDA.
+ */
+la_status la_state_init(float *S, float *z, int B, int H, int r, int dv, la_stream_t stream);
+
+/*
+ * la_prefill_workspace_bytes -- device scratch that la_prefill_chunked needs for
+ * these sizes.  The current kernels keep every intermediate on chip, so this is
+ * 0; callers should still ask and pass a buffer of that size.
+ */
+size_t la_prefill_workspace_bytes(int B, int H, int T, int r, int dv, int chunk);
+
+/*
+ * la_prefill_chunked -- run T tokens of every (b, h) sequence through the
+ * recurrence, starting from (S0, z0), and return every output y_t and the final
+ * state ([LA] "一个 chunk 的输出由两部分组成": per chunk, the read of the carried
+ * state Q~c Sprev plus the masked in-chunk product [(Q~c K~c^T) . M] Vc, the same
+ * two parts for the denominator, and the hand-off Snext, znext; with a gate, each
+ * term is scaled by the product of the gates between its write and its read).
+ *
+ *   q, k   device [B,H,T,r]  dtype          v, y   device [B,H,T,dv]  dtype
+ *   alpha  device FP32 [B,H,T], 0 <= alpha <= 1, or NULL for alpha == 1.
+ *          alpha_t scales the state carried into token t (alpha of the first
+ *          token scales S0, z0).
+ *   S0     device FP32 [B,H,r,dv] or NULL (zero);  z0 device FP32 [B,H,r] or NULL.
+ *          S0 may equal S_out and z0 may equal z_out (in-place continuation).
+ *   S_out  device FP32 [B,H,r,dv] final state;  z_out device FP32 [B,H,r].
+ *   eps    added once to the whole denominator: y = num / (den + eps).
+ *   chunk  chunk length in tokens.  The result does not depend on it beyond
+ *          rounding ([LA] "动手实验": chunk boundaries do not change the semantics).
+ *   workspace, workspace_bytes: at least la_prefill_workspace_bytes(...) bytes
+ *          (may be NULL when that is 0).
+ *
+ * Kernels:
+ *   BF16: tensor-core kernel (tcgen05 MMAs with TMEM accumulators, TMA tile
+ *         loads and stores).  Requires r == 128, dv in {64, 128}, chunk == 64,
+ *         q, k, v, y 16-byte aligned.
+ *   FP32: exact FP32 token recurrence on CUDA cores (chunk is not used).
+ *         Requires 1 <= r <= 128, 1 <= dv <= 128, 4-byte alignment.
+ * T may be any length >= 1 (a final partial chunk is masked).
+ * Errors: LA_ERR_NULL, LA_ERR_SHAPE (B, H, T, r, dv or chunk < 1), LA_ERR_DTYPE,
+ *         LA_ERR_ALIGN, LA_ERR_UNSUPPORTED, LA_ERR_WORKSPACE, LA_ERR_CUDA.
+ */
+la_status la_prefill_chunked(const void *q, const void *k, const void *v, la_dtype dtype,
+                             const float *alpha, const float *S0, const float *z0,
+                             int B, int H, int T, int r, int dv, int chunk, float eps,
+                             void *y, float *S_out, float *z_out,
+                             void *workspace, size_t workspace_bytes, la_stream_t stream);
+
+/*
+ * la_decode_step -- one new token per (b, h), state updated in place:
+ *   S <- alpha S + phi(k) v^T,  z <- alpha z + phi(k),  y = phi(q)^T S / (phi(q)^T z + eps)
+ * ([LA] "公式里的每个维度" and "查询时，分子和分母一起读"; update before read).
+ *   q, k   device [B,H,1,r] dtype;  v, y device [B,H,1,dv] dtype
+ *   alpha  device FP32 [B,H] or NULL (alpha == 1)
+ *   S      device FP32 [B,H,r,dv], read and overwritten;  z device FP32 [B,H,r], likewise.
+ * Requires 1 <= r <= 256, 1 <= dv <= 256; 4-byte alignment (the r = dv = 128 fast
+ * path is taken when S is 16-byte aligned).
+ * Errors: LA_ERR_NULL, LA_ERR_SHAPE, LA_ERR_DTYPE, LA_ERR_ALIGN, LA_ERR_UNSUPPORTED, LA_ERR_CUDA.
+ */
+la_status la_decode_step(const void *q, const void *k, const void *v, la_dtype dtype,
+                         const float *alpha, float *S, float *z, int B, int H, int r, int dv,
+                         float eps, void *y, la_stream_t stream);
+
+/*
+ * la_last_device_status -- synchronise `stream`, then read and clear the device
+ * status word of the current device: LA_OK, or LA_ERR_TIMEOUT when a kernel
+ * gave up waiting on an on-chip barrier since the last read.  Returns
+ * LA_ERR_CUDA when the synchronisation itself reports an error.
+ */
+la_status la_last_device_status(la_stream_t stream);
+
+/* la_status_string -- a static, human-readable name for a status code. */
+const char *la_status_string(la_status status);
+
+/*
+ * la_debug_wait_probe -- diagnostic: launches one block that waits on an
+ * on-chip barrier that nothing ever completes, with a limit of `limit_ns`
+ * nanoseconds (at most 1e9).  The wait runs out and records LA_ERR_TIMEOUT in the
+ * device status word exactly as a stuck kernel would; the context stays usable.
+ * Used to test the timeout path without faulting or hanging a GPU.
+ */
+la_status la_debug_wait_probe(unsigned long long limit_ns, la_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LINATTN_H */

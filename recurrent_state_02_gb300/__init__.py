@@ -1,0 +1,122 @@
+"""GB300 (sm_103a) normalised causal linear attention with a recurrent S/z state.
+
+    phi(x) = ELU(x) + 1
+    S_t = alpha_t S_{t-1} + phi(k_t) v_t^T,   z_t = alpha_t z_{t-1} + phi(k_t)
+    y_t = phi(q_t)^T S_t / (phi(q_t)^T z_t + eps)
+
+Every step runs in the CUDA kernels of liblinattn.so, reached through its C ABI
+(include/linattn.h).  The functions below only check tensor metadata, allocate
+outputs with torch, and pass raw device pointers and the current CUDA stream;
+PyTorch supplies device memory and streams, nothing else.
+"""
+from __future__ import annotations
+
+import torch
+
+from . import _native
+from ._native import LinAttnError  # noqa: F401
+
+_DTYPES = {torch.bfloat16: _native.LA_DTYPE_BF16, torch.float32: _native.LA_DTYPE_FP32}
+
+
+def _ptr(t):
+    return None if t is None else t.data_ptr()
+
+
+def _stream(device):
+    return torch.cuda.current_stream(device).cuda_stream
+
+
+def _require(t, name, shape, dtype, device):
+    if t is None:
+        return
+    if not t.is_cuda or t.device != device:
+        raise ValueError(f"{name} must be on {device}")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+    if t.dtype != dtype:
+        raise ValueError(f"{name} has dtype {t.dtype}, expected {dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def state_init(B, H, r, dv, device="cuda", S=None, z=None):
+    """Zero state: returns (S [B,H,r,dv], z [B,H,r]) in FP32."""
+    device = torch.device(device)
+    if S is None:
+        S = torch.empty((B, H, r, dv), device=device, dtype=torch.float32)
+    if z is None:
+        z = torch.empty((B, H, r), device=device, dtype=torch.float32)
+    _require(S, "S", (B, H, r, dv), torch.float32, S.device)
+    _require(z, "z", (B, H, r), torch.float32, S.device)
+    _native.check(_native.lib().la_state_init(_ptr(S), _ptr(z), B, H, r, dv, _stream(S.device)), "la_state_init")
+    return S, z
+
+
+def prefill_workspace_bytes(B, H, T, r, dv, chunk=64) -> int:
+    return int(_native.lib().la_prefill_workspace_bytes(B, H, T, r, dv, chunk))
+
+
+def prefill_chunked(q, k, v, alpha=None, S0=None, z0=None, chunk=64, eps=1e-6, y=None, S_out=None, z_out=None,
+                    workspace=None):
+    """Chunkwise prefill.  q, k [B,H,T,r], v [B,H,T,dv] (bf16 or fp32, same dtype);
+    alpha [B,H,T] fp32 or None; S0 [B,H,r,dv], z0 [B,H,r] fp32 or None.
+    Returns (y [B,H,T,dv] in the input dtype, S_T, z_T)."""
+    if q.dtype not in _DTYPES:
+        raise ValueError(f"unsupported dtype {q.dtype}")
+    B, H, T, r = q.shape
+    dv = v.shape[3]
+    dev = q.device
+    _require(q, "q", (B, H, T, r), q.dtype, dev)
+    _require(k, "k", (B, H, T, r), q.dtype, dev)
+    _require(v, "v", (B, H, T, dv), q.dtype, dev)
+    _require(alpha, "alpha", (B, H, T), torch.float32, dev)
+    _require(S0, "S0", (B, H, r, dv), torch.float32, dev)
+    _require(z0, "z0", (B, H, r), torch.float32, dev)
+    if y is None:
+        y = torch.empty((B, H, T, dv), device=dev, dtype=q.dtype)
+    if S_out is None:
+        S_out = torch.empty((B, H, r, dv), device=dev, dtype=torch.float32)
+    if z_out is None:
+        z_out = torch.empty((B, H, r), device=dev, dtype=torch.float32)
+    _require(y, "y", (B, H, T, dv), q.dtype, dev)
+    _require(S_out, "S_out", (B, H, r, dv), torch.float32, dev)
+    _require(z_out, "z_out", (B, H, r), torch.float32, dev)
+    need = prefill_workspace_bytes(B, H, T, r, dv, chunk)
+    if need and workspace is None:
+        workspace = torch.empty(need, device=dev, dtype=torch.uint8)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    st = _native.lib().la_prefill_chunked(
+        _ptr(q), _ptr(k), _ptr(v), _DTYPES[q.dtype], _ptr(alpha), _ptr(S0), _ptr(z0), B, H, T, r, dv, chunk,
+        float(eps), _ptr(y), _ptr(S_out), _ptr(z_out), _ptr(workspace), ws_bytes, _stream(dev))
+    _native.check(st, "la_prefill_chunked")
+    return y, S_out, z_out
+
+
+def decode_step(q, k, v, S, z, alpha=None, eps=1e-6, y=None):
+    """One token per request, state updated in place.  q, k [B,H,1,r], v [B,H,1,dv];
+    S [B,H,r,dv], z [B,H,r] fp32 (overwritten); alpha [B,H] fp32 or None.  Returns y [B,H,1,dv]."""
+    if q.dtype not in _DTYPES:
+        raise ValueError(f"unsupported dtype {q.dtype}")
+    B, H, one, r = q.shape
+    dv = v.shape[3]
+    dev = q.device
+    if one != 1:
+        raise ValueError("decode takes one token per request")
+    _require(k, "k", (B, H, 1, r), q.dtype, dev)
+    _require(v, "v", (B, H, 1, dv), q.dtype, dev)
+    _require(S, "S", (B, H, r, dv), torch.float32, dev)
+    _require(z, "z", (B, H, r), torch.float32, dev)
+    _require(alpha, "alpha", (B, H), torch.float32, dev)
+    if y is None:
+        y = torch.empty((B, H, 1, dv), device=dev, dtype=q.dtype)
+    _require(y, "y", (B, H, 1, dv), q.dtype, dev)
+    st = _native.lib().la_decode_step(_ptr(q), _ptr(k), _ptr(v), _DTYPES[q.dtype], _ptr(alpha), _ptr(S), _ptr(z),
+                                      B, H, r, dv, float(eps), _ptr(y), _stream(dev))
+    _native.check(st, "la_decode_step")
+    return y
+
+
+def last_device_status(device="cuda") -> int:
+    """Synchronises the current stream and returns (and clears) the device status word."""
+    return int(_native.lib().la_last_device_status(_stream(torch.device(device))))

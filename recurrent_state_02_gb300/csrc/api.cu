@@ -1,0 +1,184 @@
+// api.cu -- the C ABI declared in include/linattn.h: argument validation,
+// kernel selection, TMA descriptor set-up and the device status word.
+#include "../../include/linattn.h"
+#include "kernels.h"
+
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace {
+
+// Device status word: 0, or the la_status of the last failure a kernel recorded.
+__device__ int g_status = 0;
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                  const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn()
+{
+    static EncodeTiledFn fn = nullptr;
+    if (!fn) {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    }
+    return fn;
+}
+
+// 3-D BF16 view [planes, rows, cols] (cols innermost), 64 x 64 boxes, 128-byte
+// swizzle; rows past the end of a plane read as zero and are never written.
+bool make_map_bf16(CUtensorMap *map, const void *ptr, long long planes, long long rows, long long cols)
+{
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    const cuuint64_t dims[3] = {(cuuint64_t)cols, (cuuint64_t)rows, (cuuint64_t)planes};
+    const cuuint64_t strides[2] = {(cuuint64_t)cols * 2, (cuuint64_t)cols * rows * 2};
+    const cuuint32_t box[3] = {64, 64, 1};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(ptr), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+int *status_word()
+{
+    void *p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_status) != cudaSuccess) return nullptr;
+    return static_cast<int *>(p);
+}
+
+bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+la_status from_cuda(cudaError_t e) { return e == cudaSuccess ? LA_OK : LA_ERR_CUDA; }
+
+}  // namespace
+
+extern "C" {
+
+const char *la_status_string(la_status s)
+{
+    switch (s) {
+    case LA_OK: return "LA_OK";
+    case LA_ERR_NULL: return "LA_ERR_NULL: a required pointer is NULL";
+    case LA_ERR_SHAPE: return "LA_ERR_SHAPE: a size is out of range or sizes disagree";
+    case LA_ERR_DTYPE: return "LA_ERR_DTYPE: unknown element type";
+    case LA_ERR_ALIGN: return "LA_ERR_ALIGN: a pointer is not aligned as the kernel requires";
+    case LA_ERR_UNSUPPORTED: return "LA_ERR_UNSUPPORTED: request not implemented by this build";
+    case LA_ERR_CUDA: return "LA_ERR_CUDA: a CUDA runtime call or launch failed";
+    case LA_ERR_TIMEOUT: return "LA_ERR_TIMEOUT: a kernel gave up waiting on an on-chip barrier";
+    case LA_ERR_WORKSPACE: return "LA_ERR_WORKSPACE: workspace too small";
+    }
+    return "unknown la_status";
+}
+
+la_status la_state_init(float *S, float *z, int B, int H, int r, int dv, la_stream_t stream)
+{
+    if (!S || !z) return LA_ERR_NULL;
+    if (B < 1 || H < 1 || r < 1 || dv < 1) return LA_ERR_SHAPE;
+    if (!aligned(S, 4) || !aligned(z, 4)) return LA_ERR_ALIGN;
+    const long long nz = (long long)B * H * r, nS = nz * dv;
+    return from_cuda(la::launch_state_init(S, z, nS, nz, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+size_t la_prefill_workspace_bytes(int B, int H, int T, int r, int dv, int chunk)
+{
+    (void)B; (void)H; (void)T; (void)r; (void)dv; (void)chunk;
+    return 0;
+}
+
+la_status la_prefill_chunked(const void *q, const void *k, const void *v, la_dtype dtype, const float *alpha,
+                             const float *S0, const float *z0, int B, int H, int T, int r, int dv, int chunk,
+                             float eps, void *y, float *S_out, float *z_out, void *workspace,
+                             size_t workspace_bytes, la_stream_t stream)
+{
+    (void)workspace;
+    if (!q || !k || !v || !y || !S_out || !z_out) return LA_ERR_NULL;
+    if (B < 1 || H < 1 || T < 1 || r < 1 || dv < 1 || chunk < 1) return LA_ERR_SHAPE;
+    if (dtype != LA_DTYPE_BF16 && dtype != LA_DTYPE_FP32) return LA_ERR_DTYPE;
+    if (workspace_bytes < la_prefill_workspace_bytes(B, H, T, r, dv, chunk)) return LA_ERR_WORKSPACE;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+
+    if (dtype == LA_DTYPE_FP32) {
+        if (r > 128 || dv > 128) return LA_ERR_UNSUPPORTED;
+        const void *ptrs[] = {q, k, v, y, S_out, z_out, alpha, S0, z0};
+        for (const void *p : ptrs)
+            if (p && !aligned(p, 4)) return LA_ERR_ALIGN;
+        return from_cuda(la::launch_prefill_f32(static_cast<const float *>(q), static_cast<const float *>(k),
+                                                static_cast<const float *>(v), alpha, S0, z0, B, H, T, r, dv, eps,
+                                                static_cast<float *>(y), S_out, z_out, st));
+    }
+
+    // BF16: tensor-core kernel
+    if (r != 128 || (dv != 64 && dv != 128) || chunk != 64) return LA_ERR_UNSUPPORTED;
+    if ((long long)B * H > 0x7fffffffLL) return LA_ERR_SHAPE;
+    {
+        const void *ptrs16[] = {q, k, v, y, S_out};
+        for (const void *p : ptrs16)
+            if (!aligned(p, 16)) return LA_ERR_ALIGN;
+        const void *ptrs4[] = {alpha, S0, z0, z_out};
+        for (const void *p : ptrs4)
+            if (p && !aligned(p, 4)) return LA_ERR_ALIGN;
+    }
+    int *status = status_word();
+    if (!status) return LA_ERR_CUDA;
+    CUtensorMap mq, mk, mv, my;
+    const long long planes = (long long)B * H;
+    if (!make_map_bf16(&mq, q, planes, T, r) || !make_map_bf16(&mk, k, planes, T, r) ||
+        !make_map_bf16(&mv, v, planes, T, dv) || !make_map_bf16(&my, y, planes, T, dv))
+        return LA_ERR_CUDA;
+    la::PrefillTcArgs a;
+    a.alpha = alpha;
+    a.S0 = S0;
+    a.z0 = z0;
+    a.S_out = S_out;
+    a.z_out = z_out;
+    a.H = H;
+    a.T = T;
+    a.dv = dv;
+    a.eps = eps;
+    a.status = status;
+    a.wait_limit_ns = la::kWaitLimitNs;
+    return from_cuda(la::launch_prefill_tc(mq, mk, mv, my, a, B, alpha != nullptr, st));
+}
+
+la_status la_decode_step(const void *q, const void *k, const void *v, la_dtype dtype, const float *alpha, float *S,
+                         float *z, int B, int H, int r, int dv, float eps, void *y, la_stream_t stream)
+{
+    if (!q || !k || !v || !S || !z || !y) return LA_ERR_NULL;
+    if (B < 1 || H < 1 || r < 1 || dv < 1) return LA_ERR_SHAPE;
+    if (dtype != LA_DTYPE_BF16 && dtype != LA_DTYPE_FP32) return LA_ERR_DTYPE;
+    if (r > 256 || dv > 256) return LA_ERR_UNSUPPORTED;
+    const uintptr_t el = dtype == LA_DTYPE_BF16 ? 2 : 4;
+    if (!aligned(q, el) || !aligned(k, el) || !aligned(v, el) || !aligned(y, el)) return LA_ERR_ALIGN;
+    if (!aligned(S, 4) || !aligned(z, 4) || (alpha && !aligned(alpha, 4))) return LA_ERR_ALIGN;
+    const bool fast = r == 128 && dv == 128 && aligned(S, 16);
+    return from_cuda(la::launch_decode(q, k, v, dtype == LA_DTYPE_BF16, alpha, S, z, B, H, r, dv, eps, y, fast,
+                                       reinterpret_cast<cudaStream_t>(stream)));
+}
+
+la_status la_last_device_status(la_stream_t stream)
+{
+    if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) return LA_ERR_CUDA;
+    int v = 0;
+    if (cudaMemcpyFromSymbol(&v, g_status, sizeof(int)) != cudaSuccess) return LA_ERR_CUDA;
+    if (v != 0) {
+        const int zero = 0;
+        if (cudaMemcpyToSymbol(g_status, &zero, sizeof(int)) != cudaSuccess) return LA_ERR_CUDA;
+    }
+    return static_cast<la_status>(v);
+}
+
+la_status la_debug_wait_probe(unsigned long long limit_ns, la_stream_t stream)
+{
+    if (limit_ns > 1000000000ull) return LA_ERR_SHAPE;
+    int *status = status_word();
+    if (!status) return LA_ERR_CUDA;
+    return from_cuda(la::launch_wait_probe(status, limit_ns, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+}  // extern "C"

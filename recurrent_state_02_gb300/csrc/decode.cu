@@ -1,0 +1,215 @@
+// decode.cu -- single-token decode on the fixed-size S/z state, state init,
+// and the diagnostic bounded-wait probe.
+//
+// Decode ("Linear attention：把历史写进状态", sections "公式里的每个维度" and
+// "查询时，分子和分母一起读"; gate from "加一个门：让旧记忆逐渐淡出"):
+//     S <- alpha S + phi(k) v^T,   z <- alpha z + phi(k),
+//     y  = phi(q)^T S / (phi(q)^T z + eps)           (update before read)
+// The step reads and rewrites r*dv + r FP32 state words per head and does two
+// FMAs per state word, so it is bound by HBM bandwidth ("它省掉了什么，又把难题放在哪？":
+// each step reads O(d_phi * dv) of state).  The r = dv = 128 kernel streams S
+// with 16-byte accesses, one warp per 16 rows, 4 columns per lane, with all
+// 16 row loads of a thread in flight before any arithmetic, and reduces the
+// numerator across warps in shared memory and the denominator with warp
+// shuffles.
+
+#include "kernels.h"
+#include "sm103_ptx.cuh"
+
+#include <cuda_bf16.h>
+
+namespace la {
+namespace {
+
+__device__ __forceinline__ float phi_exact(float x) { return x > 0.f ? x + 1.f : expf(x); }
+
+template <bool BF16>
+__device__ __forceinline__ float load_elem(const void *p, size_t i)
+{
+    if (BF16) return __bfloat162float(reinterpret_cast<const __nv_bfloat16 *>(p)[i]);
+    return reinterpret_cast<const float *>(p)[i];
+}
+
+template <bool BF16>
+__device__ __forceinline__ void store_elem(void *p, size_t i, float x)
+{
+    if (BF16) reinterpret_cast<__nv_bfloat16 *>(p)[i] = __float2bfloat16_rn(x);
+    else reinterpret_cast<float *>(p)[i] = x;
+}
+
+__device__ __forceinline__ float4 ld_stream(const float4 *p)
+{
+    float4 v;
+    asm volatile("ld.global.L1::no_allocate.v4.f32 {%0,%1,%2,%3}, [%4];"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "l"(p));
+    return v;
+}
+
+__device__ __forceinline__ void st_stream(float4 *p, float4 v)
+{
+    asm volatile("st.global.cs.v4.f32 [%0], {%1,%2,%3,%4};" ::"l"(p), "f"(v.x), "f"(v.y), "f"(v.z), "f"(v.w)
+                 : "memory");
+}
+
+// r = dv = 128: one CTA of 256 threads per (b, h).
+template <bool BF16>
+__global__ void __launch_bounds__(256)
+decode128_kernel(const void *__restrict__ q, const void *__restrict__ k, const void *__restrict__ v,
+                 const float *__restrict__ alpha, float *__restrict__ S, float *__restrict__ z, float eps,
+                 void *__restrict__ y)
+{
+    constexpr int R = 128, DV = 128;
+    __shared__ float qf[R], kf[R];
+    __shared__ float4 num_part[8][32];
+    __shared__ float den_part[4];
+    const int bh = blockIdx.x;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const float a = alpha ? alpha[bh] : 1.f;
+
+    // 16 rows of S per warp, 4 columns per lane: issue every load first.
+    float4 *Srow = reinterpret_cast<float4 *>(S + (size_t)bh * R * DV) + (size_t)warp * 16 * (DV / 4) + lane;
+    float4 s[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) s[i] = ld_stream(Srow + i * (DV / 4));
+
+    if (tid < R) {
+        qf[tid] = phi_exact(load_elem<BF16>(q, (size_t)bh * R + tid));
+        kf[tid] = phi_exact(load_elem<BF16>(k, (size_t)bh * R + tid));
+    }
+    float4 vv;
+    vv.x = load_elem<BF16>(v, (size_t)bh * DV + lane * 4 + 0);
+    vv.y = load_elem<BF16>(v, (size_t)bh * DV + lane * 4 + 1);
+    vv.z = load_elem<BF16>(v, (size_t)bh * DV + lane * 4 + 2);
+    vv.w = load_elem<BF16>(v, (size_t)bh * DV + lane * 4 + 3);
+    __syncthreads();
+
+    // z and the denominator: warps 0..3 own features 0..127
+    if (tid < R) {
+        const float zn = fmaf(a, z[(size_t)bh * R + tid], kf[tid]);
+        z[(size_t)bh * R + tid] = zn;
+        float part = qf[tid] * zn;
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) part += __shfl_xor_sync(0xffffffffu, part, off);
+        if (lane == 0) den_part[warp] = part;
+    }
+
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+        const int row = warp * 16 + i;
+        const float kr = kf[row], qr = qf[row];
+        float4 t;
+        t.x = fmaf(a, s[i].x, kr * vv.x);
+        t.y = fmaf(a, s[i].y, kr * vv.y);
+        t.z = fmaf(a, s[i].z, kr * vv.z);
+        t.w = fmaf(a, s[i].w, kr * vv.w);
+        st_stream(Srow + i * (DV / 4), t);
+        acc.x = fmaf(qr, t.x, acc.x);
+        acc.y = fmaf(qr, t.y, acc.y);
+        acc.z = fmaf(qr, t.z, acc.z);
+        acc.w = fmaf(qr, t.w, acc.w);
+    }
+    num_part[warp][lane] = acc;
+    __syncthreads();
+    if (tid < DV) {
+        const float *np = reinterpret_cast<const float *>(num_part);
+        float n = 0.f;
+#pragma unroll
+        for (int w = 0; w < 8; ++w) n += np[w * DV + tid];
+        const float den = den_part[0] + den_part[1] + den_part[2] + den_part[3];
+        store_elem<BF16>(y, (size_t)bh * DV + tid, n / (den + eps));
+    }
+}
+
+// Any r, dv <= 256: thread j owns column j (and feature j for z), rows in order.
+template <bool BF16>
+__global__ void __launch_bounds__(256)
+decode_generic_kernel(const void *__restrict__ q, const void *__restrict__ k, const void *__restrict__ v,
+                      const float *__restrict__ alpha, float *__restrict__ S, float *__restrict__ z, int r,
+                      int dv, float eps, void *__restrict__ y)
+{
+    __shared__ float qf[256], kf[256], red[8];
+    const int bh = blockIdx.x, tid = threadIdx.x;
+    const float a = alpha ? alpha[bh] : 1.f;
+    float part = 0.f;
+    if (tid < r) {
+        qf[tid] = phi_exact(load_elem<BF16>(q, (size_t)bh * r + tid));
+        kf[tid] = phi_exact(load_elem<BF16>(k, (size_t)bh * r + tid));
+        const float zn = fmaf(a, z[(size_t)bh * r + tid], kf[tid]);
+        z[(size_t)bh * r + tid] = zn;
+        part = qf[tid] * zn;
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) part += __shfl_xor_sync(0xffffffffu, part, off);
+    if ((tid & 31) == 0) red[tid >> 5] = part;
+    __syncthreads();
+    if (tid < dv) {
+        float den = 0.f;
+        for (int w = 0; w < 8; ++w) den += red[w];
+        const float vj = load_elem<BF16>(v, (size_t)bh * dv + tid);
+        float *Sc = S + (size_t)bh * r * dv + tid;
+        float n = 0.f;
+        for (int i = 0; i < r; ++i) {
+            const float t = fmaf(a, Sc[(size_t)i * dv], kf[i] * vj);
+            Sc[(size_t)i * dv] = t;
+            n = fmaf(qf[i], t, n);
+        }
+        store_elem<BF16>(y, (size_t)bh * dv + tid, n / (den + eps));
+    }
+}
+
+__global__ void state_init_kernel(float *__restrict__ S, float *__restrict__ z, long long nS, long long nz)
+{
+    const long long stride = (long long)gridDim.x * blockDim.x;
+    for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < nS; i += stride) S[i] = 0.f;
+    for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < nz; i += stride) z[i] = 0.f;
+}
+
+// Waits on a barrier that nothing completes, for at most limit_ns, then records
+// a timeout in the status word -- the same path every kernel takes when a wait
+// runs out.
+__global__ void wait_probe_kernel(int *status, unsigned long long limit_ns)
+{
+    __shared__ uint64_t bar;
+    if (threadIdx.x == 0) {
+        mbar_init(&bar, 1);
+        fence_mbarrier_init();
+    }
+    __syncthreads();
+    if (threadIdx.x == 0 && !mbar_wait(&bar, 0, limit_ns)) atomicExch(status, kStatusTimeout);
+}
+
+}  // namespace
+
+cudaError_t launch_decode(const void *q, const void *k, const void *v, bool bf16, const float *alpha, float *S,
+                          float *z, int B, int H, int r, int dv, float eps, void *y, bool fast128,
+                          cudaStream_t stream)
+{
+    const int nbh = B * H;
+    if (fast128) {
+        if (bf16) decode128_kernel<true><<<nbh, 256, 0, stream>>>(q, k, v, alpha, S, z, eps, y);
+        else decode128_kernel<false><<<nbh, 256, 0, stream>>>(q, k, v, alpha, S, z, eps, y);
+    } else {
+        if (bf16) decode_generic_kernel<true><<<nbh, 256, 0, stream>>>(q, k, v, alpha, S, z, r, dv, eps, y);
+        else decode_generic_kernel<false><<<nbh, 256, 0, stream>>>(q, k, v, alpha, S, z, r, dv, eps, y);
+    }
+    return cudaGetLastError();
+}
+
+cudaError_t launch_state_init(float *S, float *z, long long n_S, long long n_z, cudaStream_t stream)
+{
+    long long n = n_S > n_z ? n_S : n_z;
+    long long blocks = (n + 255) / 256;
+    if (blocks > 152 * 16) blocks = 152 * 16;
+    if (blocks < 1) blocks = 1;
+    state_init_kernel<<<(unsigned)blocks, 256, 0, stream>>>(S, z, n_S, n_z);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_wait_probe(int *status, unsigned long long limit_ns, cudaStream_t stream)
+{
+    wait_probe_kernel<<<1, 32, 0, stream>>>(status, limit_ns);
+    return cudaGetLastError();
+}
+
+}  // namespace la

@@ -1,0 +1,87 @@
+// prefill_f32.cu -- exact FP32 prefill on CUDA cores, for FP32 inputs.
+//
+// The chunk formula is an exact reorganisation of the token recurrence
+// ("Linear attention：把历史写进状态", sections "一个 chunk 的输出由两部分组成" and
+// "动手实验": chunk boundaries do not change the result), so for FP32 inputs, where
+// BF16 tensor-core operands would not meet a 1e-5 tolerance, this kernel runs
+// the recurrence itself in FP32 (section "最小递推里，每一行都有张量意义"):
+//     S <- alpha_t S + phi(k_t) v_t^T,  z <- alpha_t z + phi(k_t),
+//     y_t = phi(q_t)^T S / (phi(q_t)^T z + eps).
+// One CTA of 128 threads per (b, h); S [r x dv] in shared memory, thread j owns
+// column j of S and feature j of z.
+
+#include "kernels.h"
+
+namespace la {
+namespace {
+
+constexpr int kMaxDim = 128;
+
+__device__ __forceinline__ float phi_exact(float x) { return x > 0.f ? x + 1.f : expf(x); }
+
+__global__ void __launch_bounds__(kMaxDim)
+prefill_f32_kernel(const float *__restrict__ q, const float *__restrict__ k, const float *__restrict__ v,
+                   const float *__restrict__ alpha, const float *__restrict__ S0, const float *__restrict__ z0,
+                   int H, int T, int r, int dv, float eps, float *__restrict__ y, float *__restrict__ S_out,
+                   float *__restrict__ z_out)
+{
+    extern __shared__ float S[];   // [r][dv]
+    __shared__ float qf[kMaxDim], kf[kMaxDim], red[kMaxDim / 32];
+    const int bh = blockIdx.y * H + blockIdx.x;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+
+    for (int e = tid; e < r * dv; e += blockDim.x) S[e] = S0 ? S0[(size_t)bh * r * dv + e] : 0.f;
+    float zi = (tid < r && z0) ? z0[(size_t)bh * r + tid] : 0.f;
+    __syncthreads();
+
+    const float *qh = q + (size_t)bh * T * r, *kh = k + (size_t)bh * T * r, *vh = v + (size_t)bh * T * dv;
+    float *yh = y + (size_t)bh * T * dv;
+    for (int t = 0; t < T; ++t) {
+        const float a = alpha ? alpha[(size_t)bh * T + t] : 1.f;
+        float part = 0.f;
+        if (tid < r) {
+            const float qv = phi_exact(qh[(size_t)t * r + tid]);
+            const float kv = phi_exact(kh[(size_t)t * r + tid]);
+            qf[tid] = qv;
+            kf[tid] = kv;
+            zi = fmaf(a, zi, kv);
+            part = qv * zi;
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) part += __shfl_xor_sync(0xffffffffu, part, off);
+        if (lane == 0) red[warp] = part;
+        __syncthreads();
+        if (tid < dv) {
+            float den = 0.f;
+#pragma unroll
+            for (int w = 0; w < kMaxDim / 32; ++w) den += red[w];
+            const float vj = vh[(size_t)t * dv + tid];
+            float n = 0.f;
+            for (int i = 0; i < r; ++i) {
+                const float s = fmaf(a, S[i * dv + tid], kf[i] * vj);
+                S[i * dv + tid] = s;
+                n = fmaf(qf[i], s, n);
+            }
+            yh[(size_t)t * dv + tid] = n / (den + eps);
+        }
+        __syncthreads();
+    }
+    for (int e = tid; e < r * dv; e += blockDim.x) S_out[(size_t)bh * r * dv + e] = S[e];
+    if (tid < r) z_out[(size_t)bh * r + tid] = zi;
+}
+
+}  // namespace
+
+cudaError_t launch_prefill_f32(const float *q, const float *k, const float *v, const float *alpha, const float *S0,
+                               const float *z0, int B, int H, int T, int r, int dv, float eps, float *y,
+                               float *S_out, float *z_out, cudaStream_t stream)
+{
+    const size_t smem = sizeof(float) * (size_t)r * dv;
+    cudaError_t e = cudaFuncSetAttribute(prefill_f32_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    prefill_f32_kernel<<<dim3(H, B), kMaxDim, smem, stream>>>(q, k, v, alpha, S0, z0, H, T, r, dv, eps, y, S_out,
+                                                              z_out);
+    return cudaGetLastError();
+}
+
+}  // namespace la

@@ -1,0 +1,185 @@
+"""CUDA path (through the C ABI) against the FP64 oracle, element by element, on
+identical seeded inputs.  Tolerances: max relative error (max|gpu-ref| / max|ref|
+per tensor) 2e-2 for BF16 inputs and 1e-5 for FP32 inputs.
+
+Sources: LA = "Linear attention：把历史写进状态" (hs-black.github.io/posts/linear-attention);
+LC = "45. Linear Attention and Recurrent State | 线性注意力与递推状态" (datawhalechina, ch. 45).
+"""
+import numpy as np
+import pytest
+import torch
+
+from conftest import max_rel_err, to_oracle
+
+pytestmark = pytest.mark.gpu
+
+TOL = {torch.bfloat16: 2e-2, torch.float32: 1e-5}
+
+
+@pytest.fixture(scope="module")
+def la():
+    from recurrent_state_02_gb300 import build
+    build.build()
+    import recurrent_state_02_gb300 as la_mod
+    assert torch.cuda.is_available()
+    return la_mod
+
+
+def _oracle_prefill(oracle_mod, inp, eps=1e-6, threads=0):
+    return oracle_mod.scan(to_oracle(inp["q"]), to_oracle(inp["k"]), to_oracle(inp["v"]),
+                           alpha=to_oracle(inp["alpha"]), S0=to_oracle(inp["S0"]), z0=to_oracle(inp["z0"]),
+                           eps=eps, threads=threads)
+
+
+def _gpu_prefill(la, inp, chunk=64, eps=1e-6):
+    d = {k: (v.cuda() if v is not None else None) for k, v in inp.items()}
+    y, S, z = la.prefill_chunked(d["q"], d["k"], d["v"], alpha=d["alpha"], S0=d["S0"], z0=d["z0"],
+                                 chunk=chunk, eps=eps)
+    assert la.last_device_status() == 0
+    return y.float().cpu().numpy(), S.cpu().numpy(), z.cpu().numpy()
+
+
+def _check(got, ref, tol, what=""):
+    for name, g, r in zip(("y", "S", "z"), got, ref):
+        assert np.isfinite(g).all(), f"{what} {name} not finite"
+        err = max_rel_err(g, r)
+        assert err <= tol, f"{what} {name}: max rel err {err:.3e} > {tol}"
+
+
+def _inputs(dtype, B, H, T, r, dv, gated=False, with_state=False, seed=0, scale=1.0):
+    from recurrent_state_02_gb300 import workloads as W
+    w = W.Workload("test", B=B, H=H, T=T, r=r, dv=dv, dtype=dtype, gated=gated, seed=seed, scale=scale)
+    return W.prefill_inputs(w, with_state=with_state)
+
+
+# ---------------------------------------------------------------- state init
+
+def test_state_init(la):
+    S = torch.randn(3, 5, 17, 9, device="cuda")
+    z = torch.randn(3, 5, 17, device="cuda")
+    la.state_init(3, 5, 17, 9, S=S, z=z)
+    torch.cuda.synchronize()
+    assert not S.any() and not z.any()
+
+
+# ------------------------------------------------------------- FP32 prefill
+
+def test_tiny_workload_fp32(la, oracle_mod):
+    """The tiny FP64 workload: FP32-rounded inputs on both sides, tolerance 1e-5."""
+    from recurrent_state_02_gb300 import workloads as W
+    inp = W.prefill_inputs(W.TINY)
+    _check(_gpu_prefill(la, inp), _oracle_prefill(oracle_mod, inp), 1e-5, "tiny")
+
+
+@pytest.mark.parametrize("gated", [False, True])
+@pytest.mark.parametrize("with_state", [False, True])
+def test_prefill_fp32_ragged(la, oracle_mod, gated, with_state):
+    inp = _inputs(torch.float32, 2, 3, 197, 48, 24, gated=gated, with_state=with_state, seed=11)
+    _check(_gpu_prefill(la, inp), _oracle_prefill(oracle_mod, inp), 1e-5, "fp32")
+
+
+# ------------------------------------------------------------- BF16 prefill
+
+@pytest.mark.parametrize("T", [1, 17, 63, 64, 65, 5 * 64 + 17])
+@pytest.mark.parametrize("dv", [64, 128])
+def test_prefill_bf16_lengths(la, oracle_mod, T, dv):
+    inp = _inputs(torch.bfloat16, 1, 3, T, 128, dv, seed=T + dv)
+    _check(_gpu_prefill(la, inp), _oracle_prefill(oracle_mod, inp), 2e-2, f"T={T} dv={dv}")
+
+
+@pytest.mark.parametrize("gated", [False, True])
+@pytest.mark.parametrize("with_state", [False, True])
+def test_prefill_bf16_several_tiles(la, oracle_mod, gated, with_state):
+    inp = _inputs(torch.bfloat16, 2, 3, 9 * 64 + 5, 128, 128, gated=gated, with_state=with_state, seed=5)
+    _check(_gpu_prefill(la, inp), _oracle_prefill(oracle_mod, inp), 2e-2, "bf16")
+
+
+def test_prefill_bf16_zero_gates(la, oracle_mod):
+    """alpha = 0 forgets everything before it, also inside a chunk (LA '加一个门')."""
+    inp = _inputs(torch.bfloat16, 1, 2, 300, 128, 128, gated=True, with_state=True, seed=8)
+    inp["alpha"][0, 0, [0, 70, 127, 128, 200]] = 0.0
+    inp["alpha"][0, 1, 64:128] = 0.0
+    _check(_gpu_prefill(la, inp), _oracle_prefill(oracle_mod, inp), 2e-2, "zero gates")
+
+
+def test_prefill_in_place_state(la, oracle_mod):
+    """S0 may alias S_out and z0 may alias z_out (continuation in place)."""
+    inp = _inputs(torch.bfloat16, 2, 4, 200, 128, 128, gated=True, with_state=True, seed=9)
+    ref = _oracle_prefill(oracle_mod, inp)
+    d = {k: v.cuda() for k, v in inp.items()}
+    S, z = d["S0"], d["z0"]
+    y, S_out, z_out = la.prefill_chunked(d["q"], d["k"], d["v"], alpha=d["alpha"], S0=S, z0=z, S_out=S, z_out=z)
+    assert S_out.data_ptr() == S.data_ptr()
+    assert la.last_device_status() == 0
+    _check((y.float().cpu().numpy(), S.cpu().numpy(), z.cpu().numpy()), ref, 2e-2, "in place")
+
+
+def test_prefix_causality_gpu(la):
+    """LC test_prefix_causality: changing later tokens leaves earlier outputs bit-identical."""
+    inp = _inputs(torch.bfloat16, 1, 2, 200, 128, 128, gated=True, seed=3)
+    y0, _, _ = _gpu_prefill(la, inp)
+    for t in (199, 150, 128, 64, 10):
+        mod = {k: (v.clone() if v is not None else None) for k, v in inp.items()}
+        mod["k"][:, :, t:] += 3.0
+        mod["v"][:, :, t:] -= 2.0
+        mod["alpha"][:, :, t:] = 0.5
+        y1, _, _ = _gpu_prefill(la, mod)
+        np.testing.assert_array_equal(y0[:, :, :t], y1[:, :, :t])
+
+
+def test_continuation_prefill_and_decode(la, oracle_mod):
+    """The state is the checkpoint: prefill T1, prefill T2 from it, then decode n
+    tokens one by one equals the oracle run over all T1 + T2 + n tokens."""
+    from recurrent_state_02_gb300 import workloads as W
+    T1, T2, n = 130, 70, 5
+    inp = _inputs(torch.bfloat16, 2, 3, T1 + T2 + n, 128, 128, gated=True, seed=21)
+    ref_y, ref_S, ref_z = _oracle_prefill(oracle_mod, inp)
+    d = {k: (v.cuda() if v is not None else None) for k, v in inp.items()}
+    y1, S, z = la.prefill_chunked(d["q"][:, :, :T1].contiguous(), d["k"][:, :, :T1].contiguous(),
+                                  d["v"][:, :, :T1].contiguous(), alpha=d["alpha"][:, :, :T1].contiguous())
+    sl = slice(T1, T1 + T2)
+    y2, S, z = la.prefill_chunked(d["q"][:, :, sl].contiguous(), d["k"][:, :, sl].contiguous(),
+                                  d["v"][:, :, sl].contiguous(), alpha=d["alpha"][:, :, sl].contiguous(),
+                                  S0=S, z0=z, S_out=S, z_out=z)
+    ys = [y1, y2]
+    for t in range(T1 + T2, T1 + T2 + n):
+        ys.append(la.decode_step(d["q"][:, :, t:t + 1].contiguous(), d["k"][:, :, t:t + 1].contiguous(),
+                                 d["v"][:, :, t:t + 1].contiguous(), S, z, alpha=d["alpha"][:, :, t].contiguous()))
+    assert la.last_device_status() == 0
+    y = torch.cat(ys, dim=2).float().cpu().numpy()
+    _check((y, S.cpu().numpy(), z.cpu().numpy()), (ref_y, ref_S, ref_z), 2e-2, "continuation")
+
+
+# ------------------------------------------------------------------- decode
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+@pytest.mark.parametrize("gated", [False, True])
+@pytest.mark.parametrize("rdv", [(128, 128), (64, 32), (200, 256), (7, 3)])
+def test_decode_step(la, oracle_mod, dtype, gated, rdv):
+    from recurrent_state_02_gb300 import workloads as W
+    r, dv = rdv
+    w = W.DECODE.with_(B=5, H=3, r=r, dv=dv, dtype=dtype, gated=gated)
+    inp = W.decode_inputs(w)
+    alpha = inp["alpha"][..., None] if gated else None
+    ref_y, ref_S, ref_z = oracle_mod.scan(to_oracle(inp["q"]), to_oracle(inp["k"]), to_oracle(inp["v"]),
+                                          alpha=to_oracle(alpha), S0=to_oracle(inp["S"]), z0=to_oracle(inp["z"]))
+    d = {k: (v.cuda() if v is not None else None) for k, v in inp.items()}
+    y = la.decode_step(d["q"], d["k"], d["v"], d["S"], d["z"], alpha=d["alpha"])
+    assert la.last_device_status() == 0
+    _check((y.float().cpu().numpy(), d["S"].cpu().numpy(), d["z"].cpu().numpy()), (ref_y, ref_S, ref_z),
+           TOL[dtype], "decode")
+
+
+# -------------------------------------------------------------- diagnostics
+
+def test_wait_timeout_is_reported(la):
+    """A barrier wait that runs out records LA_ERR_TIMEOUT; the context stays usable."""
+    from recurrent_state_02_gb300 import _native
+    assert la.last_device_status() == 0
+    st = _native.lib().la_debug_wait_probe(2_000_000, torch.cuda.current_stream().cuda_stream)
+    assert st == 0
+    assert la.last_device_status() == _native.LA_ERR_TIMEOUT
+    assert la.last_device_status() == 0
+    S, z = la.state_init(2, 2, 4, 4)
+    torch.cuda.synchronize()
+    assert not S.any()
