@@ -1,0 +1,488 @@
+#!/usr/bin/env python
+"""Benchmark of the linear-attention hot path on GB300.
+
+One step = the whole hot path over one batch of the ungated prefill workload
+(B=4, H=16, T=4096, r=dv=128, BF16, chunk 64): la_state_init (zero S/z),
+la_prefill_chunked over the batch from that state (state updated in place),
+then la_decode_step of one more token per request on the resulting state.
+Tokens per step = B * (T + 1).  Inputs are synthetic (seeded), resident in HBM
+when timing starts, and rotated over 4 sets (> L2) so no step reads a warm L2.
+Each step is replayed as a CUDA graph of its three kernel launches.
+
+Printed (rank 0, one JSON line): tokens/s of the step, the prefill kernel's
+roofline (algorithmic bytes / mean launch time vs measured HBM bandwidth), the
+decode step on its own workload (B=256, H=16) in GB/s, an end-to-end figure
+through the public API with host buffers, clocks sampled during timing, and
+the FP64 CPU oracle timed on the host cores.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "prefill tokens/s (B4 H16 T4096 d128) & decode GB/s; % of roofline"
+PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
+PROFILES = os.path.join(ROOT, "profiles")
+FALLBACK_HBM_GBS = 6800.0
+N_ROT = 4
+
+
+# ----------------------------------------------------------------- helpers
+
+def prefill_bytes(B, H, T, r, dv, with_state_in=True):
+    """Algorithmic bytes of one prefill launch: q, k, v read and y written
+    (BF16, 2*(r+r+dv+dv) bytes per token-head = 1024 at r = dv = 128), the final
+    state written and, when given, the initial state read (FP32 r*dv + r per head)."""
+    per_token_head = 2 * (2 * r + 2 * dv)
+    state = 4 * (r * dv + r)
+    return B * H * T * per_token_head + B * H * state * (2 if with_state_in else 1)
+
+
+def decode_bytes(B, H, r, dv, elem=2):
+    """S and z read and written (FP32), q, k, v read and y written (elem bytes)."""
+    return B * H * (2 * 4 * (r * dv + r) + elem * (2 * r + 2 * dv))
+
+
+def read_peaks():
+    try:
+        with open(PEAKS_FILE) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def source_sha1(path):
+    with open(path, "rb") as f:
+        return hashlib.sha1(f.read()).hexdigest()[:12]
+
+
+def profile_traffic(kernel, workload, src):
+    """DRAM bytes per launch from a committed ncu summary, only when that summary
+    was taken on the current kernel source (else None)."""
+    sha = source_sha1(src)
+    if not os.path.isdir(PROFILES):
+        return None
+    for name in sorted(os.listdir(PROFILES)):
+        if not name.endswith((".txt", ".md")):
+            continue
+        fields = {}
+        for line in open(os.path.join(PROFILES, name)):
+            if "=" in line and line.strip().startswith("traffic."):
+                k, v = line.strip().split("=", 1)
+                fields[k.strip()] = v.strip()
+        if (fields.get("traffic.kernel") == kernel and fields.get("traffic.workload") == workload
+                and fields.get("traffic.source_sha1") == sha):
+            try:
+                return float(fields["traffic.dram_bytes_per_launch"])
+            except (KeyError, ValueError):
+                return None
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi samples (every 100 ms) of SM clock, power and clock-event reasons."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu_index = gpu_index
+        self.lines = []
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits", "-lms", "100",
+                 "-i", str(self.gpu_index)], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line.strip()))
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self, t0, t1):
+        rows = []
+        for ts, line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append((ts, float(parts[1]), float(parts[2]), parts[5:9], parts[4]))
+            except ValueError:
+                continue
+        window = [r for r in rows if t0 - 0.15 <= r[0] <= t1 + 0.15] or rows
+        if not window:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no nvidia-smi samples"], "samples": 0}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in window for i, v in enumerate(r[3]) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(r[1] for r in window), "sm_max_mhz": max(r[2] for r in window),
+                "reasons": reasons, "samples": len(window)}
+
+
+def gpu_index(local_rank):
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+    if vis:
+        ids = [v for v in vis.split(",") if v.strip()]
+        if local_rank < len(ids):
+            return ids[local_rank]
+    return str(local_rank)
+
+
+# --------------------------------------------------------- CPU oracle legs
+
+def oracle_tokens_per_s(w, seconds, max_tokens=None):
+    """Times the FP64 oracle (token recurrence, all host cores) over all B*H heads of
+    the workload, on the first T' tokens (T' <= T, sized to ~`seconds`).
+    Returns (tokens/s, cores, sample description, elapsed)."""
+    import numpy as np
+    import torch
+
+    import oracle
+    from recurrent_state_02_gb300 import workloads as W
+
+    oracle.build()
+    cores = oracle.num_cpus()
+    bits = lambda t: t.contiguous().view(torch.int16).numpy().view(np.uint16)
+    # calibrate on a short prefix, then size the sample
+    Tc = min(w.T, 64)
+    inp = W.prefill_inputs(w.with_(T=Tc))
+    t0 = time.perf_counter()
+    oracle.scan(bits(inp["q"]), bits(inp["k"]), bits(inp["v"]), threads=cores)
+    per_token = (time.perf_counter() - t0) / (w.B * Tc)
+    Ts = int(max(1, min(w.T, seconds / max(per_token, 1e-9) / w.B)))
+    if max_tokens:
+        Ts = min(Ts, max(1, max_tokens // w.B))
+    inp = W.prefill_inputs(w.with_(T=Ts))
+    q, k, v = bits(inp["q"]), bits(inp["k"]), bits(inp["v"])
+    reps, elapsed = 0, 0.0
+    while True:
+        t0 = time.perf_counter()
+        oracle.scan(q, k, v, eps=w.eps, threads=cores)
+        elapsed += time.perf_counter() - t0
+        reps += 1
+        if elapsed >= seconds or reps >= 8:
+            break
+    tok = w.B * Ts * reps
+    desc = (f"FP64 token recurrence on {cores} threads over all {w.B}x{w.H} heads of '{w.name}', first {Ts} of "
+            f"{w.T} tokens, {reps} pass(es), {elapsed:.1f} s")
+    return tok / elapsed, cores, desc, elapsed
+
+
+def run_reference(args, rank, world):
+    """Reference arm: the FP64 CPU oracle, as it stands, on the host cores."""
+    if rank != 0:
+        return
+    from recurrent_state_02_gb300 import workloads as W
+    w = W.UNGATED
+    budget = 120.0
+    per_step = max(0.05, budget / max(1, args.steps + args.warmup))
+    # warm-up steps (untimed), then exactly K timed steps
+    import numpy as np
+    import torch
+
+    import oracle
+    oracle.build()
+    cores = oracle.num_cpus()
+    bits = lambda t: t.contiguous().view(torch.int16).numpy().view(np.uint16)
+    Tc = 32
+    inp = W.prefill_inputs(w.with_(T=Tc))
+    t0 = time.perf_counter()
+    oracle.scan(bits(inp["q"]), bits(inp["k"]), bits(inp["v"]), threads=cores)
+    per_token = (time.perf_counter() - t0) / (w.B * Tc)
+    Ts = int(max(1, min(w.T, per_step / max(per_token, 1e-9) / w.B)))
+    inp = W.prefill_inputs(w.with_(T=Ts + 1))
+    q, k, v = bits(inp["q"]), bits(inp["k"]), bits(inp["v"])
+    for _ in range(args.warmup):
+        oracle.scan(q, k, v, eps=w.eps, threads=cores)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.scan(q, k, v, eps=w.eps, threads=cores)
+    el = time.perf_counter() - t0
+    tokens = w.B * (Ts + 1) * args.steps
+    value = tokens / el
+    sample = (f"each step: FP64 token recurrence over all {w.B}x{w.H} heads of '{w.name}', first {Ts + 1} of "
+              f"{w.T + 1} tokens (prefill + the decoded token), {cores} threads")
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": el / args.steps * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": w.name + " + state init + 1 decode token", "sample_tokens_per_head": Ts + 1},
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------- GPU arm
+
+def run_ours(args, rank, world, local_rank):
+    import torch
+
+    import recurrent_state_02_gb300 as la
+    from recurrent_state_02_gb300 import _native, build as native_build
+    from recurrent_state_02_gb300 import workloads as W
+
+    native_build.build()
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+    stream = torch.cuda.Stream(dev)
+    L = _native.lib()
+
+    w = W.UNGATED
+    B, H, T, r, dv = w.B, w.H, w.T, w.r, w.dv
+    base = W.prefill_inputs(w, seed=w.seed + 1000 * rank)
+    dec = W.decode_inputs(W.DECODE.with_(B=B, H=H), seed=w.seed + 7 + 1000 * rank)
+    sets = []
+    for i in range(N_ROT):
+        s = dict(q=base["q"].to(dev), k=base["k"].to(dev), v=base["v"].to(dev),
+                 y=torch.empty((B, H, T, dv), device=dev, dtype=torch.bfloat16),
+                 S=torch.empty((B, H, r, dv), device=dev, dtype=torch.float32),
+                 z=torch.empty((B, H, r), device=dev, dtype=torch.float32),
+                 qd=dec["q"].to(dev), kd=dec["k"].to(dev), vd=dec["v"].to(dev),
+                 yd=torch.empty((B, H, 1, dv), device=dev, dtype=torch.bfloat16))
+        sets.append(s)
+    sh = stream.cuda_stream
+    P = lambda t: t.data_ptr()
+
+    def k_init(s):
+        _native.check(L.la_state_init(P(s["S"]), P(s["z"]), B, H, r, dv, sh), "la_state_init")
+
+    def k_prefill(s):
+        _native.check(L.la_prefill_chunked(P(s["q"]), P(s["k"]), P(s["v"]), _native.LA_DTYPE_BF16, None,
+                                           P(s["S"]), P(s["z"]), B, H, T, r, dv, w.chunk, w.eps, P(s["y"]),
+                                           P(s["S"]), P(s["z"]), None, 0, sh), "la_prefill_chunked")
+
+    def k_decode(s):
+        _native.check(L.la_decode_step(P(s["qd"]), P(s["kd"]), P(s["vd"]), _native.LA_DTYPE_BF16, None, P(s["S"]),
+                                       P(s["z"]), B, H, r, dv, w.eps, P(s["yd"]), sh), "la_decode_step")
+
+    # eager run once (sets kernel attributes, checks status), then capture graphs
+    with torch.cuda.stream(stream):
+        for s in sets:
+            k_init(s); k_prefill(s); k_decode(s)
+    assert _native.lib().la_last_device_status(sh) == 0
+    step_graphs, prefill_graphs = [], []
+    for s in sets:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            k_init(s); k_prefill(s); k_decode(s)
+        step_graphs.append(g)
+        g2 = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g2, stream=stream):
+            k_prefill(s)
+        prefill_graphs.append(g2)
+    launches_per_step = 3
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+
+    def timed(graphs, K, W_):
+        with torch.cuda.stream(stream):
+            for i in range(W_):
+                graphs[i % N_ROT].replay()
+            barrier()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for i in range(K):
+                graphs[i % N_ROT].replay()
+            e1.record(stream)
+            barrier()
+        return e0.elapsed_time(e1) / 1e3  # seconds
+
+    peak, peak_kind = read_peaks()
+    with ClockSampler(gpu_index(local_rank)) as clk:
+        # extra warm-up so the clock sampler sees the GPU under load
+        t_start = time.time()
+        with torch.cuda.stream(stream):
+            n = 0
+            while time.time() - t_start < args.clock_warmup_seconds or n < args.warmup:
+                step_graphs[n % N_ROT].replay()
+                n += 1
+                if n % 50 == 0:
+                    torch.cuda.synchronize(dev)
+        torch.cuda.synchronize(dev)
+        t0 = time.time()
+        step_s = timed(step_graphs, args.steps, args.warmup)
+        t1 = time.time()
+        prefill_s = timed(prefill_graphs, args.steps, args.warmup)
+    clocks = clk.summary(t0, t1)
+    assert _native.lib().la_last_device_status(sh) == 0
+
+    # max over ranks
+    if dist is not None:
+        tt = torch.tensor([step_s, prefill_s], device=dev, dtype=torch.float64)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        step_s, prefill_s = tt.tolist()
+    tokens_per_step = B * (T + 1)
+    value = tokens_per_step * world * args.steps / step_s
+    ms_per_step = step_s / args.steps * 1e3
+    pre_bytes = prefill_bytes(B, H, T, r, dv, with_state_in=True)
+    pre_launch = prefill_s / args.steps
+    achieved = pre_bytes / pre_launch / 1e9
+    src = os.path.join(ROOT, "recurrent_state_02_gb300", "csrc", "prefill_tc.cu")
+    roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                "traffic": profile_traffic("prefill_tc_kernel<false>", "B4 H16 T4096", src),
+                "kernel": "prefill_tc_kernel<false> (ungated)", "algorithmic_bytes_per_launch": pre_bytes,
+                "launch_us": pre_launch * 1e6, "peak_kind": peak_kind,
+                "prefill_tokens_per_s": B * T * world / pre_launch}
+
+    # decode on its own workload: B=256, H=16, state 256 MiB (> L2), in place
+    dw = W.DECODE
+    dinp = W.decode_inputs(dw, seed=dw.seed + 1000 * rank)
+    dd = {k: (v.to(dev) if v is not None else None) for k, v in dinp.items()}
+    ydec = torch.empty((dw.B, dw.H, 1, dw.dv), device=dev, dtype=torch.bfloat16)
+
+    def k_dec_big():
+        _native.check(L.la_decode_step(P(dd["q"]), P(dd["k"]), P(dd["v"]), _native.LA_DTYPE_BF16, None, P(dd["S"]),
+                                       P(dd["z"]), dw.B, dw.H, dw.r, dw.dv, dw.eps, P(ydec), sh), "decode")
+
+    with torch.cuda.stream(stream):
+        k_dec_big()
+    gd = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(gd, stream=stream):
+        k_dec_big()
+    dec_s = timed([gd] * N_ROT, args.steps, args.warmup)
+    if dist is not None:
+        tt = torch.tensor([dec_s], device=dev, dtype=torch.float64)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        dec_s = tt.item()
+    dbytes = decode_bytes(dw.B, dw.H, dw.r, dw.dv)
+    dec_launch = dec_s / args.steps
+    dec_gbs = dbytes / dec_launch / 1e9
+    decode = {"workload": dw.name, "gb_per_s": dec_gbs * world, "per_gpu_gb_per_s": dec_gbs,
+              "frac_of_hbm_peak": dec_gbs / peak, "launch_us": dec_launch * 1e6,
+              "algorithmic_bytes_per_launch": dbytes, "tokens_per_s": dw.B * world / dec_launch,
+              "traffic": profile_traffic("decode128_kernel<true>", "B256 H16",
+                                         os.path.join(ROOT, "recurrent_state_02_gb300", "csrc", "decode.cu"))}
+
+    # end to end through the public API with host buffers (pinned), every step:
+    # H2D of q, k, v (+ the decode token), the three calls, D2H of y, S, z, y_decode
+    hq, hk, hv = (base[n].pin_memory() for n in ("q", "k", "v"))
+    hqd, hkd, hvd = (dec[n].pin_memory() for n in ("q", "k", "v"))
+    hy = torch.empty((B, H, T, dv), dtype=torch.bfloat16).pin_memory()
+    hS = torch.empty((B, H, r, dv), dtype=torch.float32).pin_memory()
+    hz = torch.empty((B, H, r), dtype=torch.float32).pin_memory()
+    hyd = torch.empty((B, H, 1, dv), dtype=torch.bfloat16).pin_memory()
+    s0 = sets[0]
+    h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hqd, hkd, hvd))
+    d2h = sum(t.numel() * t.element_size() for t in (hy, hS, hz, hyd))
+
+    def e2e_step():
+        s0["q"].copy_(hq, non_blocking=True); s0["k"].copy_(hk, non_blocking=True)
+        s0["v"].copy_(hv, non_blocking=True); s0["qd"].copy_(hqd, non_blocking=True)
+        s0["kd"].copy_(hkd, non_blocking=True); s0["vd"].copy_(hvd, non_blocking=True)
+        S, z = la.state_init(B, H, r, dv, S=s0["S"], z=s0["z"])
+        la.prefill_chunked(s0["q"], s0["k"], s0["v"], S0=S, z0=z, S_out=S, z_out=z, y=s0["y"], chunk=w.chunk,
+                           eps=w.eps)
+        la.decode_step(s0["qd"], s0["kd"], s0["vd"], S, z, eps=w.eps, y=s0["yd"])
+        hy.copy_(s0["y"], non_blocking=True); hS.copy_(S, non_blocking=True)
+        hz.copy_(z, non_blocking=True); hyd.copy_(s0["yd"], non_blocking=True)
+
+    e2e_steps = max(1, min(args.steps, 50))
+    with torch.cuda.stream(stream):
+        for _ in range(max(1, min(args.warmup, 5))):
+            e2e_step()
+        barrier()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(e2e_steps):
+            e2e_step()
+        e1.record(stream)
+        barrier()
+    e2e_s = e0.elapsed_time(e1) / 1e3
+    if dist is not None:
+        tt = torch.tensor([e2e_s], device=dev, dtype=torch.float64)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        e2e_s = tt.item()
+    assert _native.lib().la_last_device_status(sh) == 0
+    e2e = {"value": tokens_per_step * world * e2e_steps / e2e_s, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+           "d2h_bytes_per_step": d2h, "steps": e2e_steps, "ms_per_step": e2e_s / e2e_steps * 1e3}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        tps, cores, desc, _ = oracle_tokens_per_s(w, args.cpu_seconds)
+        cpu = {"value": tps, "unit": "tokens/s", "cores": cores, "kind": "oracle", "sample": desc}
+
+    if rank == 0:
+        line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+                "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+                "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+                "config": {"workload": w.name + " + state init + 1 decode token per request",
+                           "B": B, "H": H, "T": T, "r": r, "dv": dv, "chunk": w.chunk, "tokens_per_step": tokens_per_step,
+                           "l2": f"{N_ROT} rotating input/output sets of "
+                                 f"{prefill_bytes(B, H, T, r, dv) / 1e6:.0f} MB (> 129 MB L2)",
+                           "parallelism": f"replicas x{world} (independent batches, no collective)",
+                           "launch": "CUDA graph per step"},
+                "roofline": roofline, "decode": decode, "cpu_baseline": cpu, "e2e": e2e,
+                "gpu_launches": launches_per_step * args.steps, "clocks": clocks}
+        print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--clock-warmup-seconds", type=float, default=0.6,
+                    help="untimed load before timing so that clock samples see the GPU busy (0 under a profiler)")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if world != args.gpus:
+        ap.error(f"--gpus {args.gpus} but WORLD_SIZE={world}")
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    try:
+        run_ours(args, rank, world, local_rank)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -77,8 +77,18 @@ cudaError_t launch_prefill_f32(const float *q, const float *k, const float *v, c
                                float *S_out, float *z_out, cudaStream_t stream)
 {
     const size_t smem = sizeof(float) * (size_t)r * dv;
-    cudaError_t e = cudaFuncSetAttribute(prefill_f32_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    // The attribute is set once per device to the largest size this kernel accepts.
+    static bool attr_set[64] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    if (!attr_set[dev]) {
+        e = cudaFuncSetAttribute(prefill_f32_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)(sizeof(float) * kMaxDim * kMaxDim));
+        if (e != cudaSuccess) return e;
+        attr_set[dev] = true;
+    }
     prefill_f32_kernel<<<dim3(H, B), kMaxDim, smem, stream>>>(q, k, v, alpha, S0, z0, H, T, r, dv, eps, y, S_out,
                                                               z_out);
     return cudaGetLastError();

@@ -204,6 +204,42 @@ __device__ __forceinline__ void tc_ld_32x32b_x32(uint32_t taddr, float (&v)[32])
     for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
 
+// 32 lanes x 32 bits, one column.
+__device__ __forceinline__ void tc_ld_32x32b_x1(uint32_t taddr, float &v)
+{
+    uint32_t r;
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x1.b32 {%0}, [%1];" : "=r"(r) : "r"(taddr));
+    v = __uint_as_float(r);
+}
+
+// 16 lanes x 32 bits, twice: threads 0..15 receive lanes (base + i), columns
+// [col, col + 16); threads 16..31 receive lanes (base + i - 16), columns
+// [col + OFF, col + OFF + 16).  Used for M = 64 accumulators, whose rows fill
+// lanes 0..15 of each quadrant.
+template <int OFF>
+__device__ __forceinline__ void tc_ld_16x32bx2_x16(uint32_t taddr, float (&v)[16])
+{
+    uint32_t r[16];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.16x32bx2.x16.b32 "
+        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16], %17;"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+          "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr), "n"(OFF));
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// Same shape, one column per half: threads 0..15 get column col, 16..31 get col + OFF.
+template <int OFF>
+__device__ __forceinline__ void tc_ld_16x32bx2_x1(uint32_t taddr, float &v)
+{
+    uint32_t r;
+    asm volatile("tcgen05.ld.sync.aligned.16x32bx2.x1.b32 {%0}, [%1], %2;" : "=r"(r) : "r"(taddr), "n"(OFF));
+    v = __uint_as_float(r);
+}
+
 // ------------------------------------------------------------- descriptors
 
 // Shared-memory matrix descriptor (tcgen05 format): start address, leading and
