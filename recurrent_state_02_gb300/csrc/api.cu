@@ -30,18 +30,19 @@ EncodeTiledFn encode_fn()
     return fn;
 }
 
-// 3-D BF16 view [planes, rows, cols] (cols innermost), 64 x 64 boxes, 128-byte
-// swizzle; rows past the end of a plane read as zero and are never written.
-bool make_map_bf16(CUtensorMap *map, const void *ptr, long long planes, long long rows, long long cols)
+// 3-D BF16 view [planes, rows, cols] (cols innermost) with boxes of box_cols x
+// box_rows; rows past the end of a plane read as zero and are never written.
+bool make_map_bf16(CUtensorMap *map, const void *ptr, long long planes, long long rows, long long cols,
+                   unsigned box_cols, unsigned box_rows, CUtensorMapSwizzle swizzle)
 {
     EncodeTiledFn fn = encode_fn();
     if (!fn) return false;
     const cuuint64_t dims[3] = {(cuuint64_t)cols, (cuuint64_t)rows, (cuuint64_t)planes};
     const cuuint64_t strides[2] = {(cuuint64_t)cols * 2, (cuuint64_t)cols * rows * 2};
-    const cuuint32_t box[3] = {64, 64, 1};
+    const cuuint32_t box[3] = {box_cols, box_rows, 1};
     const cuuint32_t estr[3] = {1, 1, 1};
     return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(ptr), dims, strides, box, estr,
-              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -128,8 +129,11 @@ la_status la_prefill_chunked(const void *q, const void *k, const void *v, la_dty
     if (!status) return LA_ERR_CUDA;
     CUtensorMap mq, mk, mv, my;
     const long long planes = (long long)B * H;
-    if (!make_map_bf16(&mq, q, planes, T, r) || !make_map_bf16(&mk, k, planes, T, r) ||
-        !make_map_bf16(&mv, v, planes, T, dv) || !make_map_bf16(&my, y, planes, T, dv))
+    // q, k, v: 64 x 64 load boxes, 128-byte swizzle; y: 32-column x 16-row store
+    // boxes (one per TMEM warp), 64-byte swizzle
+    const CUtensorMapSwizzle sw128 = CU_TENSOR_MAP_SWIZZLE_128B, sw64 = CU_TENSOR_MAP_SWIZZLE_64B;
+    if (!make_map_bf16(&mq, q, planes, T, r, 64, 64, sw128) || !make_map_bf16(&mk, k, planes, T, r, 64, 64, sw128) ||
+        !make_map_bf16(&mv, v, planes, T, dv, 64, 64, sw128) || !make_map_bf16(&my, y, planes, T, dv, 32, 16, sw64))
         return LA_ERR_CUDA;
     la::PrefillTcArgs a;
     a.alpha = alpha;

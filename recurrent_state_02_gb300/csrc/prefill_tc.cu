@@ -51,22 +51,31 @@ constexpr int kDVS = 64;        // value columns per CTA
 constexpr int kThreads = 512;   // 16 warps
 constexpr int kWarpTma = 0, kWarpMma = 1, kWarpTm0 = 4;
 constexpr int kTmWarps = 8, kPhiWarps = 6, kPhiThreads = kPhiWarps * 32;
+#ifndef LA_WAIT_HINT_NS
+#define LA_WAIT_HINT_NS 20000
+#endif
+constexpr uint32_t kWaitHintNs = LA_WAIT_HINT_NS;
 
 constexpr uint32_t kTileQ = kC * kR * 2;      // 16 KB: two 64-feature blocks of 64 rows x 128 B
 constexpr uint32_t kTileV = kC * kDVS * 2;    // 8 KB
 constexpr uint32_t kTileA = kC * kC * 2;      // 8 KB
-constexpr uint32_t kTileSp = kR * kDVS * 2;   // 16 KB: 128 feature rows x 128 B
-constexpr uint32_t kTileZ = 2 * 16 * 128;     // 4 KB: [zhi; zlo; 0..] 16 rows x 128 features, 2 blocks
-constexpr uint32_t kTileW = 16 * 128;         // 2 KB: [w; 0..] 16 rows x 64 tokens
+// [Sprev | zhi zlo 0..]: 128 feature rows x 80 columns, 32-byte swizzle, five
+// blocks of 16 columns (4 KB each); column 64 holds zhi and 65 zlo.
+constexpr uint32_t kTileSpZ = 5 * kR * 32;    // 20 KB
+// gated [w . V | w 0..]: 64 token rows x 80 columns, 32-byte swizzle, five blocks of 2 KB
+constexpr uint32_t kTileVw = 5 * kC * 32;     // 10 KB
+// ungated: the second 64-column block of [V | 1 0..] (128-byte swizzle, column 0 = 1)
+constexpr uint32_t kTileOnes = kC * 128;      // 8 KB
 constexpr uint32_t kTileY = kC * kDVS * 2;    // 8 KB
 
 __host__ __device__ constexpr bool is_phi_warp(int w) { return w == 2 || w == 3 || w >= 12; }
 
 template <bool GATED>
 struct Cfg {
-    static constexpr int kStages = GATED ? 2 : 3;
+    static constexpr int kStages = GATED ? 3 : 4;
     static constexpr int kNP = GATED ? 1 : 2;                  // P accumulator buffers
-    // TMEM columns: P, then [dS | dz] and [O | dn] blocks of 80 (x2), then O_intra (gated, x2)
+    // TMEM columns: P, then [dS | dz] and [O | dn] blocks of 80 (x2), then O_intra (gated, x2);
+    // dz is column 64 of a [dS | dz] block, dn columns 64 and 65 of an [O | dn] block
     static constexpr uint32_t kColP = 0;
     static constexpr uint32_t kColDS = kNP * 64;
     static constexpr uint32_t kColO = kColDS + 2 * 80;
@@ -76,26 +85,27 @@ struct Cfg {
     // shared memory (offsets from a 1024-aligned base)
     static constexpr uint32_t kOffQ = 0, kOffK = kTileQ, kOffV = 2 * kTileQ;
     static constexpr uint32_t kOffVw = kOffV + kTileV;                      // gated
-    static constexpr uint32_t kOffWg = kOffVw + (GATED ? kTileV : 0);       // gated: [w; 0] per stage
-    static constexpr uint32_t kStageBytes = kOffWg + (GATED ? kTileW : 0);
+    static constexpr uint32_t kStageBytes = kOffVw + (GATED ? kTileVw : 0);
+    static_assert(kStageBytes % 1024 == 0, "stage tiles stay 1024-byte aligned");
+    // A and [Sprev | z] are single tiles: each is read by the MMAs issued right
+    // after it is written, long before the TMEM warps write it again
     static constexpr uint32_t kOffA = kStages * kStageBytes;
-    static constexpr uint32_t kOffSp = kOffA + 2 * kTileA;
-    static constexpr uint32_t kOffZ = kOffSp + 2 * kTileSp;
-    static constexpr uint32_t kOffY = kOffZ + 2 * kTileZ;
-    static constexpr uint32_t kOffW1 = kOffY + 2 * kTileY;                  // ungated: [1; 0]
-    static constexpr uint32_t kOffSmall = kOffW1 + kTileW;
+    static constexpr uint32_t kOffSpZ = kOffA + kTileA;
+    static constexpr uint32_t kOffY = kOffSpZ + kTileSpZ;                   // 8 warps x 2 x 1 KB
+    static constexpr uint32_t kOffOnes = kOffY + 2 * kTileY;                // ungated only
+    static constexpr uint32_t kOffSmall = kOffOnes + (GATED ? 0 : kTileOnes);
 };
 
 struct alignas(16) Small {
-    float gb[2][kC];            // cumulative log gate inside the chunk
-    int gz[2][kC];              // last row <= i whose gate is 0 (-1: none)
-    float gG[2][kC];            // Gamma_i
-    float gw[2][kC];            // w_j
+    float gb[4][kC];            // cumulative log gate inside the chunk (chunk c in buffer c % 4)
+    int gz[4][kC];              // last row <= i whose gate is 0 (-1: none)
+    float gG[4][kC];            // Gamma_i
+    float gw[4][kC];            // w_j
     float densum[2][2][kC];     // in-chunk row sums, two column halves
     float carry[4];
-    uint64_t full[3], empty[3], phi_done[3];
+    uint64_t full[4], empty[4], phi_done[4];
     uint64_t P_full[2], P_empty[2], dS_full[2], dS_empty[2], Sp_full[2], Sp_empty[2];
-    uint64_t A_full[2], A_empty[2], O_full[2], O_empty[2], aux_empty[2];
+    uint64_t A_full[2], A_empty[2], O_full[2], O_empty[2], aux_empty[4];
     uint64_t mma_done, tm_sync, phi_sync;
     uint32_t tmem_base;
     int abort_flag;
@@ -106,8 +116,15 @@ constexpr uint32_t smem_bytes() { return Cfg<GATED>::kOffSmall + sizeof(Small) +
 static_assert(smem_bytes<false>() <= 232448, "shared memory budget");
 static_assert(smem_bytes<true>() <= 232448, "shared memory budget");
 
-// phi(x) = ELU(x) + 1: x + 1 for x > 0, e^x otherwise (NaN propagates).
-__device__ __forceinline__ float phi_elu1(float x) { return x > 0.f ? x + 1.f : __expf(x); }
+// phi(x) = ELU(x) + 1: x + 1 for x > 0, e^x = 2^(x log2 e) otherwise (NaN
+// propagates).  The base-2 exponential is the hardware approximation with
+// flush-to-zero (results below 2^-126, i.e. x < -87.3, become 0).
+__device__ __forceinline__ float phi_elu1(float x)
+{
+    float e;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e) : "f"(x * 1.4426950408889634f));
+    return x > 0.f ? x + 1.f : e;
+}
 
 struct Ctx {
     Small *sm;
@@ -135,24 +152,28 @@ __device__ __forceinline__ bool wait(Ctx &cx, uint64_t *bar, uint32_t parity)
 {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = global_timer_ns();
-    for (uint32_t it = 1;; ++it) {
-        if (mbar_try_wait(bar, parity)) return true;
-        if ((it & 63u) == 0) {
-            if (aborted(cx)) return false;
-            if (global_timer_ns() - t0 > cx.limit) {
-                fail(cx);
-                return false;
-            }
+    for (;;) {
+        // suspended in hardware while the phase is incomplete (bounded per try)
+        if (kWaitHintNs ? mbar_try_wait_hint(bar, parity, kWaitHintNs) : mbar_try_wait(bar, parity)) return true;
+        if (aborted(cx)) return false;
+        if (global_timer_ns() - t0 > cx.limit) {
+            fail(cx);
+            return false;
         }
     }
 }
 
-// Every lane waits; the outcome is made uniform across the warp so that the
-// warp stays converged for the .sync.aligned instructions that follow.
+// Lane 0 waits while the other lanes are parked at the warp barrier; the
+// outcome is broadcast so that the warp stays converged for the .sync.aligned
+// instructions that follow, and the warp barrier orders the other lanes'
+// later accesses after lane 0's acquire.
 __device__ __forceinline__ bool warp_wait(Ctx &cx, uint64_t *bar, uint32_t parity)
 {
-    const bool ok = wait(cx, bar, parity);
-    return __all_sync(0xffffffffu, ok);
+    int ok = 1;
+    if ((threadIdx.x & 31) == 0) ok = wait(cx, bar, parity);
+    ok = __shfl_sync(0xffffffffu, ok, 0);
+    __syncwarp();
+    return ok != 0;
 }
 
 // One arrival per warp, after every lane's preceding writes and fences.
@@ -239,8 +260,8 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
             mbar_init(&sm->A_empty[i], 1);
             mbar_init(&sm->O_full[i], 1);
             mbar_init(&sm->O_empty[i], kTmWarps);
-            mbar_init(&sm->aux_empty[i], kTmWarps);
         }
+        for (int i = 0; i < 4; ++i) mbar_init(&sm->aux_empty[i], kTmWarps);
         mbar_init(&sm->mma_done, 1);
         mbar_init(&sm->tm_sync, kTmWarps);
         mbar_init(&sm->phi_sync, kPhiWarps);
@@ -251,21 +272,22 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
         tma_prefetch_desc(&map_v);
         tma_prefetch_desc(&map_y);
     }
-    // Constant operand tiles: rows 1..15 of [w; 0] and rows 2..15 of [zhi; zlo; 0]
-    // stay zero; the ungated [1; 0] tile is complete here.
-    for (int i = threadIdx.x; i < 2 * (int)kTileZ / 16; i += kThreads)
-        reinterpret_cast<uint4 *>(base + L::kOffZ)[i] = make_uint4(0, 0, 0, 0);
+    // Constant operand parts: the z block (columns 64..79) of the [Sprev | z]
+    // tile and the w block of every gated [w . V | w] tile start at zero (only
+    // columns 64, 65 resp. 64 are written later); the ungated ones block is
+    // complete here (column 0 = 1 in every token row).
+    for (int i = threadIdx.x; i < kR * 32 / 16; i += kThreads)
+        reinterpret_cast<uint4 *>(base + L::kOffSpZ + 4 * kR * 32)[i] = make_uint4(0, 0, 0, 0);
     if (GATED) {
         for (int s = 0; s < NST; ++s)
-            for (int i = threadIdx.x; i < (int)kTileW / 16; i += kThreads)
-                reinterpret_cast<uint4 *>(stage_ptr(s) + L::kOffWg)[i] = make_uint4(0, 0, 0, 0);
+            for (int i = threadIdx.x; i < kC * 32 / 16; i += kThreads)
+                reinterpret_cast<uint4 *>(stage_ptr(s) + L::kOffVw + 4 * kC * 32)[i] = make_uint4(0, 0, 0, 0);
     } else {
-        for (int i = threadIdx.x; i < (int)kTileW / 16; i += kThreads) {
-            const int row = (i * 16) >> 7;
-            const uint32_t one2 = 0x3F803F80u;   // two BF16 ones
-            reinterpret_cast<uint4 *>(base + L::kOffW1)[i] =
-                row == 0 ? make_uint4(one2, one2, one2, one2) : make_uint4(0, 0, 0, 0);
-        }
+        for (int i = threadIdx.x; i < (int)kTileOnes / 16; i += kThreads)
+            reinterpret_cast<uint4 *>(base + L::kOffOnes)[i] = make_uint4(0, 0, 0, 0);
+        __syncthreads();
+        if (threadIdx.x < kC)   // element (column 0, token row k): 16-byte chunk 0 of row k after the swizzle
+            *reinterpret_cast<uint16_t *>(base + L::kOffOnes + sw128_offset(threadIdx.x, 0)) = 0x3F80u;
     }
     fence_proxy_async_smem();
     if (warp == kWarpMma) {
@@ -313,79 +335,120 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
         }
     } else if (warp == kWarpMma) {
         // ------------------------------------------------------------ MMA
-        if (lane == 0) {
+        // The whole warp runs this loop so that descriptors and loop state are
+        // warp-uniform; lane 0 alone issues the MMAs and commits.
+        // Issue order per iteration: chunk c's O = Q~ Sprev (+) A V, then the
+        // scores of chunk c + NP and the state increment of chunk c + 1, so that
+        // the TMEM warps' waits are on work issued an iteration earlier.
+        {
+            const bool leader = lane == 0;
             constexpr uint32_t idP = idesc_bf16_f32(64, 64, false, false);
-            constexpr uint32_t idDS = idesc_bf16_f32(128, 64, true, true);
-            constexpr uint32_t idDZ = idesc_bf16_f32(128, 16, true, false);
-            constexpr uint32_t idQS = idesc_bf16_f32(64, 64, false, true);
-            constexpr uint32_t idDN = idesc_bf16_f32(64, 16, false, false);
-            constexpr uint32_t idAV = idesc_bf16_f32(64, 64, false, true);
-            const uint32_t aW1 = smem_u32(base + L::kOffW1);
-            for (int c = 0; c < nch && !aborted(cx); ++c) {
-                const int s = c % NST, bb = c & 1, n = c >> 1;
-                const int pb = c % NP, pn = c / NP;
-                uint8_t *st = stage_ptr(s);
-                const uint32_t aQ = smem_u32(st + L::kOffQ), aK = smem_u32(st + L::kOffK);
-                const uint32_t aV = smem_u32(st + L::kOffV);
-                const uint32_t aVw = GATED ? smem_u32(st + L::kOffVw) : aV;
-                const uint32_t aW = GATED ? smem_u32(st + L::kOffWg) : aW1;
-                const uint32_t aA = smem_u32(base + L::kOffA + bb * kTileA);
-                const uint32_t aSp = smem_u32(base + L::kOffSp + bb * kTileSp);
-                const uint32_t aZ = smem_u32(base + L::kOffZ + bb * kTileZ);
-                if (!wait(cx, &sm->phi_done[s], (c / NST) & 1)) break;
-                // P = Q~ K~^T
-                if (c >= NP && !wait(cx, &sm->P_empty[pb], (pn - 1) & 1)) break;
+            constexpr uint32_t idDS = idesc_bf16_f32(128, 80, true, true);   // [dS | dz]
+            constexpr uint32_t idQS = idesc_bf16_f32(64, 80, false, true);   // [O | dn]
+            // gated: O_intra = A V; ungated: [O | dn] += A [V | 1] (column 64 gains the row sums of A)
+            constexpr uint32_t idAV = GATED ? idesc_bf16_f32(64, 64, false, true) : idesc_bf16_f32(64, 80, false, true);
+            const uint32_t aOnes = smem_u32(base + L::kOffOnes);
+            // P = Q~ K~^T for chunk c
+            auto issue_p = [&](int c) -> bool {
+                const int s = c % NST, pb = c % NP, pn = c / NP;
+                const uint32_t st = smem_u32(stage_ptr(s));
+                const uint32_t aQ = st + L::kOffQ, aK = st + L::kOffK;
+                if (!warp_wait(cx, &sm->phi_done[s], (c / NST) & 1)) return false;
+                if (c >= NP && !warp_wait(cx, &sm->P_empty[pb], (pn - 1) & 1)) return false;
                 tc_fence_after();
+                if (leader) {
 #pragma unroll
-                for (int kk = 0; kk < 8; ++kk) {
-                    const uint32_t off = (kk >> 2) * (kTileQ / 2) + (kk & 3) * 32;
-                    tc_mma_bf16(tmem + L::kColP + pb * 64, smem_desc_sw128(aQ + off, 16, 1024),
-                                smem_desc_sw128(aK + off, 16, 1024), idP, kk > 0);
+                    for (int kk = 0; kk < 8; ++kk) {
+                        const uint32_t off = (kk >> 2) * (kTileQ / 2) + (kk & 3) * 32;
+                        tc_mma_bf16(tmem + L::kColP + pb * 64, smem_desc_sw128(aQ + off, 16, 1024),
+                                    smem_desc_sw128(aK + off, 16, 1024), idP, kk > 0);
+                    }
+                    tc_commit(&sm->P_full[pb]);
                 }
-                tc_commit(&sm->P_full[pb]);
-                // dS = K~^T (w . V), dz = K~^T w
-                if (c >= 2 && !wait(cx, &sm->dS_empty[bb], (n - 1) & 1)) break;
+                __syncwarp();
+                return true;
+            };
+            // [dS | dz] = K~^T [w . V | w] for chunk c (phi_done of chunk c was
+            // waited for by issue_p(c), which always comes first)
+            auto issue_ds = [&](int c) -> bool {
+                const int s = c % NST, bb = c & 1, n = c >> 1;
+                const uint32_t st = smem_u32(stage_ptr(s));
+                const uint32_t aK = st + L::kOffK;
+                // B = [w . V | w] (gated, 32-byte swizzle) or [V | 1] (V tile + the ones block at LBO)
+                const uint64_t bDS = GATED ? smem_desc_sw32(st + L::kOffVw, kC * 32, 256)
+                                           : smem_desc_sw128(st + L::kOffV, aOnes - (st + L::kOffV), 1024);
+                const uint32_t bStep = GATED ? 512 : 2048;   // 16 token rows
+                if (c >= 2 && !warp_wait(cx, &sm->dS_empty[bb], (n - 1) & 1)) return false;
                 tc_fence_after();
                 const uint32_t dDS = tmem + L::kColDS + bb * 80;
+                if (leader) {
 #pragma unroll
-                for (int kk = 0; kk < 4; ++kk) {
-                    const uint64_t aKt = smem_desc_sw128(aK + kk * 2048, kTileQ / 2, 1024);
-                    tc_mma_bf16(dDS, aKt, smem_desc_sw128(aVw + kk * 2048, kTileV, 1024), idDS, kk > 0);
-                    tc_mma_bf16(dDS + 64, aKt, smem_desc_sw128(aW + kk * 32, 16, 1024), idDZ, kk > 0);
+                    for (int kk = 0; kk < 4; ++kk)
+                        tc_mma_bf16(dDS, smem_desc_sw128(aK + kk * 2048, kTileQ / 2, 1024),
+                                    bDS + ((kk * bStep) >> 4), idDS, kk > 0);
+                    tc_commit(&sm->dS_full[bb]);
                 }
-                tc_commit(&sm->dS_full[bb]);
-                // O (inter) = Q~ Sprev, dn = Q~ [zhi, zlo]
-                if (c >= 2 && !wait(cx, &sm->O_empty[bb], (n - 1) & 1)) break;
-                if (!wait(cx, &sm->Sp_full[bb], n & 1)) break;
+                __syncwarp();
+                return true;
+            };
+            bool ok = true;
+            if (nch >= 1) ok = issue_p(0);
+            if (ok && NP == 2 && nch >= 2) ok = issue_p(1);
+            if (ok && nch >= 1) ok = issue_ds(0);
+            for (int c = 0; c < nch && ok && !aborted(cx); ++c) {
+                const int s = c % NST, bb = c & 1, n = c >> 1;
+                const uint32_t st = smem_u32(stage_ptr(s));
+                const uint32_t aQ = st + L::kOffQ, aV = st + L::kOffV;
+                const uint32_t aA = smem_u32(base + L::kOffA);
+                const uint32_t aSpZ = smem_u32(base + L::kOffSpZ);
+                // [O | dn] = Q~ [Sprev | zhi zlo]
+                if (c >= 2 && !warp_wait(cx, &sm->O_empty[bb], (n - 1) & 1)) break;
+                if (!warp_wait(cx, &sm->Sp_full[0], c & 1)) break;
                 tc_fence_after();
                 const uint32_t dO = tmem + L::kColO + bb * 80;
+                if (leader) {
 #pragma unroll
-                for (int kk = 0; kk < 8; ++kk) {
-                    const uint32_t off = (kk >> 2) * (kTileQ / 2) + (kk & 3) * 32;
-                    const uint64_t aQd = smem_desc_sw128(aQ + off, 16, 1024);
-                    tc_mma_bf16(dO, aQd, smem_desc_sw128(aSp + kk * 2048, kTileSp, 1024), idQS, kk > 0);
-                    tc_mma_bf16(dO + 64, aQd, smem_desc_sw128(aZ + (kk >> 2) * (kTileZ / 2) + (kk & 3) * 32, 16, 1024),
-                                idDN, kk > 0);
+                    for (int kk = 0; kk < 8; ++kk) {
+                        const uint32_t off = (kk >> 2) * (kTileQ / 2) + (kk & 3) * 32;
+                        tc_mma_bf16(dO, smem_desc_sw128(aQ + off, 16, 1024),
+                                    smem_desc_sw32(aSpZ + kk * 512, kR * 32, 256), idQS, kk > 0);
+                    }
+                    tc_commit(&sm->Sp_empty[0]);
                 }
-                tc_commit(&sm->Sp_empty[bb]);
+                __syncwarp();
                 // O (intra) (+)= A V
-                if (!wait(cx, &sm->A_full[bb], n & 1)) break;
+                if (!warp_wait(cx, &sm->A_full[0], c & 1)) break;
                 tc_fence_after();
                 const uint32_t dIn = GATED ? tmem + L::kColO2 + bb * 64 : dO;
+                if (leader) {
 #pragma unroll
-                for (int kk = 0; kk < 4; ++kk)
-                    tc_mma_bf16(dIn, smem_desc_sw128(aA + kk * 32, 16, 1024),
-                                smem_desc_sw128(aV + kk * 2048, kTileV, 1024), idAV, GATED ? kk > 0 : true);
-                tc_commit(&sm->A_empty[bb]);
-                tc_commit(&sm->O_full[bb]);
-                tc_commit(&sm->empty[s]);
+                    const uint64_t bAV = GATED ? smem_desc_sw128(aV, kTileV, 1024)
+                                               : smem_desc_sw128(aV, aOnes - aV, 1024);
+                    for (int kk = 0; kk < 4; ++kk)
+                        tc_mma_bf16(dIn, smem_desc_sw128(aA + kk * 32, 16, 1024), bAV + ((kk * 2048) >> 4), idAV,
+                                    GATED ? kk > 0 : true);
+                    tc_commit(&sm->A_empty[0]);
+                    tc_commit(&sm->O_full[bb]);
+                    tc_commit(&sm->empty[s]);
+                }
+                __syncwarp();
+                // look-ahead: the stage of chunk c is released above before these
+                // wait for the stages of chunks c + 1 .. c + NP
+                if (c + NP < nch && !issue_p(c + NP)) break;
+                if (c + 1 < nch && !issue_ds(c + 1)) break;
             }
-            // Every MMA this thread issued completes before TMEM is released.
-            tc_commit(&sm->mma_done);
-            mbar_wait(&sm->mma_done, 0, cx.limit);
+            // Every MMA the leader issued completes before TMEM is released.
+            if (leader) {
+                tc_commit(&sm->mma_done);
+                mbar_wait(&sm->mma_done, 0, cx.limit);
+            }
+            __syncwarp();
         }
     } else if (warp >= kWarpTm0 && warp < kWarpTm0 + kTmWarps) {
         // ----------------------------------------------------- TMEM warps
+        // Iteration c: fold dS of chunk c-1 into the state (the state chunk c
+        // reads), turn the scores of chunk c into A, and finish the outputs of
+        // chunk c-2.  Each warp stores its own 16 x 32 piece of y by TMA.
         const int tw = warp - kWarpTm0;          // 0..7
         const int qd = warp & 3;                 // TMEM lane quadrant this warp may access
         const int hf = tw >> 2;                  // column half (0: columns 0..31, 1: 32..63)
@@ -393,7 +456,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
         const int srow = qd * 32 + lane;         // state row (feature index) of this thread
         const int prow = qd * 16 + (lane & 15);  // row of the M = 64 tiles (16x32bx2 loads)
         const int pcol = hf * 32 + (lane >> 4) * 16;   // first of this thread's 16 columns
-        const bool store_thread = (threadIdx.x == kWarpTm0 * 32);
+        uint8_t *ystage = base + L::kOffY + tw * 2 * 1024;   // two 1 KB staging tiles of this warp
         uint32_t sync_phase = 0;
 
         float S[32];
@@ -403,62 +466,83 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
 #pragma unroll
             for (int j = 0; j < 32; ++j) S[j] = src ? src[j] : 0.f;
         }
-        float dintra_prev = 0.f, gam_prev = 1.f;
+        // gated: in-chunk row sums and Gamma_i of chunks c-1 and c-2
+        float dint1 = 0.f, dint2 = 0.f, gam1 = 1.f, gam2 = 1.f;
 
-        // Outputs of chunk j: y = O / (den + eps) -> swizzled staging tile -> TMA store.
-        auto epilogue = [&](int j, float dintra_j, float gam_j) -> bool {
-            const int jb = j & 1;
-            if (!warp_wait(cx, &sm->O_full[jb], (j >> 1) & 1)) return false;
-            tc_fence_after();
-            float o[16], o2[16], dn;
-            tc_ld_16x32bx2_x16<16>(tmem + lane_base + L::kColO + jb * 80 + hf * 32, o);
-            if (GATED) tc_ld_16x32bx2_x16<16>(tmem + lane_base + L::kColO2 + jb * 64 + hf * 32, o2);
-            tc_ld_16x32bx2_x1<1>(tmem + lane_base + L::kColO + jb * 80 + 64, dn);
-            tc_wait_ld();
-            tc_fence_before();
-            warp_arrive(&sm->O_empty[jb]);
-            dn += __shfl_xor_sync(0xffffffffu, dn, 16);          // Q~ . zhi + Q~ . zlo
-            const float inv = 1.f / (fmaf(gam_j, dn, dintra_j) + args.eps);
-            float yv[16];
-#pragma unroll
-            for (int e = 0; e < 16; ++e) yv[e] = (GATED ? fmaf(gam_j, o[e], o2[e]) : o[e]) * inv;
-            store_bf16x16(base + L::kOffY + jb * kTileY, prow, pcol >> 3, yv);
-            fence_proxy_async_smem();
-            if (!group_sync(cx, &sm->tm_sync, sync_phase)) return false;
-            if (store_thread) {
-                tma_store_3d(&map_y, base + L::kOffY + jb * kTileY, slice * kDVS, j * kC, bh);
-                tma_store_commit();
-                // The next epilogue fills the other staging tile; before the one
-                // after it refills this tile, this store must have read it.
-                tma_store_wait_read<1>();
-            }
-            if (GATED) warp_arrive(&sm->aux_empty[jb]);
-            return true;
-        };
-
-        bool ok = true;
-        for (int c = 0; c < nch; ++c) {
-            const int bb = c & 1, n = c >> 1, s = c % NST;
-            const int pb = c % NP, pn = c / NP;
-            // a(c): the state chunk c reads is the state after chunk c-1
-            if (c >= 1) {
-                const int ob = (c - 1) & 1;
-                if (!warp_wait(cx, &sm->dS_full[ob], ((c - 1) >> 1) & 1)) { ok = false; break; }
+        for (int c = 0; c < nch + 2; ++c) {
+            const bool has_a = c >= 1 && c <= nch;   // dS of chunk c-1
+            const bool has_b = c < nch;               // Sprev and scores of chunk c
+            const bool has_e = c >= 2;                // outputs of chunk c-2
+            const int bb = c & 1, pb = c % NP, pn = c / NP;
+            const int ab = (c - 1) & 1;
+            // outputs of chunk c-2 (its O was complete a full iteration ago)
+            uint32_t yp[8];
+            if (has_e) {
+                if (!warp_wait(cx, &sm->O_full[bb], ((c - 2) >> 1) & 1)) break;
                 tc_fence_after();
-                float d[32], dz;
-                tc_ld_32x32b_x32(tmem + lane_base + L::kColDS + ob * 80 + hf * 32, d);
-                tc_ld_32x32b_x1(tmem + lane_base + L::kColDS + ob * 80 + 64, dz);
+                float o[16], o2[16], dn;
+                tc_ld_16x32bx2_x16<16>(tmem + lane_base + L::kColO + bb * 80 + hf * 32, o);
+                if (GATED) tc_ld_16x32bx2_x16<16>(tmem + lane_base + L::kColO2 + bb * 64 + hf * 32, o2);
+                tc_ld_16x32bx2_x1<1>(tmem + lane_base + L::kColO + bb * 80 + 64, dn);
                 tc_wait_ld();
                 tc_fence_before();
-                warp_arrive(&sm->dS_empty[ob]);
-                const float g = GATED ? sm->gG[ob][kC - 1] : 1.f;
+                warp_arrive(&sm->O_empty[bb]);
+                // columns 64 + 65: Q~ . zprev (two parts), plus the row sums of A without a gate
+                dn += __shfl_xor_sync(0xffffffffu, dn, 16);
+                const float inv = __frcp_rn((GATED ? fmaf(gam2, dn, dint2) : dn) + args.eps);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    const float y0 = (GATED ? fmaf(gam2, o[2 * e], o2[2 * e]) : o[2 * e]) * inv;
+                    const float y1 = (GATED ? fmaf(gam2, o[2 * e + 1], o2[2 * e + 1]) : o[2 * e + 1]) * inv;
+                    yp[e] = pack_bf16x2(y0, y1);
+                }
+            }
+            // dS of chunk c-1 and the scores of chunk c
+            if (has_a && !warp_wait(cx, &sm->dS_full[ab], ((c - 1) >> 1) & 1)) break;
+            if (has_b && GATED && !warp_wait(cx, &sm->phi_done[c % NST], (c / NST) & 1)) break;
+            if (has_b && !warp_wait(cx, &sm->P_full[pb], pn & 1)) break;
+            tc_fence_after();
+            float d[32], dz = 0.f, p[16];
+            if (has_a) {
+                tc_ld_32x32b_x32(tmem + lane_base + L::kColDS + ab * 80 + hf * 32, d);
+                tc_ld_32x32b_x1(tmem + lane_base + L::kColDS + ab * 80 + 64, dz);
+            }
+            if (has_b) tc_ld_16x32bx2_x16<16>(tmem + lane_base + L::kColP + pb * 64 + hf * 32, p);
+            tc_wait_ld();
+            tc_fence_before();
+            if (has_a) warp_arrive(&sm->dS_empty[ab]);
+            if (has_b) warp_arrive(&sm->P_empty[pb]);
+
+            if (has_a) {
+                const float g = GATED ? sm->gG[(c - 1) & 3][kC - 1] : 1.f;
 #pragma unroll
                 for (int j = 0; j < 32; ++j) S[j] = GATED ? fmaf(g, S[j], d[j]) : S[j] + d[j];
                 zr = GATED ? fmaf(g, zr, dz) : zr + dz;
             }
-            if (c >= 2 && !warp_wait(cx, &sm->Sp_empty[bb], (n - 1) & 1)) { ok = false; break; }
-            {
-                uint8_t *sp = base + L::kOffSp + bb * kTileSp;
+            float rowsum = 0.f;
+            if (has_b) {
+                const int gq = c & 3;
+                const float bi = GATED ? sm->gb[gq][prow] : 0.f;
+                const int zi = GATED ? sm->gz[gq][prow] : -1;
+#pragma unroll
+                for (int e = 0; e < 16; ++e) {
+                    const int j = pcol + e;
+                    float a = (j <= prow) ? p[e] : 0.f;
+                    if (GATED) {
+                        a = (j <= prow && zi <= j) ? a * __expf(bi - sm->gb[gq][j]) : 0.f;
+                        rowsum += a;
+                    }
+                    p[e] = a;
+                }
+                if (GATED) rowsum += __shfl_xor_sync(0xffffffffu, rowsum, 16);
+            }
+
+            // shared-memory operands and outputs
+            if (has_b) {
+                if (c >= 1 && !warp_wait(cx, &sm->Sp_empty[0], (c - 1) & 1)) break;
+                if (c >= 1 && !warp_wait(cx, &sm->A_empty[0], (c - 1) & 1)) break;
+                // Sprev (BF16) into columns hf*32 .. +31 of row srow: two 16-column blocks
+                uint8_t *spz = base + L::kOffSpZ;
 #pragma unroll
                 for (int q4 = 0; q4 < 4; ++q4) {
                     uint4 w;
@@ -466,96 +550,69 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
                     w.y = pack_bf16x2(S[q4 * 8 + 2], S[q4 * 8 + 3]);
                     w.z = pack_bf16x2(S[q4 * 8 + 4], S[q4 * 8 + 5]);
                     w.w = pack_bf16x2(S[q4 * 8 + 6], S[q4 * 8 + 7]);
-                    *reinterpret_cast<uint4 *>(sp + sw128_offset(srow, hf * 4 + q4)) = w;
+                    *reinterpret_cast<uint4 *>(spz + (hf * 2 + (q4 >> 1)) * (kR * 32) + sw32_offset(srow, (q4 & 1) * 8)) = w;
                 }
                 if (hf == 0) {
-                    // z as two BF16 parts, rows 0 and 1 of the K-major [zhi; zlo; 0] tile
-                    const __nv_bfloat16 zhi = __float2bfloat16_rn(zr);
-                    const __nv_bfloat16 zlo = __float2bfloat16_rn(zr - __bfloat162float(zhi));
-                    uint8_t *zt = base + L::kOffZ + bb * kTileZ + (srow >> 6) * (kTileZ / 2);
-                    const int f = srow & 63;
-                    *reinterpret_cast<__nv_bfloat16 *>(zt + sw128_offset(0, f >> 3) + (f & 7) * 2) = zhi;
-                    *reinterpret_cast<__nv_bfloat16 *>(zt + sw128_offset(1, f >> 3) + (f & 7) * 2) = zlo;
+                    // z as two BF16 parts in columns 64 (zhi) and 65 (zlo)
+                    const float zhi = __bfloat162float(__float2bfloat16_rn(zr));
+                    *reinterpret_cast<uint32_t *>(spz + 4 * (kR * 32) + sw32_offset(srow, 0)) = pack_bf16x2(zhi, zr - zhi);
                 }
-            }
-            fence_proxy_async_smem();
-            warp_arrive(&sm->Sp_full[bb]);
-
-            // b(c): scores -> masked, decayed BF16 operand A and FP32 row sums
-            if (GATED && !warp_wait(cx, &sm->phi_done[s], (c / NST) & 1)) { ok = false; break; }
-            if (!warp_wait(cx, &sm->P_full[pb], pn & 1)) { ok = false; break; }
-            tc_fence_after();
-            float p[16];
-            tc_ld_16x32bx2_x16<16>(tmem + lane_base + L::kColP + pb * 64 + hf * 32, p);
-            tc_wait_ld();
-            tc_fence_before();
-            warp_arrive(&sm->P_empty[pb]);
-            float rowsum = 0.f;
-            {
-                const float bi = GATED ? sm->gb[bb][prow] : 0.f;
-                const int zi = GATED ? sm->gz[bb][prow] : -1;
-#pragma unroll
-                for (int e = 0; e < 16; ++e) {
-                    const int j = pcol + e;
-                    float a = (j <= prow) ? p[e] : 0.f;
-                    if (GATED) a = (j <= prow && zi <= j) ? a * __expf(bi - sm->gb[bb][j]) : 0.f;
-                    p[e] = a;
-                    rowsum += a;
-                }
-            }
-            rowsum += __shfl_xor_sync(0xffffffffu, rowsum, 16);
-            if (c >= 2 && !warp_wait(cx, &sm->A_empty[bb], (n - 1) & 1)) { ok = false; break; }
-            store_bf16x16(base + L::kOffA + bb * kTileA, prow, pcol >> 3, p);
-            if (lane < 16) sm->densum[bb][hf][prow] = rowsum;
-            fence_proxy_async_smem();
-            warp_arrive(&sm->A_full[bb]);
-            if (!group_sync(cx, &sm->tm_sync, sync_phase)) { ok = false; break; }
-            const float dintra_cur = sm->densum[bb][0][prow] + sm->densum[bb][1][prow];
-            const float gam_cur = GATED ? sm->gG[bb][prow] : 1.f;
-            // e(c-1): outputs of the previous chunk
-            if (c >= 1 && !epilogue(c - 1, dintra_prev, gam_prev)) { ok = false; break; }
-            dintra_prev = dintra_cur;
-            gam_prev = gam_cur;
-        }
-        if (ok && nch >= 1) {
-            // final state: fold in the last chunk's dS and dz, then the last outputs
-            const int lb = (nch - 1) & 1;
-            if (warp_wait(cx, &sm->dS_full[lb], ((nch - 1) >> 1) & 1)) {
-                tc_fence_after();
-                float d[32], dz;
-                tc_ld_32x32b_x32(tmem + lane_base + L::kColDS + lb * 80 + hf * 32, d);
-                tc_ld_32x32b_x1(tmem + lane_base + L::kColDS + lb * 80 + 64, dz);
-                tc_wait_ld();
-                tc_fence_before();
-                const float g = GATED ? sm->gG[lb][kC - 1] : 1.f;
+                store_bf16x16(base + L::kOffA, prow, pcol >> 3, p);
+                if (GATED && lane < 16) sm->densum[bb][hf][prow] = rowsum;
+            } else if (has_a) {
+                // c == nch: the state after the last chunk
                 float *dst = args.S_out + ((size_t)bh * kR + srow) * args.dv + slice * kDVS + hf * 32;
 #pragma unroll
-                for (int j = 0; j < 32; j += 4) {
-                    float4 v4;
-                    v4.x = GATED ? fmaf(g, S[j], d[j]) : S[j] + d[j];
-                    v4.y = GATED ? fmaf(g, S[j + 1], d[j + 1]) : S[j + 1] + d[j + 1];
-                    v4.z = GATED ? fmaf(g, S[j + 2], d[j + 2]) : S[j + 2] + d[j + 2];
-                    v4.w = GATED ? fmaf(g, S[j + 3], d[j + 3]) : S[j + 3] + d[j + 3];
-                    *reinterpret_cast<float4 *>(dst + j) = v4;
+                for (int j = 0; j < 32; j += 4)
+                    *reinterpret_cast<float4 *>(dst + j) = make_float4(S[j], S[j + 1], S[j + 2], S[j + 3]);
+                if (slice == 0 && hf == 0) args.z_out[(size_t)bh * kR + srow] = zr;
+            }
+            if (has_e) {
+                // this warp's staging tile (c & 1) was last read by its store two iterations ago
+                if (lane == 0) tma_store_wait_read<1>();
+                __syncwarp();
+                uint8_t *yt = ystage + bb * 1024;
+                const int r = lane & 15, ch = (lane >> 4) * 2;   // row, first 16-byte chunk of 64-byte rows
+                *reinterpret_cast<uint4 *>(yt + sw64_offset(r, ch)) = make_uint4(yp[0], yp[1], yp[2], yp[3]);
+                *reinterpret_cast<uint4 *>(yt + sw64_offset(r, ch + 1)) = make_uint4(yp[4], yp[5], yp[6], yp[7]);
+            }
+            fence_proxy_async_smem();
+            if (has_b) {
+                warp_arrive(&sm->Sp_full[0]);
+                warp_arrive(&sm->A_full[0]);
+            }
+            if (has_e) {
+                __syncwarp();
+                if (lane == 0) {
+                    tma_store_3d(&map_y, ystage + bb * 1024, slice * kDVS + hf * 32, (c - 2) * kC + qd * 16, bh);
+                    tma_store_commit();
                 }
-                if (slice == 0 && hf == 0) args.z_out[(size_t)bh * kR + srow] = GATED ? fmaf(g, zr, dz) : zr + dz;
-                // publishes the store thread's last read-completion wait to every TMEM warp
-                if (group_sync(cx, &sm->tm_sync, sync_phase)) epilogue(nch - 1, dintra_prev, gam_prev);
+            }
+            if (GATED) {
+                // exchange the two column halves of the row sums
+                if (!group_sync(cx, &sm->tm_sync, sync_phase)) break;
+                if (has_a) warp_arrive(&sm->aux_empty[(c - 1) & 3]);   // gate data of chunk c-1 is done
+                dint2 = dint1;
+                gam2 = gam1;
+                if (has_b) {
+                    dint1 = sm->densum[bb][0][prow] + sm->densum[bb][1][prow];
+                    gam1 = sm->gG[c & 3][prow];
+                }
             }
         }
-        if (store_thread) tma_store_wait_all<0>();
+        if (lane == 0) tma_store_wait_all<0>();
     } else if (is_phi_warp(warp)) {
         // ------------------------------------------------------ phi warps
         const int pp = (warp < 4 ? (warp - 2) * 32 : 64 + (warp - 12) * 32) + lane;   // 0..191
         uint32_t sync_phase = 0;
         bool ok = true;
         for (int c = 0; c < nch && ok; ++c) {
-            const int s = c % NST, bb = c & 1;
+            const int s = c % NST, gq = c & 3;
             const int nvalid = min(kC, T - c * kC);
             if (!warp_wait(cx, &sm->full[s], (c / NST) & 1)) { ok = false; break; }
             uint8_t *st = stage_ptr(s);
             if (GATED) {
-                if (c >= 2 && !warp_wait(cx, &sm->aux_empty[bb], ((c >> 1) - 1) & 1)) { ok = false; break; }
+                if (c >= 4 && !warp_wait(cx, &sm->aux_empty[gq], ((c >> 2) - 1) & 1)) { ok = false; break; }
                 // in-chunk cumulative log gate and the last zero gate, rows 0..63 (warps 2, 3)
                 float la = 0.f;
                 int zl = -1;
@@ -577,36 +634,45 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
                     zl = max(zl, __float_as_int(sm->carry[1]));
                 }
                 if (pp < kC) {
-                    sm->gb[bb][pp] = la;
-                    sm->gz[bb][pp] = zl;
-                    sm->gG[bb][pp] = zl < 0 ? expf(la) : 0.f;
+                    sm->gb[gq][pp] = la;
+                    sm->gz[gq][pp] = zl;
+                    sm->gG[gq][pp] = zl < 0 ? expf(la) : 0.f;
                 }
             }
-            // phi(Q), phi(K) in place; key rows past the end of the sequence become 0
-            for (int ci = pp; ci < 2048; ci += kPhiThreads) {
-                const bool isk = ci >= 1024;
-                const uint32_t off = (uint32_t)(ci & 1023) * 16u;
-                uint4 *ptr = reinterpret_cast<uint4 *>(st + (isk ? L::kOffK : L::kOffQ) + off);
-                const int row = (off & 8191u) >> 7;
-                *ptr = (isk && row >= nvalid) ? make_uint4(0, 0, 0, 0) : phi8(*ptr);
+            // phi(Q), phi(K) in place (the two tiles are contiguous: 2048 chunks of
+            // 16 bytes); key rows past the end of the sequence become 0
+            static_assert(L::kOffK == L::kOffQ + kTileQ, "Q and K tiles are contiguous");
+            uint4 *qk = reinterpret_cast<uint4 *>(st + L::kOffQ);
+            constexpr int kFull = 2048 / kPhiThreads, kRest = 2048 - kFull * kPhiThreads;
+            if (nvalid == kC) {
+#pragma unroll
+                for (int it = 0; it < kFull; ++it) qk[pp + it * kPhiThreads] = phi8(qk[pp + it * kPhiThreads]);
+                if (pp < kRest) qk[pp + kFull * kPhiThreads] = phi8(qk[pp + kFull * kPhiThreads]);
+            } else {
+                for (int ci = pp; ci < 2048; ci += kPhiThreads) {
+                    const int row = (ci & 511) >> 3;   // 8 chunks per 128-byte row, 64 rows per block
+                    qk[ci] = (ci >= 1024 && row >= nvalid) ? make_uint4(0, 0, 0, 0) : phi8(qk[ci]);
+                }
             }
             if (GATED) {
                 if (!group_sync(cx, &sm->phi_sync, sync_phase)) { ok = false; break; }
                 if (pp < kC) {
-                    const float blast = sm->gb[bb][kC - 1];
-                    const int zlast = sm->gz[bb][kC - 1];
-                    const float wj = (zlast <= pp) ? expf(blast - sm->gb[bb][pp]) : 0.f;
-                    sm->gw[bb][pp] = wj;
-                    // row 0 of the K-major [w; 0] operand
-                    *reinterpret_cast<__nv_bfloat16 *>(st + L::kOffWg + sw128_offset(0, pp >> 3) + (pp & 7) * 2) =
+                    const float blast = sm->gb[gq][kC - 1];
+                    const int zlast = sm->gz[gq][kC - 1];
+                    const float wj = (zlast <= pp) ? expf(blast - sm->gb[gq][pp]) : 0.f;
+                    sm->gw[gq][pp] = wj;
+                    // column 64 (block 4, column 0) of [w . V | w]
+                    *reinterpret_cast<__nv_bfloat16 *>(st + L::kOffVw + 4 * (kC * 32) + sw32_offset(pp, 0)) =
                         __float2bfloat16_rn(wj);
                 }
                 if (!group_sync(cx, &sm->phi_sync, sync_phase)) { ok = false; break; }
-                // w . V for the state update (same swizzled layout as V)
+                // w . V for the state update: 8-column chunk c8 of token row k, from
+                // the 128-byte-swizzled V tile into the 32-byte-swizzled operand
                 for (int ci = pp; ci < (int)kTileV / 16; ci += kPhiThreads) {
-                    const uint32_t off = (uint32_t)ci * 16u;
-                    const uint4 raw = *reinterpret_cast<const uint4 *>(st + L::kOffV + off);
-                    *reinterpret_cast<uint4 *>(st + L::kOffVw + off) = scale8(raw, sm->gw[bb][off >> 7]);
+                    const int k = ci >> 3, c8 = ci & 7;
+                    const uint4 raw = *reinterpret_cast<const uint4 *>(st + L::kOffV + sw128_offset(k, c8));
+                    *reinterpret_cast<uint4 *>(st + L::kOffVw + (c8 >> 1) * (kC * 32) + sw32_offset(k, (c8 & 1) * 8)) =
+                        scale8(raw, sm->gw[gq][k]);
                 }
             }
             fence_proxy_async_smem();

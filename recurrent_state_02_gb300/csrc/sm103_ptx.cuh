@@ -65,15 +65,31 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity)
     return ok != 0;
 }
 
+// As mbar_try_wait, but the thread may be suspended in hardware for up to
+// `hint_ns` nanoseconds while the phase is incomplete (it resumes as soon as the
+// phase completes), so a waiting warp does not compete for issue slots.
+__device__ __forceinline__ bool mbar_try_wait_hint(uint64_t *bar, uint32_t parity, uint32_t hint_ns)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
+        : "memory");
+    return ok != 0;
+}
+
 // Waits until the phase with the given parity has completed, for at most
 // `limit_ns` nanoseconds.  Returns false when the limit ran out.
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, uint64_t limit_ns)
 {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = global_timer_ns();
-    for (uint32_t it = 1;; ++it) {
-        if (mbar_try_wait(bar, parity)) return true;
-        if ((it & 63u) == 0 && global_timer_ns() - t0 > limit_ns) return false;
+    for (;;) {
+        if (mbar_try_wait_hint(bar, parity, 20000u)) return true;
+        if (global_timer_ns() - t0 > limit_ns) return false;
     }
 }
 
@@ -245,15 +261,28 @@ __device__ __forceinline__ void tc_ld_16x32bx2_x1(uint32_t taddr, float &v)
 // Shared-memory matrix descriptor (tcgen05 format): start address, leading and
 // stride byte offsets (all >> 4), the fixed version bits 46..48 = 0b001, and the
 // swizzle mode in bits 61..63 (2 = 128-byte swizzle).
-__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo_bytes, uint32_t sbo_bytes)
+// Swizzle modes (bits 61..63): 2 = 128-byte, 6 = 32-byte.
+__device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo_bytes, uint32_t sbo_bytes, uint32_t mode)
 {
     uint64_t d = 0;
     d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
     d |= static_cast<uint64_t>((lbo_bytes >> 4) & 0x3FFFu) << 16;
     d |= static_cast<uint64_t>((sbo_bytes >> 4) & 0x3FFFu) << 32;
     d |= static_cast<uint64_t>(1) << 46;
-    d |= static_cast<uint64_t>(2) << 61;
+    d |= static_cast<uint64_t>(mode & 7u) << 61;
     return d;
+}
+
+__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo_bytes, uint32_t sbo_bytes)
+{
+    return smem_desc(saddr, lbo_bytes, sbo_bytes, 2u);
+}
+
+// 32-byte swizzle: atoms of 8 rows x 32 bytes (256 bytes, 256-byte aligned);
+// the 16-byte half of a row is XOR-ed with bit 2 of the row index.
+__device__ __forceinline__ uint64_t smem_desc_sw32(uint32_t saddr, uint32_t lbo_bytes, uint32_t sbo_bytes)
+{
+    return smem_desc(saddr, lbo_bytes, sbo_bytes, 6u);
 }
 
 // Instruction descriptor for kind::f16 with BF16 A and B and an FP32 accumulator.
@@ -272,6 +301,22 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool a_mn, b
 // Byte offset of the 16-byte chunk `chunk` (0..7) of row `row` inside a tile of
 // 128-byte rows stored with the 128-byte swizzle (atoms of 8 rows x 128 bytes,
 // 1024-byte aligned): the chunk index is XOR-ed with the row index modulo 8.
+// Byte offset of element `col` (0..15, 16-bit elements) of row `row` in a
+// 32-byte-swizzled block of 16-element rows (atoms of 8 rows, 256 bytes).
+__device__ __forceinline__ uint32_t sw32_offset(int row, int col)
+{
+    return static_cast<uint32_t>((row >> 3) * 256 + (row & 7) * 32 + ((((col >> 3) ^ (row >> 2)) & 1) << 4) +
+                                 (col & 7) * 2);
+}
+
+// Byte offset of 16-byte chunk `chunk` (0..3) of row `row` in a tile of 64-byte
+// rows stored with the 64-byte swizzle (atoms of 8 rows x 64 bytes, 512-byte
+// aligned): the chunk index is XOR-ed with bits 1..2 of the row index.
+__device__ __forceinline__ uint32_t sw64_offset(int row, int chunk)
+{
+    return static_cast<uint32_t>(row * 64 + ((chunk ^ ((row >> 1) & 3)) << 4));
+}
+
 __device__ __forceinline__ uint32_t sw128_offset(int row, int chunk)
 {
     return static_cast<uint32_t>(row * 128 + ((chunk ^ (row & 7)) << 4));
