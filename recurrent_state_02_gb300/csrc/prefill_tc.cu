@@ -50,7 +50,7 @@ constexpr int kR = 128;         // feature width r
 constexpr int kDVS = 64;        // value columns per CTA
 constexpr int kThreads = 512;   // 16 warps
 constexpr int kWarpTma = 0, kWarpMma = 1, kWarpTm0 = 4;
-constexpr int kTmWarps = 8, kPhiWarps = 6, kPhiThreads = kPhiWarps * 32;
+constexpr int kTmWarps = 8, kPhiWarps = 5, kPhiThreads = kPhiWarps * 32;
 #ifndef LA_WAIT_HINT_NS
 #define LA_WAIT_HINT_NS 20000
 #endif
@@ -68,11 +68,22 @@ constexpr uint32_t kTileVw = 5 * kC * 32;     // 10 KB
 constexpr uint32_t kTileOnes = kC * 128;      // 8 KB
 constexpr uint32_t kTileY = kC * kDVS * 2;    // 8 KB
 
-__host__ __device__ constexpr bool is_phi_warp(int w) { return w == 2 || w == 3 || w >= 12; }
+// The phi warps avoid scheduler 1 (warps w with w % 4 == 1), which the MMA warp
+// shares with two TMEM warps: a busy neighbour there starves the MMA issue.
+__host__ __device__ constexpr bool is_phi_warp(int w) { return w == 2 || w == 3 || w == 12 || w == 14 || w == 15; }
+__host__ __device__ constexpr int phi_index(int w) { return w < 4 ? w - 2 : (w == 12 ? 2 : w - 11); }
+
+#ifndef LA_STAGES_UNGATED
+#define LA_STAGES_UNGATED 4
+#endif
+#ifndef LA_SP_BUFS
+#define LA_SP_BUFS 1
+#endif
 
 template <bool GATED>
 struct Cfg {
-    static constexpr int kStages = GATED ? 3 : 4;
+    static constexpr int kStages = GATED ? 3 : LA_STAGES_UNGATED;
+    static constexpr int kSpBufs = LA_SP_BUFS;                 // [Sprev | z] tiles
     static constexpr int kNP = GATED ? 1 : 2;                  // P accumulator buffers
     // TMEM columns: P, then [dS | dz] and [O | dn] blocks of 80 (x2), then O_intra (gated, x2);
     // dz is column 64 of a [dS | dz] block, dn columns 64 and 65 of an [O | dn] block
@@ -87,12 +98,13 @@ struct Cfg {
     static constexpr uint32_t kOffVw = kOffV + kTileV;                      // gated
     static constexpr uint32_t kStageBytes = kOffVw + (GATED ? kTileVw : 0);
     static_assert(kStageBytes % 1024 == 0, "stage tiles stay 1024-byte aligned");
-    // A and [Sprev | z] are single tiles: each is read by the MMAs issued right
-    // after it is written, long before the TMEM warps write it again
+    // A is double-buffered; [Sprev | z] is a single tile (the MMAs that read it
+    // are issued first, right after it is written); one 1 KB y staging tile per
+    // TMEM warp
     static constexpr uint32_t kOffA = kStages * kStageBytes;
-    static constexpr uint32_t kOffSpZ = kOffA + kTileA;
-    static constexpr uint32_t kOffY = kOffSpZ + kTileSpZ;                   // 8 warps x 2 x 1 KB
-    static constexpr uint32_t kOffOnes = kOffY + 2 * kTileY;                // ungated only
+    static constexpr uint32_t kOffSpZ = kOffA + 2 * kTileA;
+    static constexpr uint32_t kOffY = kOffSpZ + kSpBufs * kTileSpZ;         // 8 warps x 1 KB
+    static constexpr uint32_t kOffOnes = kOffY + kTileY;                    // ungated only
     static constexpr uint32_t kOffSmall = kOffOnes + (GATED ? 0 : kTileOnes);
 };
 
@@ -276,8 +288,10 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
     // tile and the w block of every gated [w . V | w] tile start at zero (only
     // columns 64, 65 resp. 64 are written later); the ungated ones block is
     // complete here (column 0 = 1 in every token row).
-    for (int i = threadIdx.x; i < kR * 32 / 16; i += kThreads)
-        reinterpret_cast<uint4 *>(base + L::kOffSpZ + 4 * kR * 32)[i] = make_uint4(0, 0, 0, 0);
+    for (int i = threadIdx.x; i < L::kSpBufs * (kR * 32 / 16); i += kThreads) {
+        const int buf = i / (kR * 32 / 16), j = i % (kR * 32 / 16);
+        reinterpret_cast<uint4 *>(base + L::kOffSpZ + buf * kTileSpZ + 4 * kR * 32)[j] = make_uint4(0, 0, 0, 0);
+    }
     if (GATED) {
         for (int s = 0; s < NST; ++s)
             for (int i = threadIdx.x; i < kC * 32 / 16; i += kThreads)
@@ -348,6 +362,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
             // gated: O_intra = A V; ungated: [O | dn] += A [V | 1] (column 64 gains the row sums of A)
             constexpr uint32_t idAV = GATED ? idesc_bf16_f32(64, 64, false, true) : idesc_bf16_f32(64, 80, false, true);
             const uint32_t aOnes = smem_u32(base + L::kOffOnes);
+            constexpr uint32_t kHi128 = desc_hi(1024, 2), kHi32 = desc_hi(256, 6);   // SBO and swizzle words
             // P = Q~ K~^T for chunk c
             auto issue_p = [&](int c) -> bool {
                 const int s = c % NST, pb = c % NP, pn = c / NP;
@@ -357,11 +372,12 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
                 if (c >= NP && !warp_wait(cx, &sm->P_empty[pb], (pn - 1) & 1)) return false;
                 tc_fence_after();
                 if (leader) {
+                    const uint32_t qlo = desc_lo(aQ, 16), klo = desc_lo(aK, 16), dP = tmem + L::kColP + pb * 64;
 #pragma unroll
                     for (int kk = 0; kk < 8; ++kk) {
-                        const uint32_t off = (kk >> 2) * (kTileQ / 2) + (kk & 3) * 32;
-                        tc_mma_bf16(tmem + L::kColP + pb * 64, smem_desc_sw128(aQ + off, 16, 1024),
-                                    smem_desc_sw128(aK + off, 16, 1024), idP, kk > 0);
+                        const uint32_t o = ((kk >> 2) * (kTileQ / 2) + (kk & 3) * 32) >> 4;
+                        if (kk == 0) tc_mma_bf16_w<false>(dP, qlo + o, kHi128, klo + o, kHi128, idP);
+                        else tc_mma_bf16_w<true>(dP, qlo + o, kHi128, klo + o, kHi128, idP);
                     }
                     tc_commit(&sm->P_full[pb]);
                 }
@@ -375,17 +391,19 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
                 const uint32_t st = smem_u32(stage_ptr(s));
                 const uint32_t aK = st + L::kOffK;
                 // B = [w . V | w] (gated, 32-byte swizzle) or [V | 1] (V tile + the ones block at LBO)
-                const uint64_t bDS = GATED ? smem_desc_sw32(st + L::kOffVw, kC * 32, 256)
-                                           : smem_desc_sw128(st + L::kOffV, aOnes - (st + L::kOffV), 1024);
-                const uint32_t bStep = GATED ? 512 : 2048;   // 16 token rows
+                const uint32_t blo = GATED ? desc_lo(st + L::kOffVw, kC * 32) : desc_lo(st + L::kOffV, aOnes - (st + L::kOffV));
+                constexpr uint32_t bhi = GATED ? kHi32 : kHi128;
+                constexpr uint32_t bStep = (GATED ? 512 : 2048) >> 4;   // 16 token rows
                 if (c >= 2 && !warp_wait(cx, &sm->dS_empty[bb], (n - 1) & 1)) return false;
                 tc_fence_after();
                 const uint32_t dDS = tmem + L::kColDS + bb * 80;
                 if (leader) {
+                    const uint32_t klo = desc_lo(aK, kTileQ / 2);   // K~^T: MN-major, two 64-feature blocks
 #pragma unroll
-                    for (int kk = 0; kk < 4; ++kk)
-                        tc_mma_bf16(dDS, smem_desc_sw128(aK + kk * 2048, kTileQ / 2, 1024),
-                                    bDS + ((kk * bStep) >> 4), idDS, kk > 0);
+                    for (int kk = 0; kk < 4; ++kk) {
+                        if (kk == 0) tc_mma_bf16_w<false>(dDS, klo, kHi128, blo, bhi, idDS);
+                        else tc_mma_bf16_w<true>(dDS, klo + kk * (2048 >> 4), kHi128, blo + kk * bStep, bhi, idDS);
+                    }
                     tc_commit(&sm->dS_full[bb]);
                 }
                 __syncwarp();
@@ -399,35 +417,38 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
                 const int s = c % NST, bb = c & 1, n = c >> 1;
                 const uint32_t st = smem_u32(stage_ptr(s));
                 const uint32_t aQ = st + L::kOffQ, aV = st + L::kOffV;
-                const uint32_t aA = smem_u32(base + L::kOffA);
-                const uint32_t aSpZ = smem_u32(base + L::kOffSpZ);
+                const uint32_t aA = smem_u32(base + L::kOffA + bb * kTileA);
+                const int sb = c % L::kSpBufs, sn = c / L::kSpBufs;
+                const uint32_t aSpZ = smem_u32(base + L::kOffSpZ + sb * kTileSpZ);
                 // [O | dn] = Q~ [Sprev | zhi zlo]
                 if (c >= 2 && !warp_wait(cx, &sm->O_empty[bb], (n - 1) & 1)) break;
-                if (!warp_wait(cx, &sm->Sp_full[0], c & 1)) break;
+                if (!warp_wait(cx, &sm->Sp_full[sb], sn & 1)) break;
                 tc_fence_after();
                 const uint32_t dO = tmem + L::kColO + bb * 80;
                 if (leader) {
+                    const uint32_t qlo = desc_lo(aQ, 16), slo = desc_lo(aSpZ, kR * 32);
 #pragma unroll
                     for (int kk = 0; kk < 8; ++kk) {
-                        const uint32_t off = (kk >> 2) * (kTileQ / 2) + (kk & 3) * 32;
-                        tc_mma_bf16(dO, smem_desc_sw128(aQ + off, 16, 1024),
-                                    smem_desc_sw32(aSpZ + kk * 512, kR * 32, 256), idQS, kk > 0);
+                        const uint32_t o = ((kk >> 2) * (kTileQ / 2) + (kk & 3) * 32) >> 4;
+                        if (kk == 0) tc_mma_bf16_w<false>(dO, qlo, kHi128, slo, kHi32, idQS);
+                        else tc_mma_bf16_w<true>(dO, qlo + o, kHi128, slo + kk * (512 >> 4), kHi32, idQS);
                     }
-                    tc_commit(&sm->Sp_empty[0]);
+                    tc_commit(&sm->Sp_empty[sb]);
                 }
                 __syncwarp();
                 // O (intra) (+)= A V
-                if (!warp_wait(cx, &sm->A_full[0], c & 1)) break;
+                if (!warp_wait(cx, &sm->A_full[bb], n & 1)) break;
                 tc_fence_after();
                 const uint32_t dIn = GATED ? tmem + L::kColO2 + bb * 64 : dO;
                 if (leader) {
+                    const uint32_t alo = desc_lo(aA, 16);
+                    const uint32_t vlo = GATED ? desc_lo(aV, kTileV) : desc_lo(aV, aOnes - aV);
 #pragma unroll
-                    const uint64_t bAV = GATED ? smem_desc_sw128(aV, kTileV, 1024)
-                                               : smem_desc_sw128(aV, aOnes - aV, 1024);
-                    for (int kk = 0; kk < 4; ++kk)
-                        tc_mma_bf16(dIn, smem_desc_sw128(aA + kk * 32, 16, 1024), bAV + ((kk * 2048) >> 4), idAV,
-                                    GATED ? kk > 0 : true);
-                    tc_commit(&sm->A_empty[0]);
+                    for (int kk = 0; kk < 4; ++kk) {
+                        if (GATED && kk == 0) tc_mma_bf16_w<false>(dIn, alo, kHi128, vlo, kHi128, idAV);
+                        else tc_mma_bf16_w<true>(dIn, alo + kk * (32 >> 4), kHi128, vlo + kk * (2048 >> 4), kHi128, idAV);
+                    }
+                    tc_commit(&sm->A_empty[bb]);
                     tc_commit(&sm->O_full[bb]);
                     tc_commit(&sm->empty[s]);
                 }
@@ -456,7 +477,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
         const int srow = qd * 32 + lane;         // state row (feature index) of this thread
         const int prow = qd * 16 + (lane & 15);  // row of the M = 64 tiles (16x32bx2 loads)
         const int pcol = hf * 32 + (lane >> 4) * 16;   // first of this thread's 16 columns
-        uint8_t *ystage = base + L::kOffY + tw * 2 * 1024;   // two 1 KB staging tiles of this warp
+        uint8_t *ystage = base + L::kOffY + tw * 1024;   // this warp's 1 KB staging tile
         uint32_t sync_phase = 0;
 
         float S[32];
@@ -539,10 +560,11 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
 
             // shared-memory operands and outputs
             if (has_b) {
-                if (c >= 1 && !warp_wait(cx, &sm->Sp_empty[0], (c - 1) & 1)) break;
-                if (c >= 1 && !warp_wait(cx, &sm->A_empty[0], (c - 1) & 1)) break;
+                const int sb = c % L::kSpBufs, sn = c / L::kSpBufs;
+                if (c >= L::kSpBufs && !warp_wait(cx, &sm->Sp_empty[sb], (sn - 1) & 1)) break;
+                if (c >= 2 && !warp_wait(cx, &sm->A_empty[bb], ((c >> 1) - 1) & 1)) break;
                 // Sprev (BF16) into columns hf*32 .. +31 of row srow: two 16-column blocks
-                uint8_t *spz = base + L::kOffSpZ;
+                uint8_t *spz = base + L::kOffSpZ + sb * kTileSpZ;
 #pragma unroll
                 for (int q4 = 0; q4 < 4; ++q4) {
                     uint4 w;
@@ -557,7 +579,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
                     const float zhi = __bfloat162float(__float2bfloat16_rn(zr));
                     *reinterpret_cast<uint32_t *>(spz + 4 * (kR * 32) + sw32_offset(srow, 0)) = pack_bf16x2(zhi, zr - zhi);
                 }
-                store_bf16x16(base + L::kOffA, prow, pcol >> 3, p);
+                store_bf16x16(base + L::kOffA + bb * kTileA, prow, pcol >> 3, p);
                 if (GATED && lane < 16) sm->densum[bb][hf][prow] = rowsum;
             } else if (has_a) {
                 // c == nch: the state after the last chunk
@@ -568,23 +590,23 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
                 if (slice == 0 && hf == 0) args.z_out[(size_t)bh * kR + srow] = zr;
             }
             if (has_e) {
-                // this warp's staging tile (c & 1) was last read by its store two iterations ago
-                if (lane == 0) tma_store_wait_read<1>();
+                // this warp's staging tile was last read by its store one iteration ago
+                if (lane == 0) tma_store_wait_read<0>();
                 __syncwarp();
-                uint8_t *yt = ystage + bb * 1024;
+                uint8_t *yt = ystage;
                 const int r = lane & 15, ch = (lane >> 4) * 2;   // row, first 16-byte chunk of 64-byte rows
                 *reinterpret_cast<uint4 *>(yt + sw64_offset(r, ch)) = make_uint4(yp[0], yp[1], yp[2], yp[3]);
                 *reinterpret_cast<uint4 *>(yt + sw64_offset(r, ch + 1)) = make_uint4(yp[4], yp[5], yp[6], yp[7]);
             }
             fence_proxy_async_smem();
             if (has_b) {
-                warp_arrive(&sm->Sp_full[0]);
-                warp_arrive(&sm->A_full[0]);
+                warp_arrive(&sm->Sp_full[c % L::kSpBufs]);
+                warp_arrive(&sm->A_full[bb]);
             }
             if (has_e) {
                 __syncwarp();
                 if (lane == 0) {
-                    tma_store_3d(&map_y, ystage + bb * 1024, slice * kDVS + hf * 32, (c - 2) * kC + qd * 16, bh);
+                    tma_store_3d(&map_y, ystage, slice * kDVS + hf * 32, (c - 2) * kC + qd * 16, bh);
                     tma_store_commit();
                 }
             }
@@ -603,7 +625,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
         if (lane == 0) tma_store_wait_all<0>();
     } else if (is_phi_warp(warp)) {
         // ------------------------------------------------------ phi warps
-        const int pp = (warp < 4 ? (warp - 2) * 32 : 64 + (warp - 12) * 32) + lane;   // 0..191
+        const int pp = phi_index(warp) * 32 + lane;   // 0..159; rows 0..63 of the gate scan on warps 2, 3
         uint32_t sync_phase = 0;
         bool ok = true;
         for (int c = 0; c < nch && ok; ++c) {

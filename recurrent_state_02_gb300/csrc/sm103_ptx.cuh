@@ -177,6 +177,23 @@ __device__ __forceinline__ void tc_mma_bf16(uint32_t d_tmem, uint64_t a_desc, ui
         : "memory");
 }
 
+// Same MMA with each descriptor passed as its two 32-bit words: the high words
+// are loop-invariant, and advancing along K only adds to the low word (the
+// start-address field), which keeps the issuing thread's instruction count low.
+template <bool ACC>
+__device__ __forceinline__ void tc_mma_bf16_w(uint32_t d_tmem, uint32_t a_lo, uint32_t a_hi, uint32_t b_lo,
+                                              uint32_t b_hi, uint32_t idesc)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t.reg .b64 da, db;\n\t"
+        "mov.b64 da, {%1, %2};\n\t"
+        "mov.b64 db, {%3, %4};\n\t"
+        "setp.ne.b32 p, %6, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %5, p;\n\t}"
+        ::"r"(d_tmem), "r"(a_lo), "r"(a_hi), "r"(b_lo), "r"(b_hi), "r"(idesc), "n"(ACC ? 1 : 0)
+        : "memory");
+}
+
 // Arrives once on `bar` when every tcgen05 operation this thread issued before
 // has completed.
 __device__ __forceinline__ void tc_commit(uint64_t *bar)
@@ -271,6 +288,17 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo_bytes
     d |= static_cast<uint64_t>(1) << 46;
     d |= static_cast<uint64_t>(mode & 7u) << 61;
     return d;
+}
+
+// The two 32-bit words of the same descriptor: the low word holds the start
+// address and LBO, the high word SBO, the version bits and the swizzle mode.
+__device__ __forceinline__ uint32_t desc_lo(uint32_t saddr, uint32_t lbo_bytes)
+{
+    return ((saddr & 0x3FFFFu) >> 4) | (((lbo_bytes >> 4) & 0x3FFFu) << 16);
+}
+__host__ __device__ constexpr uint32_t desc_hi(uint32_t sbo_bytes, uint32_t mode)
+{
+    return ((sbo_bytes >> 4) & 0x3FFFu) | (1u << 14) | ((mode & 7u) << 29);
 }
 
 __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo_bytes, uint32_t sbo_bytes)
