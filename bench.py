@@ -147,6 +147,21 @@ class ClockSampler:
                 "reasons": reasons, "samples": len(window)}
 
 
+def reduce_max(values, device, dist=None):
+    """Max over ranks of a list of floats (timings); identity without a process group."""
+    if dist is None:
+        return list(values)
+    import torch
+    t = torch.tensor(list(values), dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return t.tolist()
+
+
+def whole_job_rate(units_per_rank_step, world, steps, seconds):
+    """Units all ranks processed per second, against the slowest rank's time."""
+    return units_per_rank_step * world * steps / seconds
+
+
 def gpu_index(local_rank):
     vis = os.environ.get("CUDA_VISIBLE_DEVICES")
     if vis:
@@ -340,12 +355,9 @@ def run_ours(args, rank, world, local_rank):
     assert _native.lib().la_last_device_status(sh) == 0
 
     # max over ranks
-    if dist is not None:
-        tt = torch.tensor([step_s, prefill_s], device=dev, dtype=torch.float64)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        step_s, prefill_s = tt.tolist()
+    step_s, prefill_s = reduce_max([step_s, prefill_s], dev, dist)
     tokens_per_step = B * (T + 1)
-    value = tokens_per_step * world * args.steps / step_s
+    value = whole_job_rate(tokens_per_step, world, args.steps, step_s)
     ms_per_step = step_s / args.steps * 1e3
     pre_bytes = prefill_bytes(B, H, T, r, dv, with_state_in=True)
     pre_launch = prefill_s / args.steps
@@ -373,10 +385,7 @@ def run_ours(args, rank, world, local_rank):
     with torch.cuda.graph(gd, stream=stream):
         k_dec_big()
     dec_s = timed([gd] * N_ROT, args.steps, args.warmup)
-    if dist is not None:
-        tt = torch.tensor([dec_s], device=dev, dtype=torch.float64)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        dec_s = tt.item()
+    dec_s, = reduce_max([dec_s], dev, dist)
     dbytes = decode_bytes(dw.B, dw.H, dw.r, dw.dv)
     dec_launch = dec_s / args.steps
     dec_gbs = dbytes / dec_launch / 1e9
@@ -421,12 +430,9 @@ def run_ours(args, rank, world, local_rank):
         e1.record(stream)
         barrier()
     e2e_s = e0.elapsed_time(e1) / 1e3
-    if dist is not None:
-        tt = torch.tensor([e2e_s], device=dev, dtype=torch.float64)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        e2e_s = tt.item()
+    e2e_s, = reduce_max([e2e_s], dev, dist)
     assert _native.lib().la_last_device_status(sh) == 0
-    e2e = {"value": tokens_per_step * world * e2e_steps / e2e_s, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+    e2e = {"value": whole_job_rate(tokens_per_step, world, e2e_steps, e2e_s), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
            "d2h_bytes_per_step": d2h, "steps": e2e_steps, "ms_per_step": e2e_s / e2e_steps * 1e3}
 
     cpu = None
