@@ -127,13 +127,12 @@ la_status la_prefill_chunked(const void *q, const void *k, const void *v, la_dty
     }
     int *status = status_word();
     if (!status) return LA_ERR_CUDA;
-    CUtensorMap mq, mk, mv, my;
+    CUtensorMap mq, mk, mv;
     const long long planes = (long long)B * H;
-    // q, k, v: 64 x 64 load boxes, 128-byte swizzle; y: 32-column x 16-row store
-    // boxes (one per TMEM warp), 64-byte swizzle
-    const CUtensorMapSwizzle sw128 = CU_TENSOR_MAP_SWIZZLE_128B, sw64 = CU_TENSOR_MAP_SWIZZLE_64B;
+    // q, k, v: 64 x 64 load boxes, 128-byte swizzle
+    const CUtensorMapSwizzle sw128 = CU_TENSOR_MAP_SWIZZLE_128B;
     if (!make_map_bf16(&mq, q, planes, T, r, 64, 64, sw128) || !make_map_bf16(&mk, k, planes, T, r, 64, 64, sw128) ||
-        !make_map_bf16(&mv, v, planes, T, dv, 64, 64, sw128) || !make_map_bf16(&my, y, planes, T, dv, 32, 16, sw64))
+        !make_map_bf16(&mv, v, planes, T, dv, 64, 64, sw128))
         return LA_ERR_CUDA;
     la::PrefillTcArgs a;
     a.alpha = alpha;
@@ -141,13 +140,14 @@ la_status la_prefill_chunked(const void *q, const void *k, const void *v, la_dty
     a.z0 = z0;
     a.S_out = S_out;
     a.z_out = z_out;
+    a.y = static_cast<uint16_t *>(y);
     a.H = H;
     a.T = T;
     a.dv = dv;
     a.eps = eps;
     a.status = status;
     a.wait_limit_ns = la::kWaitLimitNs;
-    return from_cuda(la::launch_prefill_tc(mq, mk, mv, my, a, B, alpha != nullptr, st));
+    return from_cuda(la::launch_prefill_tc(mq, mk, mv, a, B, alpha != nullptr, st));
 }
 
 la_status la_decode_step(const void *q, const void *k, const void *v, la_dtype dtype, const float *alpha, float *S,

@@ -19,6 +19,7 @@ struct PrefillTcArgs {
     const float *z0;      // [B,H,128] or nullptr
     float *S_out;         // [B,H,128,dv]
     float *z_out;         // [B,H,128]
+    uint16_t *y;          // [B,H,T,dv] BF16 bits
     int H, T, dv;
     float eps;
     int *status;          // device status word
@@ -26,11 +27,11 @@ struct PrefillTcArgs {
 };
 
 // BF16 tensor-core prefill; r == 128, dv a multiple of 64, chunk 64.
-// Tensor maps: q, k over [B*H, T, 128]; v, y over [B*H, T, dv] (BF16, 128-byte
+// Tensor maps: q, k over [B*H, T, 128]; v over [B*H, T, dv] (BF16, 128-byte
 // swizzle, boxes of 64 x 64).
 cudaError_t launch_prefill_tc(const CUtensorMap &map_q, const CUtensorMap &map_k,
-                              const CUtensorMap &map_v, const CUtensorMap &map_y,
-                              const PrefillTcArgs &a, int B, bool gated, cudaStream_t stream);
+                              const CUtensorMap &map_v, const PrefillTcArgs &a, int B, bool gated,
+                              cudaStream_t stream);
 
 // Exact FP32 token recurrence (CUDA cores), r, dv <= 128.
 cudaError_t launch_prefill_f32(const float *q, const float *k, const float *v, const float *alpha,

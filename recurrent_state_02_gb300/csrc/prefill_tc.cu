@@ -22,18 +22,22 @@
 // carrying the FP32 state on chip (S and z in registers of the TMEM warps).
 // Per chunk (C = 64, r = 128):
 //   TMA    q, k (64 x 128) and the v slice (64 x 64) as BF16 tiles, 128-byte swizzle
+//   gate   (with a gate) the producer warp forms the chunk's gate products and
+//          the row w while the tiles are in flight
 //   phi    warps apply phi in place (FP32 math, BF16 result); with a gate they
-//          also form the gate products, w . V and the row w
+//          scale, once P is done, the rows of Q~ by Gamma_i and those of K~ by w_j
 //   MMA    P   = Q~ K~^T            M=64  N=64  K=128  -> TMEM
-//          dS  = K~^T (w . V)       M=128 N=64  K=64   -> TMEM
-//          dz  = K~^T w             M=128 N=16  K=64   (column 0; w = 1 without a gate)
-//          O   = Q~ Sprev           M=64  N=64  K=128  (Sprev as a BF16 operand)
-//          dn  = Q~ [zhi, zlo]      M=64  N=16  K=128  (zprev split into two BF16 parts,
-//                                                       so Q~ . zprev keeps ~16 bits)
-//          O  += A V                M=64  N=64  K=64   (A = masked, decayed P in BF16)
-//   TMEM   warps: S <- Gamma S + dS and z <- Gamma z + dz in FP32, Sprev and
-//          [zhi, zlo] -> shared memory; P -> A and its FP32 row sums;
-//          y = O / (Gamma dn + rowsum + eps) -> TMA store
+//          dS  = K~'^T V            M=128 N=64  K=64   -> TMEM (K~' = diag(w) K~, or K~
+//          dz  = K~'^T 1            M=128 N=16  K=64    without a gate; [V | 1] operand)
+//          O   = Q~' Sprev          M=64  N=64  K=128  (Sprev as a BF16 operand;
+//                                                       Q~' = Gamma Q~, or Q~ without a gate)
+//          dn  = Q~' [zhi, zlo]     M=64  N=16  K=128  (zprev split into two BF16 parts,
+//                                                       so Q~' . zprev keeps ~16 bits)
+//          O  += A [V | 1]          M=64  N=80  K=64   (A = masked, decayed P in BF16;
+//                                                       column 64 gains the row sums of A)
+//   TMEM   warps: S <- Gamma_last S + dS and z <- Gamma_last z + dz in FP32,
+//          Sprev and [zhi, zlo] -> shared memory; P -> A;
+//          y = O / (dn + eps) -> TMA store
 // Every barrier wait is bounded; on expiry the kernel records a timeout in the
 // device status word, drains its own copies and MMAs, frees TMEM and returns.
 
@@ -62,63 +66,64 @@ constexpr uint32_t kTileA = kC * kC * 2;      // 8 KB
 // [Sprev | zhi zlo 0..]: 128 feature rows x 80 columns, 32-byte swizzle, five
 // blocks of 16 columns (4 KB each); column 64 holds zhi and 65 zlo.
 constexpr uint32_t kTileSpZ = 5 * kR * 32;    // 20 KB
-// gated [w . V | w 0..]: 64 token rows x 80 columns, 32-byte swizzle, five blocks of 2 KB
-constexpr uint32_t kTileVw = 5 * kC * 32;     // 10 KB
-// ungated: the second 64-column block of [V | 1 0..] (128-byte swizzle, column 0 = 1)
+// the second 64-column block of [V | 1 0..] (128-byte swizzle, column 0 = 1)
 constexpr uint32_t kTileOnes = kC * 128;      // 8 KB
-constexpr uint32_t kTileY = kC * kDVS * 2;    // 8 KB
 
 // The phi warps avoid scheduler 1 (warps w with w % 4 == 1), which the MMA warp
 // shares with two TMEM warps: a busy neighbour there starves the MMA issue.
 __host__ __device__ constexpr bool is_phi_warp(int w) { return w == 2 || w == 3 || w == 12 || w == 14 || w == 15; }
 __host__ __device__ constexpr int phi_index(int w) { return w < 4 ? w - 2 : (w == 12 ? 2 : w - 11); }
 
-#ifndef LA_STAGES_UNGATED
-#define LA_STAGES_UNGATED 4
+// Gate data ring depth: the producer writes chunk c's entry up to a stage ring
+// ahead of its consumers, so the ring is deep enough that the entry it
+// overwrites (chunk c - kAux) was released long before.
+constexpr int kAux = 8;
+
+// Gate products of the chunks in flight (gated kernel only; chunk c in entry c % kAux).
+struct alignas(16) GateRing {
+    float gb[kAux][kC];         // cumulative log gate inside the chunk
+    int gz[kAux][kC];           // last row <= i whose gate is 0 (-1: none)
+    float gG[kAux][kC];         // Gamma_i
+    float gw[kAux][kC];         // w_j
+};
+
+#ifndef LA_STAGES
+#define LA_STAGES 4
 #endif
 #ifndef LA_SP_BUFS
-#define LA_SP_BUFS 1
+#define LA_SP_BUFS 2
 #endif
 
 template <bool GATED>
 struct Cfg {
-    static constexpr int kStages = GATED ? 3 : LA_STAGES_UNGATED;
-    static constexpr int kSpBufs = LA_SP_BUFS;                 // [Sprev | z] tiles
-    static constexpr int kNP = GATED ? 1 : 2;                  // P accumulator buffers
-    // TMEM columns: P, then [dS | dz] and [O | dn] blocks of 80 (x2), then O_intra (gated, x2);
-    // dz is column 64 of a [dS | dz] block, dn columns 64 and 65 of an [O | dn] block
+    static constexpr int kStages = LA_STAGES;
+    static constexpr int kSpBufs = GATED ? 1 : LA_SP_BUFS;     // [Sprev | z] tiles
+    static constexpr int kNP = 2;                              // P accumulator buffers
+    // TMEM columns: P (x2), then [dS | dz] and [O | dn] blocks of 80 (x2); dz is
+    // column 64 of a [dS | dz] block, dn columns 64 and 65 of an [O | dn] block
     static constexpr uint32_t kColP = 0;
     static constexpr uint32_t kColDS = kNP * 64;
     static constexpr uint32_t kColO = kColDS + 2 * 80;
-    static constexpr uint32_t kColO2 = kColO + 2 * 80;
-    static constexpr uint32_t kCols = kColO2 + (GATED ? 2 * 64 : 0);
+    static constexpr uint32_t kCols = kColO + 2 * 80;
     static_assert(kCols <= 512, "TMEM budget");
     // shared memory (offsets from a 1024-aligned base)
     static constexpr uint32_t kOffQ = 0, kOffK = kTileQ, kOffV = 2 * kTileQ;
-    static constexpr uint32_t kOffVw = kOffV + kTileV;                      // gated
-    static constexpr uint32_t kStageBytes = kOffVw + (GATED ? kTileVw : 0);
+    static constexpr uint32_t kStageBytes = kOffV + kTileV;
     static_assert(kStageBytes % 1024 == 0, "stage tiles stay 1024-byte aligned");
-    // A is double-buffered; [Sprev | z] is a single tile (the MMAs that read it
-    // are issued first, right after it is written); one 1 KB y staging tile per
-    // TMEM warp
+    // A is double-buffered; so is [Sprev | z] where shared memory allows (the
+    // gated kernel keeps its gate ring there instead)
     static constexpr uint32_t kOffA = kStages * kStageBytes;
     static constexpr uint32_t kOffSpZ = kOffA + 2 * kTileA;
-    static constexpr uint32_t kOffY = kOffSpZ + kSpBufs * kTileSpZ;         // 8 warps x 1 KB
-    static constexpr uint32_t kOffOnes = kOffY + kTileY;                    // ungated only
-    static constexpr uint32_t kOffSmall = kOffOnes + (GATED ? 0 : kTileOnes);
+    static constexpr uint32_t kOffOnes = kOffSpZ + kSpBufs * kTileSpZ;
+    static constexpr uint32_t kOffGate = kOffOnes + kTileOnes;
+    static constexpr uint32_t kOffSmall = kOffGate + (GATED ? sizeof(GateRing) : 0);
 };
 
 struct alignas(16) Small {
-    float gb[4][kC];            // cumulative log gate inside the chunk (chunk c in buffer c % 4)
-    int gz[4][kC];              // last row <= i whose gate is 0 (-1: none)
-    float gG[4][kC];            // Gamma_i
-    float gw[4][kC];            // w_j
-    float densum[2][2][kC];     // in-chunk row sums, two column halves
-    float carry[4];
-    uint64_t full[4], empty[4], phi_done[4];
+    uint64_t full[4], empty[4], phi_done[4], sc_done[4];
     uint64_t P_full[2], P_empty[2], dS_full[2], dS_empty[2], Sp_full[2], Sp_empty[2];
-    uint64_t A_full[2], A_empty[2], O_full[2], O_empty[2], aux_empty[4];
-    uint64_t mma_done, tm_sync, phi_sync;
+    uint64_t A_full[2], A_empty[2], O_full[2], O_empty[2], aux_empty[kAux];
+    uint64_t mma_done;
     uint32_t tmem_base;
     int abort_flag;
 };
@@ -128,14 +133,26 @@ constexpr uint32_t smem_bytes() { return Cfg<GATED>::kOffSmall + sizeof(Small) +
 static_assert(smem_bytes<false>() <= 232448, "shared memory budget");
 static_assert(smem_bytes<true>() <= 232448, "shared memory budget");
 
-// phi(x) = ELU(x) + 1: x + 1 for x > 0, e^x = 2^(x log2 e) otherwise (NaN
-// propagates).  The base-2 exponential is the hardware approximation with
-// flush-to-zero (results below 2^-126, i.e. x < -87.3, become 0).
-__device__ __forceinline__ float phi_elu1(float x)
+// phi(x) = ELU(x) + 1 on a pair of BF16 values, in packed BF16 arithmetic:
+// phi(x) = max(min(e^x, 1), x + 1).  For x <= 0, e^x >= 1 + x picks e^x; for
+// x > 0, min(e^x, 1) = 1 <= x + 1 picks x + 1 (NaN propagates through the .NaN
+// forms).  e^x = 2^(x log2 e) with log2 e split into two BF16 parts, so that
+// the product is rounded once; the base-2 exponential is the hardware
+// approximation with flush-to-zero (phi = 0 below x = -87.3).
+__device__ __forceinline__ uint32_t phi_bf16x2(uint32_t x)
 {
-    float e;
-    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e) : "f"(x * 1.4426950408889634f));
-    return x > 0.f ? x + 1.f : e;
+    constexpr uint32_t kLog2eHi = 0x3FB93FB9u;   // 1.4453125
+    constexpr uint32_t kLog2eLo = 0xBB2CBB2Cu;   // -0.00262451171875
+    constexpr uint32_t kOne = 0x3F803F80u;
+    constexpr uint32_t kZero = 0x80008000u;      // -0
+    uint32_t t, e, p, r;
+    asm("fma.rn.bf16x2 %0, %1, %2, %3;" : "=r"(t) : "r"(x), "r"(kLog2eLo), "r"(kZero));
+    asm("fma.rn.bf16x2 %0, %1, %2, %3;" : "=r"(t) : "r"(x), "r"(kLog2eHi), "r"(t));
+    asm("ex2.approx.ftz.bf16x2 %0, %1;" : "=r"(e) : "r"(t));
+    asm("min.NaN.bf16x2 %0, %1, %2;" : "=r"(e) : "r"(e), "r"(kOne));
+    asm("fma.rn.bf16x2 %0, %1, %2, %3;" : "=r"(p) : "r"(x), "r"(kOne), "r"(kOne));
+    asm("max.NaN.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(e), "r"(p));
+    return r;
 }
 
 struct Ctx {
@@ -195,30 +212,64 @@ __device__ __forceinline__ void warp_arrive(uint64_t *bar)
     if ((threadIdx.x & 31) == 0) mbar_arrive(bar);
 }
 
-// Bounded barrier among the warps that share `bar` (count = number of warps).
-__device__ __forceinline__ bool group_sync(Ctx &cx, uint64_t *bar, uint32_t &phase)
-{
-    warp_arrive(bar);
-    const bool ok = warp_wait(cx, bar, phase);
-    phase ^= 1u;
-    return ok;
-}
-
 // Applies phi to the 8 BF16 values of one 16-byte chunk.
 __device__ __forceinline__ uint4 phi8(uint4 raw)
 {
+    return make_uint4(phi_bf16x2(raw.x), phi_bf16x2(raw.y), phi_bf16x2(raw.z), phi_bf16x2(raw.w));
+}
+
+// Multiplies the 8 BF16 values of one 16-byte chunk by s: s is split into two
+// BF16 parts (s = hi + lo to about 2^-16), so each product is rounded once.
+__device__ __forceinline__ uint4 scale8(uint4 raw, float s)
+{
+    const uint32_t hi = pack_bf16x2(s, s);
+    const float lo_f = s - bf16_lo(hi);
+    const uint32_t lo = pack_bf16x2(lo_f, lo_f);
+    constexpr uint32_t kZero = 0x80008000u;
     uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
 #pragma unroll
-    for (int e = 0; e < 4; ++e) w[e] = pack_bf16x2(phi_elu1(bf16_lo(w[e])), phi_elu1(bf16_hi(w[e])));
+    for (int e = 0; e < 4; ++e) {
+        uint32_t t;
+        asm("fma.rn.bf16x2 %0, %1, %2, %3;" : "=r"(t) : "r"(w[e]), "r"(lo), "r"(kZero));
+        asm("fma.rn.bf16x2 %0, %1, %2, %3;" : "=r"(w[e]) : "r"(w[e]), "r"(hi), "r"(t));
+    }
     return make_uint4(w[0], w[1], w[2], w[3]);
 }
 
-__device__ __forceinline__ uint4 scale8(uint4 raw, float s)
+// Gate products of one chunk, by one warp; lane l holds tokens 2l and 2l + 1
+// (gates past the end of the sequence are 1).  b_i is the in-chunk inclusive
+// sum of log alpha, zl_i the last row <= i whose gate is exactly 0 (-1: none);
+// Gamma_i = e^{b_i} (0 once a zero gate has been passed) and w_j =
+// e^{b_last - b_j} (0 for keys before the chunk's last zero gate).
+__device__ __forceinline__ void gate_products(float a0, float a1, int lane, int gq, GateRing *gr)
 {
-    uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+    const int j0 = 2 * lane;
+    const float l0 = a0 > 0.f ? logf(a0) : 0.f;
+    const float l1 = a1 > 0.f ? logf(a1) : 0.f;
+    const int zp0 = a0 > 0.f ? -1 : j0;
+    const int zp1 = a1 > 0.f ? zp0 : j0 + 1;
+    // inclusive warp scan of the pair totals (sum) and the pair's last zero gate (max)
+    float inc = l0 + l1;
+    int zinc = zp1;
 #pragma unroll
-    for (int e = 0; e < 4; ++e) w[e] = pack_bf16x2(s * bf16_lo(w[e]), s * bf16_hi(w[e]));
-    return make_uint4(w[0], w[1], w[2], w[3]);
+    for (int off = 1; off < 32; off <<= 1) {
+        const float lo = __shfl_up_sync(0xffffffffu, inc, off);
+        const int zo = __shfl_up_sync(0xffffffffu, zinc, off);
+        if (lane >= off) { inc += lo; zinc = max(zinc, zo); }
+    }
+    float ex = __shfl_up_sync(0xffffffffu, inc, 1);
+    int zex = __shfl_up_sync(0xffffffffu, zinc, 1);
+    if (lane == 0) { ex = 0.f; zex = -1; }
+    const float b0 = ex + l0, b1 = b0 + l1;
+    const int z0 = max(zex, zp0), z1 = max(zex, zp1);
+    const float blast = __shfl_sync(0xffffffffu, b1, 31);
+    const int zlast = __shfl_sync(0xffffffffu, z1, 31);
+    const float w0 = zlast <= j0 ? expf(blast - b0) : 0.f;
+    const float w1 = zlast <= j0 + 1 ? expf(blast - b1) : 0.f;
+    *reinterpret_cast<float2 *>(&gr->gb[gq][j0]) = make_float2(b0, b1);
+    *reinterpret_cast<int2 *>(&gr->gz[gq][j0]) = make_int2(z0, z1);
+    *reinterpret_cast<float2 *>(&gr->gG[gq][j0]) = make_float2(z0 < 0 ? expf(b0) : 0.f, z1 < 0 ? expf(b1) : 0.f);
+    *reinterpret_cast<float2 *>(&gr->gw[gq][j0]) = make_float2(w0, w1);
 }
 
 __device__ __forceinline__ void store_bf16x16(uint8_t *tile, int row, int chunk0, const float (&v)[16])
@@ -235,14 +286,14 @@ __device__ __forceinline__ void store_bf16x16(uint8_t *tile, int row, int chunk0
 template <bool GATED>
 __global__ void __launch_bounds__(kThreads, 1)
 prefill_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
-                  const __grid_constant__ CUtensorMap map_v, const __grid_constant__ CUtensorMap map_y,
-                  const PrefillTcArgs args)
+                  const __grid_constant__ CUtensorMap map_v, const PrefillTcArgs args)
 {
     using L = Cfg<GATED>;
     constexpr int NST = L::kStages, NP = L::kNP;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *base = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     Small *sm = reinterpret_cast<Small *>(base + L::kOffSmall);
+    GateRing *gr = reinterpret_cast<GateRing *>(base + L::kOffGate);   // gated only
     Ctx cx{sm, args.wait_limit_ns, args.status};
 
     const int slice = blockIdx.x;
@@ -257,9 +308,10 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
     // ------------------------------------------------------------ set-up
     if (threadIdx.x == 0) {
         for (int s = 0; s < NST; ++s) {
-            mbar_init(&sm->full[s], 1);
+            mbar_init(&sm->full[s], GATED ? 2 : 1);   // TMA bytes (+ gate data)
             mbar_init(&sm->empty[s], 1);
             mbar_init(&sm->phi_done[s], kPhiWarps);
+            mbar_init(&sm->sc_done[s], kPhiWarps);
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&sm->P_full[i], 1);
@@ -273,36 +325,26 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
             mbar_init(&sm->O_full[i], 1);
             mbar_init(&sm->O_empty[i], kTmWarps);
         }
-        for (int i = 0; i < 4; ++i) mbar_init(&sm->aux_empty[i], kTmWarps);
+        for (int i = 0; i < kAux; ++i) mbar_init(&sm->aux_empty[i], kTmWarps);
         mbar_init(&sm->mma_done, 1);
-        mbar_init(&sm->tm_sync, kTmWarps);
-        mbar_init(&sm->phi_sync, kPhiWarps);
         sm->abort_flag = 0;
         fence_mbarrier_init();
         tma_prefetch_desc(&map_q);
         tma_prefetch_desc(&map_k);
         tma_prefetch_desc(&map_v);
-        tma_prefetch_desc(&map_y);
     }
     // Constant operand parts: the z block (columns 64..79) of the [Sprev | z]
-    // tile and the w block of every gated [w . V | w] tile start at zero (only
-    // columns 64, 65 resp. 64 are written later); the ungated ones block is
-    // complete here (column 0 = 1 in every token row).
+    // tile starts at zero (only columns 64 and 65 are written later); the ones
+    // block is complete here (column 0 = 1 in every token row).
     for (int i = threadIdx.x; i < L::kSpBufs * (kR * 32 / 16); i += kThreads) {
         const int buf = i / (kR * 32 / 16), j = i % (kR * 32 / 16);
         reinterpret_cast<uint4 *>(base + L::kOffSpZ + buf * kTileSpZ + 4 * kR * 32)[j] = make_uint4(0, 0, 0, 0);
     }
-    if (GATED) {
-        for (int s = 0; s < NST; ++s)
-            for (int i = threadIdx.x; i < kC * 32 / 16; i += kThreads)
-                reinterpret_cast<uint4 *>(stage_ptr(s) + L::kOffVw + 4 * kC * 32)[i] = make_uint4(0, 0, 0, 0);
-    } else {
-        for (int i = threadIdx.x; i < (int)kTileOnes / 16; i += kThreads)
-            reinterpret_cast<uint4 *>(base + L::kOffOnes)[i] = make_uint4(0, 0, 0, 0);
-        __syncthreads();
-        if (threadIdx.x < kC)   // element (column 0, token row k): 16-byte chunk 0 of row k after the swizzle
-            *reinterpret_cast<uint16_t *>(base + L::kOffOnes + sw128_offset(threadIdx.x, 0)) = 0x3F80u;
-    }
+    for (int i = threadIdx.x; i < (int)kTileOnes / 16; i += kThreads)
+        reinterpret_cast<uint4 *>(base + L::kOffOnes)[i] = make_uint4(0, 0, 0, 0);
+    __syncthreads();
+    if (threadIdx.x < kC)   // element (column 0, token row k): 16-byte chunk 0 of row k after the swizzle
+        *reinterpret_cast<uint16_t *>(base + L::kOffOnes + sw128_offset(threadIdx.x, 0)) = 0x3F80u;
     fence_proxy_async_smem();
     if (warp == kWarpMma) {
         tmem_alloc(&sm->tmem_base, 512);
@@ -325,42 +367,57 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
 
     if (warp == kWarpTma) {
         // ------------------------------------------------------- producer
-        if (lane == 0) {
-            int issued = 0;
-            for (int c = 0; c < nch; ++c) {
-                const int s = c % NST;
-                if (c >= NST && !wait(cx, &sm->empty[s], ((c / NST) - 1) & 1)) break;
-                if (aborted(cx)) break;
-                uint8_t *st = stage_ptr(s);
+        // Lane 0 issues the tile loads of a stage.  With a gate the whole warp
+        // then forms the chunk's gate products and makes the stage's second
+        // arrival; the gates are read before the wait for the free stage, so
+        // their latency hides behind it.
+        int issued = 0;
+        for (int c = 0; c < nch; ++c) {
+            const int s = c % NST;
+            const int t0 = c * kC;
+            float a0 = 1.f, a1 = 1.f;
+            if (GATED) {
+                const float *ap = args.alpha + (size_t)bh * T;
+                if (t0 + 2 * lane < T) a0 = ap[t0 + 2 * lane];
+                if (t0 + 2 * lane + 1 < T) a1 = ap[t0 + 2 * lane + 1];
+            }
+            if (c >= NST && !warp_wait(cx, &sm->empty[s], ((c / NST) - 1) & 1)) break;
+            if (GATED && c >= kAux && !warp_wait(cx, &sm->aux_empty[c % kAux], ((c / kAux) - 1) & 1)) break;
+            if (__shfl_sync(0xffffffffu, aborted(cx) ? 1 : 0, 0)) break;
+            uint8_t *st = stage_ptr(s);
+            if (lane == 0) {
                 mbar_arrive_expect_tx(&sm->full[s], 2 * kTileQ + kTileV);
-                const int t0 = c * kC;
                 tma_load_3d(st + L::kOffQ, &map_q, &sm->full[s], 0, t0, bh);
                 tma_load_3d(st + L::kOffQ + kTileQ / 2, &map_q, &sm->full[s], 64, t0, bh);
                 tma_load_3d(st + L::kOffK, &map_k, &sm->full[s], 0, t0, bh);
                 tma_load_3d(st + L::kOffK + kTileQ / 2, &map_k, &sm->full[s], 64, t0, bh);
                 tma_load_3d(st + L::kOffV, &map_v, &sm->full[s], slice * kDVS, t0, bh);
-                issued = c + 1;
             }
-            if (aborted(cx)) {
-                // Drain: every issued load must land before the CTA may exit.
-                for (int c = (issued > NST ? issued - NST : 0); c < issued; ++c)
-                    mbar_wait(&sm->full[c % NST], (c / NST) & 1, cx.limit);
+            if (GATED) {
+                gate_products(a0, a1, lane, c % kAux, gr);
+                warp_arrive(&sm->full[s]);
             }
+            issued = c + 1;
         }
+        if (lane == 0 && aborted(cx)) {
+            // Drain: every issued load must land before the CTA may exit.
+            for (int c = (issued > NST ? issued - NST : 0); c < issued; ++c)
+                mbar_wait(&sm->full[c % NST], (c / NST) & 1, cx.limit);
+        }
+        __syncwarp();
     } else if (warp == kWarpMma) {
         // ------------------------------------------------------------ MMA
-        // The whole warp runs this loop so that descriptors and loop state are
-        // warp-uniform; lane 0 alone issues the MMAs and commits.
-        // Issue order per iteration: chunk c's O = Q~ Sprev (+) A V, then the
+        // Lane 0 alone runs the issue loop (tcgen05.mma and tcgen05.commit are
+        // issued by one thread); the other lanes wait at the teardown barrier.
+        // Issue order per iteration: chunk c's O = Q~ Sprev + A V, then the
         // scores of chunk c + NP and the state increment of chunk c + 1, so that
         // the TMEM warps' waits are on work issued an iteration earlier.
-        {
-            const bool leader = lane == 0;
+        if (lane == 0) {
             constexpr uint32_t idP = idesc_bf16_f32(64, 64, false, false);
             constexpr uint32_t idDS = idesc_bf16_f32(128, 80, true, true);   // [dS | dz]
             constexpr uint32_t idQS = idesc_bf16_f32(64, 80, false, true);   // [O | dn]
-            // gated: O_intra = A V; ungated: [O | dn] += A [V | 1] (column 64 gains the row sums of A)
-            constexpr uint32_t idAV = GATED ? idesc_bf16_f32(64, 64, false, true) : idesc_bf16_f32(64, 80, false, true);
+            // [O | dn] += A [V | 1]: column 64 gains the row sums of A
+            constexpr uint32_t idAV = idesc_bf16_f32(64, 80, false, true);
             const uint32_t aOnes = smem_u32(base + L::kOffOnes);
             constexpr uint32_t kHi128 = desc_hi(1024, 2), kHi32 = desc_hi(256, 6);   // SBO and swizzle words
             // P = Q~ K~^T for chunk c
@@ -368,45 +425,39 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
                 const int s = c % NST, pb = c % NP, pn = c / NP;
                 const uint32_t st = smem_u32(stage_ptr(s));
                 const uint32_t aQ = st + L::kOffQ, aK = st + L::kOffK;
-                if (!warp_wait(cx, &sm->phi_done[s], (c / NST) & 1)) return false;
-                if (c >= NP && !warp_wait(cx, &sm->P_empty[pb], (pn - 1) & 1)) return false;
+                if (!wait(cx, &sm->phi_done[s], (c / NST) & 1)) return false;
+                if (c >= NP && !wait(cx, &sm->P_empty[pb], (pn - 1) & 1)) return false;
                 tc_fence_after();
-                if (leader) {
-                    const uint32_t qlo = desc_lo(aQ, 16), klo = desc_lo(aK, 16), dP = tmem + L::kColP + pb * 64;
+                const uint32_t qlo = desc_lo(aQ, 16), klo = desc_lo(aK, 16), dP = tmem + L::kColP + pb * 64;
 #pragma unroll
-                    for (int kk = 0; kk < 8; ++kk) {
-                        const uint32_t o = ((kk >> 2) * (kTileQ / 2) + (kk & 3) * 32) >> 4;
-                        if (kk == 0) tc_mma_bf16_w<false>(dP, qlo + o, kHi128, klo + o, kHi128, idP);
-                        else tc_mma_bf16_w<true>(dP, qlo + o, kHi128, klo + o, kHi128, idP);
-                    }
-                    tc_commit(&sm->P_full[pb]);
+                for (int kk = 0; kk < 8; ++kk) {
+                    const uint32_t o = ((kk >> 2) * (kTileQ / 2) + (kk & 3) * 32) >> 4;
+                    if (kk == 0) tc_mma_bf16_w<false>(dP, qlo + o, kHi128, klo + o, kHi128, idP);
+                    else tc_mma_bf16_w<true>(dP, qlo + o, kHi128, klo + o, kHi128, idP);
                 }
-                __syncwarp();
+                tc_commit(&sm->P_full[pb]);
                 return true;
             };
-            // [dS | dz] = K~^T [w . V | w] for chunk c (phi_done of chunk c was
-            // waited for by issue_p(c), which always comes first)
+            // [dS | dz] = K~'^T [V | 1] for chunk c, K~' = diag(w) K~ with a gate
+            // (phi_done of chunk c was waited for by issue_p(c), which always
+            // comes first; the gated row scaling follows P of chunk c)
             auto issue_ds = [&](int c) -> bool {
                 const int s = c % NST, bb = c & 1, n = c >> 1;
                 const uint32_t st = smem_u32(stage_ptr(s));
                 const uint32_t aK = st + L::kOffK;
-                // B = [w . V | w] (gated, 32-byte swizzle) or [V | 1] (V tile + the ones block at LBO)
-                const uint32_t blo = GATED ? desc_lo(st + L::kOffVw, kC * 32) : desc_lo(st + L::kOffV, aOnes - (st + L::kOffV));
-                constexpr uint32_t bhi = GATED ? kHi32 : kHi128;
-                constexpr uint32_t bStep = (GATED ? 512 : 2048) >> 4;   // 16 token rows
-                if (c >= 2 && !warp_wait(cx, &sm->dS_empty[bb], (n - 1) & 1)) return false;
+                // B = [V | 1]: the V tile, then the ones block at LBO
+                const uint32_t blo = desc_lo(st + L::kOffV, aOnes - (st + L::kOffV));
+                if (GATED && !wait(cx, &sm->sc_done[s], (c / NST) & 1)) return false;
+                if (c >= 2 && !wait(cx, &sm->dS_empty[bb], (n - 1) & 1)) return false;
                 tc_fence_after();
                 const uint32_t dDS = tmem + L::kColDS + bb * 80;
-                if (leader) {
-                    const uint32_t klo = desc_lo(aK, kTileQ / 2);   // K~^T: MN-major, two 64-feature blocks
+                const uint32_t klo = desc_lo(aK, kTileQ / 2);   // K~^T: MN-major, two 64-feature blocks
 #pragma unroll
-                    for (int kk = 0; kk < 4; ++kk) {
-                        if (kk == 0) tc_mma_bf16_w<false>(dDS, klo, kHi128, blo, bhi, idDS);
-                        else tc_mma_bf16_w<true>(dDS, klo + kk * (2048 >> 4), kHi128, blo + kk * bStep, bhi, idDS);
-                    }
-                    tc_commit(&sm->dS_full[bb]);
+                for (int kk = 0; kk < 4; ++kk) {
+                    if (kk == 0) tc_mma_bf16_w<false>(dDS, klo, kHi128, blo, kHi128, idDS);
+                    else tc_mma_bf16_w<true>(dDS, klo + kk * (2048 >> 4), kHi128, blo + kk * (2048 >> 4), kHi128, idDS);
                 }
-                __syncwarp();
+                tc_commit(&sm->dS_full[bb]);
                 return true;
             };
             bool ok = true;
@@ -420,51 +471,41 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
                 const uint32_t aA = smem_u32(base + L::kOffA + bb * kTileA);
                 const int sb = c % L::kSpBufs, sn = c / L::kSpBufs;
                 const uint32_t aSpZ = smem_u32(base + L::kOffSpZ + sb * kTileSpZ);
-                // [O | dn] = Q~ [Sprev | zhi zlo]
-                if (c >= 2 && !warp_wait(cx, &sm->O_empty[bb], (n - 1) & 1)) break;
-                if (!warp_wait(cx, &sm->Sp_full[sb], sn & 1)) break;
+                // [O | dn] = Q~ [Sprev | zhi zlo] (gated: Q~ rows already scaled by Gamma_i)
+                if (c >= 2 && !wait(cx, &sm->O_empty[bb], (n - 1) & 1)) break;
+                if (GATED && !wait(cx, &sm->sc_done[s], (c / NST) & 1)) break;
+                if (!wait(cx, &sm->Sp_full[sb], sn & 1)) break;
                 tc_fence_after();
                 const uint32_t dO = tmem + L::kColO + bb * 80;
-                if (leader) {
-                    const uint32_t qlo = desc_lo(aQ, 16), slo = desc_lo(aSpZ, kR * 32);
+                const uint32_t qlo = desc_lo(aQ, 16), slo = desc_lo(aSpZ, kR * 32);
 #pragma unroll
-                    for (int kk = 0; kk < 8; ++kk) {
-                        const uint32_t o = ((kk >> 2) * (kTileQ / 2) + (kk & 3) * 32) >> 4;
-                        if (kk == 0) tc_mma_bf16_w<false>(dO, qlo, kHi128, slo, kHi32, idQS);
-                        else tc_mma_bf16_w<true>(dO, qlo + o, kHi128, slo + kk * (512 >> 4), kHi32, idQS);
-                    }
-                    tc_commit(&sm->Sp_empty[sb]);
+                for (int kk = 0; kk < 8; ++kk) {
+                    const uint32_t o = ((kk >> 2) * (kTileQ / 2) + (kk & 3) * 32) >> 4;
+                    if (kk == 0) tc_mma_bf16_w<false>(dO, qlo, kHi128, slo, kHi32, idQS);
+                    else tc_mma_bf16_w<true>(dO, qlo + o, kHi128, slo + kk * (512 >> 4), kHi32, idQS);
                 }
-                __syncwarp();
-                // O (intra) (+)= A V
-                if (!warp_wait(cx, &sm->A_full[bb], n & 1)) break;
+                tc_commit(&sm->Sp_empty[sb]);
+                // [O | dn] += A [V | 1]
+                if (!wait(cx, &sm->A_full[bb], n & 1)) break;
                 tc_fence_after();
-                const uint32_t dIn = GATED ? tmem + L::kColO2 + bb * 64 : dO;
-                if (leader) {
-                    const uint32_t alo = desc_lo(aA, 16);
-                    const uint32_t vlo = GATED ? desc_lo(aV, kTileV) : desc_lo(aV, aOnes - aV);
+                const uint32_t alo = desc_lo(aA, 16);
+                const uint32_t vlo = desc_lo(aV, aOnes - aV);
 #pragma unroll
-                    for (int kk = 0; kk < 4; ++kk) {
-                        if (GATED && kk == 0) tc_mma_bf16_w<false>(dIn, alo, kHi128, vlo, kHi128, idAV);
-                        else tc_mma_bf16_w<true>(dIn, alo + kk * (32 >> 4), kHi128, vlo + kk * (2048 >> 4), kHi128, idAV);
-                    }
-                    tc_commit(&sm->A_empty[bb]);
-                    tc_commit(&sm->O_full[bb]);
-                    tc_commit(&sm->empty[s]);
-                }
-                __syncwarp();
+                for (int kk = 0; kk < 4; ++kk)
+                    tc_mma_bf16_w<true>(dO, alo + kk * (32 >> 4), kHi128, vlo + kk * (2048 >> 4), kHi128, idAV);
+                tc_commit(&sm->A_empty[bb]);
+                tc_commit(&sm->O_full[bb]);
+                tc_commit(&sm->empty[s]);
                 // look-ahead: the stage of chunk c is released above before these
                 // wait for the stages of chunks c + 1 .. c + NP
                 if (c + NP < nch && !issue_p(c + NP)) break;
                 if (c + 1 < nch && !issue_ds(c + 1)) break;
             }
-            // Every MMA the leader issued completes before TMEM is released.
-            if (leader) {
-                tc_commit(&sm->mma_done);
-                mbar_wait(&sm->mma_done, 0, cx.limit);
-            }
-            __syncwarp();
+            // Every MMA issued above completes before TMEM is released.
+            tc_commit(&sm->mma_done);
+            mbar_wait(&sm->mma_done, 0, cx.limit);
         }
+        __syncwarp();
     } else if (warp >= kWarpTm0 && warp < kWarpTm0 + kTmWarps) {
         // ----------------------------------------------------- TMEM warps
         // Iteration c: fold dS of chunk c-1 into the state (the state chunk c
@@ -477,8 +518,6 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
         const int srow = qd * 32 + lane;         // state row (feature index) of this thread
         const int prow = qd * 16 + (lane & 15);  // row of the M = 64 tiles (16x32bx2 loads)
         const int pcol = hf * 32 + (lane >> 4) * 16;   // first of this thread's 16 columns
-        uint8_t *ystage = base + L::kOffY + tw * 1024;   // this warp's 1 KB staging tile
-        uint32_t sync_phase = 0;
 
         float S[32];
         float zr = z_init;
@@ -487,8 +526,6 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
 #pragma unroll
             for (int j = 0; j < 32; ++j) S[j] = src ? src[j] : 0.f;
         }
-        // gated: in-chunk row sums and Gamma_i of chunks c-1 and c-2
-        float dint1 = 0.f, dint2 = 0.f, gam1 = 1.f, gam2 = 1.f;
 
         for (int c = 0; c < nch + 2; ++c) {
             const bool has_a = c >= 1 && c <= nch;   // dS of chunk c-1
@@ -497,25 +534,28 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
             const int bb = c & 1, pb = c % NP, pn = c / NP;
             const int ab = (c - 1) & 1;
             // outputs of chunk c-2 (its O was complete a full iteration ago)
-            uint32_t yp[8];
             if (has_e) {
                 if (!warp_wait(cx, &sm->O_full[bb], ((c - 2) >> 1) & 1)) break;
                 tc_fence_after();
-                float o[16], o2[16], dn;
+                float o[16], dn;
                 tc_ld_16x32bx2_x16<16>(tmem + lane_base + L::kColO + bb * 80 + hf * 32, o);
-                if (GATED) tc_ld_16x32bx2_x16<16>(tmem + lane_base + L::kColO2 + bb * 64 + hf * 32, o2);
                 tc_ld_16x32bx2_x1<1>(tmem + lane_base + L::kColO + bb * 80 + 64, dn);
                 tc_wait_ld();
                 tc_fence_before();
                 warp_arrive(&sm->O_empty[bb]);
-                // columns 64 + 65: Q~ . zprev (two parts), plus the row sums of A without a gate
+                // columns 64 + 65: (Gamma_i) Q~ . zprev in two parts, plus the row sums of A
                 dn += __shfl_xor_sync(0xffffffffu, dn, 16);
-                const float inv = __frcp_rn((GATED ? fmaf(gam2, dn, dint2) : dn) + args.eps);
+                const float inv = __frcp_rn(dn + args.eps);
+                uint32_t yp[8];
 #pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    const float y0 = (GATED ? fmaf(gam2, o[2 * e], o2[2 * e]) : o[2 * e]) * inv;
-                    const float y1 = (GATED ? fmaf(gam2, o[2 * e + 1], o2[2 * e + 1]) : o[2 * e + 1]) * inv;
-                    yp[e] = pack_bf16x2(y0, y1);
+                for (int e = 0; e < 8; ++e) yp[e] = pack_bf16x2(o[2 * e] * inv, o[2 * e + 1] * inv);
+                // 16 columns (32 bytes) of token row prow, straight to global memory
+                // (streaming stores: y is not read again here)
+                const int t = (c - 2) * kC + prow;
+                if (t < T) {
+                    uint4 *dst = reinterpret_cast<uint4 *>(args.y + ((size_t)bh * T + t) * args.dv + slice * kDVS + pcol);
+                    __stcs(dst, make_uint4(yp[0], yp[1], yp[2], yp[3]));
+                    __stcs(dst + 1, make_uint4(yp[4], yp[5], yp[6], yp[7]));
                 }
             }
             // dS of chunk c-1 and the scores of chunk c
@@ -535,27 +575,23 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
             if (has_b) warp_arrive(&sm->P_empty[pb]);
 
             if (has_a) {
-                const float g = GATED ? sm->gG[(c - 1) & 3][kC - 1] : 1.f;
+                const float g = GATED ? gr->gG[(c - 1) % kAux][kC - 1] : 1.f;
 #pragma unroll
                 for (int j = 0; j < 32; ++j) S[j] = GATED ? fmaf(g, S[j], d[j]) : S[j] + d[j];
                 zr = GATED ? fmaf(g, zr, dz) : zr + dz;
+                if (GATED) warp_arrive(&sm->aux_empty[(c - 1) % kAux]);   // gate data of chunk c-1 is done
             }
-            float rowsum = 0.f;
             if (has_b) {
-                const int gq = c & 3;
-                const float bi = GATED ? sm->gb[gq][prow] : 0.f;
-                const int zi = GATED ? sm->gz[gq][prow] : -1;
+                const int gq = c % kAux;
+                const float bi = GATED ? gr->gb[gq][prow] : 0.f;
+                const int zi = GATED ? gr->gz[gq][prow] : -1;
 #pragma unroll
                 for (int e = 0; e < 16; ++e) {
                     const int j = pcol + e;
                     float a = (j <= prow) ? p[e] : 0.f;
-                    if (GATED) {
-                        a = (j <= prow && zi <= j) ? a * __expf(bi - sm->gb[gq][j]) : 0.f;
-                        rowsum += a;
-                    }
+                    if (GATED) a = (j <= prow && zi <= j) ? a * __expf(bi - gr->gb[gq][j]) : 0.f;
                     p[e] = a;
                 }
-                if (GATED) rowsum += __shfl_xor_sync(0xffffffffu, rowsum, 16);
             }
 
             // shared-memory operands and outputs
@@ -580,7 +616,6 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
                     *reinterpret_cast<uint32_t *>(spz + 4 * (kR * 32) + sw32_offset(srow, 0)) = pack_bf16x2(zhi, zr - zhi);
                 }
                 store_bf16x16(base + L::kOffA + bb * kTileA, prow, pcol >> 3, p);
-                if (GATED && lane < 16) sm->densum[bb][hf][prow] = rowsum;
             } else if (has_a) {
                 // c == nch: the state after the last chunk
                 float *dst = args.S_out + ((size_t)bh * kR + srow) * args.dv + slice * kDVS + hf * 32;
@@ -589,78 +624,40 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
                     *reinterpret_cast<float4 *>(dst + j) = make_float4(S[j], S[j + 1], S[j + 2], S[j + 3]);
                 if (slice == 0 && hf == 0) args.z_out[(size_t)bh * kR + srow] = zr;
             }
-            if (has_e) {
-                // this warp's staging tile was last read by its store one iteration ago
-                if (lane == 0) tma_store_wait_read<0>();
-                __syncwarp();
-                uint8_t *yt = ystage;
-                const int r = lane & 15, ch = (lane >> 4) * 2;   // row, first 16-byte chunk of 64-byte rows
-                *reinterpret_cast<uint4 *>(yt + sw64_offset(r, ch)) = make_uint4(yp[0], yp[1], yp[2], yp[3]);
-                *reinterpret_cast<uint4 *>(yt + sw64_offset(r, ch + 1)) = make_uint4(yp[4], yp[5], yp[6], yp[7]);
-            }
             fence_proxy_async_smem();
             if (has_b) {
                 warp_arrive(&sm->Sp_full[c % L::kSpBufs]);
                 warp_arrive(&sm->A_full[bb]);
             }
-            if (has_e) {
-                __syncwarp();
-                if (lane == 0) {
-                    tma_store_3d(&map_y, ystage, slice * kDVS + hf * 32, (c - 2) * kC + qd * 16, bh);
-                    tma_store_commit();
-                }
-            }
-            if (GATED) {
-                // exchange the two column halves of the row sums
-                if (!group_sync(cx, &sm->tm_sync, sync_phase)) break;
-                if (has_a) warp_arrive(&sm->aux_empty[(c - 1) & 3]);   // gate data of chunk c-1 is done
-                dint2 = dint1;
-                gam2 = gam1;
-                if (has_b) {
-                    dint1 = sm->densum[bb][0][prow] + sm->densum[bb][1][prow];
-                    gam1 = sm->gG[c & 3][prow];
-                }
-            }
         }
-        if (lane == 0) tma_store_wait_all<0>();
     } else if (is_phi_warp(warp)) {
         // ------------------------------------------------------ phi warps
-        const int pp = phi_index(warp) * 32 + lane;   // 0..159; rows 0..63 of the gate scan on warps 2, 3
-        uint32_t sync_phase = 0;
+        const int pp = phi_index(warp) * 32 + lane;   // 0..159
+        // gated: once P of chunk x is complete (it read the unscaled tiles), the
+        // rows of Q~ are scaled in place by Gamma_i (O = (Gamma Q~) Sprev) and
+        // the rows of K~ by w_j (dS = (w K~)^T V, dz = (w K~)^T 1)
+        auto scale_qk = [&](int x) -> bool {
+            const int sx = x % NST;
+            if (!warp_wait(cx, &sm->P_full[x % NP], (x / NP) & 1)) return false;
+            uint4 *qk = reinterpret_cast<uint4 *>(stage_ptr(sx) + L::kOffQ);
+            const float *gam = gr->gG[x % kAux];
+            const float *w = gr->gw[x % kAux];
+            constexpr int kFull = 2048 / kPhiThreads, kRest = 2048 - kFull * kPhiThreads;
+#pragma unroll
+            for (int it = 0; it <= kFull; ++it) {
+                const int ci = pp + it * kPhiThreads;   // 16-byte chunk; token row (ci & 511) >> 3
+                if (it < kFull || pp < kRest) qk[ci] = scale8(qk[ci], (ci < 1024 ? gam : w)[(ci & 511) >> 3]);
+            }
+            fence_proxy_async_smem();
+            warp_arrive(&sm->sc_done[sx]);
+            return true;
+        };
         bool ok = true;
         for (int c = 0; c < nch && ok; ++c) {
-            const int s = c % NST, gq = c & 3;
+            const int s = c % NST;
             const int nvalid = min(kC, T - c * kC);
             if (!warp_wait(cx, &sm->full[s], (c / NST) & 1)) { ok = false; break; }
             uint8_t *st = stage_ptr(s);
-            if (GATED) {
-                if (c >= 4 && !warp_wait(cx, &sm->aux_empty[gq], ((c >> 2) - 1) & 1)) { ok = false; break; }
-                // in-chunk cumulative log gate and the last zero gate, rows 0..63 (warps 2, 3)
-                float la = 0.f;
-                int zl = -1;
-                if (pp < kC) {
-                    const float a = (pp < nvalid) ? args.alpha[(size_t)bh * T + (size_t)c * kC + pp] : 1.f;
-                    la = a > 0.f ? logf(a) : 0.f;
-                    zl = a > 0.f ? -1 : pp;
-#pragma unroll
-                    for (int off = 1; off < 32; off <<= 1) {
-                        const float lo = __shfl_up_sync(0xffffffffu, la, off);
-                        const int zo = __shfl_up_sync(0xffffffffu, zl, off);
-                        if (lane >= off) { la += lo; zl = max(zl, zo); }
-                    }
-                    if (pp == 31) { sm->carry[0] = la; sm->carry[1] = __int_as_float(zl); }
-                }
-                if (!group_sync(cx, &sm->phi_sync, sync_phase)) { ok = false; break; }
-                if (pp >= 32 && pp < kC) {
-                    la += sm->carry[0];
-                    zl = max(zl, __float_as_int(sm->carry[1]));
-                }
-                if (pp < kC) {
-                    sm->gb[gq][pp] = la;
-                    sm->gz[gq][pp] = zl;
-                    sm->gG[gq][pp] = zl < 0 ? expf(la) : 0.f;
-                }
-            }
             // phi(Q), phi(K) in place (the two tiles are contiguous: 2048 chunks of
             // 16 bytes); key rows past the end of the sequence become 0
             static_assert(L::kOffK == L::kOffQ + kTileQ, "Q and K tiles are contiguous");
@@ -676,30 +673,13 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
                     qk[ci] = (ci >= 1024 && row >= nvalid) ? make_uint4(0, 0, 0, 0) : phi8(qk[ci]);
                 }
             }
-            if (GATED) {
-                if (!group_sync(cx, &sm->phi_sync, sync_phase)) { ok = false; break; }
-                if (pp < kC) {
-                    const float blast = sm->gb[gq][kC - 1];
-                    const int zlast = sm->gz[gq][kC - 1];
-                    const float wj = (zlast <= pp) ? expf(blast - sm->gb[gq][pp]) : 0.f;
-                    sm->gw[gq][pp] = wj;
-                    // column 64 (block 4, column 0) of [w . V | w]
-                    *reinterpret_cast<__nv_bfloat16 *>(st + L::kOffVw + 4 * (kC * 32) + sw32_offset(pp, 0)) =
-                        __float2bfloat16_rn(wj);
-                }
-                if (!group_sync(cx, &sm->phi_sync, sync_phase)) { ok = false; break; }
-                // w . V for the state update: 8-column chunk c8 of token row k, from
-                // the 128-byte-swizzled V tile into the 32-byte-swizzled operand
-                for (int ci = pp; ci < (int)kTileV / 16; ci += kPhiThreads) {
-                    const int k = ci >> 3, c8 = ci & 7;
-                    const uint4 raw = *reinterpret_cast<const uint4 *>(st + L::kOffV + sw128_offset(k, c8));
-                    *reinterpret_cast<uint4 *>(st + L::kOffVw + (c8 >> 1) * (kC * 32) + sw32_offset(k, (c8 & 1) * 8)) =
-                        scale8(raw, sm->gw[gq][k]);
-                }
-            }
             fence_proxy_async_smem();
             warp_arrive(&sm->phi_done[s]);
+            // P of chunk c-1 was issued once phi of chunk c-1 was done and has
+            // normally completed while phi of chunk c ran
+            if (GATED && c >= 1 && !scale_qk(c - 1)) ok = false;
         }
+        if (GATED && ok && nch >= 1) scale_qk(nch - 1);
     }
 
     // ---------------------------------------------------------- teardown
@@ -714,8 +694,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
 }  // namespace
 
 cudaError_t launch_prefill_tc(const CUtensorMap &map_q, const CUtensorMap &map_k, const CUtensorMap &map_v,
-                              const CUtensorMap &map_y, const PrefillTcArgs &a, int B, bool gated,
-                              cudaStream_t stream)
+                              const PrefillTcArgs &a, int B, bool gated, cudaStream_t stream)
 {
     const dim3 grid(a.dv / kDVS, a.H, B);
     const uint32_t bytes = gated ? smem_bytes<true>() : smem_bytes<false>();
@@ -743,7 +722,7 @@ cudaError_t launch_prefill_tc(const CUtensorMap &map_q, const CUtensorMap &map_k
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kern, map_q, map_k, map_v, map_y, a);
+    return cudaLaunchKernelEx(&cfg, kern, map_q, map_k, map_v, a);
 }
 
 }  // namespace la
