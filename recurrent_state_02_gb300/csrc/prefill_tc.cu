@@ -53,8 +53,27 @@ constexpr int kC = 64;          // tokens per chunk
 constexpr int kR = 128;         // feature width r
 constexpr int kDVS = 64;        // value columns per CTA
 constexpr int kThreads = 512;   // 16 warps
-constexpr int kWarpTma = 0, kWarpMma = 1, kWarpTm0 = 4;
-constexpr int kTmWarps = 8, kPhiWarps = 5, kPhiThreads = kPhiWarps * 32;
+#ifndef LA_PHI_WARPS
+#define LA_PHI_WARPS 0x300Cu   // warps 2, 3, 12, 13: one per scheduler
+#endif
+// MMA issuers: warp 1 for O (chunk c's Q~ Sprev + A V), kWarpMmaP for the
+// scores, kWarpMmaS for the state increments
+#ifndef LA_MMAS_WARP
+#define LA_MMAS_WARP 14
+#endif
+#ifndef LA_MMAP_WARP
+#define LA_MMAP_WARP 15
+#endif
+constexpr int kWarpTma = 0, kWarpMma = 1, kWarpMmaS = LA_MMAS_WARP, kWarpMmaP = LA_MMAP_WARP, kWarpTm0 = 4;
+constexpr uint32_t kPhiMask = LA_PHI_WARPS;
+constexpr int kTmWarps = 8, kPhiWarps = __builtin_popcount(kPhiMask), kPhiThreads = kPhiWarps * 32;
+constexpr int kIssuers = 3;
+static_assert((kPhiMask & (0x0FF3u | (1u << kWarpMmaS) | (1u << kWarpMmaP))) == 0 && kWarpMmaS != kWarpMmaP &&
+                  kWarpMmaS >= 12 && kWarpMmaP >= 12, "warp roles overlap");
+// TMEM warp (quadrant qd, column half hf) owns rows 16 qd .. +15 and columns
+// 32 hf .. +31 of A; for hf = 1, qd <= 1 that piece lies strictly above the
+// diagonal (always zero), so those two warps never read P.
+constexpr int kPWarps = kTmWarps - 2;
 #ifndef LA_WAIT_HINT_NS
 #define LA_WAIT_HINT_NS 20000
 #endif
@@ -69,10 +88,10 @@ constexpr uint32_t kTileSpZ = 5 * kR * 32;    // 20 KB
 // the second 64-column block of [V | 1 0..] (128-byte swizzle, column 0 = 1)
 constexpr uint32_t kTileOnes = kC * 128;      // 8 KB
 
-// The phi warps avoid scheduler 1 (warps w with w % 4 == 1), which the MMA warp
-// shares with two TMEM warps: a busy neighbour there starves the MMA issue.
-__host__ __device__ constexpr bool is_phi_warp(int w) { return w == 2 || w == 3 || w == 12 || w == 14 || w == 15; }
-__host__ __device__ constexpr int phi_index(int w) { return w < 4 ? w - 2 : (w == 12 ? 2 : w - 11); }
+// Warp w runs on scheduler w % 4, which it shares with two TMEM warps (those
+// of lane quadrant w % 4); the phi warps are spread over the schedulers.
+__host__ __device__ constexpr bool is_phi_warp(int w) { return (kPhiMask >> w) & 1u; }
+__host__ __device__ constexpr int phi_index(int w) { return __builtin_popcount(kPhiMask & ((1u << w) - 1u)); }
 
 // Gate data ring depth: the producer writes chunk c's entry up to a stage ring
 // ahead of its consumers, so the ring is deep enough that the entry it
@@ -99,11 +118,11 @@ struct Cfg {
     static constexpr int kStages = LA_STAGES;
     static constexpr int kSpBufs = GATED ? 1 : LA_SP_BUFS;     // [Sprev | z] tiles
     static constexpr int kNP = 2;                              // P accumulator buffers
-    // TMEM columns: P (x2), then [dS | dz] and [O | dn] blocks of 80 (x2); dz is
-    // column 64 of a [dS | dz] block, dn columns 64 and 65 of an [O | dn] block
+    // TMEM columns: P (x2), the state [S | z] (80: z is column 64) and [O | dn]
+    // blocks of 80 (x2; dn is columns 64 and 65)
     static constexpr uint32_t kColP = 0;
-    static constexpr uint32_t kColDS = kNP * 64;
-    static constexpr uint32_t kColO = kColDS + 2 * 80;
+    static constexpr uint32_t kColS = kNP * 64;
+    static constexpr uint32_t kColO = kColS + 80;
     static constexpr uint32_t kCols = kColO + 2 * 80;
     static_assert(kCols <= 512, "TMEM budget");
     // shared memory (offsets from a 1024-aligned base)
@@ -121,9 +140,9 @@ struct Cfg {
 
 struct alignas(16) Small {
     uint64_t full[4], empty[4], phi_done[4], sc_done[4];
-    uint64_t P_full[2], P_empty[2], dS_full[2], dS_empty[2], Sp_full[2], Sp_empty[2];
+    uint64_t P_full[2], P_empty[2], dS_full, S_read, Sp_full[2], Sp_empty[2];
     uint64_t A_full[2], A_empty[2], O_full[2], O_empty[2], aux_empty[kAux];
-    uint64_t mma_done;
+    uint64_t mma_done[kIssuers];
     uint32_t tmem_base;
     int abort_flag;
 };
@@ -309,15 +328,13 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
     if (threadIdx.x == 0) {
         for (int s = 0; s < NST; ++s) {
             mbar_init(&sm->full[s], GATED ? 2 : 1);   // TMA bytes (+ gate data)
-            mbar_init(&sm->empty[s], 1);
+            mbar_init(&sm->empty[s], kIssuers);   // one commit from each MMA issuer
             mbar_init(&sm->phi_done[s], kPhiWarps);
             mbar_init(&sm->sc_done[s], kPhiWarps);
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&sm->P_full[i], 1);
-            mbar_init(&sm->P_empty[i], kTmWarps);
-            mbar_init(&sm->dS_full[i], 1);
-            mbar_init(&sm->dS_empty[i], kTmWarps);
+            mbar_init(&sm->P_empty[i], kPWarps);
             mbar_init(&sm->Sp_full[i], kTmWarps);
             mbar_init(&sm->Sp_empty[i], 1);
             mbar_init(&sm->A_full[i], kTmWarps);
@@ -326,7 +343,9 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
             mbar_init(&sm->O_empty[i], kTmWarps);
         }
         for (int i = 0; i < kAux; ++i) mbar_init(&sm->aux_empty[i], kTmWarps);
-        mbar_init(&sm->mma_done, 1);
+        mbar_init(&sm->dS_full, 1);
+        mbar_init(&sm->S_read, kTmWarps);
+        for (int i = 0; i < kIssuers; ++i) mbar_init(&sm->mma_done[i], 1);
         sm->abort_flag = 0;
         fence_mbarrier_init();
         tma_prefetch_desc(&map_q);
@@ -336,6 +355,8 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
     // Constant operand parts: the z block (columns 64..79) of the [Sprev | z]
     // tile starts at zero (only columns 64 and 65 are written later); the ones
     // block is complete here (column 0 = 1 in every token row).
+    for (int i = threadIdx.x; i < (int)(2 * kTileA / 16); i += kThreads)   // A: the blocks above the diagonal stay 0
+        reinterpret_cast<uint4 *>(base + L::kOffA)[i] = make_uint4(0, 0, 0, 0);
     for (int i = threadIdx.x; i < L::kSpBufs * (kR * 32 / 16); i += kThreads) {
         const int buf = i / (kR * 32 / 16), j = i % (kR * 32 / 16);
         reinterpret_cast<uint4 *>(base + L::kOffSpZ + buf * kTileSpZ + 4 * kR * 32)[j] = make_uint4(0, 0, 0, 0);
@@ -392,6 +413,18 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
                 tma_load_3d(st + L::kOffK, &map_k, &sm->full[s], 0, t0, bh);
                 tma_load_3d(st + L::kOffK + kTileQ / 2, &map_k, &sm->full[s], 64, t0, bh);
                 tma_load_3d(st + L::kOffV, &map_v, &sm->full[s], slice * kDVS, t0, bh);
+                // The load of chunk c + NST waits for this stage to come free, which
+                // takes about as long as a load from HBM: warm L2 for it now.
+                if (c + NST < nch) {
+                    const int tp = t0 + NST * kC;
+                    if (slice == 0) {   // the other slices of the head read the same q, k
+                        tma_prefetch_l2_3d(&map_q, 0, tp, bh);
+                        tma_prefetch_l2_3d(&map_q, 64, tp, bh);
+                        tma_prefetch_l2_3d(&map_k, 0, tp, bh);
+                        tma_prefetch_l2_3d(&map_k, 64, tp, bh);
+                    }
+                    tma_prefetch_l2_3d(&map_v, slice * kDVS, tp, bh);
+                }
             }
             if (GATED) {
                 gate_products(a0, a1, lane, c % kAux, gr);
@@ -405,16 +438,18 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
                 mbar_wait(&sm->full[c % NST], (c / NST) & 1, cx.limit);
         }
         __syncwarp();
-    } else if (warp == kWarpMma) {
+    } else if (warp == kWarpMma || warp == kWarpMmaS || warp == kWarpMmaP) {
         // ------------------------------------------------------------ MMA
-        // Lane 0 alone runs the issue loop (tcgen05.mma and tcgen05.commit are
-        // issued by one thread); the other lanes wait at the teardown barrier.
-        // Issue order per iteration: chunk c's O = Q~ Sprev + A V, then the
-        // scores of chunk c + NP and the state increment of chunk c + 1, so that
-        // the TMEM warps' waits are on work issued an iteration earlier.
+        // Three issuers, each lane 0 of its warp (tcgen05.mma and tcgen05.commit
+        // are issued by one thread; the other lanes wait at the teardown
+        // barrier), share the tensor pipe: warp kWarpMma issues chunk c's
+        // O = Q~ Sprev + A V, warp kWarpMmaP the scores P = Q~ K~^T up to NP
+        // chunks ahead, warp kWarpMmaS the state increments as soon as the
+        // TMEM warps have read the state.  Each commits its own arrival on a
+        // stage's empty barrier after its last read of it.
         if (lane == 0) {
             constexpr uint32_t idP = idesc_bf16_f32(64, 64, false, false);
-            constexpr uint32_t idDS = idesc_bf16_f32(128, 80, true, true);   // [dS | dz]
+            constexpr uint32_t idDS = idesc_bf16_f32(128, 80, true, true);   // [S | z] increment
             constexpr uint32_t idQS = idesc_bf16_f32(64, 80, false, true);   // [O | dn]
             // [O | dn] += A [V | 1]: column 64 gains the row sums of A
             constexpr uint32_t idAV = idesc_bf16_f32(64, 80, false, true);
@@ -436,35 +471,39 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
                     else tc_mma_bf16_w<true>(dP, qlo + o, kHi128, klo + o, kHi128, idP);
                 }
                 tc_commit(&sm->P_full[pb]);
+                tc_commit(&sm->empty[s]);   // this issuer's last read of stage s
                 return true;
             };
-            // [dS | dz] = K~'^T [V | 1] for chunk c, K~' = diag(w) K~ with a gate
-            // (phi_done of chunk c was waited for by issue_p(c), which always
-            // comes first; the gated row scaling follows P of chunk c)
+            // [S | z] += K~'^T [V | 1] for chunk c, K~' = diag(w) K~ with a gate,
+            // once phi of chunk c is done (with a gate: its rows scaled, after P
+            // of chunk c) and the TMEM warps have read (and, with a gate,
+            // decayed) the state after chunk c-1
             auto issue_ds = [&](int c) -> bool {
-                const int s = c % NST, bb = c & 1, n = c >> 1;
+                const int s = c % NST;
                 const uint32_t st = smem_u32(stage_ptr(s));
                 const uint32_t aK = st + L::kOffK;
                 // B = [V | 1]: the V tile, then the ones block at LBO
                 const uint32_t blo = desc_lo(st + L::kOffV, aOnes - (st + L::kOffV));
+                if (!GATED && !wait(cx, &sm->phi_done[s], (c / NST) & 1)) return false;
                 if (GATED && !wait(cx, &sm->sc_done[s], (c / NST) & 1)) return false;
-                if (c >= 2 && !wait(cx, &sm->dS_empty[bb], (n - 1) & 1)) return false;
+                if (!wait(cx, &sm->S_read, c & 1)) return false;
                 tc_fence_after();
-                const uint32_t dDS = tmem + L::kColDS + bb * 80;
+                const uint32_t dS = tmem + L::kColS;
                 const uint32_t klo = desc_lo(aK, kTileQ / 2);   // K~^T: MN-major, two 64-feature blocks
 #pragma unroll
-                for (int kk = 0; kk < 4; ++kk) {
-                    if (kk == 0) tc_mma_bf16_w<false>(dDS, klo, kHi128, blo, kHi128, idDS);
-                    else tc_mma_bf16_w<true>(dDS, klo + kk * (2048 >> 4), kHi128, blo + kk * (2048 >> 4), kHi128, idDS);
-                }
-                tc_commit(&sm->dS_full[bb]);
+                for (int kk = 0; kk < 4; ++kk)
+                    tc_mma_bf16_w<true>(dS, klo + kk * (2048 >> 4), kHi128, blo + kk * (2048 >> 4), kHi128, idDS);
+                tc_commit(&sm->dS_full);
+                tc_commit(&sm->empty[s]);   // this issuer's last read of stage s
                 return true;
             };
             bool ok = true;
-            if (nch >= 1) ok = issue_p(0);
-            if (ok && NP == 2 && nch >= 2) ok = issue_p(1);
-            if (ok && nch >= 1) ok = issue_ds(0);
-            for (int c = 0; c < nch && ok && !aborted(cx); ++c) {
+            if (warp == kWarpMmaP) {
+                for (int c = 0; c < nch && ok && !aborted(cx); ++c) ok = issue_p(c);
+            } else if (warp == kWarpMmaS) {
+                for (int c = 0; c < nch && ok && !aborted(cx); ++c) ok = issue_ds(c);
+            }
+            for (int c = 0; warp == kWarpMma && c < nch && ok && !aborted(cx); ++c) {
                 const int s = c % NST, bb = c & 1, n = c >> 1;
                 const uint32_t st = smem_u32(stage_ptr(s));
                 const uint32_t aQ = st + L::kOffQ, aV = st + L::kOffV;
@@ -496,21 +535,21 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
                 tc_commit(&sm->A_empty[bb]);
                 tc_commit(&sm->O_full[bb]);
                 tc_commit(&sm->empty[s]);
-                // look-ahead: the stage of chunk c is released above before these
-                // wait for the stages of chunks c + 1 .. c + NP
-                if (c + NP < nch && !issue_p(c + NP)) break;
-                if (c + 1 < nch && !issue_ds(c + 1)) break;
             }
             // Every MMA issued above completes before TMEM is released.
-            tc_commit(&sm->mma_done);
-            mbar_wait(&sm->mma_done, 0, cx.limit);
+            uint64_t *done = &sm->mma_done[warp == kWarpMma ? 0 : warp == kWarpMmaP ? 1 : 2];
+            tc_commit(done);
+            mbar_wait(done, 0, cx.limit);
         }
         __syncwarp();
     } else if (warp >= kWarpTm0 && warp < kWarpTm0 + kTmWarps) {
         // ----------------------------------------------------- TMEM warps
-        // Iteration c: fold dS of chunk c-1 into the state (the state chunk c
-        // reads), turn the scores of chunk c into A, and finish the outputs of
-        // chunk c-2.  Each warp stores its own 16 x 32 piece of y by TMA.
+        // The FP32 state [S | z] lives in TMEM, where the MMAs accumulate the
+        // state increments.  Iteration c reads the state after chunk c-1 (it
+        // becomes Sprev of chunk c; with a gate it is then decayed by Gamma_last
+        // of chunk c in place, ahead of chunk c's increment), turns the scores of
+        // chunk c into A, and finishes the outputs of chunk c-2.  Each warp
+        // stores its own 16 x 32 piece of y.
         const int tw = warp - kWarpTm0;          // 0..7
         const int qd = warp & 3;                 // TMEM lane quadrant this warp may access
         const int hf = tw >> 2;                  // column half (0: columns 0..31, 1: 32..63)
@@ -518,32 +557,68 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
         const int srow = qd * 32 + lane;         // state row (feature index) of this thread
         const int prow = qd * 16 + (lane & 15);  // row of the M = 64 tiles (16x32bx2 loads)
         const int pcol = hf * 32 + (lane >> 4) * 16;   // first of this thread's 16 columns
-
-        float S[32];
-        float zr = z_init;
+        const bool a_zero = 2 * hf > qd;         // this warp's piece of A is above the diagonal
+        const uint32_t tS = tmem + lane_base + L::kColS + hf * 32;   // this thread's 32 state columns
+        const uint32_t tz = tmem + lane_base + L::kColS + 64;        // z (column 64; hf == 0 warps)
         {
+            // initial state
+            float S[32];
             const float *src = args.S0 ? args.S0 + ((size_t)bh * kR + srow) * args.dv + slice * kDVS + hf * 32 : nullptr;
 #pragma unroll
             for (int j = 0; j < 32; ++j) S[j] = src ? src[j] : 0.f;
+            tc_st_32x32b_x32(tS, S);
+            if (hf == 0) tc_st_32x32b_x1(tz, z_init);
+            tc_wait_st();
         }
 
         for (int c = 0; c < nch + 2; ++c) {
-            const bool has_a = c >= 1 && c <= nch;   // dS of chunk c-1
+            const bool has_s = c <= nch;              // the state after chunk c-1
             const bool has_b = c < nch;               // Sprev and scores of chunk c
+            const bool has_p = has_b && !a_zero;
             const bool has_e = c >= 2;                // outputs of chunk c-2
             const int bb = c & 1, pb = c % NP, pn = c / NP;
-            const int ab = (c - 1) & 1;
-            // outputs of chunk c-2 (its O was complete a full iteration ago)
+            if (has_s && c >= 1 && !warp_wait(cx, &sm->dS_full, (c - 1) & 1)) break;
+            if (has_b && GATED && !warp_wait(cx, &sm->phi_done[c % NST], (c / NST) & 1)) break;
+            if (has_p && !warp_wait(cx, &sm->P_full[pb], pn & 1)) break;
+            if (has_e && !warp_wait(cx, &sm->O_full[bb], ((c - 2) >> 1) & 1)) break;
+            tc_fence_after();
+            float S[32], zr = 0.f, p[16], o[16], dn = 0.f;
+            if (has_s) {
+                tc_ld_32x32b_x32(tS, S);
+                if (hf == 0) tc_ld_32x32b_x1(tz, zr);
+            }
+            if (has_p) tc_ld_16x32bx2_x16<16>(tmem + lane_base + L::kColP + pb * 64 + hf * 32, p);
             if (has_e) {
-                if (!warp_wait(cx, &sm->O_full[bb], ((c - 2) >> 1) & 1)) break;
-                tc_fence_after();
-                float o[16], dn;
                 tc_ld_16x32bx2_x16<16>(tmem + lane_base + L::kColO + bb * 80 + hf * 32, o);
                 tc_ld_16x32bx2_x1<1>(tmem + lane_base + L::kColO + bb * 80 + 64, dn);
-                tc_wait_ld();
-                tc_fence_before();
-                warp_arrive(&sm->O_empty[bb]);
-                // columns 64 + 65: (Gamma_i) Q~ . zprev in two parts, plus the row sums of A
+            }
+            tc_wait_ld();
+            // Sprev of chunk c (BF16) and z split into two BF16 parts
+            uint32_t spk[16];
+            float zhi = 0.f;
+            if (has_b) {
+#pragma unroll
+                for (int j = 0; j < 16; ++j) spk[j] = pack_bf16x2(S[2 * j], S[2 * j + 1]);
+                zhi = __bfloat162float(__float2bfloat16_rn(zr));
+            }
+            if (GATED && has_b) {
+                // decay the state by the gate product of chunk c before its increment lands
+                const float g = gr->gG[c % kAux][kC - 1];
+                float Sd[32];
+#pragma unroll
+                for (int j = 0; j < 32; ++j) Sd[j] = g * S[j];
+                tc_st_32x32b_x32(tS, Sd);
+                if (hf == 0) tc_st_32x32b_x1(tz, g * zr);
+                tc_wait_st();
+            }
+            tc_fence_before();
+            if (has_b) warp_arrive(&sm->S_read);
+            if (has_p) warp_arrive(&sm->P_empty[pb]);
+            if (has_e) warp_arrive(&sm->O_empty[bb]);
+
+            // outputs of chunk c-2: columns 64 + 65 of [O | dn] hold Q~' . zprev in
+            // two parts plus the row sums of A
+            if (has_e) {
                 dn += __shfl_xor_sync(0xffffffffu, dn, 16);
                 const float inv = __frcp_rn(dn + args.eps);
                 uint32_t yp[8];
@@ -558,30 +633,8 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
                     __stcs(dst + 1, make_uint4(yp[4], yp[5], yp[6], yp[7]));
                 }
             }
-            // dS of chunk c-1 and the scores of chunk c
-            if (has_a && !warp_wait(cx, &sm->dS_full[ab], ((c - 1) >> 1) & 1)) break;
-            if (has_b && GATED && !warp_wait(cx, &sm->phi_done[c % NST], (c / NST) & 1)) break;
-            if (has_b && !warp_wait(cx, &sm->P_full[pb], pn & 1)) break;
-            tc_fence_after();
-            float d[32], dz = 0.f, p[16];
-            if (has_a) {
-                tc_ld_32x32b_x32(tmem + lane_base + L::kColDS + ab * 80 + hf * 32, d);
-                tc_ld_32x32b_x1(tmem + lane_base + L::kColDS + ab * 80 + 64, dz);
-            }
-            if (has_b) tc_ld_16x32bx2_x16<16>(tmem + lane_base + L::kColP + pb * 64 + hf * 32, p);
-            tc_wait_ld();
-            tc_fence_before();
-            if (has_a) warp_arrive(&sm->dS_empty[ab]);
-            if (has_b) warp_arrive(&sm->P_empty[pb]);
-
-            if (has_a) {
-                const float g = GATED ? gr->gG[(c - 1) % kAux][kC - 1] : 1.f;
-#pragma unroll
-                for (int j = 0; j < 32; ++j) S[j] = GATED ? fmaf(g, S[j], d[j]) : S[j] + d[j];
-                zr = GATED ? fmaf(g, zr, dz) : zr + dz;
-                if (GATED) warp_arrive(&sm->aux_empty[(c - 1) % kAux]);   // gate data of chunk c-1 is done
-            }
-            if (has_b) {
+            // A = the causal mask (and, with a gate, the in-chunk decay) applied to P
+            if (has_p) {
                 const int gq = c % kAux;
                 const float bi = GATED ? gr->gb[gq][prow] : 0.f;
                 const int zi = GATED ? gr->gz[gq][prow] : -1;
@@ -593,30 +646,24 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
                     p[e] = a;
                 }
             }
+            if (GATED && has_b) warp_arrive(&sm->aux_empty[c % kAux]);   // gate data of chunk c is done
 
-            // shared-memory operands and outputs
+            // shared-memory operands
             if (has_b) {
                 const int sb = c % L::kSpBufs, sn = c / L::kSpBufs;
                 if (c >= L::kSpBufs && !warp_wait(cx, &sm->Sp_empty[sb], (sn - 1) & 1)) break;
                 if (c >= 2 && !warp_wait(cx, &sm->A_empty[bb], ((c >> 1) - 1) & 1)) break;
-                // Sprev (BF16) into columns hf*32 .. +31 of row srow: two 16-column blocks
+                // Sprev into columns hf*32 .. +31 of row srow: two 16-column blocks
                 uint8_t *spz = base + L::kOffSpZ + sb * kTileSpZ;
 #pragma unroll
-                for (int q4 = 0; q4 < 4; ++q4) {
-                    uint4 w;
-                    w.x = pack_bf16x2(S[q4 * 8 + 0], S[q4 * 8 + 1]);
-                    w.y = pack_bf16x2(S[q4 * 8 + 2], S[q4 * 8 + 3]);
-                    w.z = pack_bf16x2(S[q4 * 8 + 4], S[q4 * 8 + 5]);
-                    w.w = pack_bf16x2(S[q4 * 8 + 6], S[q4 * 8 + 7]);
-                    *reinterpret_cast<uint4 *>(spz + (hf * 2 + (q4 >> 1)) * (kR * 32) + sw32_offset(srow, (q4 & 1) * 8)) = w;
-                }
-                if (hf == 0) {
-                    // z as two BF16 parts in columns 64 (zhi) and 65 (zlo)
-                    const float zhi = __bfloat162float(__float2bfloat16_rn(zr));
+                for (int q4 = 0; q4 < 4; ++q4)
+                    *reinterpret_cast<uint4 *>(spz + (hf * 2 + (q4 >> 1)) * (kR * 32) + sw32_offset(srow, (q4 & 1) * 8)) =
+                        make_uint4(spk[4 * q4], spk[4 * q4 + 1], spk[4 * q4 + 2], spk[4 * q4 + 3]);
+                // z as two BF16 parts in columns 64 (zhi) and 65 (zlo)
+                if (hf == 0)
                     *reinterpret_cast<uint32_t *>(spz + 4 * (kR * 32) + sw32_offset(srow, 0)) = pack_bf16x2(zhi, zr - zhi);
-                }
-                store_bf16x16(base + L::kOffA + bb * kTileA, prow, pcol >> 3, p);
-            } else if (has_a) {
+                if (!a_zero) store_bf16x16(base + L::kOffA + bb * kTileA, prow, pcol >> 3, p);
+            } else if (has_s) {
                 // c == nch: the state after the last chunk
                 float *dst = args.S_out + ((size_t)bh * kR + srow) * args.dv + slice * kDVS + hf * 32;
 #pragma unroll
