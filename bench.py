@@ -65,9 +65,19 @@ def read_peaks():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def source_sha1(path):
-    with open(path, "rb") as f:
-        return hashlib.sha1(f.read()).hexdigest()[:12]
+def source_sha1(paths):
+    """First 12 hex digits of the SHA-1 of the concatenated source files."""
+    h = hashlib.sha1()
+    for path in paths:
+        with open(path, "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:12]
+
+
+def kernel_sources(name):
+    """The files a kernel is compiled from (its .cu and the headers it includes)."""
+    csrc = os.path.join(ROOT, "recurrent_state_02_gb300", "csrc")
+    return [os.path.join(csrc, f) for f in (name, "kernels.h", "sm103_ptx.cuh")]
 
 
 def profile_traffic(kernel, workload, src):
@@ -362,7 +372,7 @@ def run_ours(args, rank, world, local_rank):
     pre_bytes = prefill_bytes(B, H, T, r, dv, with_state_in=True)
     pre_launch = prefill_s / args.steps
     achieved = pre_bytes / pre_launch / 1e9
-    src = os.path.join(ROOT, "recurrent_state_02_gb300", "csrc", "prefill_tc.cu")
+    src = kernel_sources("prefill_tc.cu")
     roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                 "traffic": profile_traffic("prefill_tc_kernel<false>", "B4 H16 T4096", src),
                 "kernel": "prefill_tc_kernel<false> (ungated)", "algorithmic_bytes_per_launch": pre_bytes,
@@ -392,8 +402,7 @@ def run_ours(args, rank, world, local_rank):
     decode = {"workload": dw.name, "gb_per_s": dec_gbs * world, "per_gpu_gb_per_s": dec_gbs,
               "frac_of_hbm_peak": dec_gbs / peak, "launch_us": dec_launch * 1e6,
               "algorithmic_bytes_per_launch": dbytes, "tokens_per_s": dw.B * world / dec_launch,
-              "traffic": profile_traffic("decode128_kernel<true>", "B256 H16",
-                                         os.path.join(ROOT, "recurrent_state_02_gb300", "csrc", "decode.cu"))}
+              "traffic": profile_traffic("decode128_kernel<true>", "B256 H16", kernel_sources("decode.cu"))}
 
     # end to end through the public API with host buffers (pinned), every step:
     # H2D of q, k, v (+ the decode token), the three calls, D2H of y, S, z, y_decode

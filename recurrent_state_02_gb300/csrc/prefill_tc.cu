@@ -52,28 +52,36 @@ namespace {
 constexpr int kC = 64;          // tokens per chunk
 constexpr int kR = 128;         // feature width r
 constexpr int kDVS = 64;        // value columns per CTA
-constexpr int kThreads = 512;   // 16 warps
+// 24 warps.  Warp w runs on scheduler w % 4 and may access TMEM lane quadrant
+// w % 4.  Warps 4..19 are the TMEM warps (four per quadrant); the producer, the
+// three MMA issuers and the phi warps are spread so that every scheduler hosts
+// four TMEM warps, one phi warp and one light warp.
+constexpr int kThreads = 768;
 #ifndef LA_PHI_WARPS
-#define LA_PHI_WARPS 0x300Cu   // warps 2, 3, 12, 13: one per scheduler
+#define LA_PHI_WARPS 0x30000Cu   // warps 2, 3, 20, 21: one per scheduler
 #endif
 // MMA issuers: warp 1 for O (chunk c's Q~ Sprev + A V), kWarpMmaP for the
 // scores, kWarpMmaS for the state increments
-#ifndef LA_MMAS_WARP
-#define LA_MMAS_WARP 14
-#endif
 #ifndef LA_MMAP_WARP
-#define LA_MMAP_WARP 15
+#define LA_MMAP_WARP 22
+#endif
+#ifndef LA_MMAS_WARP
+#define LA_MMAS_WARP 23
 #endif
 constexpr int kWarpTma = 0, kWarpMma = 1, kWarpMmaS = LA_MMAS_WARP, kWarpMmaP = LA_MMAP_WARP, kWarpTm0 = 4;
 constexpr uint32_t kPhiMask = LA_PHI_WARPS;
-constexpr int kTmWarps = 8, kPhiWarps = __builtin_popcount(kPhiMask), kPhiThreads = kPhiWarps * 32;
+constexpr int kTmWarps = 16, kPhiWarps = __builtin_popcount(kPhiMask), kPhiThreads = kPhiWarps * 32;
 constexpr int kIssuers = 3;
-static_assert((kPhiMask & (0x0FF3u | (1u << kWarpMmaS) | (1u << kWarpMmaP))) == 0 && kWarpMmaS != kWarpMmaP &&
-                  kWarpMmaS >= 12 && kWarpMmaP >= 12, "warp roles overlap");
-// TMEM warp (quadrant qd, column half hf) owns rows 16 qd .. +15 and columns
-// 32 hf .. +31 of A; for hf = 1, qd <= 1 that piece lies strictly above the
-// diagonal (always zero), so those two warps never read P.
-constexpr int kPWarps = kTmWarps - 2;
+constexpr uint32_t kFixedRoles = 0x3u | (((1u << kTmWarps) - 1u) << kWarpTm0);   // producer, O issuer, TMEM warps
+static_assert((kPhiMask & (kFixedRoles | (1u << kWarpMmaS) | (1u << kWarpMmaP))) == 0 && kWarpMmaS != kWarpMmaP &&
+                  kWarpMmaS >= kWarpTm0 + kTmWarps && kWarpMmaP >= kWarpTm0 + kTmWarps && kWarpMmaS < kThreads / 32 &&
+                  kWarpMmaP < kThreads / 32 && (kPhiMask >> (kThreads / 32)) == 0,
+              "warp roles overlap");
+// TMEM warp (quadrant qd, column quarter qq) owns rows 16 qd .. +15 and columns
+// 16 qq .. +15 of the 64 x 64 tiles P, A and O, and state columns 16 qq .. +15
+// of feature rows 32 qd .. +31.  Its piece of A lies strictly above the
+// diagonal (always zero) when qq > qd: 6 of the 16 warps never read P.
+constexpr int kPWarps = 10;
 #ifndef LA_WAIT_HINT_NS
 #define LA_WAIT_HINT_NS 20000
 #endif
@@ -88,8 +96,6 @@ constexpr uint32_t kTileSpZ = 5 * kR * 32;    // 20 KB
 // the second 64-column block of [V | 1 0..] (128-byte swizzle, column 0 = 1)
 constexpr uint32_t kTileOnes = kC * 128;      // 8 KB
 
-// Warp w runs on scheduler w % 4, which it shares with two TMEM warps (those
-// of lane quadrant w % 4); the phi warps are spread over the schedulers.
 __host__ __device__ constexpr bool is_phi_warp(int w) { return (kPhiMask >> w) & 1u; }
 __host__ __device__ constexpr int phi_index(int w) { return __builtin_popcount(kPhiMask & ((1u << w) - 1u)); }
 
@@ -211,12 +217,15 @@ __device__ __forceinline__ bool wait(Ctx &cx, uint64_t *bar, uint32_t parity)
     }
 }
 
-// Lane 0 waits while the other lanes are parked at the warp barrier; the
-// outcome is broadcast so that the warp stays converged for the .sync.aligned
+// Warp-wide wait.  Fast path: every lane tests the phase (each lane acquires
+// for itself) and the vote keeps the branch uniform.  Otherwise lane 0 waits
+// (bounded) while the other lanes are parked at the warp barrier; the outcome
+// is broadcast so that the warp stays converged for the .sync.aligned
 // instructions that follow, and the warp barrier orders the other lanes'
 // later accesses after lane 0's acquire.
 __device__ __forceinline__ bool warp_wait(Ctx &cx, uint64_t *bar, uint32_t parity)
 {
+    if (__all_sync(0xffffffffu, mbar_try_wait(bar, parity))) return true;
     int ok = 1;
     if ((threadIdx.x & 31) == 0) ok = wait(cx, bar, parity);
     ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -224,11 +233,12 @@ __device__ __forceinline__ bool warp_wait(Ctx &cx, uint64_t *bar, uint32_t parit
     return ok != 0;
 }
 
-// One arrival per warp, after every lane's preceding writes and fences.
+// One arrival per warp, after every lane's preceding writes and fences (the
+// warp barrier orders them before lane 0's release).
 __device__ __forceinline__ void warp_arrive(uint64_t *bar)
 {
     __syncwarp();
-    if ((threadIdx.x & 31) == 0) mbar_arrive(bar);
+    mbar_arrive_if(bar, (threadIdx.x & 31) == 0);
 }
 
 // Applies phi to the 8 BF16 values of one 16-byte chunk.
@@ -289,17 +299,6 @@ __device__ __forceinline__ void gate_products(float a0, float a1, int lane, int 
     *reinterpret_cast<int2 *>(&gr->gz[gq][j0]) = make_int2(z0, z1);
     *reinterpret_cast<float2 *>(&gr->gG[gq][j0]) = make_float2(z0 < 0 ? expf(b0) : 0.f, z1 < 0 ? expf(b1) : 0.f);
     *reinterpret_cast<float2 *>(&gr->gw[gq][j0]) = make_float2(w0, w1);
-}
-
-__device__ __forceinline__ void store_bf16x16(uint8_t *tile, int row, int chunk0, const float (&v)[16])
-{
-    uint4 a, b;
-    a.x = pack_bf16x2(v[0], v[1]);   a.y = pack_bf16x2(v[2], v[3]);
-    a.z = pack_bf16x2(v[4], v[5]);   a.w = pack_bf16x2(v[6], v[7]);
-    b.x = pack_bf16x2(v[8], v[9]);   b.y = pack_bf16x2(v[10], v[11]);
-    b.z = pack_bf16x2(v[12], v[13]); b.w = pack_bf16x2(v[14], v[15]);
-    *reinterpret_cast<uint4 *>(tile + sw128_offset(row, chunk0)) = a;
-    *reinterpret_cast<uint4 *>(tile + sw128_offset(row, chunk0 + 1)) = b;
 }
 
 template <bool GATED>
@@ -549,25 +548,25 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
         // becomes Sprev of chunk c; with a gate it is then decayed by Gamma_last
         // of chunk c in place, ahead of chunk c's increment), turns the scores of
         // chunk c into A, and finishes the outputs of chunk c-2.  Each warp
-        // stores its own 16 x 32 piece of y.
-        const int tw = warp - kWarpTm0;          // 0..7
+        // stores its own 16 x 16 piece of y.
+        const int tw = warp - kWarpTm0;          // 0..15
         const int qd = warp & 3;                 // TMEM lane quadrant this warp may access
-        const int hf = tw >> 2;                  // column half (0: columns 0..31, 1: 32..63)
+        const int qq = tw >> 2;                  // column quarter: columns 16 qq .. +15
         const uint32_t lane_base = static_cast<uint32_t>(qd * 32) << 16;
         const int srow = qd * 32 + lane;         // state row (feature index) of this thread
         const int prow = qd * 16 + (lane & 15);  // row of the M = 64 tiles (16x32bx2 loads)
-        const int pcol = hf * 32 + (lane >> 4) * 16;   // first of this thread's 16 columns
-        const bool a_zero = 2 * hf > qd;         // this warp's piece of A is above the diagonal
-        const uint32_t tS = tmem + lane_base + L::kColS + hf * 32;   // this thread's 32 state columns
-        const uint32_t tz = tmem + lane_base + L::kColS + 64;        // z (column 64; hf == 0 warps)
+        const int pcol = qq * 16 + (lane >> 4) * 8;   // first of this thread's 8 columns
+        const bool a_zero = qq > qd;             // this warp's piece of A is above the diagonal
+        const uint32_t tS = tmem + lane_base + L::kColS + qq * 16;   // this thread's 16 state columns
+        const uint32_t tz = tmem + lane_base + L::kColS + 64;        // z (column 64; qq == 0 warps)
         {
             // initial state
-            float S[32];
-            const float *src = args.S0 ? args.S0 + ((size_t)bh * kR + srow) * args.dv + slice * kDVS + hf * 32 : nullptr;
+            float S[16];
+            const float *src = args.S0 ? args.S0 + ((size_t)bh * kR + srow) * args.dv + slice * kDVS + qq * 16 : nullptr;
 #pragma unroll
-            for (int j = 0; j < 32; ++j) S[j] = src ? src[j] : 0.f;
-            tc_st_32x32b_x32(tS, S);
-            if (hf == 0) tc_st_32x32b_x1(tz, z_init);
+            for (int j = 0; j < 16; ++j) S[j] = src ? src[j] : 0.f;
+            tc_st_32x32b_x16(tS, S);
+            if (qq == 0) tc_st_32x32b_x1(tz, z_init);
             tc_wait_st();
         }
 
@@ -582,33 +581,33 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
             if (has_p && !warp_wait(cx, &sm->P_full[pb], pn & 1)) break;
             if (has_e && !warp_wait(cx, &sm->O_full[bb], ((c - 2) >> 1) & 1)) break;
             tc_fence_after();
-            float S[32], zr = 0.f, p[16], o[16], dn = 0.f;
+            float S[16], zr = 0.f, p[8], o[8], dn = 0.f;
             if (has_s) {
-                tc_ld_32x32b_x32(tS, S);
-                if (hf == 0) tc_ld_32x32b_x1(tz, zr);
+                tc_ld_32x32b_x16(tS, S);
+                if (qq == 0) tc_ld_32x32b_x1(tz, zr);
             }
-            if (has_p) tc_ld_16x32bx2_x16<16>(tmem + lane_base + L::kColP + pb * 64 + hf * 32, p);
+            if (has_p) tc_ld_16x32bx2_x8<8>(tmem + lane_base + L::kColP + pb * 64 + qq * 16, p);
             if (has_e) {
-                tc_ld_16x32bx2_x16<16>(tmem + lane_base + L::kColO + bb * 80 + hf * 32, o);
+                tc_ld_16x32bx2_x8<8>(tmem + lane_base + L::kColO + bb * 80 + qq * 16, o);
                 tc_ld_16x32bx2_x1<1>(tmem + lane_base + L::kColO + bb * 80 + 64, dn);
             }
             tc_wait_ld();
             // Sprev of chunk c (BF16) and z split into two BF16 parts
-            uint32_t spk[16];
+            uint32_t spk[8];
             float zhi = 0.f;
             if (has_b) {
 #pragma unroll
-                for (int j = 0; j < 16; ++j) spk[j] = pack_bf16x2(S[2 * j], S[2 * j + 1]);
+                for (int j = 0; j < 8; ++j) spk[j] = pack_bf16x2(S[2 * j], S[2 * j + 1]);
                 zhi = __bfloat162float(__float2bfloat16_rn(zr));
             }
             if (GATED && has_b) {
                 // decay the state by the gate product of chunk c before its increment lands
                 const float g = gr->gG[c % kAux][kC - 1];
-                float Sd[32];
+                float Sd[16];
 #pragma unroll
-                for (int j = 0; j < 32; ++j) Sd[j] = g * S[j];
-                tc_st_32x32b_x32(tS, Sd);
-                if (hf == 0) tc_st_32x32b_x1(tz, g * zr);
+                for (int j = 0; j < 16; ++j) Sd[j] = g * S[j];
+                tc_st_32x32b_x16(tS, Sd);
+                if (qq == 0) tc_st_32x32b_x1(tz, g * zr);
                 tc_wait_st();
             }
             tc_fence_before();
@@ -621,17 +620,15 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
             if (has_e) {
                 dn += __shfl_xor_sync(0xffffffffu, dn, 16);
                 const float inv = __frcp_rn(dn + args.eps);
-                uint32_t yp[8];
-#pragma unroll
-                for (int e = 0; e < 8; ++e) yp[e] = pack_bf16x2(o[2 * e] * inv, o[2 * e + 1] * inv);
-                // 16 columns (32 bytes) of token row prow, straight to global memory
+                uint4 yp;
+                yp.x = pack_bf16x2(o[0] * inv, o[1] * inv);
+                yp.y = pack_bf16x2(o[2] * inv, o[3] * inv);
+                yp.z = pack_bf16x2(o[4] * inv, o[5] * inv);
+                yp.w = pack_bf16x2(o[6] * inv, o[7] * inv);
+                // 8 columns (16 bytes) of token row prow, straight to global memory
                 // (streaming stores: y is not read again here)
                 const int t = (c - 2) * kC + prow;
-                if (t < T) {
-                    uint4 *dst = reinterpret_cast<uint4 *>(args.y + ((size_t)bh * T + t) * args.dv + slice * kDVS + pcol);
-                    __stcs(dst, make_uint4(yp[0], yp[1], yp[2], yp[3]));
-                    __stcs(dst + 1, make_uint4(yp[4], yp[5], yp[6], yp[7]));
-                }
+                if (t < T) __stcs(reinterpret_cast<uint4 *>(args.y + ((size_t)bh * T + t) * args.dv + slice * kDVS + pcol), yp);
             }
             // A = the causal mask (and, with a gate, the in-chunk decay) applied to P
             if (has_p) {
@@ -639,7 +636,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
                 const float bi = GATED ? gr->gb[gq][prow] : 0.f;
                 const int zi = GATED ? gr->gz[gq][prow] : -1;
 #pragma unroll
-                for (int e = 0; e < 16; ++e) {
+                for (int e = 0; e < 8; ++e) {
                     const int j = pcol + e;
                     float a = (j <= prow) ? p[e] : 0.f;
                     if (GATED) a = (j <= prow && zi <= j) ? a * __expf(bi - gr->gb[gq][j]) : 0.f;
@@ -653,23 +650,25 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
                 const int sb = c % L::kSpBufs, sn = c / L::kSpBufs;
                 if (c >= L::kSpBufs && !warp_wait(cx, &sm->Sp_empty[sb], (sn - 1) & 1)) break;
                 if (c >= 2 && !warp_wait(cx, &sm->A_empty[bb], ((c >> 1) - 1) & 1)) break;
-                // Sprev into columns hf*32 .. +31 of row srow: two 16-column blocks
-                uint8_t *spz = base + L::kOffSpZ + sb * kTileSpZ;
-#pragma unroll
-                for (int q4 = 0; q4 < 4; ++q4)
-                    *reinterpret_cast<uint4 *>(spz + (hf * 2 + (q4 >> 1)) * (kR * 32) + sw32_offset(srow, (q4 & 1) * 8)) =
-                        make_uint4(spk[4 * q4], spk[4 * q4 + 1], spk[4 * q4 + 2], spk[4 * q4 + 3]);
+                // Sprev columns 16 qq .. +15 of row srow: 16-column block qq
+                uint8_t *spz = base + L::kOffSpZ + sb * kTileSpZ + qq * (kR * 32);
+                *reinterpret_cast<uint4 *>(spz + sw32_offset(srow, 0)) = make_uint4(spk[0], spk[1], spk[2], spk[3]);
+                *reinterpret_cast<uint4 *>(spz + sw32_offset(srow, 8)) = make_uint4(spk[4], spk[5], spk[6], spk[7]);
                 // z as two BF16 parts in columns 64 (zhi) and 65 (zlo)
-                if (hf == 0)
-                    *reinterpret_cast<uint32_t *>(spz + 4 * (kR * 32) + sw32_offset(srow, 0)) = pack_bf16x2(zhi, zr - zhi);
-                if (!a_zero) store_bf16x16(base + L::kOffA + bb * kTileA, prow, pcol >> 3, p);
+                if (qq == 0)
+                    *reinterpret_cast<uint32_t *>(base + L::kOffSpZ + sb * kTileSpZ + 4 * (kR * 32) + sw32_offset(srow, 0)) =
+                        pack_bf16x2(zhi, zr - zhi);
+                if (!a_zero)
+                    *reinterpret_cast<uint4 *>(base + L::kOffA + bb * kTileA + sw128_offset(prow, pcol >> 3)) =
+                        make_uint4(pack_bf16x2(p[0], p[1]), pack_bf16x2(p[2], p[3]), pack_bf16x2(p[4], p[5]),
+                                   pack_bf16x2(p[6], p[7]));
             } else if (has_s) {
                 // c == nch: the state after the last chunk
-                float *dst = args.S_out + ((size_t)bh * kR + srow) * args.dv + slice * kDVS + hf * 32;
+                float *dst = args.S_out + ((size_t)bh * kR + srow) * args.dv + slice * kDVS + qq * 16;
 #pragma unroll
-                for (int j = 0; j < 32; j += 4)
+                for (int j = 0; j < 16; j += 4)
                     *reinterpret_cast<float4 *>(dst + j) = make_float4(S[j], S[j + 1], S[j + 2], S[j + 3]);
-                if (slice == 0 && hf == 0) args.z_out[(size_t)bh * kR + srow] = zr;
+                if (slice == 0 && qq == 0) args.z_out[(size_t)bh * kR + srow] = zr;
             }
             fence_proxy_async_smem();
             if (has_b) {

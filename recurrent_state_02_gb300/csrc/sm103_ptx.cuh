@@ -46,6 +46,17 @@ __device__ __forceinline__ void mbar_arrive(uint64_t *bar)
     asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
 
+// Arrives once if `pred` holds (a predicated instruction, no branch).
+__device__ __forceinline__ void mbar_arrive_if(uint64_t *bar, bool pred)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.u32 p, %1, 0;\n\t"
+        "@p mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];\n\t}"
+        ::"r"(smem_u32(bar)), "r"(static_cast<uint32_t>(pred))
+        : "memory");
+}
+
 __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes)
 {
     asm volatile("mbarrier.arrive.expect_tx.release.cta.shared::cta.b64 _, [%0], %1;"
@@ -273,6 +284,20 @@ __device__ __forceinline__ void tc_ld_16x32bx2_x16(uint32_t taddr, float (&v)[16
     for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }
 
+// Same shape, 8 columns per half: threads 0..15 receive columns [col, col + 8),
+// threads 16..31 columns [col + OFF, col + OFF + 8).
+template <int OFF>
+__device__ __forceinline__ void tc_ld_16x32bx2_x8(uint32_t taddr, float (&v)[8])
+{
+    uint32_t r[8];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.16x32bx2.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8], %9;"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
+        : "r"(taddr), "n"(OFF));
+#pragma unroll
+    for (int i = 0; i < 8; ++i) v[i] = __uint_as_float(r[i]);
+}
+
 // Same shape, one column per half: threads 0..15 get column col, 16..31 get col + OFF.
 template <int OFF>
 __device__ __forceinline__ void tc_ld_16x32bx2_x1(uint32_t taddr, float &v)
@@ -299,6 +324,20 @@ __device__ __forceinline__ void tc_st_32x32b_x32(uint32_t taddr, const float (&v
           "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]),
           "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]),
           "r"(r[31])
+        : "memory");
+}
+
+__device__ __forceinline__ void tc_st_32x32b_x16(uint32_t taddr, const float (&v)[16])
+{
+    uint32_t r[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) r[i] = __float_as_uint(v[i]);
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+        "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};"
+        ::"r"(taddr), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]),
+          "r"(r[7]), "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
+          "r"(r[15])
         : "memory");
 }
 
