@@ -69,8 +69,17 @@ la_status la_state_init(float *S, float *z, int B, int H, int r, int dv, la_stre
 
 /*
  * la_prefill_workspace_bytes -- device scratch that la_prefill_chunked needs for
- * these sizes.  The current kernels keep every intermediate on chip, so this is
- * 0; callers should still ask and pass a buffer of that size.
+ * these sizes on the current device.  It is non-zero only for the BF16 path
+ * when B*H*(dv/64) CTAs would leave at least half of the device's SMs idle and
+ * T is long enough (>= 2048 tokens): the kernel then splits every sequence
+ * into segments that run in parallel ([LA] "门控递推为什么能做并行 scan？": the
+ * per-token updates are affine maps of the state, so a segment's map (the
+ * product A of its gates and the state dS, dz it writes from a zero state)
+ * can be computed first, scanned, and each segment started from its state).
+ * The scratch holds A, dS, dz per segment part and every segment's start
+ * state: FP32, about 66 KB per head per entry at r = dv = 128.  The answer
+ * depends on the device's SM count: ask with the device current that will run
+ * the call.  Returns 0 for sizes the BF16 path does not support.
  */
 size_t la_prefill_workspace_bytes(int B, int H, int T, int r, int dv, int chunk);
 
@@ -92,13 +101,17 @@ size_t la_prefill_workspace_bytes(int B, int H, int T, int r, int dv, int chunk)
  *   eps    added once to the whole denominator: y = num / (den + eps).
  *   chunk  chunk length in tokens.  The result does not depend on it beyond
  *          rounding ([LA] "动手实验": chunk boundaries do not change the semantics).
- *   workspace, workspace_bytes: at least la_prefill_workspace_bytes(...) bytes
- *          (may be NULL when that is 0).
+ *   workspace, workspace_bytes: device scratch of at least
+ *          la_prefill_workspace_bytes(...) bytes, 256-byte aligned, owned by the
+ *          caller and not read after the call's kernels finish (may be NULL
+ *          when that is 0).  Calls sharing one workspace must be ordered.
  *
  * Kernels:
  *   BF16: tensor-core kernel (tcgen05 MMAs with TMEM accumulators, TMA tile
- *         loads and stores).  Requires r == 128, dv in {64, 128}, chunk == 64,
- *         q, k, v, y 16-byte aligned.
+ *         loads).  Requires r == 128, dv in {64, 128}, chunk == 64, q, k, v, y,
+ *         S_out 16-byte aligned.  With a workspace (see above) three launches:
+ *         the state pass, the scan of segment start states, and the chunk
+ *         kernel over all segments at once.
  *   FP32: exact FP32 token recurrence on CUDA cores (chunk is not used).
  *         Requires 1 <= r <= 128, 1 <= dv <= 128, 4-byte alignment.
  * T may be any length >= 1 (a final partial chunk is masked).

@@ -30,6 +30,62 @@ EncodeTiledFn encode_fn()
     return fn;
 }
 
+// Sequence segmentation of the BF16 prefill.  A launch has B*H*(dv/64) CTAs,
+// one per (b, h, 64-column slice); when that leaves at least half of the SMs
+// idle and the sequence is long enough, every head's chunks are split into
+// nseg segments that run in parallel from scanned start states.  The first
+// nseg - 1 segments are each cut into sub_per_seg parts for the state pass,
+// again sized to fill the GPU.
+constexpr int kMinSegChunks = 16;   // at least 1024 tokens per segment
+
+struct SegPlan {
+    int nseg = 1, seg_chunks = 0, sub_per_seg = 1, sub_chunks = 0, nsub = 0;
+};
+
+int sm_count()
+{
+    static int count[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+    if (!count[dev] && cudaDeviceGetAttribute(&count[dev], cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        count[dev] = 0;
+    return count[dev];
+}
+
+SegPlan seg_plan(int B, int H, int T, int dv)
+{
+    SegPlan p;
+    const long long units = (long long)B * H * (dv / 64);
+    const long long sms = sm_count();
+    const int nch = (T + 63) / 64;
+    long long g = units > 0 ? sms / units : 0;
+    g = g < nch / kMinSegChunks ? g : nch / kMinSegChunks;
+    if (g < 2) return p;
+    const int L = (int)((nch + g - 1) / g);
+    const int G = (nch + L - 1) / L;
+    if (G < 2) return p;
+    long long per = sms / (units * (G - 1));
+    per = per < 1 ? 1 : (per > L ? L : per);
+    const int L1 = (int)((L + per - 1) / per);
+    p.nseg = G;
+    p.seg_chunks = L;
+    p.sub_chunks = L1;
+    p.sub_per_seg = (L + L1 - 1) / L1;
+    p.nsub = (G - 1) * p.sub_per_seg;
+    return p;
+}
+
+size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// Workspace (FP32): A [nsub][B*H], dS [nsub][B*H][state], S_start [nseg][B*H][state],
+// state = 128*dv + 128 (S then z); every part starts on a 256-byte boundary.
+size_t seg_workspace_bytes(const SegPlan &p, int B, int H, int dv)
+{
+    if (p.nseg <= 1) return 0;
+    const size_t BH = (size_t)B * H, state = 128 * (size_t)dv + 128;
+    return round_up((size_t)p.nsub * BH * 4, 256) + (size_t)p.nsub * BH * state * 4 + (size_t)p.nseg * BH * state * 4;
+}
+
 // 3-D BF16 view [planes, rows, cols] (cols innermost) with boxes of box_cols x
 // box_rows; rows past the end of a plane read as zero and are never written.
 bool make_map_bf16(CUtensorMap *map, const void *ptr, long long planes, long long rows, long long cols,
@@ -88,8 +144,8 @@ la_status la_state_init(float *S, float *z, int B, int H, int r, int dv, la_stre
 
 size_t la_prefill_workspace_bytes(int B, int H, int T, int r, int dv, int chunk)
 {
-    (void)B; (void)H; (void)T; (void)r; (void)dv; (void)chunk;
-    return 0;
+    if (B < 1 || H < 1 || T < 1 || r != 128 || (dv != 64 && dv != 128) || chunk != 64) return 0;
+    return seg_workspace_bytes(seg_plan(B, H, T, dv), B, H, dv);
 }
 
 la_status la_prefill_chunked(const void *q, const void *k, const void *v, la_dtype dtype, const float *alpha,
@@ -97,11 +153,9 @@ la_status la_prefill_chunked(const void *q, const void *k, const void *v, la_dty
                              float eps, void *y, float *S_out, float *z_out, void *workspace,
                              size_t workspace_bytes, la_stream_t stream)
 {
-    (void)workspace;
     if (!q || !k || !v || !y || !S_out || !z_out) return LA_ERR_NULL;
     if (B < 1 || H < 1 || T < 1 || r < 1 || dv < 1 || chunk < 1) return LA_ERR_SHAPE;
     if (dtype != LA_DTYPE_BF16 && dtype != LA_DTYPE_FP32) return LA_ERR_DTYPE;
-    if (workspace_bytes < la_prefill_workspace_bytes(B, H, T, r, dv, chunk)) return LA_ERR_WORKSPACE;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
 
     if (dtype == LA_DTYPE_FP32) {
@@ -125,6 +179,12 @@ la_status la_prefill_chunked(const void *q, const void *k, const void *v, la_dty
         for (const void *p : ptrs4)
             if (p && !aligned(p, 4)) return LA_ERR_ALIGN;
     }
+    const SegPlan plan = seg_plan(B, H, T, dv);
+    const size_t need = seg_workspace_bytes(plan, B, H, dv);
+    if (need) {
+        if (!workspace || workspace_bytes < need) return LA_ERR_WORKSPACE;
+        if (!aligned(workspace, 256)) return LA_ERR_ALIGN;
+    }
     int *status = status_word();
     if (!status) return LA_ERR_CUDA;
     CUtensorMap mq, mk, mv;
@@ -147,6 +207,37 @@ la_status la_prefill_chunked(const void *q, const void *k, const void *v, la_dty
     a.eps = eps;
     a.status = status;
     a.wait_limit_ns = la::kWaitLimitNs;
+    a.nseg = 1;
+    a.seg_chunks = 0;
+    a.S_start = nullptr;
+    if (need) {
+        // state pass over the first nseg - 1 segments, scan, then every segment in parallel
+        const size_t BH = (size_t)B * H, state = 128 * (size_t)dv + 128;
+        float *ws = static_cast<float *>(workspace);
+        float *A = ws;
+        float *dS = ws + round_up((size_t)plan.nsub * BH * 4, 256) / 4;
+        float *S_start = dS + (size_t)plan.nsub * BH * state;
+        la::StateTcArgs sa;
+        sa.alpha = alpha;
+        sa.dS = dS;
+        sa.A = A;
+        sa.H = H;
+        sa.T = T;
+        sa.dv = dv;
+        sa.nsub = plan.nsub;
+        sa.sub_per_seg = plan.sub_per_seg;
+        sa.sub_chunks = plan.sub_chunks;
+        sa.seg_chunks = plan.seg_chunks;
+        sa.status = status;
+        sa.wait_limit_ns = la::kWaitLimitNs;
+        cudaError_t e = la::launch_state_tc(mk, mv, sa, B, alpha != nullptr, st);
+        if (e == cudaSuccess)
+            e = la::launch_seg_scan(S0, z0, A, dS, S_start, (int)BH, dv, plan.nsub, plan.sub_per_seg, plan.nseg, st);
+        if (e != cudaSuccess) return from_cuda(e);
+        a.nseg = plan.nseg;
+        a.seg_chunks = plan.seg_chunks;
+        a.S_start = S_start;
+    }
     return from_cuda(la::launch_prefill_tc(mq, mk, mv, a, B, alpha != nullptr, st));
 }
 

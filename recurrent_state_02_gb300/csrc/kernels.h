@@ -21,6 +21,9 @@ struct PrefillTcArgs {
     float *z_out;         // [B,H,128]
     uint16_t *y;          // [B,H,T,dv] BF16 bits
     int H, T, dv;
+    int nseg;             // sequence segments per head (1: the whole sequence in one CTA)
+    int seg_chunks;       // chunks per segment (nseg > 1)
+    const float *S_start; // nseg > 1: [nseg][B*H][128*dv + 128] start state of each segment (S then z)
     float eps;
     int *status;          // device status word
     unsigned long long wait_limit_ns;
@@ -32,6 +35,32 @@ struct PrefillTcArgs {
 cudaError_t launch_prefill_tc(const CUtensorMap &map_q, const CUtensorMap &map_k,
                               const CUtensorMap &map_v, const PrefillTcArgs &a, int B, bool gated,
                               cudaStream_t stream);
+
+// State pass of the sequence-segmented BF16 prefill (r == 128, dv a multiple of
+// 64, chunk 64): for every sub-segment of a head's sequence, the state it would
+// produce from a zero state and the product of its gates.
+struct StateTcArgs {
+    const float *alpha;   // [B,H,T] or nullptr
+    float *dS;            // [nsub][B*H][128*dv + 128]: S then z of each sub-segment
+    float *A;             // [nsub][B*H]: product of each sub-segment's gates (1 without a gate)
+    int H, T, dv;
+    int nsub;             // sub-segments per head: the first nseg - 1 output segments,
+    int sub_per_seg;      //   each split into sub_per_seg parts
+    int sub_chunks;       // chunks per part (the last part of a segment may be shorter)
+    int seg_chunks;       // chunks per output segment
+    int *status;          // device status word
+    unsigned long long wait_limit_ns;
+};
+
+// grid (dv/64, H, B*nsub); tensor maps k over [B*H, T, 128] and v over [B*H, T, dv]
+// as for launch_prefill_tc.
+cudaError_t launch_state_tc(const CUtensorMap &map_k, const CUtensorMap &map_v, const StateTcArgs &a, int B,
+                            bool gated, cudaStream_t stream);
+
+// S_start[g][bh] (S then z) for g < nseg: S0/z0 (zero if null) carried through the
+// sub-segment maps S -> A S + dS in order.
+cudaError_t launch_seg_scan(const float *S0, const float *z0, const float *A, const float *dS, float *S_start,
+                            int BH, int dv, int nsub, int sub_per_seg, int nseg, cudaStream_t stream);
 
 // Exact FP32 token recurrence (CUDA cores), r, dv <= 128.
 cudaError_t launch_prefill_f32(const float *q, const float *k, const float *v, const float *alpha,

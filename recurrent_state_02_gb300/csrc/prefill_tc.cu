@@ -41,16 +41,11 @@
 // Every barrier wait is bounded; on expiry the kernel records a timeout in the
 // device status word, drains its own copies and MMAs, frees TMEM and returns.
 
-#include "kernels.h"
-#include "sm103_ptx.cuh"
-
-#include <cuda_bf16.h>
+#include "tc_common.cuh"
 
 namespace la {
 namespace {
 
-constexpr int kC = 64;          // tokens per chunk
-constexpr int kR = 128;         // feature width r
 constexpr int kDVS = 64;        // value columns per CTA
 // 24 warps.  Warp w runs on scheduler w % 4 and may access TMEM lane quadrant
 // w % 4.  Warps 4..19 are the TMEM warps (four per quadrant); the producer, the
@@ -82,11 +77,6 @@ static_assert((kPhiMask & (kFixedRoles | (1u << kWarpMmaS) | (1u << kWarpMmaP)))
 // of feature rows 32 qd .. +31.  Its piece of A lies strictly above the
 // diagonal (always zero) when qq > qd: 6 of the 16 warps never read P.
 constexpr int kPWarps = 10;
-#ifndef LA_WAIT_HINT_NS
-#define LA_WAIT_HINT_NS 20000
-#endif
-constexpr uint32_t kWaitHintNs = LA_WAIT_HINT_NS;
-
 constexpr uint32_t kTileQ = kC * kR * 2;      // 16 KB: two 64-feature blocks of 64 rows x 128 B
 constexpr uint32_t kTileV = kC * kDVS * 2;    // 8 KB
 constexpr uint32_t kTileA = kC * kC * 2;      // 8 KB
@@ -98,19 +88,6 @@ constexpr uint32_t kTileOnes = kC * 128;      // 8 KB
 
 __host__ __device__ constexpr bool is_phi_warp(int w) { return (kPhiMask >> w) & 1u; }
 __host__ __device__ constexpr int phi_index(int w) { return __builtin_popcount(kPhiMask & ((1u << w) - 1u)); }
-
-// Gate data ring depth: the producer writes chunk c's entry up to a stage ring
-// ahead of its consumers, so the ring is deep enough that the entry it
-// overwrites (chunk c - kAux) was released long before.
-constexpr int kAux = 8;
-
-// Gate products of the chunks in flight (gated kernel only; chunk c in entry c % kAux).
-struct alignas(16) GateRing {
-    float gb[kAux][kC];         // cumulative log gate inside the chunk
-    int gz[kAux][kC];           // last row <= i whose gate is 0 (-1: none)
-    float gG[kAux][kC];         // Gamma_i
-    float gw[kAux][kC];         // w_j
-};
 
 #ifndef LA_STAGES
 #define LA_STAGES 4
@@ -158,149 +135,6 @@ constexpr uint32_t smem_bytes() { return Cfg<GATED>::kOffSmall + sizeof(Small) +
 static_assert(smem_bytes<false>() <= 232448, "shared memory budget");
 static_assert(smem_bytes<true>() <= 232448, "shared memory budget");
 
-// phi(x) = ELU(x) + 1 on a pair of BF16 values, in packed BF16 arithmetic:
-// phi(x) = max(min(e^x, 1), x + 1).  For x <= 0, e^x >= 1 + x picks e^x; for
-// x > 0, min(e^x, 1) = 1 <= x + 1 picks x + 1 (NaN propagates through the .NaN
-// forms).  e^x = 2^(x log2 e) with log2 e split into two BF16 parts, so that
-// the product is rounded once; the base-2 exponential is the hardware
-// approximation with flush-to-zero (phi = 0 below x = -87.3).
-__device__ __forceinline__ uint32_t phi_bf16x2(uint32_t x)
-{
-    constexpr uint32_t kLog2eHi = 0x3FB93FB9u;   // 1.4453125
-    constexpr uint32_t kLog2eLo = 0xBB2CBB2Cu;   // -0.00262451171875
-    constexpr uint32_t kOne = 0x3F803F80u;
-    constexpr uint32_t kZero = 0x80008000u;      // -0
-    uint32_t t, e, p, r;
-    asm("fma.rn.bf16x2 %0, %1, %2, %3;" : "=r"(t) : "r"(x), "r"(kLog2eLo), "r"(kZero));
-    asm("fma.rn.bf16x2 %0, %1, %2, %3;" : "=r"(t) : "r"(x), "r"(kLog2eHi), "r"(t));
-    asm("ex2.approx.ftz.bf16x2 %0, %1;" : "=r"(e) : "r"(t));
-    asm("min.NaN.bf16x2 %0, %1, %2;" : "=r"(e) : "r"(e), "r"(kOne));
-    asm("fma.rn.bf16x2 %0, %1, %2, %3;" : "=r"(p) : "r"(x), "r"(kOne), "r"(kOne));
-    asm("max.NaN.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(e), "r"(p));
-    return r;
-}
-
-struct Ctx {
-    Small *sm;
-    uint64_t limit;
-    int *status;
-};
-
-// Records a timeout once and raises the CTA-wide abort flag.
-__device__ __noinline__ void fail(Ctx &cx)
-{
-    if (!*reinterpret_cast<volatile int *>(&cx.sm->abort_flag)) {
-        atomicExch(cx.status, kStatusTimeout);
-        *reinterpret_cast<volatile int *>(&cx.sm->abort_flag) = 1;
-    }
-}
-
-__device__ __forceinline__ bool aborted(const Ctx &cx)
-{
-    return *reinterpret_cast<volatile int *>(&cx.sm->abort_flag) != 0;
-}
-
-// Bounded wait by one thread.  Gives up when the time limit runs out (and then
-// raises the abort flag) or as soon as another thread has raised it.
-__device__ __forceinline__ bool wait(Ctx &cx, uint64_t *bar, uint32_t parity)
-{
-    if (mbar_try_wait(bar, parity)) return true;
-    const uint64_t t0 = global_timer_ns();
-    for (;;) {
-        // suspended in hardware while the phase is incomplete (bounded per try)
-        if (kWaitHintNs ? mbar_try_wait_hint(bar, parity, kWaitHintNs) : mbar_try_wait(bar, parity)) return true;
-        if (aborted(cx)) return false;
-        if (global_timer_ns() - t0 > cx.limit) {
-            fail(cx);
-            return false;
-        }
-    }
-}
-
-// Warp-wide wait.  Fast path: every lane tests the phase (each lane acquires
-// for itself) and the vote keeps the branch uniform.  Otherwise lane 0 waits
-// (bounded) while the other lanes are parked at the warp barrier; the outcome
-// is broadcast so that the warp stays converged for the .sync.aligned
-// instructions that follow, and the warp barrier orders the other lanes'
-// later accesses after lane 0's acquire.
-__device__ __forceinline__ bool warp_wait(Ctx &cx, uint64_t *bar, uint32_t parity)
-{
-    if (__all_sync(0xffffffffu, mbar_try_wait(bar, parity))) return true;
-    int ok = 1;
-    if ((threadIdx.x & 31) == 0) ok = wait(cx, bar, parity);
-    ok = __shfl_sync(0xffffffffu, ok, 0);
-    __syncwarp();
-    return ok != 0;
-}
-
-// One arrival per warp, after every lane's preceding writes and fences (the
-// warp barrier orders them before lane 0's release).
-__device__ __forceinline__ void warp_arrive(uint64_t *bar)
-{
-    __syncwarp();
-    mbar_arrive_if(bar, (threadIdx.x & 31) == 0);
-}
-
-// Applies phi to the 8 BF16 values of one 16-byte chunk.
-__device__ __forceinline__ uint4 phi8(uint4 raw)
-{
-    return make_uint4(phi_bf16x2(raw.x), phi_bf16x2(raw.y), phi_bf16x2(raw.z), phi_bf16x2(raw.w));
-}
-
-// Multiplies the 8 BF16 values of one 16-byte chunk by s: s is split into two
-// BF16 parts (s = hi + lo to about 2^-16), so each product is rounded once.
-__device__ __forceinline__ uint4 scale8(uint4 raw, float s)
-{
-    const uint32_t hi = pack_bf16x2(s, s);
-    const float lo_f = s - bf16_lo(hi);
-    const uint32_t lo = pack_bf16x2(lo_f, lo_f);
-    constexpr uint32_t kZero = 0x80008000u;
-    uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-        uint32_t t;
-        asm("fma.rn.bf16x2 %0, %1, %2, %3;" : "=r"(t) : "r"(w[e]), "r"(lo), "r"(kZero));
-        asm("fma.rn.bf16x2 %0, %1, %2, %3;" : "=r"(w[e]) : "r"(w[e]), "r"(hi), "r"(t));
-    }
-    return make_uint4(w[0], w[1], w[2], w[3]);
-}
-
-// Gate products of one chunk, by one warp; lane l holds tokens 2l and 2l + 1
-// (gates past the end of the sequence are 1).  b_i is the in-chunk inclusive
-// sum of log alpha, zl_i the last row <= i whose gate is exactly 0 (-1: none);
-// Gamma_i = e^{b_i} (0 once a zero gate has been passed) and w_j =
-// e^{b_last - b_j} (0 for keys before the chunk's last zero gate).
-__device__ __forceinline__ void gate_products(float a0, float a1, int lane, int gq, GateRing *gr)
-{
-    const int j0 = 2 * lane;
-    const float l0 = a0 > 0.f ? logf(a0) : 0.f;
-    const float l1 = a1 > 0.f ? logf(a1) : 0.f;
-    const int zp0 = a0 > 0.f ? -1 : j0;
-    const int zp1 = a1 > 0.f ? zp0 : j0 + 1;
-    // inclusive warp scan of the pair totals (sum) and the pair's last zero gate (max)
-    float inc = l0 + l1;
-    int zinc = zp1;
-#pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-        const float lo = __shfl_up_sync(0xffffffffu, inc, off);
-        const int zo = __shfl_up_sync(0xffffffffu, zinc, off);
-        if (lane >= off) { inc += lo; zinc = max(zinc, zo); }
-    }
-    float ex = __shfl_up_sync(0xffffffffu, inc, 1);
-    int zex = __shfl_up_sync(0xffffffffu, zinc, 1);
-    if (lane == 0) { ex = 0.f; zex = -1; }
-    const float b0 = ex + l0, b1 = b0 + l1;
-    const int z0 = max(zex, zp0), z1 = max(zex, zp1);
-    const float blast = __shfl_sync(0xffffffffu, b1, 31);
-    const int zlast = __shfl_sync(0xffffffffu, z1, 31);
-    const float w0 = zlast <= j0 ? expf(blast - b0) : 0.f;
-    const float w1 = zlast <= j0 + 1 ? expf(blast - b1) : 0.f;
-    *reinterpret_cast<float2 *>(&gr->gb[gq][j0]) = make_float2(b0, b1);
-    *reinterpret_cast<int2 *>(&gr->gz[gq][j0]) = make_int2(z0, z1);
-    *reinterpret_cast<float2 *>(&gr->gG[gq][j0]) = make_float2(z0 < 0 ? expf(b0) : 0.f, z1 < 0 ? expf(b1) : 0.f);
-    *reinterpret_cast<float2 *>(&gr->gw[gq][j0]) = make_float2(w0, w1);
-}
-
 template <bool GATED>
 __global__ void __launch_bounds__(kThreads, 1)
 prefill_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
@@ -312,13 +146,24 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
     uint8_t *base = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     Small *sm = reinterpret_cast<Small *>(base + L::kOffSmall);
     GateRing *gr = reinterpret_cast<GateRing *>(base + L::kOffGate);   // gated only
-    Ctx cx{sm, args.wait_limit_ns, args.status};
+    Ctx cx{&sm->abort_flag, args.wait_limit_ns, args.status};
 
     const int slice = blockIdx.x;
-    const int h = blockIdx.y, b = blockIdx.z;
+    // grid.z enumerates (b, sequence segment); one segment unless the caller
+    // split the sequence (then every segment starts from a scanned state)
+    const int h = blockIdx.y, b = blockIdx.z / args.nseg, seg = blockIdx.z % args.nseg;
     const int bh = b * args.H + h;
     const int T = args.T;
-    const int nch = (T + kC - 1) / kC;
+    const int nch_all = (T + kC - 1) / kC;
+    const int c0 = seg * args.seg_chunks;                                     // first chunk of the segment
+    const int nch = args.nseg > 1 ? min(args.seg_chunks, nch_all - c0) : nch_all;   // its chunk count
+    const int tb = c0 * kC;                                                   // its first token
+    const bool last_seg = seg == args.nseg - 1;
+    // start state of this head: S0/z0, or the scanned state of the segment
+    const size_t state_len = (size_t)kR * args.dv + kR;
+    const float *S_init = args.S_start ? args.S_start + ((size_t)seg * (gridDim.z / args.nseg) * args.H + bh) * state_len
+                                       : (args.S0 ? args.S0 + (size_t)bh * kR * args.dv : nullptr);
+    const float *z_init_src = args.S_start ? S_init + (size_t)kR * args.dv : (args.z0 ? args.z0 + (size_t)bh * kR : nullptr);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
     auto stage_ptr = [&](int s) { return base + s * L::kStageBytes; };
@@ -374,12 +219,13 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = sm->tmem_base;
-    // The dv slices of one head form a cluster: no slice may write z_out (which
-    // may alias z0) before every slice has read z0.  Every thread takes part.
+    // The dv slices of one head (and segment) form a cluster: no slice may write
+    // z_out (which may alias z0) before every slice has read z0.  Every thread
+    // takes part.  (Segmented runs read their start state from the workspace.)
     const bool clustered = gridDim.x > 1;
     float z_init = 0.f;
-    if (warp >= kWarpTm0 && warp < kWarpTm0 + kTmWarps && args.z0)
-        z_init = args.z0[(size_t)bh * kR + (warp & 3) * 32 + lane];
+    if (warp >= kWarpTm0 && warp < kWarpTm0 + kTmWarps && z_init_src)
+        z_init = z_init_src[(warp & 3) * 32 + lane];
     if (clustered) {
         asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
         asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
@@ -394,7 +240,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
         int issued = 0;
         for (int c = 0; c < nch; ++c) {
             const int s = c % NST;
-            const int t0 = c * kC;
+            const int t0 = tb + c * kC;
             float a0 = 1.f, a1 = 1.f;
             if (GATED) {
                 const float *ap = args.alpha + (size_t)bh * T;
@@ -562,7 +408,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
         {
             // initial state
             float S[16];
-            const float *src = args.S0 ? args.S0 + ((size_t)bh * kR + srow) * args.dv + slice * kDVS + qq * 16 : nullptr;
+            const float *src = S_init ? S_init + (size_t)srow * args.dv + slice * kDVS + qq * 16 : nullptr;
 #pragma unroll
             for (int j = 0; j < 16; ++j) S[j] = src ? src[j] : 0.f;
             tc_st_32x32b_x16(tS, S);
@@ -627,7 +473,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
                 yp.w = pack_bf16x2(o[6] * inv, o[7] * inv);
                 // 8 columns (16 bytes) of token row prow, straight to global memory
                 // (streaming stores: y is not read again here)
-                const int t = (c - 2) * kC + prow;
+                const int t = tb + (c - 2) * kC + prow;
                 if (t < T) __stcs(reinterpret_cast<uint4 *>(args.y + ((size_t)bh * T + t) * args.dv + slice * kDVS + pcol), yp);
             }
             // A = the causal mask (and, with a gate, the in-chunk decay) applied to P
@@ -662,7 +508,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
                     *reinterpret_cast<uint4 *>(base + L::kOffA + bb * kTileA + sw128_offset(prow, pcol >> 3)) =
                         make_uint4(pack_bf16x2(p[0], p[1]), pack_bf16x2(p[2], p[3]), pack_bf16x2(p[4], p[5]),
                                    pack_bf16x2(p[6], p[7]));
-            } else if (has_s) {
+            } else if (has_s && last_seg) {
                 // c == nch: the state after the last chunk
                 float *dst = args.S_out + ((size_t)bh * kR + srow) * args.dv + slice * kDVS + qq * 16;
 #pragma unroll
@@ -701,7 +547,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
         bool ok = true;
         for (int c = 0; c < nch && ok; ++c) {
             const int s = c % NST;
-            const int nvalid = min(kC, T - c * kC);
+            const int nvalid = min(kC, T - tb - c * kC);
             if (!warp_wait(cx, &sm->full[s], (c / NST) & 1)) { ok = false; break; }
             uint8_t *st = stage_ptr(s);
             // phi(Q), phi(K) in place (the two tiles are contiguous: 2048 chunks of
@@ -742,7 +588,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
 cudaError_t launch_prefill_tc(const CUtensorMap &map_q, const CUtensorMap &map_k, const CUtensorMap &map_v,
                               const PrefillTcArgs &a, int B, bool gated, cudaStream_t stream)
 {
-    const dim3 grid(a.dv / kDVS, a.H, B);
+    const dim3 grid(a.dv / kDVS, a.H, B * a.nseg);
     const uint32_t bytes = gated ? smem_bytes<true>() : smem_bytes<false>();
     auto kern = gated ? prefill_tc_kernel<true> : prefill_tc_kernel<false>;
     // The attribute is set once per device (not during stream capture of later calls).

@@ -1,0 +1,334 @@
+// state_tc.cu -- the state pass and the scan of the sequence-segmented prefill.
+//
+// Method ("Linear attention：把历史写进状态", hs-black.github.io/posts/linear-attention,
+// section "门控递推为什么能做并行 scan？"): the per-token updates
+//     S_t = alpha_t S_{t-1} + phi(k_t) v_t^T,   z_t = alpha_t z_{t-1} + phi(k_t)
+// are affine maps of the state, and a run of them composes into one affine map
+//     S -> A S + dS,   z -> A z + dz,
+// with A the product of the run's gates and (dS, dz) the state the run would
+// produce from a zero state.  state_tc_kernel computes (A, dS, dz) for each
+// sub-segment of a head's sequence, chunk by chunk exactly as the prefill
+// kernel updates its state (the same gate products, feature map and operand
+// rounding); seg_scan_kernel then applies the maps in sequence order to S0, z0
+// and writes the start state of every output segment, from which the prefill
+// kernel processes the segments in parallel.
+
+#include "tc_common.cuh"
+
+namespace la {
+namespace {
+
+constexpr int kDVS = 64;            // value columns per CTA
+constexpr int kThreads = 384;       // 12 warps
+constexpr int kWarpTma = 0, kWarpMma = 1, kWarpTm0 = 4, kTmWarps = 4;
+// phi warps: 2, 3 and 8..11 (spread over the four schedulers)
+__host__ __device__ constexpr bool is_phi_warp(int w) { return w == 2 || w == 3 || w >= 8; }
+__host__ __device__ constexpr int phi_index(int w) { return w < 4 ? w - 2 : w - 6; }
+constexpr int kPhiWarps = 6, kPhiThreads = kPhiWarps * 32;
+constexpr int kStages = 6;
+constexpr uint32_t kTileK = kC * kR * 2;       // 16 KB: two 64-feature blocks of 64 rows x 128 B
+constexpr uint32_t kTileV = kC * kDVS * 2;     // 8 KB
+constexpr uint32_t kTileOnes = kC * 128;       // 8 KB: the second 64-column block of [V | 1 0..]
+constexpr uint32_t kOffK = 0, kOffV = kTileK, kStageBytes = kTileK + kTileV;
+static_assert(kStageBytes % 1024 == 0, "stage tiles stay 1024-byte aligned");
+constexpr uint32_t kOffOnes = kStages * kStageBytes;
+constexpr uint32_t kOffGate = kOffOnes + kTileOnes;
+constexpr uint32_t kTmemCols = 128;            // [S | z]: 80 columns (z is column 64)
+
+struct alignas(16) SmallS {
+    uint64_t full[kStages], empty[kStages], phi_done[kStages];
+    uint64_t dS_full, S_read, mma_done, aux_empty[kAux];
+    uint32_t tmem_base;
+    int abort_flag;
+};
+
+template <bool GATED>
+__host__ __device__ constexpr uint32_t off_small() { return kOffGate + (GATED ? sizeof(GateRing) : 0); }
+template <bool GATED>
+__host__ __device__ constexpr uint32_t smem_bytes() { return off_small<GATED>() + sizeof(SmallS) + 1024; }
+static_assert(smem_bytes<true>() <= 232448, "shared memory budget");
+
+template <bool GATED>
+__global__ void __launch_bounds__(kThreads, 1)
+state_tc_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant__ CUtensorMap map_v,
+                const StateTcArgs args)
+{
+    constexpr int NST = kStages;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *base = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    SmallS *sm = reinterpret_cast<SmallS *>(base + off_small<GATED>());
+    GateRing *gr = reinterpret_cast<GateRing *>(base + kOffGate);   // gated only
+    Ctx cx{&sm->abort_flag, args.wait_limit_ns, args.status};
+
+    // grid: (dv slice, h, b * nsub + m); sub-segment m is part j of output segment g
+    const int slice = blockIdx.x, h = blockIdx.y;
+    const int b = blockIdx.z / args.nsub, m = blockIdx.z % args.nsub;
+    const int BH = (gridDim.z / args.nsub) * args.H;
+    const int bh = b * args.H + h;
+    const int T = args.T;
+    const int g = m / args.sub_per_seg, j = m % args.sub_per_seg;
+    const int cs = g * args.seg_chunks + j * args.sub_chunks;                 // first chunk
+    const int nch = max(0, min(cs + args.sub_chunks, (g + 1) * args.seg_chunks) - cs);
+    const int tb = cs * kC;                                                   // first token
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    auto stage_ptr = [&](int s) { return base + s * kStageBytes; };
+
+    // ------------------------------------------------------------ set-up
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < NST; ++s) {
+            mbar_init(&sm->full[s], GATED ? 2 : 1);   // TMA bytes (+ gate data)
+            mbar_init(&sm->empty[s], 1);
+            mbar_init(&sm->phi_done[s], kPhiWarps);
+        }
+        for (int i = 0; i < kAux; ++i) mbar_init(&sm->aux_empty[i], kTmWarps);
+        mbar_init(&sm->dS_full, 1);
+        mbar_init(&sm->S_read, kTmWarps);
+        mbar_init(&sm->mma_done, 1);
+        sm->abort_flag = 0;
+        fence_mbarrier_init();
+        tma_prefetch_desc(&map_k);
+        tma_prefetch_desc(&map_v);
+    }
+    for (int i = threadIdx.x; i < (int)kTileOnes / 16; i += kThreads)
+        reinterpret_cast<uint4 *>(base + kOffOnes)[i] = make_uint4(0, 0, 0, 0);
+    __syncthreads();
+    if (threadIdx.x < kC)   // element (column 0, token row k): 16-byte chunk 0 of row k after the swizzle
+        *reinterpret_cast<uint16_t *>(base + kOffOnes + sw128_offset(threadIdx.x, 0)) = 0x3F80u;
+    fence_proxy_async_smem();
+    if (warp == kWarpMma) {
+        tmem_alloc(&sm->tmem_base, kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = sm->tmem_base;
+    // the state starts at zero, before any increment is issued
+    if (warp >= kWarpTm0 && warp < kWarpTm0 + kTmWarps) {
+        const uint32_t lb = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
+        float zero[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) zero[i] = 0.f;
+        tc_st_32x32b_x32(lb, zero);
+        tc_st_32x32b_x32(lb + 32, zero);
+        tc_st_32x32b_x1(lb + 64, 0.f);
+        tc_wait_st();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+
+    if (warp == kWarpTma) {
+        // ------------------------------------------------------- producer
+        int issued = 0;
+        for (int c = 0; c < nch; ++c) {
+            const int s = c % NST;
+            const int t0 = tb + c * kC;
+            float a0 = 1.f, a1 = 1.f;
+            if (GATED) {
+                const float *ap = args.alpha + (size_t)bh * T;
+                if (t0 + 2 * lane < T) a0 = ap[t0 + 2 * lane];
+                if (t0 + 2 * lane + 1 < T) a1 = ap[t0 + 2 * lane + 1];
+            }
+            if (c >= NST && !warp_wait(cx, &sm->empty[s], ((c / NST) - 1) & 1)) break;
+            if (GATED && c >= kAux && !warp_wait(cx, &sm->aux_empty[c % kAux], ((c / kAux) - 1) & 1)) break;
+            if (__shfl_sync(0xffffffffu, aborted(cx) ? 1 : 0, 0)) break;
+            uint8_t *st = stage_ptr(s);
+            if (lane == 0) {
+                mbar_arrive_expect_tx(&sm->full[s], kTileK + kTileV);
+                tma_load_3d(st + kOffK, &map_k, &sm->full[s], 0, t0, bh);
+                tma_load_3d(st + kOffK + kTileK / 2, &map_k, &sm->full[s], 64, t0, bh);
+                tma_load_3d(st + kOffV, &map_v, &sm->full[s], slice * kDVS, t0, bh);
+                if (c + NST < nch) {   // warm L2 for the load that reuses this stage
+                    const int tp = t0 + NST * kC;
+                    if (slice == 0) {
+                        tma_prefetch_l2_3d(&map_k, 0, tp, bh);
+                        tma_prefetch_l2_3d(&map_k, 64, tp, bh);
+                    }
+                    tma_prefetch_l2_3d(&map_v, slice * kDVS, tp, bh);
+                }
+            }
+            if (GATED) {
+                gate_products(a0, a1, lane, c % kAux, gr);
+                warp_arrive(&sm->full[s]);
+            }
+            issued = c + 1;
+        }
+        if (lane == 0 && aborted(cx)) {
+            // Drain: every issued load must land before the CTA may exit.
+            for (int c = (issued > NST ? issued - NST : 0); c < issued; ++c)
+                mbar_wait(&sm->full[c % NST], (c / NST) & 1, cx.limit);
+        }
+        __syncwarp();
+    } else if (warp == kWarpMma) {
+        // ------------------------------------------------------------ MMA
+        // [S | z] += K~'^T [V | 1] per chunk (K~' = diag(w) K~ with a gate), once
+        // phi of the chunk is done and, with a gate, the TMEM warps have decayed
+        // the state by the chunk's gate product.
+        if (lane == 0) {
+            constexpr uint32_t idDS = idesc_bf16_f32(128, 80, true, true);
+            constexpr uint32_t kHi128 = desc_hi(1024, 2);
+            const uint32_t aOnes = smem_u32(base + kOffOnes);
+            for (int c = 0; c < nch && !aborted(cx); ++c) {
+                const int s = c % NST;
+                const uint32_t st = smem_u32(stage_ptr(s));
+                if (!wait(cx, &sm->phi_done[s], (c / NST) & 1)) break;
+                if (GATED && !wait(cx, &sm->S_read, c & 1)) break;
+                tc_fence_after();
+                const uint32_t klo = desc_lo(st + kOffK, kTileK / 2);   // K~^T: MN-major, two 64-feature blocks
+                const uint32_t blo = desc_lo(st + kOffV, aOnes - (st + kOffV));   // [V | 1]
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk)
+                    tc_mma_bf16_w<true>(tmem, klo + kk * (2048 >> 4), kHi128, blo + kk * (2048 >> 4), kHi128, idDS);
+                tc_commit(&sm->dS_full);
+                tc_commit(&sm->empty[s]);
+            }
+            tc_commit(&sm->mma_done);
+            mbar_wait(&sm->mma_done, 0, cx.limit);
+        }
+        __syncwarp();
+    } else if (warp >= kWarpTm0 && warp < kWarpTm0 + kTmWarps) {
+        // ----------------------------------------------------- TMEM warps
+        // Warp w holds feature rows 32 (w % 4) .. +31, all 64 columns and z.
+        const int qd = warp & 3;
+        const uint32_t lane_base = static_cast<uint32_t>(qd * 32) << 16;
+        const int srow = qd * 32 + lane;
+        float decay = 1.f;
+        if (GATED) {
+            // decay the state by the gate product of chunk c before its increment lands
+            for (int c = 0; c < nch; ++c) {
+                if (c >= 1 && !warp_wait(cx, &sm->dS_full, (c - 1) & 1)) break;
+                if (!warp_wait(cx, &sm->phi_done[c % NST], (c / NST) & 1)) break;   // gate data of chunk c
+                tc_fence_after();
+                const float gl = gr->gG[c % kAux][kC - 1];
+                decay *= gl;
+                float s0[32], s1[32], zz;
+                tc_ld_32x32b_x32(tmem + lane_base, s0);
+                tc_ld_32x32b_x32(tmem + lane_base + 32, s1);
+                tc_ld_32x32b_x1(tmem + lane_base + 64, zz);
+                tc_wait_ld();
+#pragma unroll
+                for (int i = 0; i < 32; ++i) { s0[i] *= gl; s1[i] *= gl; }
+                tc_st_32x32b_x32(tmem + lane_base, s0);
+                tc_st_32x32b_x32(tmem + lane_base + 32, s1);
+                tc_st_32x32b_x1(tmem + lane_base + 64, zz * gl);
+                tc_wait_st();
+                tc_fence_before();
+                warp_arrive(&sm->S_read);
+                warp_arrive(&sm->aux_empty[c % kAux]);
+            }
+        }
+        // the sub-segment's (A, dS, dz) once every increment has landed
+        if (!aborted(cx)) {
+            int ok = 1;
+            if (lane == 0) ok = mbar_wait(&sm->mma_done, 0, cx.limit);
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            __syncwarp();
+            if (ok) {
+                tc_fence_after();
+                float s0[32], s1[32], zz;
+                tc_ld_32x32b_x32(tmem + lane_base, s0);
+                tc_ld_32x32b_x32(tmem + lane_base + 32, s1);
+                tc_ld_32x32b_x1(tmem + lane_base + 64, zz);
+                tc_wait_ld();
+                const size_t state_len = (size_t)kR * args.dv + kR;
+                float *out = args.dS + ((size_t)m * BH + bh) * state_len;
+                float *dst = out + (size_t)srow * args.dv + slice * kDVS;
+#pragma unroll
+                for (int i = 0; i < 32; i += 4) {
+                    *reinterpret_cast<float4 *>(dst + i) = make_float4(s0[i], s0[i + 1], s0[i + 2], s0[i + 3]);
+                    *reinterpret_cast<float4 *>(dst + 32 + i) = make_float4(s1[i], s1[i + 1], s1[i + 2], s1[i + 3]);
+                }
+                if (slice == 0) {
+                    out[(size_t)kR * args.dv + srow] = zz;
+                    if (warp == kWarpTm0 && lane == 0) args.A[(size_t)m * BH + bh] = decay;
+                }
+            } else {
+                fail(cx);
+            }
+        }
+    } else if (is_phi_warp(warp)) {
+        // ------------------------------------------------------ phi warps
+        // phi(K) in place, with a gate times w_j on key row j; rows past the end
+        // of the sequence become 0
+        const int pp = phi_index(warp) * 32 + lane;
+        for (int c = 0; c < nch; ++c) {
+            const int s = c % NST;
+            if (!warp_wait(cx, &sm->full[s], (c / NST) & 1)) break;
+            const int nvalid = min(kC, T - tb - c * kC);
+            uint4 *kt = reinterpret_cast<uint4 *>(stage_ptr(s) + kOffK);
+            for (int ci = pp; ci < (int)kTileK / 16; ci += kPhiThreads) {
+                const int row = (ci & 511) >> 3;   // 8 chunks per 128-byte row, 64 rows per block
+                uint4 v = row < nvalid ? phi8(kt[ci]) : make_uint4(0, 0, 0, 0);
+                if (GATED) v = scale8(v, gr->gw[c % kAux][row]);
+                kt[ci] = v;
+            }
+            fence_proxy_async_smem();
+            warp_arrive(&sm->phi_done[s]);
+        }
+    }
+
+    // ---------------------------------------------------------- teardown
+    tc_fence_before();
+    __syncthreads();
+    if (warp == kWarpMma) {
+        tc_fence_after();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+// S_start[g] for every output segment g: the state before its first chunk.
+// One thread per element of a head's state (S then z).
+__global__ void seg_scan_kernel(const float *S0, const float *z0, const float *A, const float *dS, float *S_start,
+                                int BH, int dv, int nsub, int sub_per_seg, int nseg)
+{
+    const int bh = blockIdx.y;
+    const int e = blockIdx.x * blockDim.x + threadIdx.x;
+    const int s_len = kR * dv;
+    const int state_len = s_len + kR;
+    if (e >= state_len) return;
+    float s;
+    if (e < s_len) s = S0 ? S0[(size_t)bh * s_len + e] : 0.f;
+    else s = z0 ? z0[(size_t)bh * kR + (e - s_len)] : 0.f;
+    S_start[(size_t)bh * state_len + e] = s;
+    for (int m = 0; m < nsub; ++m) {
+        s = fmaf(A[(size_t)m * BH + bh], s, dS[((size_t)m * BH + bh) * state_len + e]);
+        if ((m + 1) % sub_per_seg == 0) {
+            const int g = (m + 1) / sub_per_seg;
+            if (g < nseg) S_start[((size_t)g * BH + bh) * state_len + e] = s;
+        }
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_state_tc(const CUtensorMap &map_k, const CUtensorMap &map_v, const StateTcArgs &a, int B,
+                            bool gated, cudaStream_t stream)
+{
+    const dim3 grid(a.dv / kDVS, a.H, B * a.nsub);
+    const uint32_t bytes = gated ? smem_bytes<true>() : smem_bytes<false>();
+    auto kern = gated ? state_tc_kernel<true> : state_tc_kernel<false>;
+    static bool attr_set[2][64] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    if (!attr_set[gated][dev]) {
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+        if (e != cudaSuccess) return e;
+        attr_set[gated][dev] = true;
+    }
+    kern<<<grid, kThreads, bytes, stream>>>(map_k, map_v, a);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_seg_scan(const float *S0, const float *z0, const float *A, const float *dS, float *S_start,
+                            int BH, int dv, int nsub, int sub_per_seg, int nseg, cudaStream_t stream)
+{
+    const int state_len = kR * dv + kR;
+    const dim3 grid((state_len + 255) / 256, BH);
+    seg_scan_kernel<<<grid, 256, 0, stream>>>(S0, z0, A, dS, S_start, BH, dv, nsub, sub_per_seg, nseg);
+    return cudaGetLastError();
+}
+
+}  // namespace la

@@ -183,3 +183,78 @@ def test_wait_timeout_is_reported(la):
     S, z = la.state_init(2, 2, 4, 4)
     torch.cuda.synchronize()
     assert not S.any()
+
+
+# ------------------------------------------------------ segmented prefill
+# Few heads and a long sequence leave most SMs idle; the kernel then splits each
+# sequence into segments that start from scanned states (LA "门控递推为什么能做并行
+# scan？": the per-token updates are affine maps of the state and compose).
+
+SEG_T = 47 * 64 - 21   # 47 chunks, ragged last chunk
+
+
+def _segments(la, B, H, T, dv=128):
+    return la.prefill_workspace_bytes(B, H, T, 128, dv)
+
+
+@pytest.mark.parametrize("gated", [False, True])
+@pytest.mark.parametrize("with_state", [False, True])
+def test_prefill_segmented(la, oracle_mod, gated, with_state):
+    assert _segments(la, 1, 3, SEG_T) > 0
+    inp = _inputs(torch.bfloat16, 1, 3, SEG_T, 128, 128, gated=gated, with_state=with_state, seed=31)
+    _check(_gpu_prefill(la, inp), _oracle_prefill(oracle_mod, inp), 2e-2, "segmented")
+
+
+def test_prefill_segmented_dv64(la, oracle_mod):
+    assert _segments(la, 2, 1, SEG_T, dv=64) > 0
+    inp = _inputs(torch.bfloat16, 2, 1, SEG_T, 128, 64, gated=True, with_state=True, seed=32)
+    _check(_gpu_prefill(la, inp), _oracle_prefill(oracle_mod, inp), 2e-2, "segmented dv64")
+
+
+def test_prefill_segmented_zero_gates(la, oracle_mod):
+    """alpha = 0 at and around segment and part boundaries is exact: nothing before it survives."""
+    assert _segments(la, 1, 2, SEG_T) > 0
+    inp = _inputs(torch.bfloat16, 1, 2, SEG_T, 128, 128, gated=True, with_state=True, seed=33)
+    for t in (0, 63, 64, 65, 1535, 1536, 1537, 2000, SEG_T - 1):
+        inp["alpha"][0, 0, t] = 0.0
+    inp["alpha"][0, 1, 1500:1600] = 0.0
+    _check(_gpu_prefill(la, inp), _oracle_prefill(oracle_mod, inp), 2e-2, "segmented zero gates")
+
+
+def test_prefill_segmented_in_place(la, oracle_mod):
+    """S0 may alias S_out with segments: every segment reads its start state from the workspace."""
+    assert _segments(la, 1, 3, SEG_T) > 0
+    inp = _inputs(torch.bfloat16, 1, 3, SEG_T, 128, 128, gated=True, with_state=True, seed=34)
+    ref = _oracle_prefill(oracle_mod, inp)
+    d = {k: v.cuda() for k, v in inp.items()}
+    S, z = d["S0"], d["z0"]
+    y, _, _ = la.prefill_chunked(d["q"], d["k"], d["v"], alpha=d["alpha"], S0=S, z0=z, S_out=S, z_out=z)
+    assert la.last_device_status() == 0
+    _check((y.float().cpu().numpy(), S.cpu().numpy(), z.cpu().numpy()), ref, 2e-2, "segmented in place")
+
+
+def test_prefill_workspace_errors(la):
+    """A segmenting shape without (enough, aligned) workspace is refused before any launch."""
+    from recurrent_state_02_gb300 import _native
+    need = _segments(la, 1, 3, SEG_T)
+    assert need > 0
+    inp = _inputs(torch.bfloat16, 1, 3, SEG_T, 128, 128, seed=35)
+    d = {k: (v.cuda() if v is not None else None) for k, v in inp.items()}
+    y = torch.empty_like(d["v"])
+    S = torch.empty(1, 3, 128, 128, device="cuda")
+    z = torch.empty(1, 3, 128, device="cuda")
+    ws = torch.empty(need + 512, device="cuda", dtype=torch.uint8)
+    L = _native.lib()
+    P = lambda t: t.data_ptr()
+    sh = torch.cuda.current_stream().cuda_stream
+
+    def call(wptr, wbytes):
+        return L.la_prefill_chunked(P(d["q"]), P(d["k"]), P(d["v"]), _native.LA_DTYPE_BF16, None, None, None,
+                                    1, 3, SEG_T, 128, 128, 64, 1e-6, P(y), P(S), P(z), wptr, wbytes, sh)
+
+    assert call(None, 0) == _native.LA_ERR_WORKSPACE
+    assert call(P(ws), need - 1) == _native.LA_ERR_WORKSPACE
+    assert call(P(ws) + 16, need) == _native.LA_ERR_ALIGN
+    assert call(P(ws), need) == 0
+    torch.cuda.synchronize()
+    assert la.last_device_status() == 0
