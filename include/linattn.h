@@ -125,6 +125,28 @@ la_status la_prefill_chunked(const void *q, const void *k, const void *v, la_dty
                              void *workspace, size_t workspace_bytes, la_stream_t stream);
 
 /*
+ * la_prefill_chunked_noalloc -- la_prefill_chunked without caller scratch: the
+ * workspace is a 16 MiB buffer compiled into the library (a static device array),
+ * one per device for the whole process.  The pages have no counterpart; it is an
+ * integration aid for callers that must not allocate device memory per call,
+ * such as a serving loop that reserved its whole memory budget up front, or C
+ * code without a caching allocator, where cudaMalloc/cudaFree would add
+ * device-wide synchronisation and can fail under memory pressure.
+ *   Arguments, results and errors are those of la_prefill_chunked, without
+ *   workspace.  LA_ERR_WORKSPACE when la_prefill_workspace_bytes for these sizes
+ *   exceeds the 16 MiB (on a 152-SM device no size needs more than about 10 MB).
+ *   The first call on a device looks up the buffer's device address with that
+ *   device current; make it before any stream capture.
+ *   Nothing in the buffer has to start at zero: a call writes every entry before
+ *   reading it.  Calls that may overlap in time (other streams, other threads)
+ *   race on the one buffer; the caller must serialise them.
+ */
+la_status la_prefill_chunked_noalloc(const void *q, const void *k, const void *v, la_dtype dtype,
+                                     const float *alpha, const float *S0, const float *z0,
+                                     int B, int H, int T, int r, int dv, int chunk, float eps,
+                                     void *y, float *S_out, float *z_out, la_stream_t stream);
+
+/*
  * la_decode_step -- one new token per (b, h), state updated in place:
  *   S <- alpha S + phi(k) v^T,  z <- alpha z + phi(k),  y = phi(q)^T S / (phi(q)^T z + eps)
  * ([LA] "公式里的每个维度" and "查询时，分子和分母一起读"; update before read).

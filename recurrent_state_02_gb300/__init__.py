@@ -93,6 +93,34 @@ def prefill_chunked(q, k, v, alpha=None, S0=None, z0=None, chunk=64, eps=1e-6, y
     return y, S_out, z_out
 
 
+def prefill_chunked_noalloc(q, k, v, y, S_out, z_out, alpha=None, S0=None, z0=None, chunk=64, eps=1e-6):
+    """As prefill_chunked, with the library's built-in scratch instead of a
+    workspace; nothing is allocated here either, so y [B,H,T,dv] (input dtype),
+    S_out [B,H,r,dv] and z_out [B,H,r] (fp32) must be given.  Calls that may
+    overlap in time share one buffer per device and must be serialised."""
+    if q.dtype not in _DTYPES:
+        raise ValueError(f"unsupported dtype {q.dtype}")
+    B, H, T, r = q.shape
+    dv = v.shape[3]
+    dev = q.device
+    _require(q, "q", (B, H, T, r), q.dtype, dev)
+    _require(k, "k", (B, H, T, r), q.dtype, dev)
+    _require(v, "v", (B, H, T, dv), q.dtype, dev)
+    _require(alpha, "alpha", (B, H, T), torch.float32, dev)
+    _require(S0, "S0", (B, H, r, dv), torch.float32, dev)
+    _require(z0, "z0", (B, H, r), torch.float32, dev)
+    if y is None or S_out is None or z_out is None:
+        raise ValueError("y, S_out and z_out must be given (this entry point allocates nothing)")
+    _require(y, "y", (B, H, T, dv), q.dtype, dev)
+    _require(S_out, "S_out", (B, H, r, dv), torch.float32, dev)
+    _require(z_out, "z_out", (B, H, r), torch.float32, dev)
+    st = _native.lib().la_prefill_chunked_noalloc(
+        _ptr(q), _ptr(k), _ptr(v), _DTYPES[q.dtype], _ptr(alpha), _ptr(S0), _ptr(z0), B, H, T, r, dv, chunk,
+        float(eps), _ptr(y), _ptr(S_out), _ptr(z_out), _stream(dev))
+    _native.check(st, "la_prefill_chunked_noalloc")
+    return y, S_out, z_out
+
+
 def decode_step(q, k, v, S, z, alpha=None, eps=1e-6, y=None):
     """One token per request, state updated in place.  q, k [B,H,1,r], v [B,H,1,dv];
     S [B,H,r,dv], z [B,H,r] fp32 (overwritten); alpha [B,H] fp32 or None.  Returns y [B,H,1,dv]."""

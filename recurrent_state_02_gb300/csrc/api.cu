@@ -86,6 +86,28 @@ size_t seg_workspace_bytes(const SegPlan &p, int B, int H, int dv)
     return round_up((size_t)p.nsub * BH * 4, 256) + (size_t)p.nsub * BH * state * 4 + (size_t)p.nseg * BH * state * 4;
 }
 
+// Scratch of la_prefill_chunked_noalloc: a fixed buffer in the library's device
+// image, for callers that cannot pass device memory of their own.  16 MiB holds
+// the segmented-prefill workspace of every plan on devices with up to about 240
+// SMs (the plan keeps (parts + segments) * heads below about 2 * SMs states).
+constexpr size_t kNoAllocScratchBytes = size_t(16) << 20;
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+// Device address of the scratch on the current device, looked up once per device
+// (the first call there does it, with that device current); nullptr on failure.
+void *noalloc_scratch()
+{
+    static void *addr[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+    if (!addr[dev]) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return nullptr;
+        addr[dev] = p;
+    }
+    return addr[dev];
+}
+
 // 3-D BF16 view [planes, rows, cols] (cols innermost) with boxes of box_cols x
 // box_rows; rows past the end of a plane read as zero and are never written.
 bool make_map_bf16(CUtensorMap *map, const void *ptr, long long planes, long long rows, long long cols,
@@ -239,6 +261,22 @@ la_status la_prefill_chunked(const void *q, const void *k, const void *v, la_dty
         a.S_start = S_start;
     }
     return from_cuda(la::launch_prefill_tc(mq, mk, mv, a, B, alpha != nullptr, st));
+}
+
+la_status la_prefill_chunked_noalloc(const void *q, const void *k, const void *v, la_dtype dtype,
+                                     const float *alpha, const float *S0, const float *z0, int B, int H, int T,
+                                     int r, int dv, int chunk, float eps, void *y, float *S_out, float *z_out,
+                                     la_stream_t stream)
+{
+    const size_t need = dtype == LA_DTYPE_BF16 ? la_prefill_workspace_bytes(B, H, T, r, dv, chunk) : 0;
+    if (need > kNoAllocScratchBytes) return LA_ERR_WORKSPACE;
+    void *scratch = nullptr;
+    if (need) {
+        scratch = noalloc_scratch();
+        if (!scratch) return LA_ERR_CUDA;
+    }
+    return la_prefill_chunked(q, k, v, dtype, alpha, S0, z0, B, H, T, r, dv, chunk, eps, y, S_out, z_out, scratch,
+                              need, stream);
 }
 
 la_status la_decode_step(const void *q, const void *k, const void *v, la_dtype dtype, const float *alpha, float *S,
