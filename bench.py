@@ -77,7 +77,8 @@ def source_sha1(paths):
 def kernel_sources(name):
     """The files a kernel is compiled from (its .cu and the headers it includes)."""
     csrc = os.path.join(ROOT, "recurrent_state_02_gb300", "csrc")
-    return [os.path.join(csrc, f) for f in (name, "kernels.h", "sm103_ptx.cuh")]
+    common = ("tc_common.cuh",) if name == "prefill_tc.cu" else ()
+    return [os.path.join(csrc, f) for f in (name, "kernels.h", "sm103_ptx.cuh") + common]
 
 
 def profile_traffic(kernel, workload, src):
