@@ -76,7 +76,6 @@ static_assert((kPhiMask & (kFixedRoles | (1u << kWarpMmaS) | (1u << kWarpMmaP)))
 // 16 qq .. +15 of the 64 x 64 tiles P, A and O, and state columns 16 qq .. +15
 // of feature rows 32 qd .. +31.  Its piece of A lies strictly above the
 // diagonal (always zero) when qq > qd: 6 of the 16 warps never read P.
-constexpr int kPWarps = 10;
 constexpr uint32_t kTileQ = kC * kR * 2;      // 16 KB: two 64-feature blocks of 64 rows x 128 B
 constexpr uint32_t kTileV = kC * kDVS * 2;    // 8 KB
 constexpr uint32_t kTileA = kC * kC * 2;      // 8 KB
@@ -123,8 +122,11 @@ struct Cfg {
 
 struct alignas(16) Small {
     uint64_t full[4], empty[4], phi_done[4], sc_done[4];
-    uint64_t P_full[2], P_empty[2], dS_full, S_read, Sp_full[2], Sp_empty[2];
-    uint64_t A_full[2], A_empty[2], O_full[2], O_empty[2], aux_empty[kAux];
+    // tm_read[c % 2]: the TMEM warps have read what chunk c's iteration reads
+    // (the state, P of chunk c, O of chunk c-2); ops_full[c % 2]: they have
+    // written Sprev and A of chunk c
+    uint64_t P_full[2], dS_full, tm_read[2], ops_full[2], Sp_empty;
+    uint64_t A_empty[2], O_full[2], aux_empty[kAux];
     uint64_t mma_done[kIssuers];
     uint32_t tmem_base;
     int abort_flag;
@@ -142,6 +144,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
 {
     using L = Cfg<GATED>;
     constexpr int NST = L::kStages, NP = L::kNP;
+    static_assert(NP == 2, "score buffers alternate with the parity of tm_read");
     extern __shared__ uint8_t smem_raw[];
     uint8_t *base = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     Small *sm = reinterpret_cast<Small *>(base + L::kOffSmall);
@@ -178,17 +181,14 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&sm->P_full[i], 1);
-            mbar_init(&sm->P_empty[i], kPWarps);
-            mbar_init(&sm->Sp_full[i], kTmWarps);
-            mbar_init(&sm->Sp_empty[i], 1);
-            mbar_init(&sm->A_full[i], kTmWarps);
+            mbar_init(&sm->tm_read[i], kTmWarps);
+            mbar_init(&sm->ops_full[i], kTmWarps);
             mbar_init(&sm->A_empty[i], 1);
             mbar_init(&sm->O_full[i], 1);
-            mbar_init(&sm->O_empty[i], kTmWarps);
         }
+        mbar_init(&sm->Sp_empty, 1);
         for (int i = 0; i < kAux; ++i) mbar_init(&sm->aux_empty[i], kTmWarps);
         mbar_init(&sm->dS_full, 1);
-        mbar_init(&sm->S_read, kTmWarps);
         for (int i = 0; i < kIssuers; ++i) mbar_init(&sm->mma_done[i], 1);
         sm->abort_flag = 0;
         fence_mbarrier_init();
@@ -302,11 +302,12 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
             constexpr uint32_t kHi128 = desc_hi(1024, 2), kHi32 = desc_hi(256, 6);   // SBO and swizzle words
             // P = Q~ K~^T for chunk c
             auto issue_p = [&](int c) -> bool {
-                const int s = c % NST, pb = c % NP, pn = c / NP;
+                const int s = c % NST, pb = c % NP;
                 const uint32_t st = smem_u32(stage_ptr(s));
                 const uint32_t aQ = st + L::kOffQ, aK = st + L::kOffK;
                 if (!wait(cx, &sm->phi_done[s], (c / NST) & 1)) return false;
-                if (c >= NP && !wait(cx, &sm->P_empty[pb], (pn - 1) & 1)) return false;
+                // the P buffer of chunk c - 2 has been read (NP == 2)
+                if (c >= NP && !wait(cx, &sm->tm_read[c & 1], ((c >> 1) - 1) & 1)) return false;
                 tc_fence_after();
                 const uint32_t qlo = desc_lo(aQ, 16), klo = desc_lo(aK, 16), dP = tmem + L::kColP + pb * 64;
 #pragma unroll
@@ -331,7 +332,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
                 const uint32_t blo = desc_lo(st + L::kOffV, aOnes - (st + L::kOffV));
                 if (!GATED && !wait(cx, &sm->phi_done[s], (c / NST) & 1)) return false;
                 if (GATED && !wait(cx, &sm->sc_done[s], (c / NST) & 1)) return false;
-                if (!wait(cx, &sm->S_read, c & 1)) return false;
+                if (!wait(cx, &sm->tm_read[c & 1], (c >> 1) & 1)) return false;   // state read (and decayed)
                 tc_fence_after();
                 const uint32_t dS = tmem + L::kColS;
                 const uint32_t klo = desc_lo(aK, kTileQ / 2);   // K~^T: MN-major, two 64-feature blocks
@@ -353,12 +354,13 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
                 const uint32_t st = smem_u32(stage_ptr(s));
                 const uint32_t aQ = st + L::kOffQ, aV = st + L::kOffV;
                 const uint32_t aA = smem_u32(base + L::kOffA + bb * kTileA);
-                const int sb = c % L::kSpBufs, sn = c / L::kSpBufs;
+                const int sb = c % L::kSpBufs;
                 const uint32_t aSpZ = smem_u32(base + L::kOffSpZ + sb * kTileSpZ);
-                // [O | dn] = Q~ [Sprev | zhi zlo] (gated: Q~ rows already scaled by Gamma_i)
-                if (c >= 2 && !wait(cx, &sm->O_empty[bb], (n - 1) & 1)) break;
+                // [O | dn] = Q~ [Sprev | zhi zlo] (gated: Q~ rows already scaled by Gamma_i),
+                // then [O | dn] += A [V | 1].  ops_full of chunk c also means the
+                // TMEM warps have read O of chunk c-2 out of this buffer.
                 if (GATED && !wait(cx, &sm->sc_done[s], (c / NST) & 1)) break;
-                if (!wait(cx, &sm->Sp_full[sb], sn & 1)) break;
+                if (!wait(cx, &sm->ops_full[bb], n & 1)) break;
                 tc_fence_after();
                 const uint32_t dO = tmem + L::kColO + bb * 80;
                 const uint32_t qlo = desc_lo(aQ, 16), slo = desc_lo(aSpZ, kR * 32);
@@ -368,10 +370,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
                     if (kk == 0) tc_mma_bf16_w<false>(dO, qlo, kHi128, slo, kHi32, idQS);
                     else tc_mma_bf16_w<true>(dO, qlo + o, kHi128, slo + kk * (512 >> 4), kHi32, idQS);
                 }
-                tc_commit(&sm->Sp_empty[sb]);
-                // [O | dn] += A [V | 1]
-                if (!wait(cx, &sm->A_full[bb], n & 1)) break;
-                tc_fence_after();
+                if (L::kSpBufs == 1) tc_commit(&sm->Sp_empty);
                 const uint32_t alo = desc_lo(aA, 16);
                 const uint32_t vlo = desc_lo(aV, aOnes - aV);
 #pragma unroll
@@ -457,15 +456,14 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
                 tc_wait_st();
             }
             tc_fence_before();
-            if (has_b) warp_arrive(&sm->S_read);
-            if (has_p) warp_arrive(&sm->P_empty[pb]);
-            if (has_e) warp_arrive(&sm->O_empty[bb]);
+            if (has_b) warp_arrive(&sm->tm_read[bb]);
 
             // outputs of chunk c-2: columns 64 + 65 of [O | dn] hold Q~' . zprev in
             // two parts plus the row sums of A
             if (has_e) {
                 dn += __shfl_xor_sync(0xffffffffu, dn, 16);
-                const float inv = __frcp_rn(dn + args.eps);
+                float inv;   // approximate reciprocal: y is rounded to BF16 below
+                asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(inv) : "f"(dn + args.eps));
                 uint4 yp;
                 yp.x = pack_bf16x2(o[0] * inv, o[1] * inv);
                 yp.y = pack_bf16x2(o[2] * inv, o[3] * inv);
@@ -476,8 +474,9 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
                 const int t = tb + (c - 2) * kC + prow;
                 if (t < T) __stcs(reinterpret_cast<uint4 *>(args.y + ((size_t)bh * T + t) * args.dv + slice * kDVS + pcol), yp);
             }
-            // A = the causal mask (and, with a gate, the in-chunk decay) applied to P
-            if (has_p) {
+            // A = the causal mask (and, with a gate, the in-chunk decay) applied to P;
+            // without a gate a piece strictly below the diagonal is P itself
+            if (has_p && (GATED || qq == qd)) {
                 const int gq = c % kAux;
                 const float bi = GATED ? gr->gb[gq][prow] : 0.f;
                 const int zi = GATED ? gr->gz[gq][prow] : -1;
@@ -493,8 +492,11 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
 
             // shared-memory operands
             if (has_b) {
-                const int sb = c % L::kSpBufs, sn = c / L::kSpBufs;
-                if (c >= L::kSpBufs && !warp_wait(cx, &sm->Sp_empty[sb], (sn - 1) & 1)) break;
+                const int sb = c % L::kSpBufs;
+                // A_empty of chunk c-2 follows that chunk's QS too, so with two
+                // Sprev buffers it also frees this one; with one, chunk c-1's QS
+                // must be done
+                if (L::kSpBufs == 1 && c >= 1 && !warp_wait(cx, &sm->Sp_empty, (c - 1) & 1)) break;
                 if (c >= 2 && !warp_wait(cx, &sm->A_empty[bb], ((c >> 1) - 1) & 1)) break;
                 // Sprev columns 16 qq .. +15 of row srow: 16-column block qq
                 uint8_t *spz = base + L::kOffSpZ + sb * kTileSpZ + qq * (kR * 32);
@@ -517,10 +519,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
                 if (slice == 0 && qq == 0) args.z_out[(size_t)bh * kR + srow] = zr;
             }
             fence_proxy_async_smem();
-            if (has_b) {
-                warp_arrive(&sm->Sp_full[c % L::kSpBufs]);
-                warp_arrive(&sm->A_full[bb]);
-            }
+            if (has_b) warp_arrive(&sm->ops_full[bb]);
         }
     } else if (is_phi_warp(warp)) {
         // ------------------------------------------------------ phi warps
