@@ -100,12 +100,13 @@ struct Cfg {
     static constexpr int kStages = LA_STAGES;
     static constexpr int kSpBufs = GATED ? 1 : LA_SP_BUFS;     // [Sprev | z] tiles
     static constexpr int kNP = 2;                              // P accumulator buffers
+    static constexpr int kNO = 3;                              // [O | dn] accumulator buffers
     // TMEM columns: P (x2), the state [S | z] (80: z is column 64) and [O | dn]
-    // blocks of 80 (x2; dn is columns 64 and 65)
+    // blocks of 80 (x3; dn is columns 64 and 65)
     static constexpr uint32_t kColP = 0;
     static constexpr uint32_t kColS = kNP * 64;
     static constexpr uint32_t kColO = kColS + 80;
-    static constexpr uint32_t kCols = kColO + 2 * 80;
+    static constexpr uint32_t kCols = kColO + kNO * 80;
     static_assert(kCols <= 512, "TMEM budget");
     // shared memory (offsets from a 1024-aligned base)
     static constexpr uint32_t kOffQ = 0, kOffK = kTileQ, kOffV = 2 * kTileQ;
@@ -122,11 +123,11 @@ struct Cfg {
 
 struct alignas(16) Small {
     uint64_t full[4], empty[4], phi_done[4], sc_done[4];
-    // tm_read[c % 2]: the TMEM warps have read what chunk c's iteration reads
-    // (the state, P of chunk c, O of chunk c-2); ops_full[c % 2]: they have
-    // written Sprev and A of chunk c
+    // tm_read[c % 2]: the TMEM warps have read the state and P of chunk c's
+    // iteration; ops_full[c % 2]: they have written its Sprev and A; O_empty[c % 3]:
+    // they have read O of chunk c
     uint64_t P_full[2], dS_full, tm_read[2], ops_full[2], Sp_empty;
-    uint64_t A_empty[2], O_full[2], aux_empty[kAux];
+    uint64_t A_empty[2], O_full[3], O_empty[3], aux_empty[kAux];
     uint64_t mma_done[kIssuers];
     uint32_t tmem_base;
     int abort_flag;
@@ -184,7 +185,10 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
             mbar_init(&sm->tm_read[i], kTmWarps);
             mbar_init(&sm->ops_full[i], kTmWarps);
             mbar_init(&sm->A_empty[i], 1);
+        }
+        for (int i = 0; i < 3; ++i) {
             mbar_init(&sm->O_full[i], 1);
+            mbar_init(&sm->O_empty[i], kTmWarps);
         }
         mbar_init(&sm->Sp_empty, 1);
         for (int i = 0; i < kAux; ++i) mbar_init(&sm->aux_empty[i], kTmWarps);
@@ -357,12 +361,13 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
                 const int sb = c % L::kSpBufs;
                 const uint32_t aSpZ = smem_u32(base + L::kOffSpZ + sb * kTileSpZ);
                 // [O | dn] = Q~ [Sprev | zhi zlo] (gated: Q~ rows already scaled by Gamma_i),
-                // then [O | dn] += A [V | 1].  ops_full of chunk c also means the
-                // TMEM warps have read O of chunk c-2 out of this buffer.
+                // then [O | dn] += A [V | 1], into the buffer that held O of chunk c-3
+                const int ob = c % L::kNO;
                 if (GATED && !wait(cx, &sm->sc_done[s], (c / NST) & 1)) break;
                 if (!wait(cx, &sm->ops_full[bb], n & 1)) break;
+                if (c >= L::kNO && !wait(cx, &sm->O_empty[ob], ((c / L::kNO) - 1) & 1)) break;
                 tc_fence_after();
-                const uint32_t dO = tmem + L::kColO + bb * 80;
+                const uint32_t dO = tmem + L::kColO + ob * 80;
                 const uint32_t qlo = desc_lo(aQ, 16), slo = desc_lo(aSpZ, kR * 32);
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk) {
@@ -377,7 +382,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
                 for (int kk = 0; kk < 4; ++kk)
                     tc_mma_bf16_w<true>(dO, alo + kk * (32 >> 4), kHi128, vlo + kk * (2048 >> 4), kHi128, idAV);
                 tc_commit(&sm->A_empty[bb]);
-                tc_commit(&sm->O_full[bb]);
+                tc_commit(&sm->O_full[ob]);
                 tc_commit(&sm->empty[s]);
             }
             // Every MMA issued above completes before TMEM is released.
@@ -424,18 +429,13 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
             if (has_s && c >= 1 && !warp_wait(cx, &sm->dS_full, (c - 1) & 1)) break;
             if (has_b && GATED && !warp_wait(cx, &sm->phi_done[c % NST], (c / NST) & 1)) break;
             if (has_p && !warp_wait(cx, &sm->P_full[pb], pn & 1)) break;
-            if (has_e && !warp_wait(cx, &sm->O_full[bb], ((c - 2) >> 1) & 1)) break;
             tc_fence_after();
-            float S[16], zr = 0.f, p[8], o[8], dn = 0.f;
+            float S[16], zr = 0.f, p[8];
             if (has_s) {
                 tc_ld_32x32b_x16(tS, S);
                 if (qq == 0) tc_ld_32x32b_x1(tz, zr);
             }
             if (has_p) tc_ld_16x32bx2_x8<8>(tmem + lane_base + L::kColP + pb * 64 + qq * 16, p);
-            if (has_e) {
-                tc_ld_16x32bx2_x8<8>(tmem + lane_base + L::kColO + bb * 80 + qq * 16, o);
-                tc_ld_16x32bx2_x1<1>(tmem + lane_base + L::kColO + bb * 80 + 64, dn);
-            }
             tc_wait_ld();
             // Sprev of chunk c (BF16) and z split into two BF16 parts
             uint32_t spk[8];
@@ -458,22 +458,6 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
             tc_fence_before();
             if (has_b) warp_arrive(&sm->tm_read[bb]);
 
-            // outputs of chunk c-2: columns 64 + 65 of [O | dn] hold Q~' . zprev in
-            // two parts plus the row sums of A
-            if (has_e) {
-                dn += __shfl_xor_sync(0xffffffffu, dn, 16);
-                float inv;   // approximate reciprocal: y is rounded to BF16 below
-                asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(inv) : "f"(dn + args.eps));
-                uint4 yp;
-                yp.x = pack_bf16x2(o[0] * inv, o[1] * inv);
-                yp.y = pack_bf16x2(o[2] * inv, o[3] * inv);
-                yp.z = pack_bf16x2(o[4] * inv, o[5] * inv);
-                yp.w = pack_bf16x2(o[6] * inv, o[7] * inv);
-                // 8 columns (16 bytes) of token row prow, straight to global memory
-                // (streaming stores: y is not read again here)
-                const int t = tb + (c - 2) * kC + prow;
-                if (t < T) __stcs(reinterpret_cast<uint4 *>(args.y + ((size_t)bh * T + t) * args.dv + slice * kDVS + pcol), yp);
-            }
             // A = the causal mask (and, with a gate, the in-chunk decay) applied to P;
             // without a gate a piece strictly below the diagonal is P itself
             if (has_p && (GATED || qq == qd)) {
@@ -490,7 +474,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
             }
             if (GATED && has_b) warp_arrive(&sm->aux_empty[c % kAux]);   // gate data of chunk c is done
 
-            // shared-memory operands
+            // shared-memory operands (ahead of the outputs: the O issuer waits for them)
             if (has_b) {
                 const int sb = c % L::kSpBufs;
                 // A_empty of chunk c-2 follows that chunk's QS too, so with two
@@ -510,6 +494,8 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
                     *reinterpret_cast<uint4 *>(base + L::kOffA + bb * kTileA + sw128_offset(prow, pcol >> 3)) =
                         make_uint4(pack_bf16x2(p[0], p[1]), pack_bf16x2(p[2], p[3]), pack_bf16x2(p[4], p[5]),
                                    pack_bf16x2(p[6], p[7]));
+                fence_proxy_async_smem();
+                warp_arrive(&sm->ops_full[bb]);
             } else if (has_s && last_seg) {
                 // c == nch: the state after the last chunk
                 float *dst = args.S_out + ((size_t)bh * kR + srow) * args.dv + slice * kDVS + qq * 16;
@@ -518,8 +504,32 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
                     *reinterpret_cast<float4 *>(dst + j) = make_float4(S[j], S[j + 1], S[j + 2], S[j + 3]);
                 if (slice == 0 && qq == 0) args.z_out[(size_t)bh * kR + srow] = zr;
             }
-            fence_proxy_async_smem();
-            if (has_b) warp_arrive(&sm->ops_full[bb]);
+
+            // outputs of chunk c-2: columns 64 + 65 of [O | dn] hold Q~' . zprev in
+            // two parts plus the row sums of A
+            if (has_e) {
+                const int ob = (c - 2) % L::kNO;
+                if (!warp_wait(cx, &sm->O_full[ob], ((c - 2) / L::kNO) & 1)) break;
+                tc_fence_after();
+                float o[8], dn;
+                tc_ld_16x32bx2_x8<8>(tmem + lane_base + L::kColO + ob * 80 + qq * 16, o);
+                tc_ld_16x32bx2_x1<1>(tmem + lane_base + L::kColO + ob * 80 + 64, dn);
+                tc_wait_ld();
+                tc_fence_before();
+                warp_arrive(&sm->O_empty[ob]);
+                dn += __shfl_xor_sync(0xffffffffu, dn, 16);
+                float inv;   // approximate reciprocal: y is rounded to BF16 below
+                asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(inv) : "f"(dn + args.eps));
+                uint4 yp;
+                yp.x = pack_bf16x2(o[0] * inv, o[1] * inv);
+                yp.y = pack_bf16x2(o[2] * inv, o[3] * inv);
+                yp.z = pack_bf16x2(o[4] * inv, o[5] * inv);
+                yp.w = pack_bf16x2(o[6] * inv, o[7] * inv);
+                // 8 columns (16 bytes) of token row prow, straight to global memory
+                // (streaming stores: y is not read again here)
+                const int t = tb + (c - 2) * kC + prow;
+                if (t < T) __stcs(reinterpret_cast<uint4 *>(args.y + ((size_t)bh * T + t) * args.dv + slice * kDVS + pcol), yp);
+            }
         }
     } else if (is_phi_warp(warp)) {
         // ------------------------------------------------------ phi warps
