@@ -123,21 +123,14 @@ __device__ __forceinline__ uint4 phi8(uint4 raw)
     return make_uint4(phi_bf16x2(raw.x), phi_bf16x2(raw.y), phi_bf16x2(raw.z), phi_bf16x2(raw.w));
 }
 
-// Multiplies the 8 BF16 values of one 16-byte chunk by s: s is split into two
-// BF16 parts (s = hi + lo to about 2^-16), so each product is rounded once.
+// Multiplies the 8 BF16 values of one 16-byte chunk by s, rounded to BF16: one
+// packed multiply per pair (the product is rounded to BF16 again).
 __device__ __forceinline__ uint4 scale8(uint4 raw, float s)
 {
-    const uint32_t hi = pack_bf16x2(s, s);
-    const float lo_f = s - bf16_lo(hi);
-    const uint32_t lo = pack_bf16x2(lo_f, lo_f);
-    constexpr uint32_t kZero = 0x80008000u;
+    const uint32_t s2 = pack_bf16x2(s, s);
     uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-        uint32_t t;
-        asm("fma.rn.bf16x2 %0, %1, %2, %3;" : "=r"(t) : "r"(w[e]), "r"(lo), "r"(kZero));
-        asm("fma.rn.bf16x2 %0, %1, %2, %3;" : "=r"(w[e]) : "r"(w[e]), "r"(hi), "r"(t));
-    }
+    for (int e = 0; e < 4; ++e) asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(w[e]) : "r"(w[e]), "r"(s2));
     return make_uint4(w[0], w[1], w[2], w[3]);
 }
 
