@@ -125,6 +125,35 @@ la_status la_prefill_chunked(const void *q, const void *k, const void *v, la_dty
                              void *workspace, size_t workspace_bytes, la_stream_t stream);
 
 /*
+ * la_prefill_varlen -- la_prefill_chunked for a batch of sequences of different
+ * lengths packed one after another, e.g. the prompts of a serving batch, each
+ * prefilled in large blocks and continuing from its own state ([LA]
+ * "训练时，状态更新也能按块并行": token-by-token steps suit decode, prefill is
+ * organised in chunks that hand the state on).  Sequence b is tokens cu_seqlens[b] ..
+ * cu_seqlens[b+1]-1; it starts from S0[b], z0[b] and leaves its final state in
+ * S_out[b], z_out[b] (an empty sequence copies S0, z0).
+ *
+ *   q, k       device BF16 [total_T, H, r]   (token-major: row t*H + h)
+ *   v, y       device BF16 [total_T, H, dv]
+ *   alpha      device FP32 [total_T, H] or NULL (alpha == 1)
+ *   S0, z0     device FP32 [B, H, r, dv], [B, H, r] or NULL (zero); may alias S_out, z_out
+ *   S_out, z_out  device FP32 [B, H, r, dv], [B, H, r]
+ *   cu_seqlens device int32 [B + 1]: 0 = cu_seqlens[0] <= ... <= cu_seqlens[B] = total_T.
+ *              The host cannot read it; a kernel finding a sequence outside
+ *              [0, total_T] or of negative length skips it and records LA_ERR_SHAPE
+ *              (read it with la_last_device_status).
+ * Requires BF16, r == 128, dv in {64, 128}, chunk == 64; q, k, v, y, S_out 16-byte
+ * aligned.  total_T may be 0.  The sequences are not split into segments (no
+ * workspace).  Rows of y outside every sequence are not written.
+ * Errors: LA_ERR_NULL, LA_ERR_SHAPE, LA_ERR_DTYPE, LA_ERR_ALIGN, LA_ERR_UNSUPPORTED
+ *         (FP32 or other sizes), LA_ERR_CUDA.
+ */
+la_status la_prefill_varlen(const void *q, const void *k, const void *v, la_dtype dtype,
+                            const float *alpha, const float *S0, const float *z0, const int *cu_seqlens,
+                            int B, int H, int total_T, int r, int dv, int chunk, float eps,
+                            void *y, float *S_out, float *z_out, la_stream_t stream);
+
+/*
  * la_prefill_chunked_noalloc -- la_prefill_chunked without caller scratch: the
  * workspace is a 16 MiB buffer compiled into the library (a static device array),
  * one per device for the whole process.  The pages have no counterpart; it is an

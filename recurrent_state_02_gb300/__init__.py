@@ -93,6 +93,43 @@ def prefill_chunked(q, k, v, alpha=None, S0=None, z0=None, chunk=64, eps=1e-6, y
     return y, S_out, z_out
 
 
+def prefill_varlen(q, k, v, cu_seqlens, alpha=None, S0=None, z0=None, chunk=64, eps=1e-6, y=None, S_out=None,
+                   z_out=None):
+    """Packed sequences of different lengths: q, k [total_T, H, r], v [total_T, H, dv]
+    (bf16, token-major); cu_seqlens int32 [B+1] on the device (sequence b is tokens
+    cu_seqlens[b] .. cu_seqlens[b+1]-1); alpha [total_T, H] fp32 or None; S0
+    [B,H,r,dv], z0 [B,H,r] fp32 or None.  Returns (y [total_T, H, dv], S_T, z_T)."""
+    if q.dtype not in _DTYPES:
+        raise ValueError(f"unsupported dtype {q.dtype}")
+    total_T, H, r = q.shape
+    dv = v.shape[2]
+    dev = q.device
+    if cu_seqlens.dtype != torch.int32 or cu_seqlens.dim() != 1 or cu_seqlens.device != dev:
+        raise ValueError("cu_seqlens must be a 1-D int32 tensor on the device of q")
+    B = cu_seqlens.numel() - 1
+    _require(q, "q", (total_T, H, r), q.dtype, dev)
+    _require(k, "k", (total_T, H, r), q.dtype, dev)
+    _require(v, "v", (total_T, H, dv), q.dtype, dev)
+    _require(cu_seqlens, "cu_seqlens", (B + 1,), torch.int32, dev)
+    _require(alpha, "alpha", (total_T, H), torch.float32, dev)
+    _require(S0, "S0", (B, H, r, dv), torch.float32, dev)
+    _require(z0, "z0", (B, H, r), torch.float32, dev)
+    if y is None:
+        y = torch.empty((total_T, H, dv), device=dev, dtype=q.dtype)
+    if S_out is None:
+        S_out = torch.empty((B, H, r, dv), device=dev, dtype=torch.float32)
+    if z_out is None:
+        z_out = torch.empty((B, H, r), device=dev, dtype=torch.float32)
+    _require(y, "y", (total_T, H, dv), q.dtype, dev)
+    _require(S_out, "S_out", (B, H, r, dv), torch.float32, dev)
+    _require(z_out, "z_out", (B, H, r), torch.float32, dev)
+    st = _native.lib().la_prefill_varlen(
+        _ptr(q), _ptr(k), _ptr(v), _DTYPES[q.dtype], _ptr(alpha), _ptr(S0), _ptr(z0), _ptr(cu_seqlens), B, H,
+        total_T, r, dv, chunk, float(eps), _ptr(y), _ptr(S_out), _ptr(z_out), _stream(dev))
+    _native.check(st, "la_prefill_varlen")
+    return y, S_out, z_out
+
+
 def prefill_chunked_noalloc(q, k, v, y, S_out, z_out, alpha=None, S0=None, z0=None, chunk=64, eps=1e-6):
     """As prefill_chunked, with the library's built-in scratch instead of a
     workspace; nothing is allocated here either, so y [B,H,T,dv] (input dtype),

@@ -124,6 +124,23 @@ bool make_map_bf16(CUtensorMap *map, const void *ptr, long long planes, long lon
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Token-major packed view [tokens, heads, cols] (cols innermost): boxes of
+// box_cols x 1 head x box_rows tokens, so a box lands in shared memory exactly
+// like a box_rows x box_cols tile of the [planes, rows, cols] view.
+bool make_map_bf16_tok(CUtensorMap *map, const void *ptr, long long tokens, long long heads, long long cols,
+                       unsigned box_cols, unsigned box_rows, CUtensorMapSwizzle swizzle)
+{
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    const cuuint64_t dims[3] = {(cuuint64_t)cols, (cuuint64_t)heads, (cuuint64_t)(tokens > 0 ? tokens : 1)};
+    const cuuint64_t strides[2] = {(cuuint64_t)cols * 2, (cuuint64_t)cols * heads * 2};
+    const cuuint32_t box[3] = {box_cols, 1, box_rows};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(ptr), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 int *status_word()
 {
     void *p = nullptr;
@@ -232,6 +249,7 @@ la_status la_prefill_chunked(const void *q, const void *k, const void *v, la_dty
     a.nseg = 1;
     a.seg_chunks = 0;
     a.S_start = nullptr;
+    a.cu_seqlens = nullptr;
     if (need) {
         // state pass over the first nseg - 1 segments, scan, then every segment in parallel
         const size_t BH = (size_t)B * H, state = 128 * (size_t)dv + 128;
@@ -261,6 +279,55 @@ la_status la_prefill_chunked(const void *q, const void *k, const void *v, la_dty
         a.S_start = S_start;
     }
     return from_cuda(la::launch_prefill_tc(mq, mk, mv, a, B, alpha != nullptr, st));
+}
+
+la_status la_prefill_varlen(const void *q, const void *k, const void *v, la_dtype dtype, const float *alpha,
+                            const float *S0, const float *z0, const int *cu_seqlens, int B, int H, int total_T,
+                            int r, int dv, int chunk, float eps, void *y, float *S_out, float *z_out,
+                            la_stream_t stream)
+{
+    if (!cu_seqlens || !S_out || !z_out) return LA_ERR_NULL;
+    if (total_T > 0 && (!q || !k || !v || !y)) return LA_ERR_NULL;
+    if (B < 1 || H < 1 || total_T < 0 || r < 1 || dv < 1 || chunk < 1) return LA_ERR_SHAPE;
+    if (dtype != LA_DTYPE_BF16 && dtype != LA_DTYPE_FP32) return LA_ERR_DTYPE;
+    if (dtype != LA_DTYPE_BF16 || r != 128 || (dv != 64 && dv != 128) || chunk != 64) return LA_ERR_UNSUPPORTED;
+    if ((long long)B * H > 0x7fffffffLL || (long long)total_T * H > 0x7fffffffLL) return LA_ERR_SHAPE;
+    {
+        const void *ptrs16[] = {q, k, v, y, S_out};
+        for (const void *p : ptrs16)
+            if (p && !aligned(p, 16)) return LA_ERR_ALIGN;
+        const void *ptrs4[] = {alpha, S0, z0, z_out, cu_seqlens};
+        for (const void *p : ptrs4)
+            if (p && !aligned(p, 4)) return LA_ERR_ALIGN;
+    }
+    int *status = status_word();
+    if (!status) return LA_ERR_CUDA;
+    // token-major views [total_T, H, d]; with no tokens at all no tile is ever
+    // loaded, and any aligned address serves as the maps' base
+    const void *qb = total_T ? q : S_out, *kb = total_T ? k : S_out, *vb = total_T ? v : S_out;
+    CUtensorMap mq, mk, mv;
+    const CUtensorMapSwizzle sw128 = CU_TENSOR_MAP_SWIZZLE_128B;
+    if (!make_map_bf16_tok(&mq, qb, total_T, H, r, 64, 64, sw128) || !make_map_bf16_tok(&mk, kb, total_T, H, r, 64, 64, sw128) ||
+        !make_map_bf16_tok(&mv, vb, total_T, H, dv, 64, 64, sw128))
+        return LA_ERR_CUDA;
+    la::PrefillTcArgs a;
+    a.alpha = alpha;
+    a.S0 = S0;
+    a.z0 = z0;
+    a.S_out = S_out;
+    a.z_out = z_out;
+    a.y = static_cast<uint16_t *>(y);
+    a.H = H;
+    a.T = total_T;
+    a.dv = dv;
+    a.eps = eps;
+    a.status = status;
+    a.wait_limit_ns = la::kWaitLimitNs;
+    a.nseg = 1;
+    a.seg_chunks = 0;
+    a.S_start = nullptr;
+    a.cu_seqlens = cu_seqlens;
+    return from_cuda(la::launch_prefill_tc(mq, mk, mv, a, B, alpha != nullptr, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 la_status la_prefill_chunked_noalloc(const void *q, const void *k, const void *v, la_dtype dtype,

@@ -8,6 +8,7 @@
 namespace la {
 
 // Device status word values (same numbering as la_status).
+constexpr int kStatusShape = 2;
 constexpr int kStatusTimeout = 7;
 
 // Default limit for every on-chip barrier wait inside a kernel.
@@ -24,6 +25,10 @@ struct PrefillTcArgs {
     int nseg;             // sequence segments per head (1: the whole sequence in one CTA)
     int seg_chunks;       // chunks per segment (nseg > 1)
     const float *S_start; // nseg > 1: [nseg][B*H][128*dv + 128] start state of each segment (S then z)
+    // Packed sequences of different lengths: sequence b is tokens cu_seqlens[b] ..
+    // cu_seqlens[b+1]-1 of q, k [T, H, 128], v, y [T, H, dv], alpha [T, H] (T the
+    // total); the tensor maps are token-major views.  nullptr: [B, H, T, d] layout.
+    const int *cu_seqlens;
     float eps;
     int *status;          // device status word
     unsigned long long wait_limit_ns;

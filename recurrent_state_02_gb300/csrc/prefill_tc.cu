@@ -157,7 +157,27 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
     // split the sequence (then every segment starts from a scanned state)
     const int h = blockIdx.y, b = blockIdx.z / args.nseg, seg = blockIdx.z % args.nseg;
     const int bh = b * args.H + h;
-    const int T = args.T;
+    // Packed sequences of different lengths (cu_seqlens; no segments) or the
+    // [B, H, T, d] layout.  A sequence whose bounds are inconsistent with the
+    // total is recorded as a shape error and processes no tokens.
+    const bool varlen = args.cu_seqlens != nullptr;
+    int seq0 = 0, T = args.T;
+    if (varlen) {
+        seq0 = args.cu_seqlens[b];
+        const int seq1 = args.cu_seqlens[b + 1];
+        if (seq0 < 0 || seq1 < seq0 || seq1 > args.T) {
+            if (threadIdx.x == 0) atomicExch(args.status, kStatusShape);
+            seq0 = 0;
+            T = 0;
+        } else {
+            T = seq1 - seq0;
+        }
+    }
+    // row of token t (of this sequence) in q, k, v, y (rows of d values) and alpha
+    auto tok_row = [&](int t) -> size_t { return varlen ? (size_t)(seq0 + t) * args.H + h : (size_t)bh * T + t; };
+    // the last two TMA coordinates of a box starting at token t0
+    auto tma_c1 = [&](int t0) { return varlen ? h : t0; };
+    auto tma_c2 = [&](int t0) { return varlen ? seq0 + t0 : bh; };
     const int nch_all = (T + kC - 1) / kC;
     const int c0 = seg * args.seg_chunks;                                     // first chunk of the segment
     const int nch = args.nseg > 1 ? min(args.seg_chunks, nch_all - c0) : nch_all;   // its chunk count
@@ -247,9 +267,8 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
             const int t0 = tb + c * kC;
             float a0 = 1.f, a1 = 1.f;
             if (GATED) {
-                const float *ap = args.alpha + (size_t)bh * T;
-                if (t0 + 2 * lane < T) a0 = ap[t0 + 2 * lane];
-                if (t0 + 2 * lane + 1 < T) a1 = ap[t0 + 2 * lane + 1];
+                if (t0 + 2 * lane < T) a0 = args.alpha[tok_row(t0 + 2 * lane)];
+                if (t0 + 2 * lane + 1 < T) a1 = args.alpha[tok_row(t0 + 2 * lane + 1)];
             }
             if (c >= NST && !warp_wait(cx, &sm->empty[s], ((c / NST) - 1) & 1)) break;
             if (GATED && c >= kAux && !warp_wait(cx, &sm->aux_empty[c % kAux], ((c / kAux) - 1) & 1)) break;
@@ -257,22 +276,23 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
             uint8_t *st = stage_ptr(s);
             if (lane == 0) {
                 mbar_arrive_expect_tx(&sm->full[s], 2 * kTileQ + kTileV);
-                tma_load_3d(st + L::kOffQ, &map_q, &sm->full[s], 0, t0, bh);
-                tma_load_3d(st + L::kOffQ + kTileQ / 2, &map_q, &sm->full[s], 64, t0, bh);
-                tma_load_3d(st + L::kOffK, &map_k, &sm->full[s], 0, t0, bh);
-                tma_load_3d(st + L::kOffK + kTileQ / 2, &map_k, &sm->full[s], 64, t0, bh);
-                tma_load_3d(st + L::kOffV, &map_v, &sm->full[s], slice * kDVS, t0, bh);
+                const int cy = tma_c1(t0), cz = tma_c2(t0);
+                tma_load_3d(st + L::kOffQ, &map_q, &sm->full[s], 0, cy, cz);
+                tma_load_3d(st + L::kOffQ + kTileQ / 2, &map_q, &sm->full[s], 64, cy, cz);
+                tma_load_3d(st + L::kOffK, &map_k, &sm->full[s], 0, cy, cz);
+                tma_load_3d(st + L::kOffK + kTileQ / 2, &map_k, &sm->full[s], 64, cy, cz);
+                tma_load_3d(st + L::kOffV, &map_v, &sm->full[s], slice * kDVS, cy, cz);
                 // The load of chunk c + NST waits for this stage to come free, which
                 // takes about as long as a load from HBM: warm L2 for it now.
                 if (c + NST < nch) {
-                    const int tp = t0 + NST * kC;
+                    const int tp = t0 + NST * kC, yp = tma_c1(tp), zp = tma_c2(tp);
                     if (slice == 0) {   // the other slices of the head read the same q, k
-                        tma_prefetch_l2_3d(&map_q, 0, tp, bh);
-                        tma_prefetch_l2_3d(&map_q, 64, tp, bh);
-                        tma_prefetch_l2_3d(&map_k, 0, tp, bh);
-                        tma_prefetch_l2_3d(&map_k, 64, tp, bh);
+                        tma_prefetch_l2_3d(&map_q, 0, yp, zp);
+                        tma_prefetch_l2_3d(&map_q, 64, yp, zp);
+                        tma_prefetch_l2_3d(&map_k, 0, yp, zp);
+                        tma_prefetch_l2_3d(&map_k, 64, yp, zp);
                     }
-                    tma_prefetch_l2_3d(&map_v, slice * kDVS, tp, bh);
+                    tma_prefetch_l2_3d(&map_v, slice * kDVS, yp, zp);
                 }
             }
             if (GATED) {
@@ -528,7 +548,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
                 // 8 columns (16 bytes) of token row prow, straight to global memory
                 // (streaming stores: y is not read again here)
                 const int t = tb + (c - 2) * kC + prow;
-                if (t < T) __stcs(reinterpret_cast<uint4 *>(args.y + ((size_t)bh * T + t) * args.dv + slice * kDVS + pcol), yp);
+                if (t < T) __stcs(reinterpret_cast<uint4 *>(args.y + tok_row(t) * args.dv + slice * kDVS + pcol), yp);
             }
         }
     } else if (is_phi_warp(warp)) {

@@ -119,3 +119,25 @@ def test_workloads_follow_the_recipe():
     t = W.prefill_inputs(W.TINY)
     assert t["q"].dtype == torch.float32 and t["q"].shape == (1, 1, 64, 16)
     assert W.LONG.scale == 2.0 and W.UNGATED.chunk == 64
+
+
+def _varlen(native, **kw):
+    a = dict(q=FAKE, k=FAKE, v=FAKE, dtype=native.LA_DTYPE_BF16, alpha=None, S0=None, z0=None, cu=FAKE, B=2, H=1,
+             T=100, r=128, dv=128, chunk=64, eps=1e-6, y=FAKE, S_out=FAKE, z_out=FAKE, stream=None)
+    a.update(kw)
+    return native.lib().la_prefill_varlen(a["q"], a["k"], a["v"], a["dtype"], a["alpha"], a["S0"], a["z0"], a["cu"],
+                                          a["B"], a["H"], a["T"], a["r"], a["dv"], a["chunk"], a["eps"], a["y"],
+                                          a["S_out"], a["z_out"], a["stream"])
+
+
+def test_varlen_rejects_bad_arguments(native):
+    assert _varlen(native, cu=None) == native.LA_ERR_NULL
+    assert _varlen(native, q=None) == native.LA_ERR_NULL
+    assert _varlen(native, S_out=None) == native.LA_ERR_NULL
+    assert _varlen(native, B=0) == native.LA_ERR_SHAPE
+    assert _varlen(native, T=-1) == native.LA_ERR_SHAPE
+    assert _varlen(native, dtype=9) == native.LA_ERR_DTYPE
+    assert _varlen(native, dtype=native.LA_DTYPE_FP32) == native.LA_ERR_UNSUPPORTED
+    assert _varlen(native, dv=96) == native.LA_ERR_UNSUPPORTED
+    assert _varlen(native, q=FAKE + 8) == native.LA_ERR_ALIGN
+    assert _varlen(native, cu=FAKE + 2) == native.LA_ERR_ALIGN

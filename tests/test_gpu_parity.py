@@ -258,3 +258,67 @@ def test_prefill_workspace_errors(la):
     assert call(P(ws), need) == 0
     torch.cuda.synchronize()
     assert la.last_device_status() == 0
+
+
+# ------------------------------------------------------- packed sequences
+# Sequences of different lengths packed one after another (token-major
+# [total, H, d]), each from its own state: every sequence must equal the oracle
+# run over that sequence alone.
+
+VARLEN_LENS = [0, 1, 63, 64, 65, 300, 17]
+
+
+def _varlen_inputs(gated, seed):
+    from recurrent_state_02_gb300 import workloads as W
+    lens = VARLEN_LENS
+    cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    H = 2
+    base = W.prefill_inputs(W.Workload("varlen", B=1, H=H, T=int(cu[-1]), dtype=torch.bfloat16, gated=gated,
+                                       seed=seed))
+    g = torch.Generator().manual_seed(seed + 1)
+    B = len(lens)
+    S0 = (torch.randn(B, H, 128, 128, generator=g) * 0.1).float()
+    z0 = (torch.rand(B, H, 128, generator=g) * 10 + 1).float()
+    return base, cu, S0, z0
+
+
+@pytest.mark.parametrize("gated", [False, True])
+def test_prefill_varlen(la, oracle_mod, gated):
+    base, cu, S0, z0 = _varlen_inputs(gated, 61)
+    pack = lambda x: x[0].permute(1, 0, 2).contiguous().cuda()          # [1,H,T,d] -> [T,H,d]
+    alpha = base["alpha"][0].permute(1, 0).contiguous().cuda() if gated else None
+    y, S, z = la.prefill_varlen(pack(base["q"]), pack(base["k"]), pack(base["v"]), torch.from_numpy(cu).cuda(),
+                                alpha=alpha, S0=S0.cuda(), z0=z0.cuda())
+    assert la.last_device_status() == 0
+    y, S, z = y.float().cpu(), S.cpu(), z.cpu()
+    for b in range(len(VARLEN_LENS)):
+        lo, hi = int(cu[b]), int(cu[b + 1])
+        if hi == lo:   # an empty sequence hands its state on unchanged
+            assert torch.equal(S[b], S0[b]) and torch.equal(z[b], z0[b])
+            continue
+        sl = lambda x: x[:, :, lo:hi].contiguous()
+        ref = oracle_mod.scan(to_oracle(sl(base["q"])), to_oracle(sl(base["k"])), to_oracle(sl(base["v"])),
+                              alpha=to_oracle(base["alpha"][:, :, lo:hi].contiguous()) if gated else None,
+                              S0=to_oracle(S0[b:b + 1]), z0=to_oracle(z0[b:b + 1]), eps=1e-6)
+        got = (y[lo:hi].permute(1, 0, 2)[None].numpy(), S[b:b + 1].numpy(), z[b:b + 1].numpy())
+        _check(got, ref, 2e-2, f"varlen seq {b} (T={hi - lo})")
+
+
+def test_prefill_varlen_bad_lengths(la, oracle_mod):
+    """Offsets that run backwards are refused on the device: that sequence is
+    skipped, the error is recorded, and the other sequences are still exact."""
+    base, cu, S0, z0 = _varlen_inputs(False, 62)
+    bad = cu.copy()
+    bad[3] = bad[2] - 1   # sequence 2 would have negative length
+    pack = lambda x: x[0].permute(1, 0, 2).contiguous().cuda()
+    y, S, z = la.prefill_varlen(pack(base["q"]), pack(base["k"]), pack(base["v"]), torch.from_numpy(bad).cuda(),
+                                S0=S0.cuda(), z0=z0.cuda())
+    from recurrent_state_02_gb300 import _native
+    assert la.last_device_status() == _native.LA_ERR_SHAPE
+    assert la.last_device_status() == 0
+    lo, hi = int(bad[5]), int(bad[6])   # a well-formed sequence
+    sl = lambda x: x[:, :, lo:hi].contiguous()
+    ref = oracle_mod.scan(to_oracle(sl(base["q"])), to_oracle(sl(base["k"])), to_oracle(sl(base["v"])),
+                          S0=to_oracle(S0[5:6]), z0=to_oracle(z0[5:6]), eps=1e-6)
+    got = (y.float().cpu()[lo:hi].permute(1, 0, 2)[None].numpy(), S.cpu()[5:6].numpy(), z.cpu()[5:6].numpy())
+    _check(got, ref, 2e-2, "varlen next to a bad sequence")
