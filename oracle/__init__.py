@@ -1,4 +1,5 @@
-"""FP64 CPU oracle for normalised causal linear attention (test infrastructure).
+"""FP64 CPU oracle for normalised causal linear attention and the delta-rule
+memory (test infrastructure).
 
 Only the tests, the smoke check and the benchmark's CPU-baseline leg import this
 package.  The product library never links, loads or calls it, and this package
@@ -10,6 +11,7 @@ from .oracle import (  # noqa: F401
     PHI_RELU1,
     build,
     chunkwise,
+    delta,
     dense,
     num_cpus,
     scan,

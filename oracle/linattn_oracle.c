@@ -26,6 +26,9 @@
  *                 version (read: every term is multiplied by the product of the gates
  *                 that act on it between its write and its read; see or_chunkwise).
  *
+ * A fourth routine, or_delta, is the delta-rule memory of [LA] "Delta rule：先读旧答案，
+ * 再写误差" (a different update rule, without the normaliser; see its comment).
+ *
  * Feature maps: ELU(x)+1 ([LA] "关键改写：让求和先发生"; [LE] feature_map), relu(x)+1
  * ([LC] reference answer of TODO 1) and the identity (so that the pages' worked
  * examples, which give feature values directly, can be replayed).
@@ -352,5 +355,94 @@ int or_chunkwise(int B, int H, int T, int r, int dv, const void *q, const void *
         }
     }
     free(Qc); free(Kc); free(Vc); free(P); free(D); free(G); free(Sn); free(zn);
+    return 0;
+}
+
+/* ------------------------------------------------------------ delta rule -- */
+
+/*
+ * The delta rule ([LA] "Delta rule：先读旧答案，再写误差"): a fast-weight memory
+ * without the normaliser.  For each token, first read the memory's current answer
+ * for the key, then write back only the error, scaled by beta:
+ *     p_t = S_{t-1}^T k_t,   e_t = v_t - p_t,   S_t = S_{t-1} + beta_t k_t e_t^T,
+ * and the output reads the updated memory with the query, y_t = S_t^T q_t (read
+ * after write, as for the accumulators).  q and k are used as given (the pages'
+ * examples give them directly; [LA] "key 的范数决定了纠错力度" discusses their norm).
+ *   q, k [B,H,T,r]; v [B,H,T,dv] (in_type); beta [B,H,T] (NULL: 1); S0 [B,H,r,dv]
+ *   (NULL: zero); y [B,H,T,dv]; S [B,H,r,dv].
+ */
+typedef struct {
+    int B, H, T, r, dv, in_type;
+    const void *q, *k, *v;
+    const double *beta, *S0;
+    double *y, *S;
+    size_t next;
+    pthread_mutex_t lock;
+} delta_problem;
+
+static void delta_one(const delta_problem *p, size_t bh, double *kt, double *pe)
+{
+    const int T = p->T, r = p->r, dv = p->dv;
+    double *S = p->S + bh * (size_t)r * dv;
+    if (p->S0) memcpy(S, p->S0 + bh * (size_t)r * dv, sizeof(double) * (size_t)r * dv);
+    else memset(S, 0, sizeof(double) * (size_t)r * dv);
+    for (int t = 0; t < T; ++t) {
+        const size_t row_qk = (bh * (size_t)T + (size_t)t) * (size_t)r;
+        const size_t row_v = (bh * (size_t)T + (size_t)t) * (size_t)dv;
+        const double beta = p->beta ? p->beta[bh * (size_t)T + (size_t)t] : 1.0;
+        for (int i = 0; i < r; ++i) kt[i] = decode(p->k, p->in_type, row_qk + i);
+        /* the memory's answer for k_t, then the error against v_t */
+        for (int j = 0; j < dv; ++j) pe[j] = 0.0;
+        for (int i = 0; i < r; ++i)
+            for (int j = 0; j < dv; ++j) pe[j] += S[(size_t)i * dv + j] * kt[i];
+        for (int j = 0; j < dv; ++j) pe[j] = decode(p->v, p->in_type, row_v + j) - pe[j];
+        /* write back beta * k_t e_t^T */
+        for (int i = 0; i < r; ++i)
+            for (int j = 0; j < dv; ++j) S[(size_t)i * dv + j] += beta * kt[i] * pe[j];
+        /* y_t = S_t^T q_t */
+        for (int j = 0; j < dv; ++j) {
+            double acc = 0.0;
+            for (int i = 0; i < r; ++i) acc += S[(size_t)i * dv + j] * decode(p->q, p->in_type, row_qk + i);
+            p->y[row_v + j] = acc;
+        }
+    }
+}
+
+static void *delta_worker(void *arg)
+{
+    delta_problem *p = (delta_problem *)arg;
+    double *buf = (double *)malloc(sizeof(double) * ((size_t)p->r + (size_t)p->dv));
+    if (!buf) return NULL;
+    const size_t nbh = (size_t)p->B * (size_t)p->H;
+    for (;;) {
+        pthread_mutex_lock(&p->lock);
+        size_t bh = p->next++;
+        pthread_mutex_unlock(&p->lock);
+        if (bh >= nbh) break;
+        delta_one(p, bh, buf, buf + p->r);
+    }
+    free(buf);
+    return NULL;
+}
+
+int or_delta(int B, int H, int T, int r, int dv, const void *q, const void *k, const void *v, int in_type,
+             const double *beta, const double *S0, int nthreads, double *y, double *S)
+{
+    if (B < 1 || H < 1 || T < 1 || r < 1 || dv < 1) return -1;
+    if (!q || !k || !v || !y || !S) return -1;
+    if (in_type < OR_F64 || in_type > OR_BF16) return -1;
+    delta_problem p = {B, H, T, r, dv, in_type, q, k, v, beta, S0, y, S, 0, PTHREAD_MUTEX_INITIALIZER};
+    const size_t nbh = (size_t)B * (size_t)H;
+    if (nthreads <= 0) nthreads = or_num_cpus();
+    if ((size_t)nthreads > nbh) nthreads = (int)nbh;
+    if (nthreads == 1) {
+        delta_worker(&p);
+    } else {
+        pthread_t *th = (pthread_t *)malloc(sizeof(pthread_t) * (size_t)nthreads);
+        if (!th) return -1;
+        for (int i = 0; i < nthreads; ++i) pthread_create(&th[i], NULL, delta_worker, &p);
+        for (int i = 0; i < nthreads; ++i) pthread_join(th[i], NULL);
+        free(th);
+    }
     return 0;
 }

@@ -47,7 +47,8 @@ def _bind(path: str):
     lib.or_scan.argtypes = common + [i, dp, dp, dp]
     lib.or_dense.argtypes = common + [dp, dp, dp]
     lib.or_chunkwise.argtypes = common + [i, dp, dp, dp]
-    for f in (lib.or_scan, lib.or_dense, lib.or_chunkwise):
+    lib.or_delta.argtypes = [i, i, i, i, i, vp, vp, vp, i, dp, dp, i, dp, dp]
+    for f in (lib.or_scan, lib.or_dense, lib.or_chunkwise, lib.or_delta):
         f.restype = ctypes.c_int
     lib.or_num_cpus.restype = ctypes.c_int
     return lib
@@ -141,6 +142,17 @@ def chunkwise(q, k, v, chunk, alpha=None, S0=None, z0=None, eps=1e-6, phi=PHI_EL
     return y, S, z
 
 
+def delta(q, k, v, beta=None, S0=None, threads=0, _lib=None):
+    """Delta-rule memory (LA "Delta rule：先读旧答案，再写误差"): returns (y, S_T) in float64."""
+    q, k, v, beta, S0, _, (B, H, T, r, dv) = _prepare(q, k, v, beta, S0, None)
+    y, S = np.empty((B, H, T, dv)), np.empty((B, H, r, dv))
+    rc = (_lib or _load()).or_delta(B, H, T, r, dv, _ptr(q), _ptr(k), _ptr(v), _in_type(q), _ptr(beta), _ptr(S0),
+                                    int(threads), _ptr(y), _ptr(S))
+    if rc:
+        raise ValueError("or_delta rejected its arguments")
+    return y, S
+
+
 class Variant:
     """The three routes bound to one compiled copy of the oracle."""
 
@@ -157,3 +169,6 @@ class Variant:
 
     def chunkwise(self, *a, **kw):
         return chunkwise(*a, _lib=self._lib, **kw)
+
+    def delta(self, *a, **kw):
+        return delta(*a, _lib=self._lib, **kw)
