@@ -191,6 +191,31 @@ la_status la_decode_step(const void *q, const void *k, const void *v, la_dtype d
                          float eps, void *y, la_stream_t stream);
 
 /*
+ * la_delta_rule -- the delta-rule memory ([LA] "Delta rule：先读旧答案，再写误差"): a
+ * state without the normaliser that, per token, reads its current answer for the
+ * key, writes back beta times the error, and is then read by the query:
+ *     p_t = S_{t-1}^T k_t,   S_t = S_{t-1} + beta_t k_t (v_t - p_t)^T,   y_t = S_t^T q_t
+ * q and k are used as given (no feature map); the read follows the write, as in
+ * the other entry points.  With a unit key and beta = 1 the memory returns v
+ * exactly for that key; the error left on k after a step is (1 - beta |k|^2)
+ * times the error before it, so the update contracts for 0 < beta |k|^2 < 2.
+ *   q, k   device [B,H,T,r] dtype          v, y  device [B,H,T,dv] dtype
+ *   beta   device FP32 [B,H,T] write strength, or NULL for beta == 1
+ *   S0     device FP32 [B,H,r,dv] or NULL (zero); may equal S_out (in place)
+ *   S_out  device FP32 [B,H,r,dv] final state
+ * Kernel: the token recurrence in FP32 on CUDA cores (the pages give no block
+ * algorithm for this rule, [LA] "训练时，状态更新也能按块并行"), the state in
+ * registers, the value columns split over CTAs.  Requires r in {32, 64, 128, 256},
+ * dv a multiple of 32, q, k, v, y 16-byte aligned, beta, S0, S_out 4-byte
+ * aligned.  T may be 0 (S_out = S0; q, k, v, y may then be NULL and are not touched).
+ * Errors: LA_ERR_NULL, LA_ERR_SHAPE (B, H, r, dv < 1, T < 0), LA_ERR_DTYPE,
+ *         LA_ERR_ALIGN, LA_ERR_UNSUPPORTED (other r or dv), LA_ERR_CUDA.
+ */
+la_status la_delta_rule(const void *q, const void *k, const void *v, la_dtype dtype, const float *beta,
+                        const float *S0, int B, int H, int T, int r, int dv, void *y, float *S_out,
+                        la_stream_t stream);
+
+/*
  * la_last_device_status -- synchronise `stream`, then read and clear the device
  * status word of the current device: LA_OK, or LA_ERR_TIMEOUT when a kernel
  * gave up waiting on an on-chip barrier since the last read.  Returns

@@ -182,6 +182,32 @@ def decode_step(q, k, v, S, z, alpha=None, eps=1e-6, y=None):
     return y
 
 
+def delta_rule(q, k, v, beta=None, S0=None, y=None, S_out=None):
+    """Delta-rule memory: p = S^T k, S += beta k (v - p)^T, y = S^T q (after the write).
+    q, k [B,H,T,r], v [B,H,T,dv] (bf16 or fp32, same dtype); beta [B,H,T] fp32 or
+    None (1); S0 [B,H,r,dv] fp32 or None (zero).  Returns (y [B,H,T,dv], S_T)."""
+    if q.dtype not in _DTYPES:
+        raise ValueError(f"unsupported dtype {q.dtype}")
+    B, H, T, r = q.shape
+    dv = v.shape[3]
+    dev = q.device
+    _require(q, "q", (B, H, T, r), q.dtype, dev)
+    _require(k, "k", (B, H, T, r), q.dtype, dev)
+    _require(v, "v", (B, H, T, dv), q.dtype, dev)
+    _require(beta, "beta", (B, H, T), torch.float32, dev)
+    _require(S0, "S0", (B, H, r, dv), torch.float32, dev)
+    if y is None:
+        y = torch.empty((B, H, T, dv), device=dev, dtype=q.dtype)
+    if S_out is None:
+        S_out = torch.empty((B, H, r, dv), device=dev, dtype=torch.float32)
+    _require(y, "y", (B, H, T, dv), q.dtype, dev)
+    _require(S_out, "S_out", (B, H, r, dv), torch.float32, dev)
+    st = _native.lib().la_delta_rule(_ptr(q), _ptr(k), _ptr(v), _DTYPES[q.dtype], _ptr(beta), _ptr(S0), B, H, T,
+                                     r, dv, _ptr(y), _ptr(S_out), _stream(dev))
+    _native.check(st, "la_delta_rule")
+    return y, S_out
+
+
 def last_device_status(device="cuda") -> int:
     """Synchronises the current stream and returns (and clears) the device status word."""
     return int(_native.lib().la_last_device_status(_stream(torch.device(device))))

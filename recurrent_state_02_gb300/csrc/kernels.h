@@ -77,6 +77,12 @@ cudaError_t launch_decode(const void *q, const void *k, const void *v, bool bf16
                           float *S, float *z, int B, int H, int r, int dv, float eps, void *y,
                           bool fast128, cudaStream_t stream);
 
+// Delta-rule memory, token recurrence in FP32 (CUDA cores): r in {32, 64, 128, 256},
+// dv a multiple of 32; q, k, v, y 16-byte aligned; bf16 selects the q/k/v/y type.
+cudaError_t launch_delta(const void *q, const void *k, const void *v, bool bf16, const float *beta, const float *S0,
+                         int B, int H, int T, int r, int dv, void *y, float *S_out, int *status,
+                         unsigned long long limit_ns, cudaStream_t stream);
+
 cudaError_t launch_state_init(float *S, float *z, long long n_S, long long n_z, cudaStream_t stream);
 
 cudaError_t launch_wait_probe(int *status, unsigned long long limit_ns, cudaStream_t stream);

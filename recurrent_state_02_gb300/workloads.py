@@ -55,6 +55,10 @@ LONG = Workload("long prefill B1 H32 T65536 d128 bf16 sigma=2 C64", B=1, H=32, T
                 scale=2.0, seed=4)
 WORKLOADS = {"tiny": TINY, "ungated": UNGATED, "gated": GATED, "decode": DECODE, "long": LONG}
 
+# The delta-rule memory on the shape of the ungated prefill.
+DELTA = Workload("delta rule B4 H16 T4096 d128 bf16, unit q and k, beta=sigmoid(N(0,1))", B=4, H=16, T=4096,
+                 seed=5)
+
 
 def prefill_inputs(w: Workload, device="cpu", with_state: bool = False, seed: int | None = None):
     """q, k [B,H,T,r], v [B,H,T,dv] in ``w.dtype``; alpha [B,H,T] FP32 or None;
@@ -97,6 +101,26 @@ def decode_inputs(w: Workload, device="cpu", seed: int | None = None):
         gl = torch.randn((w.B, w.H), generator=g, dtype=torch.float64) * w.gate_sigma + w.gate_mu
         alpha = torch.sigmoid(gl).to(torch.float32)
     out = dict(q=q, k=k, v=v, alpha=alpha, S=S, z=z)
+    if device != "cpu":
+        out = {n: (t.to(device) if t is not None else None) for n, t in out.items()}
+    return out
+
+
+def delta_inputs(w: Workload, device="cpu", with_state: bool = False, seed: int | None = None):
+    """Inputs of the delta-rule memory: q, k [B,H,T,r] drawn N(0,1) and divided by
+    their Euclidean norm in FP32 (unit vectors, as in the pages' examples, so that
+    beta |k|^2 = beta < 1 keeps every write a contraction), v [B,H,T,dv] ~
+    N(0, scale^2), all rounded once to ``w.dtype``; beta [B,H,T] = sigmoid(N(0,1))
+    in FP64 rounded to FP32; S0 [B,H,r,dv] ~ N(0,1)*0.1 when ``with_state``."""
+    g = torch.Generator().manual_seed(w.seed if seed is None else seed)
+    shape_qk = (w.B, w.H, w.T, w.r)
+    unit = lambda x: x / x.norm(dim=-1, keepdim=True).clamp_min(1e-30)
+    q = unit(torch.randn(shape_qk, generator=g, dtype=torch.float32)).to(w.dtype)
+    k = unit(torch.randn(shape_qk, generator=g, dtype=torch.float32)).to(w.dtype)
+    v = (torch.randn((w.B, w.H, w.T, w.dv), generator=g, dtype=torch.float32) * w.scale).to(w.dtype)
+    beta = torch.sigmoid(torch.randn((w.B, w.H, w.T), generator=g, dtype=torch.float64)).to(torch.float32)
+    S0 = torch.randn((w.B, w.H, w.r, w.dv), generator=g, dtype=torch.float32) * 0.1 if with_state else None
+    out = dict(q=q, k=k, v=v, beta=beta, S0=S0)
     if device != "cpu":
         out = {n: (t.to(device) if t is not None else None) for n, t in out.items()}
     return out
