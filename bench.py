@@ -11,7 +11,8 @@ Each step is replayed as a CUDA graph of its three kernel launches.
 
 Printed (rank 0, one JSON line): tokens/s of the step, the prefill kernel's
 roofline (algorithmic bytes / mean launch time vs measured HBM bandwidth), the
-decode step on its own workload (B=256, H=16) in GB/s, an end-to-end figure
+decode step on its own workload (B=256, H=16) in GB/s, the delta-rule memory
+on the prefill's shape against the FP32 ALU peak, an end-to-end figure
 through the public API with host buffers, clocks sampled during timing, and
 the FP64 CPU oracle timed on the host cores.
 
@@ -56,6 +57,23 @@ def decode_bytes(B, H, r, dv, elem=2):
     return B * H * (2 * 4 * (r * dv + r) + elem * (2 * r + 2 * dv))
 
 
+def delta_flops(B, H, T, r, dv):
+    """Algorithmic FLOPs of one delta-rule launch: per token and head, the read
+    S^T k, the rank-1 write and the read S^T q, 2 r dv each."""
+    return B * H * T * 6 * r * dv
+
+
+def fp32_alu_peak_tflops(sm_count):
+    """FP32 FMA peak of the CUDA cores: SMs x 128 FP32 lanes x 2 FLOP x the
+    maximum SM clock (MEASURED_PEAKS.json, else the nominal 2070 MHz)."""
+    try:
+        with open(PEAKS_FILE) as f:
+            mhz = float(json.load(f)["sm_max_mhz"])
+    except Exception:
+        mhz = 2070.0
+    return sm_count * 128 * 2 * mhz * 1e6 / 1e12
+
+
 def read_peaks():
     try:
         with open(PEAKS_FILE) as f:
@@ -77,7 +95,7 @@ def source_sha1(paths):
 def kernel_sources(name):
     """The files a kernel is compiled from (its .cu and the headers it includes)."""
     csrc = os.path.join(ROOT, "recurrent_state_02_gb300", "csrc")
-    common = ("tc_common.cuh",) if name == "prefill_tc.cu" else ()
+    common = ("tc_common.cuh",) if name in ("prefill_tc.cu", "delta.cu") else ()
     return [os.path.join(csrc, f) for f in (name, "kernels.h", "sm103_ptx.cuh") + common]
 
 
@@ -405,6 +423,35 @@ def run_ours(args, rank, world, local_rank):
               "algorithmic_bytes_per_launch": dbytes, "tokens_per_s": dw.B * world / dec_launch,
               "traffic": profile_traffic("decode128_kernel<true>", "B256 H16", kernel_sources("decode.cu"))}
 
+    # delta-rule memory on its own workload (B=4, H=16, T=4096, r = dv = 128, BF16;
+    # q, k, v 201 MB > L2): one launch per replay
+    xw = W.DELTA
+    xin = {k: (v.to(dev) if v is not None else None) for k, v in W.delta_inputs(xw, seed=xw.seed + 1000 * rank).items()}
+    ydel = torch.empty((xw.B, xw.H, xw.T, xw.dv), device=dev, dtype=torch.bfloat16)
+    Sdel = torch.empty((xw.B, xw.H, xw.r, xw.dv), device=dev, dtype=torch.float32)
+
+    def k_delta():
+        _native.check(L.la_delta_rule(P(xin["q"]), P(xin["k"]), P(xin["v"]), _native.LA_DTYPE_BF16, P(xin["beta"]),
+                                      None, xw.B, xw.H, xw.T, xw.r, xw.dv, P(ydel), P(Sdel), sh), "la_delta_rule")
+
+    with torch.cuda.stream(stream):
+        k_delta()
+    gx = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(gx, stream=stream):
+        k_delta()
+    x_s = timed([gx] * N_ROT, args.steps, args.warmup)
+    x_s, = reduce_max([x_s], dev, dist)
+    assert _native.lib().la_last_device_status(sh) == 0
+    x_launch = x_s / args.steps
+    x_tflops = delta_flops(xw.B, xw.H, xw.T, xw.r, xw.dv) / x_launch / 1e12
+    alu_peak = fp32_alu_peak_tflops(torch.cuda.get_device_properties(dev).multi_processor_count)
+    delta = {"workload": xw.name, "launch_us": x_launch * 1e6, "tokens_per_s": xw.B * xw.T * world / x_launch,
+             "roofline": {"bound": "alu", "achieved": x_tflops, "peak": alu_peak, "unit": "TFLOP/s",
+                          "frac": x_tflops / alu_peak, "peak_kind": "nominal FP32 FMA (SMs x 128 x 2 x max clock)",
+                          "traffic": profile_traffic("delta_kernel<bf16,128>", "B4 H16 T4096",
+                                                     kernel_sources("delta.cu")),
+                          "algorithmic_flops_per_launch": delta_flops(xw.B, xw.H, xw.T, xw.r, xw.dv)}}
+
     # end to end through the public API with host buffers (pinned), every step:
     # H2D of q, k, v (+ the decode token), the three calls, D2H of y, S, z, y_decode
     hq, hk, hv = (base[n].pin_memory() for n in ("q", "k", "v"))
@@ -460,7 +507,7 @@ def run_ours(args, rank, world, local_rank):
                                  f"{prefill_bytes(B, H, T, r, dv) / 1e6:.0f} MB (> 129 MB L2)",
                            "parallelism": f"replicas x{world} (independent batches, no collective)",
                            "launch": "CUDA graph per step"},
-                "roofline": roofline, "decode": decode, "cpu_baseline": cpu, "e2e": e2e,
+                "roofline": roofline, "decode": decode, "delta_rule": delta, "cpu_baseline": cpu, "e2e": e2e,
                 "gpu_launches": launches_per_step * args.steps, "clocks": clocks}
         print(json.dumps(line), flush=True)
 

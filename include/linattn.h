@@ -206,8 +206,8 @@ la_status la_decode_step(const void *q, const void *k, const void *v, la_dtype d
  * Kernel: the token recurrence in FP32 on CUDA cores (the pages give no block
  * algorithm for this rule, [LA] "训练时，状态更新也能按块并行"), the state in
  * registers, the value columns split over CTAs.  Requires r in {32, 64, 128, 256},
- * dv a multiple of 32, q, k, v, y 16-byte aligned, beta, S0, S_out 4-byte
- * aligned.  T may be 0 (S_out = S0; q, k, v, y may then be NULL and are not touched).
+ * dv a multiple of 32, q, k, v, y 16-byte aligned, S0, S_out 8-byte aligned,
+ * beta 4-byte aligned.  T may be 0 (S_out = S0; q, k, v, y may then be NULL and are not touched).
  * Errors: LA_ERR_NULL, LA_ERR_SHAPE (B, H, r, dv < 1, T < 0), LA_ERR_DTYPE,
  *         LA_ERR_ALIGN, LA_ERR_UNSUPPORTED (other r or dv), LA_ERR_CUDA.
  */

@@ -369,10 +369,10 @@ la_status la_delta_rule(const void *q, const void *k, const void *v, la_dtype dt
     if (B < 1 || H < 1 || T < 0 || r < 1 || dv < 1) return LA_ERR_SHAPE;
     if (dtype != LA_DTYPE_BF16 && dtype != LA_DTYPE_FP32) return LA_ERR_DTYPE;
     if ((r != 32 && r != 64 && r != 128 && r != 256) || dv % 32 != 0) return LA_ERR_UNSUPPORTED;
-    // one CTA per (b, h, column slice); the narrowest slice is 16 columns
-    if ((long long)B * H * ((dv + 15) / 16) > 0x7fffffffLL) return LA_ERR_UNSUPPORTED;
+    // one CTA per (b, h, 32-column slice)
+    if ((long long)B * H * (dv / 32) > 0x7fffffffLL) return LA_ERR_UNSUPPORTED;
     if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(y, 16)) return LA_ERR_ALIGN;
-    if (!aligned(S_out, 4) || (S0 && !aligned(S0, 4)) || (beta && !aligned(beta, 4))) return LA_ERR_ALIGN;
+    if (!aligned(S_out, 8) || (S0 && !aligned(S0, 8)) || (beta && !aligned(beta, 4))) return LA_ERR_ALIGN;
     int *status = status_word();
     if (!status) return LA_ERR_CUDA;
     return from_cuda(la::launch_delta(q, k, v, dtype == LA_DTYPE_BF16, beta, S0, B, H, T, r, dv, y, S_out, status,

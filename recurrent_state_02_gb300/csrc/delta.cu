@@ -9,23 +9,29 @@
 // (section "训练时，状态更新也能按块并行"); this kernel runs the recurrence as
 // written, in FP32 with the state in registers.
 //
-// Every column j of S is an independent recurrence: p_j, the error e_j and the
+// Every column j of S is an independent recurrence: p_j, the error and the
 // update of column j involve column j alone.  So the value columns are split
 // over CTAs and warps with no exchange between them; only the sums over the r
 // rows (S^T k and S^T q) are reduced, inside a warp.
 //
-// A CTA has 4 warps and covers NC = 4 * (32 / G) columns of one (b, h), with
-// G = r / 32 row groups: lane (g, jj) of warp w owns column w * 32/G + jj and
-// the 32 rows {4 (G m + g) + e : m < 8, e < 4}.  Interleaving the row groups in
-// blocks of 4 makes the 16-byte shared loads of k and q conflict-free: the G
-// groups of a warp read G adjacent 16-byte words.
+// The limit of this token loop is shared-memory bandwidth: every lane needs the
+// token's k and q values for each of its rows, and a warp-wide 16-byte shared
+// load costs at least two cycles even when it broadcasts.  So a lane holds a
+// few rows of two columns (the loaded k, q values serve both), and a warp splits
+// the rows into 8 groups: lane (g, jj), g = lane / 4, owns the r/8 rows
+// {4 (8 m + g) + e : m < r/32, e < 4} of columns 2 jj and 2 jj + 1 of its
+// warp's 8.  A quarter-warp then reads two adjacent 16-byte words per load.
+// A CTA has 4 warps and 32 columns.
 //
 // The output is read after the write, y_t = S_t^T q_t.  Since S_t = S_{t-1} +
 // k_t c_t^T with c_t = beta_t (v_t - p_t), it equals S_{t-1}^T q_t + c_t (k_t . q_t):
-// both reads then use S_{t-1}, share one shuffle tree, and the next token's read
-// of S_t waits only for the write.  Per token a lane does 48 packed FP32 FMAs
-// (f32x2: S^T k, S^T q, the rank-1 write) and one log2(G)-step reduction of two
-// values; k . q comes once per token from the staged rows.
+// both reads use S_{t-1}, and the next token's reads wait only for the write.
+// The four partial sums of a lane (p and S^T q for its two columns) are
+// reduced over the 8 row groups by a reduce-scatter (each step sends half of
+// what a lane holds), after which each lane holds one total; three shuffles
+// hand c back to every lane of the column pair.  Per token a lane does
+// 3 r/4 packed FP32 FMAs (f32x2) and 8 shuffles; k . q comes once per token
+// from the staged rows.
 //
 // Tokens arrive in blocks of kTB: the TMA unit copies the block's q and k
 // (contiguous) and the CTA's slice of each v row into a double-buffered raw
@@ -42,18 +48,17 @@ namespace {
 constexpr int kTB = 32;                  // tokens per staged block
 constexpr int kWarps = 4;
 constexpr int kThreads = 32 * kWarps;
+constexpr int NC = 32;                   // value columns per CTA (8 per warp, 2 per lane)
 
-template <typename Tin, int G>
+template <typename Tin, int r>
 struct DeltaCfg {
-    static constexpr int r = 32 * G;               // key width
-    static constexpr int kCols = 32 / G;           // value columns per warp
-    static constexpr int NC = kWarps * kCols;      // value columns per CTA
+    static constexpr int F = r / 32;               // float4 row blocks per lane (r/8 rows)
     static constexpr int kEl = (int)sizeof(Tin);
+    static constexpr int RS = r + 4;               // FP32 row stride of q, k (16-byte pad)
     // byte offsets in dynamic shared memory
     static constexpr int kRawQ = kTB * r * kEl;    // one raw q (or k) block
     static constexpr int kRawV = kTB * NC * kEl;   // one raw v block (row stride NC)
     static constexpr int kRawStage = 2 * kRawQ + kRawV;
-    static constexpr int RS = r + 4;               // FP32 row stride of q, k (16-byte pad)
     static constexpr int kOffQ = 2 * kRawStage;    // FP32 q [kTB][RS]
     static constexpr int kOffK = kOffQ + kTB * RS * 4;
     static constexpr int kOffV = kOffK + kTB * RS * 4;    // FP32 v [kTB][NC]
@@ -94,8 +99,21 @@ __device__ __forceinline__ void to_f32(const unsigned char *src, float *dst, int
     }
 }
 
-__device__ __forceinline__ void store_out(float *p, size_t i, float x) { p[i] = x; }
-__device__ __forceinline__ void store_out(__nv_bfloat16 *p, size_t i, float x) { p[i] = __float2bfloat16_rn(x); }
+// 8 FP32 values as one 16-byte (FP32: two) global store of the output type.
+__device__ __forceinline__ void store8(__nv_bfloat16 *p, const float *f)
+{
+    uint4 w;
+    w.x = pack_bf16x2(f[0], f[1]);
+    w.y = pack_bf16x2(f[2], f[3]);
+    w.z = pack_bf16x2(f[4], f[5]);
+    w.w = pack_bf16x2(f[6], f[7]);
+    *reinterpret_cast<uint4 *>(p) = w;
+}
+__device__ __forceinline__ void store8(float *p, const float *f)
+{
+    reinterpret_cast<float4 *>(p)[0] = make_float4(f[0], f[1], f[2], f[3]);
+    reinterpret_cast<float4 *>(p)[1] = make_float4(f[4], f[5], f[6], f[7]);
+}
 
 __device__ __forceinline__ float2 lo2(float4 a) { return make_float2(a.x, a.y); }
 __device__ __forceinline__ float2 hi2(float4 a) { return make_float2(a.z, a.w); }
@@ -121,61 +139,93 @@ __device__ __forceinline__ float kq_of_lane(const float *fk, const float *fq, in
     return s.x + s.y;
 }
 
-// One token for one lane, from S_{t-1} (S2) and the token's k, q (kk, qq):
-//  - over the lane's rows, p = S_{t-1}^T k and u = S_{t-1}^T q, then both summed
-//    over the warp's row groups in one shuffle tree;
-//  - c = beta (v_j - p), the write S += k c, and the output
-//    y_j = u + c (k . q), which equals S_t^T q since S_t = S_{t-1} + k c^T.
-// So the read of the query does not wait for the write.  The next token's k and
-// q are loaded into kn, qn meanwhile (token tn of the staged block).
-template <int G, int kCols, int RS>
-__device__ __forceinline__ void token_step(float2 (&S2)[16], const float4 (&kk)[8], const float4 (&qq)[8],
-                                           float4 (&kn)[8], float4 (&qn)[8], const float *fk, const float *fq,
-                                           float vj, float bt, float kq, int tn, int g, float *yout)
+// Per-lane view of one token: its rows of k and q, and where the token's v, beta
+// and output live in the staged block.
+struct TokenIo {
+    const float *fk, *fq;   // staged rows (stride RS), offset to this lane's first row block
+    const float *fv;        // v of the token, column 0 of the CTA
+    const float *fb;        // beta of the token
+    float *fy;              // output row of the token
+};
+
+// One token for one lane.  S2[m][c][h] holds rows 4 (8 m + g) + 2h, + 1 of the
+// lane's column c (of 2); kk, qq hold the same rows of k_t and q_t.
+//  - partial sums over the lane's rows: p_c = S_{t-1}^T k, u_c = S_{t-1}^T q;
+//  - reduce-scatter over the 8 row groups (lane bits 4, 3, 2): after it, lane
+//    bit 4 says whether the lane holds a p (0) or a u (1), bit 3 which column;
+//  - the p lanes form c = beta (v_j - p_j); the u lanes take it from their
+//    partner and write y_j = u_j + c (k . q); every lane fetches c of both its
+//    columns and writes S += k c.
+// The next token's k and q are loaded into kn, qn meanwhile (token offset tn).
+template <int F, int RS>
+__device__ __forceinline__ void token_step(float2 (&S2)[F][2][2], const float4 (&kk)[F], const float4 (&qq)[F],
+                                           float4 (&kn)[F], float4 (&qn)[F], const TokenIo &io, int tn, float kq,
+                                           int lane, int col)
 {
-    float2 p0 = make_float2(0.f, 0.f), p1 = p0, p2 = p0, p3 = p0, u0 = p0, u1 = p0, u2 = p0, u3 = p0;
+    float2 pa[2][2], ua[2][2];
 #pragma unroll
-    for (int m = 0; m < 8; m += 2) {
-        p0 = __ffma2_rn(S2[2 * m], lo2(kk[m]), p0);
-        p1 = __ffma2_rn(S2[2 * m + 1], hi2(kk[m]), p1);
-        p2 = __ffma2_rn(S2[2 * m + 2], lo2(kk[m + 1]), p2);
-        p3 = __ffma2_rn(S2[2 * m + 3], hi2(kk[m + 1]), p3);
-        u0 = __ffma2_rn(S2[2 * m], lo2(qq[m]), u0);
-        u1 = __ffma2_rn(S2[2 * m + 1], hi2(qq[m]), u1);
-        u2 = __ffma2_rn(S2[2 * m + 2], lo2(qq[m + 1]), u2);
-        u3 = __ffma2_rn(S2[2 * m + 3], hi2(qq[m + 1]), u3);
+    for (int c = 0; c < 2; ++c)
+#pragma unroll
+        for (int h = 0; h < 2; ++h) pa[c][h] = ua[c][h] = make_float2(0.f, 0.f);
+#pragma unroll
+    for (int m = 0; m < F; ++m)
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+            pa[c][0] = __ffma2_rn(S2[m][c][0], lo2(kk[m]), pa[c][0]);
+            pa[c][1] = __ffma2_rn(S2[m][c][1], hi2(kk[m]), pa[c][1]);
+            ua[c][0] = __ffma2_rn(S2[m][c][0], lo2(qq[m]), ua[c][0]);
+            ua[c][1] = __ffma2_rn(S2[m][c][1], hi2(qq[m]), ua[c][1]);
+        }
+    {
+        const float4 *kr = reinterpret_cast<const float4 *>(io.fk + tn * RS);
+        const float4 *qr = reinterpret_cast<const float4 *>(io.fq + tn * RS);
+#pragma unroll
+        for (int m = 0; m < F; ++m) {
+            kn[m] = kr[8 * m];
+            qn[m] = qr[8 * m];
+        }
     }
-    const float4 *kr = reinterpret_cast<const float4 *>(fk + tn * RS) + g;
-    const float4 *qr = reinterpret_cast<const float4 *>(fq + tn * RS) + g;
+    float val[4];   // p_0, p_1, u_0, u_1 over this lane's rows
 #pragma unroll
-    for (int m = 0; m < 8; ++m) {
-        kn[m] = kr[G * m];
-        qn[m] = qr[G * m];
+    for (int c = 0; c < 2; ++c) {
+        const float2 ps = __fadd2_rn(pa[c][0], pa[c][1]), us = __fadd2_rn(ua[c][0], ua[c][1]);
+        val[c] = ps.x + ps.y;
+        val[2 + c] = us.x + us.y;
     }
-    const float2 ps = __fadd2_rn(__fadd2_rn(p0, p1), __fadd2_rn(p2, p3));
-    const float2 us = __fadd2_rn(__fadd2_rn(u0, u1), __fadd2_rn(u2, u3));
-    float2 s = make_float2(ps.x + ps.y, us.x + us.y);
+    // reduce-scatter: bit 4 keeps p (0) or u (1), bit 3 keeps column 0 or 1
+    const bool b4 = lane & 16, b3 = lane & 8;
+    float k0 = b4 ? val[2] : val[0], k1 = b4 ? val[3] : val[1];
+    const float s0 = b4 ? val[0] : val[2], s1 = b4 ? val[1] : val[3];
+    k0 += __shfl_xor_sync(0xffffffffu, s0, 16);
+    k1 += __shfl_xor_sync(0xffffffffu, s1, 16);
+    float tot = b3 ? k1 : k0;
+    tot += __shfl_xor_sync(0xffffffffu, b3 ? k0 : k1, 8);
+    tot += __shfl_xor_sync(0xffffffffu, tot, 4);
+    // p lanes: c = beta (v_j - p_j); u lanes take c from their partner (lane ^ 16)
+    const float cp = b4 ? 0.f : *io.fb * (io.fv[col] - tot);
+    const float cu = __shfl_xor_sync(0xffffffffu, cp, 16);
+    if (b4 && !(lane & 4)) io.fy[col] = fmaf(cu, kq, tot);
+    // c of columns 0 and 1 of this lane's pair: the p lanes jj and jj + 8
+    const int jj = lane & 3;
+    const float c0 = __shfl_sync(0xffffffffu, cp, jj), c1 = __shfl_sync(0xffffffffu, cp, jj + 8);
+    const float2 cc[2] = {make_float2(c0, c0), make_float2(c1, c1)};
 #pragma unroll
-    for (int o = kCols; o < 32; o <<= 1)
-        s = __fadd2_rn(s, make_float2(__shfl_xor_sync(0xffffffffu, s.x, o), __shfl_xor_sync(0xffffffffu, s.y, o)));
-    const float c = bt * (vj - s.x);
-    if (g == 0) *yout = fmaf(c, kq, s.y);
-    const float2 c2 = make_float2(c, c);
+    for (int m = 0; m < F; ++m)
 #pragma unroll
-    for (int m = 0; m < 8; ++m) {
-        S2[2 * m] = __ffma2_rn(lo2(kk[m]), c2, S2[2 * m]);
-        S2[2 * m + 1] = __ffma2_rn(hi2(kk[m]), c2, S2[2 * m + 1]);
-    }
+        for (int c = 0; c < 2; ++c) {
+            S2[m][c][0] = __ffma2_rn(lo2(kk[m]), cc[c], S2[m][c][0]);
+            S2[m][c][1] = __ffma2_rn(hi2(kk[m]), cc[c], S2[m][c][1]);
+        }
 }
 
-template <typename Tin, int G>
+template <typename Tin, int r>
 __global__ void __launch_bounds__(kThreads)
 delta_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k, const Tin *__restrict__ v,
              const float *__restrict__ beta, const float *S0, int T, int dv, int nslice, Tin *__restrict__ y,
              float *S_out, int *status, unsigned long long limit_ns)
 {
-    using Cfg = DeltaCfg<Tin, G>;
-    constexpr int r = Cfg::r, kCols = Cfg::kCols, NC = Cfg::NC, RS = Cfg::RS;
+    using Cfg = DeltaCfg<Tin, r>;
+    constexpr int F = Cfg::F, RS = Cfg::RS;
     extern __shared__ __align__(128) unsigned char smem[];
     float *fq = reinterpret_cast<float *>(smem + Cfg::kOffQ);
     float *fk = reinterpret_cast<float *>(smem + Cfg::kOffK);
@@ -186,13 +236,11 @@ delta_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k, const Tin *__
     int *flag = reinterpret_cast<int *>(smem + Cfg::kOffFlag);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int jj = lane % kCols, g = lane / kCols;
+    const int g = lane >> 2, jj = lane & 3;
     const int bh = blockIdx.x / nslice;
     const int c0 = (blockIdx.x % nslice) * NC;     // first value column of this CTA
-    const int ncv = min(NC, dv - c0);              // its columns (a multiple of kCols)
-    const int jl = warp * kCols + jj;              // local column of this lane
-    const bool active = warp * kCols < ncv;        // warp-uniform
-    const int j = c0 + jl;
+    const int jl = warp * 8 + 2 * jj;              // local column of the lane's pair
+    const int col = jl + ((lane >> 3) & 1);        // local column of this lane's reduced total
     const int nblk = (T + kTB - 1) / kTB;
     Ctx cx{flag, limit_ns, status};
 
@@ -210,42 +258,43 @@ delta_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k, const Tin *__
     auto issue = [&](int b) {
         const int st = b & 1, t0 = b * kTB, nt = min(kTB, T - t0);
         unsigned char *raw = smem + st * Cfg::kRawStage;
-        const uint32_t qbytes = (uint32_t)(nt * r * Cfg::kEl), vrow = (uint32_t)(ncv * Cfg::kEl);
+        const uint32_t qbytes = (uint32_t)(nt * r * Cfg::kEl), vrow = (uint32_t)(NC * Cfg::kEl);
         if (lane == 0) mbar_arrive_expect_tx(&full[st], 2 * qbytes + nt * vrow);
         __syncwarp();
         if (lane == 0) bulk_load(raw, qh + (size_t)t0 * r, qbytes, &full[st]);
         if (lane == 1) bulk_load(raw + Cfg::kRawQ, kh + (size_t)t0 * r, qbytes, &full[st]);
-        if (lane < nt) bulk_load(raw + 2 * Cfg::kRawQ + lane * NC * Cfg::kEl, vh + (size_t)(t0 + lane) * dv, vrow,
-                                 &full[st]);
+        if (lane < nt) bulk_load(raw + 2 * Cfg::kRawQ + lane * vrow, vh + (size_t)(t0 + lane) * dv, vrow, &full[st]);
     };
     if (warp == 0) {
         if (nblk > 0) issue(0);
         if (nblk > 1) issue(1);
     }
 
-    // S2[2m + h] holds rows 4 (G m + g) + 2h and + 1 of column j.
-    float2 S2[16];
+    // S2[m][c][h]: rows 4 (8 m + g) + 2h and + 1 of column c0 + jl + c
+    float2 S2[F][2][2];
 #pragma unroll
-    for (int i = 0; i < 16; ++i) S2[i] = make_float2(0.f, 0.f);
-    if (S0 && active) {
-        const float *src = S0 + (size_t)bh * r * dv + j;
+    for (int m = 0; m < F; ++m)
 #pragma unroll
-        for (int m = 0; m < 8; ++m)
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                const int row = 4 * (G * m + g) + 2 * h;
-                S2[2 * m + h] = make_float2(src[(size_t)row * dv], src[(size_t)(row + 1) * dv]);
+        for (int h = 0; h < 2; ++h) {
+            const int row = 4 * (8 * m + g) + 2 * h;
+            float2 a = make_float2(0.f, 0.f), b = a;
+            if (S0) {
+                const float *src = S0 + ((size_t)bh * r + row) * dv + c0 + jl;
+                a = *reinterpret_cast<const float2 *>(src);        // row, columns jl, jl + 1
+                b = *reinterpret_cast<const float2 *>(src + dv);   // row + 1
             }
-    }
+            S2[m][0][h] = make_float2(a.x, b.x);
+            S2[m][1][h] = make_float2(a.y, b.y);
+        }
     float b_next = 1.f;
     if (beta && tid < kTB && tid < T) b_next = beta[(size_t)bh * T + tid];
 
     Tin *yh = y + (size_t)bh * T * dv + c0;
-    auto store_y = [&](int b) {
+    auto store_y = [&](int b) {   // NC columns of nt rows, 8 per thread per pass
         const int t0 = b * kTB, nt = min(kTB, T - t0);
-        for (int e = tid; e < nt * ncv; e += kThreads) {
-            const int t = e / ncv, c = e - t * ncv;
-            store_out(yh, (size_t)(t0 + t) * dv + c, fy[t * NC + c]);
+        for (int e = tid; e < nt * (NC / 8); e += kThreads) {
+            const int t = e / (NC / 8), c = (e % (NC / 8)) * 8;
+            store8(yh + (size_t)(t0 + t) * dv + c, fy + t * NC + c);
         }
     };
 
@@ -263,28 +312,30 @@ delta_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k, const Tin *__
         __syncthreads();                    // FP32 block ready; the raw stage is free again
         if (warp == 0 && b + 2 < nblk) issue(b + 2);
         if (beta && tid < kTB && t0 + kTB + tid < T) b_next = beta[(size_t)bh * T + t0 + kTB + tid];
-        if (!active) continue;
         const float kq_reg = kq_of_lane<r, RS>(fk, fq, lane, nt);   // lane l: token l of the block
-        float4 kA[8], qA[8], kB[8], qB[8];
+        float4 kA[F], qA[F], kB[F], qB[F];
         {
             const float4 *kr = reinterpret_cast<const float4 *>(fk) + g;
             const float4 *qr = reinterpret_cast<const float4 *>(fq) + g;
 #pragma unroll
-            for (int m = 0; m < 8; ++m) {
-                kA[m] = kr[G * m];
-                qA[m] = qr[G * m];
+            for (int m = 0; m < F; ++m) {
+                kA[m] = kr[8 * m];
+                qA[m] = qr[8 * m];
             }
         }
+        TokenIo io{fk + 4 * g, fq + 4 * g, fv, fb, fy};
         // tokens in pairs, the operand registers alternating between A and B
 #pragma unroll 1
         for (int t = 0; t < nt; t += 2) {
-            token_step<G, kCols, RS>(S2, kA, qA, kB, qB, fk, fq, fv[t * NC + jl], fb[t],
-                                        __shfl_sync(0xffffffffu, kq_reg, t), min(t + 1, nt - 1), g,
-                                        fy + t * NC + jl);
-            if (t + 1 < nt)
-                token_step<G, kCols, RS>(S2, kB, qB, kA, qA, fk, fq, fv[(t + 1) * NC + jl], fb[t + 1],
-                                            __shfl_sync(0xffffffffu, kq_reg, t + 1), min(t + 2, nt - 1), g,
-                                            fy + (t + 1) * NC + jl);
+            TokenIo it = io;
+            it.fv += t * NC; it.fb += t; it.fy += t * NC;
+            token_step<F, RS>(S2, kA, qA, kB, qB, it, min(t + 1, nt - 1), __shfl_sync(0xffffffffu, kq_reg, t), lane,
+                              col);
+            if (t + 1 < nt) {
+                it.fv += NC; it.fb += 1; it.fy += NC;
+                token_step<F, RS>(S2, kB, qB, kA, qA, it, min(t + 2, nt - 1), __shfl_sync(0xffffffffu, kq_reg, t + 1),
+                                  lane, col);
+            }
         }
     }
 
@@ -297,29 +348,27 @@ delta_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k, const Tin *__
     }
     __syncthreads();
     if (nblk > 0) store_y(nblk - 1);
-    if (active) {
-        float *dst = S_out + (size_t)bh * r * dv + j;
 #pragma unroll
-        for (int m = 0; m < 8; ++m)
+    for (int m = 0; m < F; ++m)
 #pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                const int row = 4 * (G * m + g) + 2 * h;
-                dst[(size_t)row * dv] = S2[2 * m + h].x;
-                dst[(size_t)(row + 1) * dv] = S2[2 * m + h].y;
-            }
-    }
+        for (int h = 0; h < 2; ++h) {
+            const int row = 4 * (8 * m + g) + 2 * h;
+            float *dst = S_out + ((size_t)bh * r + row) * dv + c0 + jl;
+            *reinterpret_cast<float2 *>(dst) = make_float2(S2[m][0][h].x, S2[m][1][h].x);
+            *reinterpret_cast<float2 *>(dst + dv) = make_float2(S2[m][0][h].y, S2[m][1][h].y);
+        }
 }
 
-template <typename Tin, int G>
-cudaError_t launch_g(const void *q, const void *k, const void *v, const float *beta, const float *S0, int B, int H,
+template <typename Tin, int r>
+cudaError_t launch_r(const void *q, const void *k, const void *v, const float *beta, const float *S0, int B, int H,
                      int T, int dv, void *y, float *S_out, int *status, unsigned long long limit_ns,
                      cudaStream_t stream)
 {
-    using Cfg = DeltaCfg<Tin, G>;
-    auto kern = delta_kernel<Tin, G>;
+    using Cfg = DeltaCfg<Tin, r>;
+    auto kern = delta_kernel<Tin, r>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kBytes);
     if (e != cudaSuccess) return e;
-    const int nslice = (dv + Cfg::NC - 1) / Cfg::NC;
+    const int nslice = dv / NC;
     kern<<<(unsigned)((long long)B * H * nslice), kThreads, Cfg::kBytes, stream>>>(
         static_cast<const Tin *>(q), static_cast<const Tin *>(k), static_cast<const Tin *>(v), beta, S0, T, dv,
         nslice, static_cast<Tin *>(y), S_out, status, limit_ns);
@@ -332,10 +381,10 @@ cudaError_t launch_t(const void *q, const void *k, const void *v, const float *b
                      cudaStream_t stream)
 {
     switch (r) {
-    case 32: return launch_g<Tin, 1>(q, k, v, beta, S0, B, H, T, dv, y, S_out, status, limit_ns, stream);
-    case 64: return launch_g<Tin, 2>(q, k, v, beta, S0, B, H, T, dv, y, S_out, status, limit_ns, stream);
-    case 128: return launch_g<Tin, 4>(q, k, v, beta, S0, B, H, T, dv, y, S_out, status, limit_ns, stream);
-    case 256: return launch_g<Tin, 8>(q, k, v, beta, S0, B, H, T, dv, y, S_out, status, limit_ns, stream);
+    case 32: return launch_r<Tin, 32>(q, k, v, beta, S0, B, H, T, dv, y, S_out, status, limit_ns, stream);
+    case 64: return launch_r<Tin, 64>(q, k, v, beta, S0, B, H, T, dv, y, S_out, status, limit_ns, stream);
+    case 128: return launch_r<Tin, 128>(q, k, v, beta, S0, B, H, T, dv, y, S_out, status, limit_ns, stream);
+    case 256: return launch_r<Tin, 256>(q, k, v, beta, S0, B, H, T, dv, y, S_out, status, limit_ns, stream);
     default: return cudaErrorInvalidValue;
     }
 }

@@ -163,4 +163,5 @@ def test_delta_rejects_bad_arguments(native):
     assert f(dv=48) == native.LA_ERR_UNSUPPORTED
     assert f(v=FAKE + 8) == native.LA_ERR_ALIGN
     assert f(beta=FAKE + 2) == native.LA_ERR_ALIGN
-    assert f(S0=FAKE + 1) == native.LA_ERR_ALIGN
+    assert f(S0=FAKE + 4) == native.LA_ERR_ALIGN
+    assert f(S_out=FAKE + 4) == native.LA_ERR_ALIGN
