@@ -446,3 +446,239 @@ int or_delta(int B, int H, int T, int r, int dv, const void *q, const void *k, c
     }
     return 0;
 }
+
+/* -------------------------------------------------------------- backward -- */
+
+/*
+ * Gradients of the token recurrence (or_scan) for a loss L whose derivatives
+ * with respect to the outputs are given: dy [B,H,T,dv], and optionally dS_T
+ * [B,H,r,dv], dz_T [B,H,r] (NULL: zero).  The pages give no backward formula;
+ * this is the chain rule applied to the recurrence of [LA] "公式里的每个维度"
+ * and "加一个门：让旧记忆逐渐淡出", step by step in reverse:
+ *   with y_t = n_t / d_t,  n_t = S_t^T q~_t,  d_t = q~_t . z_t + eps:
+ *     dn_t = dy_t / d_t,   dd_t = -(dy_t . y_t) / d_t;
+ *   G_t = dL/dS_t = q~_t dn_t^T + alpha_{t+1} G_{t+1}   (G_T from dS_T),
+ *   g_t = dL/dz_t = dd_t q~_t  + alpha_{t+1} g_{t+1}    (g_T from dz_T);
+ *     dq~_t = S_t dn_t + dd_t z_t,   dk~_t = G_t v_t + g_t,   dv_t = G_t^T k~_t,
+ *     dalpha_t = <G_t, S_{t-1}> + <g_t, z_{t-1}>,   dS0 = alpha_1 G_1,  dz0 = alpha_1 g_1;
+ *   dq_t = dq~_t * phi'(q_t), dk_t = dk~_t * phi'(k_t), phi'(x) = 1 for x > 0 and
+ *   e^x otherwise (ELU+1), 0 otherwise for relu+1, 1 for the identity.
+ * The reverse sweep needs S_t and S_{t-1} at every step.  They are recomputed
+ * segment by segment from states saved every kSeg tokens during a first forward
+ * sweep; the recomputation repeats the forward arithmetic exactly, so the states
+ * are the same numbers as in or_scan.
+ *   dq, dk [B,H,T,r]; dv [B,H,T,dv]; dalpha [B,H,T] (written when alpha is given);
+ *   dS0 [B,H,r,dv]; dz0 [B,H,r].
+ */
+enum { kSeg = 64 };
+
+typedef struct {
+    problem f;                 /* forward problem (y, S, z point at per-thread scratch) */
+    const double *dy, *dS_T, *dz_T;
+    double *dq, *dk, *dvo, *dalpha, *dS0, *dz0;
+    size_t next;
+    pthread_mutex_t lock;
+} bwd_problem;
+
+static double dphi(double x, int kind)
+{
+    if (kind == OR_PHI_ELU1) return x > 0.0 ? 1.0 : exp(x);
+    if (kind == OR_PHI_RELU1) return x > 0.0 ? 1.0 : 0.0;
+    return 1.0;
+}
+
+/* One forward step on (S, z) in place, exactly as scan_one does it. */
+static void fwd_step(const problem *p, size_t bh, int t, double *S, double *z, double *kt)
+{
+    const int T = p->T, r = p->r, dv = p->dv;
+    const size_t row_qk = (bh * (size_t)T + (size_t)t) * (size_t)r;
+    const size_t row_v = (bh * (size_t)T + (size_t)t) * (size_t)dv;
+    const double a = gate(p, bh, t);
+    for (int i = 0; i < r; ++i) kt[i] = phi(decode(p->k, p->in_type, row_qk + i), p->phi_kind);
+    for (int i = 0; i < r; ++i) {
+        double *Si = S + (size_t)i * dv;
+        for (int j = 0; j < dv; ++j) Si[j] = a * Si[j] + kt[i] * decode(p->v, p->in_type, row_v + j);
+        z[i] = a * z[i] + kt[i];
+    }
+}
+
+/* scratch per thread: checkpoints, one segment of states, y, d and vectors */
+typedef struct {
+    double *ckS, *ckz;         /* [nseg][r*dv], [nseg][r]: state before the segment's first token */
+    double *segS, *segz;       /* [kSeg+1][r*dv], [kSeg+1][r]: S_{t0-1} .. S_{t0+kSeg-1} */
+    double *y, *d;             /* [T][dv], [T] */
+    double *G, *g, *qt, *kt, *dn;
+} bwd_scratch;
+
+static void backward_one(const bwd_problem *bp, size_t bh, bwd_scratch *w)
+{
+    const problem *p = &bp->f;
+    const int T = p->T, r = p->r, dv = p->dv;
+    const size_t rd = (size_t)r * dv;
+    const int nseg = (T + kSeg - 1) / kSeg;
+
+    /* forward sweep: checkpoints, outputs y_t and denominators d_t */
+    double *S = w->segS, *z = w->segz;
+    if (p->S0) memcpy(S, p->S0 + bh * rd, sizeof(double) * rd);
+    else memset(S, 0, sizeof(double) * rd);
+    if (p->z0) memcpy(z, p->z0 + bh * (size_t)r, sizeof(double) * (size_t)r);
+    else memset(z, 0, sizeof(double) * (size_t)r);
+    for (int t = 0; t < T; ++t) {
+        if (t % kSeg == 0) {
+            memcpy(w->ckS + (size_t)(t / kSeg) * rd, S, sizeof(double) * rd);
+            memcpy(w->ckz + (size_t)(t / kSeg) * r, z, sizeof(double) * (size_t)r);
+        }
+        fwd_step(p, bh, t, S, z, w->kt);
+        const size_t row_qk = (bh * (size_t)T + (size_t)t) * (size_t)r;
+        for (int i = 0; i < r; ++i) w->qt[i] = phi(decode(p->q, p->in_type, row_qk + i), p->phi_kind);
+        double den = 0.0;
+        for (int i = 0; i < r; ++i) den += w->qt[i] * z[i];
+        den += p->eps;
+        w->d[t] = den;
+        for (int j = 0; j < dv; ++j) {
+            double num = 0.0;
+            for (int i = 0; i < r; ++i) num += w->qt[i] * S[(size_t)i * dv + j];
+            w->y[(size_t)t * dv + j] = num / den;
+        }
+    }
+
+    /* reverse sweep */
+    double *G = w->G, *g = w->g;
+    if (bp->dS_T) memcpy(G, bp->dS_T + bh * rd, sizeof(double) * rd);
+    else memset(G, 0, sizeof(double) * rd);
+    if (bp->dz_T) memcpy(g, bp->dz_T + bh * (size_t)r, sizeof(double) * (size_t)r);
+    else memset(g, 0, sizeof(double) * (size_t)r);
+    for (int s = nseg - 1; s >= 0; --s) {
+        const int t0 = s * kSeg, t1 = t0 + kSeg < T ? t0 + kSeg : T;
+        /* states S_{t0-1} .. S_{t1-1} of this segment, recomputed from its checkpoint */
+        memcpy(w->segS, w->ckS + (size_t)s * rd, sizeof(double) * rd);
+        memcpy(w->segz, w->ckz + (size_t)s * r, sizeof(double) * (size_t)r);
+        for (int t = t0; t < t1; ++t) {
+            const int e = t - t0 + 1;
+            memcpy(w->segS + (size_t)e * rd, w->segS + (size_t)(e - 1) * rd, sizeof(double) * rd);
+            memcpy(w->segz + (size_t)e * r, w->segz + (size_t)(e - 1) * r, sizeof(double) * (size_t)r);
+            fwd_step(p, bh, t, w->segS + (size_t)e * rd, w->segz + (size_t)e * r, w->kt);
+        }
+        for (int t = t1 - 1; t >= t0; --t) {
+            const int e = t - t0 + 1;
+            const double *St = w->segS + (size_t)e * rd, *Sp = w->segS + (size_t)(e - 1) * rd;
+            const double *zt = w->segz + (size_t)e * r, *zp = w->segz + (size_t)(e - 1) * r;
+            const size_t row_qk = (bh * (size_t)T + (size_t)t) * (size_t)r;
+            const size_t row_v = (bh * (size_t)T + (size_t)t) * (size_t)dv;
+            for (int i = 0; i < r; ++i) {
+                w->qt[i] = phi(decode(p->q, p->in_type, row_qk + i), p->phi_kind);
+                w->kt[i] = phi(decode(p->k, p->in_type, row_qk + i), p->phi_kind);
+            }
+            /* dn_t = dy_t / d_t, dd_t = -(dy_t . y_t) / d_t */
+            double dd = 0.0;
+            for (int j = 0; j < dv; ++j) {
+                w->dn[j] = bp->dy[row_v + j] / w->d[t];
+                dd -= bp->dy[row_v + j] * w->y[(size_t)t * dv + j];
+            }
+            dd /= w->d[t];
+            /* G_t = q~_t dn_t^T + (alpha_{t+1} G_{t+1}),  g_t = dd_t q~_t + (alpha_{t+1} g_{t+1}) */
+            for (int i = 0; i < r; ++i) {
+                for (int j = 0; j < dv; ++j) G[(size_t)i * dv + j] += w->qt[i] * w->dn[j];
+                g[i] += dd * w->qt[i];
+            }
+            /* dq~_t = S_t dn_t + dd_t z_t ;  dk~_t = G_t v_t + g_t ;  dv_t = G_t^T k~_t */
+            for (int i = 0; i < r; ++i) {
+                double aq = dd * zt[i], ak = g[i];
+                for (int j = 0; j < dv; ++j) {
+                    aq += St[(size_t)i * dv + j] * w->dn[j];
+                    ak += G[(size_t)i * dv + j] * decode(p->v, p->in_type, row_v + j);
+                }
+                bp->dq[row_qk + i] = aq * dphi(decode(p->q, p->in_type, row_qk + i), p->phi_kind);
+                bp->dk[row_qk + i] = ak * dphi(decode(p->k, p->in_type, row_qk + i), p->phi_kind);
+            }
+            for (int j = 0; j < dv; ++j) {
+                double av = 0.0;
+                for (int i = 0; i < r; ++i) av += G[(size_t)i * dv + j] * w->kt[i];
+                bp->dvo[row_v + j] = av;
+            }
+            /* dalpha_t = <G_t, S_{t-1}> + <g_t, z_{t-1}>; then G_{t-1} part: alpha_t G_t */
+            const double a = gate(p, bh, t);
+            if (p->alpha) {
+                double da = 0.0;
+                for (size_t x = 0; x < rd; ++x) da += G[x] * Sp[x];
+                for (int i = 0; i < r; ++i) da += g[i] * zp[i];
+                bp->dalpha[bh * (size_t)T + (size_t)t] = da;
+            }
+            for (size_t x = 0; x < rd; ++x) G[x] *= a;
+            for (int i = 0; i < r; ++i) g[i] *= a;
+        }
+    }
+    memcpy(bp->dS0 + bh * rd, G, sizeof(double) * rd);
+    memcpy(bp->dz0 + bh * (size_t)r, g, sizeof(double) * (size_t)r);
+}
+
+static void *backward_worker(void *arg)
+{
+    bwd_problem *bp = (bwd_problem *)arg;
+    const problem *p = &bp->f;
+    const size_t rd = (size_t)p->r * p->dv, r = (size_t)p->r, dv = (size_t)p->dv, T = (size_t)p->T;
+    const size_t nseg = (T + kSeg - 1) / kSeg;
+    bwd_scratch w;
+    double *buf = (double *)malloc(sizeof(double) * (nseg * (rd + r) + (kSeg + 1) * (rd + r) + T * dv + T +
+                                                     rd + 3 * r + dv));
+    if (!buf) return NULL;
+    w.ckS = buf;
+    w.ckz = w.ckS + nseg * rd;
+    w.segS = w.ckz + nseg * r;
+    w.segz = w.segS + (kSeg + 1) * rd;
+    w.y = w.segz + (kSeg + 1) * r;
+    w.d = w.y + T * dv;
+    w.G = w.d + T;
+    w.g = w.G + rd;
+    w.qt = w.g + r;
+    w.kt = w.qt + r;
+    w.dn = w.kt + r;
+    const size_t nbh = (size_t)p->B * (size_t)p->H;
+    for (;;) {
+        pthread_mutex_lock(&bp->lock);
+        size_t bh = bp->next++;
+        pthread_mutex_unlock(&bp->lock);
+        if (bh >= nbh) break;
+        backward_one(bp, bh, &w);
+    }
+    free(buf);
+    return NULL;
+}
+
+int or_backward(int B, int H, int T, int r, int dv, const void *q, const void *k, const void *v, int in_type,
+                const double *alpha, const double *S0, const double *z0, double eps, int phi_kind,
+                const double *dy, const double *dS_T, const double *dz_T, int nthreads,
+                double *dq, double *dk, double *dvo, double *dalpha, double *dS0, double *dz0)
+{
+    double dummy = 0.0;
+    bwd_problem bp;
+    problem f = {B, H, T, r, dv, in_type, phi_kind, 0, q, k, v, alpha, S0, z0, eps, &dummy, &dummy, &dummy};
+    if (check(&f)) return -1;
+    if (!dy || !dq || !dk || !dvo || !dS0 || !dz0 || (alpha && !dalpha)) return -1;
+    bp.f = f;
+    bp.dy = dy;
+    bp.dS_T = dS_T;
+    bp.dz_T = dz_T;
+    bp.dq = dq;
+    bp.dk = dk;
+    bp.dvo = dvo;
+    bp.dalpha = dalpha;
+    bp.dS0 = dS0;
+    bp.dz0 = dz0;
+    bp.next = 0;
+    pthread_mutex_init(&bp.lock, NULL);
+    const size_t nbh = (size_t)B * (size_t)H;
+    if (nthreads <= 0) nthreads = or_num_cpus();
+    if ((size_t)nthreads > nbh) nthreads = (int)nbh;
+    if (nthreads == 1) {
+        backward_worker(&bp);
+    } else {
+        pthread_t *th = (pthread_t *)malloc(sizeof(pthread_t) * (size_t)nthreads);
+        if (!th) return -1;
+        for (int i = 0; i < nthreads; ++i) pthread_create(&th[i], NULL, backward_worker, &bp);
+        for (int i = 0; i < nthreads; ++i) pthread_join(th[i], NULL);
+        free(th);
+    }
+    pthread_mutex_destroy(&bp.lock);
+    return 0;
+}

@@ -48,7 +48,8 @@ def _bind(path: str):
     lib.or_dense.argtypes = common + [dp, dp, dp]
     lib.or_chunkwise.argtypes = common + [i, dp, dp, dp]
     lib.or_delta.argtypes = [i, i, i, i, i, vp, vp, vp, i, dp, dp, i, dp, dp]
-    for f in (lib.or_scan, lib.or_dense, lib.or_chunkwise, lib.or_delta):
+    lib.or_backward.argtypes = common + [dp, dp, dp, i, dp, dp, dp, dp, dp, dp]
+    for f in (lib.or_scan, lib.or_dense, lib.or_chunkwise, lib.or_delta, lib.or_backward):
         f.restype = ctypes.c_int
     lib.or_num_cpus.restype = ctypes.c_int
     return lib
@@ -142,6 +143,29 @@ def chunkwise(q, k, v, chunk, alpha=None, S0=None, z0=None, eps=1e-6, phi=PHI_EL
     return y, S, z
 
 
+def backward(q, k, v, dy, alpha=None, S0=None, z0=None, dS_T=None, dz_T=None, eps=1e-6, phi=PHI_ELU1, threads=0,
+             _lib=None):
+    """Gradients of or_scan's outputs (y, S_T, z_T) for a loss with the given output
+    gradients dy [B,H,T,dv] and, optionally, dS_T [B,H,r,dv], dz_T [B,H,r].
+    Returns (dq, dk, dv, dalpha or None, dS0, dz0) in float64."""
+    q, k, v, alpha, S0, z0, (B, H, T, r, dv) = _prepare(q, k, v, alpha, S0, z0)
+    dy = np.ascontiguousarray(dy, dtype=np.float64).reshape(B, H, T, dv)
+    if dS_T is not None:
+        dS_T = np.ascontiguousarray(dS_T, dtype=np.float64).reshape(B, H, r, dv)
+    if dz_T is not None:
+        dz_T = np.ascontiguousarray(dz_T, dtype=np.float64).reshape(B, H, r)
+    dq, dk = np.empty((B, H, T, r)), np.empty((B, H, T, r))
+    dvo, dS0, dz0 = np.empty((B, H, T, dv)), np.empty((B, H, r, dv)), np.empty((B, H, r))
+    dalpha = np.empty((B, H, T)) if alpha is not None else None
+    rc = (_lib or _load()).or_backward(B, H, T, r, dv, _ptr(q), _ptr(k), _ptr(v), _in_type(q), _ptr(alpha),
+                                       _ptr(S0), _ptr(z0), float(eps), int(phi), _ptr(dy), _ptr(dS_T),
+                                       _ptr(dz_T), int(threads), _ptr(dq), _ptr(dk), _ptr(dvo), _ptr(dalpha),
+                                       _ptr(dS0), _ptr(dz0))
+    if rc:
+        raise ValueError("or_backward rejected its arguments")
+    return dq, dk, dvo, dalpha, dS0, dz0
+
+
 def delta(q, k, v, beta=None, S0=None, threads=0, _lib=None):
     """Delta-rule memory (LA "Delta rule：先读旧答案，再写误差"): returns (y, S_T) in float64."""
     q, k, v, beta, S0, _, (B, H, T, r, dv) = _prepare(q, k, v, beta, S0, None)
@@ -172,3 +196,6 @@ class Variant:
 
     def delta(self, *a, **kw):
         return delta(*a, _lib=self._lib, **kw)
+
+    def backward(self, *a, **kw):
+        return backward(*a, _lib=self._lib, **kw)
