@@ -191,6 +191,48 @@ la_status la_decode_step(const void *q, const void *k, const void *v, la_dtype d
                          float eps, void *y, la_stream_t stream);
 
 /*
+ * la_backward_workspace_bytes -- device scratch that la_prefill_backward needs:
+ * 4 * B*H*(3T + 1) bytes (FP32 per-token terms and one value per head).
+ */
+size_t la_backward_workspace_bytes(int B, int H, int T);
+
+/*
+ * la_prefill_backward -- gradients of la_prefill_chunked's outputs for training.
+ * Given dy = dL/dy and optionally dS_T = dL/dS_T, dz_T = dL/dz_T, returns
+ * dL/dq, dL/dk, dL/dv, dL/dalpha, dL/dS0 and dL/dz0.  The pages give no backward
+ * formula; this is the chain rule through the recurrence of [LA] "公式里的每个维度"
+ * and "加一个门：让旧记忆逐渐淡出", with y_t = n_t / d_t:
+ *   dn_t = dy_t / d_t,  dd_t = -(dy_t . y_t) / d_t,
+ *   G_t = phi(q_t) dn_t^T + alpha_{t+1} G_{t+1},  g_t = dd_t phi(q_t) + alpha_{t+1} g_{t+1},
+ *   dq_t = phi'(q_t) * (S_t dn_t + dd_t z_t),  dk_t = phi'(k_t) * (G_t v_t + g_t),
+ *   dv_t = G_t^T phi(k_t),  dS0 = alpha_1 G_1,  dz0 = alpha_1 g_1,
+ *   dalpha_u = (sum_{t >= u} (phi(q_t) . dq~_t - phi(k_t) . dk~_t) + <dS_T, S_T> + <dz_T, z_T>) / alpha_u
+ * (dq~, dk~: the gradients before the phi' factor).
+ *   q, k, v, alpha, S0, z0, eps: as passed to the forward call.
+ *   y      device [B,H,T,dv] dtype: the forward's output (used for dd_t).
+ *   dy     device [B,H,T,dv] dtype.
+ *   dS_T, dz_T  device FP32 [B,H,r,dv], [B,H,r], or NULL (zero).
+ *   dq, dk device [B,H,T,r] dtype;  dv_out device [B,H,T,dv] dtype.
+ *   dalpha device FP32 [B,H,T], or NULL (not computed; ignored without alpha).
+ *          Defined where alpha > 0 (it is the log-gate derivative over alpha).
+ *   dS0, dz0  device FP32 [B,H,r,dv], [B,H,r] (written also when S0, z0 are NULL).
+ *   workspace: >= la_backward_workspace_bytes device bytes, 16-byte aligned, owned by
+ *          the caller; calls sharing it must be ordered.
+ * Kernels (FP32 on CUDA cores): one pass for d_t and dd_t, three gated rank-1
+ * recurrences (dq forward in time, dk and dv in reverse), and a reverse running
+ * sum for dalpha.  Requires r, dv in {32, 64, 128}, T >= 1, 16-byte aligned
+ * token arrays (q, k, v, y, dy, dq, dk, dv_out), 4-byte aligned FP32 arrays
+ * (dS_T 8-byte aligned).
+ * Errors: LA_ERR_NULL, LA_ERR_SHAPE, LA_ERR_DTYPE, LA_ERR_ALIGN, LA_ERR_UNSUPPORTED,
+ *         LA_ERR_WORKSPACE, LA_ERR_CUDA.
+ */
+la_status la_prefill_backward(const void *q, const void *k, const void *v, la_dtype dtype, const float *alpha,
+                              const float *S0, const float *z0, int B, int H, int T, int r, int dv, float eps,
+                              const void *y, const void *dy, const float *dS_T, const float *dz_T, void *dq,
+                              void *dk, void *dv_out, float *dalpha, float *dS0, float *dz0, void *workspace,
+                              size_t workspace_bytes, la_stream_t stream);
+
+/*
  * la_delta_rule -- the delta-rule memory ([LA] "Delta rule：先读旧答案，再写误差"): a
  * state without the normaliser that, per token, reads its current answer for the
  * key, writes back beta times the error, and is then read by the query:

@@ -182,6 +182,39 @@ def decode_step(q, k, v, S, z, alpha=None, eps=1e-6, y=None):
     return y
 
 
+def prefill_backward(q, k, v, y, dy, alpha=None, S0=None, z0=None, dS_T=None, dz_T=None, eps=1e-6, workspace=None):
+    """Gradients of prefill_chunked: given the forward inputs, its output y and
+    dy [B,H,T,dv] (and optionally dS_T [B,H,r,dv], dz_T [B,H,r] in fp32), returns
+    (dq, dk, dv, dalpha or None, dS0, dz0); dq, dk, dv in the input dtype."""
+    if q.dtype not in _DTYPES:
+        raise ValueError(f"unsupported dtype {q.dtype}")
+    B, H, T, r = q.shape
+    dvd = v.shape[3]
+    dev = q.device
+    for t, name, shape in ((q, "q", (B, H, T, r)), (k, "k", (B, H, T, r)), (v, "v", (B, H, T, dvd)),
+                           (y, "y", (B, H, T, dvd)), (dy, "dy", (B, H, T, dvd))):
+        _require(t, name, shape, q.dtype, dev)
+    _require(alpha, "alpha", (B, H, T), torch.float32, dev)
+    _require(S0, "S0", (B, H, r, dvd), torch.float32, dev)
+    _require(z0, "z0", (B, H, r), torch.float32, dev)
+    _require(dS_T, "dS_T", (B, H, r, dvd), torch.float32, dev)
+    _require(dz_T, "dz_T", (B, H, r), torch.float32, dev)
+    dq, dk, dv_out = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    dalpha = torch.empty((B, H, T), device=dev, dtype=torch.float32) if alpha is not None else None
+    dS0 = torch.empty((B, H, r, dvd), device=dev, dtype=torch.float32)
+    dz0 = torch.empty((B, H, r), device=dev, dtype=torch.float32)
+    need = int(_native.lib().la_backward_workspace_bytes(B, H, T))
+    if workspace is None:
+        workspace = torch.empty(need, device=dev, dtype=torch.uint8)
+    ws_bytes = workspace.numel() * workspace.element_size()
+    st = _native.lib().la_prefill_backward(
+        _ptr(q), _ptr(k), _ptr(v), _DTYPES[q.dtype], _ptr(alpha), _ptr(S0), _ptr(z0), B, H, T, r, dvd, float(eps),
+        _ptr(y), _ptr(dy), _ptr(dS_T), _ptr(dz_T), _ptr(dq), _ptr(dk), _ptr(dv_out), _ptr(dalpha), _ptr(dS0),
+        _ptr(dz0), _ptr(workspace), ws_bytes, _stream(dev))
+    _native.check(st, "la_prefill_backward")
+    return dq, dk, dv_out, dalpha, dS0, dz0
+
+
 def delta_rule(q, k, v, beta=None, S0=None, y=None, S_out=None):
     """Delta-rule memory: p = S^T k, S += beta k (v - p)^T, y = S^T q (after the write).
     q, k [B,H,T,r], v [B,H,T,dv] (bf16 or fp32, same dtype); beta [B,H,T] fp32 or

@@ -361,6 +361,44 @@ la_status la_decode_step(const void *q, const void *k, const void *v, la_dtype d
                                        reinterpret_cast<cudaStream_t>(stream)));
 }
 
+size_t la_backward_workspace_bytes(int B, int H, int T)
+{
+    if (B < 1 || H < 1 || T < 1) return 0;
+    return sizeof(float) * la::backward_workspace_floats(B, H, T);
+}
+
+la_status la_prefill_backward(const void *q, const void *k, const void *v, la_dtype dtype, const float *alpha,
+                              const float *S0, const float *z0, int B, int H, int T, int r, int dv, float eps,
+                              const void *y, const void *dy, const float *dS_T, const float *dz_T, void *dq,
+                              void *dk, void *dv_out, float *dalpha, float *dS0, float *dz0, void *workspace,
+                              size_t workspace_bytes, la_stream_t stream)
+{
+    if (!q || !k || !v || !y || !dy || !dq || !dk || !dv_out || !dS0 || !dz0) return LA_ERR_NULL;
+    if (B < 1 || H < 1 || T < 1 || r < 1 || dv < 1) return LA_ERR_SHAPE;
+    if (dtype != LA_DTYPE_BF16 && dtype != LA_DTYPE_FP32) return LA_ERR_DTYPE;
+    if ((r != 32 && r != 64 && r != 128) || (dv != 32 && dv != 64 && dv != 128)) return LA_ERR_UNSUPPORTED;
+    if ((long long)B * H * 4 > 0x7fffffffLL) return LA_ERR_UNSUPPORTED;
+    // token arrays are staged by TMA bulk copies and written 16 bytes at a time
+    for (const void *p : {q, k, v, y, dy, (const void *)dq, (const void *)dk, (const void *)dv_out})
+        if (!aligned(p, 16)) return LA_ERR_ALIGN;
+    for (const void *p : {(const void *)alpha, (const void *)S0, (const void *)z0, (const void *)dz_T,
+                          (const void *)dalpha, (const void *)dS0, (const void *)dz0})
+        if (p && !aligned(p, 4)) return LA_ERR_ALIGN;
+    if (dS_T && !aligned(dS_T, 8)) return LA_ERR_ALIGN;
+    if (!workspace || workspace_bytes < la_backward_workspace_bytes(B, H, T)) return LA_ERR_WORKSPACE;
+    if (!aligned(workspace, 16)) return LA_ERR_ALIGN;
+    la::BackwardArgs a;
+    a.q = q; a.k = k; a.v = v; a.y = y; a.dy = dy;
+    a.alpha = alpha; a.S0 = S0; a.z0 = z0; a.dS_T = dS_T; a.dz_T = dz_T;
+    a.dq = dq; a.dk = dk; a.dv_out = dv_out; a.dalpha = dalpha; a.dS0 = dS0; a.dz0 = dz0;
+    a.ws = static_cast<float *>(workspace);
+    a.H = H; a.T = T; a.r = r; a.dv = dv; a.eps = eps;
+    a.status = status_word();
+    a.limit_ns = la::kWaitLimitNs;
+    if (!a.status) return LA_ERR_CUDA;
+    return from_cuda(la::launch_backward(a, B, dtype == LA_DTYPE_BF16, reinterpret_cast<cudaStream_t>(stream)));
+}
+
 la_status la_delta_rule(const void *q, const void *k, const void *v, la_dtype dtype, const float *beta,
                         const float *S0, int B, int H, int T, int r, int dv, void *y, float *S_out,
                         la_stream_t stream)

@@ -1,0 +1,571 @@
+// backward.cu -- gradients of the gated linear-attention recurrence, in FP32 on
+// CUDA cores.
+//
+// The pages give no backward formula; these kernels apply the chain rule to the
+// recurrence of "Linear attention：把历史写进状态" (hs-black.github.io/posts/linear-attention),
+// sections "公式里的每个维度" and "加一个门：让旧记忆逐渐淡出".  With q~ = phi(q),
+// k~ = phi(k), y_t = n_t / d_t, n_t = S_t^T q~_t, d_t = q~_t . z_t + eps:
+//   dn_t = dy_t / d_t,   dd_t = -(dy_t . y_t) / d_t
+//   G_t = q~_t dn_t^T + alpha_{t+1} G_{t+1},   g_t = dd_t q~_t + alpha_{t+1} g_{t+1}
+//   dq~_t = S_t dn_t + dd_t z_t,   dk~_t = G_t v_t + g_t,   dv_t = G_t^T k~_t
+//   dS0 = alpha_1 G_1,   dz0 = alpha_1 g_1
+// and, for the gates, with A_t the running sum of log alpha (the state terms
+// depend on alpha only through e^{A_t} on the read side and e^{-A_s} on the
+// write side):
+//   dL/d log alpha_u = sum_{t >= u} (q~_t . dq~_t - k~_t . dk~_t) + <dS_T, S_T> + <dz_T, z_T>.
+//
+// Each of dq, dk and dv is a gated rank-1 recurrence with a read that does not
+// feed back into the state, so the three are one kernel in three modes:
+//   kFwdDq: forward in time, one column per feature i, state S[i, :] and z_i;
+//   kRevDk: reverse in time, one column per feature i, state G[i, :] and g_i;
+//   kRevDv: reverse in time, one column per value j, state G[:, j].
+// A CTA holds 32 columns; a lane holds L/8 state rows of two columns, the row
+// groups interleaved in blocks of 4 as in the delta-rule kernel, and reduces its
+// two reads over the 8 row groups with three shuffles.  Tokens come 32 at a
+// time: the TMA unit copies a block's two vector rows (contiguous) and its two
+// column slices into a double-buffered raw stage two blocks ahead, and the CTA
+// converts a landed block once to FP32, already transformed (phi, dy / d_t).
+
+#include "tc_common.cuh"
+
+#include <cuda_bf16.h>
+
+namespace la {
+namespace {
+
+constexpr int kBT = 32;          // tokens per staged block
+constexpr int kBWarps = 4;
+constexpr int kBThreads = 32 * kBWarps;
+constexpr int kBCols = 32;       // columns per CTA
+
+enum Mode { kFwdDq = 0, kRevDk = 1, kRevDv = 2 };
+
+__device__ __forceinline__ float ld_in(const float *p, size_t i) { return p[i]; }
+__device__ __forceinline__ float ld_in(const __nv_bfloat16 *p, size_t i) { return __bfloat162float(p[i]); }
+
+__device__ __forceinline__ float phi_f(float x) { return x > 0.f ? x + 1.f : expf(x); }
+__device__ __forceinline__ float dphi_f(float x) { return x > 0.f ? 1.f : expf(x); }
+
+__device__ __forceinline__ float2 lo2(float4 a) { return make_float2(a.x, a.y); }
+__device__ __forceinline__ float2 hi2(float4 a) { return make_float2(a.z, a.w); }
+
+// ------------------------------------------------------------ d_t and dd_t
+
+// One CTA of 128 threads per (b, h), one thread per feature (r <= 128): z_t by
+// the recurrence, then per block of tokens the sums over features (q~_t . z_t)
+// and over values (dy_t . y_t) through shared memory.  A block's loads are all
+// issued before its z chain runs.
+template <typename Tin>
+__global__ void __launch_bounds__(128)
+bwd_prep_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k, const float *__restrict__ alpha,
+                const float *__restrict__ z0, const Tin *__restrict__ y, const Tin *__restrict__ dy, int T, int r,
+                int dv, float eps, float *__restrict__ d_out, float *__restrict__ dd_out)
+{
+    constexpr int kV = 16 / (int)sizeof(Tin);   // elements per 16-byte load
+    __shared__ float part[kBT][129];            // [token][feature, or 16-byte chunk of the value row]
+    __shared__ float sa[kBT], den[kBT];
+    const int bh = blockIdx.x, i = threadIdx.x;
+    float z = (z0 && i < r) ? z0[(size_t)bh * r + i] : 0.f;
+    for (int t0 = 0; t0 < T; t0 += kBT) {
+        const int nt = min(kBT, T - t0);
+        float kk[kBT], qq[kBT];
+#pragma unroll
+        for (int t = 0; t < kBT; ++t) {
+            kk[t] = qq[t] = 0.f;
+            if (t < nt && i < r) {
+                const size_t row = ((size_t)bh * T + t0 + t) * r + i;
+                kk[t] = ld_in(k, row);
+                qq[t] = ld_in(q, row);
+            }
+        }
+        if (i < nt) sa[i] = alpha ? alpha[(size_t)bh * T + t0 + i] : 1.f;
+        __syncthreads();
+        if (i < r) {
+#pragma unroll
+            for (int t = 0; t < kBT; ++t)
+                if (t < nt) {
+                    z = sa[t] * z + phi_f(kk[t]);
+                    part[t][i] = phi_f(qq[t]) * z;
+                }
+        }
+        __syncthreads();
+        // d_t = sum over features + eps, 8 threads per token
+        for (int t = i >> 3; t < kBT; t += 16) {
+            float s = 0.f;
+            if (t < nt)
+                for (int f = i & 7; f < r; f += 8) s += part[t][f];
+            s += __shfl_xor_sync(0xffffffffu, s, 1);
+            s += __shfl_xor_sync(0xffffffffu, s, 2);
+            s += __shfl_xor_sync(0xffffffffu, s, 4);
+            if ((i & 7) == 0) den[t] = s + eps;
+        }
+        __syncthreads();
+        // dy_t . y_t, one 16-byte chunk of both rows per step
+        const int nch = dv / kV;
+#pragma unroll 4
+        for (int c = i; c < nt * nch; c += 128) {
+            const int t = c / nch, ch = c - t * nch;
+            const size_t off = ((size_t)bh * T + t0 + t) * dv + (size_t)ch * kV;
+            const uint4 a = *reinterpret_cast<const uint4 *>(dy + off), b = *reinterpret_cast<const uint4 *>(y + off);
+            float s = 0.f;
+            if constexpr (sizeof(Tin) == 2) {
+                const uint32_t ua[4] = {a.x, a.y, a.z, a.w}, ub[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) s += bf16_lo(ua[e]) * bf16_lo(ub[e]) + bf16_hi(ua[e]) * bf16_hi(ub[e]);
+            } else {
+                s = __uint_as_float(a.x) * __uint_as_float(b.x) + __uint_as_float(a.y) * __uint_as_float(b.y) +
+                    __uint_as_float(a.z) * __uint_as_float(b.z) + __uint_as_float(a.w) * __uint_as_float(b.w);
+            }
+            part[t][ch] = s;
+        }
+        __syncthreads();
+        for (int t = i >> 3; t < kBT; t += 16) {
+            float s = 0.f;
+            if (t < nt)
+                for (int f = i & 7; f < nch; f += 8) s += part[t][f];
+            s += __shfl_xor_sync(0xffffffffu, s, 1);
+            s += __shfl_xor_sync(0xffffffffu, s, 2);
+            s += __shfl_xor_sync(0xffffffffu, s, 4);
+            if (t < nt && (i & 7) == 0) {
+                d_out[(size_t)bh * T + t0 + t] = den[t];
+                dd_out[(size_t)bh * T + t0 + t] = -s / den[t];
+            }
+        }
+        __syncthreads();
+    }
+}
+
+// ------------------------------------------------------- the three sweeps
+
+template <typename Tin, int L>
+struct RecSmem {
+    // raw stages, written by the TMA unit: the block's rows of the two vector
+    // sources, and its slices of the two column sources
+    Tin rb[2][kBT][L];
+    Tin rw[2][kBT][L];
+    Tin ra[2][kBT][kBCols];
+    Tin rx[2][kBT][kBCols];
+    // the converted block
+    float b[kBT][L];        // the rank-1 write's vector (b_t)
+    float w[kBT][L];        // the read's vector (w_t)
+    float a[kBT][kBCols];   // the write's per-column coefficient
+    float x[kBT][kBCols];   // the column's own q or k (dq, dk: for phi and phi')
+    float o[kBT][kBCols];   // outputs of the block
+    float gam[kBT];         // gate applied to the state before this token's write
+    float dd[kBT];          // dd_t
+    float invd[kBT];        // 1 / d_t
+    float sum[kBT];         // per-token sum over this CTA's columns (dalpha terms)
+    uint64_t full[2];
+    int flag;
+};
+
+struct RecArgs {
+    const void *q, *k, *v, *dy;
+    const float *alpha, *S0, *z0, *dS_T, *dz_T, *d, *dd;
+    void *out;              // dq, dk or dv
+    float *tok_sum;         // [B*H*T] dalpha terms (atomic adds), kFwdDq and kRevDk
+    float *fin;             // [B*H] <dS_T, S_T> + <dz_T, z_T>, kFwdDq
+    float *dS0, *dz0;       // kRevDk
+    int *status;
+    unsigned long long limit_ns;
+    int H, T, r, dv;
+};
+
+enum Op { kPlain = 0, kPhi = 1, kScale = 2 };
+
+// nrows rows of W elements (row stride W in both) from a raw block to FP32,
+// transformed by op (kScale: times invd[row]); 8 (BF16) or 4 (FP32) per step.
+template <typename Tin, int W, int op>
+__device__ __forceinline__ void convert(const Tin *src, float *dst, int nrows, const float *invd)
+{
+    constexpr int kV = 16 / (int)sizeof(Tin), nch = W / kV;
+    for (int c = threadIdx.x; c < nrows * nch; c += kBThreads) {
+        const int t = c / nch;
+        const uint4 u = reinterpret_cast<const uint4 *>(src)[c];
+        float f[kV];
+        if constexpr (sizeof(Tin) == 2) {
+            const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                f[2 * e] = bf16_lo(w4[e]);
+                f[2 * e + 1] = bf16_hi(w4[e]);
+            }
+        } else {
+            f[0] = __uint_as_float(u.x); f[1] = __uint_as_float(u.y);
+            f[2] = __uint_as_float(u.z); f[3] = __uint_as_float(u.w);
+        }
+        const float s = op == kScale ? invd[t] : 1.f;
+#pragma unroll
+        for (int e = 0; e < kV; ++e) f[e] = op == kPhi ? phi_f(f[e]) : (op == kScale ? f[e] * s : f[e]);
+#pragma unroll
+        for (int e = 0; e < kV; e += 4)
+            *reinterpret_cast<float4 *>(dst + (size_t)c * kV + e) = make_float4(f[e], f[e + 1], f[e + 2], f[e + 3]);
+    }
+}
+
+__device__ __forceinline__ void store8(__nv_bfloat16 *p, const float *f)
+{
+    *reinterpret_cast<uint4 *>(p) = make_uint4(pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]),
+                                               pack_bf16x2(f[4], f[5]), pack_bf16x2(f[6], f[7]));
+}
+__device__ __forceinline__ void store8(float *p, const float *f)
+{
+    reinterpret_cast<float4 *>(p)[0] = make_float4(f[0], f[1], f[2], f[3]);
+    reinterpret_cast<float4 *>(p)[1] = make_float4(f[4], f[5], f[6], f[7]);
+}
+
+template <typename Tin, int Mode, int L>
+__global__ void __launch_bounds__(kBThreads)
+rec_kernel(RecArgs p)
+{
+    constexpr int F = L / 32;                   // float4 row blocks per lane
+    constexpr int kEl = (int)sizeof(Tin);
+    extern __shared__ __align__(16) unsigned char smem_raw[];
+    RecSmem<Tin, L> &sm = *reinterpret_cast<RecSmem<Tin, L> *>(smem_raw);
+    const int T = p.T, r = p.r, dv = p.dv;
+    const int ncol_total = Mode == kRevDv ? dv : r;
+    const int nslice = ncol_total / kBCols;
+    const int bh = blockIdx.x / nslice, c0 = (blockIdx.x % nslice) * kBCols;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int g = lane >> 2, jj = lane & 3;
+    const int jl = warp * 8 + 2 * jj;           // first of the lane's two columns (local)
+    const int b4 = (lane >> 4) & 1;             // which of the two columns this lane's total is for
+    const bool writer = (lane & 12) == 0;
+    const Tin *qi = static_cast<const Tin *>(p.q), *ki = static_cast<const Tin *>(p.k);
+    const Tin *vi = static_cast<const Tin *>(p.v), *dyi = static_cast<const Tin *>(p.dy);
+    Tin *out = static_cast<Tin *>(p.out);
+    // the sources of the staged arrays
+    const Tin *srcB = Mode == kFwdDq ? vi : (Mode == kRevDk ? dyi : qi);   // rows of length L
+    const Tin *srcW = Mode == kFwdDq ? dyi : (Mode == kRevDk ? vi : ki);
+    const Tin *srcA = Mode == kFwdDq ? ki : (Mode == kRevDk ? qi : dyi);   // rows of length ncol_total
+    const Tin *srcX = Mode == kFwdDq ? qi : ki;
+    const int nblk = (T + kBT - 1) / kBT;
+    auto block_of = [&](int bi) { return Mode == kFwdDq ? bi : nblk - 1 - bi; };
+    Ctx cx{&sm.flag, p.limit_ns, p.status};
+
+    if (tid == 0) {
+        mbar_init(&sm.full[0], 1);
+        mbar_init(&sm.full[1], 1);
+        sm.flag = 0;
+        fence_mbarrier_init();
+    }
+    __syncthreads();
+
+    // Warp 0 starts the copies of the bi-th block in processing order into stage bi & 1.
+    auto issue = [&](int bi) {
+        const int st = bi & 1, t0 = block_of(bi) * kBT, nt = min(kBT, T - t0);
+        const size_t tok0 = (size_t)bh * T + t0;
+        const uint32_t rowbytes = (uint32_t)(nt * L * kEl), colbytes = (uint32_t)(kBCols * kEl);
+        const uint32_t ncolsrc = Mode == kRevDv ? 1u : 2u;
+        if (lane == 0) mbar_arrive_expect_tx(&sm.full[st], 2 * rowbytes + ncolsrc * nt * colbytes);
+        __syncwarp();
+        if (lane == 0) bulk_load(&sm.rb[st][0][0], srcB + tok0 * L, rowbytes, &sm.full[st]);
+        if (lane == 1) bulk_load(&sm.rw[st][0][0], srcW + tok0 * L, rowbytes, &sm.full[st]);
+        if (lane < nt) {
+            const size_t off = (tok0 + lane) * (size_t)ncol_total + c0;
+            bulk_load(&sm.ra[st][lane][0], srcA + off, colbytes, &sm.full[st]);
+            if (Mode != kRevDv) bulk_load(&sm.rx[st][lane][0], srcX + off, colbytes, &sm.full[st]);
+        }
+    };
+    if (warp == 0) {
+        if (nblk > 0) issue(0);
+        if (nblk > 1) issue(1);
+    }
+    // per-token scalars of the bi-th block, one token per thread of warp 0
+    struct Scalars { float gam, dd, invd; };
+    auto fetch = [&](int bi) -> Scalars {
+        const int t0 = block_of(bi) * kBT, nt = min(kBT, T - t0);
+        Scalars sc{1.f, 0.f, 1.f};
+        if (tid < nt) {
+            const size_t tok = (size_t)bh * T + t0 + tid;
+            // forward: alpha_t acts before token t's write; reverse: alpha_{t+1} (1 after the last token)
+            const int ta = Mode == kFwdDq ? t0 + tid : t0 + tid + 1;
+            sc.gam = (p.alpha && ta < T) ? p.alpha[(size_t)bh * T + ta] : 1.f;
+            sc.dd = Mode == kRevDv ? 0.f : p.dd[tok];
+            sc.invd = 1.f / p.d[tok];
+        }
+        return sc;
+    };
+    Scalars sc = fetch(0);
+
+    // state: X[m][c][h] holds rows 4 (8 m + g) + 2h, + 1 of column c0 + jl + c
+    float2 X[F][2][2];
+    float e[2] = {0.f, 0.f};                    // z_i (kFwdDq) or g_i (kRevDk) of the two columns
+#pragma unroll
+    for (int m = 0; m < F; ++m)
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int row = 4 * (8 * m + g) + 2 * h;
+            float2 u = make_float2(0.f, 0.f), w2 = u;   // (row, columns 0/1), (row + 1, ...)
+            const float *s0 = Mode == kFwdDq ? p.S0 : p.dS_T;
+            if (s0 && Mode != kRevDv) {
+                // state of column (feature) c = row c of S0 or dS_T, length dv
+                const float *s = s0 + (size_t)bh * r * dv;
+                u = make_float2(s[(size_t)(c0 + jl) * dv + row], s[(size_t)(c0 + jl + 1) * dv + row]);
+                w2 = make_float2(s[(size_t)(c0 + jl) * dv + row + 1], s[(size_t)(c0 + jl + 1) * dv + row + 1]);
+            } else if (s0) {
+                // state of column (value) c = column c of dS_T, length r
+                const float *s = s0 + (size_t)bh * r * dv;
+                u = *reinterpret_cast<const float2 *>(s + (size_t)row * dv + c0 + jl);
+                w2 = *reinterpret_cast<const float2 *>(s + (size_t)(row + 1) * dv + c0 + jl);
+            }
+            X[m][0][h] = make_float2(u.x, w2.x);
+            X[m][1][h] = make_float2(u.y, w2.y);
+        }
+    {
+        const float *e0 = Mode == kFwdDq ? p.z0 : (Mode == kRevDk ? p.dz_T : nullptr);
+        if (e0) {
+            e[0] = e0[(size_t)bh * r + c0 + jl];
+            e[1] = e0[(size_t)bh * r + c0 + jl + 1];
+        }
+    }
+
+    // the outputs of a processed block: 8 columns per step, and the dalpha terms
+    auto flush = [&](int bi) {
+        const int t0 = block_of(bi) * kBT, nt = min(kBT, T - t0);
+        for (int c = tid; c < nt * (kBCols / 8); c += kBThreads) {
+            const int t = c / (kBCols / 8), ch = (c % (kBCols / 8)) * 8;
+            store8(out + ((size_t)bh * T + t0 + t) * ncol_total + c0 + ch, &sm.o[t][ch]);
+        }
+        if (Mode != kRevDv && tid < nt) {
+            const float v = sm.sum[tid];
+            atomicAdd(&p.tok_sum[(size_t)bh * T + t0 + tid], Mode == kFwdDq ? v : -v);
+        }
+    };
+
+    int bi = 0;
+    for (; bi < nblk; ++bi) {
+        const int st = bi & 1, nt = min(kBT, T - block_of(bi) * kBT);
+        const bool ok = wait(cx, &sm.full[st], (bi >> 1) & 1);
+        if (__syncthreads_or(!ok)) break;   // also: the previous block's compute has finished
+        if (bi > 0) flush(bi - 1);
+        if (tid < kBT) {
+            sm.gam[tid] = sc.gam;
+            sm.dd[tid] = sc.dd;
+            sm.invd[tid] = sc.invd;
+            sm.sum[tid] = 0.f;
+        }
+        __syncthreads();
+        convert<Tin, L, Mode == kRevDv ? kPhi : (Mode == kRevDk ? kScale : kPlain)>(&sm.rb[st][0][0], &sm.b[0][0], nt,
+                                                                                     sm.invd);
+        convert<Tin, L, Mode == kRevDv ? kPhi : (Mode == kFwdDq ? kScale : kPlain)>(&sm.rw[st][0][0], &sm.w[0][0], nt,
+                                                                                     sm.invd);
+        convert<Tin, kBCols, Mode == kRevDv ? kScale : kPhi>(&sm.ra[st][0][0], &sm.a[0][0], nt, sm.invd);
+        if (Mode != kRevDv) convert<Tin, kBCols, kPlain>(&sm.rx[st][0][0], &sm.x[0][0], nt, sm.invd);
+        __syncthreads();                    // FP32 block ready; the raw stage is free again
+        if (warp == 0 && bi + 2 < nblk) issue(bi + 2);
+        if (bi + 1 < nblk) sc = fetch(bi + 1);
+
+#pragma unroll 2
+        for (int s = 0; s < nt; ++s) {
+            const int t = Mode == kFwdDq ? s : nt - 1 - s;
+            const float gm = sm.gam[t];
+            const float2 a0 = make_float2(sm.a[t][jl], sm.a[t][jl]), a1 = make_float2(sm.a[t][jl + 1], sm.a[t][jl + 1]);
+            const float4 *br = reinterpret_cast<const float4 *>(&sm.b[t][0]) + g;
+            const float4 *wr = reinterpret_cast<const float4 *>(&sm.w[t][0]) + g;
+            float2 r0a = make_float2(0.f, 0.f), r0b = r0a, r1a = r0a, r1b = r0a;
+            if (p.alpha) {
+                const float2 g2 = make_float2(gm, gm);
+#pragma unroll
+                for (int m = 0; m < F; ++m) {
+                    const float4 bb = br[8 * m], ww = wr[8 * m];
+                    X[m][0][0] = __ffma2_rn(lo2(bb), a0, __fmul2_rn(X[m][0][0], g2));
+                    X[m][0][1] = __ffma2_rn(hi2(bb), a0, __fmul2_rn(X[m][0][1], g2));
+                    X[m][1][0] = __ffma2_rn(lo2(bb), a1, __fmul2_rn(X[m][1][0], g2));
+                    X[m][1][1] = __ffma2_rn(hi2(bb), a1, __fmul2_rn(X[m][1][1], g2));
+                    r0a = __ffma2_rn(X[m][0][0], lo2(ww), r0a);
+                    r0b = __ffma2_rn(X[m][0][1], hi2(ww), r0b);
+                    r1a = __ffma2_rn(X[m][1][0], lo2(ww), r1a);
+                    r1b = __ffma2_rn(X[m][1][1], hi2(ww), r1b);
+                }
+            } else {
+#pragma unroll
+                for (int m = 0; m < F; ++m) {
+                    const float4 bb = br[8 * m], ww = wr[8 * m];
+                    X[m][0][0] = __ffma2_rn(lo2(bb), a0, X[m][0][0]);
+                    X[m][0][1] = __ffma2_rn(hi2(bb), a0, X[m][0][1]);
+                    X[m][1][0] = __ffma2_rn(lo2(bb), a1, X[m][1][0]);
+                    X[m][1][1] = __ffma2_rn(hi2(bb), a1, X[m][1][1]);
+                    r0a = __ffma2_rn(X[m][0][0], lo2(ww), r0a);
+                    r0b = __ffma2_rn(X[m][0][1], hi2(ww), r0b);
+                    r1a = __ffma2_rn(X[m][1][0], lo2(ww), r1a);
+                    r1b = __ffma2_rn(X[m][1][1], hi2(ww), r1b);
+                }
+            }
+            // the scalar recurrences: z_i += k~ (forward), g_i += dd q~ (reverse dk)
+            if (Mode == kFwdDq) {
+                e[0] = fmaf(gm, e[0], a0.x);
+                e[1] = fmaf(gm, e[1], a1.x);
+            } else if (Mode == kRevDk) {
+                const float ddt = sm.dd[t];
+                e[0] = fmaf(gm, e[0], ddt * a0.x);
+                e[1] = fmaf(gm, e[1], ddt * a1.x);
+            }
+            const float2 s0 = __fadd2_rn(r0a, r0b), s1 = __fadd2_rn(r1a, r1b);
+            // reduce over the 8 row groups: bit 4 keeps column b4, then bits 3 and 2
+            float kept = b4 ? s1.x + s1.y : s0.x + s0.y;
+            const float sent = b4 ? s0.x + s0.y : s1.x + s1.y;
+            kept += __shfl_xor_sync(0xffffffffu, sent, 16);
+            kept += __shfl_xor_sync(0xffffffffu, kept, 8);
+            kept += __shfl_xor_sync(0xffffffffu, kept, 4);
+            const int c = jl + b4;
+            if (Mode == kRevDv) {                   // dv = G_t^T k~_t
+                if (writer) sm.o[t][c] = kept;
+            } else {
+                // dq~ = S_t dn_t + dd_t z_t, or dk~ = G_t v_t + g_t
+                const float ec = b4 ? e[1] : e[0];
+                const float dt = Mode == kFwdDq ? kept + sm.dd[t] * ec : kept + ec;
+                const float xv = sm.x[t][c];
+                if (writer) sm.o[t][c] = dt * dphi_f(xv);
+                // q~ . dq~ (or k~ . dk~) over the warp's 8 columns: the writers hold
+                // distinct columns and differ in lane bits 0, 1 and 4
+                float ts = writer ? phi_f(xv) * dt : 0.f;
+                ts += __shfl_xor_sync(0xffffffffu, ts, 1);
+                ts += __shfl_xor_sync(0xffffffffu, ts, 2);
+                ts += __shfl_xor_sync(0xffffffffu, ts, 16);
+                if (lane == 0) atomicAdd(&sm.sum[t], ts);
+            }
+        }
+    }
+
+    if (bi < nblk) {
+        // gave up waiting: let the copies already started land before the CTA exits
+        if (tid == 0)
+            for (int bb = bi; bb < nblk && bb < bi + 2; ++bb) mbar_wait(&sm.full[bb & 1], (bb >> 1) & 1, p.limit_ns);
+        __syncthreads();
+        return;
+    }
+    __syncthreads();
+    if (nblk > 0) flush(nblk - 1);
+
+    // final state terms
+    if (Mode == kFwdDq && (p.dS_T || p.dz_T)) {
+        // <dS_T, S_T> + <dz_T, z_T> over this CTA's rows of S
+        float acc = 0.f;
+        if (p.dS_T) {
+            const float *s = p.dS_T + (size_t)bh * r * dv;
+#pragma unroll
+            for (int m = 0; m < F; ++m)
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const int row = 4 * (8 * m + g) + 2 * h;
+#pragma unroll
+                    for (int c = 0; c < 2; ++c) {
+                        acc += X[m][c][h].x * s[(size_t)(c0 + jl + c) * dv + row];
+                        acc += X[m][c][h].y * s[(size_t)(c0 + jl + c) * dv + row + 1];
+                    }
+                }
+        }
+        if (p.dz_T && g == 0)   // one lane per column pair adds z
+            acc += e[0] * p.dz_T[(size_t)bh * r + c0 + jl] + e[1] * p.dz_T[(size_t)bh * r + c0 + jl + 1];
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+        if (lane == 0) atomicAdd(&p.fin[bh], acc);
+    }
+    if (Mode == kRevDk) {
+        // dS0 = alpha_1 G_1, dz0 = alpha_1 g_1 (alpha_1: the first token's gate)
+        const float a1 = p.alpha ? p.alpha[(size_t)bh * T] : 1.f;
+        float *s = p.dS0 + (size_t)bh * r * dv;
+#pragma unroll
+        for (int m = 0; m < F; ++m)
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const int row = 4 * (8 * m + g) + 2 * h;
+#pragma unroll
+                for (int c = 0; c < 2; ++c) {
+                    s[(size_t)(c0 + jl + c) * dv + row] = a1 * X[m][c][h].x;
+                    s[(size_t)(c0 + jl + c) * dv + row + 1] = a1 * X[m][c][h].y;
+                }
+            }
+        if (g == 0) {
+            p.dz0[(size_t)bh * r + c0 + jl] = a1 * e[0];
+            p.dz0[(size_t)bh * r + c0 + jl + 1] = a1 * e[1];
+        }
+    }
+}
+
+// ------------------------------------------------------------------ dalpha
+
+// One warp per (b, h): dlog alpha_u = sum_{t >= u} tok_sum[t] + fin, then
+// dalpha_u = dlog alpha_u / alpha_u.  The reverse running sum goes 32 tokens at a
+// time (a warp scan), from the end of the sequence.
+__global__ void bwd_dalpha_kernel(const float *__restrict__ tok_sum, const float *__restrict__ fin,
+                                  const float *__restrict__ alpha, int T, int BH, float *__restrict__ dalpha)
+{
+    const int bh = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5), lane = threadIdx.x & 31;
+    if (bh >= BH) return;
+    float carry = fin[bh];
+    for (int t0 = ((T - 1) / 32) * 32; t0 >= 0; t0 -= 32) {
+        const int t = t0 + 31 - lane;             // lane 0 takes the latest token of the group
+        float x = t < T ? tok_sum[(size_t)bh * T + t] : 0.f;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const float y = __shfl_up_sync(0xffffffffu, x, o);
+            if (lane >= o) x += y;
+        }
+        const float total = __shfl_sync(0xffffffffu, x, 31);
+        if (t < T) dalpha[(size_t)bh * T + t] = (x + carry) / alpha[(size_t)bh * T + t];
+        carry += total;
+    }
+}
+
+template <typename Tin, int Mode>
+cudaError_t launch_rec(const RecArgs &a, int B, int L, cudaStream_t stream)
+{
+    const int ncol = Mode == kRevDv ? a.dv : a.r;
+    const unsigned grid = (unsigned)((long long)B * a.H * (ncol / kBCols));
+    auto go = [&](auto kern, size_t bytes) -> cudaError_t {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+        if (e != cudaSuccess) return e;
+        kern<<<grid, kBThreads, bytes, stream>>>(a);
+        return cudaGetLastError();
+    };
+    switch (L) {
+    case 32: return go(rec_kernel<Tin, Mode, 32>, sizeof(RecSmem<Tin, 32>));
+    case 64: return go(rec_kernel<Tin, Mode, 64>, sizeof(RecSmem<Tin, 64>));
+    case 128: return go(rec_kernel<Tin, Mode, 128>, sizeof(RecSmem<Tin, 128>));
+    default: return cudaErrorInvalidValue;
+    }
+}
+
+template <typename Tin>
+cudaError_t launch_bwd_t(const BackwardArgs &a, int B, cudaStream_t stream)
+{
+    const int BH = B * a.H;
+    const size_t n = (size_t)BH * a.T;
+    float *d = a.ws, *dd = d + n, *tok_sum = dd + n, *fin = tok_sum + n;
+    cudaError_t e = cudaMemsetAsync(tok_sum, 0, sizeof(float) * (n + BH), stream);
+    if (e != cudaSuccess) return e;
+    bwd_prep_kernel<Tin><<<BH, 128, 0, stream>>>(
+        static_cast<const Tin *>(a.q), static_cast<const Tin *>(a.k), a.alpha, a.z0, static_cast<const Tin *>(a.y),
+        static_cast<const Tin *>(a.dy), a.T, a.r, a.dv, a.eps, d, dd);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    RecArgs p;
+    p.q = a.q; p.k = a.k; p.v = a.v; p.dy = a.dy;
+    p.alpha = a.alpha; p.S0 = a.S0; p.z0 = a.z0; p.dS_T = a.dS_T; p.dz_T = a.dz_T; p.d = d; p.dd = dd;
+    p.tok_sum = tok_sum; p.fin = fin; p.dS0 = a.dS0; p.dz0 = a.dz0;
+    p.status = a.status; p.limit_ns = a.limit_ns;
+    p.H = a.H; p.T = a.T; p.r = a.r; p.dv = a.dv;
+    p.out = a.dq;
+    if ((e = launch_rec<Tin, kFwdDq>(p, B, a.dv, stream)) != cudaSuccess) return e;
+    p.out = a.dk;
+    if ((e = launch_rec<Tin, kRevDk>(p, B, a.dv, stream)) != cudaSuccess) return e;
+    p.out = a.dv_out;
+    if ((e = launch_rec<Tin, kRevDv>(p, B, a.r, stream)) != cudaSuccess) return e;
+    if (a.alpha && a.dalpha) {
+        bwd_dalpha_kernel<<<(BH + 3) / 4, 128, 0, stream>>>(tok_sum, fin, a.alpha, a.T, BH, a.dalpha);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    }
+    return cudaSuccess;
+}
+
+}  // namespace
+
+size_t backward_workspace_floats(int B, int H, int T) { return (size_t)B * H * ((size_t)3 * T + 1); }
+
+cudaError_t launch_backward(const BackwardArgs &a, int B, bool bf16, cudaStream_t stream)
+{
+    return bf16 ? launch_bwd_t<__nv_bfloat16>(a, B, stream) : launch_bwd_t<float>(a, B, stream);
+}
+
+}  // namespace la

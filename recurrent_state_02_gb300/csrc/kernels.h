@@ -83,6 +83,23 @@ cudaError_t launch_delta(const void *q, const void *k, const void *v, bool bf16,
                          int B, int H, int T, int r, int dv, void *y, float *S_out, int *status,
                          unsigned long long limit_ns, cudaStream_t stream);
 
+// Gradients of the gated recurrence (FP32 on CUDA cores): r, dv in {32, 64, 128};
+// q, k, v, y, dy, dq, dk, dv_out 16-byte aligned.
+struct BackwardArgs {
+    const void *q, *k, *v, *y, *dy;             // [B,H,T,r] / [B,H,T,dv], element type per bf16 flag
+    const float *alpha, *S0, *z0, *dS_T, *dz_T; // optional (nullptr)
+    void *dq, *dk, *dv_out;                     // [B,H,T,r], [B,H,T,r], [B,H,T,dv]
+    float *dalpha;                              // [B,H,T] (with alpha)
+    float *dS0, *dz0;                           // [B,H,r,dv], [B,H,r]
+    float *ws;                                  // backward_workspace_floats(B, H, T) floats
+    int H, T, r, dv;
+    float eps;
+    int *status;                                // device status word
+    unsigned long long limit_ns;
+};
+size_t backward_workspace_floats(int B, int H, int T);
+cudaError_t launch_backward(const BackwardArgs &a, int B, bool bf16, cudaStream_t stream);
+
 cudaError_t launch_state_init(float *S, float *z, long long n_S, long long n_z, cudaStream_t stream);
 
 cudaError_t launch_wait_probe(int *status, unsigned long long limit_ns, cudaStream_t stream);

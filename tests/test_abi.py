@@ -165,3 +165,27 @@ def test_delta_rejects_bad_arguments(native):
     assert f(beta=FAKE + 2) == native.LA_ERR_ALIGN
     assert f(S0=FAKE + 4) == native.LA_ERR_ALIGN
     assert f(S_out=FAKE + 4) == native.LA_ERR_ALIGN
+
+
+def test_backward_rejects_bad_arguments(native):
+    L = native.lib()
+
+    def f(**kw):
+        a = dict(q=FAKE, dtype=native.LA_DTYPE_BF16, alpha=None, B=1, H=1, T=64, r=128, dv=128, y=FAKE, dS_T=None,
+                 dalpha=None, dS0=FAKE, ws=FAKE, ws_bytes=1 << 20)
+        a.update(kw)
+        return L.la_prefill_backward(a["q"], FAKE, FAKE, a["dtype"], a["alpha"], None, None, a["B"], a["H"], a["T"],
+                                     a["r"], a["dv"], 1e-6, a["y"], FAKE, a["dS_T"], None, FAKE, FAKE, FAKE,
+                                     a["dalpha"], a["dS0"], FAKE, a["ws"], a["ws_bytes"], None)
+
+    assert f(q=None) == native.LA_ERR_NULL
+    assert f(dS0=None) == native.LA_ERR_NULL
+    assert f(T=0) == native.LA_ERR_SHAPE
+    assert f(dtype=3) == native.LA_ERR_DTYPE
+    assert f(r=96) == native.LA_ERR_UNSUPPORTED
+    assert f(dv=256) == native.LA_ERR_UNSUPPORTED
+    assert f(y=FAKE + 1) == native.LA_ERR_ALIGN
+    assert f(dS_T=FAKE + 4) == native.LA_ERR_ALIGN
+    assert f(ws=None) == native.LA_ERR_WORKSPACE
+    assert f(ws_bytes=16) == native.LA_ERR_WORKSPACE
+    assert L.la_backward_workspace_bytes(4, 16, 4096) == 4 * 4 * 16 * (3 * 4096 + 1)

@@ -1,0 +1,118 @@
+"""Backward pass on the GPU (la_prefill_backward) against the FP64 oracle's gradients
+(oracle.backward, pinned by finite differences in test_backward_oracle.py).
+
+The backward takes the forward's output y; here y comes from the oracle, rounded
+to the I/O type, so that these tests do not depend on the forward kernels.
+Tolerances (max |gpu - ref| / max |ref| per tensor): BF16 inputs 2e-2 (dq, dk,
+dv are rounded to BF16, and dd_t uses the BF16 y); FP32 inputs 1e-4 (FP32
+accumulation over T tokens in three sweeps, and dalpha is formed as a
+difference of running sums divided by alpha)."""
+import numpy as np
+import pytest
+import torch
+
+from conftest import max_rel_err, to_oracle
+
+pytestmark = pytest.mark.gpu
+
+TOL = {torch.float32: 1e-4, torch.bfloat16: 2e-2}
+EPS = 1e-6
+
+
+@pytest.fixture(scope="module")
+def la():
+    from recurrent_state_02_gb300 import build
+    build.build()
+    import recurrent_state_02_gb300 as la_mod
+    assert torch.cuda.is_available()
+    return la_mod
+
+
+def _case(oracle_mod, B, H, T, r, dv, dtype, gated, with_state, seed):
+    from recurrent_state_02_gb300 import workloads as W
+    w = W.Workload("bwd", B=B, H=H, T=T, r=r, dv=dv, dtype=dtype, gated=gated, seed=seed)
+    d = W.prefill_inputs(w, with_state=with_state)
+    g = torch.Generator().manual_seed(seed + 1)
+    d["dy"] = torch.randn((B, H, T, dv), generator=g).to(dtype)
+    d["dS_T"] = torch.randn((B, H, r, dv), generator=g) * 0.1 if with_state else None
+    d["dz_T"] = torch.randn((B, H, r), generator=g) * 0.1 if with_state else None
+    args = [to_oracle(d[n]) for n in ("q", "k", "v")]
+    y, _, _ = oracle_mod.scan(*args, alpha=to_oracle(d["alpha"]), S0=to_oracle(d["S0"]), z0=to_oracle(d["z0"]),
+                              eps=EPS, threads=0)
+    d["y"] = torch.from_numpy(y).to(dtype)
+    ref = oracle_mod.backward(*args, d["dy"].double().numpy(), alpha=to_oracle(d["alpha"]), S0=to_oracle(d["S0"]),
+                              z0=to_oracle(d["z0"]), dS_T=to_oracle(d["dS_T"]), dz_T=to_oracle(d["dz_T"]), eps=EPS,
+                              threads=0)
+    return d, ref
+
+
+def _gpu(la, d):
+    g = {k: (v.cuda() if v is not None else None) for k, v in d.items()}
+    out = la.prefill_backward(g["q"], g["k"], g["v"], g["y"], g["dy"], alpha=g["alpha"], S0=g["S0"], z0=g["z0"],
+                              dS_T=g["dS_T"], dz_T=g["dz_T"], eps=EPS)
+    assert la.last_device_status() == 0
+    return [None if t is None else t.float().cpu().numpy() for t in out]
+
+
+CASES = [
+    # dtype, r, dv, T, gated, with_state
+    (torch.float32, 128, 128, 200, True, True),
+    (torch.float32, 64, 32, 75, False, True),
+    (torch.float32, 32, 64, 33, True, False),
+    (torch.float32, 128, 64, 1, True, True),
+    (torch.bfloat16, 128, 128, 300, True, True),
+    (torch.bfloat16, 128, 128, 97, False, False),
+    (torch.bfloat16, 64, 128, 64, True, True),
+]
+
+
+@pytest.mark.parametrize("dtype,r,dv,T,gated,with_state", CASES,
+                         ids=[f"{str(c[0])[6:]}-r{c[1]}-dv{c[2]}-T{c[3]}-g{int(c[4])}-S{int(c[5])}" for c in CASES])
+def test_backward_parity(la, oracle_mod, dtype, r, dv, T, gated, with_state):
+    d, ref = _case(oracle_mod, 2, 2, T, r, dv, dtype, gated, with_state, seed=300 + r + dv + T)
+    got = _gpu(la, d)
+    names = ("dq", "dk", "dv", "dalpha", "dS0", "dz0")
+    for name, a, b in zip(names, got, ref):
+        if b is None:
+            assert a is None
+            continue
+        assert np.isfinite(a).all(), name
+        err = max_rel_err(a, b)
+        assert err <= TOL[dtype], (name, err)
+
+
+def test_backward_full_size_sampled_heads(la, oracle_mod):
+    """B4 H16 T4096 r = dv = 128 BF16 with a gate, the shape the benchmark times;
+    the oracle recomputes two sampled heads (heads are independent)."""
+    from recurrent_state_02_gb300 import workloads as W
+    w = W.UNGATED.with_(gated=True)
+    d = W.prefill_inputs(w)
+    g = torch.Generator().manual_seed(99)
+    d["dy"] = torch.randn(d["v"].shape, generator=g).to(torch.bfloat16)
+    heads = ((0, 0), (3, 11))
+    refs = {}
+    for b, h in heads:
+        one = {n: (t[b:b + 1, h:h + 1].contiguous() if t is not None else None) for n, t in d.items()}
+        args = [to_oracle(one[n]) for n in ("q", "k", "v")]
+        y, _, _ = oracle_mod.scan(*args, alpha=to_oracle(one["alpha"]), eps=EPS)
+        refs[(b, h)] = (y, oracle_mod.backward(*args, one["dy"].double().numpy(), alpha=to_oracle(one["alpha"]),
+                                               eps=EPS))
+    # y for every head from the GPU forward (the sampled heads are checked against the oracle's y too)
+    gd = {k: (v.cuda() if v is not None else None) for k, v in d.items()}
+    y, _, _ = la.prefill_chunked(gd["q"], gd["k"], gd["v"], alpha=gd["alpha"], eps=EPS)
+    out = la.prefill_backward(gd["q"], gd["k"], gd["v"], y, gd["dy"], alpha=gd["alpha"], eps=EPS)
+    assert la.last_device_status() == 0
+    got = [t.float().cpu().numpy() for t in out]
+    for (b, h), (y_ref, ref) in refs.items():
+        assert max_rel_err(y[b:b + 1, h:h + 1].float().cpu().numpy(), y_ref) <= 2e-2
+        for name, a, r_ in zip(("dq", "dk", "dv", "dalpha", "dS0", "dz0"), got, ref):
+            err = max_rel_err(a[b:b + 1, h:h + 1], r_)
+            assert err <= 2e-2, (name, b, h, err)
+
+
+def test_backward_workspace_errors(la):
+    q = torch.zeros(1, 1, 8, 32, device="cuda")
+    v = torch.zeros(1, 1, 8, 32, device="cuda")
+    small = torch.empty(16, device="cuda", dtype=torch.uint8)
+    with pytest.raises(la.LinAttnError):
+        la.prefill_backward(q, q, v, v, v, workspace=small)
