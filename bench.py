@@ -12,7 +12,8 @@ Each step is replayed as a CUDA graph of its three kernel launches.
 Printed (rank 0, one JSON line): tokens/s of the step, the prefill kernel's
 roofline (algorithmic bytes / mean launch time vs measured HBM bandwidth), the
 decode step on its own workload (B=256, H=16) in GB/s, the delta-rule memory
-on the prefill's shape against the FP32 ALU peak, an end-to-end figure
+on the prefill's shape and the backward pass of the gated prefill, both against
+the FP32 ALU peak, an end-to-end figure
 through the public API with host buffers, clocks sampled during timing, and
 the FP64 CPU oracle timed on the host cores.
 
@@ -61,6 +62,14 @@ def delta_flops(B, H, T, r, dv):
     """Algorithmic FLOPs of one delta-rule launch: per token and head, the read
     S^T k, the rank-1 write and the read S^T q, 2 r dv each."""
     return B * H * T * 6 * r * dv
+
+
+def backward_flops(B, H, T, r, dv, gated):
+    """Algorithmic FLOPs of the backward: per token and head, the state write and
+    the read S_t dn_t for dq (2 r dv each), the write of G and the reads G_t v_t
+    and G_t^T k~_t for dk and dv (2 r dv each), plus the gate's scaling of S and
+    G (r dv each) when gated."""
+    return B * H * T * (10 + (2 if gated else 0)) * r * dv
 
 
 def fp32_alu_peak_tflops(sm_count):
@@ -452,6 +461,48 @@ def run_ours(args, rank, world, local_rank):
                                                      kernel_sources("delta.cu")),
                           "algorithmic_flops_per_launch": delta_flops(xw.B, xw.H, xw.T, xw.r, xw.dv)}}
 
+    # backward pass on the gated shape of the prefill (B=4, H=16, T=4096, BF16,
+    # alpha = sigmoid(N(3,1))): its five launches replayed as one CUDA graph
+    bw = W.UNGATED.with_(gated=True)
+    bin_ = {k: (v.to(dev) if v is not None else None)
+            for k, v in W.prefill_inputs(bw, seed=bw.seed + 11 + 1000 * rank).items()}
+    ybw = torch.empty((bw.B, bw.H, bw.T, bw.dv), device=dev, dtype=torch.bfloat16)
+    Sbw = torch.empty((bw.B, bw.H, bw.r, bw.dv), device=dev, dtype=torch.float32)
+    zbw = torch.empty((bw.B, bw.H, bw.r), device=dev, dtype=torch.float32)
+    dybw = torch.randn((bw.B, bw.H, bw.T, bw.dv), generator=torch.Generator().manual_seed(bw.seed + 12)).to(dev,
+                                                                                                              torch.bfloat16)
+    gq, gk, gv = (torch.empty_like(bin_[n]) for n in ("q", "k", "v"))
+    ga = torch.empty((bw.B, bw.H, bw.T), device=dev, dtype=torch.float32)
+    gS0 = torch.empty((bw.B, bw.H, bw.r, bw.dv), device=dev, dtype=torch.float32)
+    gz0 = torch.empty((bw.B, bw.H, bw.r), device=dev, dtype=torch.float32)
+    wsb = torch.empty(int(L.la_backward_workspace_bytes(bw.B, bw.H, bw.T)), device=dev, dtype=torch.uint8)
+
+    def k_backward():
+        _native.check(L.la_prefill_backward(P(bin_["q"]), P(bin_["k"]), P(bin_["v"]), _native.LA_DTYPE_BF16,
+                                            P(bin_["alpha"]), None, None, bw.B, bw.H, bw.T, bw.r, bw.dv, bw.eps,
+                                            P(ybw), P(dybw), None, None, P(gq), P(gk), P(gv), P(ga), P(gS0), P(gz0),
+                                            P(wsb), wsb.numel(), sh), "la_prefill_backward")
+
+    with torch.cuda.stream(stream):
+        _native.check(L.la_prefill_chunked(P(bin_["q"]), P(bin_["k"]), P(bin_["v"]), _native.LA_DTYPE_BF16,
+                                           P(bin_["alpha"]), None, None, bw.B, bw.H, bw.T, bw.r, bw.dv, bw.chunk,
+                                           bw.eps, P(ybw), P(Sbw), P(zbw), None, 0, sh), "la_prefill_chunked")
+        k_backward()
+    gb = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(gb, stream=stream):
+        k_backward()
+    bsteps = max(1, min(args.steps, 20))
+    b_s = timed([gb] * N_ROT, bsteps, max(3, min(args.warmup, 3)))
+    b_s, = reduce_max([b_s], dev, dist)
+    assert _native.lib().la_last_device_status(sh) == 0
+    b_call = b_s / bsteps
+    b_tflops = backward_flops(bw.B, bw.H, bw.T, bw.r, bw.dv, True) / b_call / 1e12
+    backward = {"workload": bw.name.replace("prefill", "backward of the gated prefill,"), "call_us": b_call * 1e6,
+                "launches_per_call": 5, "tokens_per_s": bw.B * bw.T * world / b_call, "steps": bsteps,
+                "roofline": {"bound": "alu", "achieved": b_tflops, "peak": alu_peak, "unit": "TFLOP/s",
+                             "frac": b_tflops / alu_peak, "peak_kind": "nominal FP32 FMA (SMs x 128 x 2 x max clock)",
+                             "algorithmic_flops_per_call": backward_flops(bw.B, bw.H, bw.T, bw.r, bw.dv, True)}}
+
     # end to end through the public API with host buffers (pinned), every step:
     # H2D of q, k, v (+ the decode token), the three calls, D2H of y, S, z, y_decode
     hq, hk, hv = (base[n].pin_memory() for n in ("q", "k", "v"))
@@ -507,7 +558,8 @@ def run_ours(args, rank, world, local_rank):
                                  f"{prefill_bytes(B, H, T, r, dv) / 1e6:.0f} MB (> 129 MB L2)",
                            "parallelism": f"replicas x{world} (independent batches, no collective)",
                            "launch": "CUDA graph per step"},
-                "roofline": roofline, "decode": decode, "delta_rule": delta, "cpu_baseline": cpu, "e2e": e2e,
+                "roofline": roofline, "decode": decode, "delta_rule": delta, "backward": backward, "cpu_baseline": cpu,
+                "e2e": e2e,
                 "gpu_launches": launches_per_step * args.steps, "clocks": clocks}
         print(json.dumps(line), flush=True)
 

@@ -14,6 +14,8 @@
 // write side):
 //   dL/d log alpha_u = sum_{t >= u} (q~_t . dq~_t - k~_t . dk~_t) + <dS_T, S_T> + <dz_T, z_T>.
 //
+// d_t comes from a pass over (head, 32 features) warps that runs z's recurrence,
+// dd_t from a bandwidth-bound pass over tokens.
 // Each of dq, dk and dv is a gated rank-1 recurrence with a read that does not
 // feed back into the state, so the three are one kernel in three modes:
 //   kFwdDq: forward in time, one column per feature i, state S[i, :] and z_i;
@@ -40,8 +42,8 @@ constexpr int kBCols = 32;       // columns per CTA
 
 enum Mode { kFwdDq = 0, kRevDk = 1, kRevDv = 2 };
 
-__device__ __forceinline__ float ld_in(const float *p, size_t i) { return p[i]; }
-__device__ __forceinline__ float ld_in(const __nv_bfloat16 *p, size_t i) { return __bfloat162float(p[i]); }
+__device__ __forceinline__ float to_f32(float x) { return x; }
+__device__ __forceinline__ float to_f32(__nv_bfloat16 x) { return __bfloat162float(x); }
 
 __device__ __forceinline__ float phi_f(float x) { return x > 0.f ? x + 1.f : expf(x); }
 __device__ __forceinline__ float dphi_f(float x) { return x > 0.f ? 1.f : expf(x); }
@@ -51,87 +53,105 @@ __device__ __forceinline__ float2 hi2(float4 a) { return make_float2(a.z, a.w); 
 
 // ------------------------------------------------------------ d_t and dd_t
 
-// One CTA of 128 threads per (b, h), one thread per feature (r <= 128): z_t by
-// the recurrence, then per block of tokens the sums over features (q~_t . z_t)
-// and over values (dy_t . y_t) through shared memory.  A block's loads are all
-// issued before its z chain runs.
+// z_t and the feature sum of d_t: one warp per (b, h, 32 features), lane = feature.
+// Blocks of 32 tokens are staged in shared memory with 16-byte loads; the loads of
+// the next block are issued before the current block's recurrence runs and stored
+// after it.  A block's products q~_{t,i} z_{t,i} are summed over the warp's
+// features through a padded tile and added to d_acc[t] (zeroed before).
 template <typename Tin>
-__global__ void __launch_bounds__(128)
-bwd_prep_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k, const float *__restrict__ alpha,
-                const float *__restrict__ z0, const Tin *__restrict__ y, const Tin *__restrict__ dy, int T, int r,
-                int dv, float eps, float *__restrict__ d_out, float *__restrict__ dd_out)
+__global__ void __launch_bounds__(32)
+bwd_z_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k, const float *__restrict__ alpha,
+             const float *__restrict__ z0, int T, int r, float *__restrict__ d_acc)
 {
-    constexpr int kV = 16 / (int)sizeof(Tin);   // elements per 16-byte load
-    __shared__ float part[kBT][129];            // [token][feature, or 16-byte chunk of the value row]
-    __shared__ float sa[kBT], den[kBT];
-    const int bh = blockIdx.x, i = threadIdx.x;
-    float z = (z0 && i < r) ? z0[(size_t)bh * r + i] : 0.f;
-    for (int t0 = 0; t0 < T; t0 += kBT) {
+    constexpr int kV = 16 / (int)sizeof(Tin);     // elements per 16-byte chunk
+    constexpr int kCh = 32 / kV;                  // chunks per row of 32 features
+    constexpr int kPer = 2 * kBT * kCh / 32;      // chunks per lane per block (q and k)
+    __shared__ __align__(16) Tin raw[2][2][kBT][32];   // [buffer][q, k][token][feature]
+    __shared__ float ga[2][kBT];
+    __shared__ float tile[kBT][kBT + 1];
+    const int nfg = r / 32, bh = blockIdx.x / nfg, lane = threadIdx.x;
+    const int i0 = (blockIdx.x % nfg) * 32;
+    float z = z0 ? z0[(size_t)bh * r + i0 + lane] : 0.f;
+    uint4 u[kPer];
+    float ad = 1.f;
+    auto load = [&](int t0) {
         const int nt = min(kBT, T - t0);
-        float kk[kBT], qq[kBT];
 #pragma unroll
-        for (int t = 0; t < kBT; ++t) {
-            kk[t] = qq[t] = 0.f;
-            if (t < nt && i < r) {
-                const size_t row = ((size_t)bh * T + t0 + t) * r + i;
-                kk[t] = ld_in(k, row);
-                qq[t] = ld_in(q, row);
-            }
+        for (int e = 0; e < kPer; ++e) {
+            const int c = lane + 32 * e, ten = c / (kBT * kCh), t = (c % (kBT * kCh)) / kCh, part = c % kCh;
+            u[e] = make_uint4(0u, 0u, 0u, 0u);
+            if (t < nt)
+                u[e] = *reinterpret_cast<const uint4 *>((ten ? k : q) + ((size_t)bh * T + t0 + t) * r + i0 + part * kV);
         }
-        if (i < nt) sa[i] = alpha ? alpha[(size_t)bh * T + t0 + i] : 1.f;
-        __syncthreads();
-        if (i < r) {
+        ad = (alpha && lane < nt) ? alpha[(size_t)bh * T + t0 + lane] : 1.f;
+    };
+    auto store = [&](int buf) {
 #pragma unroll
-            for (int t = 0; t < kBT; ++t)
-                if (t < nt) {
-                    z = sa[t] * z + phi_f(kk[t]);
-                    part[t][i] = phi_f(qq[t]) * z;
+        for (int e = 0; e < kPer; ++e) {
+            const int c = lane + 32 * e, ten = c / (kBT * kCh), t = (c % (kBT * kCh)) / kCh, part = c % kCh;
+            *reinterpret_cast<uint4 *>(&raw[buf][ten][t][part * kV]) = u[e];
+        }
+        ga[buf][lane] = ad;
+    };
+    load(0);
+    store(0);
+    __syncwarp();
+    for (int t0 = 0, cur = 0; t0 < T; t0 += kBT, cur ^= 1) {
+        const int nt = min(kBT, T - t0);
+        const bool more = t0 + kBT < T;
+        if (more) load(t0 + kBT);
+#pragma unroll
+        for (int t = 0; t < kBT; ++t)
+            if (t < nt) {
+                z = ga[cur][t] * z + phi_f(to_f32(raw[cur][1][t][lane]));
+                tile[t][lane] = phi_f(to_f32(raw[cur][0][t][lane])) * z;
+            }
+        __syncwarp();
+        float s = 0.f;
+#pragma unroll 8
+        for (int f = 0; f < 32; ++f) s += tile[lane][f];
+        if (lane < nt) atomicAdd(&d_acc[(size_t)bh * T + t0 + lane], s);
+        if (more) store(cur ^ 1);
+        __syncwarp();
+    }
+}
+
+// d_t = d_acc[t] + eps and dd_t = -(dy_t . y_t) / d_t: two tokens per warp step,
+// 16 lanes per token, 16-byte loads.
+template <typename Tin>
+__global__ void __launch_bounds__(256)
+bwd_dd_kernel(const Tin *__restrict__ y, const Tin *__restrict__ dy, int dv, long long n, float eps,
+              float *__restrict__ d, float *__restrict__ dd)
+{
+    constexpr int kV = 16 / (int)sizeof(Tin);
+    const int nch = dv / kV;
+    const long long warp = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const long long nwarps = ((long long)gridDim.x * blockDim.x) >> 5;
+    const int lane = threadIdx.x & 31, hl = lane & 15;
+    for (long long tok0 = warp * 2; tok0 < n; tok0 += nwarps * 2) {
+        const long long tok = tok0 + (lane >> 4);
+        float s = 0.f;
+        if (tok < n) {
+            for (int c = hl; c < nch; c += 16) {
+                const size_t off = (size_t)tok * dv + (size_t)c * kV;
+                const uint4 a = *reinterpret_cast<const uint4 *>(dy + off), b = *reinterpret_cast<const uint4 *>(y + off);
+                if constexpr (sizeof(Tin) == 2) {
+                    const uint32_t ua[4] = {a.x, a.y, a.z, a.w}, ub[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) s += bf16_lo(ua[e]) * bf16_lo(ub[e]) + bf16_hi(ua[e]) * bf16_hi(ub[e]);
+                } else {
+                    s += __uint_as_float(a.x) * __uint_as_float(b.x) + __uint_as_float(a.y) * __uint_as_float(b.y) +
+                         __uint_as_float(a.z) * __uint_as_float(b.z) + __uint_as_float(a.w) * __uint_as_float(b.w);
                 }
+            }
         }
-        __syncthreads();
-        // d_t = sum over features + eps, 8 threads per token
-        for (int t = i >> 3; t < kBT; t += 16) {
-            float s = 0.f;
-            if (t < nt)
-                for (int f = i & 7; f < r; f += 8) s += part[t][f];
-            s += __shfl_xor_sync(0xffffffffu, s, 1);
-            s += __shfl_xor_sync(0xffffffffu, s, 2);
-            s += __shfl_xor_sync(0xffffffffu, s, 4);
-            if ((i & 7) == 0) den[t] = s + eps;
-        }
-        __syncthreads();
-        // dy_t . y_t, one 16-byte chunk of both rows per step
-        const int nch = dv / kV;
-#pragma unroll 4
-        for (int c = i; c < nt * nch; c += 128) {
-            const int t = c / nch, ch = c - t * nch;
-            const size_t off = ((size_t)bh * T + t0 + t) * dv + (size_t)ch * kV;
-            const uint4 a = *reinterpret_cast<const uint4 *>(dy + off), b = *reinterpret_cast<const uint4 *>(y + off);
-            float s = 0.f;
-            if constexpr (sizeof(Tin) == 2) {
-                const uint32_t ua[4] = {a.x, a.y, a.z, a.w}, ub[4] = {b.x, b.y, b.z, b.w};
 #pragma unroll
-                for (int e = 0; e < 4; ++e) s += bf16_lo(ua[e]) * bf16_lo(ub[e]) + bf16_hi(ua[e]) * bf16_hi(ub[e]);
-            } else {
-                s = __uint_as_float(a.x) * __uint_as_float(b.x) + __uint_as_float(a.y) * __uint_as_float(b.y) +
-                    __uint_as_float(a.z) * __uint_as_float(b.z) + __uint_as_float(a.w) * __uint_as_float(b.w);
-            }
-            part[t][ch] = s;
+        for (int o = 1; o < 16; o <<= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+        if (tok < n && hl == 0) {
+            const float den = d[tok] + eps;
+            d[tok] = den;
+            dd[tok] = -s / den;
         }
-        __syncthreads();
-        for (int t = i >> 3; t < kBT; t += 16) {
-            float s = 0.f;
-            if (t < nt)
-                for (int f = i & 7; f < nch; f += 8) s += part[t][f];
-            s += __shfl_xor_sync(0xffffffffu, s, 1);
-            s += __shfl_xor_sync(0xffffffffu, s, 2);
-            s += __shfl_xor_sync(0xffffffffu, s, 4);
-            if (t < nt && (i & 7) == 0) {
-                d_out[(size_t)bh * T + t0 + t] = den[t];
-                dd_out[(size_t)bh * T + t0 + t] = -s / den[t];
-            }
-        }
-        __syncthreads();
     }
 }
 
@@ -229,8 +249,6 @@ rec_kernel(RecArgs p)
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int g = lane >> 2, jj = lane & 3;
     const int jl = warp * 8 + 2 * jj;           // first of the lane's two columns (local)
-    const int b4 = (lane >> 4) & 1;             // which of the two columns this lane's total is for
-    const bool writer = (lane & 12) == 0;
     const Tin *qi = static_cast<const Tin *>(p.q), *ki = static_cast<const Tin *>(p.k);
     const Tin *vi = static_cast<const Tin *>(p.v), *dyi = static_cast<const Tin *>(p.dy);
     Tin *out = static_cast<Tin *>(p.out);
@@ -356,74 +374,112 @@ rec_kernel(RecArgs p)
         if (warp == 0 && bi + 2 < nblk) issue(bi + 2);
         if (bi + 1 < nblk) sc = fetch(bi + 1);
 
-#pragma unroll 2
-        for (int s = 0; s < nt; ++s) {
-            const int t = Mode == kFwdDq ? s : nt - 1 - s;
-            const float gm = sm.gam[t];
-            const float2 a0 = make_float2(sm.a[t][jl], sm.a[t][jl]), a1 = make_float2(sm.a[t][jl + 1], sm.a[t][jl + 1]);
-            const float4 *br = reinterpret_cast<const float4 *>(&sm.b[t][0]) + g;
-            const float4 *wr = reinterpret_cast<const float4 *>(&sm.w[t][0]) + g;
-            float2 r0a = make_float2(0.f, 0.f), r0b = r0a, r1a = r0a, r1b = r0a;
-            if (p.alpha) {
-                const float2 g2 = make_float2(gm, gm);
+        // Tokens in groups of 8 (in processing order).  Each lane keeps its partial
+        // reads of the group (8 tokens x 2 columns) and the scalar recurrence after
+        // each token; one reduce-scatter over the 8 row groups then leaves row-group
+        // lane g with both column totals of the group's token g.
+        for (int s0 = 0; s0 < nt; s0 += 8) {
+            float part[8][2], eh[8][2];
 #pragma unroll
-                for (int m = 0; m < F; ++m) {
-                    const float4 bb = br[8 * m], ww = wr[8 * m];
-                    X[m][0][0] = __ffma2_rn(lo2(bb), a0, __fmul2_rn(X[m][0][0], g2));
-                    X[m][0][1] = __ffma2_rn(hi2(bb), a0, __fmul2_rn(X[m][0][1], g2));
-                    X[m][1][0] = __ffma2_rn(lo2(bb), a1, __fmul2_rn(X[m][1][0], g2));
-                    X[m][1][1] = __ffma2_rn(hi2(bb), a1, __fmul2_rn(X[m][1][1], g2));
-                    r0a = __ffma2_rn(X[m][0][0], lo2(ww), r0a);
-                    r0b = __ffma2_rn(X[m][0][1], hi2(ww), r0b);
-                    r1a = __ffma2_rn(X[m][1][0], lo2(ww), r1a);
-                    r1b = __ffma2_rn(X[m][1][1], hi2(ww), r1b);
-                }
-            } else {
+            for (int u = 0; u < 8; ++u) {
+                part[u][0] = part[u][1] = 0.f;
+                eh[u][0] = eh[u][1] = 0.f;
+                if (s0 + u < nt) {   // warp-uniform
+                    const int t = Mode == kFwdDq ? s0 + u : nt - 1 - (s0 + u);
+                    const float gm = sm.gam[t];
+                    const float2 a0 = make_float2(sm.a[t][jl], sm.a[t][jl]);
+                    const float2 a1 = make_float2(sm.a[t][jl + 1], sm.a[t][jl + 1]);
+                    const float4 *br = reinterpret_cast<const float4 *>(&sm.b[t][0]) + g;
+                    const float4 *wr = reinterpret_cast<const float4 *>(&sm.w[t][0]) + g;
+                    float2 r0a = make_float2(0.f, 0.f), r0b = r0a, r1a = r0a, r1b = r0a;
+                    const float2 g2 = make_float2(gm, gm);
 #pragma unroll
-                for (int m = 0; m < F; ++m) {
-                    const float4 bb = br[8 * m], ww = wr[8 * m];
-                    X[m][0][0] = __ffma2_rn(lo2(bb), a0, X[m][0][0]);
-                    X[m][0][1] = __ffma2_rn(hi2(bb), a0, X[m][0][1]);
-                    X[m][1][0] = __ffma2_rn(lo2(bb), a1, X[m][1][0]);
-                    X[m][1][1] = __ffma2_rn(hi2(bb), a1, X[m][1][1]);
-                    r0a = __ffma2_rn(X[m][0][0], lo2(ww), r0a);
-                    r0b = __ffma2_rn(X[m][0][1], hi2(ww), r0b);
-                    r1a = __ffma2_rn(X[m][1][0], lo2(ww), r1a);
-                    r1b = __ffma2_rn(X[m][1][1], hi2(ww), r1b);
+                    for (int m = 0; m < F; ++m) {
+                        const float4 bb = br[8 * m], ww = wr[8 * m];
+                        if (p.alpha) {
+                            X[m][0][0] = __fmul2_rn(X[m][0][0], g2);
+                            X[m][0][1] = __fmul2_rn(X[m][0][1], g2);
+                            X[m][1][0] = __fmul2_rn(X[m][1][0], g2);
+                            X[m][1][1] = __fmul2_rn(X[m][1][1], g2);
+                        }
+                        X[m][0][0] = __ffma2_rn(lo2(bb), a0, X[m][0][0]);
+                        X[m][0][1] = __ffma2_rn(hi2(bb), a0, X[m][0][1]);
+                        X[m][1][0] = __ffma2_rn(lo2(bb), a1, X[m][1][0]);
+                        X[m][1][1] = __ffma2_rn(hi2(bb), a1, X[m][1][1]);
+                        r0a = __ffma2_rn(X[m][0][0], lo2(ww), r0a);
+                        r0b = __ffma2_rn(X[m][0][1], hi2(ww), r0b);
+                        r1a = __ffma2_rn(X[m][1][0], lo2(ww), r1a);
+                        r1b = __ffma2_rn(X[m][1][1], hi2(ww), r1b);
+                    }
+                    // the scalar recurrences: z_i += k~ (forward), g_i += dd q~ (reverse dk)
+                    if (Mode == kFwdDq) {
+                        e[0] = fmaf(gm, e[0], a0.x);
+                        e[1] = fmaf(gm, e[1], a1.x);
+                    } else if (Mode == kRevDk) {
+                        const float ddt = sm.dd[t];
+                        e[0] = fmaf(gm, e[0], ddt * a0.x);
+                        e[1] = fmaf(gm, e[1], ddt * a1.x);
+                    }
+                    const float2 s0v = __fadd2_rn(r0a, r0b), s1v = __fadd2_rn(r1a, r1b);
+                    part[u][0] = s0v.x + s0v.y;
+                    part[u][1] = s1v.x + s1v.y;
+                    eh[u][0] = e[0];
+                    eh[u][1] = e[1];
                 }
             }
-            // the scalar recurrences: z_i += k~ (forward), g_i += dd q~ (reverse dk)
-            if (Mode == kFwdDq) {
-                e[0] = fmaf(gm, e[0], a0.x);
-                e[1] = fmaf(gm, e[1], a1.x);
-            } else if (Mode == kRevDk) {
-                const float ddt = sm.dd[t];
-                e[0] = fmaf(gm, e[0], ddt * a0.x);
-                e[1] = fmaf(gm, e[1], ddt * a1.x);
+            // reduce-scatter over lane bits 4, 3, 2 (row-group bits 2, 1, 0): each step
+            // keeps the half of the tokens whose index bit matches the lane's bit
+            const bool lb4 = lane & 16, lb3 = lane & 8, lb2 = lane & 4;
+            float h4[4][2], h4e[4][2];
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+#pragma unroll
+                for (int c = 0; c < 2; ++c) {
+                    const float keep = lb4 ? part[4 + u][c] : part[u][c], send = lb4 ? part[u][c] : part[4 + u][c];
+                    h4[u][c] = keep + __shfl_xor_sync(0xffffffffu, send, 16);
+                    h4e[u][c] = lb4 ? eh[4 + u][c] : eh[u][c];
+                }
+            float h2[2][2], h2e[2][2];
+#pragma unroll
+            for (int u = 0; u < 2; ++u)
+#pragma unroll
+                for (int c = 0; c < 2; ++c) {
+                    const float keep = lb3 ? h4[2 + u][c] : h4[u][c], send = lb3 ? h4[u][c] : h4[2 + u][c];
+                    h2[u][c] = keep + __shfl_xor_sync(0xffffffffu, send, 8);
+                    h2e[u][c] = lb3 ? h4e[2 + u][c] : h4e[u][c];
+                }
+            float tot[2], ev[2];
+#pragma unroll
+            for (int c = 0; c < 2; ++c) {
+                const float keep = lb2 ? h2[1][c] : h2[0][c], send = lb2 ? h2[0][c] : h2[1][c];
+                tot[c] = keep + __shfl_xor_sync(0xffffffffu, send, 4);
+                ev[c] = lb2 ? h2e[1][c] : h2e[0][c];
             }
-            const float2 s0 = __fadd2_rn(r0a, r0b), s1 = __fadd2_rn(r1a, r1b);
-            // reduce over the 8 row groups: bit 4 keeps column b4, then bits 3 and 2
-            float kept = b4 ? s1.x + s1.y : s0.x + s0.y;
-            const float sent = b4 ? s0.x + s0.y : s1.x + s1.y;
-            kept += __shfl_xor_sync(0xffffffffu, sent, 16);
-            kept += __shfl_xor_sync(0xffffffffu, kept, 8);
-            kept += __shfl_xor_sync(0xffffffffu, kept, 4);
-            const int c = jl + b4;
+            // this lane's token of the group: u = g
+            const bool have = s0 + g < nt;
+            const int t = Mode == kFwdDq ? s0 + g : nt - 1 - (s0 + g);
             if (Mode == kRevDv) {                   // dv = G_t^T k~_t
-                if (writer) sm.o[t][c] = kept;
+                if (have) {
+                    sm.o[t][jl] = tot[0];
+                    sm.o[t][jl + 1] = tot[1];
+                }
             } else {
-                // dq~ = S_t dn_t + dd_t z_t, or dk~ = G_t v_t + g_t
-                const float ec = b4 ? e[1] : e[0];
-                const float dt = Mode == kFwdDq ? kept + sm.dd[t] * ec : kept + ec;
-                const float xv = sm.x[t][c];
-                if (writer) sm.o[t][c] = dt * dphi_f(xv);
-                // q~ . dq~ (or k~ . dk~) over the warp's 8 columns: the writers hold
-                // distinct columns and differ in lane bits 0, 1 and 4
-                float ts = writer ? phi_f(xv) * dt : 0.f;
+                // dq~ = S_t dn_t + dd_t z_t, or dk~ = G_t v_t + g_t; then phi' and the dalpha term
+                float ts = 0.f;
+                if (have) {
+                    const float ddt = Mode == kFwdDq ? sm.dd[t] : 1.f;
+#pragma unroll
+                    for (int c = 0; c < 2; ++c) {
+                        const float dt = tot[c] + ddt * ev[c];
+                        const float xv = sm.x[t][jl + c];
+                        sm.o[t][jl + c] = dt * dphi_f(xv);
+                        ts += phi_f(xv) * dt;
+                    }
+                }
+                // the warp's 8 columns of this token: lanes jj = 0..3 of row group g
                 ts += __shfl_xor_sync(0xffffffffu, ts, 1);
                 ts += __shfl_xor_sync(0xffffffffu, ts, 2);
-                ts += __shfl_xor_sync(0xffffffffu, ts, 16);
-                if (lane == 0) atomicAdd(&sm.sum[t], ts);
+                if (have && jj == 0) atomicAdd(&sm.sum[t], ts);
             }
         }
     }
@@ -534,11 +590,14 @@ cudaError_t launch_bwd_t(const BackwardArgs &a, int B, cudaStream_t stream)
     const int BH = B * a.H;
     const size_t n = (size_t)BH * a.T;
     float *d = a.ws, *dd = d + n, *tok_sum = dd + n, *fin = tok_sum + n;
-    cudaError_t e = cudaMemsetAsync(tok_sum, 0, sizeof(float) * (n + BH), stream);
+    // d accumulates the feature sums; tok_sum and fin accumulate dalpha terms
+    cudaError_t e = cudaMemsetAsync(a.ws, 0, sizeof(float) * (3 * n + BH), stream);
     if (e != cudaSuccess) return e;
-    bwd_prep_kernel<Tin><<<BH, 128, 0, stream>>>(
-        static_cast<const Tin *>(a.q), static_cast<const Tin *>(a.k), a.alpha, a.z0, static_cast<const Tin *>(a.y),
-        static_cast<const Tin *>(a.dy), a.T, a.r, a.dv, a.eps, d, dd);
+    bwd_z_kernel<Tin><<<(unsigned)(BH * (a.r / 32)), 32, 0, stream>>>(
+        static_cast<const Tin *>(a.q), static_cast<const Tin *>(a.k), a.alpha, a.z0, a.T, a.r, d);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    bwd_dd_kernel<Tin><<<152 * 8, 256, 0, stream>>>(static_cast<const Tin *>(a.y), static_cast<const Tin *>(a.dy),
+                                                      a.dv, (long long)n, a.eps, d, dd);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     RecArgs p;
     p.q = a.q; p.k = a.k; p.v = a.v; p.dy = a.dy;
