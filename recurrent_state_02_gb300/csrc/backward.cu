@@ -542,26 +542,27 @@ rec_kernel(RecArgs p)
 
 // ------------------------------------------------------------------ dalpha
 
-// One warp per (b, h): dlog alpha_u = sum_{t >= u} tok_sum[t] + fin, then
-// dalpha_u = dlog alpha_u / alpha_u.  The reverse running sum goes 32 tokens at a
-// time (a warp scan), from the end of the sequence.
-__global__ void bwd_dalpha_kernel(const float *__restrict__ tok_sum, const float *__restrict__ fin,
-                                  const float *__restrict__ alpha, int T, int BH, float *__restrict__ dalpha)
+// One CTA of 128 threads per (b, h): dlog alpha_u = sum_{t >= u} tok_sum[t] + fin,
+// then dalpha_u = dlog alpha_u / alpha_u.  Thread i owns a contiguous chunk of
+// tokens: it sums its chunk, takes the sum of the later chunks (plus fin) from
+// shared memory, and walks its chunk backwards.
+__global__ void __launch_bounds__(128)
+bwd_dalpha_kernel(const float *__restrict__ tok_sum, const float *__restrict__ fin, const float *__restrict__ alpha,
+                  int T, float *__restrict__ dalpha)
 {
-    const int bh = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5), lane = threadIdx.x & 31;
-    if (bh >= BH) return;
+    __shared__ float part[128];
+    const int bh = blockIdx.x, i = threadIdx.x;
+    const int per = (T + 127) / 128, lo = min(T, i * per), hi = min(T, lo + per);
+    const float *ts = tok_sum + (size_t)bh * T;
+    float s = 0.f;
+    for (int t = lo; t < hi; ++t) s += ts[t];
+    part[i] = s;
+    __syncthreads();
     float carry = fin[bh];
-    for (int t0 = ((T - 1) / 32) * 32; t0 >= 0; t0 -= 32) {
-        const int t = t0 + 31 - lane;             // lane 0 takes the latest token of the group
-        float x = t < T ? tok_sum[(size_t)bh * T + t] : 0.f;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const float y = __shfl_up_sync(0xffffffffu, x, o);
-            if (lane >= o) x += y;
-        }
-        const float total = __shfl_sync(0xffffffffu, x, 31);
-        if (t < T) dalpha[(size_t)bh * T + t] = (x + carry) / alpha[(size_t)bh * T + t];
-        carry += total;
+    for (int j = i + 1; j < 128; ++j) carry += part[j];
+    for (int t = hi - 1; t >= lo; --t) {
+        carry += ts[t];
+        dalpha[(size_t)bh * T + t] = carry / alpha[(size_t)bh * T + t];
     }
 }
 
@@ -612,7 +613,7 @@ cudaError_t launch_bwd_t(const BackwardArgs &a, int B, cudaStream_t stream)
     p.out = a.dv_out;
     if ((e = launch_rec<Tin, kRevDv>(p, B, a.r, stream)) != cudaSuccess) return e;
     if (a.alpha && a.dalpha) {
-        bwd_dalpha_kernel<<<(BH + 3) / 4, 128, 0, stream>>>(tok_sum, fin, a.alpha, a.T, BH, a.dalpha);
+        bwd_dalpha_kernel<<<BH, 128, 0, stream>>>(tok_sum, fin, a.alpha, a.T, a.dalpha);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
     return cudaSuccess;
