@@ -249,6 +249,43 @@ def oracle_tokens_per_s(w, seconds, max_tokens=None):
     return tok / elapsed, cores, desc, elapsed
 
 
+def oracle_rate(kind, w, seconds):
+    """Times the FP64 oracle of the delta rule (kind "delta") or of the backward
+    ("backward", gated) over all B*H heads of the workload on the first T' tokens,
+    T' sized to about `seconds` from a 32-token calibration.  Returns the
+    cpu_baseline object (tokens/s)."""
+    import numpy as np
+    import torch
+
+    import oracle
+    from recurrent_state_02_gb300 import workloads as W
+
+    oracle.build()
+    cores = oracle.num_cpus()
+    bits = lambda t: t.contiguous().view(torch.int16).numpy().view(np.uint16)
+
+    def run(Tn):
+        if kind == "delta":
+            d = W.delta_inputs(w.with_(T=Tn))
+            t0 = time.perf_counter()
+            oracle.delta(bits(d["q"]), bits(d["k"]), bits(d["v"]), beta=d["beta"].numpy(), threads=cores)
+        else:
+            d = W.prefill_inputs(w.with_(T=Tn))
+            dy = np.random.default_rng(0).standard_normal((w.B, w.H, Tn, w.dv))
+            t0 = time.perf_counter()
+            oracle.backward(bits(d["q"]), bits(d["k"]), bits(d["v"]), dy, alpha=d["alpha"].numpy(), eps=w.eps,
+                            threads=cores)
+        return time.perf_counter() - t0
+
+    per_token = run(32) / (w.B * 32)
+    Ts = int(max(1, min(w.T, seconds / max(per_token, 1e-9) / w.B)))
+    elapsed = run(Ts)
+    what = "delta-rule memory" if kind == "delta" else "gradients of the gated token recurrence"
+    return {"value": w.B * Ts / elapsed, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+            "sample": f"FP64 {what} on {cores} threads over all {w.B}x{w.H} heads of '{w.name}', first {Ts} of "
+                      f"{w.T} tokens, {elapsed:.1f} s"}
+
+
 def run_reference(args, rank, world):
     """Reference arm: the FP64 CPU oracle, as it stands, on the host cores."""
     if rank != 0:
@@ -557,6 +594,9 @@ def run_ours(args, rank, world, local_rank):
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         tps, cores, desc, _ = oracle_tokens_per_s(w, args.cpu_seconds)
         cpu = {"value": tps, "unit": "tokens/s", "cores": cores, "kind": "oracle", "sample": desc}
+        # the oracles of the delta rule and of the backward, beside their GPU figures
+        delta["cpu_baseline"] = oracle_rate("delta", xw, args.cpu_seconds / 4)
+        backward["cpu_baseline"] = oracle_rate("backward", bw, args.cpu_seconds / 4)
 
     if rank == 0:
         line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
