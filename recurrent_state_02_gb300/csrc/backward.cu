@@ -45,8 +45,12 @@ enum Mode { kFwdDq = 0, kRevDk = 1, kRevDv = 2 };
 __device__ __forceinline__ float to_f32(float x) { return x; }
 __device__ __forceinline__ float to_f32(__nv_bfloat16 x) { return __bfloat162float(x); }
 
-__device__ __forceinline__ float phi_f(float x) { return x > 0.f ? x + 1.f : expf(x); }
-__device__ __forceinline__ float dphi_f(float x) { return x > 0.f ? 1.f : expf(x); }
+// phi and its derivative with the hardware exponential: for the arguments
+// x <= 0 where it is used, the relative error is about 2.4e-7 + 6e-8 |x| (the
+// rounding of x log2 e and of the base-2 exponential), far inside the
+// backward's tolerance
+__device__ __forceinline__ float phi_f(float x) { return x > 0.f ? x + 1.f : __expf(x); }
+__device__ __forceinline__ float dphi_f(float x) { return x > 0.f ? 1.f : __expf(x); }
 
 __device__ __forceinline__ float2 lo2(float4 a) { return make_float2(a.x, a.y); }
 __device__ __forceinline__ float2 hi2(float4 a) { return make_float2(a.z, a.w); }
