@@ -91,14 +91,21 @@ __host__ __device__ constexpr int phi_index(int w) { return __builtin_popcount(k
 #ifndef LA_STAGES
 #define LA_STAGES 4
 #endif
+// The gated kernel spends about twice as long per chunk, so three stages cover its
+// load latency; the shared memory of the fourth holds its gate ring and a second
+// [Sprev | z] tile, which lets the TMEM warps write chunk c+1's operand while the
+// O MMA of chunk c still reads the other one.
+#ifndef LA_STAGES_GATED
+#define LA_STAGES_GATED 3
+#endif
 #ifndef LA_SP_BUFS
 #define LA_SP_BUFS 2
 #endif
 
 template <bool GATED>
 struct Cfg {
-    static constexpr int kStages = LA_STAGES;
-    static constexpr int kSpBufs = GATED ? 1 : LA_SP_BUFS;     // [Sprev | z] tiles
+    static constexpr int kStages = GATED ? LA_STAGES_GATED : LA_STAGES;
+    static constexpr int kSpBufs = LA_SP_BUFS;                 // [Sprev | z] tiles
     static constexpr int kNP = 2;                              // P accumulator buffers
     static constexpr int kNO = 3;                              // [O | dn] accumulator buffers
     // TMEM columns: P (x2), the state [S | z] (80: z is column 64) and [O | dn]
@@ -112,8 +119,7 @@ struct Cfg {
     static constexpr uint32_t kOffQ = 0, kOffK = kTileQ, kOffV = 2 * kTileQ;
     static constexpr uint32_t kStageBytes = kOffV + kTileV;
     static_assert(kStageBytes % 1024 == 0, "stage tiles stay 1024-byte aligned");
-    // A is double-buffered; so is [Sprev | z] where shared memory allows (the
-    // gated kernel keeps its gate ring there instead)
+    // A and [Sprev | z] are double-buffered
     static constexpr uint32_t kOffA = kStages * kStageBytes;
     static constexpr uint32_t kOffSpZ = kOffA + 2 * kTileA;
     static constexpr uint32_t kOffOnes = kOffSpZ + kSpBufs * kTileSpZ;
