@@ -25,7 +25,7 @@ constexpr int kWarpTma = 0, kWarpMma = 1, kWarpTm0 = 4, kTmWarps = 4;
 __host__ __device__ constexpr bool is_phi_warp(int w) { return w == 2 || w == 3 || w >= 8; }
 __host__ __device__ constexpr int phi_index(int w) { return w < 4 ? w - 2 : w - 6; }
 constexpr int kPhiWarps = 6, kPhiThreads = kPhiWarps * 32;
-constexpr int kStages = 6;
+constexpr int kStages = 8;
 constexpr uint32_t kTileK = kC * kR * 2;       // 16 KB: two 64-feature blocks of 64 rows x 128 B
 constexpr uint32_t kTileV = kC * kDVS * 2;     // 8 KB
 constexpr uint32_t kTileOnes = kC * 128;       // 8 KB: the second 64-column block of [V | 1 0..]
