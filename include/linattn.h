@@ -113,7 +113,7 @@ size_t la_prefill_workspace_bytes(int B, int H, int T, int r, int dv, int chunk)
  *         the state pass, the scan of segment start states, and the chunk
  *         kernel over all segments at once.
  *   FP32: exact FP32 token recurrence on CUDA cores (chunk is not used).
- *         Requires 1 <= r <= 128, 1 <= dv <= 128, 4-byte alignment.
+ *         Requires 1 <= r <= 256, 1 <= dv <= 256, 4-byte alignment.
  * T may be any length >= 1 (a final partial chunk is masked).
  * Errors: LA_ERR_NULL, LA_ERR_SHAPE (B, H, T, r, dv or chunk < 1), LA_ERR_DTYPE,
  *         LA_ERR_ALIGN, LA_ERR_UNSUPPORTED, LA_ERR_WORKSPACE, LA_ERR_CUDA.

@@ -198,7 +198,7 @@ la_status la_prefill_chunked(const void *q, const void *k, const void *v, la_dty
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
 
     if (dtype == LA_DTYPE_FP32) {
-        if (r > 128 || dv > 128) return LA_ERR_UNSUPPORTED;
+        if (r > 256 || dv > 256) return LA_ERR_UNSUPPORTED;
         const void *ptrs[] = {q, k, v, y, S_out, z_out, alpha, S0, z0};
         for (const void *p : ptrs)
             if (p && !aligned(p, 4)) return LA_ERR_ALIGN;

@@ -67,7 +67,7 @@ cudaError_t launch_state_tc(const CUtensorMap &map_k, const CUtensorMap &map_v, 
 cudaError_t launch_seg_scan(const float *S0, const float *z0, const float *A, const float *dS, float *S_start,
                             int BH, int dv, int nsub, int sub_per_seg, int nseg, cudaStream_t stream);
 
-// Exact FP32 token recurrence (CUDA cores), r, dv <= 128.
+// Exact FP32 token recurrence (CUDA cores), r, dv <= 256.
 cudaError_t launch_prefill_f32(const float *q, const float *k, const float *v, const float *alpha,
                                const float *S0, const float *z0, int B, int H, int T, int r, int dv,
                                float eps, float *y, float *S_out, float *z_out, cudaStream_t stream);

@@ -7,35 +7,48 @@
 // the recurrence itself in FP32 (section "最小递推里，每一行都有张量意义"):
 //     S <- alpha_t S + phi(k_t) v_t^T,  z <- alpha_t z + phi(k_t),
 //     y_t = phi(q_t)^T S / (phi(q_t)^T z + eps).
-// One CTA of 128 threads per (b, h); S [r x dv] in shared memory, thread j owns
-// column j of S and feature j of z.
+// One CTA of 256 threads per (b, h, slice of up to 128 value columns): the slice
+// of S [r x 128] lives in shared memory, thread j owns column j of the slice;
+// thread i < r owns feature i of z (z and the denominator are recomputed by the
+// CTAs of every slice, which need them alike).  The slices of a head run as one
+// thread-block cluster.
 
 #include "kernels.h"
 
 namespace la {
 namespace {
 
-constexpr int kMaxDim = 128;
+constexpr int kMaxR = 256;       // features (threads)
+constexpr int kSlice = 128;      // value columns per CTA
 
 __device__ __forceinline__ float phi_exact(float x) { return x > 0.f ? x + 1.f : expf(x); }
 
-__global__ void __launch_bounds__(kMaxDim)
+__global__ void __launch_bounds__(kMaxR)
 prefill_f32_kernel(const float *__restrict__ q, const float *__restrict__ k, const float *__restrict__ v,
                    const float *__restrict__ alpha, const float *__restrict__ S0, const float *__restrict__ z0,
-                   int H, int T, int r, int dv, float eps, float *__restrict__ y, float *__restrict__ S_out,
-                   float *__restrict__ z_out)
+                   int H, int T, int r, int dv, float eps, float *__restrict__ y, float *S_out, float *z_out)
 {
-    extern __shared__ float S[];   // [r][dv]
-    __shared__ float qf[kMaxDim], kf[kMaxDim], red[kMaxDim / 32];
+    extern __shared__ float S[];   // [r][ds]
+    __shared__ float qf[kMaxR], kf[kMaxR], red[kMaxR / 32];
     const int bh = blockIdx.y * H + blockIdx.x;
+    const int c0 = blockIdx.z * kSlice, ds = min(kSlice, dv - c0);   // this CTA's value columns
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
 
-    for (int e = tid; e < r * dv; e += blockDim.x) S[e] = S0 ? S0[(size_t)bh * r * dv + e] : 0.f;
+    for (int e = tid; e < r * ds; e += blockDim.x) {
+        const int i = e / ds, j = e - i * ds;
+        S[e] = S0 ? S0[((size_t)bh * r + i) * dv + c0 + j] : 0.f;
+    }
     float zi = (tid < r && z0) ? z0[(size_t)bh * r + tid] : 0.f;
+    // The slices of one head form a cluster: no slice may write z_out (which may
+    // alias z0) before every slice has read z0.
+    if (gridDim.z > 1) {
+        asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+        asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+    }
     __syncthreads();
 
-    const float *qh = q + (size_t)bh * T * r, *kh = k + (size_t)bh * T * r, *vh = v + (size_t)bh * T * dv;
-    float *yh = y + (size_t)bh * T * dv;
+    const float *qh = q + (size_t)bh * T * r, *kh = k + (size_t)bh * T * r, *vh = v + (size_t)bh * T * dv + c0;
+    float *yh = y + (size_t)bh * T * dv + c0;
     for (int t = 0; t < T; ++t) {
         const float a = alpha ? alpha[(size_t)bh * T + t] : 1.f;
         float part = 0.f;
@@ -51,23 +64,26 @@ prefill_f32_kernel(const float *__restrict__ q, const float *__restrict__ k, con
         for (int off = 16; off > 0; off >>= 1) part += __shfl_xor_sync(0xffffffffu, part, off);
         if (lane == 0) red[warp] = part;
         __syncthreads();
-        if (tid < dv) {
+        if (tid < ds) {
             float den = 0.f;
 #pragma unroll
-            for (int w = 0; w < kMaxDim / 32; ++w) den += red[w];
+            for (int w = 0; w < kMaxR / 32; ++w) den += red[w];
             const float vj = vh[(size_t)t * dv + tid];
             float n = 0.f;
             for (int i = 0; i < r; ++i) {
-                const float s = fmaf(a, S[i * dv + tid], kf[i] * vj);
-                S[i * dv + tid] = s;
+                const float s = fmaf(a, S[i * ds + tid], kf[i] * vj);
+                S[i * ds + tid] = s;
                 n = fmaf(qf[i], s, n);
             }
             yh[(size_t)t * dv + tid] = n / (den + eps);
         }
         __syncthreads();
     }
-    for (int e = tid; e < r * dv; e += blockDim.x) S_out[(size_t)bh * r * dv + e] = S[e];
-    if (tid < r) z_out[(size_t)bh * r + tid] = zi;
+    for (int e = tid; e < r * ds; e += blockDim.x) {
+        const int i = e / ds, j = e - i * ds;
+        S_out[((size_t)bh * r + i) * dv + c0 + j] = S[e];
+    }
+    if (tid < r && blockIdx.z == 0) z_out[(size_t)bh * r + tid] = zi;
 }
 
 }  // namespace
@@ -76,7 +92,8 @@ cudaError_t launch_prefill_f32(const float *q, const float *k, const float *v, c
                                const float *z0, int B, int H, int T, int r, int dv, float eps, float *y,
                                float *S_out, float *z_out, cudaStream_t stream)
 {
-    const size_t smem = sizeof(float) * (size_t)r * dv;
+    const int ds = dv < kSlice ? dv : kSlice;
+    const size_t smem = sizeof(float) * (size_t)r * ds;
     // The attribute is set once per device to the largest size this kernel accepts.
     static bool attr_set[64] = {};
     int dev = 0;
@@ -85,13 +102,24 @@ cudaError_t launch_prefill_f32(const float *q, const float *k, const float *v, c
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
     if (!attr_set[dev]) {
         e = cudaFuncSetAttribute(prefill_f32_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)(sizeof(float) * kMaxDim * kMaxDim));
+                                 (int)(sizeof(float) * kMaxR * kSlice));
         if (e != cudaSuccess) return e;
         attr_set[dev] = true;
     }
-    prefill_f32_kernel<<<dim3(H, B), kMaxDim, smem, stream>>>(q, k, v, alpha, S0, z0, H, T, r, dv, eps, y, S_out,
-                                                              z_out);
-    return cudaGetLastError();
+    const int nslice = (dv + kSlice - 1) / kSlice;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(H, B, nslice);
+    cfg.blockDim = dim3(kMaxR, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 1;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = nslice;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, prefill_f32_kernel, q, k, v, alpha, S0, z0, H, T, r, dv, eps, y, S_out, z_out);
 }
 
 }  // namespace la

@@ -78,7 +78,8 @@ def test_prefill_rejects_bad_arguments(native):
     assert _prefill(native, q=FAKE + 2) == native.LA_ERR_ALIGN
     assert _prefill(native, y=FAKE + 8) == native.LA_ERR_ALIGN
     assert _prefill(native, alpha=FAKE + 1) == native.LA_ERR_ALIGN
-    assert _prefill(native, dtype=native.LA_DTYPE_FP32, r=129) == native.LA_ERR_UNSUPPORTED
+    assert _prefill(native, dtype=native.LA_DTYPE_FP32, r=257) == native.LA_ERR_UNSUPPORTED
+    assert _prefill(native, dtype=native.LA_DTYPE_FP32, dv=300) == native.LA_ERR_UNSUPPORTED
     assert _prefill(native, dtype=native.LA_DTYPE_FP32, q=FAKE + 2) == native.LA_ERR_ALIGN
 
 

@@ -78,6 +78,25 @@ def test_prefill_fp32_ragged(la, oracle_mod, gated, with_state):
     _check(_gpu_prefill(la, inp), _oracle_prefill(oracle_mod, inp), 1e-5, "fp32")
 
 
+@pytest.mark.parametrize("r,dv", [(256, 256), (200, 160), (256, 33), (1, 129)])
+def test_prefill_fp32_wide(la, oracle_mod, r, dv):
+    """Widths up to 256: value columns beyond 128 go to a second CTA of the head."""
+    inp = _inputs(torch.float32, 1, 2, 45, r, dv, gated=True, with_state=True, seed=12 + r + dv, scale=0.5)
+    _check(_gpu_prefill(la, inp), _oracle_prefill(oracle_mod, inp), 1e-5, f"fp32 r={r} dv={dv}")
+
+
+def test_prefill_fp32_wide_in_place(la, oracle_mod):
+    """S0, z0 aliasing S_out, z_out with two column slices per head: no slice writes z
+    before the other has read it."""
+    inp = _inputs(torch.float32, 2, 2, 30, 256, 256, gated=True, with_state=True, seed=13, scale=0.5)
+    ref = _oracle_prefill(oracle_mod, inp)
+    d = {k: v.cuda() for k, v in inp.items()}
+    S, z = d["S0"], d["z0"]
+    y, _, _ = la.prefill_chunked(d["q"], d["k"], d["v"], alpha=d["alpha"], S0=S, z0=z, S_out=S, z_out=z)
+    assert la.last_device_status() == 0
+    _check((y.cpu().numpy(), S.cpu().numpy(), z.cpu().numpy()), ref, 1e-5, "fp32 wide in place")
+
+
 # ------------------------------------------------------------- BF16 prefill
 
 @pytest.mark.parametrize("T", [1, 17, 63, 64, 65, 5 * 64 + 17])
