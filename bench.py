@@ -551,44 +551,64 @@ def run_ours(args, rank, world, local_rank):
                              "algorithmic_flops_per_call": backward_flops(bw.B, bw.H, bw.T, bw.r, bw.dv, True)}}
 
     # end to end through the public API with host buffers (pinned), every step:
-    # H2D of q, k, v (+ the decode token), the three calls, D2H of y, S, z, y_decode
+    # H2D of q, k, v (+ the decode token), the three calls, D2H of y, S, z, y_decode.
+    # Steps are pipelined as a serving loop would run them: the copies in of step
+    # i+1 and the copies out of step i-1 run on their own streams while step i
+    # computes.  Two device buffer sets (and two pinned host output sets)
+    # alternate; events order every reuse of a buffer after its last reader.
     hq, hk, hv = (base[n].pin_memory() for n in ("q", "k", "v"))
     hqd, hkd, hvd = (dec[n].pin_memory() for n in ("q", "k", "v"))
-    hy = torch.empty((B, H, T, dv), dtype=torch.bfloat16).pin_memory()
-    hS = torch.empty((B, H, r, dv), dtype=torch.float32).pin_memory()
-    hz = torch.empty((B, H, r), dtype=torch.float32).pin_memory()
-    hyd = torch.empty((B, H, 1, dv), dtype=torch.bfloat16).pin_memory()
-    s0 = sets[0]
+    hout = [dict(y=torch.empty((B, H, T, dv), dtype=torch.bfloat16).pin_memory(),
+                 S=torch.empty((B, H, r, dv), dtype=torch.float32).pin_memory(),
+                 z=torch.empty((B, H, r), dtype=torch.float32).pin_memory(),
+                 yd=torch.empty((B, H, 1, dv), dtype=torch.bfloat16).pin_memory()) for _ in range(2)]
     h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hqd, hkd, hvd))
-    d2h = sum(t.numel() * t.element_size() for t in (hy, hS, hz, hyd))
+    d2h = sum(t.numel() * t.element_size() for t in hout[0].values())
+    s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    ev = {n: [torch.cuda.Event(), torch.cuda.Event()] for n in ("in", "comp", "out")}
 
-    def e2e_step():
-        s0["q"].copy_(hq, non_blocking=True); s0["k"].copy_(hk, non_blocking=True)
-        s0["v"].copy_(hv, non_blocking=True); s0["qd"].copy_(hqd, non_blocking=True)
-        s0["kd"].copy_(hkd, non_blocking=True); s0["vd"].copy_(hvd, non_blocking=True)
-        S, z = la.state_init(B, H, r, dv, S=s0["S"], z=s0["z"])
-        la.prefill_chunked(s0["q"], s0["k"], s0["v"], S0=S, z0=z, S_out=S, z_out=z, y=s0["y"], chunk=w.chunk,
-                           eps=w.eps)
-        la.decode_step(s0["qd"], s0["kd"], s0["vd"], S, z, eps=w.eps, y=s0["yd"])
-        hy.copy_(s0["y"], non_blocking=True); hS.copy_(S, non_blocking=True)
-        hz.copy_(z, non_blocking=True); hyd.copy_(s0["yd"], non_blocking=True)
+    def e2e_step(i):
+        b = i % 2
+        s, ho = sets[b], hout[b]
+        with torch.cuda.stream(s_in):          # inputs of step i, once step i-2 stopped reading them
+            if i >= 2:
+                s_in.wait_event(ev["comp"][b])
+            s["q"].copy_(hq, non_blocking=True); s["k"].copy_(hk, non_blocking=True)
+            s["v"].copy_(hv, non_blocking=True); s["qd"].copy_(hqd, non_blocking=True)
+            s["kd"].copy_(hkd, non_blocking=True); s["vd"].copy_(hvd, non_blocking=True)
+            ev["in"][b].record(s_in)
+        with torch.cuda.stream(stream):        # the step, once its inputs are in and step i-2 was read back
+            stream.wait_event(ev["in"][b])
+            if i >= 2:
+                stream.wait_event(ev["out"][b])
+            S, z = la.state_init(B, H, r, dv, S=s["S"], z=s["z"])
+            la.prefill_chunked(s["q"], s["k"], s["v"], S0=S, z0=z, S_out=S, z_out=z, y=s["y"], chunk=w.chunk,
+                               eps=w.eps)
+            la.decode_step(s["qd"], s["kd"], s["vd"], S, z, eps=w.eps, y=s["yd"])
+            ev["comp"][b].record(stream)
+        with torch.cuda.stream(s_out):         # its results back to the host
+            s_out.wait_event(ev["comp"][b])
+            ho["y"].copy_(s["y"], non_blocking=True); ho["S"].copy_(s["S"], non_blocking=True)
+            ho["z"].copy_(s["z"], non_blocking=True); ho["yd"].copy_(s["yd"], non_blocking=True)
+            ev["out"][b].record(s_out)
 
     e2e_steps = max(1, min(args.steps, 50))
-    with torch.cuda.stream(stream):
-        for _ in range(max(1, min(args.warmup, 5))):
-            e2e_step()
-        barrier()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        for _ in range(e2e_steps):
-            e2e_step()
-        e1.record(stream)
-        barrier()
+    n_warm = max(2, min(args.warmup, 5))
+    for i in range(n_warm):
+        e2e_step(i)
+    barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(s_in)
+    for i in range(n_warm, n_warm + e2e_steps):
+        e2e_step(i)
+    e1.record(s_out)
+    barrier()
     e2e_s = e0.elapsed_time(e1) / 1e3
     e2e_s, = reduce_max([e2e_s], dev, dist)
     assert _native.lib().la_last_device_status(sh) == 0
     e2e = {"value": whole_job_rate(tokens_per_step, world, e2e_steps, e2e_s), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
-           "d2h_bytes_per_step": d2h, "steps": e2e_steps, "ms_per_step": e2e_s / e2e_steps * 1e3}
+           "d2h_bytes_per_step": d2h, "steps": e2e_steps, "ms_per_step": e2e_s / e2e_steps * 1e3,
+           "pipelining": "copies in (step i+1), compute (step i) and copies out (step i-1) on three streams"}
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
