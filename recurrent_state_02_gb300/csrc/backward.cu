@@ -22,11 +22,14 @@
 //   kRevDk: reverse in time, one column per feature i, state G[i, :] and g_i;
 //   kRevDv: reverse in time, one column per value j, state G[:, j].
 // A CTA holds 32 columns; a lane holds L/8 state rows of two columns, the row
-// groups interleaved in blocks of 4 as in the delta-rule kernel, and reduces its
-// two reads over the 8 row groups with three shuffles.  Tokens come 32 at a
+// groups interleaved in blocks of 4 as in the delta-rule kernel.  A lane keeps
+// its partial reads of 8 tokens (2 columns each) and reduce-scatters them over
+// the 8 row groups at once (14 shuffles per 8 tokens), after which row-group
+// lane g holds both column totals of the group's token g.  Tokens come 32 at a
 // time: the TMA unit copies a block's two vector rows (contiguous) and its two
 // column slices into a double-buffered raw stage two blocks ahead, and the CTA
 // converts a landed block once to FP32, already transformed (phi, dy / d_t).
+// Finally a pass of one CTA per head turns the per-token terms into dalpha.
 
 #include "tc_common.cuh"
 
