@@ -258,6 +258,28 @@ la_status la_delta_rule(const void *q, const void *k, const void *v, la_dtype dt
                         la_stream_t stream);
 
 /*
+ * la_delta_rule_chunked -- the memory of la_delta_rule, computed in chunks of 64
+ * tokens on the tensor cores.  The pages give no block algorithm for this rule
+ * ([LA] "训练时，状态更新也能按块并行"); this one follows from the update: for a
+ * chunk with rows K, Q, V and the state S_prev before it, the written rows
+ * V' = beta (V - K S) of the chunk's tokens solve (I + L) V' = diag(beta) X with
+ * X = V - K S_prev and L = diag(beta) strictly-lower(K K^T), so
+ *     V' = T X,  T = (I + L)^{-1} diag(beta),
+ *     S_next = S_prev + K^T V',   Y = Q S_prev + (Q K^T masked causally, diagonal kept) V'.
+ * The products take BF16 operands (q, k, v as given, S_prev, X, T and V'
+ * rounded to BF16) with FP32 accumulation; the state stays FP32 across chunks
+ * and T is solved in FP32.  Same arguments, layouts and ownership as
+ * la_delta_rule; requires dtype BF16, r == 128, dv a multiple of 64, q, k, v, y,
+ * S0 and S_out 16-byte aligned, beta 4-byte aligned.  T may be 0 (S_out = S0).
+ * One CTA per (b, h, 64-column slice of v).
+ * Errors: LA_ERR_NULL, LA_ERR_SHAPE, LA_ERR_DTYPE (not BF16), LA_ERR_ALIGN,
+ *         LA_ERR_UNSUPPORTED (other r or dv), LA_ERR_CUDA.
+ */
+la_status la_delta_rule_chunked(const void *q, const void *k, const void *v, la_dtype dtype, const float *beta,
+                                const float *S0, int B, int H, int T, int r, int dv, void *y, float *S_out,
+                                la_stream_t stream);
+
+/*
  * la_last_device_status -- synchronise `stream`, then read and clear the device
  * status word of the current device: LA_OK, or LA_ERR_TIMEOUT when a kernel
  * gave up waiting on an on-chip barrier since the last read.  Returns

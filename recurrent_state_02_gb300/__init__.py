@@ -218,7 +218,19 @@ def prefill_backward(q, k, v, y, dy, alpha=None, S0=None, z0=None, dS_T=None, dz
 def delta_rule(q, k, v, beta=None, S0=None, y=None, S_out=None):
     """Delta-rule memory: p = S^T k, S += beta k (v - p)^T, y = S^T q (after the write).
     q, k [B,H,T,r], v [B,H,T,dv] (bf16 or fp32, same dtype); beta [B,H,T] fp32 or
-    None (1); S0 [B,H,r,dv] fp32 or None (zero).  Returns (y [B,H,T,dv], S_T)."""
+    None (1); S0 [B,H,r,dv] fp32 or None (zero).  Returns (y [B,H,T,dv], S_T).
+    The token recurrence in FP32 (la_delta_rule)."""
+    return _delta("la_delta_rule", q, k, v, beta, S0, y, S_out)
+
+
+def delta_rule_chunked(q, k, v, beta=None, S0=None, y=None, S_out=None):
+    """The same memory in chunks of 64 tokens on the tensor cores (la_delta_rule_chunked):
+    bf16 q, k [B,H,T,128], v [B,H,T,dv] with dv a multiple of 64; BF16 operands,
+    FP32 state.  Returns (y [B,H,T,dv], S_T)."""
+    return _delta("la_delta_rule_chunked", q, k, v, beta, S0, y, S_out)
+
+
+def _delta(entry, q, k, v, beta, S0, y, S_out):
     if q.dtype not in _DTYPES:
         raise ValueError(f"unsupported dtype {q.dtype}")
     B, H, T, r = q.shape
@@ -235,9 +247,9 @@ def delta_rule(q, k, v, beta=None, S0=None, y=None, S_out=None):
         S_out = torch.empty((B, H, r, dv), device=dev, dtype=torch.float32)
     _require(y, "y", (B, H, T, dv), q.dtype, dev)
     _require(S_out, "S_out", (B, H, r, dv), torch.float32, dev)
-    st = _native.lib().la_delta_rule(_ptr(q), _ptr(k), _ptr(v), _DTYPES[q.dtype], _ptr(beta), _ptr(S0), B, H, T,
-                                     r, dv, _ptr(y), _ptr(S_out), _stream(dev))
-    _native.check(st, "la_delta_rule")
+    st = getattr(_native.lib(), entry)(_ptr(q), _ptr(k), _ptr(v), _DTYPES[q.dtype], _ptr(beta), _ptr(S0), B, H, T,
+                                       r, dv, _ptr(y), _ptr(S_out), _stream(dev))
+    _native.check(st, entry)
     return y, S_out
 
 

@@ -1,6 +1,7 @@
 // api.cu -- the C ABI declared in include/linattn.h: argument validation,
 // kernel selection, TMA descriptor set-up and the device status word.
 #include "../../include/linattn.h"
+#include "delta_tc.h"
 #include "kernels.h"
 
 #include <cstdint>
@@ -415,6 +416,44 @@ la_status la_delta_rule(const void *q, const void *k, const void *v, la_dtype dt
     if (!status) return LA_ERR_CUDA;
     return from_cuda(la::launch_delta(q, k, v, dtype == LA_DTYPE_BF16, beta, S0, B, H, T, r, dv, y, S_out, status,
                                       la::kWaitLimitNs, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+la_status la_delta_rule_chunked(const void *q, const void *k, const void *v, la_dtype dtype, const float *beta,
+                                const float *S0, int B, int H, int T, int r, int dv, void *y, float *S_out,
+                                la_stream_t stream)
+{
+    if (!S_out || (T > 0 && (!q || !k || !v || !y))) return LA_ERR_NULL;
+    if (B < 1 || H < 1 || T < 0 || r < 1 || dv < 1) return LA_ERR_SHAPE;
+    if (dtype != LA_DTYPE_BF16) return LA_ERR_DTYPE;
+    if (r != 128 || dv % 64 != 0) return LA_ERR_UNSUPPORTED;
+    // one CTA per (b, h, 64-column slice)
+    if ((long long)B * H * (dv / 64) > 0x7fffffffLL) return LA_ERR_UNSUPPORTED;
+    if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(y, 16)) return LA_ERR_ALIGN;
+    if (!aligned(S_out, 16) || (S0 && !aligned(S0, 16)) || (beta && !aligned(beta, 4))) return LA_ERR_ALIGN;
+    int *status = status_word();
+    if (!status) return LA_ERR_CUDA;
+    const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    // no tokens: S_out = S0, as the token kernel does it
+    if (T == 0)
+        return from_cuda(la::launch_delta(q, k, v, true, beta, S0, B, H, T, r, dv, y, S_out, status,
+                                          la::kWaitLimitNs, st));
+    CUtensorMap mq, mk, mv;
+    const long long planes = (long long)B * H;
+    const CUtensorMapSwizzle sw128 = CU_TENSOR_MAP_SWIZZLE_128B;
+    if (!make_map_bf16(&mq, q, planes, T, r, 64, 64, sw128) || !make_map_bf16(&mk, k, planes, T, r, 64, 64, sw128) ||
+        !make_map_bf16(&mv, v, planes, T, dv, 64, 64, sw128))
+        return LA_ERR_CUDA;
+    la::DeltaTcArgs a;
+    a.beta = beta;
+    a.S0 = S0;
+    a.S_out = S_out;
+    a.y = static_cast<uint16_t *>(y);
+    a.H = H;
+    a.T = T;
+    a.dv = dv;
+    a.status = status;
+    a.wait_limit_ns = la::kWaitLimitNs;
+    return from_cuda(la::launch_delta_tc(mq, mk, mv, a, B, st));
 }
 
 la_status la_last_device_status(la_stream_t stream)

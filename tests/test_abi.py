@@ -168,6 +168,29 @@ def test_delta_rejects_bad_arguments(native):
     assert f(S_out=FAKE + 4) == native.LA_ERR_ALIGN
 
 
+def test_delta_chunked_rejects_bad_arguments(native):
+    L = native.lib()
+
+    def f(**kw):
+        a = dict(q=FAKE, k=FAKE, v=FAKE, dtype=native.LA_DTYPE_BF16, beta=None, S0=None, B=1, H=1, T=64, r=128,
+                 dv=128, y=FAKE, S_out=FAKE)
+        a.update(kw)
+        return L.la_delta_rule_chunked(a["q"], a["k"], a["v"], a["dtype"], a["beta"], a["S0"], a["B"], a["H"],
+                                       a["T"], a["r"], a["dv"], a["y"], a["S_out"], None)
+
+    assert f(k=None) == native.LA_ERR_NULL
+    assert f(S_out=None) == native.LA_ERR_NULL
+    assert f(H=0) == native.LA_ERR_SHAPE
+    assert f(T=-1) == native.LA_ERR_SHAPE
+    assert f(dtype=native.LA_DTYPE_FP32) == native.LA_ERR_DTYPE
+    assert f(r=64) == native.LA_ERR_UNSUPPORTED
+    assert f(dv=96) == native.LA_ERR_UNSUPPORTED
+    assert f(y=FAKE + 8) == native.LA_ERR_ALIGN
+    assert f(S0=FAKE + 8) == native.LA_ERR_ALIGN     # 16-byte alignment for the FP32 state here
+    assert f(S_out=FAKE + 8) == native.LA_ERR_ALIGN
+    assert f(beta=FAKE + 2) == native.LA_ERR_ALIGN
+
+
 def test_backward_rejects_bad_arguments(native):
     L = native.lib()
 

@@ -150,3 +150,100 @@ def test_delta_full_size_sampled_heads(la, oracle_mod):
         y_ref, S_ref = _oracle(oracle_mod, one)
         assert max_rel_err(S[b:b + 1, h:h + 1], S_ref) <= TOL_F32
         assert max_rel_err(y[b:b + 1, h:h + 1], y_ref) <= TOL_BF16
+
+
+# ---------------------------------------------------------------- chunked form
+# la_delta_rule_chunked rounds the operands of its products to BF16 (S_prev,
+# X = V - K S_prev, T and V'), with FP32 accumulation and an FP32 state; a
+# simulation of that rounding on unit keys gives about 5e-3 relative to the
+# largest entry on y and S over 2048 tokens.  Both are held to 2e-2.
+TOL_TC = 2e-2
+
+TC_CASES = [
+    # T, dv, H, with_state, with_beta
+    (1, 64, 2, True, True),
+    (63, 128, 2, False, True),
+    (64, 128, 2, True, True),
+    (65, 64, 3, True, False),
+    (200, 192, 2, True, True),     # three 64-column slices, ragged last chunk
+    (1000, 128, 1, True, True),
+    (2048, 64, 1, False, False),   # beta = 1
+]
+
+
+def _run_tc(la, d):
+    g = {k: (v.cuda() if v is not None else None) for k, v in d.items()}
+    y, S = la.delta_rule_chunked(g["q"], g["k"], g["v"], beta=g["beta"], S0=g["S0"])
+    assert la.last_device_status() == 0
+    return y.float().cpu().numpy(), S.cpu().numpy()
+
+
+@pytest.mark.parametrize("T,dv,H,with_state,with_beta", TC_CASES,
+                         ids=[f"T{c[0]}-dv{c[1]}-H{c[2]}-S{int(c[3])}-b{int(c[4])}" for c in TC_CASES])
+def test_delta_chunked_parity(la, oracle_mod, T, dv, H, with_state, with_beta):
+    d = _inputs(2, H, T, 128, dv, torch.bfloat16, with_state, with_beta, seed=300 + T + dv)
+    y_ref, S_ref = _oracle(oracle_mod, d)
+    y, S = _run_tc(la, d)
+    assert np.isfinite(y).all() and np.isfinite(S).all()
+    assert max_rel_err(S, S_ref) <= TOL_TC
+    assert max_rel_err(y, y_ref) <= TOL_TC
+
+
+def test_delta_chunked_pages_example(la):
+    """Three writes of one unit key with beta = 1/2 from S = 2 (the pages' repeated
+    writes): every product is exact in BF16, so the chunked form returns the
+    printed values exactly."""
+    cases = {c["name"]: c for c in json.load(open(GOLDEN))["cases"]}
+    c = cases["repeated_writes"]
+    n, r, dv = len(c["k"]), 128, 64
+    q = torch.zeros(1, 1, n, r, dtype=torch.bfloat16)
+    q[0, 0, :, 0] = 1.0
+    k = q.clone()
+    v = torch.zeros(1, 1, n, dv, dtype=torch.bfloat16)
+    v[0, 0, :, 0] = torch.tensor([x[0] for x in c["v"]], dtype=torch.bfloat16)
+    S0 = torch.zeros(1, 1, r, dv)
+    S0[0, 0, 0, 0] = c["S0"][0][0]
+    beta = torch.tensor(c["beta"], dtype=torch.float32).view(1, 1, n)
+    y, S = _run_tc(la, dict(q=q, k=k, v=v, beta=beta, S0=S0))
+    assert list(y[0, 0, :, 0]) == [s[0][0] for s in c["S_after_each_token"]]
+    assert S[0, 0, 0, 0] == c["S_after_each_token"][-1][0][0] and np.count_nonzero(S) == 1
+
+
+def test_delta_chunked_empty_sequence_copies_state(la):
+    d = _inputs(1, 2, 0, 128, 64, torch.bfloat16, True, True, seed=92)
+    g = {k: v.cuda() for k, v in d.items()}
+    y, S = la.delta_rule_chunked(g["q"], g["k"], g["v"], beta=g["beta"], S0=g["S0"])
+    assert la.last_device_status() == 0
+    assert y.shape == (1, 2, 0, 64) and torch.equal(S.cpu(), d["S0"])
+
+
+def test_delta_chunked_in_place_continuation(la):
+    """S0 may be S_out; split at a chunk boundary, two calls chained through the
+    FP32 state give the bits of one call."""
+    d = _inputs(1, 2, 300, 128, 128, torch.bfloat16, True, True, seed=93)
+    g = {k: v.cuda() for k, v in d.items()}
+    y_full, S_full = la.delta_rule_chunked(g["q"], g["k"], g["v"], beta=g["beta"], S0=g["S0"])
+    S = g["S0"].clone()
+    h = 128
+    y1, _ = la.delta_rule_chunked(g["q"][:, :, :h].contiguous(), g["k"][:, :, :h].contiguous(),
+                                  g["v"][:, :, :h].contiguous(), beta=g["beta"][:, :, :h].contiguous(), S0=S, S_out=S)
+    y2, _ = la.delta_rule_chunked(g["q"][:, :, h:].contiguous(), g["k"][:, :, h:].contiguous(),
+                                  g["v"][:, :, h:].contiguous(), beta=g["beta"][:, :, h:].contiguous(), S0=S, S_out=S)
+    assert la.last_device_status() == 0
+    assert torch.equal(torch.cat([y1, y2], dim=2), y_full)
+    assert torch.equal(S, S_full)
+
+
+def test_delta_chunked_full_size_sampled_heads(la, oracle_mod):
+    """B4 H16 T4096 r = dv = 128 BF16 through the chunked kernel, in the launch the
+    benchmark times; the oracle recomputes three sampled heads."""
+    from recurrent_state_02_gb300 import workloads as W
+    d = W.delta_inputs(W.DELTA)
+    y, S = _run_tc(la, d)
+    assert np.isfinite(y).all() and np.isfinite(S).all()
+    for b, h in ((0, 0), (1, 9), (3, 15)):
+        one = {k: v[b:b + 1, h:h + 1].contiguous() for k, v in d.items() if v is not None}
+        one["S0"] = None
+        y_ref, S_ref = _oracle(oracle_mod, one)
+        assert max_rel_err(S[b:b + 1, h:h + 1], S_ref) <= TOL_TC
+        assert max_rel_err(y[b:b + 1, h:h + 1], y_ref) <= TOL_TC
