@@ -53,7 +53,7 @@ typedef enum {
     LA_ERR_UNSUPPORTED = 5, /* a valid request that this build does not implement              */
     LA_ERR_CUDA = 6,        /* a CUDA runtime call or launch failed                            */
     LA_ERR_TIMEOUT = 7,     /* a kernel gave up waiting on an on-chip barrier                   */
-    LA_ERR_WORKSPACE = 8    /* workspace smaller than la_prefill_workspace_bytes, or NULL      */
+    LA_ERR_WORKSPACE = 8    /* workspace NULL or smaller than the entry point needs             */
 } la_status;
 
 typedef enum { LA_DTYPE_BF16 = 0, LA_DTYPE_FP32 = 1 } la_dtype;
@@ -258,6 +258,12 @@ la_status la_delta_rule(const void *q, const void *k, const void *v, la_dtype dt
                         la_stream_t stream);
 
 /*
+ * la_delta_chunked_workspace_bytes -- bytes of device workspace la_delta_rule_chunked
+ * needs for (B, H, T): 8 KB per chunk of 64 tokens per (b, h); 0 when T < 1.
+ */
+size_t la_delta_chunked_workspace_bytes(int B, int H, int T);
+
+/*
  * la_delta_rule_chunked -- the memory of la_delta_rule, computed in chunks of 64
  * tokens on the tensor cores.  The pages give no block algorithm for this rule
  * ([LA] "训练时，状态更新也能按块并行"); this one follows from the update: for a
@@ -269,14 +275,20 @@ la_status la_delta_rule(const void *q, const void *k, const void *v, la_dtype dt
  * The products take BF16 operands (q, k, v as given, S_prev, X, T and V'
  * rounded to BF16) with FP32 accumulation; the state stays FP32 across chunks
  * and T is solved in FP32.  Same arguments, layouts and ownership as
- * la_delta_rule; requires dtype BF16, r == 128, dv a multiple of 64, q, k, v, y,
- * S0 and S_out 16-byte aligned, beta 4-byte aligned.  T may be 0 (S_out = S0).
- * One CTA per (b, h, 64-column slice of v).
+ * la_delta_rule, plus
+ *   workspace  device buffer of >= la_delta_chunked_workspace_bytes(B, H, T) bytes,
+ *              16-byte aligned, owned by the caller (may be NULL when T == 0);
+ *              calls sharing it must be ordered.
+ * Kernels: T of every chunk (one CTA per chunk) into the workspace, then the
+ * state chain, one CTA per (b, h, 64-column slice of v).  Requires dtype BF16,
+ * r == 128, dv a multiple of 64, q, k, v, y, S0 and S_out 16-byte aligned, beta
+ * 4-byte aligned.  T may be 0 (S_out = S0).
  * Errors: LA_ERR_NULL, LA_ERR_SHAPE, LA_ERR_DTYPE (not BF16), LA_ERR_ALIGN,
- *         LA_ERR_UNSUPPORTED (other r or dv), LA_ERR_CUDA.
+ *         LA_ERR_UNSUPPORTED (other r or dv), LA_ERR_WORKSPACE, LA_ERR_CUDA.
  */
 la_status la_delta_rule_chunked(const void *q, const void *k, const void *v, la_dtype dtype, const float *beta,
                                 const float *S0, int B, int H, int T, int r, int dv, void *y, float *S_out,
+                                void *workspace, size_t workspace_bytes,
                                 la_stream_t stream);
 
 /*

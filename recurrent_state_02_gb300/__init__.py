@@ -220,17 +220,25 @@ def delta_rule(q, k, v, beta=None, S0=None, y=None, S_out=None):
     q, k [B,H,T,r], v [B,H,T,dv] (bf16 or fp32, same dtype); beta [B,H,T] fp32 or
     None (1); S0 [B,H,r,dv] fp32 or None (zero).  Returns (y [B,H,T,dv], S_T).
     The token recurrence in FP32 (la_delta_rule)."""
-    return _delta("la_delta_rule", q, k, v, beta, S0, y, S_out)
+    return _delta("la_delta_rule", q, k, v, beta, S0, y, S_out, None)
 
 
-def delta_rule_chunked(q, k, v, beta=None, S0=None, y=None, S_out=None):
+def delta_chunked_workspace_bytes(B, H, T) -> int:
+    return int(_native.lib().la_delta_chunked_workspace_bytes(B, H, T))
+
+
+def delta_rule_chunked(q, k, v, beta=None, S0=None, y=None, S_out=None, workspace=None):
     """The same memory in chunks of 64 tokens on the tensor cores (la_delta_rule_chunked):
     bf16 q, k [B,H,T,128], v [B,H,T,dv] with dv a multiple of 64; BF16 operands,
-    FP32 state.  Returns (y [B,H,T,dv], S_T)."""
-    return _delta("la_delta_rule_chunked", q, k, v, beta, S0, y, S_out)
+    FP32 state.  workspace: a device buffer of delta_chunked_workspace_bytes bytes
+    (allocated here when None).  Returns (y [B,H,T,dv], S_T)."""
+    B, H, T = q.shape[:3]
+    if workspace is None and T > 0:
+        workspace = torch.empty(delta_chunked_workspace_bytes(B, H, T), device=q.device, dtype=torch.uint8)
+    return _delta("la_delta_rule_chunked", q, k, v, beta, S0, y, S_out, workspace)
 
 
-def _delta(entry, q, k, v, beta, S0, y, S_out):
+def _delta(entry, q, k, v, beta, S0, y, S_out, workspace):
     if q.dtype not in _DTYPES:
         raise ValueError(f"unsupported dtype {q.dtype}")
     B, H, T, r = q.shape
@@ -247,8 +255,10 @@ def _delta(entry, q, k, v, beta, S0, y, S_out):
         S_out = torch.empty((B, H, r, dv), device=dev, dtype=torch.float32)
     _require(y, "y", (B, H, T, dv), q.dtype, dev)
     _require(S_out, "S_out", (B, H, r, dv), torch.float32, dev)
-    st = getattr(_native.lib(), entry)(_ptr(q), _ptr(k), _ptr(v), _DTYPES[q.dtype], _ptr(beta), _ptr(S0), B, H, T,
-                                       r, dv, _ptr(y), _ptr(S_out), _stream(dev))
+    args = [_ptr(q), _ptr(k), _ptr(v), _DTYPES[q.dtype], _ptr(beta), _ptr(S0), B, H, T, r, dv, _ptr(y), _ptr(S_out)]
+    if entry == "la_delta_rule_chunked":
+        args += [_ptr(workspace), 0 if workspace is None else workspace.numel() * workspace.element_size()]
+    st = getattr(_native.lib(), entry)(*args, _stream(dev))
     _native.check(st, entry)
     return y, S_out
 

@@ -27,7 +27,8 @@ SIGNATURES = {
                                         _fp, _vp]),
     "la_decode_step": (_i, [_vp, _vp, _vp, _i, _fp, _fp, _fp, _i, _i, _i, _i, _f, _vp, _vp]),
     "la_delta_rule": (_i, [_vp, _vp, _vp, _i, _fp, _fp, _i, _i, _i, _i, _i, _vp, _fp, _vp]),
-    "la_delta_rule_chunked": (_i, [_vp, _vp, _vp, _i, _fp, _fp, _i, _i, _i, _i, _i, _vp, _fp, _vp]),
+    "la_delta_chunked_workspace_bytes": (_sz, [_i, _i, _i]),
+    "la_delta_rule_chunked": (_i, [_vp, _vp, _vp, _i, _fp, _fp, _i, _i, _i, _i, _i, _vp, _fp, _vp, _sz, _vp]),
     "la_backward_workspace_bytes": (_sz, [_i, _i, _i]),
     "la_prefill_backward": (_i, [_vp, _vp, _vp, _i, _fp, _fp, _fp, _i, _i, _i, _i, _i, _f, _vp, _vp, _fp, _fp,
                                  _vp, _vp, _vp, _fp, _fp, _fp, _vp, _sz, _vp]),

@@ -418,9 +418,14 @@ la_status la_delta_rule(const void *q, const void *k, const void *v, la_dtype dt
                                       la::kWaitLimitNs, reinterpret_cast<cudaStream_t>(stream)));
 }
 
+size_t la_delta_chunked_workspace_bytes(int B, int H, int T)
+{
+    return la::delta_tc_workspace_bytes(B, H, T);
+}
+
 la_status la_delta_rule_chunked(const void *q, const void *k, const void *v, la_dtype dtype, const float *beta,
                                 const float *S0, int B, int H, int T, int r, int dv, void *y, float *S_out,
-                                la_stream_t stream)
+                                void *workspace, size_t workspace_bytes, la_stream_t stream)
 {
     if (!S_out || (T > 0 && (!q || !k || !v || !y))) return LA_ERR_NULL;
     if (B < 1 || H < 1 || T < 0 || r < 1 || dv < 1) return LA_ERR_SHAPE;
@@ -430,6 +435,10 @@ la_status la_delta_rule_chunked(const void *q, const void *k, const void *v, la_
     if ((long long)B * H * (dv / 64) > 0x7fffffffLL) return LA_ERR_UNSUPPORTED;
     if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(y, 16)) return LA_ERR_ALIGN;
     if (!aligned(S_out, 16) || (S0 && !aligned(S0, 16)) || (beta && !aligned(beta, 4))) return LA_ERR_ALIGN;
+    if (T > 0) {
+        if (!workspace || workspace_bytes < la::delta_tc_workspace_bytes(B, H, T)) return LA_ERR_WORKSPACE;
+        if (!aligned(workspace, 16)) return LA_ERR_ALIGN;
+    }
     int *status = status_word();
     if (!status) return LA_ERR_CUDA;
     const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
@@ -448,6 +457,7 @@ la_status la_delta_rule_chunked(const void *q, const void *k, const void *v, la_
     a.S0 = S0;
     a.S_out = S_out;
     a.y = static_cast<uint16_t *>(y);
+    a.ws = workspace;
     a.H = H;
     a.T = T;
     a.dv = dv;
