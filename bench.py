@@ -64,6 +64,12 @@ def delta_flops(B, H, T, r, dv):
     return B * H * T * 6 * r * dv
 
 
+def delta_bytes(B, H, T, r, dv, elem=2):
+    """Compulsory HBM bytes of one delta-rule call: q, k, v read and y written
+    (elem bytes each), beta read and the final state written (FP32)."""
+    return B * H * (T * (elem * (2 * r + 2 * dv) + 4) + 4 * r * dv)
+
+
 def backward_flops(B, H, T, r, dv, gated):
     """Algorithmic FLOPs of the backward: per token and head, the state write and
     the read S_t dn_t for dq (2 r dv each), the write of G and the reads G_t v_t
@@ -104,7 +110,9 @@ def source_sha1(paths):
 def kernel_sources(name):
     """The files a kernel is compiled from (its .cu and the headers it includes)."""
     csrc = os.path.join(ROOT, "recurrent_state_02_gb300", "csrc")
-    common = ("tc_common.cuh",) if name in ("prefill_tc.cu", "delta.cu") else ()
+    common = ("tc_common.cuh",) if name in ("prefill_tc.cu", "delta.cu", "delta_tc.cu") else ()
+    if name == "delta_tc.cu":
+        common += ("delta_tc.h",)
     return [os.path.join(csrc, f) for f in (name, "kernels.h", "sm103_ptx.cuh") + common]
 
 
@@ -480,33 +488,56 @@ def run_ours(args, rank, world, local_rank):
               "traffic": profile_traffic("decode128_kernel<true>", "B256 H16", kernel_sources("decode.cu"))}
 
     # delta-rule memory on its own workload (B=4, H=16, T=4096, r = dv = 128, BF16;
-    # q, k, v 201 MB > L2): one launch per replay
+    # q, k, v 201 MB > L2): the chunked tensor-core entry point (its two launches,
+    # T of every chunk and then the state chain) and the FP32 token recurrence,
+    # each replayed as a CUDA graph
     xw = W.DELTA
     xin = {k: (v.to(dev) if v is not None else None) for k, v in W.delta_inputs(xw, seed=xw.seed + 1000 * rank).items()}
     ydel = torch.empty((xw.B, xw.H, xw.T, xw.dv), device=dev, dtype=torch.bfloat16)
     Sdel = torch.empty((xw.B, xw.H, xw.r, xw.dv), device=dev, dtype=torch.float32)
+    xws_bytes = _native.lib().la_delta_chunked_workspace_bytes(xw.B, xw.H, xw.T)
+    xws = torch.empty(xws_bytes, device=dev, dtype=torch.uint8)
+
+    def k_delta_tc():
+        _native.check(L.la_delta_rule_chunked(P(xin["q"]), P(xin["k"]), P(xin["v"]), _native.LA_DTYPE_BF16,
+                                              P(xin["beta"]), None, xw.B, xw.H, xw.T, xw.r, xw.dv, P(ydel), P(Sdel),
+                                              P(xws), xws_bytes, sh), "la_delta_rule_chunked")
 
     def k_delta():
         _native.check(L.la_delta_rule(P(xin["q"]), P(xin["k"]), P(xin["v"]), _native.LA_DTYPE_BF16, P(xin["beta"]),
                                       None, xw.B, xw.H, xw.T, xw.r, xw.dv, P(ydel), P(Sdel), sh), "la_delta_rule")
 
-    with torch.cuda.stream(stream):
-        k_delta()
-    gx = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(gx, stream=stream):
-        k_delta()
-    x_s = timed([gx] * N_ROT, args.steps, args.warmup)
-    x_s, = reduce_max([x_s], dev, dist)
+    x_times = []
+    for fn in (k_delta_tc, k_delta):
+        with torch.cuda.stream(stream):
+            fn()
+        gx = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gx, stream=stream):
+            fn()
+        x_times.append(timed([gx] * N_ROT, args.steps, args.warmup))
+    xc_s, x_s = reduce_max(x_times, dev, dist)
     assert _native.lib().la_last_device_status(sh) == 0
-    x_launch = x_s / args.steps
+    xc_launch, x_launch = xc_s / args.steps, x_s / args.steps
+    xbytes = delta_bytes(xw.B, xw.H, xw.T, xw.r, xw.dv)
+    xc_gbs = xbytes / xc_launch / 1e9
     x_tflops = delta_flops(xw.B, xw.H, xw.T, xw.r, xw.dv) / x_launch / 1e12
     alu_peak = fp32_alu_peak_tflops(torch.cuda.get_device_properties(dev).multi_processor_count)
-    delta = {"workload": xw.name, "launch_us": x_launch * 1e6, "tokens_per_s": xw.B * xw.T * world / x_launch,
-             "roofline": {"bound": "alu", "achieved": x_tflops, "peak": alu_peak, "unit": "TFLOP/s",
-                          "frac": x_tflops / alu_peak, "peak_kind": "nominal FP32 FMA (SMs x 128 x 2 x max clock)",
-                          "traffic": profile_traffic("delta_kernel<bf16,128>", "B4 H16 T4096",
-                                                     kernel_sources("delta.cu")),
-                          "algorithmic_flops_per_launch": delta_flops(xw.B, xw.H, xw.T, xw.r, xw.dv)}}
+    delta = {"workload": xw.name, "entry": "la_delta_rule_chunked", "launch_us": xc_launch * 1e6,
+             "tokens_per_s": xw.B * xw.T * world / xc_launch,
+             "roofline": {"bound": "hbm", "achieved": xc_gbs, "peak": peak, "unit": "GB/s",
+                          "frac": xc_gbs / peak, "peak_kind": peak_kind,
+                          "timed": "the whole call (both launches)",
+                          "traffic": profile_traffic("delta_tc_kernel", "B4 H16 T4096",
+                                                     kernel_sources("delta_tc.cu")),
+                          "algorithmic_bytes_per_launch": xbytes},
+             "token_recurrence": {
+                 "entry": "la_delta_rule", "launch_us": x_launch * 1e6,
+                 "tokens_per_s": xw.B * xw.T * world / x_launch,
+                 "roofline": {"bound": "alu", "achieved": x_tflops, "peak": alu_peak, "unit": "TFLOP/s",
+                              "frac": x_tflops / alu_peak, "peak_kind": "nominal FP32 FMA (SMs x 128 x 2 x max clock)",
+                              "traffic": profile_traffic("delta_kernel<bf16,128>", "B4 H16 T4096",
+                                                         kernel_sources("delta.cu")),
+                              "algorithmic_flops_per_launch": delta_flops(xw.B, xw.H, xw.T, xw.r, xw.dv)}}}
 
     # backward pass on the gated shape of the prefill (B=4, H=16, T=4096, BF16,
     # alpha = sigmoid(N(3,1))): its five launches replayed as one CUDA graph
