@@ -60,65 +60,77 @@ __device__ __forceinline__ float2 hi2(float4 a) { return make_float2(a.z, a.w); 
 
 // ------------------------------------------------------------ d_t and dd_t
 
-// z_t and the feature sum of d_t: one warp per (b, h, 32 features), lane = feature.
-// Blocks of 32 tokens are staged in shared memory with 16-byte loads; the loads of
-// the next block are issued before the current block's recurrence runs and stored
-// after it.  A block's products q~_{t,i} z_{t,i} are summed over the warp's
-// features through a padded tile and added to d_acc[t] (zeroed before).
+// z_t and the feature sum of d_t: one CTA of kZSeg warps per (b, h, 32 features),
+// lane = feature.  z_t = alpha_t z_{t-1} + phi(k_t) is affine in z, so the sequence
+// is cut into kZSeg segments, one per warp.  Each warp first runs its segment from
+// z = 0, which gives the segment's map z -> P z + zs (P the product of its gates);
+// the maps of the segments before it, applied to z0 in order, give the warp its
+// true start, and it runs the segment again from there.  The products
+// q~_{t,i} z_{t,i} of blocks of kZB tokens are summed over the warp's features
+// through a padded tile and added to d_acc[t] (zeroed before).
+constexpr int kZSeg = 32;        // segments (warps) per sequence
+constexpr int kZB = 8;           // tokens per block of the second pass
+
 template <typename Tin>
-__global__ void __launch_bounds__(32)
+__global__ void __launch_bounds__(32 * kZSeg)
 bwd_z_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k, const float *__restrict__ alpha,
              const float *__restrict__ z0, int T, int r, float *__restrict__ d_acc)
 {
-    constexpr int kV = 16 / (int)sizeof(Tin);     // elements per 16-byte chunk
-    constexpr int kCh = 32 / kV;                  // chunks per row of 32 features
-    constexpr int kPer = 2 * kBT * kCh / 32;      // chunks per lane per block (q and k)
-    __shared__ __align__(16) Tin raw[2][2][kBT][32];   // [buffer][q, k][token][feature]
-    __shared__ float ga[2][kBT];
-    __shared__ float tile[kBT][kBT + 1];
-    const int nfg = r / 32, bh = blockIdx.x / nfg, lane = threadIdx.x;
-    const int i0 = (blockIdx.x % nfg) * 32;
-    float z = z0 ? z0[(size_t)bh * r + i0 + lane] : 0.f;
-    uint4 u[kPer];
-    float ad = 1.f;
-    auto load = [&](int t0) {
-        const int nt = min(kBT, T - t0);
+    __shared__ float tile[kZSeg][kZB][33];
+    __shared__ float segP[kZSeg], segZ[kZSeg][32];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int nfg = r / 32, bh = blockIdx.x / nfg, i0 = (blockIdx.x % nfg) * 32;
+    const int len = (T + kZSeg - 1) / kZSeg;
+    const int ta = min(T, warp * len), te = min(T, ta + len);
+    const Tin *kp = k + (size_t)bh * T * r + i0 + lane, *qp = q + (size_t)bh * T * r + i0 + lane;
+    const float *ap = alpha ? alpha + (size_t)bh * T : nullptr;
+
+    // 1: the segment's map, from z = 0
+    float z = 0.f, P = 1.f;
+    for (int t0 = ta; t0 < te; t0 += kZB) {
+        const int nt = min(kZB, te - t0);
+        float kv[kZB], av[kZB];
 #pragma unroll
-        for (int e = 0; e < kPer; ++e) {
-            const int c = lane + 32 * e, ten = c / (kBT * kCh), t = (c % (kBT * kCh)) / kCh, part = c % kCh;
-            u[e] = make_uint4(0u, 0u, 0u, 0u);
-            if (t < nt)
-                u[e] = *reinterpret_cast<const uint4 *>((ten ? k : q) + ((size_t)bh * T + t0 + t) * r + i0 + part * kV);
+        for (int t = 0; t < kZB; ++t) {
+            kv[t] = t < nt ? to_f32(kp[(size_t)(t0 + t) * r]) : 0.f;
+            av[t] = (ap && t < nt) ? ap[t0 + t] : 1.f;
         }
-        ad = (alpha && lane < nt) ? alpha[(size_t)bh * T + t0 + lane] : 1.f;
-    };
-    auto store = [&](int buf) {
 #pragma unroll
-        for (int e = 0; e < kPer; ++e) {
-            const int c = lane + 32 * e, ten = c / (kBT * kCh), t = (c % (kBT * kCh)) / kCh, part = c % kCh;
-            *reinterpret_cast<uint4 *>(&raw[buf][ten][t][part * kV]) = u[e];
-        }
-        ga[buf][lane] = ad;
-    };
-    load(0);
-    store(0);
-    __syncwarp();
-    for (int t0 = 0, cur = 0; t0 < T; t0 += kBT, cur ^= 1) {
-        const int nt = min(kBT, T - t0);
-        const bool more = t0 + kBT < T;
-        if (more) load(t0 + kBT);
-#pragma unroll
-        for (int t = 0; t < kBT; ++t)
+        for (int t = 0; t < kZB; ++t)
             if (t < nt) {
-                z = ga[cur][t] * z + phi_f(to_f32(raw[cur][1][t][lane]));
-                tile[t][lane] = phi_f(to_f32(raw[cur][0][t][lane])) * z;
+                z = av[t] * z + phi_f(kv[t]);
+                P *= av[t];
+            }
+    }
+    if (lane == 0) segP[warp] = P;
+    segZ[warp][lane] = z;
+    __syncthreads();
+
+    // 2: the true start of the segment, then the segment again with its products
+    z = z0 ? z0[(size_t)bh * r + i0 + lane] : 0.f;
+    for (int u = 0; u < warp; ++u) z = segP[u] * z + segZ[u][lane];
+    for (int t0 = ta; t0 < te; t0 += kZB) {
+        const int nt = min(kZB, te - t0);
+        float kv[kZB], qv[kZB], av[kZB];
+#pragma unroll
+        for (int t = 0; t < kZB; ++t) {
+            kv[t] = t < nt ? to_f32(kp[(size_t)(t0 + t) * r]) : 0.f;
+            qv[t] = t < nt ? to_f32(qp[(size_t)(t0 + t) * r]) : 0.f;
+            av[t] = (ap && t < nt) ? ap[t0 + t] : 1.f;
+        }
+#pragma unroll
+        for (int t = 0; t < kZB; ++t)
+            if (t < nt) {
+                z = av[t] * z + phi_f(kv[t]);
+                tile[warp][t][lane] = phi_f(qv[t]) * z;
             }
         __syncwarp();
-        float s = 0.f;
+        if (lane < nt) {
+            float s = 0.f;
 #pragma unroll 8
-        for (int f = 0; f < 32; ++f) s += tile[lane][f];
-        if (lane < nt) atomicAdd(&d_acc[(size_t)bh * T + t0 + lane], s);
-        if (more) store(cur ^ 1);
+            for (int f = 0; f < 32; ++f) s += tile[warp][lane][f];
+            atomicAdd(&d_acc[(size_t)bh * T + t0 + lane], s);
+        }
         __syncwarp();
     }
 }
@@ -601,7 +613,7 @@ cudaError_t launch_bwd_t(const BackwardArgs &a, int B, cudaStream_t stream)
     // d accumulates the feature sums; tok_sum and fin accumulate dalpha terms
     cudaError_t e = cudaMemsetAsync(a.ws, 0, sizeof(float) * (3 * n + BH), stream);
     if (e != cudaSuccess) return e;
-    bwd_z_kernel<Tin><<<(unsigned)(BH * (a.r / 32)), 32, 0, stream>>>(
+    bwd_z_kernel<Tin><<<(unsigned)(BH * (a.r / 32)), 32 * kZSeg, 0, stream>>>(
         static_cast<const Tin *>(a.q), static_cast<const Tin *>(a.k), a.alpha, a.z0, a.T, a.r, d);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     bwd_dd_kernel<Tin><<<152 * 8, 256, 0, stream>>>(static_cast<const Tin *>(a.y), static_cast<const Tin *>(a.dy),
