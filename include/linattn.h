@@ -259,7 +259,7 @@ la_status la_delta_rule(const void *q, const void *k, const void *v, la_dtype dt
 
 /*
  * la_delta_chunked_workspace_bytes -- bytes of device workspace la_delta_rule_chunked
- * needs for (B, H, T): 8 KB per chunk of 64 tokens per (b, h); 0 when T < 1.
+ * needs for (B, H, T): 16 KB per chunk of 64 tokens per (b, h); 0 when T < 1.
  */
 size_t la_delta_chunked_workspace_bytes(int B, int H, int T);
 
@@ -279,8 +279,9 @@ size_t la_delta_chunked_workspace_bytes(int B, int H, int T);
  *   workspace  device buffer of >= la_delta_chunked_workspace_bytes(B, H, T) bytes,
  *              16-byte aligned, owned by the caller (may be NULL when T == 0);
  *              calls sharing it must be ordered.
- * Kernels: T of every chunk (one CTA per chunk) into the workspace, then the
- * state chain, one CTA per (b, h, 64-column slice of v).  Requires dtype BF16,
+ * Kernels: T and the masked scores (Q K^T) . M of every chunk (one CTA per
+ * chunk) into the workspace, then the state chain, one CTA per (b, h, 64-column
+ * slice of v).  Requires dtype BF16,
  * r == 128, dv a multiple of 64, q, k, v, y, S0 and S_out 16-byte aligned, beta
  * 4-byte aligned.  T may be 0 (S_out = S0).
  * Errors: LA_ERR_NULL, LA_ERR_SHAPE, LA_ERR_DTYPE (not BF16), LA_ERR_ALIGN,

@@ -12,20 +12,21 @@
 //     V' = T X,   S_next = S_prev + K^T V',   O = Q S_prev + ((Q K^T) . M) V',
 // M the causal mask with its diagonal (the read follows the write).
 //
-// T depends on the keys and beta alone, so it is solved for every chunk at once
-// by a first kernel (delta_t_kernel: one CTA per chunk, G = K K^T on the tensor
-// cores, the solve in FP32 on CUDA cores in 2 x 2 blocks of 32 tokens: T00 and
-// T11 by forward substitution with one column per lane, T10 = -T11 (K1 K0^T) T00)
-// and stored as the BF16 shared-memory image of the chunk's T tile.  The second
-// kernel (delta_tc_kernel) then runs only the part that carries the state:
-//   1  [KS; QS] = [K; Q] S_prev (M = 128), P = Q K^T        (MMA)
-//   2  X = V - KS, A = P . M (BF16)
+// T and A = (Q K^T) . M depend on q, k and beta alone, so a first kernel
+// (delta_t_kernel: one CTA per chunk) forms them for every chunk at once:
+// [G; P] = [K; Q] K^T on the tensor cores, A from P, and T from G, solved in FP32
+// on CUDA cores in 2 x 2 blocks of 32 tokens (T00 and T11 by forward
+// substitution with one column per lane, T10 = -T11 (K1 K0^T) T00).  Both are
+// stored as the BF16 shared-memory images of the chunk's operand tiles.  The
+// second kernel (delta_tc_kernel) then runs only the part that carries the state:
+//   1  [KS; QS] = [K; Q] S_prev (M = 128)                  (MMA)
+//   2  X = V - KS (BF16)
 //   3  V' = T X                                            (MMA)
 //   4  V' (BF16)
 //   5  [.; O] = [KS; QS] + [0; A] V', S += K^T V'          (MMA)
 //   6  y = O (BF16), S_prev = S (BF16)
 // with one CTA of 256 threads per (b, h, 64-column slice of v); lane 0 of warp 0
-// loads the tiles of a chunk (q, k, v by TMA, T by a bulk copy; two stages),
+// loads the tiles of a chunk (q, k, v by TMA, A and T by a bulk copy; two stages),
 // lane 0 of warp 1 issues the MMAs, and all 8 warps move accumulators between
 // TMEM and shared memory (warp w: TMEM lane quadrant w % 4, column half w / 4).
 // Operand layouts follow the prefill kernel's: 64-feature blocks and V-shaped
@@ -47,14 +48,19 @@ constexpr uint32_t kHi128 = desc_hi(1024, 2), kHi32 = desc_hi(256, 6);   // SBO 
 
 // ------------------------------------------------------------- T per chunk
 constexpr int kPThreads = 128;
-constexpr uint32_t kPK = 0;                      // K tile
-constexpr uint32_t kPT = kTQ;                    // T (BF16 image)
-constexpr uint32_t kPL = kPT + kTV;              // Lt (FP32, 64 x LD): Lt[u][i] holds row i, column u
+// K and Q interleaved by 64-feature block ([K; Q] is one 128-row operand per
+// block); once [G; P] is complete the region holds L and the solve's FP32 blocks
+constexpr uint32_t kPKQ = 0;
+constexpr uint32_t kPL = 0;                      // Lt (FP32, 64 x LD): Lt[u][i] holds row i, column u
 constexpr uint32_t kPT00 = kPL + kC * LD * 4;    // T00 (FP32, [u][j])
 constexpr uint32_t kPT11t = kPT00 + 32 * LDT * 4;   // T11 transposed (FP32, [u][i])
 constexpr uint32_t kPM = kPT11t + 32 * LDT * 4;  // M = (K1 K0^T) T00 (FP32, [u][j])
-constexpr uint32_t kPBeta = kPM + 32 * LDT * 4;  // beta of the chunk
+constexpr uint32_t kPT = 2 * kTQ;                // T (BF16 image)
+constexpr uint32_t kPBeta = kPT + kTV;           // beta of the chunk
 constexpr uint32_t kPSmall = kPBeta + kC * 4;
+static_assert(kPM + 32 * LDT * 4 <= 2 * kTQ, "L and the solve's blocks fit in the K, Q region");
+// workspace per chunk: the A image, then the T image
+constexpr uint32_t kWsChunk = 2 * kTV;
 static_assert(kPT % 1024 == 0 && kPL % 16 == 0 && kPT00 % 16 == 0 && kPT11t % 16 == 0 && kPM % 16 == 0 &&
                   kPSmall % 16 == 0,
               "alignment");
@@ -62,20 +68,19 @@ static_assert(kPT % 1024 == 0 && kPL % 16 == 0 && kPT00 % 16 == 0 && kPT11t % 16
 // --------------------------------------------------------- the state chain
 constexpr int kMThreads = 256;
 // a stage: K and Q interleaved by 64-feature block, so that [K; Q] is one
-// 128-row operand per block, then V and T
-constexpr uint32_t kSK0 = 0, kSQ0 = kTQ / 2, kSK1 = kTQ, kSQ1 = kTQ + kTQ / 2, kSV = 2 * kTQ, kST = kSV + kTV;
-constexpr uint32_t kStage = kST + kTV;           // 48 KB
-constexpr uint32_t kMZ = 2 * kStage;             // zero rows 0..63 of the operand [0; A]
-constexpr uint32_t kMA = kMZ + kTV;              // A = P . M (BF16)
-constexpr uint32_t kMX = kMA + kTV;              // X (BF16, V-shaped)
+// 128-row operand per block, then V, a zero tile (rows 0..63 of the operand
+// [0; A]), A and T (A and T arrive together from the workspace)
+constexpr uint32_t kSK0 = 0, kSQ0 = kTQ / 2, kSK1 = kTQ, kSQ1 = kTQ + kTQ / 2, kSV = 2 * kTQ;
+constexpr uint32_t kSZ = kSV + kTV, kSA = kSZ + kTV, kST = kSA + kTV;
+constexpr uint32_t kStage = kST + kTV;           // 64 KB
+constexpr uint32_t kMX = 2 * kStage;             // X (BF16, V-shaped)
 constexpr uint32_t kMVp = kMX + kTV;             // V' (BF16, V-shaped)
 constexpr uint32_t kMSp = kMVp + kTV;            // S_prev (BF16, 128 x 64: 4 blocks of 16 columns)
 constexpr uint32_t kMSmall = kMSp + kR * kDS * 2;
-static_assert(kStage % 1024 == 0 && kMZ % 1024 == 0 && kMA % 1024 == 0 && kMX % 1024 == 0 && kMVp % 1024 == 0 &&
-                  kMSp % 1024 == 0,
+static_assert(kStage % 1024 == 0 && kMX % 1024 == 0 && kMVp % 1024 == 0 && kMSp % 1024 == 0,
               "swizzled tiles stay 1024-byte aligned");
-// TMEM columns: [KS; QS] then O (M = 128), P (M = 64), V' (M = 64), S (M = 128)
-constexpr uint32_t kCKQ = 0, kCP = 64, kCV = 128, kCS = 192, kMCols = 256;
+// TMEM columns: [KS; QS] then O (M = 128), V' (M = 64), S (M = 128)
+constexpr uint32_t kCKQ = 0, kCV = 64, kCS = 128, kMCols = 256;
 
 struct alignas(16) DSmall {
     uint64_t full[2], mma;
@@ -116,10 +121,12 @@ __device__ __forceinline__ uint32_t tile_off(int row, int col)
     return sw128_offset(row, col >> 3) + (uint32_t)(col & 7) * 2;
 }
 
-// T = (I + L)^{-1} diag(beta) of one chunk: one CTA of 128 threads per
-// (b, h, chunk).  Writes the 8 KB BF16 image of the T tile to ws.
+// A = (Q K^T) . M and T = (I + L)^{-1} diag(beta) of one chunk: one CTA of 128
+// threads per (b, h, chunk).  Writes the 8 KB BF16 images of the A and T tiles
+// to ws.
 __global__ void __launch_bounds__(kPThreads)
-delta_t_kernel(const __grid_constant__ CUtensorMap map_k, const DeltaTcArgs args, int nch)
+delta_t_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
+               const DeltaTcArgs args, int nch)
 {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *base = align1024(smem_raw);
@@ -155,24 +162,27 @@ delta_t_kernel(const __grid_constant__ CUtensorMap map_k, const DeltaTcArgs args
     tc_fence_after();
     const uint32_t tmem = sm->tmem_base;
     if (tid == 0) {
-        mbar_arrive_expect_tx(&sm->full[0], kTQ);
-        tma_load_3d(base + kPK, &map_k, &sm->full[0], 0, t0, bh);
-        tma_load_3d(base + kPK + kTQ / 2, &map_k, &sm->full[0], 64, t0, bh);
+        mbar_arrive_expect_tx(&sm->full[0], 2 * kTQ);
+        tma_load_3d(base + kPKQ, &map_k, &sm->full[0], 0, t0, bh);
+        tma_load_3d(base + kPKQ + kTQ / 2, &map_q, &sm->full[0], 0, t0, bh);
+        tma_load_3d(base + kPKQ + kTQ, &map_k, &sm->full[0], 64, t0, bh);
+        tma_load_3d(base + kPKQ + kTQ + kTQ / 2, &map_q, &sm->full[0], 64, t0, bh);
     }
+    uint8_t *wsc = static_cast<uint8_t *>(args.ws) + ((size_t)bh * nch + c) * kWsChunk;
 
-    // G = K K^T (M = 64: row i in lane 16 (i / 16) + i % 16)
+    // [G; P] = [K; Q] K^T (M = 128: G in TMEM lanes 0..63, P in lanes 64..127)
     bool issued = false, ok = true;
     if (warp == 1) {
         ok = warp_wait(cx, &sm->full[0], 0);
         if (ok && lane == 0) {
             tc_fence_after();
-            constexpr uint32_t idKK = idesc_bf16_f32(64, 64, false, false);
-            const uint32_t klo = desc_lo(smem_u32(base + kPK), 16);
+            constexpr uint32_t idGP = idesc_bf16_f32(128, 64, false, false);
+            const uint32_t klo = desc_lo(smem_u32(base + kPKQ), 16);
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk) {
-                const uint32_t o = ((kk >> 2) * (kTQ / 2) + (kk & 3) * 32) >> 4;
-                if (kk == 0) tc_mma_bf16_w<false>(tmem, klo, kHi128, klo, kHi128, idKK);
-                else tc_mma_bf16_w<true>(tmem, klo + o, kHi128, klo + o, kHi128, idKK);
+                const uint32_t o = ((kk >> 2) * kTQ + (kk & 3) * 32) >> 4;
+                if (kk == 0) tc_mma_bf16_w<false>(tmem, klo, kHi128, klo, kHi128, idGP);
+                else tc_mma_bf16_w<true>(tmem, klo + o, kHi128, klo + o, kHi128, idGP);
             }
             tc_commit(&sm->mma);
             issued = true;
@@ -182,27 +192,37 @@ delta_t_kernel(const __grid_constant__ CUtensorMap map_k, const DeltaTcArgs args
     ok = warp_wait(cx, &sm->mma, 0) && ok;
     tc_fence_after();
     if (!__syncthreads_or(!ok)) {
-        // L = diag(beta) strictly-lower(G) in the two diagonal 32-blocks and the
-        // raw block G10 = K1 K0^T, stored transposed: Lt[j][i] = L[i][j].  Warp q
-        // holds rows 16 q .. 16 q + 15; lanes 16..31 the right half of the columns.
+        // Warps 0, 1 (TMEM lanes 0..63): L = diag(beta) strictly-lower(G) in the two
+        // diagonal 32-blocks and the raw block G10 = K1 K0^T, stored transposed:
+        // Lt[j][i] = L[i][j].  Warps 2, 3 (lanes 64..127): A = P . M, stored as the
+        // BF16 image of its tile (row i: 128 bytes, 16-byte chunk x at x ^ (i % 8)).
         {
-            const int ri = 16 * warp + (lane & 15), hh = lane >> 4;
-            float g[32], a[16], b[16];
+            const int ri = 32 * (warp & 1) + lane;   // token row of G (warps 0, 1) or P (2, 3)
+            float v0[32], v1[32];
             const uint32_t tq = tmem + ((uint32_t)(32 * warp) << 16);
-            tc_ld_16x32bx2_x16<32>(tq, a);
-            tc_ld_16x32bx2_x16<32>(tq + 16, b);
+            tc_ld_32x32b_x32(tq, v0);
+            tc_ld_32x32b_x32(tq + 32, v1);
             tc_wait_ld();
+            if (warp < 2) {
+                const float bi = bc[ri];
 #pragma unroll
-            for (int e = 0; e < 16; ++e) {
-                g[e] = a[e];
-                g[16 + e] = b[e];
-            }
-            const bool raw = ri >= 32 && hh == 0, diag = (hh == 0) == (ri < 32);
-            const float sc = raw ? 1.f : bc[ri];
+                for (int j = 0; j < 64; ++j) {
+                    const float g = j < 32 ? v0[j] : v1[j - 32];
+                    const bool raw = ri >= 32 && j < 32, diag = (j < 32) == (ri < 32);
+                    if (raw || (diag && j < ri)) Lt[j * LD + ri] = (raw ? 1.f : bi) * g;
+                }
+            } else {
+                uint8_t *arow = wsc + (size_t)ri * 128;
 #pragma unroll
-            for (int e = 0; e < 32; ++e) {
-                const int j = 32 * hh + e;
-                if (raw || (diag && j < ri)) Lt[j * LD + ri] = sc * g[e];
+                for (int x = 0; x < 8; ++x) {
+                    float a[8];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        const int j = 8 * x + e;
+                        a[e] = j <= ri ? (j < 32 ? v0[j] : v1[j - 32]) : 0.f;
+                    }
+                    *reinterpret_cast<uint4 *>(arow + ((x ^ (ri & 7)) << 4)) = pack8(a);
+                }
             }
         }
         __syncthreads();
@@ -276,7 +296,7 @@ delta_t_kernel(const __grid_constant__ CUtensorMap map_k, const DeltaTcArgs args
                 *reinterpret_cast<uint16_t *>(base + kPT + tile_off(32 + 8 * warp + e, lane)) = bf16_bits(-o8[e]);
         }
         __syncthreads();
-        uint4 *dst = reinterpret_cast<uint4 *>(static_cast<uint8_t *>(args.ws) + ((size_t)bh * nch + c) * kTV);
+        uint4 *dst = reinterpret_cast<uint4 *>(wsc + kTV);
         const uint4 *src = reinterpret_cast<const uint4 *>(base + kPT);
         for (int x = tid; x < (int)(kTV / 16); x += kPThreads) dst[x] = src[x];
     } else {
@@ -309,7 +329,7 @@ delta_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
     const int bh = blockIdx.x / nslice, slice = blockIdx.x % nslice;
     const int T = args.T;
     Ctx cx{&sm->abort_flag, args.wait_limit_ns, args.status};
-    const uint8_t *tws = static_cast<const uint8_t *>(args.ws) + (size_t)bh * nch * kTV;
+    const uint8_t *tws = static_cast<const uint8_t *>(args.ws) + (size_t)bh * nch * kWsChunk;
 
     if (tid == 0) {
         mbar_init(&sm->full[0], 1);
@@ -322,8 +342,9 @@ delta_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
         tmem_alloc(&sm->tmem_base, kMCols);
         tmem_relinquish();
     }
-    for (int x = tid; x < (int)(kTV / 16); x += kMThreads)   // rows 0..63 of [0; A]
-        reinterpret_cast<uint4 *>(base + kMZ)[x] = make_uint4(0, 0, 0, 0);
+    for (int x = tid; x < (int)(2 * kTV / 16); x += kMThreads)   // rows 0..63 of [0; A], both stages
+        reinterpret_cast<uint4 *>(base + (x >= (int)(kTV / 16) ? kStage : 0) + kSZ)[x % (kTV / 16)] =
+            make_uint4(0, 0, 0, 0);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -333,13 +354,13 @@ delta_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
     auto issue = [&](int c) {
         const int s = c & 1, t0 = c * kC;
         uint8_t *st = base + s * kStage;
-        mbar_arrive_expect_tx(&sm->full[s], kStage);
+        mbar_arrive_expect_tx(&sm->full[s], kStage - kTV);   // all but the zero tile
         tma_load_3d(st + kSK0, &map_k, &sm->full[s], 0, t0, bh);
         tma_load_3d(st + kSQ0, &map_q, &sm->full[s], 0, t0, bh);
         tma_load_3d(st + kSK1, &map_k, &sm->full[s], 64, t0, bh);
         tma_load_3d(st + kSQ1, &map_q, &sm->full[s], 64, t0, bh);
         tma_load_3d(st + kSV, &map_v, &sm->full[s], slice * kDS, t0, bh);
-        bulk_load(st + kST, tws + (size_t)c * kTV, kTV, &sm->full[s]);
+        bulk_load(st + kSA, tws + (size_t)c * kWsChunk, kWsChunk, &sm->full[s]);   // A, T
     };
     int issued = 0;   // chunks whose loads were started (lane 0 of warp 0)
     if (tid == 0) {
@@ -386,10 +407,9 @@ delta_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
     __syncthreads();
 
     constexpr uint32_t idKQ = idesc_bf16_f32(128, 64, false, true);   // [K; Q] S_prev, [0; A] V'
-    constexpr uint32_t idP = idesc_bf16_f32(64, 64, false, false);    // Q K^T
     constexpr uint32_t idTX = idesc_bf16_f32(64, 64, false, true);    // T X
     constexpr uint32_t idS = idesc_bf16_f32(128, 64, true, true);     // K^T V'
-    const uint32_t aZ = smem_u32(base + kMZ), aA = smem_u32(base + kMA), aX = smem_u32(base + kMX);
+    const uint32_t aX = smem_u32(base + kMX);
     const uint32_t aVp = smem_u32(base + kMVp), aSp = smem_u32(base + kMSp);
     uint32_t mph = 0;       // completions of sm->mma consumed (every thread)
     int commits = 0;        // commits on sm->mma issued (lane 0 of warp 1)
@@ -405,7 +425,7 @@ delta_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
         const int s = c & 1, t0 = c * kC;
         const uint32_t st = smem_u32(base + s * kStage);
 
-        // ---- 1: [KS; QS] = [K; Q] S_prev, P = Q K^T
+        // ---- 1: [KS; QS] = [K; Q] S_prev
         if (warp == 1) {
             const bool ok = warp_wait(cx, &sm->full[s], (c >> 1) & 1);
             if (ok && lane == 0) {
@@ -413,15 +433,9 @@ delta_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
                 const uint32_t slo = desc_lo(aSp, kR * 32);
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk) {
-                    const uint32_t o = ((kk >> 2) * kTQ + (kk & 3) * 32) >> 4;
-                    const uint32_t kqlo = desc_lo(st + kSK0, 16) + o, qlo = desc_lo(st + kSQ0, 16) + o;
-                    if (kk == 0) {
-                        tc_mma_bf16_w<false>(tmem + kCKQ, kqlo, kHi128, slo, kHi32, idKQ);
-                        tc_mma_bf16_w<false>(tmem + kCP, qlo, kHi128, kqlo, kHi128, idP);
-                    } else {
-                        tc_mma_bf16_w<true>(tmem + kCKQ, kqlo, kHi128, slo + kk * (512 >> 4), kHi32, idKQ);
-                        tc_mma_bf16_w<true>(tmem + kCP, qlo, kHi128, kqlo, kHi128, idP);
-                    }
+                    const uint32_t kqlo = desc_lo(st + kSK0, 16) + (((kk >> 2) * kTQ + (kk & 3) * 32) >> 4);
+                    if (kk == 0) tc_mma_bf16_w<false>(tmem + kCKQ, kqlo, kHi128, slo, kHi32, idKQ);
+                    else tc_mma_bf16_w<true>(tmem + kCKQ, kqlo, kHi128, slo + kk * (512 >> 4), kHi32, idKQ);
                 }
                 tc_commit(&sm->mma);
                 ++commits;
@@ -430,33 +444,20 @@ delta_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
         }
         if (__syncthreads_or(!mma_wait())) break;
 
-        // ---- 2: X = V - KS (token rows 0..63 are lanes 0..63), A = P . M
-        {
-            float p[16];
-            tc_ld_16x32bx2_x16<16>(tq + kCP + 32 * ch, p);
-            if (q4 < 2) {
-                float ks[32];
-                tc_ld_32x32b_x32(tq + kCKQ + 32 * ch, ks);
-                tc_wait_ld();
-                const uint8_t *vt = base + s * kStage + kSV;
+        // ---- 2: X = V - KS (token rows 0..63 are TMEM lanes 0..63)
+        if (q4 < 2) {
+            float ks[32];
+            tc_ld_32x32b_x32(tq + kCKQ + 32 * ch, ks);
+            tc_wait_ld();
+            const uint8_t *vt = base + s * kStage + kSV;
 #pragma unroll
-                for (int m = 0; m < 4; ++m) {
-                    const uint32_t off = sw128_offset(f, 4 * ch + m);
-                    float vf[8];
-                    unpack8(*reinterpret_cast<const uint4 *>(vt + off), vf);
+            for (int m = 0; m < 4; ++m) {
+                const uint32_t off = sw128_offset(f, 4 * ch + m);
+                float vf[8];
+                unpack8(*reinterpret_cast<const uint4 *>(vt + off), vf);
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) vf[e] -= ks[8 * m + e];
-                    *reinterpret_cast<uint4 *>(base + kMX + off) = pack8(vf);
-                }
-            } else {
-                tc_wait_ld();
-            }
-#pragma unroll
-            for (int m = 0; m < 2; ++m) {
-                float a[8];
-#pragma unroll
-                for (int e = 0; e < 8; ++e) a[e] = cm + 8 * m + e <= rm ? p[8 * m + e] : 0.f;
-                *reinterpret_cast<uint4 *>(base + kMA + sw128_offset(rm, (cm >> 3) + m)) = pack8(a);
+                for (int e = 0; e < 8; ++e) vf[e] -= ks[8 * m + e];
+                *reinterpret_cast<uint4 *>(base + kMX + off) = pack8(vf);
             }
             fence_proxy_async_smem();
             tc_fence_before();
@@ -497,7 +498,7 @@ delta_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
         if (warp == 1) {
             if (lane == 0) {
                 tc_fence_after();
-                const uint32_t zlo = desc_lo(aZ, 16), vlo = desc_lo(aVp, kTV), klo = desc_lo(st + kSK0, kTQ);
+                const uint32_t zlo = desc_lo(st + kSZ, 16), vlo = desc_lo(aVp, kTV), klo = desc_lo(st + kSK0, kTQ);
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk)
                     tc_mma_bf16_w<true>(tmem + kCKQ, zlo + kk * (32 >> 4), kHi128, vlo + kk * (2048 >> 4), kHi128, idKQ);
@@ -584,7 +585,7 @@ cudaError_t set_smem_once(K kern, uint32_t bytes, bool (&done)[64])
 size_t delta_tc_workspace_bytes(int B, int H, int T)
 {
     if (B < 1 || H < 1 || T < 1) return 0;
-    return (size_t)B * H * ((T + kC - 1) / kC) * kTV;
+    return (size_t)B * H * ((T + kC - 1) / kC) * kWsChunk;
 }
 
 cudaError_t launch_delta_tc(const CUtensorMap &map_q, const CUtensorMap &map_k, const CUtensorMap &map_v,
@@ -599,7 +600,7 @@ cudaError_t launch_delta_tc(const CUtensorMap &map_q, const CUtensorMap &map_k, 
     if (e != cudaSuccess) return e;
     e = set_smem_once(delta_tc_kernel, kMSmemBytes, done_m);
     if (e != cudaSuccess) return e;
-    delta_t_kernel<<<(unsigned)nprep, kPThreads, kPSmemBytes, stream>>>(map_k, a, nch);
+    delta_t_kernel<<<(unsigned)nprep, kPThreads, kPSmemBytes, stream>>>(map_q, map_k, a, nch);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     delta_tc_kernel<<<(unsigned)nmain, kMThreads, kMSmemBytes, stream>>>(map_q, map_k, map_v, a, nch);

@@ -173,13 +173,13 @@ def test_delta_chunked_rejects_bad_arguments(native):
 
     def f(**kw):
         a = dict(q=FAKE, k=FAKE, v=FAKE, dtype=native.LA_DTYPE_BF16, beta=None, S0=None, B=1, H=1, T=64, r=128,
-                 dv=128, y=FAKE, S_out=FAKE, ws=FAKE, ws_bytes=8192)
+                 dv=128, y=FAKE, S_out=FAKE, ws=FAKE, ws_bytes=16384)
         a.update(kw)
         return L.la_delta_rule_chunked(a["q"], a["k"], a["v"], a["dtype"], a["beta"], a["S0"], a["B"], a["H"],
                                        a["T"], a["r"], a["dv"], a["y"], a["S_out"], a["ws"], a["ws_bytes"], None)
 
-    assert L.la_delta_chunked_workspace_bytes(4, 16, 4096) == 4 * 16 * 64 * 8192
-    assert L.la_delta_chunked_workspace_bytes(1, 1, 65) == 2 * 8192
+    assert L.la_delta_chunked_workspace_bytes(4, 16, 4096) == 4 * 16 * 64 * 16384
+    assert L.la_delta_chunked_workspace_bytes(1, 1, 65) == 2 * 16384
     assert L.la_delta_chunked_workspace_bytes(1, 1, 0) == 0
 
     assert f(k=None) == native.LA_ERR_NULL
@@ -194,8 +194,8 @@ def test_delta_chunked_rejects_bad_arguments(native):
     assert f(S_out=FAKE + 8) == native.LA_ERR_ALIGN
     assert f(beta=FAKE + 2) == native.LA_ERR_ALIGN
     assert f(ws=None) == native.LA_ERR_WORKSPACE
-    assert f(ws_bytes=8191) == native.LA_ERR_WORKSPACE
-    assert f(T=65) == native.LA_ERR_WORKSPACE           # two chunks need 16 KB
+    assert f(ws_bytes=16383) == native.LA_ERR_WORKSPACE
+    assert f(T=65) == native.LA_ERR_WORKSPACE           # two chunks need 32 KB
     assert f(ws=FAKE + 8) == native.LA_ERR_ALIGN
 
 
