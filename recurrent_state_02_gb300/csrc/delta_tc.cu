@@ -261,39 +261,43 @@ delta_t_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant_
                 *reinterpret_cast<uint16_t *>(base + kPT + tile_off(bb + u, bb + lane)) = bf16_bits(acc[u]);
         }
         __syncthreads();
-        // M = G10 T00: rows 8 warp .. 8 warp + 7, column lane
+        // M = G10 T00 and then T10 = -T11 M: thread (warp, lane) computes rows
+        // 4 rg .. 4 rg + 3 and columns 2 cp, 2 cp + 1, rg = 2 warp + lane / 16
+        const int rg = 2 * warp + (lane >> 4), cp = lane & 15;
         {
-            float m8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+            float2 m4[4] = {};
 #pragma unroll 8
             for (int u = 0; u < 32; ++u) {
-                const float tj = T00f[u * LDT + lane];
-                const float4 g0 = *reinterpret_cast<const float4 *>(Lt + u * LD + 32 + 8 * warp);
-                const float4 g1 = *reinterpret_cast<const float4 *>(Lt + u * LD + 36 + 8 * warp);
-                m8[0] = fmaf(g0.x, tj, m8[0]); m8[1] = fmaf(g0.y, tj, m8[1]);
-                m8[2] = fmaf(g0.z, tj, m8[2]); m8[3] = fmaf(g0.w, tj, m8[3]);
-                m8[4] = fmaf(g1.x, tj, m8[4]); m8[5] = fmaf(g1.y, tj, m8[5]);
-                m8[6] = fmaf(g1.z, tj, m8[6]); m8[7] = fmaf(g1.w, tj, m8[7]);
+                const float2 tj = *reinterpret_cast<const float2 *>(T00f + u * LDT + 2 * cp);
+                const float4 g = *reinterpret_cast<const float4 *>(Lt + u * LD + 32 + 4 * rg);
+                const float gv[4] = {g.x, g.y, g.z, g.w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    m4[e].x = fmaf(gv[e], tj.x, m4[e].x);
+                    m4[e].y = fmaf(gv[e], tj.y, m4[e].y);
+                }
             }
 #pragma unroll
-            for (int e = 0; e < 8; ++e) Mf[(8 * warp + e) * LDT + lane] = m8[e];
+            for (int e = 0; e < 4; ++e) *reinterpret_cast<float2 *>(Mf + (4 * rg + e) * LDT + 2 * cp) = m4[e];
         }
         __syncthreads();
-        // T10 = -T11 M
         {
-            float o8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+            float2 o4[4] = {};
 #pragma unroll 8
             for (int u = 0; u < 32; ++u) {
-                const float mj = Mf[u * LDT + lane];
-                const float4 a0 = *reinterpret_cast<const float4 *>(T11t + u * LDT + 8 * warp);
-                const float4 a1 = *reinterpret_cast<const float4 *>(T11t + u * LDT + 4 + 8 * warp);
-                o8[0] = fmaf(a0.x, mj, o8[0]); o8[1] = fmaf(a0.y, mj, o8[1]);
-                o8[2] = fmaf(a0.z, mj, o8[2]); o8[3] = fmaf(a0.w, mj, o8[3]);
-                o8[4] = fmaf(a1.x, mj, o8[4]); o8[5] = fmaf(a1.y, mj, o8[5]);
-                o8[6] = fmaf(a1.z, mj, o8[6]); o8[7] = fmaf(a1.w, mj, o8[7]);
+                const float2 mj = *reinterpret_cast<const float2 *>(Mf + u * LDT + 2 * cp);
+                const float4 a = *reinterpret_cast<const float4 *>(T11t + u * LDT + 4 * rg);
+                const float av[4] = {a.x, a.y, a.z, a.w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    o4[e].x = fmaf(av[e], mj.x, o4[e].x);
+                    o4[e].y = fmaf(av[e], mj.y, o4[e].y);
+                }
             }
 #pragma unroll
-            for (int e = 0; e < 8; ++e)
-                *reinterpret_cast<uint16_t *>(base + kPT + tile_off(32 + 8 * warp + e, lane)) = bf16_bits(-o8[e]);
+            for (int e = 0; e < 4; ++e)
+                *reinterpret_cast<uint32_t *>(base + kPT + tile_off(32 + 4 * rg + e, 2 * cp)) =
+                    pack_bf16x2(-o4[e].x, -o4[e].y);
         }
         __syncthreads();
         uint4 *dst = reinterpret_cast<uint4 *>(wsc + kTV);
