@@ -11,7 +11,9 @@ Each step is replayed as a CUDA graph of its three kernel launches.
 
 Printed (rank 0, one JSON line): tokens/s of the step, the prefill kernel's
 roofline (algorithmic bytes / mean launch time vs measured HBM bandwidth), the
-decode step on its own workload (B=256, H=16) in GB/s, the delta-rule memory
+decode step on its own workload (B=256, H=16) in GB/s, the gated (B=2, H=16,
+T=16384) and long (B=1, H=32, T=65536) prefill workloads with their own
+rooflines, the delta-rule memory
 on the prefill's shape and the backward pass of the gated prefill, both against
 the FP32 ALU peak, an end-to-end figure
 through the public API with host buffers, clocks sampled during timing, and
@@ -233,26 +235,28 @@ def oracle_tokens_per_s(w, seconds, max_tokens=None):
     cores = oracle.num_cpus()
     bits = lambda t: t.contiguous().view(torch.int16).numpy().view(np.uint16)
     # calibrate on a short prefix, then size the sample
+    gates = lambda inp: None if inp["alpha"] is None else inp["alpha"].numpy()
     Tc = min(w.T, 64)
     inp = W.prefill_inputs(w.with_(T=Tc))
     t0 = time.perf_counter()
-    oracle.scan(bits(inp["q"]), bits(inp["k"]), bits(inp["v"]), threads=cores)
+    oracle.scan(bits(inp["q"]), bits(inp["k"]), bits(inp["v"]), alpha=gates(inp), threads=cores)
     per_token = (time.perf_counter() - t0) / (w.B * Tc)
     Ts = int(max(1, min(w.T, seconds / max(per_token, 1e-9) / w.B)))
     if max_tokens:
         Ts = min(Ts, max(1, max_tokens // w.B))
     inp = W.prefill_inputs(w.with_(T=Ts))
-    q, k, v = bits(inp["q"]), bits(inp["k"]), bits(inp["v"])
+    q, k, v, alpha = bits(inp["q"]), bits(inp["k"]), bits(inp["v"]), gates(inp)
     reps, elapsed = 0, 0.0
     while True:
         t0 = time.perf_counter()
-        oracle.scan(q, k, v, eps=w.eps, threads=cores)
+        oracle.scan(q, k, v, alpha=alpha, eps=w.eps, threads=cores)
         elapsed += time.perf_counter() - t0
         reps += 1
         if elapsed >= seconds or reps >= 8:
             break
     tok = w.B * Ts * reps
-    desc = (f"FP64 token recurrence on {cores} threads over all {w.B}x{w.H} heads of '{w.name}', first {Ts} of "
+    desc = (f"FP64 token recurrence{' with gates' if w.gated else ''} on {cores} threads over all {w.B}x{w.H} "
+            f"heads of '{w.name}', first {Ts} of "
             f"{w.T} tokens, {reps} pass(es), {elapsed:.1f} s")
     return tok / elapsed, cores, desc, elapsed
 
@@ -487,6 +491,61 @@ def run_ours(args, rank, world, local_rank):
               "algorithmic_bytes_per_launch": dbytes, "tokens_per_s": dw.B * world / dec_launch,
               "traffic": profile_traffic("decode128_kernel<true>", "B256 H16", kernel_sources("decode.cu"))}
 
+    # the gated (B2 H16 T16384, alpha = sigmoid(N(3,1))) and long (B1 H32 T65536,
+    # sigma = 2) prefill workloads, each on its own inputs from a zero state: the
+    # whole la_prefill_chunked call (state pass, scan and chunk kernel when the
+    # sequences are split into segments) replayed as a CUDA graph; two input sets
+    # of 270 MB alternate for the gated workload, the long one's 2.1 GB set
+    # exceeds L2 by itself
+    def prefill_workload(pw, nsets, kernel):
+        pin = W.prefill_inputs(pw, seed=pw.seed + 1000 * rank)
+        psets = []
+        for _ in range(nsets):
+            psets.append(dict(q=pin["q"].to(dev), k=pin["k"].to(dev), v=pin["v"].to(dev),
+                              alpha=pin["alpha"].to(dev) if pin["alpha"] is not None else None,
+                              y=torch.empty((pw.B, pw.H, pw.T, pw.dv), device=dev, dtype=torch.bfloat16),
+                              S=torch.empty((pw.B, pw.H, pw.r, pw.dv), device=dev, dtype=torch.float32),
+                              z=torch.empty((pw.B, pw.H, pw.r), device=dev, dtype=torch.float32)))
+        del pin
+        nws = int(L.la_prefill_workspace_bytes(pw.B, pw.H, pw.T, pw.r, pw.dv, pw.chunk))
+        pws = torch.empty(max(nws, 256), device=dev, dtype=torch.uint8)
+
+        def call(s):
+            _native.check(L.la_prefill_chunked(P(s["q"]), P(s["k"]), P(s["v"]), _native.LA_DTYPE_BF16,
+                                               P(s["alpha"]) if s["alpha"] is not None else None, None, None,
+                                               pw.B, pw.H, pw.T, pw.r, pw.dv, pw.chunk, pw.eps, P(s["y"]),
+                                               P(s["S"]), P(s["z"]), P(pws), nws, sh), "la_prefill_chunked")
+
+        graphs = []
+        for s in psets:
+            with torch.cuda.stream(stream):
+                call(s)
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                call(s)
+            graphs.append(g)
+        t_s = timed([graphs[i % nsets] for i in range(N_ROT)], args.steps, args.warmup)
+        t_s, = reduce_max([t_s], dev, dist)
+        assert _native.lib().la_last_device_status(sh) == 0
+        t_call = t_s / args.steps
+        nbytes = prefill_bytes(pw.B, pw.H, pw.T, pw.r, pw.dv, with_state_in=False) + (
+            pw.B * pw.H * pw.T * 4 if pw.gated else 0)
+        gbs = nbytes / t_call / 1e9
+        del psets, graphs, pws
+        torch.cuda.empty_cache()
+        return {"workload": pw.name, "call_us": t_call * 1e6, "tokens_per_s": pw.B * pw.T * world / t_call,
+                "launches_per_call": 3 if nws else 1,
+                "l2": f"{nsets} input set(s) of {nbytes / 1e6:.0f} MB (> 129 MB L2)",
+                "roofline": {"bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s", "frac": gbs / peak,
+                             "peak_kind": peak_kind,
+                             "timed": "the whole call" + (" (state pass, scan and chunk kernel)" if nws else ""),
+                             "kernel": kernel, "algorithmic_bytes_per_launch": nbytes,
+                             "traffic": profile_traffic(kernel, f"B{pw.B} H{pw.H} T{pw.T}",
+                                                        kernel_sources("prefill_tc.cu"))}}
+
+    gated_prefill = prefill_workload(W.GATED, 2, "prefill_tc_kernel<true>")
+    long_prefill = prefill_workload(W.LONG, 1, "prefill_tc_kernel<false>")
+
     # delta-rule memory on its own workload (B=4, H=16, T=4096, r = dv = 128, BF16;
     # q, k, v 201 MB > L2): the chunked tensor-core entry point (its two launches,
     # T of every chunk and then the state chain) and the FP32 token recurrence,
@@ -647,6 +706,10 @@ def run_ours(args, rank, world, local_rank):
         cpu = {"value": tps, "unit": "tokens/s", "cores": cores, "kind": "oracle", "sample": desc}
         # the oracles of the delta rule and of the backward, beside their GPU figures
         delta["cpu_baseline"] = oracle_rate("delta", xw, args.cpu_seconds / 4)
+        for entry, pw in ((gated_prefill, W.GATED), (long_prefill, W.LONG)):
+            tps_p, cores_p, desc_p, _ = oracle_tokens_per_s(pw, args.cpu_seconds / 4)
+            entry["cpu_baseline"] = {"value": tps_p, "unit": "tokens/s", "cores": cores_p, "kind": "oracle",
+                                     "sample": desc_p}
         backward["cpu_baseline"] = oracle_rate("backward", bw, args.cpu_seconds / 4)
 
     if rank == 0:
@@ -659,7 +722,8 @@ def run_ours(args, rank, world, local_rank):
                                  f"{prefill_bytes(B, H, T, r, dv) / 1e6:.0f} MB (> 129 MB L2)",
                            "parallelism": f"replicas x{world} (independent batches, no collective)",
                            "launch": "CUDA graph per step"},
-                "roofline": roofline, "decode": decode, "delta_rule": delta, "backward": backward, "cpu_baseline": cpu,
+                "roofline": roofline, "decode": decode, "gated_prefill": gated_prefill, "long_prefill": long_prefill,
+                "delta_rule": delta, "backward": backward, "cpu_baseline": cpu,
                 "e2e": e2e,
                 "gpu_launches": launches_per_step * args.steps, "clocks": clocks}
         print(json.dumps(line), flush=True)

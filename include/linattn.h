@@ -99,8 +99,10 @@ size_t la_prefill_workspace_bytes(int B, int H, int T, int r, int dv, int chunk)
  *          S0 may equal S_out and z0 may equal z_out (in-place continuation).
  *   S_out  device FP32 [B,H,r,dv] final state;  z_out device FP32 [B,H,r].
  *   eps    added once to the whole denominator: y = num / (den + eps).
- *   chunk  chunk length in tokens.  The result does not depend on it beyond
- *          rounding ([LA] "动手实验": chunk boundaries do not change the semantics).
+ *   chunk  chunk length in tokens, >= 1.  The result does not depend on it
+ *          beyond rounding ([LA] "动手实验": chunk boundaries do not change the
+ *          semantics), so the BF16 kernel computes in chunks of 64 tokens
+ *          whatever value is given; the FP32 path runs token by token.
  *   workspace, workspace_bytes: device scratch of at least
  *          la_prefill_workspace_bytes(...) bytes, 256-byte aligned, owned by the
  *          caller and not read after the call's kernels finish (may be NULL
@@ -108,8 +110,8 @@ size_t la_prefill_workspace_bytes(int B, int H, int T, int r, int dv, int chunk)
  *
  * Kernels:
  *   BF16: tensor-core kernel (tcgen05 MMAs with TMEM accumulators, TMA tile
- *         loads).  Requires r == 128, dv in {64, 128}, chunk == 64, q, k, v, y,
- *         S_out 16-byte aligned.  With a workspace (see above) three launches:
+ *         loads), chunks of 64 tokens.  Requires r == 128, dv in {64, 128}, q, k,
+ *         v, y, S_out 16-byte aligned.  With a workspace (see above) three launches:
  *         the state pass, the scan of segment start states, and the chunk
  *         kernel over all segments at once.
  *   FP32: exact FP32 token recurrence on CUDA cores (chunk is not used).
@@ -142,8 +144,8 @@ la_status la_prefill_chunked(const void *q, const void *k, const void *v, la_dty
  *              The host cannot read it; a kernel finding a sequence outside
  *              [0, total_T] or of negative length skips it and records LA_ERR_SHAPE
  *              (read it with la_last_device_status).
- * Requires BF16, r == 128, dv in {64, 128}, chunk == 64; q, k, v, y, S_out 16-byte
- * aligned.  total_T may be 0.  The sequences are not split into segments (no
+ * Requires BF16, r == 128, dv in {64, 128}, chunk >= 1 (computed in chunks of 64
+ * tokens, as la_prefill_chunked); q, k, v, y, S_out 16-byte aligned.  total_T may be 0.  The sequences are not split into segments (no
  * workspace).  Rows of y outside every sequence are not written.
  * Errors: LA_ERR_NULL, LA_ERR_SHAPE, LA_ERR_DTYPE, LA_ERR_ALIGN, LA_ERR_UNSUPPORTED
  *         (FP32 or other sizes), LA_ERR_CUDA.
@@ -165,7 +167,8 @@ la_status la_prefill_varlen(const void *q, const void *k, const void *v, la_dtyp
  *   workspace.  LA_ERR_WORKSPACE when la_prefill_workspace_bytes for these sizes
  *   exceeds the 16 MiB (on a 152-SM device no size needs more than about 10 MB).
  *   The first call on a device looks up the buffer's device address with that
- *   device current; make it before any stream capture.
+ *   device current; make it before any stream capture.  The look-up is cached
+ *   per device in an atomic, so first calls from several host threads are safe.
  *   Nothing in the buffer has to start at zero: a call writes every entry before
  *   reading it.  Calls that may overlap in time (other streams, other threads)
  *   race on the one buffer; the caller must serialise them.

@@ -27,6 +27,14 @@ def _stream(device):
     return torch.cuda.current_stream(device).cuda_stream
 
 
+def _device_guard(device):
+    """Makes `device` current for the duration of a library call.  The library
+    launches on the current device (the default stream's handle 0 names that
+    device's stream) and keeps its per-device state (status word, scratch, SM
+    count) for the current device, so the tensors' device must be current."""
+    return torch.cuda.device(device)
+
+
 def _require(t, name, shape, dtype, device):
     if t is None:
         return
@@ -49,12 +57,19 @@ def state_init(B, H, r, dv, device="cuda", S=None, z=None):
         z = torch.empty((B, H, r), device=device, dtype=torch.float32)
     _require(S, "S", (B, H, r, dv), torch.float32, S.device)
     _require(z, "z", (B, H, r), torch.float32, S.device)
-    _native.check(_native.lib().la_state_init(_ptr(S), _ptr(z), B, H, r, dv, _stream(S.device)), "la_state_init")
+    with _device_guard(S.device):
+        st = _native.lib().la_state_init(_ptr(S), _ptr(z), B, H, r, dv, _stream(S.device))
+    _native.check(st, "la_state_init")
     return S, z
 
 
-def prefill_workspace_bytes(B, H, T, r, dv, chunk=64) -> int:
-    return int(_native.lib().la_prefill_workspace_bytes(B, H, T, r, dv, chunk))
+def prefill_workspace_bytes(B, H, T, r, dv, chunk=64, device=None) -> int:
+    """Scratch bytes of prefill_chunked for these sizes on `device` (default: the
+    current device); the plan depends on the device's SM count."""
+    if device is None:
+        return int(_native.lib().la_prefill_workspace_bytes(B, H, T, r, dv, chunk))
+    with _device_guard(torch.device(device)):
+        return int(_native.lib().la_prefill_workspace_bytes(B, H, T, r, dv, chunk))
 
 
 def prefill_chunked(q, k, v, alpha=None, S0=None, z0=None, chunk=64, eps=1e-6, y=None, S_out=None, z_out=None,
@@ -82,13 +97,14 @@ def prefill_chunked(q, k, v, alpha=None, S0=None, z0=None, chunk=64, eps=1e-6, y
     _require(y, "y", (B, H, T, dv), q.dtype, dev)
     _require(S_out, "S_out", (B, H, r, dv), torch.float32, dev)
     _require(z_out, "z_out", (B, H, r), torch.float32, dev)
-    need = prefill_workspace_bytes(B, H, T, r, dv, chunk)
+    need = prefill_workspace_bytes(B, H, T, r, dv, chunk, device=dev)
     if need and workspace is None:
         workspace = torch.empty(need, device=dev, dtype=torch.uint8)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
-    st = _native.lib().la_prefill_chunked(
-        _ptr(q), _ptr(k), _ptr(v), _DTYPES[q.dtype], _ptr(alpha), _ptr(S0), _ptr(z0), B, H, T, r, dv, chunk,
-        float(eps), _ptr(y), _ptr(S_out), _ptr(z_out), _ptr(workspace), ws_bytes, _stream(dev))
+    with _device_guard(dev):
+        st = _native.lib().la_prefill_chunked(
+            _ptr(q), _ptr(k), _ptr(v), _DTYPES[q.dtype], _ptr(alpha), _ptr(S0), _ptr(z0), B, H, T, r, dv, chunk,
+            float(eps), _ptr(y), _ptr(S_out), _ptr(z_out), _ptr(workspace), ws_bytes, _stream(dev))
     _native.check(st, "la_prefill_chunked")
     return y, S_out, z_out
 
@@ -123,9 +139,10 @@ def prefill_varlen(q, k, v, cu_seqlens, alpha=None, S0=None, z0=None, chunk=64, 
     _require(y, "y", (total_T, H, dv), q.dtype, dev)
     _require(S_out, "S_out", (B, H, r, dv), torch.float32, dev)
     _require(z_out, "z_out", (B, H, r), torch.float32, dev)
-    st = _native.lib().la_prefill_varlen(
-        _ptr(q), _ptr(k), _ptr(v), _DTYPES[q.dtype], _ptr(alpha), _ptr(S0), _ptr(z0), _ptr(cu_seqlens), B, H,
-        total_T, r, dv, chunk, float(eps), _ptr(y), _ptr(S_out), _ptr(z_out), _stream(dev))
+    with _device_guard(dev):
+        st = _native.lib().la_prefill_varlen(
+            _ptr(q), _ptr(k), _ptr(v), _DTYPES[q.dtype], _ptr(alpha), _ptr(S0), _ptr(z0), _ptr(cu_seqlens), B, H,
+            total_T, r, dv, chunk, float(eps), _ptr(y), _ptr(S_out), _ptr(z_out), _stream(dev))
     _native.check(st, "la_prefill_varlen")
     return y, S_out, z_out
 
@@ -151,9 +168,10 @@ def prefill_chunked_noalloc(q, k, v, y, S_out, z_out, alpha=None, S0=None, z0=No
     _require(y, "y", (B, H, T, dv), q.dtype, dev)
     _require(S_out, "S_out", (B, H, r, dv), torch.float32, dev)
     _require(z_out, "z_out", (B, H, r), torch.float32, dev)
-    st = _native.lib().la_prefill_chunked_noalloc(
-        _ptr(q), _ptr(k), _ptr(v), _DTYPES[q.dtype], _ptr(alpha), _ptr(S0), _ptr(z0), B, H, T, r, dv, chunk,
-        float(eps), _ptr(y), _ptr(S_out), _ptr(z_out), _stream(dev))
+    with _device_guard(dev):
+        st = _native.lib().la_prefill_chunked_noalloc(
+            _ptr(q), _ptr(k), _ptr(v), _DTYPES[q.dtype], _ptr(alpha), _ptr(S0), _ptr(z0), B, H, T, r, dv, chunk,
+            float(eps), _ptr(y), _ptr(S_out), _ptr(z_out), _stream(dev))
     _native.check(st, "la_prefill_chunked_noalloc")
     return y, S_out, z_out
 
@@ -176,8 +194,9 @@ def decode_step(q, k, v, S, z, alpha=None, eps=1e-6, y=None):
     if y is None:
         y = torch.empty((B, H, 1, dv), device=dev, dtype=q.dtype)
     _require(y, "y", (B, H, 1, dv), q.dtype, dev)
-    st = _native.lib().la_decode_step(_ptr(q), _ptr(k), _ptr(v), _DTYPES[q.dtype], _ptr(alpha), _ptr(S), _ptr(z),
-                                      B, H, r, dv, float(eps), _ptr(y), _stream(dev))
+    with _device_guard(dev):
+        st = _native.lib().la_decode_step(_ptr(q), _ptr(k), _ptr(v), _DTYPES[q.dtype], _ptr(alpha), _ptr(S), _ptr(z),
+                                          B, H, r, dv, float(eps), _ptr(y), _stream(dev))
     _native.check(st, "la_decode_step")
     return y
 
@@ -207,10 +226,11 @@ def prefill_backward(q, k, v, y, dy, alpha=None, S0=None, z0=None, dS_T=None, dz
     if workspace is None:
         workspace = torch.empty(need, device=dev, dtype=torch.uint8)
     ws_bytes = workspace.numel() * workspace.element_size()
-    st = _native.lib().la_prefill_backward(
-        _ptr(q), _ptr(k), _ptr(v), _DTYPES[q.dtype], _ptr(alpha), _ptr(S0), _ptr(z0), B, H, T, r, dvd, float(eps),
-        _ptr(y), _ptr(dy), _ptr(dS_T), _ptr(dz_T), _ptr(dq), _ptr(dk), _ptr(dv_out), _ptr(dalpha), _ptr(dS0),
-        _ptr(dz0), _ptr(workspace), ws_bytes, _stream(dev))
+    with _device_guard(dev):
+        st = _native.lib().la_prefill_backward(
+            _ptr(q), _ptr(k), _ptr(v), _DTYPES[q.dtype], _ptr(alpha), _ptr(S0), _ptr(z0), B, H, T, r, dvd, float(eps),
+            _ptr(y), _ptr(dy), _ptr(dS_T), _ptr(dz_T), _ptr(dq), _ptr(dk), _ptr(dv_out), _ptr(dalpha), _ptr(dS0),
+            _ptr(dz0), _ptr(workspace), ws_bytes, _stream(dev))
     _native.check(st, "la_prefill_backward")
     return dq, dk, dv_out, dalpha, dS0, dz0
 
@@ -258,11 +278,14 @@ def _delta(entry, q, k, v, beta, S0, y, S_out, workspace):
     args = [_ptr(q), _ptr(k), _ptr(v), _DTYPES[q.dtype], _ptr(beta), _ptr(S0), B, H, T, r, dv, _ptr(y), _ptr(S_out)]
     if entry == "la_delta_rule_chunked":
         args += [_ptr(workspace), 0 if workspace is None else workspace.numel() * workspace.element_size()]
-    st = getattr(_native.lib(), entry)(*args, _stream(dev))
+    with _device_guard(dev):
+        st = getattr(_native.lib(), entry)(*args, _stream(dev))
     _native.check(st, entry)
     return y, S_out
 
 
 def last_device_status(device="cuda") -> int:
     """Synchronises the current stream and returns (and clears) the device status word."""
-    return int(_native.lib().la_last_device_status(_stream(torch.device(device))))
+    dev = torch.device(device)
+    with _device_guard(dev):
+        return int(_native.lib().la_last_device_status(_stream(dev)))

@@ -4,6 +4,7 @@
 #include "delta_tc.h"
 #include "kernels.h"
 
+#include <atomic>
 #include <cstdint>
 #include <cuda.h>
 #include <cuda_runtime.h>
@@ -19,14 +20,18 @@ typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t
 
 EncodeTiledFn encode_fn()
 {
-    static EncodeTiledFn fn = nullptr;
+    // looked up once; concurrent first calls may each look it up (same value)
+    static std::atomic<EncodeTiledFn> cached{nullptr};
+    EncodeTiledFn fn = cached.load(std::memory_order_acquire);
     if (!fn) {
         void *p = nullptr;
         cudaDriverEntryPointQueryResult q;
         if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
                 cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
+            q == cudaDriverEntryPointSuccess) {
             fn = reinterpret_cast<EncodeTiledFn>(p);
+            cached.store(fn, std::memory_order_release);
+        }
     }
     return fn;
 }
@@ -45,12 +50,15 @@ struct SegPlan {
 
 int sm_count()
 {
-    static int count[64] = {};
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
-    if (!count[dev] && cudaDeviceGetAttribute(&count[dev], cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-        count[dev] = 0;
-    return count[dev];
+    static std::atomic<int> count[la::kMaxDevices];
+    const int dev = la::current_device_index();
+    if (dev < 0) return 0;
+    int n = count[dev].load(std::memory_order_relaxed);
+    if (!n) {
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+        count[dev].store(n, std::memory_order_relaxed);
+    }
+    return n;
 }
 
 SegPlan seg_plan(int B, int H, int T, int dv)
@@ -96,17 +104,19 @@ static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratch
 
 // Device address of the scratch on the current device, looked up once per device
 // (the first call there does it, with that device current); nullptr on failure.
+// Host threads whose first calls on a device meet may each look it up: the
+// cache is an atomic, and every look-up yields the same address.
 void *noalloc_scratch()
 {
-    static void *addr[64] = {};
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
-    if (!addr[dev]) {
-        void *p = nullptr;
+    static std::atomic<void *> addr[la::kMaxDevices];
+    const int dev = la::current_device_index();
+    if (dev < 0) return nullptr;
+    void *p = addr[dev].load(std::memory_order_acquire);
+    if (!p) {
         if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return nullptr;
-        addr[dev] = p;
+        addr[dev].store(p, std::memory_order_release);
     }
-    return addr[dev];
+    return p;
 }
 
 // 3-D BF16 view [planes, rows, cols] (cols innermost) with boxes of box_cols x
@@ -184,7 +194,7 @@ la_status la_state_init(float *S, float *z, int B, int H, int r, int dv, la_stre
 
 size_t la_prefill_workspace_bytes(int B, int H, int T, int r, int dv, int chunk)
 {
-    if (B < 1 || H < 1 || T < 1 || r != 128 || (dv != 64 && dv != 128) || chunk != 64) return 0;
+    if (B < 1 || H < 1 || T < 1 || r != 128 || (dv != 64 && dv != 128) || chunk < 1) return 0;
     return seg_workspace_bytes(seg_plan(B, H, T, dv), B, H, dv);
 }
 
@@ -208,8 +218,10 @@ la_status la_prefill_chunked(const void *q, const void *k, const void *v, la_dty
                                                 static_cast<float *>(y), S_out, z_out, st));
     }
 
-    // BF16: tensor-core kernel
-    if (r != 128 || (dv != 64 && dv != 128) || chunk != 64) return LA_ERR_UNSUPPORTED;
+    // BF16: tensor-core kernel.  It computes in chunks of 64 tokens whatever chunk
+    // length is asked for: the result does not depend on the chunk length beyond
+    // rounding ("Linear attention：把历史写进状态", section "动手实验").
+    if (r != 128 || (dv != 64 && dv != 128)) return LA_ERR_UNSUPPORTED;
     if ((long long)B * H > 0x7fffffffLL) return LA_ERR_SHAPE;
     {
         const void *ptrs16[] = {q, k, v, y, S_out};
@@ -291,7 +303,7 @@ la_status la_prefill_varlen(const void *q, const void *k, const void *v, la_dtyp
     if (total_T > 0 && (!q || !k || !v || !y)) return LA_ERR_NULL;
     if (B < 1 || H < 1 || total_T < 0 || r < 1 || dv < 1 || chunk < 1) return LA_ERR_SHAPE;
     if (dtype != LA_DTYPE_BF16 && dtype != LA_DTYPE_FP32) return LA_ERR_DTYPE;
-    if (dtype != LA_DTYPE_BF16 || r != 128 || (dv != 64 && dv != 128) || chunk != 64) return LA_ERR_UNSUPPORTED;
+    if (dtype != LA_DTYPE_BF16 || r != 128 || (dv != 64 && dv != 128)) return LA_ERR_UNSUPPORTED;
     if ((long long)B * H > 0x7fffffffLL || (long long)total_T * H > 0x7fffffffLL) return LA_ERR_SHAPE;
     {
         const void *ptrs16[] = {q, k, v, y, S_out};
@@ -354,6 +366,7 @@ la_status la_decode_step(const void *q, const void *k, const void *v, la_dtype d
     if (B < 1 || H < 1 || r < 1 || dv < 1) return LA_ERR_SHAPE;
     if (dtype != LA_DTYPE_BF16 && dtype != LA_DTYPE_FP32) return LA_ERR_DTYPE;
     if (r > 256 || dv > 256) return LA_ERR_UNSUPPORTED;
+    if ((long long)B * H > 0x7fffffffLL) return LA_ERR_SHAPE;   // one CTA per (b, h)
     const uintptr_t el = dtype == LA_DTYPE_BF16 ? 2 : 4;
     if (!aligned(q, el) || !aligned(k, el) || !aligned(v, el) || !aligned(y, el)) return LA_ERR_ALIGN;
     if (!aligned(S, 4) || !aligned(z, 4) || (alpha && !aligned(alpha, 4))) return LA_ERR_ALIGN;

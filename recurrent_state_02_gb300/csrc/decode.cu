@@ -185,13 +185,14 @@ cudaError_t launch_decode(const void *q, const void *k, const void *v, bool bf16
                           float *z, int B, int H, int r, int dv, float eps, void *y, bool fast128,
                           cudaStream_t stream)
 {
-    const int nbh = B * H;
+    const long long nbh = (long long)B * H;   // the caller bounds it by INT_MAX
+    if (nbh < 1 || nbh > 0x7fffffffLL) return cudaErrorInvalidValue;
     if (fast128) {
-        if (bf16) decode128_kernel<true><<<nbh, 256, 0, stream>>>(q, k, v, alpha, S, z, eps, y);
-        else decode128_kernel<false><<<nbh, 256, 0, stream>>>(q, k, v, alpha, S, z, eps, y);
+        if (bf16) decode128_kernel<true><<<(unsigned)nbh, 256, 0, stream>>>(q, k, v, alpha, S, z, eps, y);
+        else decode128_kernel<false><<<(unsigned)nbh, 256, 0, stream>>>(q, k, v, alpha, S, z, eps, y);
     } else {
-        if (bf16) decode_generic_kernel<true><<<nbh, 256, 0, stream>>>(q, k, v, alpha, S, z, r, dv, eps, y);
-        else decode_generic_kernel<false><<<nbh, 256, 0, stream>>>(q, k, v, alpha, S, z, r, dv, eps, y);
+        if (bf16) decode_generic_kernel<true><<<(unsigned)nbh, 256, 0, stream>>>(q, k, v, alpha, S, z, r, dv, eps, y);
+        else decode_generic_kernel<false><<<(unsigned)nbh, 256, 0, stream>>>(q, k, v, alpha, S, z, r, dv, eps, y);
     }
     return cudaGetLastError();
 }

@@ -569,21 +569,6 @@ delta_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
     }
 }
 
-template <typename K>
-cudaError_t set_smem_once(K kern, uint32_t bytes, bool (&done)[64])
-{
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return e;
-    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-    if (!done[dev]) {
-        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
-        if (e != cudaSuccess) return e;
-        done[dev] = true;
-    }
-    return cudaSuccess;
-}
-
 }  // namespace
 
 size_t delta_tc_workspace_bytes(int B, int H, int T)
@@ -599,7 +584,7 @@ cudaError_t launch_delta_tc(const CUtensorMap &map_q, const CUtensorMap &map_k, 
     const long long nprep = (long long)B * a.H * nch, nmain = (long long)B * a.H * (a.dv / kDS);
     if (a.T < 1 || nprep > 0x7fffffffLL || nmain < 1 || nmain > 0x7fffffffLL) return cudaErrorInvalidValue;
     // The attributes are set once per device (not during stream capture of later calls).
-    static bool done_p[64] = {}, done_m[64] = {};
+    static OncePerDevice done_p, done_m;
     cudaError_t e = set_smem_once(delta_t_kernel, kPSmemBytes, done_p);
     if (e != cudaSuccess) return e;
     e = set_smem_once(delta_tc_kernel, kMSmemBytes, done_m);

@@ -1,11 +1,44 @@
 // kernels.h -- launchers behind the C ABI (internal; not part of the public header).
 #pragma once
 
+#include <atomic>
 #include <cstdint>
 #include <cuda.h>
 #include <cuda_runtime.h>
 
 namespace la {
+
+// Per-device one-time set-up (kernel attributes, cached look-ups) for devices
+// 0 .. kMaxDevices-1.  The flags and cached values are atomics: host threads
+// that make their first call on a device at the same time may each do the
+// (idempotent) set-up, and none reads a half-written value.
+constexpr int kMaxDevices = 64;
+struct OncePerDevice {
+    std::atomic<bool> done[kMaxDevices];
+};
+
+// The current device, or -1 when it cannot be read or lies beyond kMaxDevices.
+inline int current_device_index()
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return -1;
+    return dev;
+}
+
+// Raises kern's dynamic shared-memory limit to `bytes`, once per device (the
+// first call on a device must not be inside a stream capture).
+template <typename K>
+cudaError_t set_smem_once(K kern, uint32_t bytes, OncePerDevice &once)
+{
+    const int dev = current_device_index();
+    if (dev < 0) return cudaErrorInvalidDevice;
+    if (!once.done[dev].load(std::memory_order_acquire)) {
+        const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+        if (e != cudaSuccess) return e;
+        once.done[dev].store(true, std::memory_order_release);
+    }
+    return cudaSuccess;
+}
 
 // Device status word values (same numbering as la_status).
 constexpr int kStatusShape = 2;

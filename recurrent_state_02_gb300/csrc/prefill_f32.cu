@@ -95,17 +95,9 @@ cudaError_t launch_prefill_f32(const float *q, const float *k, const float *v, c
     const int ds = dv < kSlice ? dv : kSlice;
     const size_t smem = sizeof(float) * (size_t)r * ds;
     // The attribute is set once per device to the largest size this kernel accepts.
-    static bool attr_set[64] = {};
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
+    static OncePerDevice attr_set;
+    const cudaError_t e = set_smem_once(prefill_f32_kernel, (uint32_t)(sizeof(float) * kMaxR * kSlice), attr_set);
     if (e != cudaSuccess) return e;
-    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-    if (!attr_set[dev]) {
-        e = cudaFuncSetAttribute(prefill_f32_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)(sizeof(float) * kMaxR * kSlice));
-        if (e != cudaSuccess) return e;
-        attr_set[dev] = true;
-    }
     const int nslice = (dv + kSlice - 1) / kSlice;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(H, B, nslice);

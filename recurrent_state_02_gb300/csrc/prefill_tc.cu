@@ -19,12 +19,13 @@
 // that alpha = 0 is exact rather than log(0)).
 //
 // One CTA owns one (b, h, 64-column slice of dv) and walks the chunks in order,
-// carrying the FP32 state on chip (S and z in registers of the TMEM warps).
+// carrying the FP32 state on chip (S and z in TMEM, where the state-increment
+// MMA accumulates them).
 // Per chunk (C = 64, r = 128):
 //   TMA    q, k (64 x 128) and the v slice (64 x 64) as BF16 tiles, 128-byte swizzle
 //   gate   (with a gate) the producer warp forms the chunk's gate products and
 //          the row w while the tiles are in flight
-//   phi    warps apply phi in place (FP32 math, BF16 result); with a gate they
+//   phi    warps apply phi in place in packed BF16 arithmetic (phi_bf16x2); with a gate they
 //          scale, once P is done, the rows of Q~ by Gamma_i and those of K~ by w_j
 //   MMA    P   = Q~ K~^T            M=64  N=64  K=128  -> TMEM
 //          dS  = K~'^T V            M=128 N=64  K=64   -> TMEM (K~' = diag(w) K~, or K~
@@ -35,9 +36,9 @@
 //                                                       so Q~' . zprev keeps ~16 bits)
 //          O  += A [V | 1]          M=64  N=80  K=64   (A = masked, decayed P in BF16;
 //                                                       column 64 gains the row sums of A)
-//   TMEM   warps: S <- Gamma_last S + dS and z <- Gamma_last z + dz in FP32,
-//          Sprev and [zhi, zlo] -> shared memory; P -> A;
-//          y = O / (dn + eps) -> TMA store
+//   TMEM   warps: decay the TMEM state by Gamma_last (with a gate) before dS and
+//          dz land on it, Sprev and [zhi, zlo] -> shared memory; P -> A;
+//          y = O / (dn + eps) -> global memory (16-byte streaming stores)
 // Every barrier wait is bounded; on expiry the kernel records a timeout in the
 // device status word, drains its own copies and MMAs, frees TMEM and returns.
 
@@ -627,16 +628,9 @@ cudaError_t launch_prefill_tc(const CUtensorMap &map_q, const CUtensorMap &map_k
     const uint32_t bytes = gated ? smem_bytes<true>() : smem_bytes<false>();
     auto kern = gated ? prefill_tc_kernel<true> : prefill_tc_kernel<false>;
     // The attribute is set once per device (not during stream capture of later calls).
-    static bool attr_set[2][64] = {};
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
+    static OncePerDevice attr_set[2];
+    const cudaError_t e = set_smem_once(kern, bytes, attr_set[gated]);
     if (e != cudaSuccess) return e;
-    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-    if (!attr_set[gated][dev]) {
-        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
-        if (e != cudaSuccess) return e;
-        attr_set[gated][dev] = true;
-    }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = grid;
     cfg.blockDim = dim3(kThreads, 1, 1);

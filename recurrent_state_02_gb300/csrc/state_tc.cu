@@ -308,16 +308,9 @@ cudaError_t launch_state_tc(const CUtensorMap &map_k, const CUtensorMap &map_v, 
     const dim3 grid(a.dv / kDVS, a.H, B * a.nsub);
     const uint32_t bytes = gated ? smem_bytes<true>() : smem_bytes<false>();
     auto kern = gated ? state_tc_kernel<true> : state_tc_kernel<false>;
-    static bool attr_set[2][64] = {};
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
+    static OncePerDevice attr_set[2];
+    const cudaError_t e = set_smem_once(kern, bytes, attr_set[gated]);
     if (e != cudaSuccess) return e;
-    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-    if (!attr_set[gated][dev]) {
-        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
-        if (e != cudaSuccess) return e;
-        attr_set[gated][dev] = true;
-    }
     kern<<<grid, kThreads, bytes, stream>>>(map_k, map_v, a);
     return cudaGetLastError();
 }

@@ -47,6 +47,7 @@ def test_status_strings(native):
 
 def test_workspace_query(native):
     assert native.lib().la_prefill_workspace_bytes(4, 16, 4096, 128, 128, 64) == 0
+    assert native.lib().la_prefill_workspace_bytes(4, 16, 4096, 128, 128, 0) == 0
 
 
 FAKE = 1 << 20  # a 16-byte aligned non-null address; never dereferenced (validation fails first)
@@ -74,7 +75,10 @@ def test_prefill_rejects_bad_arguments(native):
     assert _prefill(native, dtype=7) == native.LA_ERR_DTYPE
     assert _prefill(native, r=64) == native.LA_ERR_UNSUPPORTED
     assert _prefill(native, dv=96) == native.LA_ERR_UNSUPPORTED
-    assert _prefill(native, chunk=32) == native.LA_ERR_UNSUPPORTED
+    # any chunk length >= 1 is accepted on BF16 (computed in chunks of 64; the result
+    # does not depend on it): validation passes it on to the alignment checks
+    assert _prefill(native, chunk=32, q=FAKE + 2) == native.LA_ERR_ALIGN
+    assert _prefill(native, chunk=1000, q=FAKE + 2) == native.LA_ERR_ALIGN
     assert _prefill(native, q=FAKE + 2) == native.LA_ERR_ALIGN
     assert _prefill(native, y=FAKE + 8) == native.LA_ERR_ALIGN
     assert _prefill(native, alpha=FAKE + 1) == native.LA_ERR_ALIGN
@@ -94,6 +98,7 @@ def test_decode_rejects_bad_arguments(native):
     assert f(r=257) == native.LA_ERR_UNSUPPORTED
     assert f(q=FAKE + 1) == native.LA_ERR_ALIGN
     assert f(S=FAKE + 2) == native.LA_ERR_ALIGN
+    assert f(B=1 << 30) == native.LA_ERR_SHAPE   # B * H = 2^31 CTAs exceed the grid
 
 
 def test_state_init_rejects_bad_arguments(native):

@@ -14,7 +14,7 @@ import numpy as np
 import pytest
 import torch
 
-from conftest import max_rel_err, to_oracle
+from conftest import assert_close, to_oracle
 
 pytestmark = pytest.mark.gpu
 
@@ -108,8 +108,8 @@ def test_delta_parity(la, oracle_mod, dtype, r, dv, T, with_state, with_beta):
     y_ref, S_ref = _oracle(oracle_mod, d)
     y, S = _run(la, d)
     assert np.isfinite(y).all() and np.isfinite(S).all()
-    assert max_rel_err(S, S_ref) <= TOL_F32
-    assert max_rel_err(y, y_ref) <= (TOL_F32 if dtype == torch.float32 else TOL_BF16)
+    assert_close(S, S_ref, TOL_F32, "delta S")
+    assert_close(y, y_ref, TOL_F32 if dtype == torch.float32 else TOL_BF16, "delta y")
 
 
 def test_delta_empty_sequence_copies_state(la):
@@ -148,8 +148,8 @@ def test_delta_full_size_sampled_heads(la, oracle_mod):
         one = {k: v[b:b + 1, h:h + 1].contiguous() for k, v in d.items() if v is not None}
         one["S0"] = None
         y_ref, S_ref = _oracle(oracle_mod, one)
-        assert max_rel_err(S[b:b + 1, h:h + 1], S_ref) <= TOL_F32
-        assert max_rel_err(y[b:b + 1, h:h + 1], y_ref) <= TOL_BF16
+        assert_close(S[b:b + 1, h:h + 1], S_ref, TOL_F32, f"delta S head {b},{h}")
+        assert_close(y[b:b + 1, h:h + 1], y_ref, TOL_BF16, f"delta y head {b},{h}")
 
 
 # ---------------------------------------------------------------- chunked form
@@ -185,8 +185,8 @@ def test_delta_chunked_parity(la, oracle_mod, T, dv, H, with_state, with_beta):
     y_ref, S_ref = _oracle(oracle_mod, d)
     y, S = _run_tc(la, d)
     assert np.isfinite(y).all() and np.isfinite(S).all()
-    assert max_rel_err(S, S_ref) <= TOL_TC
-    assert max_rel_err(y, y_ref) <= TOL_TC
+    assert_close(S, S_ref, TOL_TC, "chunked delta S")
+    assert_close(y, y_ref, TOL_TC, "chunked delta y")
 
 
 def test_delta_chunked_pages_example(la):
@@ -245,5 +245,5 @@ def test_delta_chunked_full_size_sampled_heads(la, oracle_mod):
         one = {k: v[b:b + 1, h:h + 1].contiguous() for k, v in d.items() if v is not None}
         one["S0"] = None
         y_ref, S_ref = _oracle(oracle_mod, one)
-        assert max_rel_err(S[b:b + 1, h:h + 1], S_ref) <= TOL_TC
-        assert max_rel_err(y[b:b + 1, h:h + 1], y_ref) <= TOL_TC
+        assert_close(S[b:b + 1, h:h + 1], S_ref, TOL_TC, f"chunked delta S head {b},{h}")
+        assert_close(y[b:b + 1, h:h + 1], y_ref, TOL_TC, f"chunked delta y head {b},{h}")

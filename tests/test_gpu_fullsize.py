@@ -1,11 +1,12 @@
 """The four full-size workloads, in the launch configuration the benchmark times,
-against the FP64 oracle on sampled (b, h) sequences (every output and the final
-state of each sampled sequence; all heads for decode)."""
+against the FP64 oracle on every (b, h) sequence: every output token and the final
+state of every head, each held to the bar per tensor and per row (every token of
+y, every feature row of S, the z vector of every head)."""
 import numpy as np
 import pytest
 import torch
 
-from conftest import max_rel_err, to_oracle
+from conftest import assert_close, to_oracle
 
 pytestmark = pytest.mark.gpu
 
@@ -18,9 +19,9 @@ def la():
     return la_mod
 
 
-def _sample_heads(B, H):
-    picks = {(0, 0), (B - 1, H - 1), (B // 2, H // 2)}
-    return sorted(picks)
+def _head_groups(B, H, per):
+    heads = [(b, h) for b in range(B) for h in range(H)]
+    return [heads[i:i + per] for i in range(0, len(heads), per)]
 
 
 @pytest.mark.parametrize("name", ["ungated", "gated", "long"])
@@ -32,16 +33,22 @@ def test_prefill_full_size(la, oracle_mod, name):
     y, S, z = la.prefill_chunked(d["q"], d["k"], d["v"], alpha=d["alpha"], chunk=w.chunk, eps=w.eps)
     assert la.last_device_status() == 0
     assert torch.isfinite(y).all() and torch.isfinite(S).all() and torch.isfinite(z).all()
-    heads = _sample_heads(w.B, w.H)
-    sel = lambda t: None if t is None else torch.stack([t[b, h] for b, h in heads])[None]
-    ref_y, ref_S, ref_z = oracle_mod.scan(to_oracle(sel(inp["q"])), to_oracle(sel(inp["k"])),
-                                          to_oracle(sel(inp["v"])), alpha=to_oracle(sel(inp["alpha"])), eps=w.eps)
-    got_y = torch.stack([y[b, h] for b, h in heads]).float().cpu().numpy()[None]
-    got_S = torch.stack([S[b, h] for b, h in heads]).cpu().numpy()[None]
-    got_z = torch.stack([z[b, h] for b, h in heads]).cpu().numpy()[None]
-    for what, g, r in (("y", got_y, ref_y), ("S", got_S, ref_S), ("z", got_z, ref_z)):
-        err = max_rel_err(g, r)
-        assert err <= 2e-2, f"{name} {what}: max rel err {err:.3e}"
+    y, S, z = y.cpu(), S.cpu(), z.cpu()
+    del d
+    torch.cuda.empty_cache()
+    # all heads, a group at a time (the oracle's threads run over the heads of a group;
+    # the group bounds the host memory of the FP64 outputs)
+    per = max(1, min(w.B * w.H, (1 << 27) // (w.T * w.dv)))
+    worst = {"y": 0.0, "S": 0.0, "z": 0.0}
+    for grp in _head_groups(w.B, w.H, per):
+        sel = lambda t: None if t is None else torch.stack([t[b, h] for b, h in grp])[None]
+        ref = oracle_mod.scan(to_oracle(sel(inp["q"])), to_oracle(sel(inp["k"])), to_oracle(sel(inp["v"])),
+                              alpha=to_oracle(sel(inp["alpha"])), eps=w.eps)
+        got = (sel(y).float().numpy(), sel(S).numpy(), sel(z).numpy())
+        for what, g, r in zip(("y", "S", "z"), got, ref):
+            _, r_err = assert_close(g, r, 2e-2, f"{name} {what} heads {grp[0]}..{grp[-1]}")
+            worst[what] = max(worst[what], r_err)
+    print(f"[parity] {name}: worst per-row error over all {w.B * w.H} heads: {worst}")
 
 
 def test_decode_full_size(la, oracle_mod):
@@ -55,5 +62,4 @@ def test_decode_full_size(la, oracle_mod):
     assert la.last_device_status() == 0
     for what, g, r in (("y", y.float().cpu().numpy(), ref_y), ("S", d["S"].cpu().numpy(), ref_S),
                        ("z", d["z"].cpu().numpy(), ref_z)):
-        err = max_rel_err(g, r)
-        assert err <= 2e-2, f"decode {what}: max rel err {err:.3e}"
+        assert_close(g, r, 2e-2, f"decode {what}")

@@ -1,6 +1,8 @@
 """CUDA path (through the C ABI) against the FP64 oracle, element by element, on
-identical seeded inputs.  Tolerances: max relative error (max|gpu-ref| / max|ref|
-per tensor) 2e-2 for BF16 inputs and 1e-5 for FP32 inputs.
+identical seeded inputs.  Tolerances: 2e-2 for BF16 inputs and 1e-5 for FP32
+inputs, on the relative error of the whole tensor (max|gpu-ref| / max|ref|) and
+on that of every row (every token of y, every feature row of S, the z vector of
+every head), so that small late-sequence outputs are held to their own size.
 
 Sources: LA = "Linear attention：把历史写进状态" (hs-black.github.io/posts/linear-attention);
 LC = "45. Linear Attention and Recurrent State | 线性注意力与递推状态" (datawhalechina, ch. 45).
@@ -9,7 +11,7 @@ import numpy as np
 import pytest
 import torch
 
-from conftest import max_rel_err, to_oracle
+from conftest import assert_close, to_oracle
 
 pytestmark = pytest.mark.gpu
 
@@ -41,9 +43,7 @@ def _gpu_prefill(la, inp, chunk=64, eps=1e-6):
 
 def _check(got, ref, tol, what=""):
     for name, g, r in zip(("y", "S", "z"), got, ref):
-        assert np.isfinite(g).all(), f"{what} {name} not finite"
-        err = max_rel_err(g, r)
-        assert err <= tol, f"{what} {name}: max rel err {err:.3e} > {tol}"
+        assert_close(g, r, tol, f"{what} {name}")
 
 
 def _inputs(dtype, B, H, T, r, dv, gated=False, with_state=False, seed=0, scale=1.0):
@@ -111,6 +111,18 @@ def test_prefill_bf16_lengths(la, oracle_mod, T, dv):
 def test_prefill_bf16_several_tiles(la, oracle_mod, gated, with_state):
     inp = _inputs(torch.bfloat16, 2, 3, 9 * 64 + 5, 128, 128, gated=gated, with_state=with_state, seed=5)
     _check(_gpu_prefill(la, inp), _oracle_prefill(oracle_mod, inp), 2e-2, "bf16")
+
+
+@pytest.mark.parametrize("chunk", [1, 32, 100])
+def test_prefill_bf16_chunk_argument(la, oracle_mod, chunk):
+    """Any chunk length is accepted: the result does not depend on it (LA "动手实验"),
+    and the tensor-core kernel computes in chunks of 64 tokens whatever is asked for."""
+    inp = _inputs(torch.bfloat16, 1, 2, 3 * 64 + 9, 128, 128, gated=True, seed=41)
+    got = _gpu_prefill(la, inp, chunk=chunk)
+    base = _gpu_prefill(la, inp, chunk=64)
+    for g, b in zip(got, base):
+        np.testing.assert_array_equal(g, b)
+    _check(got, _oracle_prefill(oracle_mod, inp), 2e-2, f"chunk={chunk}")
 
 
 def test_prefill_bf16_zero_gates(la, oracle_mod):

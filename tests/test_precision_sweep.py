@@ -10,7 +10,7 @@ import numpy as np
 import pytest
 import torch
 
-from conftest import max_rel_err, to_oracle
+from conftest import max_rel_err, row_rel_err, to_oracle
 
 TOL = 2e-2
 
@@ -53,11 +53,13 @@ def test_precision_sweep_gpu(la, oracle_mod, T, scale, gated):
     assert la.last_device_status() == 0
     got = (y.float().cpu().numpy(), S.cpu().numpy(), z.cpu().numpy())
     errs = [max_rel_err(g, r) for g, r in zip(got, ref)]
+    rows = [row_rel_err(g, r) for g, r in zip(got, ref)]
     den = _min_denominator(inp["q"], inp["k"], inp["alpha"], 1e-6)
     print(f"\nsweep T={T:5d} scale={scale:3.1f} gated={int(gated)}  max rel err y {errs[0]:.2e} "
-          f"S {errs[1]:.2e} z {errs[2]:.2e}  min denominator {den:.3e}")
+          f"S {errs[1]:.2e} z {errs[2]:.2e}  per row y {rows[0]:.2e} S {rows[1]:.2e} z {rows[2]:.2e}  "
+          f"min denominator {den:.3e}")
     assert all(np.isfinite(g).all() for g in got)
-    assert max(errs) <= TOL
+    assert max(errs) <= TOL and max(rows) <= TOL
 
 
 @pytest.mark.parametrize("C", [1, 16, 64, 256])
