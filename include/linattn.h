@@ -157,7 +157,7 @@ la_status la_prefill_varlen(const void *q, const void *k, const void *v, la_dtyp
 
 /*
  * la_prefill_chunked_noalloc -- la_prefill_chunked without caller scratch: the
- * workspace is a 16 MiB buffer compiled into the library (a static device array),
+ * workspace is a 32 MiB buffer compiled into the library (a static device array),
  * one per device for the whole process.  The pages have no counterpart; it is an
  * integration aid for callers that must not allocate device memory per call,
  * such as a serving loop that reserved its whole memory budget up front, or C
@@ -165,7 +165,8 @@ la_status la_prefill_varlen(const void *q, const void *k, const void *v, la_dtyp
  * device-wide synchronisation and can fail under memory pressure.
  *   Arguments, results and errors are those of la_prefill_chunked, without
  *   workspace.  LA_ERR_WORKSPACE when la_prefill_workspace_bytes for these sizes
- *   exceeds the 16 MiB (on a 152-SM device no size needs more than about 10 MB).
+ *   exceeds the 32 MiB (the largest workspace la_prefill_workspace_bytes returns on
+ *   devices with up to about 240 SMs).
  *   The first call on a device looks up the buffer's device address with that
  *   device current; make it before any stream capture.  The look-up is cached
  *   per device in an atomic, so first calls from several host threads are safe.

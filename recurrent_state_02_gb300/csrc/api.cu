@@ -36,17 +36,45 @@ EncodeTiledFn encode_fn()
     return fn;
 }
 
-// Sequence segmentation of the BF16 prefill.  A launch has B*H*(dv/64) CTAs,
-// one per (b, h, 64-column slice); when that leaves at least half of the SMs
-// idle and the sequence is long enough, every head's chunks are split into
-// nseg segments that run in parallel from scanned start states.  The first
-// nseg - 1 segments are each cut into sub_per_seg parts for the state pass,
-// again sized to fill the GPU.
-constexpr int kMinSegChunks = 16;   // at least 1024 tokens per segment
+// Sequence segmentation of the BF16 prefill.  The chunk kernel runs one CTA per
+// (b, h, dvs-column slice): 64-column slices when they fill one wave of the GPU
+// without segments, a whole head (dv == 128) otherwise -- it forms phi(Q),
+// phi(K) and the scores once per head, about half the instructions of two
+// slices per chunk, but a chunk takes longer; when that leaves at least half of
+// the SMs idle and
+// the sequence is long enough, every head's chunks are split into nseg segments
+// that run in parallel from scanned start states.  The state pass over the first
+// nseg - 1 segments runs one CTA per (b, h, dvs-column slice, part), two resident
+// per SM; each segment is cut into sub_per_seg parts, the count that minimises
+// (waves of state CTAs) x (chunks per part + a per-CTA set-up cost).
+// LA_HEAD_CTA: 0 = always slices, 1 = the rule above, 2 = whole heads whenever dv == 128
+#ifndef LA_HEAD_CTA
+#define LA_HEAD_CTA 1
+#endif
+constexpr int kMinSegChunks = 16;    // at least 1024 tokens per segment
+constexpr int kStateCtasPerSm = 2;   // resident state-pass CTAs per SM
+constexpr int kStateCtaSetup = 2;    // set-up and pipeline fill of a state CTA, in chunks
+// Largest workspace a plan may ask for.  With one part per segment every plan of
+// a device with up to about 240 SMs stays below it (the plan keeps
+// (parts + segments) * heads below about 2 * SMs states of 66 KB); finer parts
+// are used only while they fit.
+constexpr size_t kMaxPlanWorkspace = size_t(32) << 20;
 
 struct SegPlan {
+    int dvs = 64;   // value columns per chunk-kernel CTA
     int nseg = 1, seg_chunks = 0, sub_per_seg = 1, sub_chunks = 0, nsub = 0;
 };
+
+size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// Workspace (FP32): A [nsub][B*H], dS [nsub][B*H][state], S_start [nseg][B*H][state],
+// state = 128*dv + 128 (S then z); every part starts on a 256-byte boundary.
+size_t seg_workspace_bytes(int nsub, int nseg, int B, int H, int dv)
+{
+    if (nseg <= 1) return 0;
+    const size_t BH = (size_t)B * H, state = 128 * (size_t)dv + 128;
+    return round_up((size_t)nsub * BH * 4, 256) + (size_t)nsub * BH * state * 4 + (size_t)nseg * BH * state * 4;
+}
 
 int sm_count()
 {
@@ -61,10 +89,20 @@ int sm_count()
     return n;
 }
 
+// Value columns per chunk-kernel CTA for B*H heads of dv columns on `sms` SMs.
+int head_width(long long B, long long H, int dv, long long sms)
+{
+    if (dv != 128 || LA_HEAD_CTA == 0) return 64;
+    if (LA_HEAD_CTA == 2) return 128;
+    const long long slices = B * H * (dv / 64);
+    return (5 * slices >= 4 * sms && slices <= sms) ? 64 : 128;
+}
+
 SegPlan seg_plan(int B, int H, int T, int dv)
 {
     SegPlan p;
-    const long long units = (long long)B * H * (dv / 64);
+    p.dvs = head_width(B, H, dv, sm_count());
+    const long long units = (long long)B * H * (dv / p.dvs);   // chunk-kernel CTAs per segment
     const long long sms = sm_count();
     const int nch = (T + 63) / 64;
     long long g = units > 0 ? sms / units : 0;
@@ -73,9 +111,22 @@ SegPlan seg_plan(int B, int H, int T, int dv)
     const int L = (int)((nch + g - 1) / g);
     const int G = (nch + L - 1) / L;
     if (G < 2) return p;
-    long long per = sms / (units * (G - 1));
-    per = per < 1 ? 1 : (per > L ? L : per);
-    const int L1 = (int)((L + per - 1) / per);
+    // parts per segment for the state pass (one CTA per (b, h, dvs-column slice, part))
+    const long long sunits = units * (G - 1);
+    const long long slots = kStateCtasPerSm * sms;
+    long long best_cost = -1;
+    int best_n = 1;
+    for (int n = 1; n <= L; ++n) {
+        const int Ln = (L + n - 1) / n, parts = (L + Ln - 1) / Ln;
+        if (n > 1 && seg_workspace_bytes((G - 1) * parts, G, B, H, dv) > kMaxPlanWorkspace) break;
+        const long long waves = (sunits * n + slots - 1) / slots;
+        const long long cost = waves * ((L + n - 1) / n + kStateCtaSetup);
+        if (best_cost < 0 || cost < best_cost) {
+            best_cost = cost;
+            best_n = n;
+        }
+    }
+    const int L1 = (L + best_n - 1) / best_n;
     p.nseg = G;
     p.seg_chunks = L;
     p.sub_chunks = L1;
@@ -84,22 +135,15 @@ SegPlan seg_plan(int B, int H, int T, int dv)
     return p;
 }
 
-size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
-
-// Workspace (FP32): A [nsub][B*H], dS [nsub][B*H][state], S_start [nseg][B*H][state],
-// state = 128*dv + 128 (S then z); every part starts on a 256-byte boundary.
 size_t seg_workspace_bytes(const SegPlan &p, int B, int H, int dv)
 {
-    if (p.nseg <= 1) return 0;
-    const size_t BH = (size_t)B * H, state = 128 * (size_t)dv + 128;
-    return round_up((size_t)p.nsub * BH * 4, 256) + (size_t)p.nsub * BH * state * 4 + (size_t)p.nseg * BH * state * 4;
+    return seg_workspace_bytes(p.nsub, p.nseg, B, H, dv);
 }
 
 // Scratch of la_prefill_chunked_noalloc: a fixed buffer in the library's device
-// image, for callers that cannot pass device memory of their own.  16 MiB holds
-// the segmented-prefill workspace of every plan on devices with up to about 240
-// SMs (the plan keeps (parts + segments) * heads below about 2 * SMs states).
-constexpr size_t kNoAllocScratchBytes = size_t(16) << 20;
+// image, for callers that cannot pass device memory of their own.  It holds the
+// largest workspace a plan asks for (kMaxPlanWorkspace).
+constexpr size_t kNoAllocScratchBytes = kMaxPlanWorkspace;
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 
 // Device address of the scratch on the current device, looked up once per device
@@ -283,7 +327,7 @@ la_status la_prefill_chunked(const void *q, const void *k, const void *v, la_dty
         sa.seg_chunks = plan.seg_chunks;
         sa.status = status;
         sa.wait_limit_ns = la::kWaitLimitNs;
-        cudaError_t e = la::launch_state_tc(mk, mv, sa, B, alpha != nullptr, st);
+        cudaError_t e = la::launch_state_tc(mk, mv, sa, B, alpha != nullptr, plan.dvs, st);
         if (e == cudaSuccess)
             e = la::launch_seg_scan(S0, z0, A, dS, S_start, (int)BH, dv, plan.nsub, plan.sub_per_seg, plan.nseg, st);
         if (e != cudaSuccess) return from_cuda(e);
@@ -291,7 +335,7 @@ la_status la_prefill_chunked(const void *q, const void *k, const void *v, la_dty
         a.seg_chunks = plan.seg_chunks;
         a.S_start = S_start;
     }
-    return from_cuda(la::launch_prefill_tc(mq, mk, mv, a, B, alpha != nullptr, st));
+    return from_cuda(la::launch_prefill_tc(mq, mk, mv, a, B, alpha != nullptr, plan.dvs, st));
 }
 
 la_status la_prefill_varlen(const void *q, const void *k, const void *v, la_dtype dtype, const float *alpha,
@@ -340,7 +384,9 @@ la_status la_prefill_varlen(const void *q, const void *k, const void *v, la_dtyp
     a.seg_chunks = 0;
     a.S_start = nullptr;
     a.cu_seqlens = cu_seqlens;
-    return from_cuda(la::launch_prefill_tc(mq, mk, mv, a, B, alpha != nullptr, reinterpret_cast<cudaStream_t>(stream)));
+    const int dvs = head_width(B, H, dv, sm_count());
+    return from_cuda(
+        la::launch_prefill_tc(mq, mk, mv, a, B, alpha != nullptr, dvs, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 la_status la_prefill_chunked_noalloc(const void *q, const void *k, const void *v, la_dtype dtype,

@@ -67,15 +67,16 @@ struct PrefillTcArgs {
     unsigned long long wait_limit_ns;
 };
 
-// BF16 tensor-core prefill; r == 128, dv a multiple of 64, chunk 64.
-// Tensor maps: q, k over [B*H, T, 128]; v over [B*H, T, dv] (BF16, 128-byte
-// swizzle, boxes of 64 x 64).
+// BF16 tensor-core prefill; r == 128, dv a multiple of dvs, chunk 64.  dvs: value
+// columns per CTA, 64 (the slices of a head form a cluster) or 128 (one CTA per
+// head and segment).  Tensor maps: q, k over [B*H, T, 128]; v over [B*H, T, dv]
+// (BF16, 128-byte swizzle, boxes of 64 x 64).
 cudaError_t launch_prefill_tc(const CUtensorMap &map_q, const CUtensorMap &map_k,
-                              const CUtensorMap &map_v, const PrefillTcArgs &a, int B, bool gated,
+                              const CUtensorMap &map_v, const PrefillTcArgs &a, int B, bool gated, int dvs,
                               cudaStream_t stream);
 
 // State pass of the sequence-segmented BF16 prefill (r == 128, dv a multiple of
-// 64, chunk 64): for every sub-segment of a head's sequence, the state it would
+// dvs, chunk 64): for every sub-segment of a head's sequence, the state it would
 // produce from a zero state and the product of its gates.
 struct StateTcArgs {
     const float *alpha;   // [B,H,T] or nullptr
@@ -90,10 +91,10 @@ struct StateTcArgs {
     unsigned long long wait_limit_ns;
 };
 
-// grid (dv/64, H, B*nsub); tensor maps k over [B*H, T, 128] and v over [B*H, T, dv]
-// as for launch_prefill_tc.
+// grid (dv/dvs, H, B*nsub) with dvs (64 or 128) value columns per CTA; tensor maps
+// k over [B*H, T, 128] and v over [B*H, T, dv] as for launch_prefill_tc.
 cudaError_t launch_state_tc(const CUtensorMap &map_k, const CUtensorMap &map_v, const StateTcArgs &a, int B,
-                            bool gated, cudaStream_t stream);
+                            bool gated, int dvs, cudaStream_t stream);
 
 // S_start[g][bh] (S then z) for g < nseg: S0/z0 (zero if null) carried through the
 // sub-segment maps S -> A S + dS in order.

@@ -47,7 +47,9 @@
 namespace la {
 namespace {
 
-constexpr int kDVS = 64;        // value columns per CTA
+// Value columns per CTA (DVS): 64 (a head's dv is split over a cluster of CTAs)
+// or 128 (one CTA owns a whole head: phi(Q), phi(K) and the scores are formed
+// once per head; sequence segments then fill the GPU).
 // 24 warps.  Warp w runs on scheduler w % 4 and may access TMEM lane quadrant
 // w % 4.  Warps 4..19 are the TMEM warps (four per quadrant); the producer, the
 // three MMA issuers and the phi warps are spread so that every scheduler hosts
@@ -78,12 +80,11 @@ static_assert((kPhiMask & (kFixedRoles | (1u << kWarpMmaS) | (1u << kWarpMmaP)))
 // of feature rows 32 qd .. +31.  Its piece of A lies strictly above the
 // diagonal (always zero) when qq > qd: 6 of the 16 warps never read P.
 constexpr uint32_t kTileQ = kC * kR * 2;      // 16 KB: two 64-feature blocks of 64 rows x 128 B
-constexpr uint32_t kTileV = kC * kDVS * 2;    // 8 KB
 constexpr uint32_t kTileA = kC * kC * 2;      // 8 KB
-// [Sprev | zhi zlo 0..]: 128 feature rows x 80 columns, 32-byte swizzle, five
-// blocks of 16 columns (4 KB each); column 64 holds zhi and 65 zlo.
-constexpr uint32_t kTileSpZ = 5 * kR * 32;    // 20 KB
-// the second 64-column block of [V | 1 0..] (128-byte swizzle, column 0 = 1)
+constexpr uint32_t kBlkV = kC * 64 * 2;       // one 64-column block of V (8 KB)
+constexpr uint32_t kBlkSpZ = kR * 32;         // one 16-column block of [Sprev | z] (4 KB)
+// the block of ones that follows V in the [V | 1 0..] operand (128-byte swizzle,
+// column 0 = 1)
 constexpr uint32_t kTileOnes = kC * 128;      // 8 KB
 
 __host__ __device__ constexpr bool is_phi_warp(int w) { return (kPhiMask >> w) & 1u; }
@@ -103,24 +104,39 @@ __host__ __device__ constexpr int phi_index(int w) { return __builtin_popcount(k
 #define LA_SP_BUFS 2
 #endif
 
-template <bool GATED>
+#ifndef LA_STAGES_HEAD
+#define LA_STAGES_HEAD 3
+#endif
+
+template <bool GATED, int DVS>
 struct Cfg {
-    static constexpr int kStages = GATED ? LA_STAGES_GATED : LA_STAGES;
-    static constexpr int kSpBufs = LA_SP_BUFS;                 // [Sprev | z] tiles
-    static constexpr int kNP = 2;                              // P accumulator buffers
-    static constexpr int kNO = 3;                              // [O | dn] accumulator buffers
-    // TMEM columns: P (x2), the state [S | z] (80: z is column 64) and [O | dn]
-    // blocks of 80 (x3; dn is columns 64 and 65)
+    static_assert(DVS == 64 || DVS == 128, "value columns per CTA");
+    static constexpr bool kHead = DVS == 128;
+    // The whole-head CTA needs 48 KB per stage and a 36 KB [Sprev | z] tile, so it
+    // keeps three stages and one such tile.
+    static constexpr int kStages = kHead ? LA_STAGES_HEAD : (GATED ? LA_STAGES_GATED : LA_STAGES);
+    static constexpr int kSpBufs = kHead ? 1 : LA_SP_BUFS;     // [Sprev | z] tiles
+    static constexpr int kNP = kHead ? 1 : 2;                  // P accumulator buffers
+    static constexpr int kNO = kHead ? 2 : 3;                  // [O | dn] accumulator buffers
+    static constexpr int kLag = kNO - 1;                       // outputs of chunk c - kLag finish in iteration c
+    static constexpr int kW = DVS + 16;                        // [S | z] and [O | dn] columns
+    static constexpr int kSC = DVS / 4;                        // state and output columns per TMEM warp
+    // TMEM columns: P (x kNP), the state [S | z] (z is column DVS) and [O | dn]
+    // blocks (x kNO; dn is columns DVS and DVS + 1)
     static constexpr uint32_t kColP = 0;
     static constexpr uint32_t kColS = kNP * 64;
-    static constexpr uint32_t kColO = kColS + 80;
-    static constexpr uint32_t kCols = kColO + kNO * 80;
+    static constexpr uint32_t kColO = kColS + kW;
+    static constexpr uint32_t kCols = kColO + kNO * kW;
     static_assert(kCols <= 512, "TMEM budget");
+    // V tile and [Sprev | zhi zlo 0..] tile: 128 feature rows x kW columns in
+    // 32-byte-swizzled blocks of 16 columns; block DVS/16 holds zhi (column 0) and zlo (1)
+    static constexpr uint32_t kTileV = (DVS / 64) * kBlkV;
+    static constexpr uint32_t kTileSpZ = (kW / 16) * kBlkSpZ;
     // shared memory (offsets from a 1024-aligned base)
     static constexpr uint32_t kOffQ = 0, kOffK = kTileQ, kOffV = 2 * kTileQ;
     static constexpr uint32_t kStageBytes = kOffV + kTileV;
     static_assert(kStageBytes % 1024 == 0, "stage tiles stay 1024-byte aligned");
-    // A and [Sprev | z] are double-buffered
+    // A is double-buffered
     static constexpr uint32_t kOffA = kStages * kStageBytes;
     static constexpr uint32_t kOffSpZ = kOffA + 2 * kTileA;
     static constexpr uint32_t kOffOnes = kOffSpZ + kSpBufs * kTileSpZ;
@@ -140,19 +156,21 @@ struct alignas(16) Small {
     int abort_flag;
 };
 
-template <bool GATED>
-constexpr uint32_t smem_bytes() { return Cfg<GATED>::kOffSmall + sizeof(Small) + 1024; }
-static_assert(smem_bytes<false>() <= 232448, "shared memory budget");
-static_assert(smem_bytes<true>() <= 232448, "shared memory budget");
+template <bool GATED, int DVS>
+constexpr uint32_t smem_bytes() { return Cfg<GATED, DVS>::kOffSmall + sizeof(Small) + 1024; }
+static_assert(smem_bytes<false, 64>() <= 232448, "shared memory budget");
+static_assert(smem_bytes<true, 64>() <= 232448, "shared memory budget");
+static_assert(smem_bytes<false, 128>() <= 232448, "shared memory budget");
+static_assert(smem_bytes<true, 128>() <= 232448, "shared memory budget");
 
-template <bool GATED>
+template <bool GATED, int DVS>
 __global__ void __launch_bounds__(kThreads, 1)
 prefill_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
                   const __grid_constant__ CUtensorMap map_v, const PrefillTcArgs args)
 {
-    using L = Cfg<GATED>;
-    constexpr int NST = L::kStages, NP = L::kNP;
-    static_assert(NP == 2, "score buffers alternate with the parity of tm_read");
+    using L = Cfg<GATED, DVS>;
+    constexpr int NST = L::kStages, NP = L::kNP, SC = L::kSC;
+    static_assert(NP == 1 || NP == 2, "score buffers");
     extern __shared__ uint8_t smem_raw[];
     uint8_t *base = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     Small *sm = reinterpret_cast<Small *>(base + L::kOffSmall);
@@ -232,9 +250,10 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
     // block is complete here (column 0 = 1 in every token row).
     for (int i = threadIdx.x; i < (int)(2 * kTileA / 16); i += kThreads)   // A: the blocks above the diagonal stay 0
         reinterpret_cast<uint4 *>(base + L::kOffA)[i] = make_uint4(0, 0, 0, 0);
-    for (int i = threadIdx.x; i < L::kSpBufs * (kR * 32 / 16); i += kThreads) {
-        const int buf = i / (kR * 32 / 16), j = i % (kR * 32 / 16);
-        reinterpret_cast<uint4 *>(base + L::kOffSpZ + buf * kTileSpZ + 4 * kR * 32)[j] = make_uint4(0, 0, 0, 0);
+    for (int i = threadIdx.x; i < L::kSpBufs * (kBlkSpZ / 16); i += kThreads) {
+        const int buf = i / (kBlkSpZ / 16), j = i % (kBlkSpZ / 16);
+        reinterpret_cast<uint4 *>(base + L::kOffSpZ + buf * L::kTileSpZ + (DVS / 16) * kBlkSpZ)[j] =
+            make_uint4(0, 0, 0, 0);
     }
     for (int i = threadIdx.x; i < (int)kTileOnes / 16; i += kThreads)
         reinterpret_cast<uint4 *>(base + L::kOffOnes)[i] = make_uint4(0, 0, 0, 0);
@@ -282,13 +301,15 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
             if (__shfl_sync(0xffffffffu, aborted(cx) ? 1 : 0, 0)) break;
             uint8_t *st = stage_ptr(s);
             if (lane == 0) {
-                mbar_arrive_expect_tx(&sm->full[s], 2 * kTileQ + kTileV);
+                mbar_arrive_expect_tx(&sm->full[s], 2 * kTileQ + L::kTileV);
                 const int cy = tma_c1(t0), cz = tma_c2(t0);
                 tma_load_3d(st + L::kOffQ, &map_q, &sm->full[s], 0, cy, cz);
                 tma_load_3d(st + L::kOffQ + kTileQ / 2, &map_q, &sm->full[s], 64, cy, cz);
                 tma_load_3d(st + L::kOffK, &map_k, &sm->full[s], 0, cy, cz);
                 tma_load_3d(st + L::kOffK + kTileQ / 2, &map_k, &sm->full[s], 64, cy, cz);
-                tma_load_3d(st + L::kOffV, &map_v, &sm->full[s], slice * kDVS, cy, cz);
+#pragma unroll
+                for (int vb = 0; vb < DVS / 64; ++vb)
+                    tma_load_3d(st + L::kOffV + vb * kBlkV, &map_v, &sm->full[s], slice * DVS + vb * 64, cy, cz);
                 // The load of chunk c + NST waits for this stage to come free, which
                 // takes about as long as a load from HBM: warm L2 for it now.
                 if (c + NST < nch) {
@@ -299,7 +320,8 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
                         tma_prefetch_l2_3d(&map_k, 0, yp, zp);
                         tma_prefetch_l2_3d(&map_k, 64, yp, zp);
                     }
-                    tma_prefetch_l2_3d(&map_v, slice * kDVS, yp, zp);
+#pragma unroll
+                    for (int vb = 0; vb < DVS / 64; ++vb) tma_prefetch_l2_3d(&map_v, slice * DVS + vb * 64, yp, zp);
                 }
             }
             if (GATED) {
@@ -325,11 +347,18 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
         // stage's empty barrier after its last read of it.
         if (lane == 0) {
             constexpr uint32_t idP = idesc_bf16_f32(64, 64, false, false);
-            constexpr uint32_t idDS = idesc_bf16_f32(128, 80, true, true);   // [S | z] increment
-            constexpr uint32_t idQS = idesc_bf16_f32(64, 80, false, true);   // [O | dn]
-            // [O | dn] += A [V | 1]: column 64 gains the row sums of A
-            constexpr uint32_t idAV = idesc_bf16_f32(64, 80, false, true);
+            // [S | z] increment and [O | dn] += A [V | 1] (column DVS gains the row
+            // sums of A).  With 64 value columns one MMA spans the V block and the
+            // first 16 columns of the ones block (at LBO); with 128 the two V blocks
+            // (LBO = one block) and the ones block are two MMAs.
+            constexpr int NV = DVS == 64 ? 80 : DVS;
+            constexpr uint32_t idDS = idesc_bf16_f32(128, NV, true, true);
+            constexpr uint32_t idDS1 = idesc_bf16_f32(128, 16, true, true);
+            constexpr uint32_t idQS = idesc_bf16_f32(64, L::kW, false, true);   // [O | dn] = Q~ [Sprev | z]
+            constexpr uint32_t idAV = idesc_bf16_f32(64, NV, false, true);
+            constexpr uint32_t idAV1 = idesc_bf16_f32(64, 16, false, true);
             const uint32_t aOnes = smem_u32(base + L::kOffOnes);
+            const uint32_t onesLo = desc_lo(aOnes, kBlkV);
             constexpr uint32_t kHi128 = desc_hi(1024, 2), kHi32 = desc_hi(256, 6);   // SBO and swizzle words
             // P = Q~ K~^T for chunk c
             auto issue_p = [&](int c) -> bool {
@@ -337,8 +366,8 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
                 const uint32_t st = smem_u32(stage_ptr(s));
                 const uint32_t aQ = st + L::kOffQ, aK = st + L::kOffK;
                 if (!wait(cx, &sm->phi_done[s], (c / NST) & 1)) return false;
-                // the P buffer of chunk c - 2 has been read (NP == 2)
-                if (c >= NP && !wait(cx, &sm->tm_read[c & 1], ((c >> 1) - 1) & 1)) return false;
+                // the P buffer of chunk c - NP has been read
+                if (c >= NP && !wait(cx, &sm->tm_read[(c - NP) & 1], ((c - NP) >> 1) & 1)) return false;
                 tc_fence_after();
                 const uint32_t qlo = desc_lo(aQ, 16), klo = desc_lo(aK, 16), dP = tmem + L::kColP + pb * 64;
 #pragma unroll
@@ -359,8 +388,8 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
                 const int s = c % NST;
                 const uint32_t st = smem_u32(stage_ptr(s));
                 const uint32_t aK = st + L::kOffK;
-                // B = [V | 1]: the V tile, then the ones block at LBO
-                const uint32_t blo = desc_lo(st + L::kOffV, aOnes - (st + L::kOffV));
+                // B = [V | 1]: the V tile, then (64 value columns) the ones block at LBO
+                const uint32_t blo = desc_lo(st + L::kOffV, DVS == 64 ? aOnes - (st + L::kOffV) : kBlkV);
                 if (!GATED && !wait(cx, &sm->phi_done[s], (c / NST) & 1)) return false;
                 if (GATED && !wait(cx, &sm->sc_done[s], (c / NST) & 1)) return false;
                 if (!wait(cx, &sm->tm_read[c & 1], (c >> 1) & 1)) return false;   // state read (and decayed)
@@ -368,8 +397,12 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
                 const uint32_t dS = tmem + L::kColS;
                 const uint32_t klo = desc_lo(aK, kTileQ / 2);   // K~^T: MN-major, two 64-feature blocks
 #pragma unroll
-                for (int kk = 0; kk < 4; ++kk)
+                for (int kk = 0; kk < 4; ++kk) {
                     tc_mma_bf16_w<true>(dS, klo + kk * (2048 >> 4), kHi128, blo + kk * (2048 >> 4), kHi128, idDS);
+                    if (DVS == 128)
+                        tc_mma_bf16_w<true>(dS + DVS, klo + kk * (2048 >> 4), kHi128, onesLo + kk * (2048 >> 4), kHi128,
+                                            idDS1);
+                }
                 tc_commit(&sm->dS_full);
                 tc_commit(&sm->empty[s]);   // this issuer's last read of stage s
                 return true;
@@ -386,16 +419,16 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
                 const uint32_t aQ = st + L::kOffQ, aV = st + L::kOffV;
                 const uint32_t aA = smem_u32(base + L::kOffA + bb * kTileA);
                 const int sb = c % L::kSpBufs;
-                const uint32_t aSpZ = smem_u32(base + L::kOffSpZ + sb * kTileSpZ);
+                const uint32_t aSpZ = smem_u32(base + L::kOffSpZ + sb * L::kTileSpZ);
                 // [O | dn] = Q~ [Sprev | zhi zlo] (gated: Q~ rows already scaled by Gamma_i),
-                // then [O | dn] += A [V | 1], into the buffer that held O of chunk c-3
+                // then [O | dn] += A [V | 1], into the buffer that held O of chunk c - kNO
                 const int ob = c % L::kNO;
                 if (GATED && !wait(cx, &sm->sc_done[s], (c / NST) & 1)) break;
                 if (!wait(cx, &sm->ops_full[bb], n & 1)) break;
                 if (c >= L::kNO && !wait(cx, &sm->O_empty[ob], ((c / L::kNO) - 1) & 1)) break;
                 tc_fence_after();
-                const uint32_t dO = tmem + L::kColO + ob * 80;
-                const uint32_t qlo = desc_lo(aQ, 16), slo = desc_lo(aSpZ, kR * 32);
+                const uint32_t dO = tmem + L::kColO + ob * L::kW;
+                const uint32_t qlo = desc_lo(aQ, 16), slo = desc_lo(aSpZ, kBlkSpZ);
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk) {
                     const uint32_t o = ((kk >> 2) * (kTileQ / 2) + (kk & 3) * 32) >> 4;
@@ -404,10 +437,14 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
                 }
                 if (L::kSpBufs == 1) tc_commit(&sm->Sp_empty);
                 const uint32_t alo = desc_lo(aA, 16);
-                const uint32_t vlo = desc_lo(aV, aOnes - aV);
+                const uint32_t vlo = desc_lo(aV, DVS == 64 ? aOnes - aV : kBlkV);
 #pragma unroll
-                for (int kk = 0; kk < 4; ++kk)
+                for (int kk = 0; kk < 4; ++kk) {
                     tc_mma_bf16_w<true>(dO, alo + kk * (32 >> 4), kHi128, vlo + kk * (2048 >> 4), kHi128, idAV);
+                    if (DVS == 128)
+                        tc_mma_bf16_w<true>(dO + DVS, alo + kk * (32 >> 4), kHi128, onesLo + kk * (2048 >> 4), kHi128,
+                                            idAV1);
+                }
                 tc_commit(&sm->A_empty[bb]);
                 tc_commit(&sm->O_full[ob]);
                 tc_commit(&sm->empty[s]);
@@ -424,61 +461,79 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
         // state increments.  Iteration c reads the state after chunk c-1 (it
         // becomes Sprev of chunk c; with a gate it is then decayed by Gamma_last
         // of chunk c in place, ahead of chunk c's increment), turns the scores of
-        // chunk c into A, and finishes the outputs of chunk c-2.  Each warp
-        // stores its own 16 x 16 piece of y.
+        // chunk c into A, and finishes the outputs of chunk c - kLag.  Each warp
+        // stores its own 16-row x SC-column piece of y.
+        constexpr int LAG = L::kLag;
         const int tw = warp - kWarpTm0;          // 0..15
         const int qd = warp & 3;                 // TMEM lane quadrant this warp may access
-        const int qq = tw >> 2;                  // column quarter: columns 16 qq .. +15
+        const int qq = tw >> 2;                  // column quarter
         const uint32_t lane_base = static_cast<uint32_t>(qd * 32) << 16;
         const int srow = qd * 32 + lane;         // state row (feature index) of this thread
         const int prow = qd * 16 + (lane & 15);  // row of the M = 64 tiles (16x32bx2 loads)
-        const int pcol = qq * 16 + (lane >> 4) * 8;   // first of this thread's 8 columns
+        const int pcol = qq * 16 + (lane >> 4) * 8;   // first of this thread's 8 columns of P and A
+        const int ocol = qq * SC + (lane >> 4) * (SC / 2);   // first of its SC/2 columns of O and y
         const bool a_zero = qq > qd;             // this warp's piece of A is above the diagonal
-        const uint32_t tS = tmem + lane_base + L::kColS + qq * 16;   // this thread's 16 state columns
-        const uint32_t tz = tmem + lane_base + L::kColS + 64;        // z (column 64; qq == 0 warps)
+        const uint32_t tS = tmem + lane_base + L::kColS + qq * SC;   // this thread's SC state columns
+        const uint32_t tz = tmem + lane_base + L::kColS + DVS;       // z (column DVS; qq == 0 warps)
+        auto ld_state = [&](float (&v)[SC]) {
+            if constexpr (SC == 16) tc_ld_32x32b_x16(tS, v);
+            else tc_ld_32x32b_x32(tS, v);
+        };
+        auto st_state = [&](const float (&v)[SC]) {
+            if constexpr (SC == 16) tc_st_32x32b_x16(tS, v);
+            else tc_st_32x32b_x32(tS, v);
+        };
         {
-            // initial state
-            float S[16];
-            const float *src = S_init ? S_init + (size_t)srow * args.dv + slice * kDVS + qq * 16 : nullptr;
+            // initial state: 16-byte loads when the start state is 16-byte aligned
+            // (the scanned segment states always are; a caller's S0 may be 4-byte aligned)
+            float S[SC];
+            const float *src = S_init ? S_init + (size_t)srow * args.dv + slice * DVS + qq * SC : nullptr;
+            if (src && (reinterpret_cast<uintptr_t>(S_init) & 15) == 0) {
 #pragma unroll
-            for (int j = 0; j < 16; ++j) S[j] = src ? src[j] : 0.f;
-            tc_st_32x32b_x16(tS, S);
+                for (int j = 0; j < SC; j += 4) {
+                    const float4 v4 = *reinterpret_cast<const float4 *>(src + j);
+                    S[j] = v4.x; S[j + 1] = v4.y; S[j + 2] = v4.z; S[j + 3] = v4.w;
+                }
+            } else {
+#pragma unroll
+                for (int j = 0; j < SC; ++j) S[j] = src ? src[j] : 0.f;
+            }
+            st_state(S);
             if (qq == 0) tc_st_32x32b_x1(tz, z_init);
             tc_wait_st();
         }
 
-        for (int c = 0; c < nch + 2; ++c) {
+        for (int c = 0; c < nch + LAG; ++c) {
             const bool has_s = c <= nch;              // the state after chunk c-1
             const bool has_b = c < nch;               // Sprev and scores of chunk c
             const bool has_p = has_b && !a_zero;
-            const bool has_e = c >= 2;                // outputs of chunk c-2
+            const bool has_e = c >= LAG;              // outputs of chunk c - LAG
             const int bb = c & 1, pb = c % NP, pn = c / NP;
             if (has_s && c >= 1 && !warp_wait(cx, &sm->dS_full, (c - 1) & 1)) break;
             if (has_b && GATED && !warp_wait(cx, &sm->phi_done[c % NST], (c / NST) & 1)) break;
             if (has_p && !warp_wait(cx, &sm->P_full[pb], pn & 1)) break;
             tc_fence_after();
-            float S[16], zr = 0.f, p[8];
+            float S[SC], zr = 0.f, p[8];
             if (has_s) {
-                tc_ld_32x32b_x16(tS, S);
+                ld_state(S);
                 if (qq == 0) tc_ld_32x32b_x1(tz, zr);
             }
             if (has_p) tc_ld_16x32bx2_x8<8>(tmem + lane_base + L::kColP + pb * 64 + qq * 16, p);
             tc_wait_ld();
             // Sprev of chunk c (BF16) and z split into two BF16 parts
-            uint32_t spk[8];
+            uint32_t spk[SC / 2];
             float zhi = 0.f;
             if (has_b) {
 #pragma unroll
-                for (int j = 0; j < 8; ++j) spk[j] = pack_bf16x2(S[2 * j], S[2 * j + 1]);
+                for (int j = 0; j < SC / 2; ++j) spk[j] = pack_bf16x2(S[2 * j], S[2 * j + 1]);
                 zhi = __bfloat162float(__float2bfloat16_rn(zr));
             }
             if (GATED && has_b) {
                 // decay the state by the gate product of chunk c before its increment lands
                 const float g = gr->gG[c % kAux][kC - 1];
-                float Sd[16];
 #pragma unroll
-                for (int j = 0; j < 16; ++j) Sd[j] = g * S[j];
-                tc_st_32x32b_x16(tS, Sd);
+                for (int j = 0; j < SC; ++j) S[j] *= g;
+                st_state(S);
                 if (qq == 0) tc_st_32x32b_x1(tz, g * zr);
                 tc_wait_st();
             }
@@ -509,13 +564,19 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
                 // must be done
                 if (L::kSpBufs == 1 && c >= 1 && !warp_wait(cx, &sm->Sp_empty, (c - 1) & 1)) break;
                 if (c >= 2 && !warp_wait(cx, &sm->A_empty[bb], ((c >> 1) - 1) & 1)) break;
-                // Sprev columns 16 qq .. +15 of row srow: 16-column block qq
-                uint8_t *spz = base + L::kOffSpZ + sb * kTileSpZ + qq * (kR * 32);
-                *reinterpret_cast<uint4 *>(spz + sw32_offset(srow, 0)) = make_uint4(spk[0], spk[1], spk[2], spk[3]);
-                *reinterpret_cast<uint4 *>(spz + sw32_offset(srow, 8)) = make_uint4(spk[4], spk[5], spk[6], spk[7]);
-                // z as two BF16 parts in columns 64 (zhi) and 65 (zlo)
+                // Sprev columns SC qq .. +SC-1 of row srow: 16-column blocks SC/16 qq ..
+                uint8_t *spz = base + L::kOffSpZ + sb * L::kTileSpZ;
+#pragma unroll
+                for (int hb = 0; hb < SC / 16; ++hb) {
+                    uint8_t *blk = spz + (qq * (SC / 16) + hb) * kBlkSpZ;
+                    *reinterpret_cast<uint4 *>(blk + sw32_offset(srow, 0)) =
+                        make_uint4(spk[8 * hb], spk[8 * hb + 1], spk[8 * hb + 2], spk[8 * hb + 3]);
+                    *reinterpret_cast<uint4 *>(blk + sw32_offset(srow, 8)) =
+                        make_uint4(spk[8 * hb + 4], spk[8 * hb + 5], spk[8 * hb + 6], spk[8 * hb + 7]);
+                }
+                // z as two BF16 parts in columns DVS (zhi) and DVS + 1 (zlo)
                 if (qq == 0)
-                    *reinterpret_cast<uint32_t *>(base + L::kOffSpZ + sb * kTileSpZ + 4 * (kR * 32) + sw32_offset(srow, 0)) =
+                    *reinterpret_cast<uint32_t *>(spz + (DVS / 16) * kBlkSpZ + sw32_offset(srow, 0)) =
                         pack_bf16x2(zhi, zr - zhi);
                 if (!a_zero)
                     *reinterpret_cast<uint4 *>(base + L::kOffA + bb * kTileA + sw128_offset(prow, pcol >> 3)) =
@@ -525,37 +586,45 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
                 warp_arrive(&sm->ops_full[bb]);
             } else if (has_s && last_seg) {
                 // c == nch: the state after the last chunk
-                float *dst = args.S_out + ((size_t)bh * kR + srow) * args.dv + slice * kDVS + qq * 16;
+                float *dst = args.S_out + ((size_t)bh * kR + srow) * args.dv + slice * DVS + qq * SC;
 #pragma unroll
-                for (int j = 0; j < 16; j += 4)
+                for (int j = 0; j < SC; j += 4)
                     *reinterpret_cast<float4 *>(dst + j) = make_float4(S[j], S[j + 1], S[j + 2], S[j + 3]);
                 if (slice == 0 && qq == 0) args.z_out[(size_t)bh * kR + srow] = zr;
             }
 
-            // outputs of chunk c-2: columns 64 + 65 of [O | dn] hold Q~' . zprev in
-            // two parts plus the row sums of A
+            // outputs of chunk c - LAG: columns DVS and DVS + 1 of [O | dn] hold
+            // Q~' . zprev in two parts plus the row sums of A
             if (has_e) {
-                const int ob = (c - 2) % L::kNO;
-                if (!warp_wait(cx, &sm->O_full[ob], ((c - 2) / L::kNO) & 1)) break;
+                const int ce = c - LAG;
+                const int ob = ce % L::kNO;
+                if (!warp_wait(cx, &sm->O_full[ob], (ce / L::kNO) & 1)) break;
                 tc_fence_after();
-                float o[8], dn;
-                tc_ld_16x32bx2_x8<8>(tmem + lane_base + L::kColO + ob * 80 + qq * 16, o);
-                tc_ld_16x32bx2_x1<1>(tmem + lane_base + L::kColO + ob * 80 + 64, dn);
+                float o[SC / 2], dn;
+                if constexpr (SC == 16) tc_ld_16x32bx2_x8<8>(tmem + lane_base + L::kColO + ob * L::kW + qq * SC, o);
+                else tc_ld_16x32bx2_x16<16>(tmem + lane_base + L::kColO + ob * L::kW + qq * SC, o);
+                tc_ld_16x32bx2_x1<1>(tmem + lane_base + L::kColO + ob * L::kW + DVS, dn);
                 tc_wait_ld();
                 tc_fence_before();
                 warp_arrive(&sm->O_empty[ob]);
                 dn += __shfl_xor_sync(0xffffffffu, dn, 16);
                 float inv;   // approximate reciprocal: y is rounded to BF16 below
                 asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(inv) : "f"(dn + args.eps));
-                uint4 yp;
-                yp.x = pack_bf16x2(o[0] * inv, o[1] * inv);
-                yp.y = pack_bf16x2(o[2] * inv, o[3] * inv);
-                yp.z = pack_bf16x2(o[4] * inv, o[5] * inv);
-                yp.w = pack_bf16x2(o[6] * inv, o[7] * inv);
-                // 8 columns (16 bytes) of token row prow, straight to global memory
-                // (streaming stores: y is not read again here)
-                const int t = tb + (c - 2) * kC + prow;
-                if (t < T) __stcs(reinterpret_cast<uint4 *>(args.y + tok_row(t) * args.dv + slice * kDVS + pcol), yp);
+                // SC/2 columns (16 or 32 bytes) of token row prow, straight to global
+                // memory (streaming stores: y is not read again here)
+                const int t = tb + ce * kC + prow;
+                if (t < T) {
+                    uint4 *dst = reinterpret_cast<uint4 *>(args.y + tok_row(t) * args.dv + slice * DVS + ocol);
+#pragma unroll
+                    for (int v8 = 0; v8 < SC / 16; ++v8) {
+                        uint4 yp;
+                        yp.x = pack_bf16x2(o[8 * v8 + 0] * inv, o[8 * v8 + 1] * inv);
+                        yp.y = pack_bf16x2(o[8 * v8 + 2] * inv, o[8 * v8 + 3] * inv);
+                        yp.z = pack_bf16x2(o[8 * v8 + 4] * inv, o[8 * v8 + 5] * inv);
+                        yp.w = pack_bf16x2(o[8 * v8 + 6] * inv, o[8 * v8 + 7] * inv);
+                        __stcs(dst + v8, yp);
+                    }
+                }
             }
         }
     } else if (is_phi_warp(warp)) {
@@ -602,6 +671,11 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
                 }
             }
             fence_proxy_async_smem();
+            // With one score buffer, P of chunk c (issued once phi of chunk c is
+            // done) reuses the barrier phase parity of chunk c-1's P: wait for
+            // chunk c-1's P before announcing phi of chunk c, so that the wait in
+            // scale_qk never falls two phases behind.
+            if (GATED && NP == 1 && c >= 1 && !warp_wait(cx, &sm->P_full[0], (c - 1) & 1)) { ok = false; break; }
             warp_arrive(&sm->phi_done[s]);
             // P of chunk c-1 was issued once phi of chunk c-1 was done and has
             // normally completed while phi of chunk c ran
@@ -622,20 +696,26 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
 }  // namespace
 
 cudaError_t launch_prefill_tc(const CUtensorMap &map_q, const CUtensorMap &map_k, const CUtensorMap &map_v,
-                              const PrefillTcArgs &a, int B, bool gated, cudaStream_t stream)
+                              const PrefillTcArgs &a, int B, bool gated, int dvs, cudaStream_t stream)
 {
-    const dim3 grid(a.dv / kDVS, a.H, B * a.nseg);
-    const uint32_t bytes = gated ? smem_bytes<true>() : smem_bytes<false>();
-    auto kern = gated ? prefill_tc_kernel<true> : prefill_tc_kernel<false>;
+    if (dvs != 64 && dvs != 128) return cudaErrorInvalidValue;
+    const dim3 grid(a.dv / dvs, a.H, B * a.nseg);
+    using KernFn = void (*)(const CUtensorMap, const CUtensorMap, const CUtensorMap, const PrefillTcArgs);
+    const int v = (gated ? 1 : 0) + (dvs == 128 ? 2 : 0);
+    static const KernFn kerns[4] = {prefill_tc_kernel<false, 64>, prefill_tc_kernel<true, 64>,
+                                    prefill_tc_kernel<false, 128>, prefill_tc_kernel<true, 128>};
+    static const uint32_t bytes[4] = {smem_bytes<false, 64>(), smem_bytes<true, 64>(), smem_bytes<false, 128>(),
+                                      smem_bytes<true, 128>()};
     // The attribute is set once per device (not during stream capture of later calls).
-    static OncePerDevice attr_set[2];
-    const cudaError_t e = set_smem_once(kern, bytes, attr_set[gated]);
+    static OncePerDevice attr_set[4];
+    const cudaError_t e = set_smem_once(kerns[v], bytes[v], attr_set[v]);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = grid;
     cfg.blockDim = dim3(kThreads, 1, 1);
-    cfg.dynamicSmemBytes = bytes;
+    cfg.dynamicSmemBytes = bytes[v];
     cfg.stream = stream;
+    // the dv slices of a head (and segment) form a cluster
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = grid.x;
@@ -643,7 +723,7 @@ cudaError_t launch_prefill_tc(const CUtensorMap &map_q, const CUtensorMap &map_k
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kern, map_q, map_k, map_v, a);
+    return cudaLaunchKernelEx(&cfg, kerns[v], map_q, map_k, map_v, a);
 }
 
 }  // namespace la

@@ -18,46 +18,60 @@
 namespace la {
 namespace {
 
-constexpr int kDVS = 64;            // value columns per CTA
+// Value columns per CTA (DVS): 64 or 128, as the chunk kernel.  A CTA owns one
+// (b, h, DVS-column slice, part).
 constexpr int kThreads = 384;       // 12 warps
 constexpr int kWarpTma = 0, kWarpMma = 1, kWarpTm0 = 4, kTmWarps = 4;
 // phi warps: 2, 3 and 8..11 (spread over the four schedulers)
 __host__ __device__ constexpr bool is_phi_warp(int w) { return w == 2 || w == 3 || w >= 8; }
 __host__ __device__ constexpr int phi_index(int w) { return w < 4 ? w - 2 : w - 6; }
 constexpr int kPhiWarps = 6, kPhiThreads = kPhiWarps * 32;
-constexpr int kStages = 8;
 constexpr uint32_t kTileK = kC * kR * 2;       // 16 KB: two 64-feature blocks of 64 rows x 128 B
-constexpr uint32_t kTileV = kC * kDVS * 2;     // 8 KB
-constexpr uint32_t kTileOnes = kC * 128;       // 8 KB: the second 64-column block of [V | 1 0..]
-constexpr uint32_t kOffK = 0, kOffV = kTileK, kStageBytes = kTileK + kTileV;
-static_assert(kStageBytes % 1024 == 0, "stage tiles stay 1024-byte aligned");
-constexpr uint32_t kOffOnes = kStages * kStageBytes;
-constexpr uint32_t kOffGate = kOffOnes + kTileOnes;
-constexpr uint32_t kTmemCols = 128;            // [S | z]: 80 columns (z is column 64)
+constexpr uint32_t kBlkV = kC * 64 * 2;        // one 64-column block of V (8 KB)
+constexpr uint32_t kTileOnes = kC * 128;       // 8 KB: the block of ones after V in [V | 1 0..]
+constexpr int kMaxStages = 4;
+
+// Two CTAs are resident per SM (each at most 113 KB of shared memory), so that
+// the many short parts of a segment stream at the bandwidth of the SM.
+template <bool GATED, int DVS>
+struct SCfg {
+    static_assert(DVS == 64 || DVS == 128, "value columns per CTA");
+    static constexpr int kStages = DVS == 128 ? (GATED ? 2 : 3) : (GATED ? 3 : 4);
+    static constexpr uint32_t kTileV = (DVS / 64) * kBlkV;
+    static constexpr uint32_t kOffK = 0, kOffV = kTileK, kStageBytes = kTileK + kTileV;
+    static_assert(kStageBytes % 1024 == 0, "stage tiles stay 1024-byte aligned");
+    static constexpr uint32_t kOffOnes = kStages * kStageBytes;
+    static constexpr uint32_t kOffGate = kOffOnes + kTileOnes;
+    static constexpr uint32_t kOffSmall = kOffGate + (GATED ? sizeof(GateRing) : 0);
+    static constexpr uint32_t kTmemCols = DVS == 128 ? 256 : 128;   // [S | z]: DVS + 16 columns (z is column DVS)
+};
 
 struct alignas(16) SmallS {
-    uint64_t full[kStages], empty[kStages], phi_done[kStages];
+    uint64_t full[kMaxStages], empty[kMaxStages], phi_done[kMaxStages];
     uint64_t dS_full, S_read, mma_done, aux_empty[kAux];
     uint32_t tmem_base;
     int abort_flag;
 };
 
-template <bool GATED>
-__host__ __device__ constexpr uint32_t off_small() { return kOffGate + (GATED ? sizeof(GateRing) : 0); }
-template <bool GATED>
-__host__ __device__ constexpr uint32_t smem_bytes() { return off_small<GATED>() + sizeof(SmallS) + 1024; }
-static_assert(smem_bytes<true>() <= 232448, "shared memory budget");
+template <bool GATED, int DVS>
+__host__ __device__ constexpr uint32_t smem_bytes() { return SCfg<GATED, DVS>::kOffSmall + sizeof(SmallS) + 1024; }
+// two resident CTAs per SM: 2 x (bytes + 1 KB reserved) within the SM's 228 KB
+static_assert(2 * (smem_bytes<true, 64>() + 1024) <= 233472, "shared memory budget");
+static_assert(2 * (smem_bytes<false, 64>() + 1024) <= 233472, "shared memory budget");
+static_assert(2 * (smem_bytes<true, 128>() + 1024) <= 233472, "shared memory budget");
+static_assert(2 * (smem_bytes<false, 128>() + 1024) <= 233472, "shared memory budget");
 
-template <bool GATED>
-__global__ void __launch_bounds__(kThreads, 1)
+template <bool GATED, int DVS>
+__global__ void __launch_bounds__(kThreads, 2)
 state_tc_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant__ CUtensorMap map_v,
                 const StateTcArgs args)
 {
-    constexpr int NST = kStages;
+    using L = SCfg<GATED, DVS>;
+    constexpr int NST = L::kStages;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *base = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    SmallS *sm = reinterpret_cast<SmallS *>(base + off_small<GATED>());
-    GateRing *gr = reinterpret_cast<GateRing *>(base + kOffGate);   // gated only
+    SmallS *sm = reinterpret_cast<SmallS *>(base + L::kOffSmall);
+    GateRing *gr = reinterpret_cast<GateRing *>(base + L::kOffGate);   // gated only
     Ctx cx{&sm->abort_flag, args.wait_limit_ns, args.status};
 
     // grid: (dv slice, h, b * nsub + m); sub-segment m is part j of output segment g
@@ -71,7 +85,7 @@ state_tc_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant
     const int nch = max(0, min(cs + args.sub_chunks, (g + 1) * args.seg_chunks) - cs);
     const int tb = cs * kC;                                                   // first token
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    auto stage_ptr = [&](int s) { return base + s * kStageBytes; };
+    auto stage_ptr = [&](int s) { return base + s * L::kStageBytes; };
 
     // ------------------------------------------------------------ set-up
     if (threadIdx.x == 0) {
@@ -90,13 +104,13 @@ state_tc_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant
         tma_prefetch_desc(&map_v);
     }
     for (int i = threadIdx.x; i < (int)kTileOnes / 16; i += kThreads)
-        reinterpret_cast<uint4 *>(base + kOffOnes)[i] = make_uint4(0, 0, 0, 0);
+        reinterpret_cast<uint4 *>(base + L::kOffOnes)[i] = make_uint4(0, 0, 0, 0);
     __syncthreads();
     if (threadIdx.x < kC)   // element (column 0, token row k): 16-byte chunk 0 of row k after the swizzle
-        *reinterpret_cast<uint16_t *>(base + kOffOnes + sw128_offset(threadIdx.x, 0)) = 0x3F80u;
+        *reinterpret_cast<uint16_t *>(base + L::kOffOnes + sw128_offset(threadIdx.x, 0)) = 0x3F80u;
     fence_proxy_async_smem();
     if (warp == kWarpMma) {
-        tmem_alloc(&sm->tmem_base, kTmemCols);
+        tmem_alloc(&sm->tmem_base, L::kTmemCols);
         tmem_relinquish();
     }
     tc_fence_before();
@@ -109,9 +123,9 @@ state_tc_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant
         float zero[32];
 #pragma unroll
         for (int i = 0; i < 32; ++i) zero[i] = 0.f;
-        tc_st_32x32b_x32(lb, zero);
-        tc_st_32x32b_x32(lb + 32, zero);
-        tc_st_32x32b_x1(lb + 64, 0.f);
+#pragma unroll
+        for (int pc = 0; pc < DVS / 32; ++pc) tc_st_32x32b_x32(lb + 32 * pc, zero);
+        tc_st_32x32b_x1(lb + DVS, 0.f);
         tc_wait_st();
     }
     tc_fence_before();
@@ -135,17 +149,20 @@ state_tc_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant
             if (__shfl_sync(0xffffffffu, aborted(cx) ? 1 : 0, 0)) break;
             uint8_t *st = stage_ptr(s);
             if (lane == 0) {
-                mbar_arrive_expect_tx(&sm->full[s], kTileK + kTileV);
-                tma_load_3d(st + kOffK, &map_k, &sm->full[s], 0, t0, bh);
-                tma_load_3d(st + kOffK + kTileK / 2, &map_k, &sm->full[s], 64, t0, bh);
-                tma_load_3d(st + kOffV, &map_v, &sm->full[s], slice * kDVS, t0, bh);
+                mbar_arrive_expect_tx(&sm->full[s], kTileK + L::kTileV);
+                tma_load_3d(st + L::kOffK, &map_k, &sm->full[s], 0, t0, bh);
+                tma_load_3d(st + L::kOffK + kTileK / 2, &map_k, &sm->full[s], 64, t0, bh);
+#pragma unroll
+                for (int vb = 0; vb < DVS / 64; ++vb)
+                    tma_load_3d(st + L::kOffV + vb * kBlkV, &map_v, &sm->full[s], slice * DVS + vb * 64, t0, bh);
                 if (c + NST < nch) {   // warm L2 for the load that reuses this stage
                     const int tp = t0 + NST * kC;
                     if (slice == 0) {
                         tma_prefetch_l2_3d(&map_k, 0, tp, bh);
                         tma_prefetch_l2_3d(&map_k, 64, tp, bh);
                     }
-                    tma_prefetch_l2_3d(&map_v, slice * kDVS, tp, bh);
+#pragma unroll
+                    for (int vb = 0; vb < DVS / 64; ++vb) tma_prefetch_l2_3d(&map_v, slice * DVS + vb * 64, tp, bh);
                 }
             }
             if (GATED) {
@@ -164,22 +181,31 @@ state_tc_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant
         // ------------------------------------------------------------ MMA
         // [S | z] += K~'^T [V | 1] per chunk (K~' = diag(w) K~ with a gate), once
         // phi of the chunk is done and, with a gate, the TMEM warps have decayed
-        // the state by the chunk's gate product.
+        // the state by the chunk's gate product.  With 64 value columns one MMA
+        // spans the V block and the first 16 columns of the ones block (at LBO);
+        // with 128 the two V blocks and the ones block are two MMAs.
         if (lane == 0) {
-            constexpr uint32_t idDS = idesc_bf16_f32(128, 80, true, true);
+            constexpr int NV = DVS == 64 ? 80 : DVS;
+            constexpr uint32_t idDS = idesc_bf16_f32(128, NV, true, true);
+            constexpr uint32_t idDS1 = idesc_bf16_f32(128, 16, true, true);
             constexpr uint32_t kHi128 = desc_hi(1024, 2);
-            const uint32_t aOnes = smem_u32(base + kOffOnes);
+            const uint32_t aOnes = smem_u32(base + L::kOffOnes);
+            const uint32_t onesLo = desc_lo(aOnes, kBlkV);
             for (int c = 0; c < nch && !aborted(cx); ++c) {
                 const int s = c % NST;
                 const uint32_t st = smem_u32(stage_ptr(s));
                 if (!wait(cx, &sm->phi_done[s], (c / NST) & 1)) break;
                 if (GATED && !wait(cx, &sm->S_read, c & 1)) break;
                 tc_fence_after();
-                const uint32_t klo = desc_lo(st + kOffK, kTileK / 2);   // K~^T: MN-major, two 64-feature blocks
-                const uint32_t blo = desc_lo(st + kOffV, aOnes - (st + kOffV));   // [V | 1]
+                const uint32_t klo = desc_lo(st + L::kOffK, kTileK / 2);   // K~^T: MN-major, two 64-feature blocks
+                const uint32_t blo = desc_lo(st + L::kOffV, DVS == 64 ? aOnes - (st + L::kOffV) : kBlkV);
 #pragma unroll
-                for (int kk = 0; kk < 4; ++kk)
+                for (int kk = 0; kk < 4; ++kk) {
                     tc_mma_bf16_w<true>(tmem, klo + kk * (2048 >> 4), kHi128, blo + kk * (2048 >> 4), kHi128, idDS);
+                    if (DVS == 128)
+                        tc_mma_bf16_w<true>(tmem + DVS, klo + kk * (2048 >> 4), kHi128, onesLo + kk * (2048 >> 4),
+                                            kHi128, idDS1);
+                }
                 tc_commit(&sm->dS_full);
                 tc_commit(&sm->empty[s]);
             }
@@ -189,7 +215,8 @@ state_tc_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant
         __syncwarp();
     } else if (warp >= kWarpTm0 && warp < kWarpTm0 + kTmWarps) {
         // ----------------------------------------------------- TMEM warps
-        // Warp w holds feature rows 32 (w % 4) .. +31, all 64 columns and z.
+        // Warp w holds feature rows 32 (w % 4) .. +31, all DVS columns and z,
+        // 32 columns at a time (two resident CTAs per SM leave 85 registers a thread).
         const int qd = warp & 3;
         const uint32_t lane_base = static_cast<uint32_t>(qd * 32) << 16;
         const int srow = qd * 32 + lane;
@@ -202,16 +229,17 @@ state_tc_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant
                 tc_fence_after();
                 const float gl = gr->gG[c % kAux][kC - 1];
                 decay *= gl;
-                float s0[32], s1[32], zz;
-                tc_ld_32x32b_x32(tmem + lane_base, s0);
-                tc_ld_32x32b_x32(tmem + lane_base + 32, s1);
-                tc_ld_32x32b_x1(tmem + lane_base + 64, zz);
-                tc_wait_ld();
+                float sh[32], zz;
+                tc_ld_32x32b_x1(tmem + lane_base + DVS, zz);
+#pragma unroll 1
+                for (int pc = 0; pc < DVS / 32; ++pc) {
+                    tc_ld_32x32b_x32(tmem + lane_base + 32 * pc, sh);
+                    tc_wait_ld();
 #pragma unroll
-                for (int i = 0; i < 32; ++i) { s0[i] *= gl; s1[i] *= gl; }
-                tc_st_32x32b_x32(tmem + lane_base, s0);
-                tc_st_32x32b_x32(tmem + lane_base + 32, s1);
-                tc_st_32x32b_x1(tmem + lane_base + 64, zz * gl);
+                    for (int i = 0; i < 32; ++i) sh[i] *= gl;
+                    tc_st_32x32b_x32(tmem + lane_base + 32 * pc, sh);
+                }
+                tc_st_32x32b_x1(tmem + lane_base + DVS, zz * gl);
                 tc_wait_st();
                 tc_fence_before();
                 warp_arrive(&sm->S_read);
@@ -226,18 +254,18 @@ state_tc_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant
             __syncwarp();
             if (ok) {
                 tc_fence_after();
-                float s0[32], s1[32], zz;
-                tc_ld_32x32b_x32(tmem + lane_base, s0);
-                tc_ld_32x32b_x32(tmem + lane_base + 32, s1);
-                tc_ld_32x32b_x1(tmem + lane_base + 64, zz);
-                tc_wait_ld();
                 const size_t state_len = (size_t)kR * args.dv + kR;
                 float *out = args.dS + ((size_t)m * BH + bh) * state_len;
-                float *dst = out + (size_t)srow * args.dv + slice * kDVS;
+                float *dst = out + (size_t)srow * args.dv + slice * DVS;
+                float sh[32], zz;
+                tc_ld_32x32b_x1(tmem + lane_base + DVS, zz);
+#pragma unroll 1
+                for (int pc = 0; pc < DVS / 32; ++pc) {
+                    tc_ld_32x32b_x32(tmem + lane_base + 32 * pc, sh);
+                    tc_wait_ld();
 #pragma unroll
-                for (int i = 0; i < 32; i += 4) {
-                    *reinterpret_cast<float4 *>(dst + i) = make_float4(s0[i], s0[i + 1], s0[i + 2], s0[i + 3]);
-                    *reinterpret_cast<float4 *>(dst + 32 + i) = make_float4(s1[i], s1[i + 1], s1[i + 2], s1[i + 3]);
+                    for (int i = 0; i < 32; i += 4)
+                        *reinterpret_cast<float4 *>(dst + 32 * pc + i) = make_float4(sh[i], sh[i + 1], sh[i + 2], sh[i + 3]);
                 }
                 if (slice == 0) {
                     out[(size_t)kR * args.dv + srow] = zz;
@@ -256,7 +284,7 @@ state_tc_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant
             const int s = c % NST;
             if (!warp_wait(cx, &sm->full[s], (c / NST) & 1)) break;
             const int nvalid = min(kC, T - tb - c * kC);
-            uint4 *kt = reinterpret_cast<uint4 *>(stage_ptr(s) + kOffK);
+            uint4 *kt = reinterpret_cast<uint4 *>(stage_ptr(s) + L::kOffK);
             for (int ci = pp; ci < (int)kTileK / 16; ci += kPhiThreads) {
                 const int row = (ci & 511) >> 3;   // 8 chunks per 128-byte row, 64 rows per block
                 uint4 v = row < nvalid ? phi8(kt[ci]) : make_uint4(0, 0, 0, 0);
@@ -273,29 +301,49 @@ state_tc_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant
     __syncthreads();
     if (warp == kWarpMma) {
         tc_fence_after();
-        tmem_dealloc(tmem, kTmemCols);
+        tmem_dealloc(tmem, L::kTmemCols);
     }
 }
 
 // S_start[g] for every output segment g: the state before its first chunk.
-// One thread per element of a head's state (S then z).
+// One thread per 4 consecutive elements of a head's state (S then z); a thread
+// issues the loads of up to 8 parts before it runs their affine maps in order.
 __global__ void seg_scan_kernel(const float *S0, const float *z0, const float *A, const float *dS, float *S_start,
                                 int BH, int dv, int nsub, int sub_per_seg, int nseg)
 {
     const int bh = blockIdx.y;
-    const int e = blockIdx.x * blockDim.x + threadIdx.x;
+    const int e = 4 * (blockIdx.x * blockDim.x + threadIdx.x);
     const int s_len = kR * dv;
     const int state_len = s_len + kR;
     if (e >= state_len) return;
-    float s;
-    if (e < s_len) s = S0 ? S0[(size_t)bh * s_len + e] : 0.f;
-    else s = z0 ? z0[(size_t)bh * kR + (e - s_len)] : 0.f;
-    S_start[(size_t)bh * state_len + e] = s;
-    for (int m = 0; m < nsub; ++m) {
-        s = fmaf(A[(size_t)m * BH + bh], s, dS[((size_t)m * BH + bh) * state_len + e]);
-        if ((m + 1) % sub_per_seg == 0) {
-            const int g = (m + 1) / sub_per_seg;
-            if (g < nseg) S_start[((size_t)g * BH + bh) * state_len + e] = s;
+    // S0 and z0 are 4-byte aligned; the workspace parts are 16-byte aligned
+    float4 s;
+    const float *src0 = e < s_len ? (S0 ? S0 + (size_t)bh * s_len + e : nullptr)
+                                  : (z0 ? z0 + (size_t)bh * kR + (e - s_len) : nullptr);
+    s = src0 ? make_float4(src0[0], src0[1], src0[2], src0[3]) : make_float4(0.f, 0.f, 0.f, 0.f);
+    *reinterpret_cast<float4 *>(S_start + (size_t)bh * state_len + e) = s;
+    for (int m0 = 0; m0 < nsub; m0 += 8) {
+        float4 d[8];
+        float a[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int m = m0 + i;
+            d[i] = m < nsub ? *reinterpret_cast<const float4 *>(dS + ((size_t)m * BH + bh) * state_len + e)
+                            : make_float4(0.f, 0.f, 0.f, 0.f);
+            a[i] = m < nsub ? A[(size_t)m * BH + bh] : 1.f;
+        }
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int m = m0 + i;
+            if (m >= nsub) break;
+            s.x = fmaf(a[i], s.x, d[i].x);
+            s.y = fmaf(a[i], s.y, d[i].y);
+            s.z = fmaf(a[i], s.z, d[i].z);
+            s.w = fmaf(a[i], s.w, d[i].w);
+            if ((m + 1) % sub_per_seg == 0) {
+                const int g = (m + 1) / sub_per_seg;
+                if (g < nseg) *reinterpret_cast<float4 *>(S_start + ((size_t)g * BH + bh) * state_len + e) = s;
+            }
         }
     }
 }
@@ -303,15 +351,20 @@ __global__ void seg_scan_kernel(const float *S0, const float *z0, const float *A
 }  // namespace
 
 cudaError_t launch_state_tc(const CUtensorMap &map_k, const CUtensorMap &map_v, const StateTcArgs &a, int B,
-                            bool gated, cudaStream_t stream)
+                            bool gated, int dvs, cudaStream_t stream)
 {
-    const dim3 grid(a.dv / kDVS, a.H, B * a.nsub);
-    const uint32_t bytes = gated ? smem_bytes<true>() : smem_bytes<false>();
-    auto kern = gated ? state_tc_kernel<true> : state_tc_kernel<false>;
-    static OncePerDevice attr_set[2];
-    const cudaError_t e = set_smem_once(kern, bytes, attr_set[gated]);
+    if (dvs != 64 && dvs != 128) return cudaErrorInvalidValue;
+    const dim3 grid(a.dv / dvs, a.H, B * a.nsub);
+    using KernFn = void (*)(const CUtensorMap, const CUtensorMap, const StateTcArgs);
+    const int v = (gated ? 1 : 0) + (dvs == 128 ? 2 : 0);
+    static const KernFn kerns[4] = {state_tc_kernel<false, 64>, state_tc_kernel<true, 64>,
+                                    state_tc_kernel<false, 128>, state_tc_kernel<true, 128>};
+    static const uint32_t bytes[4] = {smem_bytes<false, 64>(), smem_bytes<true, 64>(), smem_bytes<false, 128>(),
+                                      smem_bytes<true, 128>()};
+    static OncePerDevice attr_set[4];
+    const cudaError_t e = set_smem_once(kerns[v], bytes[v], attr_set[v]);
     if (e != cudaSuccess) return e;
-    kern<<<grid, kThreads, bytes, stream>>>(map_k, map_v, a);
+    kerns[v]<<<grid, kThreads, bytes[v], stream>>>(map_k, map_v, a);
     return cudaGetLastError();
 }
 
@@ -319,7 +372,7 @@ cudaError_t launch_seg_scan(const float *S0, const float *z0, const float *A, co
                             int BH, int dv, int nsub, int sub_per_seg, int nseg, cudaStream_t stream)
 {
     const int state_len = kR * dv + kR;
-    const dim3 grid((state_len + 255) / 256, BH);
+    const dim3 grid((state_len / 4 + 255) / 256, BH);
     seg_scan_kernel<<<grid, 256, 0, stream>>>(S0, z0, A, dS, S_start, BH, dv, nsub, sub_per_seg, nseg);
     return cudaGetLastError();
 }
