@@ -458,38 +458,44 @@ def run_ours(args, rank, world, local_rank):
     achieved = pre_bytes / pre_launch / 1e9
     src = kernel_sources("prefill_tc.cu")
     roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-                "traffic": profile_traffic("prefill_tc_kernel<false>", "B4 H16 T4096", src),
-                "kernel": "prefill_tc_kernel<false> (ungated)" + (
+                "traffic": profile_traffic("prefill_tc_kernel<false, 64>", "B4 H16 T4096", src),
+                "kernel": "prefill_tc_kernel<false, 64> (ungated, two 64-column CTAs per head)" + (
                     " timed with its state pass and scan (the sequences are split into a short first "
                     "segment and a long rest)" if ws_bytes else ""),
                 "launches_per_prefill": prefill_launches, "algorithmic_bytes_per_launch": pre_bytes,
                 "launch_us": pre_launch * 1e6, "peak_kind": peak_kind,
                 "prefill_tokens_per_s": B * T * world / pre_launch}
 
-    # decode on its own workload: B=256, H=16, state 256 MiB (> L2), in place
-    dw = W.DECODE
-    dinp = W.decode_inputs(dw, seed=dw.seed + 1000 * rank)
-    dd = {k: (v.to(dev) if v is not None else None) for k, v in dinp.items()}
-    ydec = torch.empty((dw.B, dw.H, 1, dw.dv), device=dev, dtype=torch.bfloat16)
+    only = set(args.only.split(",")) if args.only else None
+    want = lambda name: only is None or name in only
+    decode = delta = backward = e2e = None
+    alu_peak = fp32_alu_peak_tflops(torch.cuda.get_device_properties(dev).multi_processor_count)
 
-    def k_dec_big():
-        _native.check(L.la_decode_step(P(dd["q"]), P(dd["k"]), P(dd["v"]), _native.LA_DTYPE_BF16, None, P(dd["S"]),
-                                       P(dd["z"]), dw.B, dw.H, dw.r, dw.dv, dw.eps, P(ydec), sh), "decode")
+    if want("decode"):
+        # decode on its own workload: B=256, H=16, state 256 MiB (> L2), in place
+        dw = W.DECODE
+        dinp = W.decode_inputs(dw, seed=dw.seed + 1000 * rank)
+        dd = {k: (v.to(dev) if v is not None else None) for k, v in dinp.items()}
+        ydec = torch.empty((dw.B, dw.H, 1, dw.dv), device=dev, dtype=torch.bfloat16)
 
-    with torch.cuda.stream(stream):
-        k_dec_big()
-    gd = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(gd, stream=stream):
-        k_dec_big()
-    dec_s = timed([gd] * N_ROT, args.steps, args.warmup)
-    dec_s, = reduce_max([dec_s], dev, dist)
-    dbytes = decode_bytes(dw.B, dw.H, dw.r, dw.dv)
-    dec_launch = dec_s / args.steps
-    dec_gbs = dbytes / dec_launch / 1e9
-    decode = {"workload": dw.name, "gb_per_s": dec_gbs * world, "per_gpu_gb_per_s": dec_gbs,
-              "frac_of_hbm_peak": dec_gbs / peak, "launch_us": dec_launch * 1e6,
-              "algorithmic_bytes_per_launch": dbytes, "tokens_per_s": dw.B * world / dec_launch,
-              "traffic": profile_traffic("decode128_kernel<true>", "B256 H16", kernel_sources("decode.cu"))}
+        def k_dec_big():
+            _native.check(L.la_decode_step(P(dd["q"]), P(dd["k"]), P(dd["v"]), _native.LA_DTYPE_BF16, None, P(dd["S"]),
+                                           P(dd["z"]), dw.B, dw.H, dw.r, dw.dv, dw.eps, P(ydec), sh), "decode")
+
+        with torch.cuda.stream(stream):
+            k_dec_big()
+        gd = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gd, stream=stream):
+            k_dec_big()
+        dec_s = timed([gd] * N_ROT, args.steps, args.warmup)
+        dec_s, = reduce_max([dec_s], dev, dist)
+        dbytes = decode_bytes(dw.B, dw.H, dw.r, dw.dv)
+        dec_launch = dec_s / args.steps
+        dec_gbs = dbytes / dec_launch / 1e9
+        decode = {"workload": dw.name, "gb_per_s": dec_gbs * world, "per_gpu_gb_per_s": dec_gbs,
+                  "frac_of_hbm_peak": dec_gbs / peak, "launch_us": dec_launch * 1e6,
+                  "algorithmic_bytes_per_launch": dbytes, "tokens_per_s": dw.B * world / dec_launch,
+                  "traffic": profile_traffic("decode128_kernel<true>", "B256 H16", kernel_sources("decode.cu"))}
 
     # the gated (B2 H16 T16384, alpha = sigmoid(N(3,1))) and long (B1 H32 T65536,
     # sigma = 2) prefill workloads, each on its own inputs from a zero state: the
@@ -543,162 +549,164 @@ def run_ours(args, rank, world, local_rank):
                              "traffic": profile_traffic(kernel, f"B{pw.B} H{pw.H} T{pw.T}",
                                                         kernel_sources("prefill_tc.cu"))}}
 
-    gated_prefill = prefill_workload(W.GATED, 2, "prefill_tc_kernel<true>")
-    long_prefill = prefill_workload(W.LONG, 1, "prefill_tc_kernel<false>")
+    gated_prefill = prefill_workload(W.GATED, 2, "prefill_tc_kernel<true, 128>") if want("gated") else None
+    long_prefill = prefill_workload(W.LONG, 1, "prefill_tc_kernel<false, 128>") if want("long") else None
 
-    # delta-rule memory on its own workload (B=4, H=16, T=4096, r = dv = 128, BF16;
-    # q, k, v 201 MB > L2): the chunked tensor-core entry point (its two launches,
-    # T of every chunk and then the state chain) and the FP32 token recurrence,
-    # each replayed as a CUDA graph
-    xw = W.DELTA
-    xin = {k: (v.to(dev) if v is not None else None) for k, v in W.delta_inputs(xw, seed=xw.seed + 1000 * rank).items()}
-    ydel = torch.empty((xw.B, xw.H, xw.T, xw.dv), device=dev, dtype=torch.bfloat16)
-    Sdel = torch.empty((xw.B, xw.H, xw.r, xw.dv), device=dev, dtype=torch.float32)
-    xws_bytes = _native.lib().la_delta_chunked_workspace_bytes(xw.B, xw.H, xw.T)
-    xws = torch.empty(xws_bytes, device=dev, dtype=torch.uint8)
+    if want("delta"):
+        # delta-rule memory on its own workload (B=4, H=16, T=4096, r = dv = 128, BF16;
+        # q, k, v 201 MB > L2): the chunked tensor-core entry point (its two launches,
+        # T of every chunk and then the state chain) and the FP32 token recurrence,
+        # each replayed as a CUDA graph
+        xw = W.DELTA
+        xin = {k: (v.to(dev) if v is not None else None) for k, v in W.delta_inputs(xw, seed=xw.seed + 1000 * rank).items()}
+        ydel = torch.empty((xw.B, xw.H, xw.T, xw.dv), device=dev, dtype=torch.bfloat16)
+        Sdel = torch.empty((xw.B, xw.H, xw.r, xw.dv), device=dev, dtype=torch.float32)
+        xws_bytes = _native.lib().la_delta_chunked_workspace_bytes(xw.B, xw.H, xw.T)
+        xws = torch.empty(xws_bytes, device=dev, dtype=torch.uint8)
 
-    def k_delta_tc():
-        _native.check(L.la_delta_rule_chunked(P(xin["q"]), P(xin["k"]), P(xin["v"]), _native.LA_DTYPE_BF16,
-                                              P(xin["beta"]), None, xw.B, xw.H, xw.T, xw.r, xw.dv, P(ydel), P(Sdel),
-                                              P(xws), xws_bytes, sh), "la_delta_rule_chunked")
+        def k_delta_tc():
+            _native.check(L.la_delta_rule_chunked(P(xin["q"]), P(xin["k"]), P(xin["v"]), _native.LA_DTYPE_BF16,
+                                                  P(xin["beta"]), None, xw.B, xw.H, xw.T, xw.r, xw.dv, P(ydel), P(Sdel),
+                                                  P(xws), xws_bytes, sh), "la_delta_rule_chunked")
 
-    def k_delta():
-        _native.check(L.la_delta_rule(P(xin["q"]), P(xin["k"]), P(xin["v"]), _native.LA_DTYPE_BF16, P(xin["beta"]),
-                                      None, xw.B, xw.H, xw.T, xw.r, xw.dv, P(ydel), P(Sdel), sh), "la_delta_rule")
+        def k_delta():
+            _native.check(L.la_delta_rule(P(xin["q"]), P(xin["k"]), P(xin["v"]), _native.LA_DTYPE_BF16, P(xin["beta"]),
+                                          None, xw.B, xw.H, xw.T, xw.r, xw.dv, P(ydel), P(Sdel), sh), "la_delta_rule")
 
-    x_times = []
-    for fn in (k_delta_tc, k_delta):
+        x_times = []
+        for fn in (k_delta_tc, k_delta):
+            with torch.cuda.stream(stream):
+                fn()
+            gx = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(gx, stream=stream):
+                fn()
+            x_times.append(timed([gx] * N_ROT, args.steps, args.warmup))
+        xc_s, x_s = reduce_max(x_times, dev, dist)
+        assert _native.lib().la_last_device_status(sh) == 0
+        xc_launch, x_launch = xc_s / args.steps, x_s / args.steps
+        xbytes = delta_bytes(xw.B, xw.H, xw.T, xw.r, xw.dv)
+        xc_gbs = xbytes / xc_launch / 1e9
+        x_tflops = delta_flops(xw.B, xw.H, xw.T, xw.r, xw.dv) / x_launch / 1e12
+        delta = {"workload": xw.name, "entry": "la_delta_rule_chunked", "launch_us": xc_launch * 1e6,
+                 "tokens_per_s": xw.B * xw.T * world / xc_launch,
+                 "roofline": {"bound": "hbm", "achieved": xc_gbs, "peak": peak, "unit": "GB/s",
+                              "frac": xc_gbs / peak, "peak_kind": peak_kind,
+                              "timed": "the whole call (both launches)",
+                              "traffic": profile_traffic("delta_tc_kernel", "B4 H16 T4096",
+                                                         kernel_sources("delta_tc.cu")),
+                              "algorithmic_bytes_per_launch": xbytes},
+                 "token_recurrence": {
+                     "entry": "la_delta_rule", "launch_us": x_launch * 1e6,
+                     "tokens_per_s": xw.B * xw.T * world / x_launch,
+                     "roofline": {"bound": "alu", "achieved": x_tflops, "peak": alu_peak, "unit": "TFLOP/s",
+                                  "frac": x_tflops / alu_peak, "peak_kind": "nominal FP32 FMA (SMs x 128 x 2 x max clock)",
+                                  "traffic": profile_traffic("delta_kernel<bf16,128>", "B4 H16 T4096",
+                                                             kernel_sources("delta.cu")),
+                                  "algorithmic_flops_per_launch": delta_flops(xw.B, xw.H, xw.T, xw.r, xw.dv)}}}
+
+    if want("backward"):
+        # backward pass on the gated shape of the prefill (B=4, H=16, T=4096, BF16,
+        # alpha = sigmoid(N(3,1))): its five launches replayed as one CUDA graph
+        bw = W.UNGATED.with_(gated=True)
+        bin_ = {k: (v.to(dev) if v is not None else None)
+                for k, v in W.prefill_inputs(bw, seed=bw.seed + 11 + 1000 * rank).items()}
+        ybw = torch.empty((bw.B, bw.H, bw.T, bw.dv), device=dev, dtype=torch.bfloat16)
+        Sbw = torch.empty((bw.B, bw.H, bw.r, bw.dv), device=dev, dtype=torch.float32)
+        zbw = torch.empty((bw.B, bw.H, bw.r), device=dev, dtype=torch.float32)
+        dybw = torch.randn((bw.B, bw.H, bw.T, bw.dv), generator=torch.Generator().manual_seed(bw.seed + 12)).to(dev,
+                                                                                                                  torch.bfloat16)
+        gq, gk, gv = (torch.empty_like(bin_[n]) for n in ("q", "k", "v"))
+        ga = torch.empty((bw.B, bw.H, bw.T), device=dev, dtype=torch.float32)
+        gS0 = torch.empty((bw.B, bw.H, bw.r, bw.dv), device=dev, dtype=torch.float32)
+        gz0 = torch.empty((bw.B, bw.H, bw.r), device=dev, dtype=torch.float32)
+        wsb = torch.empty(int(L.la_backward_workspace_bytes(bw.B, bw.H, bw.T)), device=dev, dtype=torch.uint8)
+
+        def k_backward():
+            _native.check(L.la_prefill_backward(P(bin_["q"]), P(bin_["k"]), P(bin_["v"]), _native.LA_DTYPE_BF16,
+                                                P(bin_["alpha"]), None, None, bw.B, bw.H, bw.T, bw.r, bw.dv, bw.eps,
+                                                P(ybw), P(dybw), None, None, P(gq), P(gk), P(gv), P(ga), P(gS0), P(gz0),
+                                                P(wsb), wsb.numel(), sh), "la_prefill_backward")
+
         with torch.cuda.stream(stream):
-            fn()
-        gx = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(gx, stream=stream):
-            fn()
-        x_times.append(timed([gx] * N_ROT, args.steps, args.warmup))
-    xc_s, x_s = reduce_max(x_times, dev, dist)
-    assert _native.lib().la_last_device_status(sh) == 0
-    xc_launch, x_launch = xc_s / args.steps, x_s / args.steps
-    xbytes = delta_bytes(xw.B, xw.H, xw.T, xw.r, xw.dv)
-    xc_gbs = xbytes / xc_launch / 1e9
-    x_tflops = delta_flops(xw.B, xw.H, xw.T, xw.r, xw.dv) / x_launch / 1e12
-    alu_peak = fp32_alu_peak_tflops(torch.cuda.get_device_properties(dev).multi_processor_count)
-    delta = {"workload": xw.name, "entry": "la_delta_rule_chunked", "launch_us": xc_launch * 1e6,
-             "tokens_per_s": xw.B * xw.T * world / xc_launch,
-             "roofline": {"bound": "hbm", "achieved": xc_gbs, "peak": peak, "unit": "GB/s",
-                          "frac": xc_gbs / peak, "peak_kind": peak_kind,
-                          "timed": "the whole call (both launches)",
-                          "traffic": profile_traffic("delta_tc_kernel", "B4 H16 T4096",
-                                                     kernel_sources("delta_tc.cu")),
-                          "algorithmic_bytes_per_launch": xbytes},
-             "token_recurrence": {
-                 "entry": "la_delta_rule", "launch_us": x_launch * 1e6,
-                 "tokens_per_s": xw.B * xw.T * world / x_launch,
-                 "roofline": {"bound": "alu", "achieved": x_tflops, "peak": alu_peak, "unit": "TFLOP/s",
-                              "frac": x_tflops / alu_peak, "peak_kind": "nominal FP32 FMA (SMs x 128 x 2 x max clock)",
-                              "traffic": profile_traffic("delta_kernel<bf16,128>", "B4 H16 T4096",
-                                                         kernel_sources("delta.cu")),
-                              "algorithmic_flops_per_launch": delta_flops(xw.B, xw.H, xw.T, xw.r, xw.dv)}}}
+            _native.check(L.la_prefill_chunked(P(bin_["q"]), P(bin_["k"]), P(bin_["v"]), _native.LA_DTYPE_BF16,
+                                               P(bin_["alpha"]), None, None, bw.B, bw.H, bw.T, bw.r, bw.dv, bw.chunk,
+                                               bw.eps, P(ybw), P(Sbw), P(zbw), None, 0, sh), "la_prefill_chunked")
+            k_backward()
+        gb = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gb, stream=stream):
+            k_backward()
+        bsteps = max(1, min(args.steps, 20))
+        b_s = timed([gb] * N_ROT, bsteps, max(3, min(args.warmup, 3)))
+        b_s, = reduce_max([b_s], dev, dist)
+        assert _native.lib().la_last_device_status(sh) == 0
+        b_call = b_s / bsteps
+        b_tflops = backward_flops(bw.B, bw.H, bw.T, bw.r, bw.dv, True) / b_call / 1e12
+        backward = {"workload": bw.name.replace("prefill", "backward of the gated prefill,"), "call_us": b_call * 1e6,
+                    "launches_per_call": 5, "tokens_per_s": bw.B * bw.T * world / b_call, "steps": bsteps,
+                    "roofline": {"bound": "alu", "achieved": b_tflops, "peak": alu_peak, "unit": "TFLOP/s",
+                                 "frac": b_tflops / alu_peak, "peak_kind": "nominal FP32 FMA (SMs x 128 x 2 x max clock)",
+                                 "algorithmic_flops_per_call": backward_flops(bw.B, bw.H, bw.T, bw.r, bw.dv, True)}}
 
-    # backward pass on the gated shape of the prefill (B=4, H=16, T=4096, BF16,
-    # alpha = sigmoid(N(3,1))): its five launches replayed as one CUDA graph
-    bw = W.UNGATED.with_(gated=True)
-    bin_ = {k: (v.to(dev) if v is not None else None)
-            for k, v in W.prefill_inputs(bw, seed=bw.seed + 11 + 1000 * rank).items()}
-    ybw = torch.empty((bw.B, bw.H, bw.T, bw.dv), device=dev, dtype=torch.bfloat16)
-    Sbw = torch.empty((bw.B, bw.H, bw.r, bw.dv), device=dev, dtype=torch.float32)
-    zbw = torch.empty((bw.B, bw.H, bw.r), device=dev, dtype=torch.float32)
-    dybw = torch.randn((bw.B, bw.H, bw.T, bw.dv), generator=torch.Generator().manual_seed(bw.seed + 12)).to(dev,
-                                                                                                              torch.bfloat16)
-    gq, gk, gv = (torch.empty_like(bin_[n]) for n in ("q", "k", "v"))
-    ga = torch.empty((bw.B, bw.H, bw.T), device=dev, dtype=torch.float32)
-    gS0 = torch.empty((bw.B, bw.H, bw.r, bw.dv), device=dev, dtype=torch.float32)
-    gz0 = torch.empty((bw.B, bw.H, bw.r), device=dev, dtype=torch.float32)
-    wsb = torch.empty(int(L.la_backward_workspace_bytes(bw.B, bw.H, bw.T)), device=dev, dtype=torch.uint8)
+    if want("e2e"):
+        # end to end through the public API with host buffers (pinned), every step:
+        # H2D of q, k, v (+ the decode token), the three calls, D2H of y, S, z, y_decode.
+        # Steps are pipelined as a serving loop would run them: the copies in of step
+        # i+1 and the copies out of step i-1 run on their own streams while step i
+        # computes.  Two device buffer sets (and two pinned host output sets)
+        # alternate; events order every reuse of a buffer after its last reader.
+        hq, hk, hv = (base[n].pin_memory() for n in ("q", "k", "v"))
+        hqd, hkd, hvd = (dec[n].pin_memory() for n in ("q", "k", "v"))
+        hout = [dict(y=torch.empty((B, H, T, dv), dtype=torch.bfloat16).pin_memory(),
+                     S=torch.empty((B, H, r, dv), dtype=torch.float32).pin_memory(),
+                     z=torch.empty((B, H, r), dtype=torch.float32).pin_memory(),
+                     yd=torch.empty((B, H, 1, dv), dtype=torch.bfloat16).pin_memory()) for _ in range(2)]
+        h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hqd, hkd, hvd))
+        d2h = sum(t.numel() * t.element_size() for t in hout[0].values())
+        s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+        ev = {n: [torch.cuda.Event(), torch.cuda.Event()] for n in ("in", "comp", "out")}
 
-    def k_backward():
-        _native.check(L.la_prefill_backward(P(bin_["q"]), P(bin_["k"]), P(bin_["v"]), _native.LA_DTYPE_BF16,
-                                            P(bin_["alpha"]), None, None, bw.B, bw.H, bw.T, bw.r, bw.dv, bw.eps,
-                                            P(ybw), P(dybw), None, None, P(gq), P(gk), P(gv), P(ga), P(gS0), P(gz0),
-                                            P(wsb), wsb.numel(), sh), "la_prefill_backward")
+        def e2e_step(i):
+            b = i % 2
+            s, ho = sets[b], hout[b]
+            with torch.cuda.stream(s_in):          # inputs of step i, once step i-2 stopped reading them
+                if i >= 2:
+                    s_in.wait_event(ev["comp"][b])
+                s["q"].copy_(hq, non_blocking=True); s["k"].copy_(hk, non_blocking=True)
+                s["v"].copy_(hv, non_blocking=True); s["qd"].copy_(hqd, non_blocking=True)
+                s["kd"].copy_(hkd, non_blocking=True); s["vd"].copy_(hvd, non_blocking=True)
+                ev["in"][b].record(s_in)
+            with torch.cuda.stream(stream):        # the step, once its inputs are in and step i-2 was read back
+                stream.wait_event(ev["in"][b])
+                if i >= 2:
+                    stream.wait_event(ev["out"][b])
+                S, z = la.state_init(B, H, r, dv, S=s["S"], z=s["z"])
+                la.prefill_chunked(s["q"], s["k"], s["v"], S0=S, z0=z, S_out=S, z_out=z, y=s["y"], chunk=w.chunk,
+                                   eps=w.eps)
+                la.decode_step(s["qd"], s["kd"], s["vd"], S, z, eps=w.eps, y=s["yd"])
+                ev["comp"][b].record(stream)
+            with torch.cuda.stream(s_out):         # its results back to the host
+                s_out.wait_event(ev["comp"][b])
+                ho["y"].copy_(s["y"], non_blocking=True); ho["S"].copy_(s["S"], non_blocking=True)
+                ho["z"].copy_(s["z"], non_blocking=True); ho["yd"].copy_(s["yd"], non_blocking=True)
+                ev["out"][b].record(s_out)
 
-    with torch.cuda.stream(stream):
-        _native.check(L.la_prefill_chunked(P(bin_["q"]), P(bin_["k"]), P(bin_["v"]), _native.LA_DTYPE_BF16,
-                                           P(bin_["alpha"]), None, None, bw.B, bw.H, bw.T, bw.r, bw.dv, bw.chunk,
-                                           bw.eps, P(ybw), P(Sbw), P(zbw), None, 0, sh), "la_prefill_chunked")
-        k_backward()
-    gb = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(gb, stream=stream):
-        k_backward()
-    bsteps = max(1, min(args.steps, 20))
-    b_s = timed([gb] * N_ROT, bsteps, max(3, min(args.warmup, 3)))
-    b_s, = reduce_max([b_s], dev, dist)
-    assert _native.lib().la_last_device_status(sh) == 0
-    b_call = b_s / bsteps
-    b_tflops = backward_flops(bw.B, bw.H, bw.T, bw.r, bw.dv, True) / b_call / 1e12
-    backward = {"workload": bw.name.replace("prefill", "backward of the gated prefill,"), "call_us": b_call * 1e6,
-                "launches_per_call": 5, "tokens_per_s": bw.B * bw.T * world / b_call, "steps": bsteps,
-                "roofline": {"bound": "alu", "achieved": b_tflops, "peak": alu_peak, "unit": "TFLOP/s",
-                             "frac": b_tflops / alu_peak, "peak_kind": "nominal FP32 FMA (SMs x 128 x 2 x max clock)",
-                             "algorithmic_flops_per_call": backward_flops(bw.B, bw.H, bw.T, bw.r, bw.dv, True)}}
-
-    # end to end through the public API with host buffers (pinned), every step:
-    # H2D of q, k, v (+ the decode token), the three calls, D2H of y, S, z, y_decode.
-    # Steps are pipelined as a serving loop would run them: the copies in of step
-    # i+1 and the copies out of step i-1 run on their own streams while step i
-    # computes.  Two device buffer sets (and two pinned host output sets)
-    # alternate; events order every reuse of a buffer after its last reader.
-    hq, hk, hv = (base[n].pin_memory() for n in ("q", "k", "v"))
-    hqd, hkd, hvd = (dec[n].pin_memory() for n in ("q", "k", "v"))
-    hout = [dict(y=torch.empty((B, H, T, dv), dtype=torch.bfloat16).pin_memory(),
-                 S=torch.empty((B, H, r, dv), dtype=torch.float32).pin_memory(),
-                 z=torch.empty((B, H, r), dtype=torch.float32).pin_memory(),
-                 yd=torch.empty((B, H, 1, dv), dtype=torch.bfloat16).pin_memory()) for _ in range(2)]
-    h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hqd, hkd, hvd))
-    d2h = sum(t.numel() * t.element_size() for t in hout[0].values())
-    s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
-    ev = {n: [torch.cuda.Event(), torch.cuda.Event()] for n in ("in", "comp", "out")}
-
-    def e2e_step(i):
-        b = i % 2
-        s, ho = sets[b], hout[b]
-        with torch.cuda.stream(s_in):          # inputs of step i, once step i-2 stopped reading them
-            if i >= 2:
-                s_in.wait_event(ev["comp"][b])
-            s["q"].copy_(hq, non_blocking=True); s["k"].copy_(hk, non_blocking=True)
-            s["v"].copy_(hv, non_blocking=True); s["qd"].copy_(hqd, non_blocking=True)
-            s["kd"].copy_(hkd, non_blocking=True); s["vd"].copy_(hvd, non_blocking=True)
-            ev["in"][b].record(s_in)
-        with torch.cuda.stream(stream):        # the step, once its inputs are in and step i-2 was read back
-            stream.wait_event(ev["in"][b])
-            if i >= 2:
-                stream.wait_event(ev["out"][b])
-            S, z = la.state_init(B, H, r, dv, S=s["S"], z=s["z"])
-            la.prefill_chunked(s["q"], s["k"], s["v"], S0=S, z0=z, S_out=S, z_out=z, y=s["y"], chunk=w.chunk,
-                               eps=w.eps)
-            la.decode_step(s["qd"], s["kd"], s["vd"], S, z, eps=w.eps, y=s["yd"])
-            ev["comp"][b].record(stream)
-        with torch.cuda.stream(s_out):         # its results back to the host
-            s_out.wait_event(ev["comp"][b])
-            ho["y"].copy_(s["y"], non_blocking=True); ho["S"].copy_(s["S"], non_blocking=True)
-            ho["z"].copy_(s["z"], non_blocking=True); ho["yd"].copy_(s["yd"], non_blocking=True)
-            ev["out"][b].record(s_out)
-
-    e2e_steps = max(1, min(args.steps, 50))
-    n_warm = max(2, min(args.warmup, 5))
-    for i in range(n_warm):
-        e2e_step(i)
-    barrier()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(s_in)
-    for i in range(n_warm, n_warm + e2e_steps):
-        e2e_step(i)
-    e1.record(s_out)
-    barrier()
-    e2e_s = e0.elapsed_time(e1) / 1e3
-    e2e_s, = reduce_max([e2e_s], dev, dist)
-    assert _native.lib().la_last_device_status(sh) == 0
-    e2e = {"value": whole_job_rate(tokens_per_step, world, e2e_steps, e2e_s), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
-           "d2h_bytes_per_step": d2h, "steps": e2e_steps, "ms_per_step": e2e_s / e2e_steps * 1e3,
-           "pipelining": "copies in (step i+1), compute (step i) and copies out (step i-1) on three streams"}
+        e2e_steps = max(1, min(args.steps, 50))
+        n_warm = max(2, min(args.warmup, 5))
+        for i in range(n_warm):
+            e2e_step(i)
+        barrier()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(s_in)
+        for i in range(n_warm, n_warm + e2e_steps):
+            e2e_step(i)
+        e1.record(s_out)
+        barrier()
+        e2e_s = e0.elapsed_time(e1) / 1e3
+        e2e_s, = reduce_max([e2e_s], dev, dist)
+        assert _native.lib().la_last_device_status(sh) == 0
+        e2e = {"value": whole_job_rate(tokens_per_step, world, e2e_steps, e2e_s), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h, "steps": e2e_steps, "ms_per_step": e2e_s / e2e_steps * 1e3,
+               "pipelining": "copies in (step i+1), compute (step i) and copies out (step i-1) on three streams"}
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -737,6 +745,9 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--only", default="",
+                    help="comma-separated subset of the extra workloads to run beside the step: "
+                         "decode,gated,long,delta,backward,e2e (default: all)")
     ap.add_argument("--clock-warmup-seconds", type=float, default=0.6,
                     help="untimed load before timing so that clock samples see the GPU busy (0 under a profiler)")
     args = ap.parse_args()

@@ -107,6 +107,9 @@ __host__ __device__ constexpr int phi_index(int w) { return __builtin_popcount(k
 #ifndef LA_STAGES_HEAD
 #define LA_STAGES_HEAD 3
 #endif
+#ifndef LA_SP_BUFS_HEAD
+#define LA_SP_BUFS_HEAD 1
+#endif
 
 template <bool GATED, int DVS>
 struct Cfg {
@@ -115,7 +118,7 @@ struct Cfg {
     // The whole-head CTA needs 48 KB per stage and a 36 KB [Sprev | z] tile, so it
     // keeps three stages and one such tile.
     static constexpr int kStages = kHead ? LA_STAGES_HEAD : (GATED ? LA_STAGES_GATED : LA_STAGES);
-    static constexpr int kSpBufs = kHead ? 1 : LA_SP_BUFS;     // [Sprev | z] tiles
+    static constexpr int kSpBufs = kHead ? LA_SP_BUFS_HEAD : LA_SP_BUFS;   // [Sprev | z] tiles
     static constexpr int kNP = kHead ? 1 : 2;                  // P accumulator buffers
     static constexpr int kNO = kHead ? 2 : 3;                  // [O | dn] accumulator buffers
     static constexpr int kLag = kNO - 1;                       // outputs of chunk c - kLag finish in iteration c
@@ -132,22 +135,26 @@ struct Cfg {
     // 32-byte-swizzled blocks of 16 columns; block DVS/16 holds zhi (column 0) and zlo (1)
     static constexpr uint32_t kTileV = (DVS / 64) * kBlkV;
     static constexpr uint32_t kTileSpZ = (kW / 16) * kBlkSpZ;
-    // shared memory (offsets from a 1024-aligned base)
+    // shared memory (offsets from a 1024-aligned base).  A stage holds Q, K and V;
+    // with 128 value columns it also holds its own block of ones right after the
+    // two V blocks, so that [V | 1] is three blocks one LBO apart and its
+    // products are one MMA per K step (the ones blocks are written once).
     static constexpr uint32_t kOffQ = 0, kOffK = kTileQ, kOffV = 2 * kTileQ;
-    static constexpr uint32_t kStageBytes = kOffV + kTileV;
+    static constexpr uint32_t kOffStageOnes = kOffV + kTileV;
+    static constexpr uint32_t kStageBytes = kOffV + kTileV + (kHead ? kTileOnes : 0);
     static_assert(kStageBytes % 1024 == 0, "stage tiles stay 1024-byte aligned");
     // A is double-buffered
     static constexpr uint32_t kOffA = kStages * kStageBytes;
     static constexpr uint32_t kOffSpZ = kOffA + 2 * kTileA;
-    static constexpr uint32_t kOffOnes = kOffSpZ + kSpBufs * kTileSpZ;
-    static constexpr uint32_t kOffGate = kOffOnes + kTileOnes;
+    static constexpr uint32_t kOffOnes = kOffSpZ + kSpBufs * kTileSpZ;   // (64 value columns)
+    static constexpr uint32_t kOffGate = kOffOnes + (kHead ? 0 : kTileOnes);
     static constexpr uint32_t kOffSmall = kOffGate + (GATED ? sizeof(GateRing) : 0);
 };
 
 struct alignas(16) Small {
     uint64_t full[4], empty[4], phi_done[4], sc_done[4];
     // tm_read[c % 2]: the TMEM warps have read the state and P of chunk c's
-    // iteration; ops_full[c % 2]: they have written its Sprev and A; O_empty[c % 3]:
+    // iteration; ops_full[c % 2]: they have written its Sprev and A; O_empty[c % kNO]:
     // they have read O of chunk c
     uint64_t P_full[2], dS_full, tm_read[2], ops_full[2], Sp_empty;
     uint64_t A_empty[2], O_full[3], O_empty[3], aux_empty[kAux];
@@ -255,11 +262,16 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
         reinterpret_cast<uint4 *>(base + L::kOffSpZ + buf * L::kTileSpZ + (DVS / 16) * kBlkSpZ)[j] =
             make_uint4(0, 0, 0, 0);
     }
-    for (int i = threadIdx.x; i < (int)kTileOnes / 16; i += kThreads)
-        reinterpret_cast<uint4 *>(base + L::kOffOnes)[i] = make_uint4(0, 0, 0, 0);
+    // the ones block(s): one after the stages (64 value columns) or one per stage
+    constexpr int kNOnes = L::kHead ? NST : 1;
+    auto ones_ptr = [&](int i) {
+        return base + (L::kHead ? i * L::kStageBytes + L::kOffStageOnes : L::kOffOnes);
+    };
+    for (int i = threadIdx.x; i < kNOnes * (int)(kTileOnes / 16); i += kThreads)
+        reinterpret_cast<uint4 *>(ones_ptr(i / (kTileOnes / 16)))[i % (kTileOnes / 16)] = make_uint4(0, 0, 0, 0);
     __syncthreads();
-    if (threadIdx.x < kC)   // element (column 0, token row k): 16-byte chunk 0 of row k after the swizzle
-        *reinterpret_cast<uint16_t *>(base + L::kOffOnes + sw128_offset(threadIdx.x, 0)) = 0x3F80u;
+    if (threadIdx.x < kNOnes * kC)   // element (column 0, token row k): 16-byte chunk 0 of row k after the swizzle
+        *reinterpret_cast<uint16_t *>(ones_ptr(threadIdx.x / kC) + sw128_offset(threadIdx.x % kC, 0)) = 0x3F80u;
     fence_proxy_async_smem();
     if (warp == kWarpMma) {
         tmem_alloc(&sm->tmem_base, 512);
@@ -348,17 +360,13 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
         if (lane == 0) {
             constexpr uint32_t idP = idesc_bf16_f32(64, 64, false, false);
             // [S | z] increment and [O | dn] += A [V | 1] (column DVS gains the row
-            // sums of A).  With 64 value columns one MMA spans the V block and the
-            // first 16 columns of the ones block (at LBO); with 128 the two V blocks
-            // (LBO = one block) and the ones block are two MMAs.
-            constexpr int NV = DVS == 64 ? 80 : DVS;
-            constexpr uint32_t idDS = idesc_bf16_f32(128, NV, true, true);
-            constexpr uint32_t idDS1 = idesc_bf16_f32(128, 16, true, true);
+            // sums of A): one MMA per K step spans the V block(s) and the first 16
+            // columns of the ones block, LBO apart (64 value columns: the shared
+            // ones block after the stages; 128: the stage's own, one block after V).
+            constexpr uint32_t idDS = idesc_bf16_f32(128, L::kW, true, true);
             constexpr uint32_t idQS = idesc_bf16_f32(64, L::kW, false, true);   // [O | dn] = Q~ [Sprev | z]
-            constexpr uint32_t idAV = idesc_bf16_f32(64, NV, false, true);
-            constexpr uint32_t idAV1 = idesc_bf16_f32(64, 16, false, true);
+            constexpr uint32_t idAV = idesc_bf16_f32(64, L::kW, false, true);
             const uint32_t aOnes = smem_u32(base + L::kOffOnes);
-            const uint32_t onesLo = desc_lo(aOnes, kBlkV);
             constexpr uint32_t kHi128 = desc_hi(1024, 2), kHi32 = desc_hi(256, 6);   // SBO and swizzle words
             // P = Q~ K~^T for chunk c
             auto issue_p = [&](int c) -> bool {
@@ -389,7 +397,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
                 const uint32_t st = smem_u32(stage_ptr(s));
                 const uint32_t aK = st + L::kOffK;
                 // B = [V | 1]: the V tile, then (64 value columns) the ones block at LBO
-                const uint32_t blo = desc_lo(st + L::kOffV, DVS == 64 ? aOnes - (st + L::kOffV) : kBlkV);
+                const uint32_t blo = desc_lo(st + L::kOffV, L::kHead ? kBlkV : aOnes - (st + L::kOffV));
                 if (!GATED && !wait(cx, &sm->phi_done[s], (c / NST) & 1)) return false;
                 if (GATED && !wait(cx, &sm->sc_done[s], (c / NST) & 1)) return false;
                 if (!wait(cx, &sm->tm_read[c & 1], (c >> 1) & 1)) return false;   // state read (and decayed)
@@ -397,12 +405,8 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
                 const uint32_t dS = tmem + L::kColS;
                 const uint32_t klo = desc_lo(aK, kTileQ / 2);   // K~^T: MN-major, two 64-feature blocks
 #pragma unroll
-                for (int kk = 0; kk < 4; ++kk) {
+                for (int kk = 0; kk < 4; ++kk)
                     tc_mma_bf16_w<true>(dS, klo + kk * (2048 >> 4), kHi128, blo + kk * (2048 >> 4), kHi128, idDS);
-                    if (DVS == 128)
-                        tc_mma_bf16_w<true>(dS + DVS, klo + kk * (2048 >> 4), kHi128, onesLo + kk * (2048 >> 4), kHi128,
-                                            idDS1);
-                }
                 tc_commit(&sm->dS_full);
                 tc_commit(&sm->empty[s]);   // this issuer's last read of stage s
                 return true;
@@ -437,14 +441,10 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
                 }
                 if (L::kSpBufs == 1) tc_commit(&sm->Sp_empty);
                 const uint32_t alo = desc_lo(aA, 16);
-                const uint32_t vlo = desc_lo(aV, DVS == 64 ? aOnes - aV : kBlkV);
+                const uint32_t vlo = desc_lo(aV, L::kHead ? kBlkV : aOnes - aV);
 #pragma unroll
-                for (int kk = 0; kk < 4; ++kk) {
+                for (int kk = 0; kk < 4; ++kk)
                     tc_mma_bf16_w<true>(dO, alo + kk * (32 >> 4), kHi128, vlo + kk * (2048 >> 4), kHi128, idAV);
-                    if (DVS == 128)
-                        tc_mma_bf16_w<true>(dO + DVS, alo + kk * (32 >> 4), kHi128, onesLo + kk * (2048 >> 4), kHi128,
-                                            idAV1);
-                }
                 tc_commit(&sm->A_empty[bb]);
                 tc_commit(&sm->O_full[ob]);
                 tc_commit(&sm->empty[s]);
@@ -520,29 +520,41 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
             }
             if (has_p) tc_ld_16x32bx2_x8<8>(tmem + lane_base + L::kColP + pb * 64 + qq * 16, p);
             tc_wait_ld();
-            // Sprev of chunk c (BF16) and z split into two BF16 parts
+            // Sprev of chunk c (BF16) and z split into two BF16 parts.  With a gate
+            // the state is decayed by the chunk's gate product Gamma_last before its
+            // increment lands; a fast chunk (whole head) reads the decayed state:
+            // its outputs are O' = w_i O (see the epilogue).
+            const bool fast = GATED && L::kHead && has_b && gr->gf[c % kAux] != 0;
             uint32_t spk[SC / 2];
-            float zhi = 0.f;
-            if (has_b) {
-#pragma unroll
-                for (int j = 0; j < SC / 2; ++j) spk[j] = pack_bf16x2(S[2 * j], S[2 * j + 1]);
-                zhi = __bfloat162float(__float2bfloat16_rn(zr));
-            }
+            float zhi = 0.f, zsp = zr;
             if (GATED && has_b) {
-                // decay the state by the gate product of chunk c before its increment lands
                 const float g = gr->gG[c % kAux][kC - 1];
+                if (!fast) {
+#pragma unroll
+                    for (int j = 0; j < SC / 2; ++j) spk[j] = pack_bf16x2(S[2 * j], S[2 * j + 1]);
+                }
 #pragma unroll
                 for (int j = 0; j < SC; ++j) S[j] *= g;
                 st_state(S);
                 if (qq == 0) tc_st_32x32b_x1(tz, g * zr);
+                if (fast) {
+#pragma unroll
+                    for (int j = 0; j < SC / 2; ++j) spk[j] = pack_bf16x2(S[2 * j], S[2 * j + 1]);
+                    zsp = g * zr;
+                }
                 tc_wait_st();
+            } else if (has_b) {
+#pragma unroll
+                for (int j = 0; j < SC / 2; ++j) spk[j] = pack_bf16x2(S[2 * j], S[2 * j + 1]);
             }
+            if (has_b) zhi = __bfloat162float(__float2bfloat16_rn(zsp));
             tc_fence_before();
             if (has_b) warp_arrive(&sm->tm_read[bb]);
 
             // A = the causal mask (and, with a gate, the in-chunk decay) applied to P;
-            // without a gate a piece strictly below the diagonal is P itself
-            if (has_p && (GATED || qq == qd)) {
+            // without a gate, or for a fast chunk, a piece strictly below the
+            // diagonal is P itself
+            if (has_p && ((GATED && !fast) || qq == qd)) {
                 const int gq = c % kAux;
                 const float bi = GATED ? gr->gb[gq][prow] : 0.f;
                 const int zi = GATED ? gr->gz[gq][prow] : -1;
@@ -550,20 +562,23 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
                 for (int e = 0; e < 8; ++e) {
                     const int j = pcol + e;
                     float a = (j <= prow) ? p[e] : 0.f;
-                    if (GATED) a = (j <= prow && zi <= j) ? a * __expf(bi - gr->gb[gq][j]) : 0.f;
+                    if (GATED && !fast) a = (j <= prow && zi <= j) ? a * __expf(bi - gr->gb[gq][j]) : 0.f;
                     p[e] = a;
                 }
             }
-            if (GATED && has_b) warp_arrive(&sm->aux_empty[c % kAux]);   // gate data of chunk c is done
 
             // shared-memory operands (ahead of the outputs: the O issuer waits for them)
             if (has_b) {
                 const int sb = c % L::kSpBufs;
-                // A_empty of chunk c-2 follows that chunk's QS too, so with two
-                // Sprev buffers it also frees this one; with one, chunk c-1's QS
-                // must be done
-                if (L::kSpBufs == 1 && c >= 1 && !warp_wait(cx, &sm->Sp_empty, (c - 1) & 1)) break;
+                // A first: its buffer held chunk c-2's, free once that chunk's O MMAs
+                // are done (which, with two Sprev buffers, also frees this Sprev buffer)
                 if (c >= 2 && !warp_wait(cx, &sm->A_empty[bb], ((c >> 1) - 1) & 1)) break;
+                if (!a_zero)
+                    *reinterpret_cast<uint4 *>(base + L::kOffA + bb * kTileA + sw128_offset(prow, pcol >> 3)) =
+                        make_uint4(pack_bf16x2(p[0], p[1]), pack_bf16x2(p[2], p[3]), pack_bf16x2(p[4], p[5]),
+                                   pack_bf16x2(p[6], p[7]));
+                // with one Sprev buffer, it is free once chunk c-1's Q~ Sprev is done
+                if (L::kSpBufs == 1 && c >= 1 && !warp_wait(cx, &sm->Sp_empty, (c - 1) & 1)) break;
                 // Sprev columns SC qq .. +SC-1 of row srow: 16-column blocks SC/16 qq ..
                 uint8_t *spz = base + L::kOffSpZ + sb * L::kTileSpZ;
 #pragma unroll
@@ -577,11 +592,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
                 // z as two BF16 parts in columns DVS (zhi) and DVS + 1 (zlo)
                 if (qq == 0)
                     *reinterpret_cast<uint32_t *>(spz + (DVS / 16) * kBlkSpZ + sw32_offset(srow, 0)) =
-                        pack_bf16x2(zhi, zr - zhi);
-                if (!a_zero)
-                    *reinterpret_cast<uint4 *>(base + L::kOffA + bb * kTileA + sw128_offset(prow, pcol >> 3)) =
-                        make_uint4(pack_bf16x2(p[0], p[1]), pack_bf16x2(p[2], p[3]), pack_bf16x2(p[4], p[5]),
-                                   pack_bf16x2(p[6], p[7]));
+                        pack_bf16x2(zhi, zsp - zhi);
                 fence_proxy_async_smem();
                 warp_arrive(&sm->ops_full[bb]);
             } else if (has_s && last_seg) {
@@ -608,8 +619,12 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
                 tc_fence_before();
                 warp_arrive(&sm->O_empty[ob]);
                 dn += __shfl_xor_sync(0xffffffffu, dn, 16);
+                // a fast chunk's row i holds O' = w_i O and dn' = w_i dn: y = O' / (dn' + eps w_i)
+                float epsw = args.eps;
+                if (GATED && L::kHead && gr->gf[ce % kAux] != 0) epsw *= gr->gw[ce % kAux][prow];
+                if (GATED) warp_arrive(&sm->aux_empty[ce % kAux]);   // gate data of chunk ce is done
                 float inv;   // approximate reciprocal: y is rounded to BF16 below
-                asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(inv) : "f"(dn + args.eps));
+                asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(inv) : "f"(dn + epsw));
                 // SC/2 columns (16 or 32 bytes) of token row prow, straight to global
                 // memory (streaming stores: y is not read again here)
                 const int t = tb + ce * kC + prow;
@@ -649,12 +664,22 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
             warp_arrive(&sm->sc_done[sx]);
             return true;
         };
-        bool ok = true;
+        // Gated, whole head: a chunk flagged fast (gate_products) carries its gates
+        // as row weights on V instead: V_j <- w_j V_j in place and w_j in column 0
+        // of the stage's column block (1 otherwise), so that neither Q~ nor K~ is
+        // scaled and the chunk's products wait for no scaling.
+        constexpr bool kFastOk = GATED && L::kHead;
+        auto is_fast = [&](int x) { return kFastOk && gr->gf[x % kAux] != 0; };
+        bool ok = true, f_last = false;
         for (int c = 0; c < nch && ok; ++c) {
             const int s = c % NST;
             const int nvalid = min(kC, T - tb - c * kC);
             if (!warp_wait(cx, &sm->full[s], (c / NST) & 1)) { ok = false; break; }
             uint8_t *st = stage_ptr(s);
+            // the flags of chunks c and c-1 (the ring entry of c-1 cannot be reused
+            // before P of chunk c, which waits for this iteration's phi_done)
+            const bool f_cur = is_fast(c), f_prev = c >= 1 && is_fast(c - 1);
+            f_last = f_cur;
             // phi(Q), phi(K) in place (the two tiles are contiguous: 2048 chunks of
             // 16 bytes); key rows past the end of the sequence become 0
             static_assert(L::kOffK == L::kOffQ + kTileQ, "Q and K tiles are contiguous");
@@ -670,18 +695,34 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
                     qk[ci] = (ci >= 1024 && row >= nvalid) ? make_uint4(0, 0, 0, 0) : phi8(qk[ci]);
                 }
             }
+            if constexpr (kFastOk) {
+                uint16_t col0 = 0x3F80u;   // 1
+                if (f_cur) {
+                    // V rows by w_j (BF16 products; both V blocks: 1024 chunks of 16 bytes)
+                    uint4 *vt = reinterpret_cast<uint4 *>(st + L::kOffV);
+                    const float *w = gr->gw[c % kAux];
+                    for (int ci = pp; ci < (int)(L::kTileV / 16); ci += kPhiThreads)
+                        vt[ci] = scale8(vt[ci], w[(ci & 511) >> 3]);
+                    if (pp < kC) col0 = __bfloat16_as_ushort(__float2bfloat16_rn(w[pp]));
+                }
+                if (pp < kC) *reinterpret_cast<uint16_t *>(st + L::kOffStageOnes + sw128_offset(pp, 0)) = col0;
+            }
             fence_proxy_async_smem();
             // With one score buffer, P of chunk c (issued once phi of chunk c is
             // done) reuses the barrier phase parity of chunk c-1's P: wait for
             // chunk c-1's P before announcing phi of chunk c, so that the wait in
             // scale_qk never falls two phases behind.
-            if (GATED && NP == 1 && c >= 1 && !warp_wait(cx, &sm->P_full[0], (c - 1) & 1)) { ok = false; break; }
+            if (GATED && NP == 1 && c >= 1 && !f_prev && !warp_wait(cx, &sm->P_full[0], (c - 1) & 1)) {
+                ok = false;
+                break;
+            }
             warp_arrive(&sm->phi_done[s]);
+            if (GATED && f_cur) warp_arrive(&sm->sc_done[s]);   // nothing to scale after P
             // P of chunk c-1 was issued once phi of chunk c-1 was done and has
             // normally completed while phi of chunk c ran
-            if (GATED && c >= 1 && !scale_qk(c - 1)) ok = false;
+            if (GATED && c >= 1 && !f_prev && !scale_qk(c - 1)) ok = false;
         }
-        if (GATED && ok && nch >= 1) scale_qk(nch - 1);
+        if (GATED && ok && nch >= 1 && !f_last) scale_qk(nch - 1);
     }
 
     // ---------------------------------------------------------- teardown

@@ -21,10 +21,10 @@ constexpr int kR = 128;         // feature width r
 constexpr uint32_t kWaitHintNs = LA_WAIT_HINT_NS;
 
 
-// Gate data ring depth: the producer writes chunk c's entry up to a stage ring
-// ahead of its consumers, so the ring is deep enough that the entry it
-// overwrites (chunk c - kAux) was released long before.
-constexpr int kAux = 8;
+// Gate data ring depth: the producer writes chunk c's entry at most a stage ring
+// (of at most kAux stages) ahead of its consumers: once it may refill the stage
+// of chunk c - stages, every consumer has released the entry of that chunk.
+constexpr int kAux = 4;
 
 // Gate products of the chunks in flight (gated kernel only; chunk c in entry c % kAux).
 struct alignas(16) GateRing {
@@ -32,7 +32,14 @@ struct alignas(16) GateRing {
     int gz[kAux][kC];           // last row <= i whose gate is 0 (-1: none)
     float gG[kAux][kC];         // Gamma_i
     float gw[kAux][kC];         // w_j
+    int gf[kAux];               // 1: no zero gate and w_0 >= 2^-64 (see kFastGateLog)
 };
+
+// A chunk whose smallest write weight w_0 = e^{b_last - b_0} is at least
+// e^{kFastGateLog} (and which has no zero gate) may carry its gates as row
+// weights w_j on V (the rows of the scaled accumulators then stay far from
+// FP32 underflow); others take the exact path of explicit gate products.
+constexpr float kFastGateLog = -44.0f;   // e^-44 ~ 2^-63.5
 
 // phi(x) = ELU(x) + 1 on a pair of BF16 values, in packed BF16 arithmetic:
 // phi(x) = max(min(e^x, 1), x + 1).  For x <= 0, e^x >= 1 + x picks e^x; for
@@ -77,14 +84,16 @@ __device__ __forceinline__ bool aborted(const Ctx &cx)
 }
 
 // Bounded wait by one thread.  Gives up when the time limit runs out (and then
-// raises the abort flag) or as soon as another thread has raised it.
+// raises the abort flag) or as soon as another thread has raised it.  HINT_NS:
+// how long the thread may be suspended in hardware per try while the phase is
+// incomplete (0: it polls).
+template <uint32_t HINT_NS = kWaitHintNs>
 __device__ __forceinline__ bool wait(Ctx &cx, uint64_t *bar, uint32_t parity)
 {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = global_timer_ns();
     for (;;) {
-        // suspended in hardware while the phase is incomplete (bounded per try)
-        if (kWaitHintNs ? mbar_try_wait_hint(bar, parity, kWaitHintNs) : mbar_try_wait(bar, parity)) return true;
+        if (HINT_NS ? mbar_try_wait_hint(bar, parity, HINT_NS) : mbar_try_wait(bar, parity)) return true;
         if (aborted(cx)) return false;
         if (global_timer_ns() - t0 > cx.limit) {
             fail(cx);
@@ -168,6 +177,8 @@ __device__ __forceinline__ void gate_products(float a0, float a1, int lane, int 
     *reinterpret_cast<int2 *>(&gr->gz[gq][j0]) = make_int2(z0, z1);
     *reinterpret_cast<float2 *>(&gr->gG[gq][j0]) = make_float2(z0 < 0 ? expf(b0) : 0.f, z1 < 0 ? expf(b1) : 0.f);
     *reinterpret_cast<float2 *>(&gr->gw[gq][j0]) = make_float2(w0, w1);
+    const float bfirst = __shfl_sync(0xffffffffu, b0, 0);
+    if (lane == 0) gr->gf[gq] = (zlast < 0 && blast - bfirst >= kFastGateLog) ? 1 : 0;
 }
 
 }  // namespace
