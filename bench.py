@@ -80,6 +80,14 @@ def backward_flops(B, H, T, r, dv, gated):
     return B * H * T * (10 + (2 if gated else 0)) * r * dv
 
 
+def backward_bytes(B, H, T, r, dv, gated, elem=2):
+    """Compulsory HBM bytes of one backward call without carried states: q, k, v,
+    y and dy read, dq, dk and dv written (elem bytes each), alpha read and dalpha
+    written (FP32, gated only), dS0 and dz0 written (FP32)."""
+    per_token_head = elem * (2 * r + 2 * dv) + elem * (2 * r + dv) + (8 if gated else 0)
+    return B * H * (T * per_token_head + 4 * (r * dv + r))
+
+
 def fp32_alu_peak_tflops(sm_count):
     """FP32 FMA peak of the CUDA cores: SMs x 128 FP32 lanes x 2 FLOP x the
     maximum SM clock (MEASURED_PEAKS.json, else the nominal 2070 MHz)."""
@@ -640,11 +648,14 @@ def run_ours(args, rank, world, local_rank):
         b_s, = reduce_max([b_s], dev, dist)
         assert _native.lib().la_last_device_status(sh) == 0
         b_call = b_s / bsteps
-        b_tflops = backward_flops(bw.B, bw.H, bw.T, bw.r, bw.dv, True) / b_call / 1e12
+        b_bytes = backward_bytes(bw.B, bw.H, bw.T, bw.r, bw.dv, True)
+        b_gbs = b_bytes / b_call / 1e9
         backward = {"workload": bw.name.replace("prefill", "backward of the gated prefill,"), "call_us": b_call * 1e6,
-                    "launches_per_call": 5, "tokens_per_s": bw.B * bw.T * world / b_call, "steps": bsteps,
-                    "roofline": {"bound": "alu", "achieved": b_tflops, "peak": alu_peak, "unit": "TFLOP/s",
-                                 "frac": b_tflops / alu_peak, "peak_kind": "nominal FP32 FMA (SMs x 128 x 2 x max clock)",
+                    "launches_per_call": 6, "tokens_per_s": bw.B * bw.T * world / b_call, "steps": bsteps,
+                    "roofline": {"bound": "hbm", "achieved": b_gbs, "peak": peak, "unit": "GB/s",
+                                 "frac": b_gbs / peak, "peak_kind": peak_kind, "scope": "whole call",
+                                 "algorithmic_bytes_per_call": b_bytes,
+                                 "tensor_tflops": backward_flops(bw.B, bw.H, bw.T, bw.r, bw.dv, True) / b_call / 1e12,
                                  "algorithmic_flops_per_call": backward_flops(bw.B, bw.H, bw.T, bw.r, bw.dv, True)}}
 
     if want("e2e"):
@@ -713,12 +724,16 @@ def run_ours(args, rank, world, local_rank):
         tps, cores, desc, _ = oracle_tokens_per_s(w, args.cpu_seconds)
         cpu = {"value": tps, "unit": "tokens/s", "cores": cores, "kind": "oracle", "sample": desc}
         # the oracles of the delta rule and of the backward, beside their GPU figures
-        delta["cpu_baseline"] = oracle_rate("delta", xw, args.cpu_seconds / 4)
+        if delta is not None:
+            delta["cpu_baseline"] = oracle_rate("delta", xw, args.cpu_seconds / 4)
         for entry, pw in ((gated_prefill, W.GATED), (long_prefill, W.LONG)):
+            if entry is None:
+                continue
             tps_p, cores_p, desc_p, _ = oracle_tokens_per_s(pw, args.cpu_seconds / 4)
             entry["cpu_baseline"] = {"value": tps_p, "unit": "tokens/s", "cores": cores_p, "kind": "oracle",
                                      "sample": desc_p}
-        backward["cpu_baseline"] = oracle_rate("backward", bw, args.cpu_seconds / 4)
+        if backward is not None:
+            backward["cpu_baseline"] = oracle_rate("backward", bw, args.cpu_seconds / 4)
 
     if rank == 0:
         line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,

@@ -222,9 +222,12 @@ size_t la_backward_workspace_bytes(int B, int H, int T);
  *   dS0, dz0  device FP32 [B,H,r,dv], [B,H,r] (written also when S0, z0 are NULL).
  *   workspace: >= la_backward_workspace_bytes device bytes, 16-byte aligned, owned by
  *          the caller; calls sharing it must be ordered.
- * Kernels (FP32 on CUDA cores): one pass for d_t and dd_t, three gated rank-1
- * recurrences (dq forward in time, dk and dv in reverse), and a reverse running
- * sum for dalpha.  Requires r, dv in {32, 64, 128}, T >= 1, 16-byte aligned
+ * Kernels: one pass for d_t and one for dd_t, then the three gradients as causal
+ * linear attentions over chunks of 64 tokens (dq forward in time, dk and dv in
+ * reverse), then a reverse running sum for dalpha.  BF16 with r = dv = 128 runs
+ * the three on the tensor cores (BF16 operands, FP32 accumulators and state);
+ * the other shapes and FP32 run them as gated rank-1 recurrences in FP32 on the
+ * CUDA cores.  Requires r, dv in {32, 64, 128}, T >= 1, 16-byte aligned
  * token arrays (q, k, v, y, dy, dq, dk, dv_out), 4-byte aligned FP32 arrays
  * (dS_T 8-byte aligned).
  * Errors: LA_ERR_NULL, LA_ERR_SHAPE, LA_ERR_DTYPE, LA_ERR_ALIGN, LA_ERR_UNSUPPORTED,

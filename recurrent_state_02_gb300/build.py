@@ -17,7 +17,7 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 LIB = os.path.join(HERE, "liblinattn.so")
 BUILD = os.path.join(HERE, "_build")
-SOURCES = ["api.cu", "backward.cu", "decode.cu", "delta.cu", "delta_tc.cu", "prefill_f32.cu", "prefill_tc.cu", "state_tc.cu"]
+SOURCES = ["api.cu", "backward.cu", "bwd_tc.cu", "decode.cu", "delta.cu", "delta_tc.cu", "prefill_f32.cu", "prefill_tc.cu", "state_tc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-std=c++17", "-O3", "-lineinfo", "-Xcompiler", "-fPIC", "-I", INCLUDE]
 

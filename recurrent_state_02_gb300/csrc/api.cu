@@ -456,6 +456,20 @@ la_status la_prefill_backward(const void *q, const void *k, const void *v, la_dt
     a.status = status_word();
     a.limit_ns = la::kWaitLimitNs;
     if (!a.status) return LA_ERR_CUDA;
+    // BF16 at r == dv == 128: the sweeps run on the tensor cores, which read q, k,
+    // v and dy through TMA descriptors
+    CUtensorMap maps[4];
+    a.maps = nullptr;
+    if (dtype == LA_DTYPE_BF16 && r == 128 && dv == 128) {
+        const long long planes = (long long)B * H;
+        const CUtensorMapSwizzle sw128 = CU_TENSOR_MAP_SWIZZLE_128B;
+        if (!make_map_bf16(&maps[0], q, planes, T, 128, 64, 64, sw128) ||
+            !make_map_bf16(&maps[1], k, planes, T, 128, 64, 64, sw128) ||
+            !make_map_bf16(&maps[2], v, planes, T, 128, 64, 64, sw128) ||
+            !make_map_bf16(&maps[3], dy, planes, T, 128, 64, 64, sw128))
+            return LA_ERR_CUDA;
+        a.maps = maps;
+    }
     return from_cuda(la::launch_backward(a, B, dtype == LA_DTYPE_BF16, reinterpret_cast<cudaStream_t>(stream)));
 }
 

@@ -619,6 +619,26 @@ cudaError_t launch_bwd_t(const BackwardArgs &a, int B, cudaStream_t stream)
     bwd_dd_kernel<Tin><<<152 * 8, 256, 0, stream>>>(static_cast<const Tin *>(a.y), static_cast<const Tin *>(a.dy),
                                                       a.dv, (long long)n, a.eps, d, dd);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    if constexpr (sizeof(Tin) == 2) {
+        if (a.maps) {
+            // the three sweeps on the tensor cores
+            BwdTcArgs t;
+            t.alpha = a.alpha; t.S0 = a.S0; t.z0 = a.z0; t.dS_T = a.dS_T; t.dz_T = a.dz_T;
+            t.d = d; t.dd = dd;
+            t.q = static_cast<const uint16_t *>(a.q); t.k = static_cast<const uint16_t *>(a.k);
+            t.dq = static_cast<uint16_t *>(a.dq); t.dk = static_cast<uint16_t *>(a.dk);
+            t.dv = static_cast<uint16_t *>(a.dv_out);
+            t.tok_sum = a.alpha ? tok_sum : nullptr; t.fin = a.alpha ? fin : nullptr;
+            t.dS0 = a.dS0; t.dz0 = a.dz0;
+            t.H = a.H; t.T = a.T; t.status = a.status; t.limit_ns = a.limit_ns;
+            if ((e = launch_bwd_tc(a.maps, t, B, a.alpha != nullptr, stream)) != cudaSuccess) return e;
+            if (a.alpha && a.dalpha) {
+                bwd_dalpha_kernel<<<BH, 128, 0, stream>>>(tok_sum, fin, a.alpha, a.T, a.dalpha);
+                if ((e = cudaGetLastError()) != cudaSuccess) return e;
+            }
+            return cudaSuccess;
+        }
+    }
     RecArgs p;
     p.q = a.q; p.k = a.k; p.v = a.v; p.dy = a.dy;
     p.alpha = a.alpha; p.S0 = a.S0; p.z0 = a.z0; p.dS_T = a.dS_T; p.dz_T = a.dz_T; p.d = d; p.dd = dd;

@@ -130,8 +130,28 @@ struct BackwardArgs {
     float eps;
     int *status;                                // device status word
     unsigned long long limit_ns;
+    // BF16 with r == dv == 128: tensor maps of q, k, v, dy over [B*H, T, 128] (boxes
+    // of 64 x 64, 128-byte swizzle); the three sweeps then run on the tensor cores.
+    // nullptr: the sweeps run on CUDA cores.
+    const CUtensorMap *maps;
 };
 size_t backward_workspace_floats(int B, int H, int T);
+
+// The three gradient sweeps on the tensor cores (BF16, r == dv == 128), given
+// d_t (with eps) and dd_t: dq, dk, dv, the dlog alpha terms (tok_sum, fin; may be
+// nullptr without a gate) and dS0, dz0.
+struct BwdTcArgs {
+    const float *alpha, *S0, *z0, *dS_T, *dz_T;  // optional (nullptr)
+    const float *d, *dd;                         // [B*H*T]
+    const uint16_t *q, *k;                       // BF16 [B,H,T,128] (phi and phi' in the epilogues)
+    uint16_t *dq, *dk, *dv;                      // BF16 [B,H,T,128]
+    float *tok_sum, *fin;                        // [B*H*T], [B*H] (accumulated), or nullptr
+    float *dS0, *dz0;                            // [B,H,128,128], [B,H,128]
+    int H, T;
+    int *status;
+    unsigned long long limit_ns;
+};
+cudaError_t launch_bwd_tc(const CUtensorMap *maps, const BwdTcArgs &a, int B, bool gated, cudaStream_t stream);
 cudaError_t launch_backward(const BackwardArgs &a, int B, bool bf16, cudaStream_t stream);
 
 cudaError_t launch_state_init(float *S, float *z, long long n_S, long long n_z, cudaStream_t stream);

@@ -87,6 +87,64 @@ def test_backward_parity(la, oracle_mod, dtype, r, dv, T, gated, with_state):
         assert err <= TOL[dtype], (name, err)
 
 
+# BF16 at r = dv = 128 runs the three sweeps on the tensor cores: ragged lengths
+# (T = 1, one chunk exactly, one token past it), zero gates at and around chunk
+# boundaries, and gates that decay by more than e^-44 inside a chunk.
+TC_EDGE = [
+    # T, gated, with_state, gate edits
+    (1, True, True, None),
+    (64, False, True, None),
+    (65, True, False, None),
+    (200, True, True, "zeros"),
+    (190, True, False, "tiny"),
+]
+
+
+@pytest.mark.parametrize("T,gated,with_state,edit", TC_EDGE,
+                         ids=[f"T{c[0]}-g{int(c[1])}-S{int(c[2])}-{c[3]}" for c in TC_EDGE])
+def test_backward_tc_edges(la, oracle_mod, T, gated, with_state, edit):
+    from recurrent_state_02_gb300 import workloads as W
+    B, H = 1, 3
+    w = W.Workload("bwd-tc", B=B, H=H, T=T, dtype=torch.bfloat16, gated=gated, seed=500 + T)
+    d = W.prefill_inputs(w, with_state=with_state)
+    if edit == "zeros":
+        for t in (0, 63, 64, 127, 150):
+            d["alpha"][0, 0, t] = 0.0
+        d["alpha"][0, 1, 70:90] = 0.0
+    elif edit == "tiny":
+        d["alpha"][0, 0, 64:128] = 0.2
+        d["alpha"][0, 2, 100] = 1e-20
+    g = torch.Generator().manual_seed(501 + T)
+    dy = torch.randn((B, H, T, 128), generator=g).to(torch.bfloat16)
+    dS_T = torch.randn((B, H, 128, 128), generator=g) * 0.1 if with_state else None
+    dz_T = torch.randn((B, H, 128), generator=g) * 0.1 if with_state else None
+    args = [to_oracle(d[n]) for n in ("q", "k", "v")]
+    y, _, _ = oracle_mod.scan(*args, alpha=to_oracle(d["alpha"]), S0=to_oracle(d["S0"]), z0=to_oracle(d["z0"]),
+                              eps=EPS)
+    ref = oracle_mod.backward(*args, dy.double().numpy(), alpha=to_oracle(d["alpha"]), S0=to_oracle(d["S0"]),
+                              z0=to_oracle(d["z0"]), dS_T=to_oracle(dS_T), dz_T=to_oracle(dz_T), eps=EPS, threads=0)
+    gd = {k: (v.cuda() if v is not None else None) for k, v in d.items()}
+    out = la.prefill_backward(gd["q"], gd["k"], gd["v"], torch.from_numpy(y).to(torch.bfloat16).cuda(), dy.cuda(),
+                              alpha=gd["alpha"], S0=gd["S0"], z0=gd["z0"],
+                              dS_T=dS_T.cuda() if dS_T is not None else None,
+                              dz_T=dz_T.cuda() if dz_T is not None else None, eps=EPS)
+    assert la.last_device_status() == 0
+    for name, a, r_ in zip(("dq", "dk", "dv", "dalpha", "dS0", "dz0"), out, ref):
+        if r_ is None:
+            assert a is None
+            continue
+        a = a.float().cpu().numpy()
+        if name == "dalpha":
+            # dalpha_u is the log-gate derivative over alpha_u: defined where alpha_u > 0,
+            # and its absolute error grows as 1 / alpha_u, so the bar covers alpha_u >= 0.05
+            keep = d["alpha"].numpy() >= 0.05
+            a, r_ = a[keep], r_[keep]
+        assert np.isfinite(a).all(), name
+        err = max_rel_err(a, r_)
+        print(f"[parity] backward (tensor cores) {name}: tensor {err:.3e}")
+        assert err <= 2e-2, (name, err)
+
+
 CHAIN_CASES = [
     # T, gated, with_state
     (300, True, True),
