@@ -60,78 +60,122 @@ __device__ __forceinline__ float2 hi2(float4 a) { return make_float2(a.z, a.w); 
 
 // ------------------------------------------------------------ d_t and dd_t
 
-// z_t and the feature sum of d_t: one CTA of kZSeg warps per (b, h, 32 features),
-// lane = feature.  z_t = alpha_t z_{t-1} + phi(k_t) is affine in z, so the sequence
-// is cut into kZSeg segments, one per warp.  Each warp first runs its segment from
-// z = 0, which gives the segment's map z -> P z + zs (P the product of its gates);
-// the maps of the segments before it, applied to z0 in order, give the warp its
-// true start, and it runs the segment again from there.  The products
-// q~_{t,i} z_{t,i} of blocks of kZB tokens are summed over the warp's features
-// through a padded tile and added to d_acc[t] (zeroed before).
-constexpr int kZSeg = 32;        // segments (warps) per sequence
-constexpr int kZB = 8;           // tokens per block of the second pass
+// z_t and the feature sum of d_t: one CTA of kZSeg warps per (b, h, 64
+// features); lane l holds features 2l, 2l + 1 (one 4-byte load per token for
+// BF16; at r = 32 the upper 16 lanes hold none).  z_t = alpha_t z_{t-1} + phi(k_t) is affine in z, so the sequence is cut
+// into kZSeg segments, one per warp.  Each warp first runs its segment from z = 0,
+// which gives the segment's map z -> P z + zs (P the product of its gates); the
+// maps of the segments before it, applied to z0 in order, give the warp its true
+// start, and it runs the segment again from there.  Tokens go in batches of
+// ZB(Tin) whose loads are all issued before the recurrence uses them; the batch's
+// products q~_{t,i} z_{t,i} are summed over the warp's features by a
+// reduce-scatter across the lanes (lane l ends with token l mod ZB) and added to
+// d_acc[t] (zeroed before).
+constexpr int kZSeg = 16;        // segments (warps) per sequence
+constexpr int kZFeat = 64;       // features per CTA
+
+template <typename Tin> struct ZBatch { static constexpr int n = 32; };
+template <> struct ZBatch<float> { static constexpr int n = 16; };
+
+// Two adjacent features of one token row, raw.
+__device__ __forceinline__ uint32_t load_pair(const __nv_bfloat16 *p) { return *reinterpret_cast<const uint32_t *>(p); }
+__device__ __forceinline__ float2 load_pair(const float *p) { return *reinterpret_cast<const float2 *>(p); }
+__device__ __forceinline__ float2 unpack_pair(uint32_t raw) { return make_float2(bf16_lo(raw), bf16_hi(raw)); }
+__device__ __forceinline__ float2 unpack_pair(float2 raw) { return raw; }
+
+// Sums v[0..NB) over the 32 lanes: afterwards v[0] of lane l holds the total of
+// index l mod NB.  Each halving step swaps the half of the values that a lane
+// gives away with its partner lane and adds the half it keeps.
+template <int NB>
+__device__ __forceinline__ float lane_reduce_scatter(float (&v)[NB], int lane)
+{
+#pragma unroll
+    for (int s = NB / 2; s >= 1; s >>= 1) {
+        const bool up = (lane & s) != 0;
+#pragma unroll
+        for (int i = 0; i < s; ++i) {
+            const float give = up ? v[i] : v[i + s];
+            const float keep = up ? v[i + s] : v[i];
+            v[i] = keep + __shfl_xor_sync(0xffffffffu, give, s);
+        }
+    }
+#pragma unroll
+    for (int s = NB; s < 32; s <<= 1) v[0] += __shfl_xor_sync(0xffffffffu, v[0], s);
+    return v[0];
+}
 
 template <typename Tin>
 __global__ void __launch_bounds__(32 * kZSeg)
 bwd_z_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k, const float *__restrict__ alpha,
              const float *__restrict__ z0, int T, int r, float *__restrict__ d_acc)
 {
-    __shared__ float tile[kZSeg][kZB][33];
-    __shared__ float segP[kZSeg], segZ[kZSeg][32];
+    constexpr int NB = ZBatch<Tin>::n;
+    using Raw = decltype(load_pair(static_cast<const Tin *>(nullptr)));
+    __shared__ float segP[kZSeg];
+    __shared__ float2 segZ[kZSeg][32];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int nfg = r / 32, bh = blockIdx.x / nfg, i0 = (blockIdx.x % nfg) * 32;
+    const int nfg = (r + kZFeat - 1) / kZFeat, bh = blockIdx.x / nfg, i0 = (blockIdx.x % nfg) * kZFeat + 2 * lane;
+    const bool live = i0 < r;
     const int len = (T + kZSeg - 1) / kZSeg;
     const int ta = min(T, warp * len), te = min(T, ta + len);
-    const Tin *kp = k + (size_t)bh * T * r + i0 + lane, *qp = q + (size_t)bh * T * r + i0 + lane;
+    const Tin *kp = k + (size_t)bh * T * r + i0, *qp = q + (size_t)bh * T * r + i0;
     const float *ap = alpha ? alpha + (size_t)bh * T : nullptr;
 
     // 1: the segment's map, from z = 0
-    float z = 0.f, P = 1.f;
-    for (int t0 = ta; t0 < te; t0 += kZB) {
-        const int nt = min(kZB, te - t0);
-        float kv[kZB], av[kZB];
+    float2 z = make_float2(0.f, 0.f);
+    float P = 1.f;
+    for (int t0 = ta; t0 < te; t0 += NB) {
+        const int nt = min(NB, te - t0);
+        Raw kr[NB];
 #pragma unroll
-        for (int t = 0; t < kZB; ++t) {
-            kv[t] = t < nt ? to_f32(kp[(size_t)(t0 + t) * r]) : 0.f;
-            av[t] = (ap && t < nt) ? ap[t0 + t] : 1.f;
-        }
+        for (int t = 0; t < NB; ++t) kr[t] = (t < nt && live) ? load_pair(kp + (size_t)(t0 + t) * r) : Raw{};
+        const float al = (ap && lane < nt) ? ap[t0 + lane] : 1.f;
 #pragma unroll
-        for (int t = 0; t < kZB; ++t)
+        for (int t = 0; t < NB; ++t) {
+            const float a = __shfl_sync(0xffffffffu, al, t);
             if (t < nt) {
-                z = av[t] * z + phi_f(kv[t]);
-                P *= av[t];
+                const float2 kv = unpack_pair(kr[t]);
+                z.x = a * z.x + phi_f(kv.x);
+                z.y = a * z.y + phi_f(kv.y);
+                P *= a;
             }
+        }
     }
     if (lane == 0) segP[warp] = P;
     segZ[warp][lane] = z;
     __syncthreads();
 
     // 2: the true start of the segment, then the segment again with its products
-    z = z0 ? z0[(size_t)bh * r + i0 + lane] : 0.f;
-    for (int u = 0; u < warp; ++u) z = segP[u] * z + segZ[u][lane];
-    for (int t0 = ta; t0 < te; t0 += kZB) {
-        const int nt = min(kZB, te - t0);
-        float kv[kZB], qv[kZB], av[kZB];
+    z = (z0 && live) ? *reinterpret_cast<const float2 *>(z0 + (size_t)bh * r + i0) : make_float2(0.f, 0.f);
+    for (int u = 0; u < warp; ++u) {
+        const float pu = segP[u];
+        const float2 zu = segZ[u][lane];
+        z.x = pu * z.x + zu.x;
+        z.y = pu * z.y + zu.y;
+    }
+    for (int t0 = ta; t0 < te; t0 += NB) {
+        const int nt = min(NB, te - t0);
+        Raw kr[NB], qr[NB];
 #pragma unroll
-        for (int t = 0; t < kZB; ++t) {
-            kv[t] = t < nt ? to_f32(kp[(size_t)(t0 + t) * r]) : 0.f;
-            qv[t] = t < nt ? to_f32(qp[(size_t)(t0 + t) * r]) : 0.f;
-            av[t] = (ap && t < nt) ? ap[t0 + t] : 1.f;
+        for (int t = 0; t < NB; ++t) {
+            kr[t] = (t < nt && live) ? load_pair(kp + (size_t)(t0 + t) * r) : Raw{};
+            qr[t] = (t < nt && live) ? load_pair(qp + (size_t)(t0 + t) * r) : Raw{};
         }
+        const float al = (ap && lane < nt) ? ap[t0 + lane] : 1.f;
+        float prod[NB];
 #pragma unroll
-        for (int t = 0; t < kZB; ++t)
+        for (int t = 0; t < NB; ++t) {
+            const float a = __shfl_sync(0xffffffffu, al, t);
+            prod[t] = 0.f;
             if (t < nt) {
-                z = av[t] * z + phi_f(kv[t]);
-                tile[warp][t][lane] = phi_f(qv[t]) * z;
+                const float2 kv = unpack_pair(kr[t]), qv = unpack_pair(qr[t]);
+                z.x = a * z.x + phi_f(kv.x);
+                z.y = a * z.y + phi_f(kv.y);
+                if (live) prod[t] = phi_f(qv.x) * z.x + phi_f(qv.y) * z.y;
             }
-        __syncwarp();
-        if (lane < nt) {
-            float s = 0.f;
-#pragma unroll 8
-            for (int f = 0; f < 32; ++f) s += tile[warp][lane][f];
-            atomicAdd(&d_acc[(size_t)bh * T + t0 + lane], s);
         }
-        __syncwarp();
+        const float sum = lane_reduce_scatter<NB>(prod, lane);
+        if (lane < nt) atomicAdd(&d_acc[(size_t)bh * T + t0 + lane], sum);
     }
 }
 
@@ -613,7 +657,7 @@ cudaError_t launch_bwd_t(const BackwardArgs &a, int B, cudaStream_t stream)
     // d accumulates the feature sums; tok_sum and fin accumulate dalpha terms
     cudaError_t e = cudaMemsetAsync(a.ws, 0, sizeof(float) * (3 * n + BH), stream);
     if (e != cudaSuccess) return e;
-    bwd_z_kernel<Tin><<<(unsigned)(BH * (a.r / 32)), 32 * kZSeg, 0, stream>>>(
+    bwd_z_kernel<Tin><<<(unsigned)(BH * ((a.r + kZFeat - 1) / kZFeat)), 32 * kZSeg, 0, stream>>>(
         static_cast<const Tin *>(a.q), static_cast<const Tin *>(a.k), a.alpha, a.z0, a.T, a.r, d);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     bwd_dd_kernel<Tin><<<152 * 8, 256, 0, stream>>>(static_cast<const Tin *>(a.y), static_cast<const Tin *>(a.dy),

@@ -111,11 +111,11 @@ static_assert(smem_bytes<kModeDq>() <= 232448 && smem_bytes<kModeDk>() <= 232448
 __device__ __forceinline__ float phi_f(float x) { return x > 0.f ? x + 1.f : __expf(x); }
 __device__ __forceinline__ float dphi_f(float x) { return x > 0.f ? 1.f : __expf(x); }
 
+// One sweep (MODE) of one head (blockIdx.y, blockIdx.z).
 template <int MODE, bool GATED>
-__global__ void __launch_bounds__(kThreads, 1)
-bwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
-              const __grid_constant__ CUtensorMap map_v, const __grid_constant__ CUtensorMap map_dy,
-              const BwdTcArgs args)
+__device__ __forceinline__ void
+bwd_sweep(const CUtensorMap &map_q, const CUtensorMap &map_k, const CUtensorMap &map_v, const CUtensorMap &map_dy,
+          const BwdTcArgs &args)
 {
     using L = BCfg<MODE>;
     constexpr bool REV = L::kRev;
@@ -535,10 +535,11 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
             for (int ci = pp; ci < (int)(kTile / 16); ci += kPrepThreads) t4[ci] = fn(t4[ci], (ci & 511) >> 3);
         };
         auto scale_rows = [&](uint8_t *tile, const float *wt) { each(tile, [&](uint4 v, int row) { return scale8(v, wt[row]); }); };
-        auto scale_pending = [&](int x) -> bool {
-            // chunk x: once its P has read the unscaled tiles
+        auto scale_pending = [&](int x, bool waited) -> bool {
+            // chunk x: once its P has read the unscaled tiles (waited: this warp has
+            // already waited for that P, and must not wait again: see below)
             const int sx = x % kStages, gx = x % kAux;
-            if (!warp_wait(cx, &sm->P_full, x & 1)) return false;
+            if (!waited && !warp_wait(cx, &sm->P_full, x & 1)) return false;
             uint8_t *st = stage_ptr(sx);
             const float *rw = MODE == kModeDq ? gr->gG[gx] : gr->gw[gx];   // read weights of the query rows
             const float *ww = MODE == kModeDq ? gr->gw[gx] : gr->gG[gx];   // write weights of the state operand rows
@@ -578,13 +579,17 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
                 scale_rows(st + L::kOffVal, invd);   // dn
             }
             fence_proxy_async_smem();
-            // one score buffer: P of chunk c reuses the barrier phase parity of chunk
-            // c-1's P, so chunk c-1's P is waited for before chunk c is announced
+            // One score buffer: P of chunk c (issued once this chunk is announced)
+            // completes the barrier phase after chunk c-1's, of the other parity; a
+            // wait for chunk c-1's parity begun after P of chunk c had completed
+            // would wait for chunk c+1's P, which needs this warp.  So chunk c-1's
+            // P is waited for here, before chunk c is announced, and not again.
             if (GATED && c >= 1 && !warp_wait(cx, &sm->P_full, (c - 1) & 1)) { ok = false; break; }
             warp_arrive(&sm->prep_done[s]);
-            if (GATED && c >= 1 && !scale_pending(c - 1)) ok = false;
+            if (GATED && c >= 1 && !scale_pending(c - 1, true)) ok = false;
         }
-        if (GATED && ok && nch >= 1) scale_pending(nch - 1);
+        // the last chunk's P is the last phase: nothing can complete after it
+        if (GATED && ok && nch >= 1) scale_pending(nch - 1, false);
     }
 
     // ---------------------------------------------------------- teardown
@@ -594,6 +599,17 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
         tc_fence_after();
         tmem_dealloc(tmem, 512);
     }
+}
+
+// One sweep per launch.  (The three side by side in one launch, 3 x B x H CTAs,
+// ran slower: SMs running different sweeps thrash the shared instruction cache.)
+template <int MODE, bool GATED>
+__global__ void __launch_bounds__(kThreads, 1)
+bwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
+              const __grid_constant__ CUtensorMap map_v, const __grid_constant__ CUtensorMap map_dy,
+              const BwdTcArgs args)
+{
+    bwd_sweep<MODE, GATED>(map_q, map_k, map_v, map_dy, args);
 }
 
 }  // namespace
@@ -607,11 +623,10 @@ cudaError_t launch_bwd_tc(const CUtensorMap *maps, const BwdTcArgs &a, int B, bo
                                         bwd_tc_kernel<kModeDv, true>}};
     static const uint32_t bytes[3] = {smem_bytes<kModeDq>(), smem_bytes<kModeDk>(), smem_bytes<kModeDv>()};
     static OncePerDevice attr_set[2][3];
-    const dim3 grid(1, a.H, B);
     for (int m = 0; m < 3; ++m) {
         cudaError_t e = set_smem_once(kerns[gated][m], bytes[m], attr_set[gated][m]);
         if (e != cudaSuccess) return e;
-        kerns[gated][m]<<<grid, kThreads, bytes[m], stream>>>(maps[0], maps[1], maps[2], maps[3], a);
+        kerns[gated][m]<<<dim3(1, a.H, B), kThreads, bytes[m], stream>>>(maps[0], maps[1], maps[2], maps[3], a);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
     return cudaSuccess;

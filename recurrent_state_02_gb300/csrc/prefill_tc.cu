@@ -647,10 +647,11 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
         const int pp = phi_index(warp) * 32 + lane;   // 0..159
         // gated: once P of chunk x is complete (it read the unscaled tiles), the
         // rows of Q~ are scaled in place by Gamma_i (O = (Gamma Q~) Sprev) and
-        // the rows of K~ by w_j (dS = (w K~)^T V, dz = (w K~)^T 1)
-        auto scale_qk = [&](int x) -> bool {
+        // the rows of K~ by w_j (dS = (w K~)^T V, dz = (w K~)^T 1).  waited: this
+        // warp has already waited for that P (and must not wait again: see below)
+        auto scale_qk = [&](int x, bool waited) -> bool {
             const int sx = x % NST;
-            if (!warp_wait(cx, &sm->P_full[x % NP], (x / NP) & 1)) return false;
+            if (!waited && !warp_wait(cx, &sm->P_full[x % NP], (x / NP) & 1)) return false;
             uint4 *qk = reinterpret_cast<uint4 *>(stage_ptr(sx) + L::kOffQ);
             const float *gam = gr->gG[x % kAux];
             const float *w = gr->gw[x % kAux];
@@ -709,10 +710,13 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
             }
             fence_proxy_async_smem();
             // With one score buffer, P of chunk c (issued once phi of chunk c is
-            // done) reuses the barrier phase parity of chunk c-1's P: wait for
-            // chunk c-1's P before announcing phi of chunk c, so that the wait in
-            // scale_qk never falls two phases behind.
-            if (GATED && NP == 1 && c >= 1 && !f_prev && !warp_wait(cx, &sm->P_full[0], (c - 1) & 1)) {
+            // done) completes the barrier phase after chunk c-1's, of the other
+            // parity; a wait for chunk c-1's parity begun after P of chunk c had
+            // completed would wait for chunk c+1's P, which needs this warp.  So
+            // chunk c-1's P is waited for here, before phi of chunk c is announced,
+            // and not again.
+            const bool waited = GATED && NP == 1 && c >= 1 && !f_prev;
+            if (waited && !warp_wait(cx, &sm->P_full[0], (c - 1) & 1)) {
                 ok = false;
                 break;
             }
@@ -720,9 +724,10 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
             if (GATED && f_cur) warp_arrive(&sm->sc_done[s]);   // nothing to scale after P
             // P of chunk c-1 was issued once phi of chunk c-1 was done and has
             // normally completed while phi of chunk c ran
-            if (GATED && c >= 1 && !f_prev && !scale_qk(c - 1)) ok = false;
+            if (GATED && c >= 1 && !f_prev && !scale_qk(c - 1, waited)) ok = false;
         }
-        if (GATED && ok && nch >= 1 && !f_last) scale_qk(nch - 1);
+        // the last chunk's P is the last phase: nothing can complete after it
+        if (GATED && ok && nch >= 1 && !f_last) scale_qk(nch - 1, false);
     }
 
     // ---------------------------------------------------------- teardown
