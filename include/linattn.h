@@ -195,8 +195,14 @@ la_status la_decode_step(const void *q, const void *k, const void *v, la_dtype d
                          float eps, void *y, la_stream_t stream);
 
 /*
- * la_backward_workspace_bytes -- device scratch that la_prefill_backward needs:
- * 4 * B*H*(3T + 1) bytes (FP32 per-token terms and one value per head).
+ * la_backward_workspace_bytes -- device scratch that la_prefill_backward needs for
+ * these sizes on the current device, for any r, dv <= 128 and either dtype: the
+ * FP32 per-token terms and one value per head (4 * B*H*(3T + 1) bytes), the maps
+ * of the z_t pass (4 * B*H*ceil(T/256)*257 bytes), and, when B*H whole-head CTAs
+ * would leave enough SMs idle and T is long enough, the two state passes of the
+ * sequence-segmented tensor-core sweeps (forward and reversed: per head and part
+ * or segment 4 * (128*128 + 128) bytes).  The size depends on the device's SM
+ * count; it is 0 only for invalid sizes.
  */
 size_t la_backward_workspace_bytes(int B, int H, int T);
 
@@ -222,12 +228,15 @@ size_t la_backward_workspace_bytes(int B, int H, int T);
  *   dS0, dz0  device FP32 [B,H,r,dv], [B,H,r] (written also when S0, z0 are NULL).
  *   workspace: >= la_backward_workspace_bytes device bytes, 16-byte aligned, owned by
  *          the caller; calls sharing it must be ordered.
- * Kernels: one pass for d_t and one for dd_t, then the three gradients as causal
- * linear attentions over chunks of 64 tokens (dq forward in time, dk and dv in
+ * Kernels: the z_t recurrence over segments of 256 tokens (maps, scan, products)
+ * for d_t, one pass for dd_t, then the three gradients as causal linear
+ * attentions over chunks of 64 tokens (dq forward in time, dk and dv in
  * reverse), then a reverse running sum for dalpha.  BF16 with r = dv = 128 runs
- * the three on the tensor cores (BF16 operands, FP32 accumulators and state);
- * the other shapes and FP32 run them as gated rank-1 recurrences in FP32 on the
- * CUDA cores.  Requires r, dv in {32, 64, 128}, T >= 1, 16-byte aligned
+ * the three on the tensor cores (BF16 operands, FP32 accumulators and state), and
+ * for few long sequences over sequence segments whose entering states a forward
+ * and a reversed state pass compute ([LA] "门控递推为什么能做并行 scan？"); the
+ * other shapes and FP32 run them as gated rank-1 recurrences in FP32 on the CUDA
+ * cores.  Requires r, dv in {32, 64, 128}, T >= 1, 16-byte aligned
  * token arrays (q, k, v, y, dy, dq, dk, dv_out), 4-byte aligned FP32 arrays
  * (dS_T 8-byte aligned).
  * Errors: LA_ERR_NULL, LA_ERR_SHAPE, LA_ERR_DTYPE, LA_ERR_ALIGN, LA_ERR_UNSUPPORTED,

@@ -59,6 +59,7 @@ constexpr int kStateCtaSetup = 2;    // set-up and pipeline fill of a state CTA,
 // (parts + segments) * heads below about 2 * SMs states of 66 KB); finer parts
 // are used only while they fit.
 constexpr size_t kMaxPlanWorkspace = size_t(32) << 20;
+constexpr size_t kMaxBwdPlanWorkspace = size_t(1) << 30;   // the backward's two state passes
 
 struct SegPlan {
     int dvs = 64;   // value columns per chunk-kernel CTA
@@ -98,27 +99,27 @@ int head_width(long long B, long long H, int dv, long long sms)
     return (5 * slices >= 4 * sms && slices <= sms) ? 64 : 128;
 }
 
-SegPlan seg_plan(int B, int H, int T, int dv)
+// Segments of nch chunks for `units` chunk-kernel CTAs per segment (one resident
+// per SM), and the parts of the state pass over nseg - 1 of them (one CTA per
+// (unit of the state pass, part), kStateCtasPerSm resident per SM), within
+// max_ws bytes of workspace (ws_of(nsub, nseg)).
+template <typename WsFn>
+SegPlan plan_segments(SegPlan p, long long units, long long state_units, int nch, long long max_ws, WsFn ws_of)
 {
-    SegPlan p;
-    p.dvs = head_width(B, H, dv, sm_count());
-    const long long units = (long long)B * H * (dv / p.dvs);   // chunk-kernel CTAs per segment
     const long long sms = sm_count();
-    const int nch = (T + 63) / 64;
     long long g = units > 0 ? sms / units : 0;
     g = g < nch / kMinSegChunks ? g : nch / kMinSegChunks;
     if (g < 2) return p;
     const int L = (int)((nch + g - 1) / g);
     const int G = (nch + L - 1) / L;
     if (G < 2) return p;
-    // parts per segment for the state pass (one CTA per (b, h, dvs-column slice, part))
-    const long long sunits = units * (G - 1);
+    const long long sunits = state_units * (G - 1);
     const long long slots = kStateCtasPerSm * sms;
     long long best_cost = -1;
     int best_n = 1;
     for (int n = 1; n <= L; ++n) {
         const int Ln = (L + n - 1) / n, parts = (L + Ln - 1) / Ln;
-        if (n > 1 && seg_workspace_bytes((G - 1) * parts, G, B, H, dv) > kMaxPlanWorkspace) break;
+        if (n > 1 && (long long)ws_of((G - 1) * parts, G) > max_ws) break;
         const long long waves = (sunits * n + slots - 1) / slots;
         const long long cost = waves * ((L + n - 1) / n + kStateCtaSetup);
         if (best_cost < 0 || cost < best_cost) {
@@ -133,6 +134,27 @@ SegPlan seg_plan(int B, int H, int T, int dv)
     p.sub_per_seg = (L + L1 - 1) / L1;
     p.nsub = (G - 1) * p.sub_per_seg;
     return p;
+}
+
+SegPlan seg_plan(int B, int H, int T, int dv)
+{
+    SegPlan p;
+    p.dvs = head_width(B, H, dv, sm_count());
+    const long long units = (long long)B * H * (dv / p.dvs);   // chunk-kernel CTAs per segment
+    return plan_segments(p, units, units, (T + 63) / 64, (long long)kMaxPlanWorkspace,
+                         [&](int nsub, int nseg) { return seg_workspace_bytes(nsub, nseg, B, H, dv); });
+}
+
+// The backward's tensor-core sweeps (one whole-head CTA per segment) over the
+// same kind of segments; their two state passes (forward for dq, reversed for
+// dk and dv) take whole heads too, and each has a workspace of the forward's layout.
+SegPlan bwd_seg_plan(int B, int H, int T)
+{
+    SegPlan p;
+    p.dvs = 128;
+    const long long units = (long long)B * H;
+    return plan_segments(p, units, units, (T + 63) / 64, (long long)kMaxBwdPlanWorkspace,
+                         [&](int nsub, int nseg) { return 2 * seg_workspace_bytes(nsub, nseg, B, H, 128); });
 }
 
 size_t seg_workspace_bytes(const SegPlan &p, int B, int H, int dv)
@@ -421,10 +443,16 @@ la_status la_decode_step(const void *q, const void *k, const void *v, la_dtype d
                                        reinterpret_cast<cudaStream_t>(stream)));
 }
 
+// Backward workspace: the per-token FP32 terms, then (when the tensor-core sweeps
+// run over segments) the forward and the reversed state passes' parts and
+// segment states, each in the prefill's layout.
+size_t bwd_base_bytes(int B, int H, int T) { return round_up(sizeof(float) * la::backward_workspace_floats(B, H, T), 256); }
+
 size_t la_backward_workspace_bytes(int B, int H, int T)
 {
     if (B < 1 || H < 1 || T < 1) return 0;
-    return sizeof(float) * la::backward_workspace_floats(B, H, T);
+    const SegPlan p = bwd_seg_plan(B, H, T);
+    return bwd_base_bytes(B, H, T) + 2 * seg_workspace_bytes(p.nsub, p.nseg, B, H, 128);
 }
 
 la_status la_prefill_backward(const void *q, const void *k, const void *v, la_dtype dtype, const float *alpha,
@@ -469,6 +497,15 @@ la_status la_prefill_backward(const void *q, const void *k, const void *v, la_dt
             !make_map_bf16(&maps[3], dy, planes, T, 128, 64, 64, sw128))
             return LA_ERR_CUDA;
         a.maps = maps;
+        const SegPlan p = bwd_seg_plan(B, H, T);
+        if (p.nseg > 1) {
+            a.nseg = p.nseg;
+            a.seg_chunks = p.seg_chunks;
+            a.sub_per_seg = p.sub_per_seg;
+            a.sub_chunks = p.sub_chunks;
+            a.nsub = p.nsub;
+            a.seg_ws = reinterpret_cast<float *>(static_cast<char *>(workspace) + bwd_base_bytes(B, H, T));
+        }
     }
     return from_cuda(la::launch_backward(a, B, dtype == LA_DTYPE_BF16, reinterpret_cast<cudaStream_t>(stream)));
 }

@@ -60,19 +60,19 @@ __device__ __forceinline__ float2 hi2(float4 a) { return make_float2(a.z, a.w); 
 
 // ------------------------------------------------------------ d_t and dd_t
 
-// z_t and the feature sum of d_t: one CTA of kZSeg warps per (b, h, 64
-// features); lane l holds features 2l, 2l + 1 (one 4-byte load per token for
-// BF16; at r = 32 the upper 16 lanes hold none).  z_t = alpha_t z_{t-1} + phi(k_t) is affine in z, so the sequence is cut
-// into kZSeg segments, one per warp.  Each warp first runs its segment from z = 0,
-// which gives the segment's map z -> P z + zs (P the product of its gates); the
-// maps of the segments before it, applied to z0 in order, give the warp its true
-// start, and it runs the segment again from there.  Tokens go in batches of
-// ZB(Tin) whose loads are all issued before the recurrence uses them; the batch's
-// products q~_{t,i} z_{t,i} are summed over the warp's features by a
-// reduce-scatter across the lanes (lane l ends with token l mod ZB) and added to
-// d_acc[t] (zeroed before).
-constexpr int kZSeg = 16;        // segments (warps) per sequence
-constexpr int kZFeat = 64;       // features per CTA
+// z_t and the feature sum of d_t, in three fully parallel steps over segments of
+// kZLen tokens (one warp per (b, h, 64 features, segment); lane l holds features
+// 2l, 2l + 1, at r = 32 the upper 16 lanes none).  z_t = alpha_t z_{t-1} + phi(k_t)
+// is affine in z: bwd_zmap_kernel runs each segment from z = 0, which gives its
+// map z -> P z + zs; bwd_zscan_kernel applies the maps in order to z0 and writes
+// the state entering every segment; bwd_zdot_kernel runs each segment again from
+// there.  Tokens go in batches of ZB(Tin) whose loads are all issued before the
+// recurrence uses them; the products q~_{t,i} z_{t,i} of a batch are summed over
+// the warp's features by a reduce-scatter across the lanes (lane l ends with
+// token l mod ZB) and added to d_acc[t] (zeroed before).
+constexpr int kZLen = 256;       // tokens per segment
+constexpr int kZFeat = 64;       // features per warp
+constexpr int kZWarps = 8;       // warps (segments) per CTA
 
 template <typename Tin> struct ZBatch { static constexpr int n = 32; };
 template <> struct ZBatch<float> { static constexpr int n = 16; };
@@ -104,31 +104,46 @@ __device__ __forceinline__ float lane_reduce_scatter(float (&v)[NB], int lane)
     return v[0];
 }
 
+// The warp's place: segment, head, first feature, whether its lane holds features.
+struct ZWarp {
+    int seg, bh, i0, ta, te;
+    bool live, valid;
+};
+
+__device__ __forceinline__ ZWarp z_warp(int r, int T, int nzs)
+{
+    ZWarp w;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    w.seg = blockIdx.y * kZWarps + warp;
+    w.bh = blockIdx.x;
+    w.i0 = blockIdx.z * kZFeat + 2 * lane;
+    w.live = w.i0 < r;
+    w.valid = w.seg < nzs;
+    w.ta = min(T, w.seg * kZLen);
+    w.te = min(T, w.ta + kZLen);
+    return w;
+}
+
+// 1: the map (P, zs) of every segment; zs [B*H][nzs][r], P [B*H][nzs].
 template <typename Tin>
-__global__ void __launch_bounds__(32 * kZSeg)
-bwd_z_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k, const float *__restrict__ alpha,
-             const float *__restrict__ z0, int T, int r, float *__restrict__ d_acc)
+__global__ void __launch_bounds__(32 * kZWarps)
+bwd_zmap_kernel(const Tin *__restrict__ k, const float *__restrict__ alpha, int T, int r, int nzs,
+                float *__restrict__ zs_out, float *__restrict__ P_out)
 {
     constexpr int NB = ZBatch<Tin>::n;
     using Raw = decltype(load_pair(static_cast<const Tin *>(nullptr)));
-    __shared__ float segP[kZSeg];
-    __shared__ float2 segZ[kZSeg][32];
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int nfg = (r + kZFeat - 1) / kZFeat, bh = blockIdx.x / nfg, i0 = (blockIdx.x % nfg) * kZFeat + 2 * lane;
-    const bool live = i0 < r;
-    const int len = (T + kZSeg - 1) / kZSeg;
-    const int ta = min(T, warp * len), te = min(T, ta + len);
-    const Tin *kp = k + (size_t)bh * T * r + i0, *qp = q + (size_t)bh * T * r + i0;
-    const float *ap = alpha ? alpha + (size_t)bh * T : nullptr;
-
-    // 1: the segment's map, from z = 0
+    const ZWarp w = z_warp(r, T, nzs);
+    if (!w.valid) return;   // whole warps only
+    const int lane = threadIdx.x & 31;
+    const Tin *kp = k + (size_t)w.bh * T * r + w.i0;
+    const float *ap = alpha ? alpha + (size_t)w.bh * T : nullptr;
     float2 z = make_float2(0.f, 0.f);
     float P = 1.f;
-    for (int t0 = ta; t0 < te; t0 += NB) {
-        const int nt = min(NB, te - t0);
+    for (int t0 = w.ta; t0 < w.te; t0 += NB) {
+        const int nt = min(NB, w.te - t0);
         Raw kr[NB];
 #pragma unroll
-        for (int t = 0; t < NB; ++t) kr[t] = (t < nt && live) ? load_pair(kp + (size_t)(t0 + t) * r) : Raw{};
+        for (int t = 0; t < NB; ++t) kr[t] = (t < nt && w.live) ? load_pair(kp + (size_t)(t0 + t) * r) : Raw{};
         const float al = (ap && lane < nt) ? ap[t0 + lane] : 1.f;
 #pragma unroll
         for (int t = 0; t < NB; ++t) {
@@ -141,25 +156,62 @@ bwd_z_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k, const float *
             }
         }
     }
-    if (lane == 0) segP[warp] = P;
-    segZ[warp][lane] = z;
-    __syncthreads();
+    const size_t sidx = (size_t)w.bh * nzs + w.seg;
+    if (w.live) *reinterpret_cast<float2 *>(zs_out + sidx * r + w.i0) = z;
+    if (blockIdx.z == 0 && lane == 0) P_out[sidx] = P;
+}
 
-    // 2: the true start of the segment, then the segment again with its products
-    z = (z0 && live) ? *reinterpret_cast<const float2 *>(z0 + (size_t)bh * r + i0) : make_float2(0.f, 0.f);
-    for (int u = 0; u < warp; ++u) {
-        const float pu = segP[u];
-        const float2 zu = segZ[u][lane];
-        z.x = pu * z.x + zu.x;
-        z.y = pu * z.y + zu.y;
+// 2: the state entering every segment, z_start [B*H][nzs][r]: one warp per (b, h,
+// 64 features) applies the maps in order to z0, loading 8 of them at a time.
+__global__ void __launch_bounds__(32)
+bwd_zscan_kernel(const float *__restrict__ z0, const float *__restrict__ zs, const float *__restrict__ P, int r,
+                 int nzs, float *__restrict__ z_start)
+{
+    const int lane = threadIdx.x, bh = blockIdx.x, i0 = blockIdx.y * kZFeat + 2 * lane;
+    const bool live = i0 < r;
+    float2 z = (z0 && live) ? *reinterpret_cast<const float2 *>(z0 + (size_t)bh * r + i0) : make_float2(0.f, 0.f);
+    for (int s0 = 0; s0 < nzs; s0 += 8) {
+        float2 m[8];
+        float p[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const size_t sidx = (size_t)bh * nzs + s0 + i;
+            const bool in = s0 + i < nzs;
+            m[i] = (in && live) ? *reinterpret_cast<const float2 *>(zs + sidx * r + i0) : make_float2(0.f, 0.f);
+            p[i] = in ? P[sidx] : 1.f;
+        }
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            if (s0 + i >= nzs) break;
+            if (live) *reinterpret_cast<float2 *>(z_start + ((size_t)bh * nzs + s0 + i) * r + i0) = z;
+            z.x = p[i] * z.x + m[i].x;
+            z.y = p[i] * z.y + m[i].y;
+        }
     }
-    for (int t0 = ta; t0 < te; t0 += NB) {
-        const int nt = min(NB, te - t0);
+}
+
+// 3: every segment again from its entering state, with the products summed into d_acc.
+template <typename Tin>
+__global__ void __launch_bounds__(32 * kZWarps)
+bwd_zdot_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k, const float *__restrict__ alpha, int T, int r,
+                int nzs, const float *__restrict__ z_start, float *__restrict__ d_acc)
+{
+    constexpr int NB = ZBatch<Tin>::n;
+    using Raw = decltype(load_pair(static_cast<const Tin *>(nullptr)));
+    const ZWarp w = z_warp(r, T, nzs);
+    if (!w.valid) return;   // whole warps only
+    const int lane = threadIdx.x & 31;
+    const Tin *kp = k + (size_t)w.bh * T * r + w.i0, *qp = q + (size_t)w.bh * T * r + w.i0;
+    const float *ap = alpha ? alpha + (size_t)w.bh * T : nullptr;
+    float2 z = w.live ? *reinterpret_cast<const float2 *>(z_start + ((size_t)w.bh * nzs + w.seg) * r + w.i0)
+                      : make_float2(0.f, 0.f);
+    for (int t0 = w.ta; t0 < w.te; t0 += NB) {
+        const int nt = min(NB, w.te - t0);
         Raw kr[NB], qr[NB];
 #pragma unroll
         for (int t = 0; t < NB; ++t) {
-            kr[t] = (t < nt && live) ? load_pair(kp + (size_t)(t0 + t) * r) : Raw{};
-            qr[t] = (t < nt && live) ? load_pair(qp + (size_t)(t0 + t) * r) : Raw{};
+            kr[t] = (t < nt && w.live) ? load_pair(kp + (size_t)(t0 + t) * r) : Raw{};
+            qr[t] = (t < nt && w.live) ? load_pair(qp + (size_t)(t0 + t) * r) : Raw{};
         }
         const float al = (ap && lane < nt) ? ap[t0 + lane] : 1.f;
         float prod[NB];
@@ -171,11 +223,11 @@ bwd_z_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k, const float *
                 const float2 kv = unpack_pair(kr[t]), qv = unpack_pair(qr[t]);
                 z.x = a * z.x + phi_f(kv.x);
                 z.y = a * z.y + phi_f(kv.y);
-                if (live) prod[t] = phi_f(qv.x) * z.x + phi_f(qv.y) * z.y;
+                if (w.live) prod[t] = phi_f(qv.x) * z.x + phi_f(qv.y) * z.y;
             }
         }
         const float sum = lane_reduce_scatter<NB>(prod, lane);
-        if (lane < nt) atomicAdd(&d_acc[(size_t)bh * T + t0 + lane], sum);
+        if (lane < nt) atomicAdd(&d_acc[(size_t)w.bh * T + t0 + lane], sum);
     }
 }
 
@@ -657,9 +709,21 @@ cudaError_t launch_bwd_t(const BackwardArgs &a, int B, cudaStream_t stream)
     // d accumulates the feature sums; tok_sum and fin accumulate dalpha terms
     cudaError_t e = cudaMemsetAsync(a.ws, 0, sizeof(float) * (3 * n + BH), stream);
     if (e != cudaSuccess) return e;
-    bwd_z_kernel<Tin><<<(unsigned)(BH * ((a.r + kZFeat - 1) / kZFeat)), 32 * kZSeg, 0, stream>>>(
-        static_cast<const Tin *>(a.q), static_cast<const Tin *>(a.k), a.alpha, a.z0, a.T, a.r, d);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    {
+        // z_t per segment of kZLen tokens: maps, scan, products
+        const int nzs = (a.T + kZLen - 1) / kZLen, nfg = (a.r + kZFeat - 1) / kZFeat;
+        // zs and z_start are read as pairs: they start on a 16-byte boundary
+        float *zP = fin + BH;
+        float *zs = a.ws + (3 * n + BH + (size_t)BH * nzs + 3) / 4 * 4, *zst = zs + (size_t)BH * nzs * a.r;
+        const dim3 grid((unsigned)BH, (nzs + kZWarps - 1) / kZWarps, nfg);
+        bwd_zmap_kernel<Tin><<<grid, 32 * kZWarps, 0, stream>>>(static_cast<const Tin *>(a.k), a.alpha, a.T, a.r, nzs, zs, zP);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+        bwd_zscan_kernel<<<dim3((unsigned)BH, nfg), 32, 0, stream>>>(a.z0, zs, zP, a.r, nzs, zst);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+        bwd_zdot_kernel<Tin><<<grid, 32 * kZWarps, 0, stream>>>(static_cast<const Tin *>(a.q), static_cast<const Tin *>(a.k),
+                                                                a.alpha, a.T, a.r, nzs, zst, d);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    }
     bwd_dd_kernel<Tin><<<152 * 8, 256, 0, stream>>>(static_cast<const Tin *>(a.y), static_cast<const Tin *>(a.dy),
                                                       a.dv, (long long)n, a.eps, d, dd);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
@@ -675,6 +739,37 @@ cudaError_t launch_bwd_t(const BackwardArgs &a, int B, cudaStream_t stream)
             t.tok_sum = a.alpha ? tok_sum : nullptr; t.fin = a.alpha ? fin : nullptr;
             t.dS0 = a.dS0; t.dz0 = a.dz0;
             t.H = a.H; t.T = a.T; t.status = a.status; t.limit_ns = a.limit_ns;
+            if (a.nseg > 1) {
+                // the states entering each segment: the prefill's state pass and scan in
+                // forward time (for dq), and their reversed form over (phi(q), dn, dd)
+                // from dS_T, dz_T (for dk and dv); each pass's workspace is A [nsub][BH]
+                // (256-byte aligned), the parts' maps [nsub][BH][state], the segment
+                // states [nseg][BH][state]
+                const size_t state = (size_t)128 * 128 + 128;
+                const size_t a_floats = ((size_t)a.nsub * BH * 4 + 255) / 256 * 64;
+                const size_t pass_floats = a_floats + (size_t)a.nsub * BH * state + (size_t)a.nseg * BH * state;
+                float *pf = a.seg_ws, *pr = a.seg_ws + pass_floats;
+                StateTcArgs sa;
+                sa.alpha = a.alpha; sa.H = a.H; sa.T = a.T; sa.dv = 128;
+                sa.nsub = a.nsub; sa.sub_per_seg = a.sub_per_seg; sa.sub_chunks = a.sub_chunks;
+                sa.seg_chunks = a.seg_chunks; sa.status = a.status; sa.wait_limit_ns = a.limit_ns;
+                const bool gated = a.alpha != nullptr;
+                // forward: segments 0 .. nseg-2 over (phi(k), v)
+                sa.A = pf; sa.dS = pf + a_floats; sa.seg_first = 0;
+                if ((e = launch_state_tc(a.maps[1], a.maps[2], sa, B, gated, 128, stream)) != cudaSuccess) return e;
+                float *Sf = pf + a_floats + (size_t)a.nsub * BH * state;
+                if ((e = launch_seg_scan(a.S0, a.z0, sa.A, sa.dS, Sf, BH, 128, a.nsub, a.sub_per_seg, a.nseg, stream)) !=
+                    cudaSuccess)
+                    return e;
+                // reversed: segments 1 .. nseg-1 over (phi(q), dy / d, dd)
+                sa.A = pr; sa.dS = pr + a_floats; sa.seg_first = 1; sa.d = d; sa.dd = dd;
+                if ((e = launch_state_tc(a.maps[0], a.maps[3], sa, B, gated, 128, stream, true)) != cudaSuccess) return e;
+                float *Sr = pr + a_floats + (size_t)a.nsub * BH * state;
+                if ((e = launch_seg_scan(a.dS_T, a.dz_T, sa.A, sa.dS, Sr, BH, 128, a.nsub, a.sub_per_seg, a.nseg, stream,
+                                         true)) != cudaSuccess)
+                    return e;
+                t.nseg = a.nseg; t.seg_chunks = a.seg_chunks; t.seg_state_f = Sf; t.seg_state_r = Sr;
+            }
             if ((e = launch_bwd_tc(a.maps, t, B, a.alpha != nullptr, stream)) != cudaSuccess) return e;
             if (a.alpha && a.dalpha) {
                 bwd_dalpha_kernel<<<BH, 128, 0, stream>>>(tok_sum, fin, a.alpha, a.T, a.dalpha);
@@ -704,7 +799,13 @@ cudaError_t launch_bwd_t(const BackwardArgs &a, int B, cudaStream_t stream)
 
 }  // namespace
 
-size_t backward_workspace_floats(int B, int H, int T) { return (size_t)B * H * ((size_t)3 * T + 1); }
+// d, dd, tok_sum [B*H*T], fin [B*H], then the z pass's segment maps: P [B*H][nzs],
+// zs and z_start [B*H][nzs][r] (r <= 128)
+size_t backward_workspace_floats(int B, int H, int T)
+{
+    const size_t BH = (size_t)B * H, nzs = ((size_t)T + kZLen - 1) / kZLen;
+    return BH * ((size_t)3 * T + 1) + BH * nzs * (1 + 2 * 128) + 4;
+}
 
 cudaError_t launch_backward(const BackwardArgs &a, int B, bool bf16, cudaStream_t stream)
 {

@@ -111,7 +111,7 @@ static_assert(smem_bytes<kModeDq>() <= 232448 && smem_bytes<kModeDk>() <= 232448
 __device__ __forceinline__ float phi_f(float x) { return x > 0.f ? x + 1.f : __expf(x); }
 __device__ __forceinline__ float dphi_f(float x) { return x > 0.f ? 1.f : __expf(x); }
 
-// One sweep (MODE) of one head (blockIdx.y, blockIdx.z).
+// One sweep (MODE) of one head (blockIdx.y, blockIdx.z), or of segment blockIdx.x of it.
 template <int MODE, bool GATED>
 __device__ __forceinline__ void
 bwd_sweep(const CUtensorMap &map_q, const CUtensorMap &map_k, const CUtensorMap &map_v, const CUtensorMap &map_dy,
@@ -129,10 +129,15 @@ bwd_sweep(const CUtensorMap &map_q, const CUtensorMap &map_k, const CUtensorMap 
     const int h = blockIdx.y, b = blockIdx.z;
     const int bh = b * args.H + h;
     const int T = args.T;
-    const int nch = (T + kC - 1) / kC;
+    // this CTA's chunks: segment blockIdx.x of the head's sequence (all of it when nseg == 1)
+    const int seg = blockIdx.x, nseg = gridDim.x;
+    const int nch_all = (T + kC - 1) / kC;
+    const int c_begin = nseg > 1 ? seg * args.seg_chunks : 0;
+    const int c_end = nseg > 1 ? min(nch_all, c_begin + args.seg_chunks) : nch_all;
+    const int nch = max(0, c_end - c_begin);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     // chunk of iteration c (reversed time walks the chunks from the end)
-    auto chunk_of = [&](int c) { return REV ? nch - 1 - c : c; };
+    auto chunk_of = [&](int c) { return REV ? c_end - 1 - c : c_begin + c; };
     auto stage_ptr = [&](int s) { return base + s * L::kStageBytes; };
     // the tensor maps of the query, key and value tiles
     const CUtensorMap *mq = MODE == kModeDq ? &map_dy : MODE == kModeDk ? &map_v : &map_k;
@@ -353,15 +358,25 @@ bwd_sweep(const CUtensorMap &map_q, const CUtensorMap &map_k, const CUtensorMap 
         const uint32_t tH = tmem + lane_base + L::kColH + qq * 32;
         const uint32_t tz = tmem + lane_base + L::kColH + 128;    // z or g (dq, dk)
         {
-            // initial state: [S0 | z0] (dq), [dS_T | dz_T] (dk), dS_T (dv), or zero
+            // initial state: [S0 | z0] (dq), [dS_T | dz_T] (dk), dS_T (dv), or zero; with
+            // segments, the state entering the segment (from the left for dq, from the
+            // right for dk and dv), which the state passes wrote [S (128 x 128) | z]
             const float *S_init = MODE == kModeDq ? args.S0 : args.dS_T;
             const float *z_init = MODE == kModeDq ? args.z0 : args.dz_T;
+            if (S_init) S_init += (size_t)bh * kR * 128;
+            if (z_init) z_init += (size_t)bh * kR;
+            if (nseg > 1) {
+                const size_t state_len = (size_t)kR * 128 + kR;
+                const int BH = gridDim.z * args.H;
+                S_init = (MODE == kModeDq ? args.seg_state_f : args.seg_state_r) + ((size_t)seg * BH + bh) * state_len;
+                z_init = S_init + (size_t)kR * 128;
+            }
             float S[32];
-            const float *src = S_init ? S_init + ((size_t)bh * kR + srow) * 128 + qq * 32 : nullptr;
+            const float *src = S_init ? S_init + (size_t)srow * 128 + qq * 32 : nullptr;
 #pragma unroll
             for (int j = 0; j < 32; ++j) S[j] = src ? src[j] : 0.f;
             tc_st_32x32b_x32(tH, S);
-            if (L::kWblk && qq == 0) tc_st_32x32b_x1(tz, z_init ? z_init[(size_t)bh * kR + srow] : 0.f);
+            if (L::kWblk && qq == 0) tc_st_32x32b_x1(tz, z_init ? z_init[srow] : 0.f);
             tc_wait_st();
         }
         float fin_acc = 0.f;
@@ -456,14 +471,15 @@ bwd_sweep(const CUtensorMap &map_q, const CUtensorMap &map_k, const CUtensorMap 
                 __syncwarp();
                 warp_arrive(&sm->ops_full[bb]);
             } else {
-                // c == nch: the final state
-                if (MODE == kModeDk) {
+                // c == nch: the final state (of the whole sequence only in the first
+                // segment for dk, in the last for dq)
+                if (MODE == kModeDk && seg == 0) {
                     // dS0 = alpha_1 G_1, dz0 = alpha_1 g_1: the state carried past the first chunk
                     float *dst = args.dS0 + ((size_t)bh * kR + srow) * 128 + qq * 32;
 #pragma unroll
                     for (int j = 0; j < 32; j += 4) *reinterpret_cast<float4 *>(dst + j) = make_float4(S[j], S[j + 1], S[j + 2], S[j + 3]);
                     if (qq == 0) args.dz0[(size_t)bh * kR + srow] = zr;
-                } else if (MODE == kModeDq && GATED && (args.dS_T || args.dz_T)) {
+                } else if (MODE == kModeDq && GATED && seg == nseg - 1 && (args.dS_T || args.dz_T)) {
                     // <dS_T, S_T> + <dz_T, z_T> over this thread's entries
                     if (args.dS_T) {
                         const float *g = args.dS_T + ((size_t)bh * kR + srow) * 128 + qq * 32;
@@ -626,7 +642,7 @@ cudaError_t launch_bwd_tc(const CUtensorMap *maps, const BwdTcArgs &a, int B, bo
     for (int m = 0; m < 3; ++m) {
         cudaError_t e = set_smem_once(kerns[gated][m], bytes[m], attr_set[gated][m]);
         if (e != cudaSuccess) return e;
-        kerns[gated][m]<<<dim3(1, a.H, B), kThreads, bytes[m], stream>>>(maps[0], maps[1], maps[2], maps[3], a);
+        kerns[gated][m]<<<dim3(a.nseg, a.H, B), kThreads, bytes[m], stream>>>(maps[0], maps[1], maps[2], maps[3], a);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
     return cudaSuccess;

@@ -87,19 +87,27 @@ struct StateTcArgs {
     int sub_per_seg;      //   each split into sub_per_seg parts
     int sub_chunks;       // chunks per part (the last part of a segment may be shorter)
     int seg_chunks;       // chunks per output segment
+    int seg_first = 0;    // segment of the first part (the reversed pass covers segments 1 .. nseg-1)
+    const float *d = nullptr;    // reversed pass: d_t and dd_t [B*H*T] of the backward
+    const float *dd = nullptr;
     int *status;          // device status word
     unsigned long long wait_limit_ns;
 };
 
 // grid (dv/dvs, H, B*nsub) with dvs (64 or 128) value columns per CTA; tensor maps
 // k over [B*H, T, 128] and v over [B*H, T, dv] as for launch_prefill_tc.
+// rev: the backward's reversed pass (dvs 128, seg_first 1): k is the map of q,
+// v the map of dy, and d, dd are given; the part maps carry [G | g].
 cudaError_t launch_state_tc(const CUtensorMap &map_k, const CUtensorMap &map_v, const StateTcArgs &a, int B,
-                            bool gated, int dvs, cudaStream_t stream);
+                            bool gated, int dvs, cudaStream_t stream, bool rev = false);
 
 // S_start[g][bh] (S then z) for g < nseg: S0/z0 (zero if null) carried through the
-// sub-segment maps S -> A S + dS in order.
+// sub-segment maps S -> A S + dS in order.  rev: the maps of the reversed pass,
+// applied from the last part backwards to S0/z0 (dL/dS_T, dL/dz_T), give the
+// state entering segment g from the right in S_start[g].
 cudaError_t launch_seg_scan(const float *S0, const float *z0, const float *A, const float *dS, float *S_start,
-                            int BH, int dv, int nsub, int sub_per_seg, int nseg, cudaStream_t stream);
+                            int BH, int dv, int nsub, int sub_per_seg, int nseg, cudaStream_t stream,
+                            bool rev = false);
 
 // Exact FP32 token recurrence (CUDA cores), r, dv <= 256.
 cudaError_t launch_prefill_f32(const float *q, const float *k, const float *v, const float *alpha,
@@ -134,6 +142,12 @@ struct BackwardArgs {
     // of 64 x 64, 128-byte swizzle); the three sweeps then run on the tensor cores.
     // nullptr: the sweeps run on CUDA cores.
     const CUtensorMap *maps;
+    // Tensor-core sweeps over sequence segments (nseg > 1): each CTA takes
+    // seg_chunks chunks of one head; the entering states come from the state
+    // passes (forward for dq, reversed for dk and dv), each split into nsub parts
+    // (sub_per_seg per segment, sub_chunks chunks each), in seg_ws.
+    int nseg = 1, seg_chunks = 0, sub_per_seg = 1, sub_chunks = 0, nsub = 0;
+    float *seg_ws = nullptr;
 };
 size_t backward_workspace_floats(int B, int H, int T);
 
@@ -148,6 +162,10 @@ struct BwdTcArgs {
     float *tok_sum, *fin;                        // [B*H*T], [B*H] (accumulated), or nullptr
     float *dS0, *dz0;                            // [B,H,128,128], [B,H,128]
     int H, T;
+    // nseg > 1: CTA (g, h, b) takes chunks g * seg_chunks .. of its head and starts
+    // from seg_state_f (dq) or seg_state_r (dk, dv) [nseg][B*H][128*128 + 128]
+    int nseg = 1, seg_chunks = 0;
+    const float *seg_state_f = nullptr, *seg_state_r = nullptr;
     int *status;
     unsigned long long limit_ns;
 };

@@ -12,6 +12,17 @@
 // rounding); seg_scan_kernel then applies the maps in sequence order to S0, z0
 // and writes the start state of every output segment, from which the prefill
 // kernel processes the segments in parallel.
+//
+// The backward's key-side sweeps carry, in reversed time, the state
+//     G_t = phi(q_t) dn_t^T + alpha_{t+1} G_{t+1},   g_t = dd_t phi(q_t) + alpha_{t+1} g_{t+1}
+// (dn_t = dy_t / d_t, dd_t = -(dy_t . y_t) / d_t), which is affine in the same
+// way.  The REV form of the state pass runs a sub-segment's chunks from its last
+// to its first with key phi(q), value dn and dd in place of the column of ones,
+// each token weighted by the product Gamma_t of the gates from the chunk's start
+// to the token (the decay back to the chunk's start); its map sends the state
+// entering the sub-segment from the right to the state it hands to the left.
+// The scan then applies the maps from the end of the sequence backwards,
+// starting from dL/dS_T, dL/dz_T.
 
 #include "tc_common.cuh"
 
@@ -33,16 +44,27 @@ constexpr int kMaxStages = 4;
 
 // Two CTAs are resident per SM (each at most 113 KB of shared memory), so that
 // the many short parts of a segment stream at the bandwidth of the SM.
-template <bool GATED, int DVS>
+// Per-chunk scalars of the reversed pass: 1 / d_t and dd_t (0 for rows past T).
+struct alignas(16) RevRing {
+    float invd[kAux][kC];
+    float dd[kAux][kC];
+};
+
+// REV: the reversed-time pass of the backward (DVS 128 only): the column block
+// holds dd_t, so each stage carries its own after the value tile.
+template <bool GATED, int DVS, bool REV = false>
 struct SCfg {
     static_assert(DVS == 64 || DVS == 128, "value columns per CTA");
-    static constexpr int kStages = DVS == 128 ? (GATED ? 2 : 3) : (GATED ? 3 : 4);
+    static_assert(!REV || DVS == 128, "the reversed pass takes whole heads");
+    static constexpr int kStages = REV ? 2 : DVS == 128 ? (GATED ? 2 : 3) : (GATED ? 3 : 4);
     static constexpr uint32_t kTileV = (DVS / 64) * kBlkV;
-    static constexpr uint32_t kOffK = 0, kOffV = kTileK, kStageBytes = kTileK + kTileV;
+    static constexpr uint32_t kOffK = 0, kOffV = kTileK, kOffStageCol = kTileK + kTileV;
+    static constexpr uint32_t kStageBytes = kTileK + kTileV + (REV ? kTileOnes : 0);
     static_assert(kStageBytes % 1024 == 0, "stage tiles stay 1024-byte aligned");
     static constexpr uint32_t kOffOnes = kStages * kStageBytes;
-    static constexpr uint32_t kOffGate = kOffOnes + kTileOnes;
-    static constexpr uint32_t kOffSmall = kOffGate + (GATED ? sizeof(GateRing) : 0);
+    static constexpr uint32_t kOffGate = kOffOnes + (REV ? 0 : kTileOnes);
+    static constexpr uint32_t kOffRev = kOffGate + (GATED ? sizeof(GateRing) : 0);
+    static constexpr uint32_t kOffSmall = kOffRev + (REV ? sizeof(RevRing) : 0);
     static constexpr uint32_t kTmemCols = DVS == 128 ? 256 : 128;   // [S | z]: DVS + 16 columns (z is column DVS)
 };
 
@@ -53,25 +75,28 @@ struct alignas(16) SmallS {
     int abort_flag;
 };
 
-template <bool GATED, int DVS>
-__host__ __device__ constexpr uint32_t smem_bytes() { return SCfg<GATED, DVS>::kOffSmall + sizeof(SmallS) + 1024; }
+template <bool GATED, int DVS, bool REV = false>
+__host__ __device__ constexpr uint32_t smem_bytes() { return SCfg<GATED, DVS, REV>::kOffSmall + sizeof(SmallS) + 1024; }
 // two resident CTAs per SM: 2 x (bytes + 1 KB reserved) within the SM's 228 KB
 static_assert(2 * (smem_bytes<true, 64>() + 1024) <= 233472, "shared memory budget");
 static_assert(2 * (smem_bytes<false, 64>() + 1024) <= 233472, "shared memory budget");
 static_assert(2 * (smem_bytes<true, 128>() + 1024) <= 233472, "shared memory budget");
 static_assert(2 * (smem_bytes<false, 128>() + 1024) <= 233472, "shared memory budget");
+static_assert(2 * (smem_bytes<true, 128, true>() + 1024) <= 233472, "shared memory budget");
+static_assert(2 * (smem_bytes<false, 128, true>() + 1024) <= 233472, "shared memory budget");
 
-template <bool GATED, int DVS>
+template <bool GATED, int DVS, bool REV>
 __global__ void __launch_bounds__(kThreads, 2)
 state_tc_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant__ CUtensorMap map_v,
                 const StateTcArgs args)
 {
-    using L = SCfg<GATED, DVS>;
+    using L = SCfg<GATED, DVS, REV>;
     constexpr int NST = L::kStages;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *base = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     SmallS *sm = reinterpret_cast<SmallS *>(base + L::kOffSmall);
     GateRing *gr = reinterpret_cast<GateRing *>(base + L::kOffGate);   // gated only
+    RevRing *rr = reinterpret_cast<RevRing *>(base + L::kOffRev);      // REV only
     Ctx cx{&sm->abort_flag, args.wait_limit_ns, args.status};
 
     // grid: (dv slice, h, b * nsub + m); sub-segment m is part j of output segment g
@@ -80,17 +105,19 @@ state_tc_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant
     const int BH = (gridDim.z / args.nsub) * args.H;
     const int bh = b * args.H + h;
     const int T = args.T;
-    const int g = m / args.sub_per_seg, j = m % args.sub_per_seg;
+    const int g = m / args.sub_per_seg + args.seg_first, j = m % args.sub_per_seg;
     const int cs = g * args.seg_chunks + j * args.sub_chunks;                 // first chunk
-    const int nch = max(0, min(cs + args.sub_chunks, (g + 1) * args.seg_chunks) - cs);
+    const int nch = max(0, min(min(cs + args.sub_chunks, (g + 1) * args.seg_chunks), (args.T + kC - 1) / kC) - cs);
     const int tb = cs * kC;                                                   // first token
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    // first token of the c-th chunk processed (REV: from the sub-segment's end)
+    auto chunk_t0 = [&](int c) { return tb + (REV ? nch - 1 - c : c) * kC; };
     auto stage_ptr = [&](int s) { return base + s * L::kStageBytes; };
 
     // ------------------------------------------------------------ set-up
     if (threadIdx.x == 0) {
         for (int s = 0; s < NST; ++s) {
-            mbar_init(&sm->full[s], GATED ? 2 : 1);   // TMA bytes (+ gate data)
+            mbar_init(&sm->full[s], (GATED || REV) ? 2 : 1);   // TMA bytes (+ gate data, scalars)
             mbar_init(&sm->empty[s], 1);
             mbar_init(&sm->phi_done[s], kPhiWarps);
         }
@@ -103,11 +130,19 @@ state_tc_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant
         tma_prefetch_desc(&map_k);
         tma_prefetch_desc(&map_v);
     }
-    for (int i = threadIdx.x; i < (int)kTileOnes / 16; i += kThreads)
-        reinterpret_cast<uint4 *>(base + L::kOffOnes)[i] = make_uint4(0, 0, 0, 0);
-    __syncthreads();
-    if (threadIdx.x < kC)   // element (column 0, token row k): 16-byte chunk 0 of row k after the swizzle
-        *reinterpret_cast<uint16_t *>(base + L::kOffOnes + sw128_offset(threadIdx.x, 0)) = 0x3F80u;
+    if (REV) {
+        // the column blocks of the stages: zero but for column 0, written per chunk
+        for (int i = threadIdx.x; i < NST * (int)(kTileOnes / 16); i += kThreads)
+            reinterpret_cast<uint4 *>(base + (i / (kTileOnes / 16)) * L::kStageBytes + L::kOffStageCol)[i % (kTileOnes / 16)] =
+                make_uint4(0, 0, 0, 0);
+        __syncthreads();
+    } else {
+        for (int i = threadIdx.x; i < (int)kTileOnes / 16; i += kThreads)
+            reinterpret_cast<uint4 *>(base + L::kOffOnes)[i] = make_uint4(0, 0, 0, 0);
+        __syncthreads();
+        if (threadIdx.x < kC)   // element (column 0, token row k): 16-byte chunk 0 of row k after the swizzle
+            *reinterpret_cast<uint16_t *>(base + L::kOffOnes + sw128_offset(threadIdx.x, 0)) = 0x3F80u;
+    }
     fence_proxy_async_smem();
     if (warp == kWarpMma) {
         tmem_alloc(&sm->tmem_base, L::kTmemCols);
@@ -137,12 +172,18 @@ state_tc_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant
         int issued = 0;
         for (int c = 0; c < nch; ++c) {
             const int s = c % NST;
-            const int t0 = tb + c * kC;
+            const int t0 = chunk_t0(c);
             float a0 = 1.f, a1 = 1.f;
             if (GATED) {
                 const float *ap = args.alpha + (size_t)bh * T;
                 if (t0 + 2 * lane < T) a0 = ap[t0 + 2 * lane];
                 if (t0 + 2 * lane + 1 < T) a1 = ap[t0 + 2 * lane + 1];
+            }
+            float2 dv2 = make_float2(1.f, 1.f), dd2 = make_float2(0.f, 0.f);
+            if (REV) {
+                const float *dp = args.d + (size_t)bh * T, *ddp = args.dd + (size_t)bh * T;
+                if (t0 + 2 * lane < T) { dv2.x = dp[t0 + 2 * lane]; dd2.x = ddp[t0 + 2 * lane]; }
+                if (t0 + 2 * lane + 1 < T) { dv2.y = dp[t0 + 2 * lane + 1]; dd2.y = ddp[t0 + 2 * lane + 1]; }
             }
             if (c >= NST && !warp_wait(cx, &sm->empty[s], ((c / NST) - 1) & 1)) break;
             if (GATED && c >= kAux && !warp_wait(cx, &sm->aux_empty[c % kAux], ((c / kAux) - 1) & 1)) break;
@@ -156,7 +197,7 @@ state_tc_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant
                 for (int vb = 0; vb < DVS / 64; ++vb)
                     tma_load_3d(st + L::kOffV + vb * kBlkV, &map_v, &sm->full[s], slice * DVS + vb * 64, t0, bh);
                 if (c + NST < nch) {   // warm L2 for the load that reuses this stage
-                    const int tp = t0 + NST * kC;
+                    const int tp = chunk_t0(c + NST);
                     if (slice == 0) {
                         tma_prefetch_l2_3d(&map_k, 0, tp, bh);
                         tma_prefetch_l2_3d(&map_k, 64, tp, bh);
@@ -165,10 +206,12 @@ state_tc_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant
                     for (int vb = 0; vb < DVS / 64; ++vb) tma_prefetch_l2_3d(&map_v, slice * DVS + vb * 64, tp, bh);
                 }
             }
-            if (GATED) {
-                gate_products(a0, a1, lane, c % kAux, gr);
-                warp_arrive(&sm->full[s]);
+            if (GATED) gate_products(a0, a1, lane, c % kAux, gr);
+            if (REV) {
+                *reinterpret_cast<float2 *>(&rr->invd[c % kAux][2 * lane]) = make_float2(1.f / dv2.x, 1.f / dv2.y);
+                *reinterpret_cast<float2 *>(&rr->dd[c % kAux][2 * lane]) = dd2;
             }
+            if (GATED || REV) warp_arrive(&sm->full[s]);
             issued = c + 1;
         }
         if (lane == 0 && aborted(cx)) {
@@ -190,10 +233,10 @@ state_tc_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant
             constexpr uint32_t idDS1 = idesc_bf16_f32(128, 16, true, true);
             constexpr uint32_t kHi128 = desc_hi(1024, 2);
             const uint32_t aOnes = smem_u32(base + L::kOffOnes);
-            const uint32_t onesLo = desc_lo(aOnes, kBlkV);
             for (int c = 0; c < nch && !aborted(cx); ++c) {
                 const int s = c % NST;
                 const uint32_t st = smem_u32(stage_ptr(s));
+                const uint32_t onesLo = desc_lo(REV ? st + L::kOffStageCol : aOnes, kBlkV);
                 if (!wait(cx, &sm->phi_done[s], (c / NST) & 1)) break;
                 if (GATED && !wait(cx, &sm->S_read, c & 1)) break;
                 tc_fence_after();
@@ -277,19 +320,29 @@ state_tc_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant
         }
     } else if (is_phi_warp(warp)) {
         // ------------------------------------------------------ phi warps
-        // phi(K) in place, with a gate times w_j on key row j; rows past the end
-        // of the sequence become 0
+        // phi(K) in place, with a gate times w_j on key row j (REV: times Gamma_j);
+        // rows past the end of the sequence become 0.  REV: the rows of V (dy)
+        // times 1 / d_t, and dd_t in column 0 of the stage's column block.
         const int pp = phi_index(warp) * 32 + lane;
         for (int c = 0; c < nch; ++c) {
             const int s = c % NST;
             if (!warp_wait(cx, &sm->full[s], (c / NST) & 1)) break;
-            const int nvalid = min(kC, T - tb - c * kC);
+            const int nvalid = min(kC, T - chunk_t0(c));
             uint4 *kt = reinterpret_cast<uint4 *>(stage_ptr(s) + L::kOffK);
+            const float *kw = REV ? gr->gG[c % kAux] : gr->gw[c % kAux];
             for (int ci = pp; ci < (int)kTileK / 16; ci += kPhiThreads) {
                 const int row = (ci & 511) >> 3;   // 8 chunks per 128-byte row, 64 rows per block
                 uint4 v = row < nvalid ? phi8(kt[ci]) : make_uint4(0, 0, 0, 0);
-                if (GATED) v = scale8(v, gr->gw[c % kAux][row]);
+                if (GATED) v = scale8(v, kw[row]);
                 kt[ci] = v;
+            }
+            if (REV) {
+                uint4 *vt = reinterpret_cast<uint4 *>(stage_ptr(s) + L::kOffV);
+                const float *invd = rr->invd[c % kAux];
+                for (int ci = pp; ci < (int)L::kTileV / 16; ci += kPhiThreads) vt[ci] = scale8(vt[ci], invd[(ci & 511) >> 3]);
+                if (pp < kC)
+                    *reinterpret_cast<uint16_t *>(stage_ptr(s) + L::kOffStageCol + sw128_offset(pp, 0)) =
+                        __bfloat16_as_ushort(__float2bfloat16_rn(rr->dd[c % kAux][pp]));
             }
             fence_proxy_async_smem();
             warp_arrive(&sm->phi_done[s]);
@@ -305,11 +358,12 @@ state_tc_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant
     }
 }
 
-// S_start[g] for every output segment g: the state before its first chunk.
-// One thread per 4 consecutive elements of a head's state (S then z); a thread
-// issues the loads of up to 8 parts before it runs their affine maps in order.
+// S_start[g] for every output segment g: the state before its first chunk
+// (rev: the state entering it from the right).  One thread per 4 consecutive
+// elements of a head's state (S then z); a thread issues the loads of up to 8
+// parts before it runs their affine maps in order (rev: from the last part).
 __global__ void seg_scan_kernel(const float *S0, const float *z0, const float *A, const float *dS, float *S_start,
-                                int BH, int dv, int nsub, int sub_per_seg, int nseg)
+                                int BH, int dv, int nsub, int sub_per_seg, int nseg, bool rev)
 {
     const int bh = blockIdx.y;
     const int e = 4 * (blockIdx.x * blockDim.x + threadIdx.x);
@@ -321,28 +375,39 @@ __global__ void seg_scan_kernel(const float *S0, const float *z0, const float *A
     const float *src0 = e < s_len ? (S0 ? S0 + (size_t)bh * s_len + e : nullptr)
                                   : (z0 ? z0 + (size_t)bh * kR + (e - s_len) : nullptr);
     s = src0 ? make_float4(src0[0], src0[1], src0[2], src0[3]) : make_float4(0.f, 0.f, 0.f, 0.f);
-    *reinterpret_cast<float4 *>(S_start + (size_t)bh * state_len + e) = s;
-    for (int m0 = 0; m0 < nsub; m0 += 8) {
+    *reinterpret_cast<float4 *>(S_start + ((size_t)(rev ? nseg - 1 : 0) * BH + bh) * state_len + e) = s;
+    for (int i0 = 0; i0 < nsub; i0 += 8) {
         float4 d[8];
         float a[8];
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-            const int m = m0 + i;
-            d[i] = m < nsub ? *reinterpret_cast<const float4 *>(dS + ((size_t)m * BH + bh) * state_len + e)
-                            : make_float4(0.f, 0.f, 0.f, 0.f);
-            a[i] = m < nsub ? A[(size_t)m * BH + bh] : 1.f;
+            const int m = rev ? nsub - 1 - (i0 + i) : i0 + i;
+            d[i] = i0 + i < nsub ? *reinterpret_cast<const float4 *>(dS + ((size_t)m * BH + bh) * state_len + e)
+                                 : make_float4(0.f, 0.f, 0.f, 0.f);
+            a[i] = i0 + i < nsub ? A[(size_t)m * BH + bh] : 1.f;
         }
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-            const int m = m0 + i;
-            if (m >= nsub) break;
+            if (i0 + i >= nsub) break;
             s.x = fmaf(a[i], s.x, d[i].x);
             s.y = fmaf(a[i], s.y, d[i].y);
             s.z = fmaf(a[i], s.z, d[i].z);
             s.w = fmaf(a[i], s.w, d[i].w);
-            if ((m + 1) % sub_per_seg == 0) {
-                const int g = (m + 1) / sub_per_seg;
-                if (g < nseg) *reinterpret_cast<float4 *>(S_start + ((size_t)g * BH + bh) * state_len + e) = s;
+            if (!rev) {
+                // part m done: after the last part of segment m / sub_per_seg comes segment + 1
+                const int m = i0 + i;
+                if ((m + 1) % sub_per_seg == 0) {
+                    const int g = (m + 1) / sub_per_seg;
+                    if (g < nseg) *reinterpret_cast<float4 *>(S_start + ((size_t)g * BH + bh) * state_len + e) = s;
+                }
+            } else {
+                // part m (of segment m / sub_per_seg + 1) done: at its segment's first part,
+                // the state entering the segment before it from the right
+                const int m = nsub - 1 - (i0 + i);
+                if (m % sub_per_seg == 0) {
+                    const int g = m / sub_per_seg;
+                    *reinterpret_cast<float4 *>(S_start + ((size_t)g * BH + bh) * state_len + e) = s;
+                }
             }
         }
     }
@@ -351,17 +416,19 @@ __global__ void seg_scan_kernel(const float *S0, const float *z0, const float *A
 }  // namespace
 
 cudaError_t launch_state_tc(const CUtensorMap &map_k, const CUtensorMap &map_v, const StateTcArgs &a, int B,
-                            bool gated, int dvs, cudaStream_t stream)
+                            bool gated, int dvs, cudaStream_t stream, bool rev)
 {
-    if (dvs != 64 && dvs != 128) return cudaErrorInvalidValue;
+    if ((dvs != 64 && dvs != 128) || (rev && (dvs != 128 || !a.d || !a.dd))) return cudaErrorInvalidValue;
     const dim3 grid(a.dv / dvs, a.H, B * a.nsub);
     using KernFn = void (*)(const CUtensorMap, const CUtensorMap, const StateTcArgs);
-    const int v = (gated ? 1 : 0) + (dvs == 128 ? 2 : 0);
-    static const KernFn kerns[4] = {state_tc_kernel<false, 64>, state_tc_kernel<true, 64>,
-                                    state_tc_kernel<false, 128>, state_tc_kernel<true, 128>};
-    static const uint32_t bytes[4] = {smem_bytes<false, 64>(), smem_bytes<true, 64>(), smem_bytes<false, 128>(),
-                                      smem_bytes<true, 128>()};
-    static OncePerDevice attr_set[4];
+    const int v = rev ? 4 + (gated ? 1 : 0) : (gated ? 1 : 0) + (dvs == 128 ? 2 : 0);
+    static const KernFn kerns[6] = {state_tc_kernel<false, 64, false>,  state_tc_kernel<true, 64, false>,
+                                    state_tc_kernel<false, 128, false>, state_tc_kernel<true, 128, false>,
+                                    state_tc_kernel<false, 128, true>,  state_tc_kernel<true, 128, true>};
+    static const uint32_t bytes[6] = {smem_bytes<false, 64>(),        smem_bytes<true, 64>(),
+                                      smem_bytes<false, 128>(),       smem_bytes<true, 128>(),
+                                      smem_bytes<false, 128, true>(), smem_bytes<true, 128, true>()};
+    static OncePerDevice attr_set[6];
     const cudaError_t e = set_smem_once(kerns[v], bytes[v], attr_set[v]);
     if (e != cudaSuccess) return e;
     kerns[v]<<<grid, kThreads, bytes[v], stream>>>(map_k, map_v, a);
@@ -369,11 +436,11 @@ cudaError_t launch_state_tc(const CUtensorMap &map_k, const CUtensorMap &map_v, 
 }
 
 cudaError_t launch_seg_scan(const float *S0, const float *z0, const float *A, const float *dS, float *S_start,
-                            int BH, int dv, int nsub, int sub_per_seg, int nseg, cudaStream_t stream)
+                            int BH, int dv, int nsub, int sub_per_seg, int nseg, cudaStream_t stream, bool rev)
 {
     const int state_len = kR * dv + kR;
     const dim3 grid((state_len / 4 + 255) / 256, BH);
-    seg_scan_kernel<<<grid, 256, 0, stream>>>(S0, z0, A, dS, S_start, BH, dv, nsub, sub_per_seg, nseg);
+    seg_scan_kernel<<<grid, 256, 0, stream>>>(S0, z0, A, dS, S_start, BH, dv, nsub, sub_per_seg, nseg, rev);
     return cudaGetLastError();
 }
 

@@ -145,6 +145,59 @@ def test_backward_tc_edges(la, oracle_mod, T, gated, with_state, edit):
         assert err <= 2e-2, (name, err)
 
 
+# Long sequences over few heads run the tensor-core sweeps over sequence segments
+# (at least 16 chunks each, as many as the SMs allow per head): the states
+# entering each segment come from a forward state pass (dq) and a reversed one
+# (dk, dv), whose parts the scans compose.  B*H = 2 or 3 on a GB300's 152 SMs
+# gives 2 to 4 segments, and state-pass parts of a single chunk.
+SEG_CASES = [
+    # B, H, T, gated, with_state, gate edits
+    (1, 2, 4100, True, True, None),
+    (1, 3, 2113, False, False, None),
+    (1, 2, 3200, True, False, "edges"),
+]
+
+
+@pytest.mark.parametrize("B,H,T,gated,with_state,edit", SEG_CASES,
+                         ids=[f"B{c[0]}H{c[1]}T{c[2]}-g{int(c[3])}-S{int(c[4])}-{c[5]}" for c in SEG_CASES])
+def test_backward_segmented(la, oracle_mod, B, H, T, gated, with_state, edit):
+    from recurrent_state_02_gb300 import workloads as W
+    w = W.Workload("bwd-seg", B=B, H=H, T=T, dtype=torch.bfloat16, gated=gated, seed=600 + T)
+    d = W.prefill_inputs(w, with_state=with_state)
+    if edit == "edges":
+        # zero gates on the tokens either side of chunk and segment boundaries, and
+        # a run of small gates across one
+        for t in (0, 1023, 1024, 1087, 1088, 2175, 2176, T - 1):
+            d["alpha"][0, 0, t] = 0.0
+        d["alpha"][0, 1, 1000:1200] = 0.3
+    g = torch.Generator().manual_seed(601 + T)
+    dy = torch.randn((B, H, T, 128), generator=g).to(torch.bfloat16)
+    dS_T = torch.randn((B, H, 128, 128), generator=g) * 0.1 if with_state else None
+    dz_T = torch.randn((B, H, 128), generator=g) * 0.1 if with_state else None
+    gd = {k: (v.cuda() if v is not None else None) for k, v in d.items()}
+    # the GPU forward's y, as training feeds it
+    y, _, _ = la.prefill_chunked(gd["q"], gd["k"], gd["v"], alpha=gd["alpha"], S0=gd["S0"], z0=gd["z0"], eps=EPS)
+    args = [to_oracle(d[n]) for n in ("q", "k", "v")]
+    ref = oracle_mod.backward(*args, dy.double().numpy(), alpha=to_oracle(d["alpha"]), S0=to_oracle(d["S0"]),
+                              z0=to_oracle(d["z0"]), dS_T=to_oracle(dS_T), dz_T=to_oracle(dz_T), eps=EPS, threads=0)
+    out = la.prefill_backward(gd["q"], gd["k"], gd["v"], y, dy.cuda(), alpha=gd["alpha"], S0=gd["S0"], z0=gd["z0"],
+                              dS_T=dS_T.cuda() if dS_T is not None else None,
+                              dz_T=dz_T.cuda() if dz_T is not None else None, eps=EPS)
+    assert la.last_device_status() == 0
+    for name, a, r_ in zip(("dq", "dk", "dv", "dalpha", "dS0", "dz0"), out, ref):
+        if r_ is None:
+            assert a is None
+            continue
+        a = a.float().cpu().numpy()
+        if name == "dalpha":
+            keep = d["alpha"].numpy() >= 0.05   # defined where alpha > 0; error grows as 1 / alpha
+            a, r_ = a[keep], r_[keep]
+        assert np.isfinite(a).all(), name
+        err = max_rel_err(a, r_)
+        print(f"[parity] segmented backward {name}: tensor {err:.3e}")
+        assert err <= 2e-2, (name, err)
+
+
 CHAIN_CASES = [
     # T, gated, with_state
     (300, True, True),
