@@ -709,13 +709,14 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
                 if (pp < kC) *reinterpret_cast<uint16_t *>(st + L::kOffStageOnes + sw128_offset(pp, 0)) = col0;
             }
             fence_proxy_async_smem();
-            // With one score buffer, P of chunk c (issued once phi of chunk c is
-            // done) completes the barrier phase after chunk c-1's, of the other
-            // parity; a wait for chunk c-1's parity begun after P of chunk c had
-            // completed would wait for chunk c+1's P, which needs this warp.  So
-            // chunk c-1's P is waited for here, before phi of chunk c is announced,
-            // and not again.
-            const bool waited = GATED && NP == 1 && c >= 1 && !f_prev;
+            // With one score buffer, whose barrier completes a phase per chunk, a
+            // wait for chunk x's parity is only sound while the barrier is in chunk
+            // x's phase or the one after it: begun later, it would wait for chunk
+            // x+2's P (which needs this warp); begun earlier, before chunk x-1's P
+            // had completed, it would return at once.  So chunk c-1's P is waited
+            // for here, for every chunk (fast or slow), before phi of chunk c is
+            // announced, and not again.
+            const bool waited = GATED && NP == 1 && c >= 1;
             if (waited && !warp_wait(cx, &sm->P_full[0], (c - 1) & 1)) {
                 ok = false;
                 break;
