@@ -170,12 +170,15 @@ static_assert(smem_bytes<true, 64>() <= 232448, "shared memory budget");
 static_assert(smem_bytes<false, 128>() <= 232448, "shared memory budget");
 static_assert(smem_bytes<true, 128>() <= 232448, "shared memory budget");
 
-template <bool GATED, int DVS>
-__global__ void __launch_bounds__(kThreads, 1)
-prefill_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
-                  const __grid_constant__ CUtensorMap map_v, const PrefillTcArgs args)
+// The kernel body for one CTA.  FAST (gated whole-head CTAs only): every chunk
+// of this CTA carries its gates as row weights (see cta_all_fast), so the body is
+// built without the explicit path.
+template <bool GATED, int DVS, bool FAST>
+__device__ __forceinline__ void
+prefill_body(const CUtensorMap &map_q, const CUtensorMap &map_k, const CUtensorMap &map_v, const PrefillTcArgs &args)
 {
     using L = Cfg<GATED, DVS>;
+    static_assert(!FAST || (GATED && L::kHead), "the row-weight body is for gated whole-head CTAs");
     constexpr int NST = L::kStages, NP = L::kNP, SC = L::kSC;
     static_assert(NP == 1 || NP == 2, "score buffers");
     extern __shared__ uint8_t smem_raw[];
@@ -524,7 +527,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
             // the state is decayed by the chunk's gate product Gamma_last before its
             // increment lands; a fast chunk (whole head) reads the decayed state:
             // its outputs are O' = w_i O (see the epilogue).
-            const bool fast = GATED && L::kHead && has_b && gr->gf[c % kAux] != 0;
+            const bool fast = GATED && L::kHead && has_b && (FAST || gr->gf[c % kAux] != 0);
             uint32_t spk[SC / 2];
             float zhi = 0.f, zsp = zr;
             if (GATED && has_b) {
@@ -621,7 +624,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
                 dn += __shfl_xor_sync(0xffffffffu, dn, 16);
                 // a fast chunk's row i holds O' = w_i O and dn' = w_i dn: y = O' / (dn' + eps w_i)
                 float epsw = args.eps;
-                if (GATED && L::kHead && gr->gf[ce % kAux] != 0) epsw *= gr->gw[ce % kAux][prow];
+                if (GATED && L::kHead && (FAST || gr->gf[ce % kAux] != 0)) epsw *= gr->gw[ce % kAux][prow];
                 if (GATED) warp_arrive(&sm->aux_empty[ce % kAux]);   // gate data of chunk ce is done
                 float inv;   // approximate reciprocal: y is rounded to BF16 below
                 asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(inv) : "f"(dn + epsw));
@@ -666,11 +669,11 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
             return true;
         };
         // Gated, whole head: a chunk flagged fast (gate_products) carries its gates
-        // as row weights on V instead: V_j <- w_j V_j in place and w_j in column 0
-        // of the stage's column block (1 otherwise), so that neither Q~ nor K~ is
-        // scaled and the chunk's products wait for no scaling.
+        // as row weights w_j on K~ instead, applied with phi: then P' = Q~ K~'^T =
+        // P diag(w), so A' [V | 1] = sum_j A_ij w_j [v_j | 1] and K~'^T [V | 1] is
+        // the state increment, and neither tile waits for a scaling after P.
         constexpr bool kFastOk = GATED && L::kHead;
-        auto is_fast = [&](int x) { return kFastOk && gr->gf[x % kAux] != 0; };
+        auto is_fast = [&](int x) { return FAST || (kFastOk && gr->gf[x % kAux] != 0); };
         bool ok = true, f_last = false;
         for (int c = 0; c < nch && ok; ++c) {
             const int s = c % NST;
@@ -682,31 +685,33 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
             const bool f_cur = is_fast(c), f_prev = c >= 1 && is_fast(c - 1);
             f_last = f_cur;
             // phi(Q), phi(K) in place (the two tiles are contiguous: 2048 chunks of
-            // 16 bytes); key rows past the end of the sequence become 0
+            // 16 bytes, K from chunk 1024); key rows past the end of the sequence
+            // become 0; a fast chunk's key rows times w_j
             static_assert(L::kOffK == L::kOffQ + kTileQ, "Q and K tiles are contiguous");
             uint4 *qk = reinterpret_cast<uint4 *>(st + L::kOffQ);
             constexpr int kFull = 2048 / kPhiThreads, kRest = 2048 - kFull * kPhiThreads;
-            if (nvalid == kC) {
+            if (nvalid == kC && !f_cur) {
 #pragma unroll
                 for (int it = 0; it < kFull; ++it) qk[pp + it * kPhiThreads] = phi8(qk[pp + it * kPhiThreads]);
                 if (pp < kRest) qk[pp + kFull * kPhiThreads] = phi8(qk[pp + kFull * kPhiThreads]);
+            } else if (nvalid == kC) {
+                const float *w = gr->gw[c % kAux];
+#pragma unroll
+                for (int it = 0; it <= kFull; ++it) {
+                    const int ci = pp + it * kPhiThreads;
+                    if (it < kFull || pp < kRest) {
+                        const uint4 v = phi8(qk[ci]);
+                        qk[ci] = ci >= 1024 ? scale8(v, w[(ci & 511) >> 3]) : v;
+                    }
+                }
             } else {
+                const float *w = gr->gw[c % kAux];
                 for (int ci = pp; ci < 2048; ci += kPhiThreads) {
                     const int row = (ci & 511) >> 3;   // 8 chunks per 128-byte row, 64 rows per block
-                    qk[ci] = (ci >= 1024 && row >= nvalid) ? make_uint4(0, 0, 0, 0) : phi8(qk[ci]);
+                    uint4 v = (ci >= 1024 && row >= nvalid) ? make_uint4(0, 0, 0, 0) : phi8(qk[ci]);
+                    if (f_cur && ci >= 1024) v = scale8(v, w[row]);
+                    qk[ci] = v;
                 }
-            }
-            if constexpr (kFastOk) {
-                uint16_t col0 = 0x3F80u;   // 1
-                if (f_cur) {
-                    // V rows by w_j (BF16 products; both V blocks: 1024 chunks of 16 bytes)
-                    uint4 *vt = reinterpret_cast<uint4 *>(st + L::kOffV);
-                    const float *w = gr->gw[c % kAux];
-                    for (int ci = pp; ci < (int)(L::kTileV / 16); ci += kPhiThreads)
-                        vt[ci] = scale8(vt[ci], w[(ci & 511) >> 3]);
-                    if (pp < kC) col0 = __bfloat16_as_ushort(__float2bfloat16_rn(w[pp]));
-                }
-                if (pp < kC) *reinterpret_cast<uint16_t *>(st + L::kOffStageOnes + sw128_offset(pp, 0)) = col0;
             }
             fence_proxy_async_smem();
             // With one score buffer, whose barrier completes a phase per chunk, a
@@ -738,6 +743,57 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
         tc_fence_after();
         tmem_dealloc(tmem, 512);
     }
+}
+
+// Whether every chunk of this CTA's sequence (segment) carries its gates as row
+// weights: no gate is exactly 0, and within every chunk the decay w_0 =
+// e^{b_last - b_0} (the product of the chunk's gates after its first) stays
+// above e^{kFastGateLog + 4}, a margin over the producer's own test (gate_products),
+// whose sums run in another order.  All threads take part; the result is the
+// same for every thread.
+__device__ __forceinline__ bool cta_all_fast(const PrefillTcArgs &args)
+{
+    const int h = blockIdx.y, b = blockIdx.z / args.nseg, seg = blockIdx.z % args.nseg;
+    const int bh = b * args.H + h;
+    const bool varlen = args.cu_seqlens != nullptr;
+    int seq0 = 0, T = args.T;
+    bool ok = args.alpha != nullptr;
+    if (varlen) {
+        seq0 = args.cu_seqlens[b];
+        const int seq1 = args.cu_seqlens[b + 1];
+        if (seq0 < 0 || seq1 < seq0 || seq1 > args.T) ok = false;   // the general body records the error
+        T = seq1 - seq0;
+    }
+    const int nch_all = ok ? (T + kC - 1) / kC : 0;
+    const int c0 = seg * args.seg_chunks;
+    const int nch = args.nseg > 1 ? min(args.seg_chunks, nch_all - c0) : nch_all;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    for (int c = warp; ok && c < nch; c += kThreads / 32) {
+        const int t0 = (c0 + c) * kC + 2 * lane;
+        float a0 = 1.f, a1 = 1.f;
+        if (t0 < T) a0 = args.alpha[varlen ? (size_t)(seq0 + t0) * args.H + h : (size_t)bh * T + t0];
+        if (t0 + 1 < T) a1 = args.alpha[varlen ? (size_t)(seq0 + t0 + 1) * args.H + h : (size_t)bh * T + t0 + 1];
+        const bool zero = !(a0 > 0.f) || !(a1 > 0.f);
+        float lsum = (lane == 0 ? 0.f : logf(fmaxf(a0, 1e-30f))) + logf(fmaxf(a1, 1e-30f));   // rows 1..63
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) lsum += __shfl_xor_sync(0xffffffffu, lsum, o);
+        ok = !__any_sync(0xffffffffu, zero) && lsum >= kFastGateLog + 4.f;
+    }
+    return __syncthreads_and(ok) != 0;
+}
+
+template <bool GATED, int DVS>
+__global__ void __launch_bounds__(kThreads, 1)
+prefill_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
+                  const __grid_constant__ CUtensorMap map_v, const PrefillTcArgs args)
+{
+    if constexpr (GATED && Cfg<GATED, DVS>::kHead) {
+        if (cta_all_fast(args)) {
+            prefill_body<GATED, DVS, true>(map_q, map_k, map_v, args);
+            return;
+        }
+    }
+    prefill_body<GATED, DVS, false>(map_q, map_k, map_v, args);
 }
 
 }  // namespace
