@@ -7,20 +7,24 @@
 //     S -> A S + dS,   z -> A z + dz,
 // with A the product of the run's gates and (dS, dz) the state the run would
 // produce from a zero state.  state_tc_kernel computes (A, dS, dz) for each
-// sub-segment of a head's sequence, chunk by chunk exactly as the prefill
-// kernel updates its state (the same gate products, feature map and operand
-// rounding); seg_scan_kernel then applies the maps in sequence order to S0, z0
-// and writes the start state of every output segment, from which the prefill
-// kernel processes the segments in parallel.
+// sub-segment (part) of a head's sequence as one accumulation over its chunks,
+// dS = sum_j e_j phi(k_j) [v_j | 1]^T with e_j the product of the gates after
+// token j within the part: each key row carries its whole decay, so the state in
+// TMEM is never rescaled.  The chunks are walked from the part's end, and e_j =
+// e^{offset} w_j with w_j the decay to the chunk's end and the offset summed
+// over the chunks already walked (0 once a zero gate has been passed).
+// seg_scan_kernel then applies the maps in sequence order to S0, z0 and writes
+// the start state of every output segment, from which the prefill kernel
+// processes the segments in parallel.
 //
 // The backward's key-side sweeps carry, in reversed time, the state
 //     G_t = phi(q_t) dn_t^T + alpha_{t+1} G_{t+1},   g_t = dd_t phi(q_t) + alpha_{t+1} g_{t+1}
 // (dn_t = dy_t / d_t, dd_t = -(dy_t . y_t) / d_t), which is affine in the same
-// way.  The REV form of the state pass runs a sub-segment's chunks from its last
-// to its first with key phi(q), value dn and dd in place of the column of ones,
-// each token weighted by the product Gamma_t of the gates from the chunk's start
-// to the token (the decay back to the chunk's start); its map sends the state
-// entering the sub-segment from the right to the state it hands to the left.
+// way.  The REV form of the state pass takes key phi(q), value dn and dd in
+// place of the column of ones, each token weighted by its decay back to the
+// part's start (Gamma_t within the chunk times the offset of the chunks before
+// it, walked from the part's start); its map sends the state entering the
+// sub-segment from the right to the state it hands to the left.
 // The scan then applies the maps from the end of the sequence backwards,
 // starting from dL/dS_T, dL/dz_T.
 
@@ -44,10 +48,13 @@ constexpr int kMaxStages = 4;
 
 // Two CTAs are resident per SM (each at most 113 KB of shared memory), so that
 // the many short parts of a segment stream at the bandwidth of the SM.
-// Per-chunk scalars of the reversed pass: 1 / d_t and dd_t (0 for rows past T).
+// Per-chunk scalars: (reversed pass) 1 / d_t and dd_t (0 for rows past T);
+// (gated) e^{offset}, the gate product between the chunk and the part's end
+// (forward) or start (reversed) over the chunks walked before it, 0 past a zero gate.
 struct alignas(16) RevRing {
     float invd[kAux][kC];
     float dd[kAux][kC];
+    float eoff[kAux];
 };
 
 // REV: the reversed-time pass of the backward (DVS 128 only): the column block
@@ -56,7 +63,7 @@ template <bool GATED, int DVS, bool REV = false>
 struct SCfg {
     static_assert(DVS == 64 || DVS == 128, "value columns per CTA");
     static_assert(!REV || DVS == 128, "the reversed pass takes whole heads");
-    static constexpr int kStages = REV ? 2 : DVS == 128 ? (GATED ? 2 : 3) : (GATED ? 3 : 4);
+    static constexpr int kStages = REV ? 2 : DVS == 128 ? 3 : 4;
     static constexpr uint32_t kTileV = (DVS / 64) * kBlkV;
     static constexpr uint32_t kOffK = 0, kOffV = kTileK, kOffStageCol = kTileK + kTileV;
     static constexpr uint32_t kStageBytes = kTileK + kTileV + (REV ? kTileOnes : 0);
@@ -64,13 +71,13 @@ struct SCfg {
     static constexpr uint32_t kOffOnes = kStages * kStageBytes;
     static constexpr uint32_t kOffGate = kOffOnes + (REV ? 0 : kTileOnes);
     static constexpr uint32_t kOffRev = kOffGate + (GATED ? sizeof(GateRing) : 0);
-    static constexpr uint32_t kOffSmall = kOffRev + (REV ? sizeof(RevRing) : 0);
+    static constexpr uint32_t kOffSmall = kOffRev + ((REV || GATED) ? sizeof(RevRing) : 0);
     static constexpr uint32_t kTmemCols = DVS == 128 ? 256 : 128;   // [S | z]: DVS + 16 columns (z is column DVS)
 };
 
 struct alignas(16) SmallS {
     uint64_t full[kMaxStages], empty[kMaxStages], phi_done[kMaxStages];
-    uint64_t dS_full, S_read, mma_done, aux_empty[kAux];
+    uint64_t mma_done;
     uint32_t tmem_base;
     int abort_flag;
 };
@@ -96,7 +103,7 @@ state_tc_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant
     uint8_t *base = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     SmallS *sm = reinterpret_cast<SmallS *>(base + L::kOffSmall);
     GateRing *gr = reinterpret_cast<GateRing *>(base + L::kOffGate);   // gated only
-    RevRing *rr = reinterpret_cast<RevRing *>(base + L::kOffRev);      // REV only
+    RevRing *rr = reinterpret_cast<RevRing *>(base + L::kOffRev);      // REV or gated
     Ctx cx{&sm->abort_flag, args.wait_limit_ns, args.status};
 
     // grid: (dv slice, h, b * nsub + m); sub-segment m is part j of output segment g
@@ -110,8 +117,10 @@ state_tc_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant
     const int nch = max(0, min(min(cs + args.sub_chunks, (g + 1) * args.seg_chunks), (args.T + kC - 1) / kC) - cs);
     const int tb = cs * kC;                                                   // first token
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    // first token of the c-th chunk processed (REV: from the sub-segment's end)
-    auto chunk_t0 = [&](int c) { return tb + (REV ? nch - 1 - c : c) * kC; };
+    // first token of the c-th chunk processed: from the part's end in forward time,
+    // from its start in reversed time, so that the chunks walked before a chunk
+    // are the ones its tokens decay through (their gate product is the offset)
+    auto chunk_t0 = [&](int c) { return tb + (REV ? c : nch - 1 - c) * kC; };
     auto stage_ptr = [&](int s) { return base + s * L::kStageBytes; };
 
     // ------------------------------------------------------------ set-up
@@ -121,9 +130,6 @@ state_tc_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant
             mbar_init(&sm->empty[s], 1);
             mbar_init(&sm->phi_done[s], kPhiWarps);
         }
-        for (int i = 0; i < kAux; ++i) mbar_init(&sm->aux_empty[i], kTmWarps);
-        mbar_init(&sm->dS_full, 1);
-        mbar_init(&sm->S_read, kTmWarps);
         mbar_init(&sm->mma_done, 1);
         sm->abort_flag = 0;
         fence_mbarrier_init();
@@ -170,6 +176,8 @@ state_tc_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant
     if (warp == kWarpTma) {
         // ------------------------------------------------------- producer
         int issued = 0;
+        float off = 0.f;   // gated: log of the gate product over the chunks walked so far
+        bool cut = false;  // a zero gate has been walked
         for (int c = 0; c < nch; ++c) {
             const int s = c % NST;
             const int t0 = chunk_t0(c);
@@ -185,8 +193,10 @@ state_tc_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant
                 if (t0 + 2 * lane < T) { dv2.x = dp[t0 + 2 * lane]; dd2.x = ddp[t0 + 2 * lane]; }
                 if (t0 + 2 * lane + 1 < T) { dv2.y = dp[t0 + 2 * lane + 1]; dd2.y = ddp[t0 + 2 * lane + 1]; }
             }
+            // the ring entry of chunk c held chunk c - kAux's, which phi (its only
+            // reader) finished before the MMA of chunk c - NST released the stage
+            static_assert(kAux >= NST, "ring entries outlive their stage");
             if (c >= NST && !warp_wait(cx, &sm->empty[s], ((c / NST) - 1) & 1)) break;
-            if (GATED && c >= kAux && !warp_wait(cx, &sm->aux_empty[c % kAux], ((c / kAux) - 1) & 1)) break;
             if (__shfl_sync(0xffffffffu, aborted(cx) ? 1 : 0, 0)) break;
             uint8_t *st = stage_ptr(s);
             if (lane == 0) {
@@ -206,7 +216,14 @@ state_tc_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant
                     for (int vb = 0; vb < DVS / 64; ++vb) tma_prefetch_l2_3d(&map_v, slice * DVS + vb * 64, tp, bh);
                 }
             }
-            if (GATED) gate_products(a0, a1, lane, c % kAux, gr);
+            if (GATED) {
+                gate_products(a0, a1, lane, c % kAux, gr);
+                __syncwarp();
+                if (lane == 0) rr->eoff[c % kAux] = cut ? 0.f : expf(off);
+                const float blast = gr->gb[c % kAux][kC - 1];
+                cut = cut || gr->gz[c % kAux][kC - 1] >= 0;
+                off += blast;
+            }
             if (REV) {
                 *reinterpret_cast<float2 *>(&rr->invd[c % kAux][2 * lane]) = make_float2(1.f / dv2.x, 1.f / dv2.y);
                 *reinterpret_cast<float2 *>(&rr->dd[c % kAux][2 * lane]) = dd2;
@@ -219,12 +236,14 @@ state_tc_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant
             for (int c = (issued > NST ? issued - NST : 0); c < issued; ++c)
                 mbar_wait(&sm->full[c % NST], (c / NST) & 1, cx.limit);
         }
+        // the part's gate product (1 without a gate or chunks)
+        if (lane == 0 && slice == 0 && !aborted(cx))
+            args.A[(size_t)m * BH + bh] = (GATED && issued == nch) ? (cut ? 0.f : expf(off)) : 1.f;
         __syncwarp();
     } else if (warp == kWarpMma) {
         // ------------------------------------------------------------ MMA
-        // [S | z] += K~'^T [V | 1] per chunk (K~' = diag(w) K~ with a gate), once
-        // phi of the chunk is done and, with a gate, the TMEM warps have decayed
-        // the state by the chunk's gate product.  With 64 value columns one MMA
+        // [S | z] += K~'^T [V | 1] per chunk (K~' = diag(weight) K~ with a gate),
+        // once phi of the chunk is done.  With 64 value columns one MMA
         // spans the V block and the first 16 columns of the ones block (at LBO);
         // with 128 the two V blocks and the ones block are two MMAs.
         if (lane == 0) {
@@ -238,7 +257,6 @@ state_tc_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant
                 const uint32_t st = smem_u32(stage_ptr(s));
                 const uint32_t onesLo = desc_lo(REV ? st + L::kOffStageCol : aOnes, kBlkV);
                 if (!wait(cx, &sm->phi_done[s], (c / NST) & 1)) break;
-                if (GATED && !wait(cx, &sm->S_read, c & 1)) break;
                 tc_fence_after();
                 const uint32_t klo = desc_lo(st + L::kOffK, kTileK / 2);   // K~^T: MN-major, two 64-feature blocks
                 const uint32_t blo = desc_lo(st + L::kOffV, DVS == 64 ? aOnes - (st + L::kOffV) : kBlkV);
@@ -249,7 +267,6 @@ state_tc_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant
                         tc_mma_bf16_w<true>(tmem + DVS, klo + kk * (2048 >> 4), kHi128, onesLo + kk * (2048 >> 4),
                                             kHi128, idDS1);
                 }
-                tc_commit(&sm->dS_full);
                 tc_commit(&sm->empty[s]);
             }
             tc_commit(&sm->mma_done);
@@ -263,33 +280,8 @@ state_tc_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant
         const int qd = warp & 3;
         const uint32_t lane_base = static_cast<uint32_t>(qd * 32) << 16;
         const int srow = qd * 32 + lane;
-        float decay = 1.f;
-        if (GATED) {
-            // decay the state by the gate product of chunk c before its increment lands
-            for (int c = 0; c < nch; ++c) {
-                if (c >= 1 && !warp_wait(cx, &sm->dS_full, (c - 1) & 1)) break;
-                if (!warp_wait(cx, &sm->phi_done[c % NST], (c / NST) & 1)) break;   // gate data of chunk c
-                tc_fence_after();
-                const float gl = gr->gG[c % kAux][kC - 1];
-                decay *= gl;
-                float sh[32], zz;
-                tc_ld_32x32b_x1(tmem + lane_base + DVS, zz);
-#pragma unroll 1
-                for (int pc = 0; pc < DVS / 32; ++pc) {
-                    tc_ld_32x32b_x32(tmem + lane_base + 32 * pc, sh);
-                    tc_wait_ld();
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) sh[i] *= gl;
-                    tc_st_32x32b_x32(tmem + lane_base + 32 * pc, sh);
-                }
-                tc_st_32x32b_x1(tmem + lane_base + DVS, zz * gl);
-                tc_wait_st();
-                tc_fence_before();
-                warp_arrive(&sm->S_read);
-                warp_arrive(&sm->aux_empty[c % kAux]);
-            }
-        }
-        // the sub-segment's (A, dS, dz) once every increment has landed
+        // the sub-segment's (dS, dz) once every increment has landed (the gates
+        // are in the increments' row weights; the producer writes A)
         if (!aborted(cx)) {
             int ok = 1;
             if (lane == 0) ok = mbar_wait(&sm->mma_done, 0, cx.limit);
@@ -310,19 +302,17 @@ state_tc_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant
                     for (int i = 0; i < 32; i += 4)
                         *reinterpret_cast<float4 *>(dst + 32 * pc + i) = make_float4(sh[i], sh[i + 1], sh[i + 2], sh[i + 3]);
                 }
-                if (slice == 0) {
-                    out[(size_t)kR * args.dv + srow] = zz;
-                    if (warp == kWarpTm0 && lane == 0) args.A[(size_t)m * BH + bh] = decay;
-                }
+                if (slice == 0) out[(size_t)kR * args.dv + srow] = zz;
             } else {
                 fail(cx);
             }
         }
     } else if (is_phi_warp(warp)) {
         // ------------------------------------------------------ phi warps
-        // phi(K) in place, with a gate times w_j on key row j (REV: times Gamma_j);
-        // rows past the end of the sequence become 0.  REV: the rows of V (dy)
-        // times 1 / d_t, and dd_t in column 0 of the stage's column block.
+        // phi(K) in place, with a gate times the row's decay to the part's end,
+        // e^{offset} w_j (REV: to its start, e^{offset} Gamma_j); rows past the end
+        // of the sequence become 0.  REV: the rows of V (dy) times 1 / d_t, and
+        // dd_t in column 0 of the stage's column block.
         const int pp = phi_index(warp) * 32 + lane;
         for (int c = 0; c < nch; ++c) {
             const int s = c % NST;
@@ -330,10 +320,11 @@ state_tc_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant
             const int nvalid = min(kC, T - chunk_t0(c));
             uint4 *kt = reinterpret_cast<uint4 *>(stage_ptr(s) + L::kOffK);
             const float *kw = REV ? gr->gG[c % kAux] : gr->gw[c % kAux];
+            const float eoff = GATED ? rr->eoff[c % kAux] : 1.f;
             for (int ci = pp; ci < (int)kTileK / 16; ci += kPhiThreads) {
                 const int row = (ci & 511) >> 3;   // 8 chunks per 128-byte row, 64 rows per block
                 uint4 v = row < nvalid ? phi8(kt[ci]) : make_uint4(0, 0, 0, 0);
-                if (GATED) v = scale8(v, kw[row]);
+                if (GATED) v = scale8(v, eoff * kw[row]);
                 kt[ci] = v;
             }
             if (REV) {
