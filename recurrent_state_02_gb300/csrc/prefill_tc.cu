@@ -172,8 +172,9 @@ static_assert(smem_bytes<true, 128>() <= 232448, "shared memory budget");
 
 // The kernel body for one CTA.  FAST (gated whole-head CTAs only): every chunk
 // of this CTA carries its gates as row weights (see cta_all_fast), so the body is
-// built without the explicit path.
-template <bool GATED, int DVS, bool FAST>
+// built without the explicit path.  PLAIN: [B, H, T, d] inputs and one segment
+// per head (no packed sequences, no scanned start states).
+template <bool GATED, int DVS, bool FAST, bool PLAIN>
 __device__ __forceinline__ void
 prefill_body(const CUtensorMap &map_q, const CUtensorMap &map_k, const CUtensorMap &map_v, const PrefillTcArgs &args)
 {
@@ -190,12 +191,13 @@ prefill_body(const CUtensorMap &map_q, const CUtensorMap &map_k, const CUtensorM
     const int slice = blockIdx.x;
     // grid.z enumerates (b, sequence segment); one segment unless the caller
     // split the sequence (then every segment starts from a scanned state)
-    const int h = blockIdx.y, b = blockIdx.z / args.nseg, seg = blockIdx.z % args.nseg;
+    const int h = blockIdx.y;
+    const int b = PLAIN ? (int)blockIdx.z : blockIdx.z / args.nseg, seg = PLAIN ? 0 : blockIdx.z % args.nseg;
     const int bh = b * args.H + h;
     // Packed sequences of different lengths (cu_seqlens; no segments) or the
     // [B, H, T, d] layout.  A sequence whose bounds are inconsistent with the
     // total is recorded as a shape error and processes no tokens.
-    const bool varlen = args.cu_seqlens != nullptr;
+    const bool varlen = !PLAIN && args.cu_seqlens != nullptr;
     int seq0 = 0, T = args.T;
     if (varlen) {
         seq0 = args.cu_seqlens[b];
@@ -215,14 +217,15 @@ prefill_body(const CUtensorMap &map_q, const CUtensorMap &map_k, const CUtensorM
     auto tma_c2 = [&](int t0) { return varlen ? seq0 + t0 : bh; };
     const int nch_all = (T + kC - 1) / kC;
     const int c0 = seg * args.seg_chunks;                                     // first chunk of the segment
-    const int nch = args.nseg > 1 ? min(args.seg_chunks, nch_all - c0) : nch_all;   // its chunk count
+    const int nch = (!PLAIN && args.nseg > 1) ? min(args.seg_chunks, nch_all - c0) : nch_all;   // its chunk count
     const int tb = c0 * kC;                                                   // its first token
-    const bool last_seg = seg == args.nseg - 1;
+    const bool last_seg = PLAIN || seg == args.nseg - 1;
     // start state of this head: S0/z0, or the scanned state of the segment
     const size_t state_len = (size_t)kR * args.dv + kR;
-    const float *S_init = args.S_start ? args.S_start + ((size_t)seg * (gridDim.z / args.nseg) * args.H + bh) * state_len
-                                       : (args.S0 ? args.S0 + (size_t)bh * kR * args.dv : nullptr);
-    const float *z_init_src = args.S_start ? S_init + (size_t)kR * args.dv : (args.z0 ? args.z0 + (size_t)bh * kR : nullptr);
+    const bool scanned = !PLAIN && args.S_start != nullptr;
+    const float *S_init = scanned ? args.S_start + ((size_t)seg * (gridDim.z / args.nseg) * args.H + bh) * state_len
+                                  : (args.S0 ? args.S0 + (size_t)bh * kR * args.dv : nullptr);
+    const float *z_init_src = scanned ? S_init + (size_t)kR * args.dv : (args.z0 ? args.z0 + (size_t)bh * kR : nullptr);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
     auto stage_ptr = [&](int s) { return base + s * L::kStageBytes; };
@@ -782,18 +785,18 @@ __device__ __forceinline__ bool cta_all_fast(const PrefillTcArgs &args)
     return __syncthreads_and(ok) != 0;
 }
 
-template <bool GATED, int DVS>
+template <bool GATED, int DVS, bool PLAIN>
 __global__ void __launch_bounds__(kThreads, 1)
 prefill_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
                   const __grid_constant__ CUtensorMap map_v, const PrefillTcArgs args)
 {
     if constexpr (GATED && Cfg<GATED, DVS>::kHead) {
         if (cta_all_fast(args)) {
-            prefill_body<GATED, DVS, true>(map_q, map_k, map_v, args);
+            prefill_body<GATED, DVS, true, PLAIN>(map_q, map_k, map_v, args);
             return;
         }
     }
-    prefill_body<GATED, DVS, false>(map_q, map_k, map_v, args);
+    prefill_body<GATED, DVS, false, PLAIN>(map_q, map_k, map_v, args);
 }
 
 }  // namespace
@@ -804,19 +807,23 @@ cudaError_t launch_prefill_tc(const CUtensorMap &map_q, const CUtensorMap &map_k
     if (dvs != 64 && dvs != 128) return cudaErrorInvalidValue;
     const dim3 grid(a.dv / dvs, a.H, B * a.nseg);
     using KernFn = void (*)(const CUtensorMap, const CUtensorMap, const CUtensorMap, const PrefillTcArgs);
-    const int v = (gated ? 1 : 0) + (dvs == 128 ? 2 : 0);
-    static const KernFn kerns[4] = {prefill_tc_kernel<false, 64>, prefill_tc_kernel<true, 64>,
-                                    prefill_tc_kernel<false, 128>, prefill_tc_kernel<true, 128>};
+    // plain: [B, H, T, d] inputs and one segment per head
+    const bool plain = a.cu_seqlens == nullptr && a.nseg == 1 && a.S_start == nullptr;
+    const int v = (gated ? 1 : 0) + (dvs == 128 ? 2 : 0) + (plain ? 4 : 0);
+    static const KernFn kerns[8] = {prefill_tc_kernel<false, 64, false>, prefill_tc_kernel<true, 64, false>,
+                                    prefill_tc_kernel<false, 128, false>, prefill_tc_kernel<true, 128, false>,
+                                    prefill_tc_kernel<false, 64, true>,  prefill_tc_kernel<true, 64, true>,
+                                    prefill_tc_kernel<false, 128, true>, prefill_tc_kernel<true, 128, true>};
     static const uint32_t bytes[4] = {smem_bytes<false, 64>(), smem_bytes<true, 64>(), smem_bytes<false, 128>(),
                                       smem_bytes<true, 128>()};
     // The attribute is set once per device (not during stream capture of later calls).
-    static OncePerDevice attr_set[4];
-    const cudaError_t e = set_smem_once(kerns[v], bytes[v], attr_set[v]);
+    static OncePerDevice attr_set[8];
+    const cudaError_t e = set_smem_once(kerns[v], bytes[v & 3], attr_set[v]);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = grid;
     cfg.blockDim = dim3(kThreads, 1, 1);
-    cfg.dynamicSmemBytes = bytes[v];
+    cfg.dynamicSmemBytes = bytes[v & 3];
     cfg.stream = stream;
     // the dv slices of a head (and segment) form a cluster
     cudaLaunchAttribute attr[1];
