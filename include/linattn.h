@@ -198,7 +198,7 @@ la_status la_decode_step(const void *q, const void *k, const void *v, la_dtype d
  * la_backward_workspace_bytes -- device scratch that la_prefill_backward needs for
  * these sizes on the current device, for any r, dv <= 128 and either dtype: the
  * FP32 per-token terms and one value per head (4 * B*H*(3T + 1) bytes), the maps
- * of the z_t pass (4 * B*H*ceil(T/256)*257 bytes), and, when B*H whole-head CTAs
+ * of the z_t pass (4 * B*H*ceil(T/128)*257 bytes), and, when B*H whole-head CTAs
  * would leave enough SMs idle and T is long enough, the two state passes of the
  * sequence-segmented tensor-core sweeps (forward and reversed: per head and part
  * or segment 4 * (128*128 + 128) bytes).  The size depends on the device's SM
@@ -228,7 +228,7 @@ size_t la_backward_workspace_bytes(int B, int H, int T);
  *   dS0, dz0  device FP32 [B,H,r,dv], [B,H,r] (written also when S0, z0 are NULL).
  *   workspace: >= la_backward_workspace_bytes device bytes, 16-byte aligned, owned by
  *          the caller; calls sharing it must be ordered.
- * Kernels: the z_t recurrence over segments of 256 tokens (maps, scan, products)
+ * Kernels: the z_t recurrence over segments of 128 tokens (maps, scan, products)
  * for d_t, one pass for dd_t, then the three gradients as causal linear
  * attentions over chunks of 64 tokens (dq forward in time, dk and dv in
  * reverse), then a reverse running sum for dalpha.  BF16 with r = dv = 128 runs

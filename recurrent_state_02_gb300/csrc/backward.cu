@@ -61,27 +61,30 @@ __device__ __forceinline__ float2 hi2(float4 a) { return make_float2(a.z, a.w); 
 // ------------------------------------------------------------ d_t and dd_t
 
 // z_t and the feature sum of d_t, in three fully parallel steps over segments of
-// kZLen tokens (one warp per (b, h, 64 features, segment); lane l holds features
-// 2l, 2l + 1, at r = 32 the upper 16 lanes none).  z_t = alpha_t z_{t-1} + phi(k_t)
-// is affine in z: bwd_zmap_kernel runs each segment from z = 0, which gives its
-// map z -> P z + zs; bwd_zscan_kernel applies the maps in order to z0 and writes
-// the state entering every segment; bwd_zdot_kernel runs each segment again from
-// there.  Tokens go in batches of ZB(Tin) whose loads are all issued before the
-// recurrence uses them; the products q~_{t,i} z_{t,i} of a batch are summed over
-// the warp's features by a reduce-scatter across the lanes (lane l ends with
-// token l mod ZB) and added to d_acc[t] (zeroed before).
-constexpr int kZLen = 256;       // tokens per segment
-constexpr int kZFeat = 64;       // features per warp
+// kZLen tokens (one warp per (b, h, segment); lane l holds features 4l .. 4l+3, so
+// that a warp reads whole 256-byte token rows; at r < 128 the upper lanes hold
+// none).  z_t = alpha_t z_{t-1} + phi(k_t) is affine in z: bwd_zmap_kernel runs
+// each segment from z = 0, which gives its map z -> P z + zs; bwd_zscan_kernel
+// applies the maps in order to z0 and writes the state entering every segment;
+// bwd_zdot_kernel runs each segment again from there.  Tokens go in batches of
+// ZB(Tin) whose loads are all issued before the recurrence uses them; the
+// products q~_{t,i} z_{t,i} of a batch are summed over the warp's features by a
+// reduce-scatter across the lanes (lane l ends with token l mod ZB) and written
+// to d_acc[t].
+constexpr int kZLen = 128;       // tokens per segment
 constexpr int kZWarps = 8;       // warps (segments) per CTA
 
-template <typename Tin> struct ZBatch { static constexpr int n = 32; };
-template <> struct ZBatch<float> { static constexpr int n = 16; };
+template <typename Tin> struct ZBatch { static constexpr int n = 16; };
+template <> struct ZBatch<float> { static constexpr int n = 8; };
 
-// Two adjacent features of one token row, raw.
-__device__ __forceinline__ uint32_t load_pair(const __nv_bfloat16 *p) { return *reinterpret_cast<const uint32_t *>(p); }
-__device__ __forceinline__ float2 load_pair(const float *p) { return *reinterpret_cast<const float2 *>(p); }
-__device__ __forceinline__ float2 unpack_pair(uint32_t raw) { return make_float2(bf16_lo(raw), bf16_hi(raw)); }
-__device__ __forceinline__ float2 unpack_pair(float2 raw) { return raw; }
+// Four adjacent features of one token row, raw.
+__device__ __forceinline__ uint2 load_quad(const __nv_bfloat16 *p) { return *reinterpret_cast<const uint2 *>(p); }
+__device__ __forceinline__ float4 load_quad(const float *p) { return *reinterpret_cast<const float4 *>(p); }
+__device__ __forceinline__ float4 unpack_quad(uint2 raw)
+{
+    return make_float4(bf16_lo(raw.x), bf16_hi(raw.x), bf16_lo(raw.y), bf16_hi(raw.y));
+}
+__device__ __forceinline__ float4 unpack_quad(float4 raw) { return raw; }
 
 // Sums v[0..NB) over the 32 lanes: afterwards v[0] of lane l holds the total of
 // index l mod NB.  Each halving step swaps the half of the values that a lane
@@ -116,12 +119,21 @@ __device__ __forceinline__ ZWarp z_warp(int r, int T, int nzs)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     w.seg = blockIdx.y * kZWarps + warp;
     w.bh = blockIdx.x;
-    w.i0 = blockIdx.z * kZFeat + 2 * lane;
+    w.i0 = 4 * lane;
     w.live = w.i0 < r;
     w.valid = w.seg < nzs;
     w.ta = min(T, w.seg * kZLen);
     w.te = min(T, w.ta + kZLen);
     return w;
+}
+
+// z <- a z + phi(k) for four features.
+__device__ __forceinline__ void z_step(float4 &z, float a, float4 k)
+{
+    z.x = a * z.x + phi_f(k.x);
+    z.y = a * z.y + phi_f(k.y);
+    z.z = a * z.z + phi_f(k.z);
+    z.w = a * z.w + phi_f(k.w);
 }
 
 // 1: the map (P, zs) of every segment; zs [B*H][nzs][r], P [B*H][nzs].
@@ -131,87 +143,92 @@ bwd_zmap_kernel(const Tin *__restrict__ k, const float *__restrict__ alpha, int 
                 float *__restrict__ zs_out, float *__restrict__ P_out)
 {
     constexpr int NB = ZBatch<Tin>::n;
-    using Raw = decltype(load_pair(static_cast<const Tin *>(nullptr)));
+    using Raw = decltype(load_quad(static_cast<const Tin *>(nullptr)));
     const ZWarp w = z_warp(r, T, nzs);
     if (!w.valid) return;   // whole warps only
     const int lane = threadIdx.x & 31;
     const Tin *kp = k + (size_t)w.bh * T * r + w.i0;
     const float *ap = alpha ? alpha + (size_t)w.bh * T : nullptr;
-    float2 z = make_float2(0.f, 0.f);
+    float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
     float P = 1.f;
     for (int t0 = w.ta; t0 < w.te; t0 += NB) {
         const int nt = min(NB, w.te - t0);
         Raw kr[NB];
 #pragma unroll
-        for (int t = 0; t < NB; ++t) kr[t] = (t < nt && w.live) ? load_pair(kp + (size_t)(t0 + t) * r) : Raw{};
+        for (int t = 0; t < NB; ++t) kr[t] = (t < nt && w.live) ? load_quad(kp + (size_t)(t0 + t) * r) : Raw{};
         const float al = (ap && lane < nt) ? ap[t0 + lane] : 1.f;
 #pragma unroll
         for (int t = 0; t < NB; ++t) {
             const float a = __shfl_sync(0xffffffffu, al, t);
             if (t < nt) {
-                const float2 kv = unpack_pair(kr[t]);
-                z.x = a * z.x + phi_f(kv.x);
-                z.y = a * z.y + phi_f(kv.y);
+                z_step(z, a, unpack_quad(kr[t]));
                 P *= a;
             }
         }
     }
     const size_t sidx = (size_t)w.bh * nzs + w.seg;
-    if (w.live) *reinterpret_cast<float2 *>(zs_out + sidx * r + w.i0) = z;
-    if (blockIdx.z == 0 && lane == 0) P_out[sidx] = P;
+    if (w.live) *reinterpret_cast<float4 *>(zs_out + sidx * r + w.i0) = z;
+    if (lane == 0) P_out[sidx] = P;
 }
 
-// 2: the state entering every segment, z_start [B*H][nzs][r]: one warp per (b, h,
-// 64 features) applies the maps in order to z0, loading 8 of them at a time.
+// 2: the state entering every segment, z_start [B*H][nzs][r]: one warp per (b, h)
+// applies the maps in order to z0, loading 8 of them at a time.
 __global__ void __launch_bounds__(32)
 bwd_zscan_kernel(const float *__restrict__ z0, const float *__restrict__ zs, const float *__restrict__ P, int r,
                  int nzs, float *__restrict__ z_start)
 {
-    const int lane = threadIdx.x, bh = blockIdx.x, i0 = blockIdx.y * kZFeat + 2 * lane;
+    const int lane = threadIdx.x, bh = blockIdx.x, i0 = 4 * lane;
     const bool live = i0 < r;
-    float2 z = (z0 && live) ? *reinterpret_cast<const float2 *>(z0 + (size_t)bh * r + i0) : make_float2(0.f, 0.f);
+    float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (z0 && live) {   // z0 is only 4-byte aligned
+        const float *zp = z0 + (size_t)bh * r + i0;
+        z = make_float4(zp[0], zp[1], zp[2], zp[3]);
+    }
     for (int s0 = 0; s0 < nzs; s0 += 8) {
-        float2 m[8];
+        float4 m[8];
         float p[8];
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
             const size_t sidx = (size_t)bh * nzs + s0 + i;
             const bool in = s0 + i < nzs;
-            m[i] = (in && live) ? *reinterpret_cast<const float2 *>(zs + sidx * r + i0) : make_float2(0.f, 0.f);
+            m[i] = (in && live) ? *reinterpret_cast<const float4 *>(zs + sidx * r + i0) : make_float4(0.f, 0.f, 0.f, 0.f);
             p[i] = in ? P[sidx] : 1.f;
         }
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
             if (s0 + i >= nzs) break;
-            if (live) *reinterpret_cast<float2 *>(z_start + ((size_t)bh * nzs + s0 + i) * r + i0) = z;
+            if (live) *reinterpret_cast<float4 *>(z_start + ((size_t)bh * nzs + s0 + i) * r + i0) = z;
             z.x = p[i] * z.x + m[i].x;
             z.y = p[i] * z.y + m[i].y;
+            z.z = p[i] * z.z + m[i].z;
+            z.w = p[i] * z.w + m[i].w;
         }
     }
 }
 
-// 3: every segment again from its entering state, with the products summed into d_acc.
+// 3: every segment again from its entering state, with the products summed into
+// d_acc (one warp holds all of a token's features: a plain store).
 template <typename Tin>
 __global__ void __launch_bounds__(32 * kZWarps)
 bwd_zdot_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k, const float *__restrict__ alpha, int T, int r,
                 int nzs, const float *__restrict__ z_start, float *__restrict__ d_acc)
 {
     constexpr int NB = ZBatch<Tin>::n;
-    using Raw = decltype(load_pair(static_cast<const Tin *>(nullptr)));
+    using Raw = decltype(load_quad(static_cast<const Tin *>(nullptr)));
     const ZWarp w = z_warp(r, T, nzs);
     if (!w.valid) return;   // whole warps only
     const int lane = threadIdx.x & 31;
     const Tin *kp = k + (size_t)w.bh * T * r + w.i0, *qp = q + (size_t)w.bh * T * r + w.i0;
     const float *ap = alpha ? alpha + (size_t)w.bh * T : nullptr;
-    float2 z = w.live ? *reinterpret_cast<const float2 *>(z_start + ((size_t)w.bh * nzs + w.seg) * r + w.i0)
-                      : make_float2(0.f, 0.f);
+    float4 z = w.live ? *reinterpret_cast<const float4 *>(z_start + ((size_t)w.bh * nzs + w.seg) * r + w.i0)
+                      : make_float4(0.f, 0.f, 0.f, 0.f);
     for (int t0 = w.ta; t0 < w.te; t0 += NB) {
         const int nt = min(NB, w.te - t0);
         Raw kr[NB], qr[NB];
 #pragma unroll
         for (int t = 0; t < NB; ++t) {
-            kr[t] = (t < nt && w.live) ? load_pair(kp + (size_t)(t0 + t) * r) : Raw{};
-            qr[t] = (t < nt && w.live) ? load_pair(qp + (size_t)(t0 + t) * r) : Raw{};
+            kr[t] = (t < nt && w.live) ? load_quad(kp + (size_t)(t0 + t) * r) : Raw{};
+            qr[t] = (t < nt && w.live) ? load_quad(qp + (size_t)(t0 + t) * r) : Raw{};
         }
         const float al = (ap && lane < nt) ? ap[t0 + lane] : 1.f;
         float prod[NB];
@@ -220,14 +237,13 @@ bwd_zdot_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k, const floa
             const float a = __shfl_sync(0xffffffffu, al, t);
             prod[t] = 0.f;
             if (t < nt) {
-                const float2 kv = unpack_pair(kr[t]), qv = unpack_pair(qr[t]);
-                z.x = a * z.x + phi_f(kv.x);
-                z.y = a * z.y + phi_f(kv.y);
-                if (w.live) prod[t] = phi_f(qv.x) * z.x + phi_f(qv.y) * z.y;
+                z_step(z, a, unpack_quad(kr[t]));
+                const float4 qv = unpack_quad(qr[t]);
+                if (w.live) prod[t] = phi_f(qv.x) * z.x + phi_f(qv.y) * z.y + phi_f(qv.z) * z.z + phi_f(qv.w) * z.w;
             }
         }
         const float sum = lane_reduce_scatter<NB>(prod, lane);
-        if (lane < nt) atomicAdd(&d_acc[(size_t)w.bh * T + t0 + lane], sum);
+        if (lane < nt) d_acc[(size_t)w.bh * T + t0 + lane] = sum;
     }
 }
 
@@ -711,14 +727,14 @@ cudaError_t launch_bwd_t(const BackwardArgs &a, int B, cudaStream_t stream)
     if (e != cudaSuccess) return e;
     {
         // z_t per segment of kZLen tokens: maps, scan, products
-        const int nzs = (a.T + kZLen - 1) / kZLen, nfg = (a.r + kZFeat - 1) / kZFeat;
-        // zs and z_start are read as pairs: they start on a 16-byte boundary
+        const int nzs = (a.T + kZLen - 1) / kZLen;
+        // zs and z_start are read as float4: they start on a 16-byte boundary (r is a multiple of 4)
         float *zP = fin + BH;
         float *zs = a.ws + (3 * n + BH + (size_t)BH * nzs + 3) / 4 * 4, *zst = zs + (size_t)BH * nzs * a.r;
-        const dim3 grid((unsigned)BH, (nzs + kZWarps - 1) / kZWarps, nfg);
+        const dim3 grid((unsigned)BH, (nzs + kZWarps - 1) / kZWarps, 1);
         bwd_zmap_kernel<Tin><<<grid, 32 * kZWarps, 0, stream>>>(static_cast<const Tin *>(a.k), a.alpha, a.T, a.r, nzs, zs, zP);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
-        bwd_zscan_kernel<<<dim3((unsigned)BH, nfg), 32, 0, stream>>>(a.z0, zs, zP, a.r, nzs, zst);
+        bwd_zscan_kernel<<<dim3((unsigned)BH, 1), 32, 0, stream>>>(a.z0, zs, zP, a.r, nzs, zst);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
         bwd_zdot_kernel<Tin><<<grid, 32 * kZWarps, 0, stream>>>(static_cast<const Tin *>(a.q), static_cast<const Tin *>(a.k),
                                                                 a.alpha, a.T, a.r, nzs, zst, d);

@@ -226,9 +226,9 @@ def test_backward_rejects_bad_arguments(native):
     assert f(ws=None) == native.LA_ERR_WORKSPACE
     assert f(ws_bytes=16) == native.LA_ERR_WORKSPACE
     # d, dd, the dalpha terms [B*H*T] and fin [B*H], then the z pass's maps (P, zs and
-    # z_start per 256-token segment, r <= 128), rounded up to 256 bytes; without a
+    # z_start per 128-token segment, r <= 128), rounded up to 256 bytes; without a
     # device (no SMs) there are no sequence segments and no state-pass workspace
     BH, T = 4 * 16, 4096
-    nzs = (T + 255) // 256
+    nzs = (T + 127) // 128
     floats = BH * (3 * T + 1) + BH * nzs * (1 + 2 * 128) + 4
     assert L.la_backward_workspace_bytes(4, 16, 4096) == (4 * floats + 255) // 256 * 256
