@@ -55,6 +55,12 @@ def prefill_bytes(B, H, T, r, dv, with_state_in=True):
     return B * H * T * per_token_head + B * H * state * (2 if with_state_in else 1)
 
 
+def prefill_flops(B, H, T, r, dv, chunk=64):
+    """Algorithmic FLOPs of the chunked prefill: per token and head the scores and
+    the in-chunk values (2 C r + 2 C dv) and the state read and write (4 r dv)."""
+    return B * H * T * (2 * chunk * r + 2 * chunk * dv + 4 * r * dv)
+
+
 def decode_bytes(B, H, r, dv, elem=2):
     """S and z read and written (FP32), q, k, v read and y written (elem bytes)."""
     return B * H * (2 * 4 * (r * dv + r) + elem * (2 * r + 2 * dv))
@@ -472,7 +478,9 @@ def run_ours(args, rank, world, local_rank):
                     "segment and a long rest)" if ws_bytes else ""),
                 "launches_per_prefill": prefill_launches, "algorithmic_bytes_per_launch": pre_bytes,
                 "launch_us": pre_launch * 1e6, "peak_kind": peak_kind,
-                "prefill_tokens_per_s": B * T * world / pre_launch}
+                "prefill_tokens_per_s": B * T * world / pre_launch,
+                "prefill_token_heads_per_s": B * H * T * world / pre_launch,
+                "tflops": prefill_flops(B, H, T, r, dv, w.chunk) / pre_launch / 1e12}
 
     only = set(args.only.split(",")) if args.only else None
     want = lambda name: only is None or name in only
@@ -548,6 +556,8 @@ def run_ours(args, rank, world, local_rank):
         del psets, graphs, pws
         torch.cuda.empty_cache()
         return {"workload": pw.name, "call_us": t_call * 1e6, "tokens_per_s": pw.B * pw.T * world / t_call,
+                "token_heads_per_s": pw.B * pw.H * pw.T * world / t_call,
+                "tflops": prefill_flops(pw.B, pw.H, pw.T, pw.r, pw.dv, pw.chunk) / t_call / 1e12,
                 "launches_per_call": 3 if nws else 1,
                 "l2": f"{nsets} input set(s) of {nbytes / 1e6:.0f} MB (> 129 MB L2)",
                 "roofline": {"bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s", "frac": gbs / peak,
