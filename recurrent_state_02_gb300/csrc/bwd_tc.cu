@@ -514,9 +514,14 @@ bwd_sweep(const CUtensorMap &map_q, const CUtensorMap &map_k, const CUtensorMap 
 #pragma unroll
                         for (int j = 0; j < 8; ++j) {
                             const float xa = bf16_lo(xw[j]), xb = bf16_hi(xw[j]);
-                            dot += phi_f(xa) * o[2 * j] + phi_f(xb) * o[2 * j + 1];
-                            o[2 * j] *= dphi_f(xa);
-                            o[2 * j + 1] *= dphi_f(xb);
+                            // phi(x) = x + 1 and phi'(x) = 1 for x > 0, both e^x otherwise:
+                            // one exponential serves both
+                            const float ea = __expf(fminf(xa, 0.f)), eb = __expf(fminf(xb, 0.f));
+                            const float pa = xa > 0.f ? xa + 1.f : ea, pb = xb > 0.f ? xb + 1.f : eb;
+                            const float da = xa > 0.f ? 1.f : ea, db = xb > 0.f ? 1.f : eb;
+                            dot += pa * o[2 * j] + pb * o[2 * j + 1];
+                            o[2 * j] *= da;
+                            o[2 * j + 1] *= db;
                         }
                     }
                     uint4 y0, y1;
