@@ -2,8 +2,8 @@
 
 Each translation unit compiles in its own nvcc process (in parallel); the
 objects are linked into one shared library next to this file.  Only the
-CUDA runtime is linked (statically); the driver entry point for TMA
-descriptors is looked up at run time.
+CUDA runtime is linked (statically); the CUDA driver API function that encodes
+TMA descriptors is looked up at run time.
 """
 from __future__ import annotations
 
