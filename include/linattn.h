@@ -275,7 +275,7 @@ la_status la_delta_rule(const void *q, const void *k, const void *v, la_dtype dt
 
 /*
  * la_delta_chunked_workspace_bytes -- bytes of device workspace la_delta_rule_chunked
- * needs for (B, H, T): 16 KB per chunk of 64 tokens per (b, h); 0 when T < 1.
+ * needs for (B, H, T): 32 KB per chunk of 64 tokens per (b, h); 0 when T < 1.
  */
 size_t la_delta_chunked_workspace_bytes(int B, int H, int T);
 
@@ -288,14 +288,15 @@ size_t la_delta_chunked_workspace_bytes(int B, int H, int T);
  * X = V - K S_prev and L = diag(beta) strictly-lower(K K^T), so
  *     V' = T X,  T = (I + L)^{-1} diag(beta),
  *     S_next = S_prev + K^T V',   Y = Q S_prev + (Q K^T masked causally, diagonal kept) V'.
- * The products take BF16 operands (q, k, v as given, S_prev, X, T and V'
- * rounded to BF16) with FP32 accumulation; the state stays FP32 across chunks
- * and T is solved in FP32.  Same arguments, layouts and ownership as
+ * The state chain evaluates V' as U - W S_prev with W = T K and U = T V, which
+ * do not depend on the state.  The products take BF16 operands (q, k, v as
+ * given, S_prev, W, T and V' rounded to BF16) with FP32 accumulation; U and the
+ * state stay FP32 and T is solved in FP32.  Same arguments, layouts and ownership as
  * la_delta_rule, plus
  *   workspace  device buffer of >= la_delta_chunked_workspace_bytes(B, H, T) bytes,
  *              16-byte aligned, owned by the caller (may be NULL when T == 0);
  *              calls sharing it must be ordered.
- * Kernels: T and the masked scores (Q K^T) . M of every chunk (one CTA per
+ * Kernels: T, the masked scores (Q K^T) . M and -W of every chunk (one CTA per
  * chunk) into the workspace, then the state chain, one CTA per (b, h, 64-column
  * slice of v).  Requires dtype BF16,
  * r == 128, dv a multiple of 64, q, k, v, y, S0 and S_out 16-byte aligned, beta

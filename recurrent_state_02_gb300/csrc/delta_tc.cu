@@ -17,18 +17,27 @@
 // [G; P] = [K; Q] K^T on the tensor cores, A from P, and T from G, solved in FP32
 // on CUDA cores in 2 x 2 blocks of 32 tokens (T00 and T11 by forward
 // substitution with one column per lane, T10 = -T11 (K1 K0^T) T00).  Both are
-// stored as the BF16 shared-memory images of the chunk's operand tiles.  The
-// second kernel (delta_tc_kernel) then runs only the part that carries the state:
-//   1  [KS; QS] = [K; Q] S_prev (M = 128)                  (MMA)
-//   2  X = V - KS (BF16)
-//   3  V' = T X                                            (MMA)
-//   4  V' (BF16)
-//   5  [.; O] = [KS; QS] + [0; A] V', S += K^T V'          (MMA)
-//   6  y = O (BF16), S_prev = S (BF16)
-// with one CTA of 256 threads per (b, h, 64-column slice of v); lane 0 of warp 0
-// loads the tiles of a chunk (q, k, v by TMA, A and T by a bulk copy; two stages),
-// lane 0 of warp 1 issues the MMAs, and all 8 warps move accumulators between
-// TMEM and shared memory (warp w: TMEM lane quadrant w % 4, column half w / 4).
+// stored as the BF16 shared-memory images of the chunk's operand tiles.
+//
+// The second kernel (delta_tc_kernel) carries the state.  With W = T K and
+// U = T V (neither depends on the state) the written rows are V' = U - W S_prev,
+// so a chunk needs two dependent rounds of products:
+//   1  [V'; QS] = [U; 0] + [-W; Q] S_prev (M = 128)       (MMA)
+//   2  V' (BF16)
+//   3  [.; O] += [0; A] V', S += K^T V'                    (MMA)
+//   4  S_prev = S (BF16)
+// The per-chunk kernel also forms -W (once per head, where the chain would form
+// it once per value slice) and stores it as the BF16 image of the operand rows,
+// so the chain only loads it.  U of chunk n + 1 = [T; 0] V is formed right after
+// round 3 of chunk n, off the chain, into the second of two accumulator buffers,
+// where round 1 of chunk n + 1 accumulates onto it.  The warps of TMEM lanes
+// 64..127, idle during rounds 1 to 3, store y of chunk n - 1 from the other
+// buffer before U of chunk n + 1 overwrites it, so only S_prev stands between
+// round 3 and the next round 1.  One CTA of 10 warps per (b, h, 64-column slice
+// of v): warps 0..7 move accumulators between TMEM and shared memory (warp w:
+// TMEM lane quadrant w % 4, column half w / 4), lane 0 of warp 8 issues every
+// MMA and lane 0 of warp 9 loads (k, v, q by TMA; A, T and -W by bulk copies;
+// two stages), so that neither waits on the other's work.
 // Operand layouts follow the prefill kernel's: 64-feature blocks and V-shaped
 // tiles of 64 rows x 128 bytes with the 128-byte swizzle, S_prev as four blocks
 // of 16 columns with the 32-byte swizzle.
@@ -55,40 +64,50 @@ constexpr uint32_t kPL = 0;                      // Lt (FP32, 64 x LD): Lt[u][i]
 constexpr uint32_t kPT00 = kPL + kC * LD * 4;    // T00 (FP32, [u][j])
 constexpr uint32_t kPT11t = kPT00 + 32 * LDT * 4;   // T11 transposed (FP32, [u][i])
 constexpr uint32_t kPM = kPT11t + 32 * LDT * 4;  // M = (K1 K0^T) T00 (FP32, [u][j])
+constexpr uint32_t kPK = 0;                      // K again once the solve is done (two 64-feature blocks)
 constexpr uint32_t kPT = 2 * kTQ;                // T (BF16 image)
 constexpr uint32_t kPBeta = kPT + kTV;           // beta of the chunk
 constexpr uint32_t kPSmall = kPBeta + kC * 4;
 static_assert(kPM + 32 * LDT * 4 <= 2 * kTQ, "L and the solve's blocks fit in the K, Q region");
-// workspace per chunk: the A image, then the T image
-constexpr uint32_t kWsChunk = 2 * kTV;
+// workspace per chunk: the A image, the T image, then -W = -T K as the images of
+// its two 64-feature blocks
+constexpr uint32_t kWsChunk = 4 * kTV;
 static_assert(kPT % 1024 == 0 && kPL % 16 == 0 && kPT00 % 16 == 0 && kPT11t % 16 == 0 && kPM % 16 == 0 &&
                   kPSmall % 16 == 0,
               "alignment");
 
 // --------------------------------------------------------- the state chain
-constexpr int kMThreads = 256;
-// a stage: K and Q interleaved by 64-feature block, so that [K; Q] is one
-// 128-row operand per block, then V, a zero tile (rows 0..63 of the operand
-// [0; A]), A and T (A and T arrive together from the workspace)
-constexpr uint32_t kSK0 = 0, kSQ0 = kTQ / 2, kSK1 = kTQ, kSQ1 = kTQ + kTQ / 2, kSV = 2 * kTQ;
-constexpr uint32_t kSZ = kSV + kTV, kSA = kSZ + kTV, kST = kSA + kTV;
-constexpr uint32_t kStage = kST + kTV;           // 64 KB
-constexpr uint32_t kMX = 2 * kStage;             // X (BF16, V-shaped)
-constexpr uint32_t kMVp = kMX + kTV;             // V' (BF16, V-shaped)
+constexpr int kMIssuer = 8, kMLoader = 9;        // warps 0..7 move accumulators, 8 issues MMAs, 9 loads
+constexpr int kMThreads = 32 * (kMLoader + 1);
+// a stage (two): K (two 64-feature blocks), T, a zero tile, A and V, so that
+// [T; 0] and [0; A] are 128-row operands
+constexpr uint32_t kSK = 0, kST = kTQ, kSZ = kST + kTV, kSA = kSZ + kTV, kSV = kSA + kTV;
+constexpr uint32_t kStage = kSV + kTV;           // 48 KB
+constexpr uint32_t kWQ = 2 * kTQ;                // [-W; Q] by 64-feature block: W_b at b kTQ, Q_b after it
+constexpr uint32_t kMWQ = 2 * kStage;            // two [-W; Q] operands
+constexpr uint32_t kMVp = kMWQ + 2 * kWQ;        // V' (BF16, V-shaped)
 constexpr uint32_t kMSp = kMVp + kTV;            // S_prev (BF16, 128 x 64: 4 blocks of 16 columns)
 constexpr uint32_t kMSmall = kMSp + kR * kDS * 2;
-static_assert(kStage % 1024 == 0 && kMX % 1024 == 0 && kMVp % 1024 == 0 && kMSp % 1024 == 0,
+static_assert(kStage % 1024 == 0 && kMWQ % 1024 == 0 && kMVp % 1024 == 0 && kMSp % 1024 == 0,
               "swizzled tiles stay 1024-byte aligned");
-// TMEM columns: [KS; QS] then O (M = 128), V' (M = 64), S (M = 128)
-constexpr uint32_t kCKQ = 0, kCV = 64, kCS = 128, kMCols = 256;
+// TMEM columns (M = 128 accumulators, row = lane): the two buffers [U / V'; QS / O]
+// of even and odd chunks, then S
+constexpr uint32_t kCD0 = 0, kCD1 = 64, kCS = 128, kMCols = 256;
 
 struct alignas(16) DSmall {
-    uint64_t full[2], mma;
+    uint64_t full[2], mma, fin;
+    uint32_t tmem_base;
+    int abort_flag;
+};
+struct alignas(16) MSmall {
+    uint64_t full_tv[2], full_ka[2], full_wq[2];   // the three load groups of a stage
+    uint64_t mma1, mma3;      // rounds 1 and 3 of a chunk complete
+    uint64_t fin;             // every MMA complete (teardown after a timeout)
     uint32_t tmem_base;
     int abort_flag;
 };
 constexpr uint32_t kPSmemBytes = kPSmall + sizeof(DSmall) + 1024;
-constexpr uint32_t kMSmemBytes = kMSmall + sizeof(DSmall) + 1024;
+constexpr uint32_t kMSmemBytes = kMSmall + sizeof(MSmall) + 1024;
 static_assert(kMSmemBytes <= 232448 && kPSmemBytes <= 232448, "shared memory budget");
 
 __device__ __forceinline__ uint8_t *align1024(uint8_t *p)
@@ -103,16 +122,6 @@ __device__ __forceinline__ uint4 pack8(const float *f)
                       pack_bf16x2(f[6], f[7]));
 }
 
-__device__ __forceinline__ void unpack8(uint4 w, float *f)
-{
-    const uint32_t x[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-        f[2 * e] = bf16_lo(x[e]);
-        f[2 * e + 1] = bf16_hi(x[e]);
-    }
-}
-
 __device__ __forceinline__ uint16_t bf16_bits(float x) { return (uint16_t)(pack_bf16x2(x, 0.f) & 0xFFFFu); }
 
 // Element (row, col) of a 64 x 64 BF16 tile with 128-byte rows and the 128-byte swizzle.
@@ -121,9 +130,9 @@ __device__ __forceinline__ uint32_t tile_off(int row, int col)
     return sw128_offset(row, col >> 3) + (uint32_t)(col & 7) * 2;
 }
 
-// A = (Q K^T) . M and T = (I + L)^{-1} diag(beta) of one chunk: one CTA of 128
-// threads per (b, h, chunk).  Writes the 8 KB BF16 images of the A and T tiles
-// to ws.
+// A = (Q K^T) . M, T = (I + L)^{-1} diag(beta) and -W = -T K of one chunk: one
+// CTA of 128 threads per (b, h, chunk).  Writes the BF16 images of the A and T
+// tiles (8 KB each) and of -W (two 64-feature blocks, 8 KB each) to ws.
 __global__ void __launch_bounds__(kPThreads)
 delta_t_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
                const DeltaTcArgs args, int nch)
@@ -143,7 +152,9 @@ delta_t_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant_
 
     if (tid == 0) {
         mbar_init(&sm->full[0], 1);
+        mbar_init(&sm->full[1], 1);
         mbar_init(&sm->mma, 1);
+        mbar_init(&sm->fin, 1);
         sm->abort_flag = 0;
         fence_mbarrier_init();
     }
@@ -299,10 +310,73 @@ delta_t_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant_
                 *reinterpret_cast<uint32_t *>(base + kPT + tile_off(32 + 4 * rg + e, 2 * cp)) =
                     pack_bf16x2(-o4[e].x, -o4[e].y);
         }
+        // the T image (read by the MMAs below) and the solve's blocks (overwritten by
+        // the reload of K) are done with in the generic proxy
+        fence_proxy_async_smem();
         __syncthreads();
+        if (tid == 0) {
+            mbar_arrive_expect_tx(&sm->full[1], kTQ);
+            tma_load_3d(base + kPK, &map_k, &sm->full[1], 0, t0, bh);
+            tma_load_3d(base + kPK + kTV, &map_k, &sm->full[1], 64, t0, bh);
+        }
         uint4 *dst = reinterpret_cast<uint4 *>(wsc + kTV);
         const uint4 *src = reinterpret_cast<const uint4 *>(base + kPT);
         for (int x = tid; x < (int)(kTV / 16); x += kPThreads) dst[x] = src[x];
+
+        // W = T K, one 64-feature block of K at a time (M = 64 into TMEM columns
+        // 0..63: row 16 q + i in lane 32 q + i), stored negated as the BF16 image of
+        // the rows the state chain multiplies by S_prev.  Thread (warp q, lane l):
+        // row 16 q + l % 16, columns 16 (l / 16) + 32 c + [0, 16), c = 0, 1.
+        constexpr uint32_t idW = idesc_bf16_f32(64, 64, false, true);
+        bool wok = true;
+        for (int b = 0; b < 2 && wok; ++b) {
+            if (warp == 1) {
+                if (b == 0) wok = warp_wait(cx, &sm->full[1], 0);
+                if (wok && lane == 0) {
+                    tc_fence_after();
+                    const uint32_t tlo = desc_lo(smem_u32(base + kPT), 16);
+                    const uint32_t klo = desc_lo(smem_u32(base + kPK + b * kTV), kTV);
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk) {
+                        if (kk == 0) tc_mma_bf16_w<false>(tmem, tlo, kHi128, klo, kHi128, idW);
+                        else tc_mma_bf16_w<true>(tmem, tlo + kk * (32 >> 4), kHi128, klo + kk * (2048 >> 4), kHi128, idW);
+                    }
+                    tc_commit(&sm->mma);
+                }
+                __syncwarp();
+            }
+            wok = warp_wait(cx, &sm->mma, (b + 1) & 1) && wok;
+            if (wok) {
+                tc_fence_after();
+                const uint32_t tq = tmem + ((uint32_t)(32 * warp) << 16);
+                const int row = 16 * warp + (lane & 15);
+                float w0[16], w1[16];
+                tc_ld_16x32bx2_x16<16>(tq, w0);
+                tc_ld_16x32bx2_x16<16>(tq + 32, w1);
+                tc_wait_ld();
+#pragma unroll
+                for (int e = 0; e < 16; ++e) {
+                    w0[e] = -w0[e];
+                    w1[e] = -w1[e];
+                }
+                uint8_t *wrow = wsc + (2 + b) * kTV + (size_t)row * 128;
+                const int x0 = 2 * (lane >> 4);   // first 16-byte chunk of the row for c = 0
+                *reinterpret_cast<uint4 *>(wrow + ((x0 ^ (row & 7)) << 4)) = pack8(&w0[0]);
+                *reinterpret_cast<uint4 *>(wrow + (((x0 + 1) ^ (row & 7)) << 4)) = pack8(&w0[8]);
+                *reinterpret_cast<uint4 *>(wrow + (((x0 + 4) ^ (row & 7)) << 4)) = pack8(&w1[0]);
+                *reinterpret_cast<uint4 *>(wrow + (((x0 + 5) ^ (row & 7)) << 4)) = pack8(&w1[8]);
+            }
+            tc_fence_before();
+            wok = !__syncthreads_or(!wok);
+        }
+        if (!wok) {
+            // gave up waiting: the reload and the MMAs already started complete before the CTA exits
+            if (tid == 0) mbar_wait(&sm->full[1], 0, cx.limit);
+            if (warp == 1 && lane == 0) {
+                tc_commit(&sm->fin);
+                mbar_wait(&sm->fin, 0, cx.limit);
+            }
+        }
     } else {
         // gave up waiting: the copy and the MMAs already started complete before the CTA exits
         if (tid == 0) mbar_wait(&sm->full[0], 0, cx.limit);
@@ -319,14 +393,14 @@ delta_t_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant_
     }
 }
 
-// The state chain: one CTA of 256 threads per (b, h, 64-column slice of v).
+// The state chain: one CTA of 10 warps per (b, h, 64-column slice of v).
 __global__ void __launch_bounds__(kMThreads, 1)
 delta_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
                 const __grid_constant__ CUtensorMap map_v, const DeltaTcArgs args, int nch)
 {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *base = align1024(smem_raw);
-    DSmall *sm = reinterpret_cast<DSmall *>(base + kMSmall);
+    MSmall *sm = reinterpret_cast<MSmall *>(base + kMSmall);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int nslice = args.dv / kDS;
@@ -334,52 +408,79 @@ delta_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
     const int T = args.T;
     Ctx cx{&sm->abort_flag, args.wait_limit_ns, args.status};
     const uint8_t *tws = static_cast<const uint8_t *>(args.ws) + (size_t)bh * nch * kWsChunk;
+    const bool issuer = warp == kMIssuer, loader = warp == kMLoader, tm = warp < kMIssuer;
 
     if (tid == 0) {
-        mbar_init(&sm->full[0], 1);
-        mbar_init(&sm->full[1], 1);
-        mbar_init(&sm->mma, 1);
+#pragma unroll
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(&sm->full_tv[s], 1);
+            mbar_init(&sm->full_ka[s], 1);
+            mbar_init(&sm->full_wq[s], 1);
+        }
+        mbar_init(&sm->mma1, 1);
+        mbar_init(&sm->mma3, 1);
+        mbar_init(&sm->fin, 1);
         sm->abort_flag = 0;
         fence_mbarrier_init();
     }
-    if (warp == 1) {
+    if (issuer) {
         tmem_alloc(&sm->tmem_base, kMCols);
         tmem_relinquish();
     }
-    for (int x = tid; x < (int)(2 * kTV / 16); x += kMThreads)   // rows 0..63 of [0; A], both stages
-        reinterpret_cast<uint4 *>(base + (x >= (int)(kTV / 16) ? kStage : 0) + kSZ)[x % (kTV / 16)] =
+    for (int x = tid; x < 2 * (int)(kTV / 16); x += kMThreads)   // the zero tile of both stages
+        reinterpret_cast<uint4 *>(base + (x / (int)(kTV / 16)) * kStage + kSZ)[x % (kTV / 16)] =
             make_uint4(0, 0, 0, 0);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = sm->tmem_base;
 
-    // lane 0 of warp 0: the loads of chunk c into stage c % 2
-    auto issue = [&](int c) {
-        const int s = c & 1, t0 = c * kC;
-        uint8_t *st = base + s * kStage;
-        mbar_arrive_expect_tx(&sm->full[s], kStage - kTV);   // all but the zero tile
-        tma_load_3d(st + kSK0, &map_k, &sm->full[s], 0, t0, bh);
-        tma_load_3d(st + kSQ0, &map_q, &sm->full[s], 0, t0, bh);
-        tma_load_3d(st + kSK1, &map_k, &sm->full[s], 64, t0, bh);
-        tma_load_3d(st + kSQ1, &map_q, &sm->full[s], 64, t0, bh);
-        tma_load_3d(st + kSV, &map_v, &sm->full[s], slice * kDS, t0, bh);
-        bulk_load(st + kSA, tws + (size_t)c * kWsChunk, kWsChunk, &sm->full[s]);   // A, T
+    // Loads of chunk n (lane 0 of the loading warp), in three groups by lifetime:
+    // T and V (read by U of the chunk), K and A (read by round 3), and the
+    // [-W; Q] operand (read by round 1; -W from the workspace, Q by TMA).
+    auto load_tv = [&](int n) {
+        uint8_t *st = base + (n & 1) * kStage;
+        mbar_arrive_expect_tx(&sm->full_tv[n & 1], 2 * kTV);
+        bulk_load(st + kST, tws + (size_t)n * kWsChunk + kTV, kTV, &sm->full_tv[n & 1]);
+        tma_load_3d(st + kSV, &map_v, &sm->full_tv[n & 1], slice * kDS, n * kC, bh);
     };
-    int issued = 0;   // chunks whose loads were started (lane 0 of warp 0)
-    if (tid == 0) {
-        tma_prefetch_desc(&map_q);
-        tma_prefetch_desc(&map_k);
-        tma_prefetch_desc(&map_v);
-        for (; issued < 2 && issued < nch; ++issued) issue(issued);
+    auto load_ka = [&](int n) {
+        uint8_t *st = base + (n & 1) * kStage;
+        mbar_arrive_expect_tx(&sm->full_ka[n & 1], kTQ + kTV);
+        tma_load_3d(st + kSK, &map_k, &sm->full_ka[n & 1], 0, n * kC, bh);
+        tma_load_3d(st + kSK + kTV, &map_k, &sm->full_ka[n & 1], 64, n * kC, bh);
+        bulk_load(st + kSA, tws + (size_t)n * kWsChunk, kTV, &sm->full_ka[n & 1]);
+    };
+    auto load_wq = [&](int n) {
+        uint8_t *wq = base + kMWQ + (n & 1) * kWQ;
+        const uint8_t *w = tws + (size_t)n * kWsChunk + 2 * kTV;
+        mbar_arrive_expect_tx(&sm->full_wq[n & 1], 2 * kTQ);
+        bulk_load(wq, w, kTV, &sm->full_wq[n & 1]);
+        bulk_load(wq + kTQ, w + kTV, kTV, &sm->full_wq[n & 1]);
+        tma_load_3d(wq + kTV, &map_q, &sm->full_wq[n & 1], 0, n * kC, bh);
+        tma_load_3d(wq + kTQ + kTV, &map_q, &sm->full_wq[n & 1], 64, n * kC, bh);
+    };
+    // chunks whose T, V and [-W; Q] loads / K, A loads were started (uniform in
+    // the loading warp)
+    int nld1 = 0, nld2 = 0;
+    if (loader) {
+        if (lane == 0) {
+            tma_prefetch_desc(&map_q);
+            tma_prefetch_desc(&map_k);
+            tma_prefetch_desc(&map_v);
+            for (int c = 0; c < 2 && c < nch; ++c) {
+                load_tv(c);
+                load_ka(c);
+                load_wq(c);
+            }
+        }
+        nld1 = nld2 = nch < 2 ? nch : 2;
     }
-    // Warp w: TMEM lane quadrant q4, column half ch.  The state: S in TMEM (FP32),
-    // S_prev in shared memory (BF16).
-    const int q4 = warp & 3, ch = warp >> 2;
+    // TMEM warps 0..7: lane quadrant q4, column half ch.  The state: S in TMEM
+    // (FP32), S_prev in shared memory (BF16).
+    const int q4 = warp & 3, ch = (warp >> 2) & 1;
     const uint32_t tq = tmem + ((uint32_t)(32 * q4) << 16);
-    const int f = 32 * q4 + lane;          // state row (M = 128 accumulators)
-    const int rm = 16 * q4 + (lane & 15);  // token row of M = 64 accumulators
-    const int cm = 32 * ch + 16 * (lane >> 4);   // their first column for this thread
+    const int f = 32 * q4 + lane;          // accumulator row: state row, or token row of [V'; O]
     auto store_sp = [&](const float (&s)[32]) {
 #pragma unroll
         for (int b = 0; b < 2; ++b) {
@@ -388,7 +489,19 @@ delta_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
             *reinterpret_cast<uint4 *>(blk + sw32_offset(f, 8)) = pack8(&s[16 * b + 8]);
         }
     };
-    {
+    // warps of lanes 64..127: y of chunk n from the rows 64..127 of its buffer
+    auto store_y = [&](int n) {
+        float o[32];
+        tc_ld_32x32b_x32(tq + ((n & 1) ? kCD1 : kCD0) + 32 * ch, o);
+        tc_wait_ld();
+        const int t = n * kC + f - 64;
+        if (t < T) {
+            uint4 *dst = reinterpret_cast<uint4 *>(args.y + ((size_t)bh * T + t) * args.dv + slice * kDS + 32 * ch);
+#pragma unroll
+            for (int m = 0; m < 4; ++m) dst[m] = pack8(&o[8 * m]);
+        }
+    };
+    if (tm) {
         float s[32];
         if (args.S0) {
             const float4 *src = reinterpret_cast<const float4 *>(args.S0 + ((size_t)bh * kR + f) * args.dv +
@@ -410,160 +523,163 @@ delta_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
     }
     __syncthreads();
 
-    constexpr uint32_t idKQ = idesc_bf16_f32(128, 64, false, true);   // [K; Q] S_prev, [0; A] V'
-    constexpr uint32_t idTX = idesc_bf16_f32(64, 64, false, true);    // T X
-    constexpr uint32_t idS = idesc_bf16_f32(128, 64, true, true);     // K^T V'
-    const uint32_t aX = smem_u32(base + kMX);
+    constexpr uint32_t idN64 = idesc_bf16_f32(128, 64, false, true);   // [-W; Q] S_prev, [T; 0] V, [0; A] V'
+    constexpr uint32_t idS = idesc_bf16_f32(128, 64, true, true);      // K^T V'
     const uint32_t aVp = smem_u32(base + kMVp), aSp = smem_u32(base + kMSp);
-    uint32_t mph = 0;       // completions of sm->mma consumed (every thread)
-    int commits = 0;        // commits on sm->mma issued (lane 0 of warp 1)
-    auto mma_wait = [&]() -> bool {
-        const bool ok = warp_wait(cx, &sm->mma, mph & 1);
-        ++mph;
-        tc_fence_after();
-        return ok;
+    // issuing lane: U = [T; 0] V of chunk n into its accumulator buffer (rows
+    // 64..127 start at zero)
+    auto mma_u = [&](int n) {
+        const uint32_t st = smem_u32(base + (n & 1) * kStage);
+        const uint32_t tlo = desc_lo(st + kST, 16), vlo = desc_lo(st + kSV, kTV);
+        const uint32_t d = tmem + ((n & 1) ? kCD1 : kCD0);
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {
+            if (kk == 0) tc_mma_bf16_w<false>(d, tlo, kHi128, vlo, kHi128, idN64);
+            else tc_mma_bf16_w<true>(d, tlo + kk * (32 >> 4), kHi128, vlo + kk * (2048 >> 4), kHi128, idN64);
+        }
     };
 
-    int c = 0;
-    for (; c < nch; ++c) {
-        const int s = c & 1, t0 = c * kC;
-        const uint32_t st = smem_u32(base + s * kStage);
+    bool ok = true;
+    if (issuer) {   // U of chunk 0
+        ok = warp_wait(cx, &sm->full_tv[0], 0);
+        if (ok && lane == 0) {
+            tc_fence_after();
+            mma_u(0);
+        }
+        __syncwarp();
+    }
+    bool failed = __syncthreads_or(!ok);
 
-        // ---- 1: [KS; QS] = [K; Q] S_prev
-        if (warp == 1) {
-            const bool ok = warp_wait(cx, &sm->full[s], (c >> 1) & 1);
+    for (int n = 0; n < nch && !failed; ++n) {
+        const int s = n & 1;
+        const uint32_t st = smem_u32(base + s * kStage);
+        const uint32_t dcol = s ? kCD1 : kCD0;
+        const bool more = n + 1 < nch;
+
+        if (issuer) {
+            // ---- 1: [V'; QS] = [U; 0] + [-W; Q] S_prev
+            ok = warp_wait(cx, &sm->full_wq[s], (n >> 1) & 1);
             if (ok && lane == 0) {
                 tc_fence_after();
-                const uint32_t slo = desc_lo(aSp, kR * 32);
+                const uint32_t slo = desc_lo(aSp, kR * 32), wqlo = desc_lo(smem_u32(base + kMWQ + s * kWQ), 16);
 #pragma unroll
-                for (int kk = 0; kk < 8; ++kk) {
-                    const uint32_t kqlo = desc_lo(st + kSK0, 16) + (((kk >> 2) * kTQ + (kk & 3) * 32) >> 4);
-                    if (kk == 0) tc_mma_bf16_w<false>(tmem + kCKQ, kqlo, kHi128, slo, kHi32, idKQ);
-                    else tc_mma_bf16_w<true>(tmem + kCKQ, kqlo, kHi128, slo + kk * (512 >> 4), kHi32, idKQ);
-                }
-                tc_commit(&sm->mma);
-                ++commits;
+                for (int kk = 0; kk < 8; ++kk)
+                    tc_mma_bf16_w<true>(tmem + dcol, wqlo + (((kk >> 2) * kTQ + (kk & 3) * 32) >> 4), kHi128,
+                                        slo + kk * (512 >> 4), kHi32, idN64);
+                tc_commit(&sm->mma1);
             }
             __syncwarp();
-        }
-        if (__syncthreads_or(!mma_wait())) break;
-
-        // ---- 2: X = V - KS (token rows 0..63 are TMEM lanes 0..63)
-        if (q4 < 2) {
-            float ks[32];
-            tc_ld_32x32b_x32(tq + kCKQ + 32 * ch, ks);
-            tc_wait_ld();
-            const uint8_t *vt = base + s * kStage + kSV;
-#pragma unroll
-            for (int m = 0; m < 4; ++m) {
-                const uint32_t off = sw128_offset(f, 4 * ch + m);
-                float vf[8];
-                unpack8(*reinterpret_cast<const uint4 *>(vt + off), vf);
-#pragma unroll
-                for (int e = 0; e < 8; ++e) vf[e] -= ks[8 * m + e];
-                *reinterpret_cast<uint4 *>(base + kMX + off) = pack8(vf);
-            }
-            fence_proxy_async_smem();
-            tc_fence_before();
-        }
-        __syncthreads();
-
-        // ---- 3: V' = T X
-        if (warp == 1) {
-            if (lane == 0) {
+            // ---- 3 (once V' is stored): O += [0; A] V', S += K^T V'
+            named_barrier_sync(1, 160);
+            ok = ok && warp_wait(cx, &sm->full_ka[s], (n >> 1) & 1);
+            if (ok && lane == 0) {
                 tc_fence_after();
-                const uint32_t tlo = desc_lo(st + kST, 16), xlo = desc_lo(aX, kTV);
-#pragma unroll
-                for (int kk = 0; kk < 4; ++kk) {
-                    if (kk == 0) tc_mma_bf16_w<false>(tmem + kCV, tlo, kHi128, xlo, kHi128, idTX);
-                    else tc_mma_bf16_w<true>(tmem + kCV, tlo + kk * (32 >> 4), kHi128, xlo + kk * (2048 >> 4), kHi128, idTX);
-                }
-                tc_commit(&sm->mma);
-                ++commits;
-            }
-            __syncwarp();
-        }
-        if (__syncthreads_or(!mma_wait())) break;
-
-        // ---- 4: V' as BF16
-        {
-            float vp[16];
-            tc_ld_16x32bx2_x16<16>(tq + kCV + 32 * ch, vp);
-            tc_wait_ld();
-#pragma unroll
-            for (int m = 0; m < 2; ++m)
-                *reinterpret_cast<uint4 *>(base + kMVp + sw128_offset(rm, (cm >> 3) + m)) = pack8(&vp[8 * m]);
-            fence_proxy_async_smem();
-            tc_fence_before();
-        }
-        __syncthreads();
-
-        // ---- 5: O = QS + A V' (rows 64..127 of [KS; QS]), S += K^T V'
-        if (warp == 1) {
-            if (lane == 0) {
-                tc_fence_after();
-                const uint32_t zlo = desc_lo(st + kSZ, 16), vlo = desc_lo(aVp, kTV), klo = desc_lo(st + kSK0, kTQ);
+                const uint32_t zlo = desc_lo(st + kSZ, 16), vlo = desc_lo(aVp, kTV), klo = desc_lo(st + kSK, kTV);
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk)
-                    tc_mma_bf16_w<true>(tmem + kCKQ, zlo + kk * (32 >> 4), kHi128, vlo + kk * (2048 >> 4), kHi128, idKQ);
+                    tc_mma_bf16_w<true>(tmem + dcol, zlo + kk * (32 >> 4), kHi128, vlo + kk * (2048 >> 4), kHi128, idN64);
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk)
                     tc_mma_bf16_w<true>(tmem + kCS, klo + kk * (2048 >> 4), kHi128, vlo + kk * (2048 >> 4), kHi128, idS);
-                tc_commit(&sm->mma);
-                ++commits;
+                tc_commit(&sm->mma3);
             }
             __syncwarp();
-        }
-        if (__syncthreads_or(!mma_wait())) break;
-        // stage s has been read for the last time: load chunk c + 2 into it
-        if (tid == 0 && c + 2 < nch) {
-            issue(c + 2);
-            issued = c + 3;
-        }
-
-        // ---- 6: y = O, S_prev = S (BF16)
-        {
-            const bool last = c + 1 == nch;
-            float sv[32], o[32];
-            if (!last) tc_ld_32x32b_x32(tq + kCS + 32 * ch, sv);
-            if (q4 >= 2) tc_ld_32x32b_x32(tq + kCKQ + 32 * ch, o);
-            tc_wait_ld();
-            const int r = f - 64;   // token row of O
-            if (q4 >= 2 && t0 + r < T) {
-                uint4 *dst = reinterpret_cast<uint4 *>(args.y + ((size_t)bh * T + t0 + r) * args.dv + slice * kDS + 32 * ch);
-#pragma unroll
-                for (int m = 0; m < 4; ++m) dst[m] = pack8(&o[8 * m]);
+            // U of the next chunk, once y of the previous one (same buffer) has been read
+            named_barrier_sync(2, 160);
+            if (more) {
+                ok = ok && warp_wait(cx, &sm->full_tv[s ^ 1], ((n + 1) >> 1) & 1);
+                if (ok && lane == 0) {
+                    tc_fence_after();
+                    mma_u(n + 1);
+                }
+                __syncwarp();
             }
-            if (!last) {
+        } else if (loader) {
+            // stage s and [-W; Q] buffer s: chunk n + 2 once chunk n has been read
+            if (n + 2 < nch) {
+                ok = warp_wait(cx, &sm->mma1, n & 1);   // round 1 read [-W; Q]; U of the chunk read T, V before it
+                if (ok) {
+                    if (lane == 0) {
+                        load_tv(n + 2);
+                        load_wq(n + 2);
+                    }
+                    nld1 = n + 3;
+                }
+                ok = ok && warp_wait(cx, &sm->mma3, n & 1);   // round 3 read K, A
+                if (ok) {
+                    if (lane == 0) load_ka(n + 2);
+                    nld2 = n + 3;
+                }
+                __syncwarp();
+            }
+        } else {
+            if (q4 < 2) {
+                // ---- 2: V' as BF16 (TMEM lanes 0..63)
+                ok = warp_wait(cx, &sm->mma1, n & 1);
+                if (ok) {
+                    tc_fence_after();
+                    float vp[32];
+                    tc_ld_32x32b_x32(tq + dcol + 32 * ch, vp);
+                    tc_wait_ld();
+#pragma unroll
+                    for (int m = 0; m < 4; ++m)
+                        *reinterpret_cast<uint4 *>(base + kMVp + sw128_offset(f, 4 * ch + m)) = pack8(&vp[8 * m]);
+                    fence_proxy_async_smem();
+                    tc_fence_before();
+                }
+                named_barrier_sync(1, 160);
+            } else {
+                // y of the previous chunk, before U of the next chunk reuses its buffer
+                if (n >= 1) {
+                    tc_fence_after();
+                    store_y(n - 1);
+                    tc_fence_before();
+                }
+                named_barrier_sync(2, 160);
+            }
+            // ---- 4: S_prev = S (BF16)
+            ok = ok && warp_wait(cx, &sm->mma3, n & 1);
+            if (ok && more) {
+                tc_fence_after();
+                float sv[32];
+                tc_ld_32x32b_x32(tq + kCS + 32 * ch, sv);
+                tc_wait_ld();
                 store_sp(sv);
                 fence_proxy_async_smem();
             }
             tc_fence_before();
         }
-        __syncthreads();
+        failed = __syncthreads_or(!ok);
     }
 
     // ---------------------------------------------------------- teardown
-    if (c == nch) {
-        float sv[32];
-        tc_ld_32x32b_x32(tq + kCS + 32 * ch, sv);
-        tc_wait_ld();
-        float4 *dst = reinterpret_cast<float4 *>(args.S_out + ((size_t)bh * kR + f) * args.dv + slice * kDS + 32 * ch);
+    if (!failed) {
+        if (tm) {
+            tc_fence_after();
+            if (q4 >= 2) store_y(nch - 1);
+            float sv[32];
+            tc_ld_32x32b_x32(tq + kCS + 32 * ch, sv);
+            tc_wait_ld();
+            float4 *dst = reinterpret_cast<float4 *>(args.S_out + ((size_t)bh * kR + f) * args.dv + slice * kDS + 32 * ch);
 #pragma unroll
-        for (int m = 0; m < 8; ++m) dst[m] = make_float4(sv[4 * m], sv[4 * m + 1], sv[4 * m + 2], sv[4 * m + 3]);
-        tc_fence_before();
-    } else {
-        // gave up waiting: the loads and MMAs already started complete before the CTA exits
-        if (tid == 0)
-            for (int cc = (issued > 2 ? issued - 2 : 0); cc < issued; ++cc)
-                mbar_wait(&sm->full[cc & 1], (cc >> 1) & 1, cx.limit);
-        if (warp == 1 && lane == 0) {
-            tc_commit(&sm->mma);
-            mbar_wait(&sm->mma, commits & 1, cx.limit);
+            for (int m = 0; m < 8; ++m) dst[m] = make_float4(sv[4 * m], sv[4 * m + 1], sv[4 * m + 2], sv[4 * m + 3]);
+            tc_fence_before();
         }
+    } else if (loader && lane == 0) {
+        // gave up waiting: the loads already started complete before the CTA exits
+        for (int cc = (nld1 > 2 ? nld1 - 2 : 0); cc < nld1; ++cc) {
+            mbar_wait(&sm->full_tv[cc & 1], (cc >> 1) & 1, cx.limit);
+            mbar_wait(&sm->full_wq[cc & 1], (cc >> 1) & 1, cx.limit);
+        }
+        for (int cc = (nld2 > 2 ? nld2 - 2 : 0); cc < nld2; ++cc)
+            mbar_wait(&sm->full_ka[cc & 1], (cc >> 1) & 1, cx.limit);
+    } else if (issuer && lane == 0) {
+        // and so do the MMAs
+        tc_commit(&sm->fin);
+        mbar_wait(&sm->fin, 0, cx.limit);
     }
     __syncthreads();
-    if (warp == 1) {
+    if (issuer) {
         tc_fence_after();
         tmem_dealloc(tmem, kMCols);
     }

@@ -178,13 +178,13 @@ def test_delta_chunked_rejects_bad_arguments(native):
 
     def f(**kw):
         a = dict(q=FAKE, k=FAKE, v=FAKE, dtype=native.LA_DTYPE_BF16, beta=None, S0=None, B=1, H=1, T=64, r=128,
-                 dv=128, y=FAKE, S_out=FAKE, ws=FAKE, ws_bytes=16384)
+                 dv=128, y=FAKE, S_out=FAKE, ws=FAKE, ws_bytes=32768)
         a.update(kw)
         return L.la_delta_rule_chunked(a["q"], a["k"], a["v"], a["dtype"], a["beta"], a["S0"], a["B"], a["H"],
                                        a["T"], a["r"], a["dv"], a["y"], a["S_out"], a["ws"], a["ws_bytes"], None)
 
-    assert L.la_delta_chunked_workspace_bytes(4, 16, 4096) == 4 * 16 * 64 * 16384
-    assert L.la_delta_chunked_workspace_bytes(1, 1, 65) == 2 * 16384
+    assert L.la_delta_chunked_workspace_bytes(4, 16, 4096) == 4 * 16 * 64 * 32768
+    assert L.la_delta_chunked_workspace_bytes(1, 1, 65) == 2 * 32768
     assert L.la_delta_chunked_workspace_bytes(1, 1, 0) == 0
 
     assert f(k=None) == native.LA_ERR_NULL

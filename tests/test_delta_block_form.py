@@ -15,6 +15,9 @@ Y = Q S_prev + ((Q K^T) . M) V' (M causal with its diagonal).  The per-chunk ker
 forms T by blocks: the diagonal blocks by forward substitution, the lower block of
 a 2 x 2 split as -T11 (K1 K0^T) T00.
 
+The chain kernel takes the state-independent products first: with W = T K and
+U = T V, V' = U - W S_prev.
+
 These tests write that algebra out in numpy (FP64) and hold it to the oracle,
 so that the reading the GPU path rests on is pinned outside the GPU path."""
 import numpy as np
@@ -33,6 +36,29 @@ def _chunk_form(q, k, v, beta, S0, C):
         Tm = np.linalg.solve(np.eye(n) + L, np.diag(b))
         Vp = Tm @ (V - K @ S)
         y[t0:t0 + n] = Q @ S + np.tril(Q @ K.T) @ Vp
+        S = S + K.T @ Vp
+    return y, S
+
+
+def _chunk_form_wu(q, k, v, beta, S0, C):
+    """The same chunk with the state-independent products taken first, as the
+    chain kernel forms them: W = T K and U = T V, then one stacked product
+    [U; 0] + [-W; Q] S_prev gives [V'; Q S_prev], and [0; A] V' adds the
+    in-chunk reads to the lower half."""
+    T = q.shape[0]
+    S = S0.copy()
+    y = np.empty((T, v.shape[1]))
+    for t0 in range(0, T, C):
+        Q, K, V, b = q[t0:t0 + C], k[t0:t0 + C], v[t0:t0 + C], beta[t0:t0 + C]
+        n = K.shape[0]
+        L = np.tril(b[:, None] * (K @ K.T), -1)
+        Tm = np.linalg.solve(np.eye(n) + L, np.diag(b))
+        W, U = Tm @ K, Tm @ V
+        D = np.vstack([U, np.zeros((n, V.shape[1]))]) + np.vstack([-W, Q]) @ S
+        Vp = D[:n]
+        A = np.tril(Q @ K.T)
+        D = D + np.vstack([np.zeros((n, n)), A]) @ Vp
+        y[t0:t0 + n] = D[n:]
         S = S + K.T @ Vp
     return y, S
 
@@ -70,6 +96,17 @@ def test_chunk_form_equals_token_recurrence(oracle_mod, T, C):
     y_ref, S_ref = oracle_mod.delta(q[None, None], k[None, None], v[None, None], beta=beta[None, None],
                                     S0=S0[None, None])
     y, S = _chunk_form(q, k, v, beta, S0, C)
+    assert np.max(np.abs(y - y_ref[0, 0])) <= 1e-12 * np.max(np.abs(y_ref))
+    assert np.max(np.abs(S - S_ref[0, 0])) <= 1e-12 * np.max(np.abs(S_ref))
+
+
+@pytest.mark.parametrize("T,C", [(1, 64), (64, 64), (200, 64), (97, 16)])
+def test_precomputed_products_form_equals_token_recurrence(oracle_mod, T, C):
+    rng = np.random.default_rng(2000 + T + C)
+    q, k, v, beta, S0 = _inputs(rng, T, 24, 16)
+    y_ref, S_ref = oracle_mod.delta(q[None, None], k[None, None], v[None, None], beta=beta[None, None],
+                                    S0=S0[None, None])
+    y, S = _chunk_form_wu(q, k, v, beta, S0, C)
     assert np.max(np.abs(y - y_ref[0, 0])) <= 1e-12 * np.max(np.abs(y_ref))
     assert np.max(np.abs(S - S_ref[0, 0])) <= 1e-12 * np.max(np.abs(S_ref))
 

@@ -154,9 +154,9 @@ def test_delta_full_size_sampled_heads(la, oracle_mod):
 
 # ---------------------------------------------------------------- chunked form
 # la_delta_rule_chunked rounds the operands of its products to BF16 (S_prev,
-# X = V - K S_prev, T and V'), with FP32 accumulation and an FP32 state; a
-# simulation of that rounding on unit keys gives about 5e-3 relative to the
-# largest entry on y and S over 2048 tokens.  Both are held to 2e-2.
+# W = T K, T and V'), with FP32 accumulation and an FP32 state; a simulation of
+# that rounding on unit keys gives about 5e-3 relative to the largest entry on
+# y and S over 2048 tokens.  Both are held to 2e-2.
 TOL_TC = 2e-2
 
 TC_CASES = [
