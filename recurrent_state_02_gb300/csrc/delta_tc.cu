@@ -540,13 +540,14 @@ delta_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
     };
 
     bool ok = true;
-    if (issuer) {   // U of chunk 0
+    if (issuer) {   // U of chunk 0; its [-W; Q] operand
         ok = warp_wait(cx, &sm->full_tv[0], 0);
         if (ok && lane == 0) {
             tc_fence_after();
             mma_u(0);
         }
         __syncwarp();
+        ok = ok && warp_wait(cx, &sm->full_wq[0], 0);
     }
     bool failed = __syncthreads_or(!ok);
 
@@ -557,8 +558,8 @@ delta_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
         const bool more = n + 1 < nch;
 
         if (issuer) {
-            // ---- 1: [V'; QS] = [U; 0] + [-W; Q] S_prev
-            ok = warp_wait(cx, &sm->full_wq[s], (n >> 1) & 1);
+            // ---- 1: [V'; QS] = [U; 0] + [-W; Q] S_prev ([-W; Q] was waited for
+            // before the previous chunk's closing barrier)
             if (ok && lane == 0) {
                 tc_fence_after();
                 const uint32_t slo = desc_lo(aSp, kR * 32), wqlo = desc_lo(smem_u32(base + kMWQ + s * kWQ), 16);
@@ -570,8 +571,8 @@ delta_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
             }
             __syncwarp();
             // ---- 3 (once V' is stored): O += [0; A] V', S += K^T V'
-            named_barrier_sync(1, 160);
             ok = ok && warp_wait(cx, &sm->full_ka[s], (n >> 1) & 1);
+            named_barrier_sync(1, 160);
             if (ok && lane == 0) {
                 tc_fence_after();
                 const uint32_t zlo = desc_lo(st + kSZ, 16), vlo = desc_lo(aVp, kTV), klo = desc_lo(st + kSK, kTV);
@@ -593,6 +594,7 @@ delta_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
                     mma_u(n + 1);
                 }
                 __syncwarp();
+                ok = ok && warp_wait(cx, &sm->full_wq[s ^ 1], ((n + 1) >> 1) & 1);
             }
         } else if (loader) {
             // stage s and [-W; Q] buffer s: chunk n + 2 once chunk n has been read
