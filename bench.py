@@ -645,20 +645,37 @@ def run_ours(args, rank, world, local_rank):
                                                 P(ybw), P(dybw), None, None, P(gq), P(gk), P(gv), P(ga), P(gS0), P(gz0),
                                                 P(wsb), wsb.numel(), sh), "la_prefill_backward")
 
+        # the same backward with the forward's saved denominators (no z pass)
+        dbw = torch.empty((bw.B, bw.H, bw.T), device=dev, dtype=torch.float32)
+
+        def k_backward_saved():
+            _native.check(L.la_prefill_backward_saved(P(bin_["q"]), P(bin_["k"]), P(bin_["v"]), _native.LA_DTYPE_BF16,
+                                                      P(bin_["alpha"]), None, None, bw.B, bw.H, bw.T, bw.r, bw.dv,
+                                                      P(ybw), P(dybw), P(dbw), None, None, P(gq), P(gk), P(gv), P(ga),
+                                                      P(gS0), P(gz0), P(wsb), wsb.numel(), sh),
+                          "la_prefill_backward_saved")
+
         with torch.cuda.stream(stream):
-            _native.check(L.la_prefill_chunked(P(bin_["q"]), P(bin_["k"]), P(bin_["v"]), _native.LA_DTYPE_BF16,
-                                               P(bin_["alpha"]), None, None, bw.B, bw.H, bw.T, bw.r, bw.dv, bw.chunk,
-                                               bw.eps, P(ybw), P(Sbw), P(zbw), None, 0, sh), "la_prefill_chunked")
+            _native.check(L.la_prefill_chunked_save(P(bin_["q"]), P(bin_["k"]), P(bin_["v"]), _native.LA_DTYPE_BF16,
+                                                    P(bin_["alpha"]), None, None, bw.B, bw.H, bw.T, bw.r, bw.dv,
+                                                    bw.chunk, bw.eps, P(ybw), P(Sbw), P(zbw), P(dbw), None, 0, sh),
+                          "la_prefill_chunked_save")
             k_backward()
+            k_backward_saved()
         gb = torch.cuda.CUDAGraph()
         with torch.cuda.graph(gb, stream=stream):
             k_backward()
+        gbs = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gbs, stream=stream):
+            k_backward_saved()
         bsteps = max(1, min(args.steps, 20))
         b_s = timed([gb] * N_ROT, bsteps, max(3, min(args.warmup, 3)))
-        b_s, = reduce_max([b_s], dev, dist)
+        bs_s = timed([gbs] * N_ROT, bsteps, max(3, min(args.warmup, 3)))
+        b_s, bs_s = reduce_max([b_s, bs_s], dev, dist)
         assert _native.lib().la_last_device_status(sh) == 0
-        b_call = b_s / bsteps
+        b_call, bs_call = b_s / bsteps, bs_s / bsteps
         b_bytes = backward_bytes(bw.B, bw.H, bw.T, bw.r, bw.dv, True)
+        bs_bytes = b_bytes + 4 * bw.B * bw.H * bw.T   # and the saved d_t (FP32) read
         b_gbs = b_bytes / b_call / 1e9
         backward = {"workload": bw.name.replace("prefill", "backward of the gated prefill,"), "call_us": b_call * 1e6,
                     "launches_per_call": 12, "tokens_per_s": bw.B * bw.T * world / b_call, "steps": bsteps,
@@ -666,7 +683,14 @@ def run_ours(args, rank, world, local_rank):
                                  "frac": b_gbs / peak, "peak_kind": peak_kind, "scope": "whole call",
                                  "algorithmic_bytes_per_call": b_bytes,
                                  "tensor_tflops": backward_flops(bw.B, bw.H, bw.T, bw.r, bw.dv, True) / b_call / 1e12,
-                                 "algorithmic_flops_per_call": backward_flops(bw.B, bw.H, bw.T, bw.r, bw.dv, True)}}
+                                 "algorithmic_flops_per_call": backward_flops(bw.B, bw.H, bw.T, bw.r, bw.dv, True)},
+                    "saved_d": {"entry": "la_prefill_backward_saved (d from la_prefill_chunked_save)",
+                                "call_us": bs_call * 1e6, "launches_per_call": 9,
+                                "tokens_per_s": bw.B * bw.T * world / bs_call,
+                                "roofline": {"bound": "hbm", "achieved": bs_bytes / bs_call / 1e9, "peak": peak,
+                                             "unit": "GB/s", "frac": bs_bytes / bs_call / 1e9 / peak,
+                                             "peak_kind": peak_kind, "scope": "whole call",
+                                             "algorithmic_bytes_per_call": bs_bytes}}}
 
     if want("e2e"):
         # end to end through the public API with host buffers (pinned), every step:

@@ -249,6 +249,37 @@ la_status la_prefill_backward(const void *q, const void *k, const void *v, la_dt
                               size_t workspace_bytes, la_stream_t stream);
 
 /*
+ * la_prefill_chunked_save -- la_prefill_chunked that also keeps, for training, the
+ * denominator of every output row: d_t = phi(q_t) . z_t + eps, the normaliser of
+ * [LA] "公式里的每个维度" (y_t = phi(q_t)^T S_t / d_t), in FP32.
+ * la_prefill_backward_saved takes it instead of recomputing it.
+ *   d_out  device FP32 [B,H,T], 4-byte aligned, owned by the caller.
+ *   Everything else as for la_prefill_chunked.
+ * BF16: the chunk kernel's own denominator (the BF16 operands of its products,
+ * FP32 accumulation), the one y was divided by; FP32: the exact recurrence's.
+ * Errors: those of la_prefill_chunked; LA_ERR_NULL when d_out is NULL.
+ */
+la_status la_prefill_chunked_save(const void *q, const void *k, const void *v, la_dtype dtype, const float *alpha,
+                                  const float *S0, const float *z0, int B, int H, int T, int r, int dv, int chunk,
+                                  float eps, void *y, float *S_out, float *z_out, float *d_out, void *workspace,
+                                  size_t workspace_bytes, la_stream_t stream);
+
+/*
+ * la_prefill_backward_saved -- la_prefill_backward with d_t taken from
+ * la_prefill_chunked_save instead of recomputed: the z_t recurrence over the
+ * sequence (three of the backward's launches) is skipped.
+ *   d      device FP32 [B,H,T] from la_prefill_chunked_save on the same inputs
+ *          (eps is included in it, so there is no eps argument).
+ *   Everything else as for la_prefill_backward.
+ * Errors: those of la_prefill_backward; LA_ERR_NULL when d is NULL.
+ */
+la_status la_prefill_backward_saved(const void *q, const void *k, const void *v, la_dtype dtype, const float *alpha,
+                                    const float *S0, const float *z0, int B, int H, int T, int r, int dv,
+                                    const void *y, const void *dy, const float *d, const float *dS_T,
+                                    const float *dz_T, void *dq, void *dk, void *dv_out, float *dalpha, float *dS0,
+                                    float *dz0, void *workspace, size_t workspace_bytes, la_stream_t stream);
+
+/*
  * la_delta_rule -- the delta-rule memory ([LA] "Delta rule：先读旧答案，再写误差"): a
  * state without the normaliser that, per token, reads its current answer for the
  * key, writes back beta times the error, and is then read by the query:

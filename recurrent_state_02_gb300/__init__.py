@@ -77,6 +77,22 @@ def prefill_chunked(q, k, v, alpha=None, S0=None, z0=None, chunk=64, eps=1e-6, y
     """Chunkwise prefill.  q, k [B,H,T,r], v [B,H,T,dv] (bf16 or fp32, same dtype);
     alpha [B,H,T] fp32 or None; S0 [B,H,r,dv], z0 [B,H,r] fp32 or None.
     Returns (y [B,H,T,dv] in the input dtype, S_T, z_T)."""
+    return _prefill(q, k, v, alpha, S0, z0, chunk, eps, y, S_out, z_out, workspace, None)
+
+
+def prefill_chunked_save(q, k, v, alpha=None, S0=None, z0=None, chunk=64, eps=1e-6, y=None, S_out=None, z_out=None,
+                         d_out=None, workspace=None):
+    """prefill_chunked that also returns d [B,H,T] fp32, the denominator of every
+    output row (phi(q_t) . z_t + eps), for prefill_backward(..., d=d).
+    Returns (y, S_T, z_T, d)."""
+    B, H, T, _ = q.shape
+    if d_out is None:
+        d_out = torch.empty((B, H, T), device=q.device, dtype=torch.float32)
+    _require(d_out, "d_out", (B, H, T), torch.float32, q.device)
+    return _prefill(q, k, v, alpha, S0, z0, chunk, eps, y, S_out, z_out, workspace, d_out) + (d_out,)
+
+
+def _prefill(q, k, v, alpha, S0, z0, chunk, eps, y, S_out, z_out, workspace, d_out):
     if q.dtype not in _DTYPES:
         raise ValueError(f"unsupported dtype {q.dtype}")
     B, H, T, r = q.shape
@@ -102,10 +118,16 @@ def prefill_chunked(q, k, v, alpha=None, S0=None, z0=None, chunk=64, eps=1e-6, y
         workspace = torch.empty(need, device=dev, dtype=torch.uint8)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     with _device_guard(dev):
-        st = _native.lib().la_prefill_chunked(
-            _ptr(q), _ptr(k), _ptr(v), _DTYPES[q.dtype], _ptr(alpha), _ptr(S0), _ptr(z0), B, H, T, r, dv, chunk,
-            float(eps), _ptr(y), _ptr(S_out), _ptr(z_out), _ptr(workspace), ws_bytes, _stream(dev))
-    _native.check(st, "la_prefill_chunked")
+        if d_out is None:
+            st = _native.lib().la_prefill_chunked(
+                _ptr(q), _ptr(k), _ptr(v), _DTYPES[q.dtype], _ptr(alpha), _ptr(S0), _ptr(z0), B, H, T, r, dv, chunk,
+                float(eps), _ptr(y), _ptr(S_out), _ptr(z_out), _ptr(workspace), ws_bytes, _stream(dev))
+            _native.check(st, "la_prefill_chunked")
+        else:
+            st = _native.lib().la_prefill_chunked_save(
+                _ptr(q), _ptr(k), _ptr(v), _DTYPES[q.dtype], _ptr(alpha), _ptr(S0), _ptr(z0), B, H, T, r, dv, chunk,
+                float(eps), _ptr(y), _ptr(S_out), _ptr(z_out), _ptr(d_out), _ptr(workspace), ws_bytes, _stream(dev))
+            _native.check(st, "la_prefill_chunked_save")
     return y, S_out, z_out
 
 
@@ -201,10 +223,13 @@ def decode_step(q, k, v, S, z, alpha=None, eps=1e-6, y=None):
     return y
 
 
-def prefill_backward(q, k, v, y, dy, alpha=None, S0=None, z0=None, dS_T=None, dz_T=None, eps=1e-6, workspace=None):
+def prefill_backward(q, k, v, y, dy, alpha=None, S0=None, z0=None, dS_T=None, dz_T=None, eps=1e-6, workspace=None,
+                     d=None):
     """Gradients of prefill_chunked: given the forward inputs, its output y and
     dy [B,H,T,dv] (and optionally dS_T [B,H,r,dv], dz_T [B,H,r] in fp32), returns
-    (dq, dk, dv, dalpha or None, dS0, dz0); dq, dk, dv in the input dtype."""
+    (dq, dk, dv, dalpha or None, dS0, dz0); dq, dk, dv in the input dtype.
+    d: the [B,H,T] fp32 denominators from prefill_chunked_save (eps is then not
+    used), or None to recompute them."""
     if q.dtype not in _DTYPES:
         raise ValueError(f"unsupported dtype {q.dtype}")
     B, H, T, r = q.shape
@@ -218,6 +243,7 @@ def prefill_backward(q, k, v, y, dy, alpha=None, S0=None, z0=None, dS_T=None, dz
     _require(z0, "z0", (B, H, r), torch.float32, dev)
     _require(dS_T, "dS_T", (B, H, r, dvd), torch.float32, dev)
     _require(dz_T, "dz_T", (B, H, r), torch.float32, dev)
+    _require(d, "d", (B, H, T), torch.float32, dev)
     dq, dk, dv_out = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
     dalpha = torch.empty((B, H, T), device=dev, dtype=torch.float32) if alpha is not None else None
     dS0 = torch.empty((B, H, r, dvd), device=dev, dtype=torch.float32)
@@ -227,11 +253,18 @@ def prefill_backward(q, k, v, y, dy, alpha=None, S0=None, z0=None, dS_T=None, dz
         workspace = torch.empty(need, device=dev, dtype=torch.uint8)
     ws_bytes = workspace.numel() * workspace.element_size()
     with _device_guard(dev):
-        st = _native.lib().la_prefill_backward(
-            _ptr(q), _ptr(k), _ptr(v), _DTYPES[q.dtype], _ptr(alpha), _ptr(S0), _ptr(z0), B, H, T, r, dvd, float(eps),
-            _ptr(y), _ptr(dy), _ptr(dS_T), _ptr(dz_T), _ptr(dq), _ptr(dk), _ptr(dv_out), _ptr(dalpha), _ptr(dS0),
-            _ptr(dz0), _ptr(workspace), ws_bytes, _stream(dev))
-    _native.check(st, "la_prefill_backward")
+        if d is None:
+            st = _native.lib().la_prefill_backward(
+                _ptr(q), _ptr(k), _ptr(v), _DTYPES[q.dtype], _ptr(alpha), _ptr(S0), _ptr(z0), B, H, T, r, dvd,
+                float(eps), _ptr(y), _ptr(dy), _ptr(dS_T), _ptr(dz_T), _ptr(dq), _ptr(dk), _ptr(dv_out), _ptr(dalpha),
+                _ptr(dS0), _ptr(dz0), _ptr(workspace), ws_bytes, _stream(dev))
+            _native.check(st, "la_prefill_backward")
+        else:
+            st = _native.lib().la_prefill_backward_saved(
+                _ptr(q), _ptr(k), _ptr(v), _DTYPES[q.dtype], _ptr(alpha), _ptr(S0), _ptr(z0), B, H, T, r, dvd,
+                _ptr(y), _ptr(dy), _ptr(d), _ptr(dS_T), _ptr(dz_T), _ptr(dq), _ptr(dk), _ptr(dv_out), _ptr(dalpha),
+                _ptr(dS0), _ptr(dz0), _ptr(workspace), ws_bytes, _stream(dev))
+            _native.check(st, "la_prefill_backward_saved")
     return dq, dk, dv_out, dalpha, dS0, dz0
 
 

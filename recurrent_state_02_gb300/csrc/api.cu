@@ -264,10 +264,11 @@ size_t la_prefill_workspace_bytes(int B, int H, int T, int r, int dv, int chunk)
     return seg_workspace_bytes(seg_plan(B, H, T, dv), B, H, dv);
 }
 
-la_status la_prefill_chunked(const void *q, const void *k, const void *v, la_dtype dtype, const float *alpha,
-                             const float *S0, const float *z0, int B, int H, int T, int r, int dv, int chunk,
-                             float eps, void *y, float *S_out, float *z_out, void *workspace,
-                             size_t workspace_bytes, la_stream_t stream)
+// la_prefill_chunked and la_prefill_chunked_save; d_out may be nullptr.
+static la_status prefill_chunked_impl(const void *q, const void *k, const void *v, la_dtype dtype,
+                                      const float *alpha, const float *S0, const float *z0, int B, int H, int T,
+                                      int r, int dv, int chunk, float eps, void *y, float *S_out, float *z_out,
+                                      float *d_out, void *workspace, size_t workspace_bytes, la_stream_t stream)
 {
     if (!q || !k || !v || !y || !S_out || !z_out) return LA_ERR_NULL;
     if (B < 1 || H < 1 || T < 1 || r < 1 || dv < 1 || chunk < 1) return LA_ERR_SHAPE;
@@ -276,12 +277,12 @@ la_status la_prefill_chunked(const void *q, const void *k, const void *v, la_dty
 
     if (dtype == LA_DTYPE_FP32) {
         if (r > 256 || dv > 256) return LA_ERR_UNSUPPORTED;
-        const void *ptrs[] = {q, k, v, y, S_out, z_out, alpha, S0, z0};
+        const void *ptrs[] = {q, k, v, y, S_out, z_out, alpha, S0, z0, d_out};
         for (const void *p : ptrs)
             if (p && !aligned(p, 4)) return LA_ERR_ALIGN;
         return from_cuda(la::launch_prefill_f32(static_cast<const float *>(q), static_cast<const float *>(k),
                                                 static_cast<const float *>(v), alpha, S0, z0, B, H, T, r, dv, eps,
-                                                static_cast<float *>(y), S_out, z_out, st));
+                                                static_cast<float *>(y), S_out, z_out, st, d_out));
     }
 
     // BF16: tensor-core kernel.  It computes in chunks of 64 tokens whatever chunk
@@ -293,7 +294,7 @@ la_status la_prefill_chunked(const void *q, const void *k, const void *v, la_dty
         const void *ptrs16[] = {q, k, v, y, S_out};
         for (const void *p : ptrs16)
             if (!aligned(p, 16)) return LA_ERR_ALIGN;
-        const void *ptrs4[] = {alpha, S0, z0, z_out};
+        const void *ptrs4[] = {alpha, S0, z0, z_out, d_out};
         for (const void *p : ptrs4)
             if (p && !aligned(p, 4)) return LA_ERR_ALIGN;
     }
@@ -319,6 +320,7 @@ la_status la_prefill_chunked(const void *q, const void *k, const void *v, la_dty
     a.S_out = S_out;
     a.z_out = z_out;
     a.y = static_cast<uint16_t *>(y);
+    a.d_out = d_out;
     a.H = H;
     a.T = T;
     a.dv = dv;
@@ -358,6 +360,25 @@ la_status la_prefill_chunked(const void *q, const void *k, const void *v, la_dty
         a.S_start = S_start;
     }
     return from_cuda(la::launch_prefill_tc(mq, mk, mv, a, B, alpha != nullptr, plan.dvs, st));
+}
+
+la_status la_prefill_chunked(const void *q, const void *k, const void *v, la_dtype dtype, const float *alpha,
+                             const float *S0, const float *z0, int B, int H, int T, int r, int dv, int chunk,
+                             float eps, void *y, float *S_out, float *z_out, void *workspace,
+                             size_t workspace_bytes, la_stream_t stream)
+{
+    return prefill_chunked_impl(q, k, v, dtype, alpha, S0, z0, B, H, T, r, dv, chunk, eps, y, S_out, z_out, nullptr,
+                                workspace, workspace_bytes, stream);
+}
+
+la_status la_prefill_chunked_save(const void *q, const void *k, const void *v, la_dtype dtype, const float *alpha,
+                                  const float *S0, const float *z0, int B, int H, int T, int r, int dv, int chunk,
+                                  float eps, void *y, float *S_out, float *z_out, float *d_out, void *workspace,
+                                  size_t workspace_bytes, la_stream_t stream)
+{
+    if (!d_out) return LA_ERR_NULL;
+    return prefill_chunked_impl(q, k, v, dtype, alpha, S0, z0, B, H, T, r, dv, chunk, eps, y, S_out, z_out, d_out,
+                                workspace, workspace_bytes, stream);
 }
 
 la_status la_prefill_varlen(const void *q, const void *k, const void *v, la_dtype dtype, const float *alpha,
@@ -455,11 +476,13 @@ size_t la_backward_workspace_bytes(int B, int H, int T)
     return bwd_base_bytes(B, H, T) + 2 * seg_workspace_bytes(p.nsub, p.nseg, B, H, 128);
 }
 
-la_status la_prefill_backward(const void *q, const void *k, const void *v, la_dtype dtype, const float *alpha,
-                              const float *S0, const float *z0, int B, int H, int T, int r, int dv, float eps,
-                              const void *y, const void *dy, const float *dS_T, const float *dz_T, void *dq,
-                              void *dk, void *dv_out, float *dalpha, float *dS0, float *dz0, void *workspace,
-                              size_t workspace_bytes, la_stream_t stream)
+// la_prefill_backward and la_prefill_backward_saved; d (the forward's d_t) may be nullptr.
+static la_status prefill_backward_impl(const void *q, const void *k, const void *v, la_dtype dtype,
+                                       const float *alpha, const float *S0, const float *z0, int B, int H, int T,
+                                       int r, int dv, float eps, const void *y, const void *dy, const float *d,
+                                       const float *dS_T, const float *dz_T, void *dq, void *dk, void *dv_out,
+                                       float *dalpha, float *dS0, float *dz0, void *workspace,
+                                       size_t workspace_bytes, la_stream_t stream)
 {
     if (!q || !k || !v || !y || !dy || !dq || !dk || !dv_out || !dS0 || !dz0) return LA_ERR_NULL;
     if (B < 1 || H < 1 || T < 1 || r < 1 || dv < 1) return LA_ERR_SHAPE;
@@ -470,7 +493,7 @@ la_status la_prefill_backward(const void *q, const void *k, const void *v, la_dt
     for (const void *p : {q, k, v, y, dy, (const void *)dq, (const void *)dk, (const void *)dv_out})
         if (!aligned(p, 16)) return LA_ERR_ALIGN;
     for (const void *p : {(const void *)alpha, (const void *)S0, (const void *)z0, (const void *)dz_T,
-                          (const void *)dalpha, (const void *)dS0, (const void *)dz0})
+                          (const void *)dalpha, (const void *)dS0, (const void *)dz0, (const void *)d})
         if (p && !aligned(p, 4)) return LA_ERR_ALIGN;
     if (dS_T && !aligned(dS_T, 8)) return LA_ERR_ALIGN;
     if (!workspace || workspace_bytes < la_backward_workspace_bytes(B, H, T)) return LA_ERR_WORKSPACE;
@@ -480,6 +503,7 @@ la_status la_prefill_backward(const void *q, const void *k, const void *v, la_dt
     a.alpha = alpha; a.S0 = S0; a.z0 = z0; a.dS_T = dS_T; a.dz_T = dz_T;
     a.dq = dq; a.dk = dk; a.dv_out = dv_out; a.dalpha = dalpha; a.dS0 = dS0; a.dz0 = dz0;
     a.ws = static_cast<float *>(workspace);
+    a.d_in = d;
     a.H = H; a.T = T; a.r = r; a.dv = dv; a.eps = eps;
     a.status = status_word();
     a.limit_ns = la::kWaitLimitNs;
@@ -508,6 +532,27 @@ la_status la_prefill_backward(const void *q, const void *k, const void *v, la_dt
         }
     }
     return from_cuda(la::launch_backward(a, B, dtype == LA_DTYPE_BF16, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+la_status la_prefill_backward(const void *q, const void *k, const void *v, la_dtype dtype, const float *alpha,
+                              const float *S0, const float *z0, int B, int H, int T, int r, int dv, float eps,
+                              const void *y, const void *dy, const float *dS_T, const float *dz_T, void *dq,
+                              void *dk, void *dv_out, float *dalpha, float *dS0, float *dz0, void *workspace,
+                              size_t workspace_bytes, la_stream_t stream)
+{
+    return prefill_backward_impl(q, k, v, dtype, alpha, S0, z0, B, H, T, r, dv, eps, y, dy, nullptr, dS_T, dz_T, dq,
+                                 dk, dv_out, dalpha, dS0, dz0, workspace, workspace_bytes, stream);
+}
+
+la_status la_prefill_backward_saved(const void *q, const void *k, const void *v, la_dtype dtype, const float *alpha,
+                                    const float *S0, const float *z0, int B, int H, int T, int r, int dv,
+                                    const void *y, const void *dy, const float *d, const float *dS_T,
+                                    const float *dz_T, void *dq, void *dk, void *dv_out, float *dalpha, float *dS0,
+                                    float *dz0, void *workspace, size_t workspace_bytes, la_stream_t stream)
+{
+    if (!d) return LA_ERR_NULL;
+    return prefill_backward_impl(q, k, v, dtype, alpha, S0, z0, B, H, T, r, dv, 0.f, y, dy, d, dS_T, dz_T, dq, dk,
+                                 dv_out, dalpha, dS0, dz0, workspace, workspace_bytes, stream);
 }
 
 la_status la_delta_rule(const void *q, const void *k, const void *v, la_dtype dtype, const float *beta,

@@ -247,12 +247,13 @@ bwd_zdot_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k, const floa
     }
 }
 
-// d_t = d_acc[t] + eps and dd_t = -(dy_t . y_t) / d_t: two tokens per warp step,
-// 16 lanes per token, 16-byte loads.
+// d_t = d_src[t] + eps and dd_t = -(dy_t . y_t) / d_t: two tokens per warp step,
+// 16 lanes per token, 16-byte loads.  d_src is d itself (the z pass's feature
+// sums) or the forward's d_t (then eps = 0).
 template <typename Tin>
 __global__ void __launch_bounds__(256)
 bwd_dd_kernel(const Tin *__restrict__ y, const Tin *__restrict__ dy, int dv, long long n, float eps,
-              float *__restrict__ d, float *__restrict__ dd)
+              const float *d_src, float *d, float *__restrict__ dd)
 {
     constexpr int kV = 16 / (int)sizeof(Tin);
     const int nch = dv / kV;
@@ -279,7 +280,7 @@ bwd_dd_kernel(const Tin *__restrict__ y, const Tin *__restrict__ dy, int dv, lon
 #pragma unroll
         for (int o = 1; o < 16; o <<= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
         if (tok < n && hl == 0) {
-            const float den = d[tok] + eps;
+            const float den = d_src[tok] + eps;
             d[tok] = den;
             dd[tok] = -s / den;
         }
@@ -725,7 +726,7 @@ cudaError_t launch_bwd_t(const BackwardArgs &a, int B, cudaStream_t stream)
     // d accumulates the feature sums; tok_sum and fin accumulate dalpha terms
     cudaError_t e = cudaMemsetAsync(a.ws, 0, sizeof(float) * (3 * n + BH), stream);
     if (e != cudaSuccess) return e;
-    {
+    if (!a.d_in) {
         // z_t per segment of kZLen tokens: maps, scan, products
         const int nzs = (a.T + kZLen - 1) / kZLen;
         // zs and z_start are read as float4: they start on a 16-byte boundary (r is a multiple of 4)
@@ -740,8 +741,10 @@ cudaError_t launch_bwd_t(const BackwardArgs &a, int B, cudaStream_t stream)
                                                                 a.alpha, a.T, a.r, nzs, zst, d);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
+    // d_t = the feature sums + eps, or the forward's d_t as it stands
     bwd_dd_kernel<Tin><<<152 * 8, 256, 0, stream>>>(static_cast<const Tin *>(a.y), static_cast<const Tin *>(a.dy),
-                                                      a.dv, (long long)n, a.eps, d, dd);
+                                                      a.dv, (long long)n, a.d_in ? 0.f : a.eps,
+                                                      a.d_in ? a.d_in : d, d, dd);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     if constexpr (sizeof(Tin) == 2) {
         if (a.maps) {

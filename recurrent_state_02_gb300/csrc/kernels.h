@@ -54,6 +54,7 @@ struct PrefillTcArgs {
     float *S_out;         // [B,H,128,dv]
     float *z_out;         // [B,H,128]
     uint16_t *y;          // [B,H,T,dv] BF16 bits
+    float *d_out = nullptr;   // alpha's layout, or nullptr: d_t = phi(q_t) . z_t + eps of every token
     int H, T, dv;
     int nseg;             // sequence segments per head (1: the whole sequence in one CTA)
     int seg_chunks;       // chunks per segment (nseg > 1)
@@ -112,7 +113,8 @@ cudaError_t launch_seg_scan(const float *S0, const float *z0, const float *A, co
 // Exact FP32 token recurrence (CUDA cores), r, dv <= 256.
 cudaError_t launch_prefill_f32(const float *q, const float *k, const float *v, const float *alpha,
                                const float *S0, const float *z0, int B, int H, int T, int r, int dv,
-                               float eps, float *y, float *S_out, float *z_out, cudaStream_t stream);
+                               float eps, float *y, float *S_out, float *z_out, cudaStream_t stream,
+                               float *d_out = nullptr);
 
 // Decode step; bf16 selects the q/k/v/y element type (else FP32).
 cudaError_t launch_decode(const void *q, const void *k, const void *v, bool bf16, const float *alpha,
@@ -134,6 +136,7 @@ struct BackwardArgs {
     float *dalpha;                              // [B,H,T] (with alpha)
     float *dS0, *dz0;                           // [B,H,r,dv], [B,H,r]
     float *ws;                                  // backward_workspace_floats(B, H, T) floats
+    const float *d_in = nullptr;                // [B,H,T] d_t from the forward, or nullptr (the z pass forms it)
     int H, T, r, dv;
     float eps;
     int *status;                                // device status word

@@ -26,7 +26,8 @@ __device__ __forceinline__ float phi_exact(float x) { return x > 0.f ? x + 1.f :
 __global__ void __launch_bounds__(kMaxR)
 prefill_f32_kernel(const float *__restrict__ q, const float *__restrict__ k, const float *__restrict__ v,
                    const float *__restrict__ alpha, const float *__restrict__ S0, const float *__restrict__ z0,
-                   int H, int T, int r, int dv, float eps, float *__restrict__ y, float *S_out, float *z_out)
+                   int H, int T, int r, int dv, float eps, float *__restrict__ y, float *S_out, float *z_out,
+                   float *__restrict__ d_out)
 {
     extern __shared__ float S[];   // [r][ds]
     __shared__ float qf[kMaxR], kf[kMaxR], red[kMaxR / 32];
@@ -76,6 +77,7 @@ prefill_f32_kernel(const float *__restrict__ q, const float *__restrict__ k, con
                 n = fmaf(qf[i], s, n);
             }
             yh[(size_t)t * dv + tid] = n / (den + eps);
+            if (d_out && tid == 0 && blockIdx.z == 0) d_out[(size_t)bh * T + t] = den + eps;
         }
         __syncthreads();
     }
@@ -90,7 +92,7 @@ prefill_f32_kernel(const float *__restrict__ q, const float *__restrict__ k, con
 
 cudaError_t launch_prefill_f32(const float *q, const float *k, const float *v, const float *alpha, const float *S0,
                                const float *z0, int B, int H, int T, int r, int dv, float eps, float *y,
-                               float *S_out, float *z_out, cudaStream_t stream)
+                               float *S_out, float *z_out, cudaStream_t stream, float *d_out)
 {
     const int ds = dv < kSlice ? dv : kSlice;
     const size_t smem = sizeof(float) * (size_t)r * ds;
@@ -111,7 +113,8 @@ cudaError_t launch_prefill_f32(const float *q, const float *k, const float *v, c
     attr[0].val.clusterDim.z = nslice;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, prefill_f32_kernel, q, k, v, alpha, S0, z0, H, T, r, dv, eps, y, S_out, z_out);
+    return cudaLaunchKernelEx(&cfg, prefill_f32_kernel, q, k, v, alpha, S0, z0, H, T, r, dv, eps, y, S_out, z_out,
+                              d_out);
 }
 
 }  // namespace la

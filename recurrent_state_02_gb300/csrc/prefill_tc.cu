@@ -626,14 +626,21 @@ prefill_body(const CUtensorMap &map_q, const CUtensorMap &map_k, const CUtensorM
                 warp_arrive(&sm->O_empty[ob]);
                 dn += __shfl_xor_sync(0xffffffffu, dn, 16);
                 // a fast chunk's row i holds O' = w_i O and dn' = w_i dn: y = O' / (dn' + eps w_i)
-                float epsw = args.eps;
-                if (GATED && L::kHead && (FAST || gr->gf[ce % kAux] != 0)) epsw *= gr->gw[ce % kAux][prow];
+                float epsw = args.eps, wrow = 1.f;
+                if (GATED && L::kHead && (FAST || gr->gf[ce % kAux] != 0)) {
+                    wrow = gr->gw[ce % kAux][prow];
+                    epsw *= wrow;
+                }
                 if (GATED) warp_arrive(&sm->aux_empty[ce % kAux]);   // gate data of chunk ce is done
                 float inv;   // approximate reciprocal: y is rounded to BF16 below
                 asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(inv) : "f"(dn + epsw));
                 // SC/2 columns (16 or 32 bytes) of token row prow, straight to global
                 // memory (streaming stores: y is not read again here)
                 const int t = tb + ce * kC + prow;
+                // d_t on request (one lane per row): the denominator of y, divided
+                // by the row weight where the chunk carries one
+                if (args.d_out && slice == 0 && qq == 0 && lane < 16 && t < T)
+                    args.d_out[tok_row(t)] = (GATED && L::kHead) ? (dn + epsw) / wrow : dn + epsw;
                 if (t < T) {
                     uint4 *dst = reinterpret_cast<uint4 *>(args.y + tok_row(t) * args.dv + slice * DVS + ocol);
 #pragma unroll
