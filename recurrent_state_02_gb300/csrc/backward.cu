@@ -674,27 +674,54 @@ rec_kernel(RecArgs p)
 
 // ------------------------------------------------------------------ dalpha
 
-// One CTA of 128 threads per (b, h): dlog alpha_u = sum_{t >= u} tok_sum[t] + fin,
-// then dalpha_u = dlog alpha_u / alpha_u.  Thread i owns a contiguous chunk of
-// tokens: it sums its chunk, takes the sum of the later chunks (plus fin) from
-// shared memory, and walks its chunk backwards.
-__global__ void __launch_bounds__(128)
+// dalpha_u = (fin + sum_{t >= u} tok_sum[t]) / alpha_u for every token of one
+// (b, h), one CTA per (b, h), in tiles of kDaTile tokens from the end of the
+// sequence: a tile is staged in shared memory (coalesced loads, padded so that
+// the runs below hit distinct banks), each thread sums a run of kDaRun
+// consecutive tokens, a suffix scan over the runs (warp shuffles, then across
+// warps) gives every run the sum of what follows it, the run is walked
+// backwards, and the tile leaves by coalesced stores.
+constexpr int kDaThreads = 256, kDaTile = 4096, kDaRun = kDaTile / kDaThreads;
+__device__ __forceinline__ int da_pad(int x) { return x + (x >> 5); }
+
+__global__ void __launch_bounds__(kDaThreads)
 bwd_dalpha_kernel(const float *__restrict__ tok_sum, const float *__restrict__ fin, const float *__restrict__ alpha,
                   int T, float *__restrict__ dalpha)
 {
-    __shared__ float part[128];
-    const int bh = blockIdx.x, i = threadIdx.x;
-    const int per = (T + 127) / 128, lo = min(T, i * per), hi = min(T, lo + per);
-    const float *ts = tok_sum + (size_t)bh * T;
-    float s = 0.f;
-    for (int t = lo; t < hi; ++t) s += ts[t];
-    part[i] = s;
-    __syncthreads();
-    float carry = fin[bh];
-    for (int j = i + 1; j < 128; ++j) carry += part[j];
-    for (int t = hi - 1; t >= lo; --t) {
-        carry += ts[t];
-        dalpha[(size_t)bh * T + t] = carry / alpha[(size_t)bh * T + t];
+    __shared__ float buf[kDaTile + kDaTile / 32];
+    __shared__ float wsum[kDaThreads / 32];
+    const int bh = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const float *ts = tok_sum + (size_t)bh * T, *al = alpha + (size_t)bh * T;
+    float *out = dalpha + (size_t)bh * T;
+    float carry = fin[bh];   // the final-state term plus every later tile
+    for (int tile = (T + kDaTile - 1) / kDaTile - 1; tile >= 0; --tile) {
+        const int t0 = tile * kDaTile, n = min(kDaTile, T - t0);
+        for (int x = tid; x < kDaTile; x += kDaThreads) buf[da_pad(x)] = x < n ? ts[t0 + x] : 0.f;
+        __syncthreads();
+        float run = 0.f;
+#pragma unroll
+        for (int j = 0; j < kDaRun; ++j) run += buf[da_pad(tid * kDaRun + j)];
+        float suf = run;   // runs tid .. the warp's last
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const float v = __shfl_down_sync(0xffffffffu, suf, o);
+            if (lane + o < 32) suf += v;
+        }
+        if (lane == 0) wsum[warp] = suf;
+        __syncthreads();
+        float c = carry + (suf - run);
+        for (int w = warp + 1; w < kDaThreads / 32; ++w) c += wsum[w];
+#pragma unroll
+        for (int j = kDaRun - 1; j >= 0; --j) {
+            const int x = da_pad(tid * kDaRun + j);
+            c += buf[x];
+            buf[x] = c;
+        }
+        __syncthreads();
+        for (int x = tid; x < n; x += kDaThreads) out[t0 + x] = buf[da_pad(x)] / al[t0 + x];
+#pragma unroll
+        for (int w = 0; w < kDaThreads / 32; ++w) carry += wsum[w];
+        __syncthreads();   // before the next tile reuses buf and wsum
     }
 }
 
@@ -791,7 +818,7 @@ cudaError_t launch_bwd_t(const BackwardArgs &a, int B, cudaStream_t stream)
             }
             if ((e = launch_bwd_tc(a.maps, t, B, a.alpha != nullptr, stream)) != cudaSuccess) return e;
             if (a.alpha && a.dalpha) {
-                bwd_dalpha_kernel<<<BH, 128, 0, stream>>>(tok_sum, fin, a.alpha, a.T, a.dalpha);
+                bwd_dalpha_kernel<<<BH, kDaThreads, 0, stream>>>(tok_sum, fin, a.alpha, a.T, a.dalpha);
                 if ((e = cudaGetLastError()) != cudaSuccess) return e;
             }
             return cudaSuccess;
@@ -810,7 +837,7 @@ cudaError_t launch_bwd_t(const BackwardArgs &a, int B, cudaStream_t stream)
     p.out = a.dv_out;
     if ((e = launch_rec<Tin, kRevDv>(p, B, a.r, stream)) != cudaSuccess) return e;
     if (a.alpha && a.dalpha) {
-        bwd_dalpha_kernel<<<BH, 128, 0, stream>>>(tok_sum, fin, a.alpha, a.T, a.dalpha);
+        bwd_dalpha_kernel<<<BH, kDaThreads, 0, stream>>>(tok_sum, fin, a.alpha, a.T, a.dalpha);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
     return cudaSuccess;
