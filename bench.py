@@ -645,20 +645,25 @@ def run_ours(args, rank, world, local_rank):
                                                 P(ybw), P(dybw), None, None, P(gq), P(gk), P(gv), P(ga), P(gS0), P(gz0),
                                                 P(wsb), wsb.numel(), sh), "la_prefill_backward")
 
-        # the same backward with the forward's saved denominators (no z pass)
+        # the same backward with what a training forward keeps: the denominators (no
+        # z pass) and the states entering the backward's segments (no forward state pass)
         dbw = torch.empty((bw.B, bw.H, bw.T), device=dev, dtype=torch.float32)
+        nstb = int(L.la_backward_states_bytes(bw.B, bw.H, bw.T))
+        stbw = torch.empty(max(1, nstb // 4), device=dev, dtype=torch.float32)
+        pst = P(stbw) if nstb else None
 
         def k_backward_saved():
             _native.check(L.la_prefill_backward_saved(P(bin_["q"]), P(bin_["k"]), P(bin_["v"]), _native.LA_DTYPE_BF16,
                                                       P(bin_["alpha"]), None, None, bw.B, bw.H, bw.T, bw.r, bw.dv,
-                                                      P(ybw), P(dybw), P(dbw), None, None, P(gq), P(gk), P(gv), P(ga),
-                                                      P(gS0), P(gz0), P(wsb), wsb.numel(), sh),
+                                                      P(ybw), P(dybw), P(dbw), pst, None, None, P(gq), P(gk), P(gv),
+                                                      P(ga), P(gS0), P(gz0), P(wsb), wsb.numel(), sh),
                           "la_prefill_backward_saved")
 
         with torch.cuda.stream(stream):
             _native.check(L.la_prefill_chunked_save(P(bin_["q"]), P(bin_["k"]), P(bin_["v"]), _native.LA_DTYPE_BF16,
                                                     P(bin_["alpha"]), None, None, bw.B, bw.H, bw.T, bw.r, bw.dv,
-                                                    bw.chunk, bw.eps, P(ybw), P(Sbw), P(zbw), P(dbw), None, 0, sh),
+                                                    bw.chunk, bw.eps, P(ybw), P(Sbw), P(zbw), P(dbw), pst, None, 0,
+                                                    sh),
                           "la_prefill_chunked_save")
             k_backward()
             k_backward_saved()
@@ -675,7 +680,7 @@ def run_ours(args, rank, world, local_rank):
         assert _native.lib().la_last_device_status(sh) == 0
         b_call, bs_call = b_s / bsteps, bs_s / bsteps
         b_bytes = backward_bytes(bw.B, bw.H, bw.T, bw.r, bw.dv, True)
-        bs_bytes = b_bytes + 4 * bw.B * bw.H * bw.T   # and the saved d_t (FP32) read
+        bs_bytes = b_bytes + 4 * bw.B * bw.H * bw.T + nstb   # and the saved d_t and states read
         b_gbs = b_bytes / b_call / 1e9
         backward = {"workload": bw.name.replace("prefill", "backward of the gated prefill,"), "call_us": b_call * 1e6,
                     "launches_per_call": 12, "tokens_per_s": bw.B * bw.T * world / b_call, "steps": bsteps,
@@ -684,8 +689,9 @@ def run_ours(args, rank, world, local_rank):
                                  "algorithmic_bytes_per_call": b_bytes,
                                  "tensor_tflops": backward_flops(bw.B, bw.H, bw.T, bw.r, bw.dv, True) / b_call / 1e12,
                                  "algorithmic_flops_per_call": backward_flops(bw.B, bw.H, bw.T, bw.r, bw.dv, True)},
-                    "saved_d": {"entry": "la_prefill_backward_saved (d from la_prefill_chunked_save)",
-                                "call_us": bs_call * 1e6, "launches_per_call": 9,
+                    "saved_d": {"entry": "la_prefill_backward_saved (d_t and the segment states from "
+                                         "la_prefill_chunked_save)",
+                                "call_us": bs_call * 1e6, "launches_per_call": 9 - (2 if nstb else 0),
                                 "tokens_per_s": bw.B * bw.T * world / bs_call,
                                 "roofline": {"bound": "hbm", "achieved": bs_bytes / bs_call / 1e9, "peak": peak,
                                              "unit": "GB/s", "frac": bs_bytes / bs_call / 1e9 / peak,

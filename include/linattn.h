@@ -249,35 +249,53 @@ la_status la_prefill_backward(const void *q, const void *k, const void *v, la_dt
                               size_t workspace_bytes, la_stream_t stream);
 
 /*
+ * la_backward_states_bytes -- bytes of the states buffer that la_prefill_chunked_save
+ * can fill for la_prefill_backward_saved: the backward splits a sequence into
+ * segments when few long sequences would leave SMs idle, and this is the state
+ * [S | z] (FP32, 128 x 128 then 128) entering each segment of every (b, h).
+ * 0 when the backward would not split (then there is nothing to keep).
+ */
+size_t la_backward_states_bytes(int B, int H, int T);
+
+/*
  * la_prefill_chunked_save -- la_prefill_chunked that also keeps, for training, the
  * denominator of every output row: d_t = phi(q_t) . z_t + eps, the normaliser of
- * [LA] "公式里的每个维度" (y_t = phi(q_t)^T S_t / d_t), in FP32.
- * la_prefill_backward_saved takes it instead of recomputing it.
- *   d_out  device FP32 [B,H,T], 4-byte aligned, owned by the caller.
+ * [LA] "公式里的每个维度" (y_t = phi(q_t)^T S_t / d_t), in FP32, and optionally the
+ * states at which the backward's sequence segments start.
+ * la_prefill_backward_saved takes them instead of recomputing them.
+ *   d_out      device FP32 [B,H,T], 4-byte aligned, owned by the caller.
+ *   states_out device buffer of la_backward_states_bytes(B, H, T) bytes, 16-byte
+ *              aligned, or NULL (not kept).  Written for BF16 with r = dv = 128
+ *              when that size is not 0; otherwise left untouched.
  *   Everything else as for la_prefill_chunked.
  * BF16: the chunk kernel's own denominator (the BF16 operands of its products,
- * FP32 accumulation), the one y was divided by; FP32: the exact recurrence's.
+ * FP32 accumulation), the one y was divided by, and its FP32 state; FP32: the
+ * exact recurrence's denominator.
  * Errors: those of la_prefill_chunked; LA_ERR_NULL when d_out is NULL.
  */
 la_status la_prefill_chunked_save(const void *q, const void *k, const void *v, la_dtype dtype, const float *alpha,
                                   const float *S0, const float *z0, int B, int H, int T, int r, int dv, int chunk,
-                                  float eps, void *y, float *S_out, float *z_out, float *d_out, void *workspace,
-                                  size_t workspace_bytes, la_stream_t stream);
+                                  float eps, void *y, float *S_out, float *z_out, float *d_out, float *states_out,
+                                  void *workspace, size_t workspace_bytes, la_stream_t stream);
 
 /*
  * la_prefill_backward_saved -- la_prefill_backward with d_t taken from
  * la_prefill_chunked_save instead of recomputed: the z_t recurrence over the
- * sequence (three of the backward's launches) is skipped.
+ * sequence (three of the backward's launches) is skipped, and with states, the
+ * forward state pass and scan of a segmented backward too.
  *   d      device FP32 [B,H,T] from la_prefill_chunked_save on the same inputs
  *          (eps is included in it, so there is no eps argument).
+ *   states the states_out of that call, or NULL (recomputed when needed).
  *   Everything else as for la_prefill_backward.
- * Errors: those of la_prefill_backward; LA_ERR_NULL when d is NULL.
+ * Errors: those of la_prefill_backward; LA_ERR_NULL when d is NULL; LA_ERR_ALIGN
+ *         when states is not 16-byte aligned.
  */
 la_status la_prefill_backward_saved(const void *q, const void *k, const void *v, la_dtype dtype, const float *alpha,
                                     const float *S0, const float *z0, int B, int H, int T, int r, int dv,
-                                    const void *y, const void *dy, const float *d, const float *dS_T,
-                                    const float *dz_T, void *dq, void *dk, void *dv_out, float *dalpha, float *dS0,
-                                    float *dz0, void *workspace, size_t workspace_bytes, la_stream_t stream);
+                                    const void *y, const void *dy, const float *d, const float *states,
+                                    const float *dS_T, const float *dz_T, void *dq, void *dk, void *dv_out,
+                                    float *dalpha, float *dS0, float *dz0, void *workspace, size_t workspace_bytes,
+                                    la_stream_t stream);
 
 /*
  * la_delta_rule -- the delta-rule memory ([LA] "Delta rule：先读旧答案，再写误差"): a

@@ -80,19 +80,35 @@ def prefill_chunked(q, k, v, alpha=None, S0=None, z0=None, chunk=64, eps=1e-6, y
     return _prefill(q, k, v, alpha, S0, z0, chunk, eps, y, S_out, z_out, workspace, None)
 
 
+def backward_states_bytes(B, H, T, device=None) -> int:
+    """Bytes of the states a training forward can keep for the backward's sequence
+    segments on `device` (0: the backward would not split the sequence)."""
+    if device is None:
+        return int(_native.lib().la_backward_states_bytes(B, H, T))
+    with _device_guard(torch.device(device)):
+        return int(_native.lib().la_backward_states_bytes(B, H, T))
+
+
 def prefill_chunked_save(q, k, v, alpha=None, S0=None, z0=None, chunk=64, eps=1e-6, y=None, S_out=None, z_out=None,
-                         d_out=None, workspace=None):
-    """prefill_chunked that also returns d [B,H,T] fp32, the denominator of every
-    output row (phi(q_t) . z_t + eps), for prefill_backward(..., d=d).
-    Returns (y, S_T, z_T, d)."""
+                         d_out=None, workspace=None, keep_states=True):
+    """prefill_chunked that also returns what the backward can reuse: d [B,H,T]
+    fp32, the denominator of every output row (phi(q_t) . z_t + eps), and the
+    states entering the backward's sequence segments (a flat fp32 tensor, or None
+    when there are none or keep_states is False), for
+    prefill_backward(..., d=d, states=states).  Returns (y, S_T, z_T, d, states)."""
     B, H, T, _ = q.shape
     if d_out is None:
         d_out = torch.empty((B, H, T), device=q.device, dtype=torch.float32)
     _require(d_out, "d_out", (B, H, T), torch.float32, q.device)
-    return _prefill(q, k, v, alpha, S0, z0, chunk, eps, y, S_out, z_out, workspace, d_out) + (d_out,)
+    states = None
+    if keep_states and q.dtype == torch.bfloat16:
+        nbytes = backward_states_bytes(B, H, T, device=q.device)
+        if nbytes:
+            states = torch.empty(nbytes // 4, device=q.device, dtype=torch.float32)
+    return _prefill(q, k, v, alpha, S0, z0, chunk, eps, y, S_out, z_out, workspace, d_out, states) + (d_out, states)
 
 
-def _prefill(q, k, v, alpha, S0, z0, chunk, eps, y, S_out, z_out, workspace, d_out):
+def _prefill(q, k, v, alpha, S0, z0, chunk, eps, y, S_out, z_out, workspace, d_out, states=None):
     if q.dtype not in _DTYPES:
         raise ValueError(f"unsupported dtype {q.dtype}")
     B, H, T, r = q.shape
@@ -126,7 +142,8 @@ def _prefill(q, k, v, alpha, S0, z0, chunk, eps, y, S_out, z_out, workspace, d_o
         else:
             st = _native.lib().la_prefill_chunked_save(
                 _ptr(q), _ptr(k), _ptr(v), _DTYPES[q.dtype], _ptr(alpha), _ptr(S0), _ptr(z0), B, H, T, r, dv, chunk,
-                float(eps), _ptr(y), _ptr(S_out), _ptr(z_out), _ptr(d_out), _ptr(workspace), ws_bytes, _stream(dev))
+                float(eps), _ptr(y), _ptr(S_out), _ptr(z_out), _ptr(d_out), _ptr(states), _ptr(workspace), ws_bytes,
+                _stream(dev))
             _native.check(st, "la_prefill_chunked_save")
     return y, S_out, z_out
 
@@ -224,12 +241,15 @@ def decode_step(q, k, v, S, z, alpha=None, eps=1e-6, y=None):
 
 
 def prefill_backward(q, k, v, y, dy, alpha=None, S0=None, z0=None, dS_T=None, dz_T=None, eps=1e-6, workspace=None,
-                     d=None):
+                     d=None, states=None):
     """Gradients of prefill_chunked: given the forward inputs, its output y and
     dy [B,H,T,dv] (and optionally dS_T [B,H,r,dv], dz_T [B,H,r] in fp32), returns
     (dq, dk, dv, dalpha or None, dS0, dz0); dq, dk, dv in the input dtype.
     d: the [B,H,T] fp32 denominators from prefill_chunked_save (eps is then not
-    used), or None to recompute them."""
+    used), or None to recompute them; states: the segment states from the same
+    call (with d only), or None."""
+    if states is not None and d is None:
+        raise ValueError("states are taken only together with d")
     if q.dtype not in _DTYPES:
         raise ValueError(f"unsupported dtype {q.dtype}")
     B, H, T, r = q.shape
@@ -262,8 +282,8 @@ def prefill_backward(q, k, v, y, dy, alpha=None, S0=None, z0=None, dS_T=None, dz
         else:
             st = _native.lib().la_prefill_backward_saved(
                 _ptr(q), _ptr(k), _ptr(v), _DTYPES[q.dtype], _ptr(alpha), _ptr(S0), _ptr(z0), B, H, T, r, dvd,
-                _ptr(y), _ptr(dy), _ptr(d), _ptr(dS_T), _ptr(dz_T), _ptr(dq), _ptr(dk), _ptr(dv_out), _ptr(dalpha),
-                _ptr(dS0), _ptr(dz0), _ptr(workspace), ws_bytes, _stream(dev))
+                _ptr(y), _ptr(dy), _ptr(d), _ptr(states), _ptr(dS_T), _ptr(dz_T), _ptr(dq), _ptr(dk), _ptr(dv_out),
+                _ptr(dalpha), _ptr(dS0), _ptr(dz0), _ptr(workspace), ws_bytes, _stream(dev))
             _native.check(st, "la_prefill_backward_saved")
     return dq, dk, dv_out, dalpha, dS0, dz0
 

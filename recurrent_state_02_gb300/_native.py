@@ -32,10 +32,11 @@ SIGNATURES = {
     "la_backward_workspace_bytes": (_sz, [_i, _i, _i]),
     "la_prefill_backward": (_i, [_vp, _vp, _vp, _i, _fp, _fp, _fp, _i, _i, _i, _i, _i, _f, _vp, _vp, _fp, _fp,
                                  _vp, _vp, _vp, _fp, _fp, _fp, _vp, _sz, _vp]),
+    "la_backward_states_bytes": (_sz, [_i, _i, _i]),
     "la_prefill_chunked_save": (_i, [_vp, _vp, _vp, _i, _fp, _fp, _fp, _i, _i, _i, _i, _i, _i, _f, _vp, _fp, _fp,
-                                     _fp, _vp, _sz, _vp]),
+                                     _fp, _fp, _vp, _sz, _vp]),
     "la_prefill_backward_saved": (_i, [_vp, _vp, _vp, _i, _fp, _fp, _fp, _i, _i, _i, _i, _i, _vp, _vp, _fp, _fp,
-                                       _fp, _vp, _vp, _vp, _fp, _fp, _fp, _vp, _sz, _vp]),
+                                       _fp, _fp, _vp, _vp, _vp, _fp, _fp, _fp, _vp, _sz, _vp]),
     "la_last_device_status": (_i, [_vp]),
     "la_status_string": (ctypes.c_char_p, [_i]),
     "la_debug_wait_probe": (_i, [_u64, _vp]),

@@ -268,13 +268,15 @@ size_t la_prefill_workspace_bytes(int B, int H, int T, int r, int dv, int chunk)
 static la_status prefill_chunked_impl(const void *q, const void *k, const void *v, la_dtype dtype,
                                       const float *alpha, const float *S0, const float *z0, int B, int H, int T,
                                       int r, int dv, int chunk, float eps, void *y, float *S_out, float *z_out,
-                                      float *d_out, void *workspace, size_t workspace_bytes, la_stream_t stream)
+                                      float *d_out, float *states_out, void *workspace, size_t workspace_bytes,
+                                      la_stream_t stream)
 {
     if (!q || !k || !v || !y || !S_out || !z_out) return LA_ERR_NULL;
     if (B < 1 || H < 1 || T < 1 || r < 1 || dv < 1 || chunk < 1) return LA_ERR_SHAPE;
     if (dtype != LA_DTYPE_BF16 && dtype != LA_DTYPE_FP32) return LA_ERR_DTYPE;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
 
+    if (states_out && !aligned(states_out, 16)) return LA_ERR_ALIGN;
     if (dtype == LA_DTYPE_FP32) {
         if (r > 256 || dv > 256) return LA_ERR_UNSUPPORTED;
         const void *ptrs[] = {q, k, v, y, S_out, z_out, alpha, S0, z0, d_out};
@@ -321,6 +323,15 @@ static la_status prefill_chunked_impl(const void *q, const void *k, const void *
     a.z_out = z_out;
     a.y = static_cast<uint16_t *>(y);
     a.d_out = d_out;
+    if (states_out && r == 128 && dv == 128) {
+        const SegPlan bp = bwd_seg_plan(B, H, T);
+        if (bp.nseg > 1) {
+            a.bwd_states = states_out;
+            a.bwd_seg_chunks = bp.seg_chunks;
+            a.bwd_nseg = bp.nseg;
+            a.bwd_heads = B * H;
+        }
+    }
     a.H = H;
     a.T = T;
     a.dv = dv;
@@ -368,17 +379,24 @@ la_status la_prefill_chunked(const void *q, const void *k, const void *v, la_dty
                              size_t workspace_bytes, la_stream_t stream)
 {
     return prefill_chunked_impl(q, k, v, dtype, alpha, S0, z0, B, H, T, r, dv, chunk, eps, y, S_out, z_out, nullptr,
-                                workspace, workspace_bytes, stream);
+                                nullptr, workspace, workspace_bytes, stream);
 }
 
 la_status la_prefill_chunked_save(const void *q, const void *k, const void *v, la_dtype dtype, const float *alpha,
                                   const float *S0, const float *z0, int B, int H, int T, int r, int dv, int chunk,
-                                  float eps, void *y, float *S_out, float *z_out, float *d_out, void *workspace,
-                                  size_t workspace_bytes, la_stream_t stream)
+                                  float eps, void *y, float *S_out, float *z_out, float *d_out, float *states_out,
+                                  void *workspace, size_t workspace_bytes, la_stream_t stream)
 {
     if (!d_out) return LA_ERR_NULL;
     return prefill_chunked_impl(q, k, v, dtype, alpha, S0, z0, B, H, T, r, dv, chunk, eps, y, S_out, z_out, d_out,
-                                workspace, workspace_bytes, stream);
+                                states_out, workspace, workspace_bytes, stream);
+}
+
+size_t la_backward_states_bytes(int B, int H, int T)
+{
+    if (B < 1 || H < 1 || T < 1) return 0;
+    const SegPlan p = bwd_seg_plan(B, H, T);
+    return p.nseg > 1 ? sizeof(float) * (size_t)p.nseg * B * H * (128 * 128 + 128) : 0;
 }
 
 la_status la_prefill_varlen(const void *q, const void *k, const void *v, la_dtype dtype, const float *alpha,
@@ -480,7 +498,8 @@ size_t la_backward_workspace_bytes(int B, int H, int T)
 static la_status prefill_backward_impl(const void *q, const void *k, const void *v, la_dtype dtype,
                                        const float *alpha, const float *S0, const float *z0, int B, int H, int T,
                                        int r, int dv, float eps, const void *y, const void *dy, const float *d,
-                                       const float *dS_T, const float *dz_T, void *dq, void *dk, void *dv_out,
+                                       const float *states, const float *dS_T, const float *dz_T, void *dq, void *dk,
+                                       void *dv_out,
                                        float *dalpha, float *dS0, float *dz0, void *workspace,
                                        size_t workspace_bytes, la_stream_t stream)
 {
@@ -504,6 +523,7 @@ static la_status prefill_backward_impl(const void *q, const void *k, const void 
     a.dq = dq; a.dk = dk; a.dv_out = dv_out; a.dalpha = dalpha; a.dS0 = dS0; a.dz0 = dz0;
     a.ws = static_cast<float *>(workspace);
     a.d_in = d;
+    if (states && !aligned(states, 16)) return LA_ERR_ALIGN;
     a.H = H; a.T = T; a.r = r; a.dv = dv; a.eps = eps;
     a.status = status_word();
     a.limit_ns = la::kWaitLimitNs;
@@ -529,6 +549,7 @@ static la_status prefill_backward_impl(const void *q, const void *k, const void 
             a.sub_chunks = p.sub_chunks;
             a.nsub = p.nsub;
             a.seg_ws = reinterpret_cast<float *>(static_cast<char *>(workspace) + bwd_base_bytes(B, H, T));
+            a.states_in = states;
         }
     }
     return from_cuda(la::launch_backward(a, B, dtype == LA_DTYPE_BF16, reinterpret_cast<cudaStream_t>(stream)));
@@ -540,19 +561,20 @@ la_status la_prefill_backward(const void *q, const void *k, const void *v, la_dt
                               void *dk, void *dv_out, float *dalpha, float *dS0, float *dz0, void *workspace,
                               size_t workspace_bytes, la_stream_t stream)
 {
-    return prefill_backward_impl(q, k, v, dtype, alpha, S0, z0, B, H, T, r, dv, eps, y, dy, nullptr, dS_T, dz_T, dq,
-                                 dk, dv_out, dalpha, dS0, dz0, workspace, workspace_bytes, stream);
+    return prefill_backward_impl(q, k, v, dtype, alpha, S0, z0, B, H, T, r, dv, eps, y, dy, nullptr, nullptr, dS_T,
+                                 dz_T, dq, dk, dv_out, dalpha, dS0, dz0, workspace, workspace_bytes, stream);
 }
 
 la_status la_prefill_backward_saved(const void *q, const void *k, const void *v, la_dtype dtype, const float *alpha,
                                     const float *S0, const float *z0, int B, int H, int T, int r, int dv,
-                                    const void *y, const void *dy, const float *d, const float *dS_T,
-                                    const float *dz_T, void *dq, void *dk, void *dv_out, float *dalpha, float *dS0,
-                                    float *dz0, void *workspace, size_t workspace_bytes, la_stream_t stream)
+                                    const void *y, const void *dy, const float *d, const float *states,
+                                    const float *dS_T, const float *dz_T, void *dq, void *dk, void *dv_out,
+                                    float *dalpha, float *dS0, float *dz0, void *workspace, size_t workspace_bytes,
+                                    la_stream_t stream)
 {
     if (!d) return LA_ERR_NULL;
-    return prefill_backward_impl(q, k, v, dtype, alpha, S0, z0, B, H, T, r, dv, 0.f, y, dy, d, dS_T, dz_T, dq, dk,
-                                 dv_out, dalpha, dS0, dz0, workspace, workspace_bytes, stream);
+    return prefill_backward_impl(q, k, v, dtype, alpha, S0, z0, B, H, T, r, dv, 0.f, y, dy, d, states, dS_T, dz_T, dq,
+                                 dk, dv_out, dalpha, dS0, dz0, workspace, workspace_bytes, stream);
 }
 
 la_status la_delta_rule(const void *q, const void *k, const void *v, la_dtype dtype, const float *beta,

@@ -800,13 +800,17 @@ cudaError_t launch_bwd_t(const BackwardArgs &a, int B, cudaStream_t stream)
                 sa.nsub = a.nsub; sa.sub_per_seg = a.sub_per_seg; sa.sub_chunks = a.sub_chunks;
                 sa.seg_chunks = a.seg_chunks; sa.status = a.status; sa.wait_limit_ns = a.limit_ns;
                 const bool gated = a.alpha != nullptr;
-                // forward: segments 0 .. nseg-2 over (phi(k), v)
-                sa.A = pf; sa.dS = pf + a_floats; sa.seg_first = 0;
-                if ((e = launch_state_tc(a.maps[1], a.maps[2], sa, B, gated, 128, stream)) != cudaSuccess) return e;
-                float *Sf = pf + a_floats + (size_t)a.nsub * BH * state;
-                if ((e = launch_seg_scan(a.S0, a.z0, sa.A, sa.dS, Sf, BH, 128, a.nsub, a.sub_per_seg, a.nseg, stream)) !=
-                    cudaSuccess)
-                    return e;
+                // forward: segments 0 .. nseg-2 over (phi(k), v), unless the forward kept them
+                const float *Sf = a.states_in;
+                if (!Sf) {
+                    sa.A = pf; sa.dS = pf + a_floats; sa.seg_first = 0;
+                    if ((e = launch_state_tc(a.maps[1], a.maps[2], sa, B, gated, 128, stream)) != cudaSuccess) return e;
+                    float *sf = pf + a_floats + (size_t)a.nsub * BH * state;
+                    if ((e = launch_seg_scan(a.S0, a.z0, sa.A, sa.dS, sf, BH, 128, a.nsub, a.sub_per_seg, a.nseg,
+                                             stream)) != cudaSuccess)
+                        return e;
+                    Sf = sf;
+                }
                 // reversed: segments 1 .. nseg-1 over (phi(q), dy / d, dd)
                 sa.A = pr; sa.dS = pr + a_floats; sa.seg_first = 1; sa.d = d; sa.dd = dd;
                 if ((e = launch_state_tc(a.maps[0], a.maps[3], sa, B, gated, 128, stream, true)) != cudaSuccess) return e;

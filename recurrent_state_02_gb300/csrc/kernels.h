@@ -55,6 +55,10 @@ struct PrefillTcArgs {
     float *z_out;         // [B,H,128]
     uint16_t *y;          // [B,H,T,dv] BF16 bits
     float *d_out = nullptr;   // alpha's layout, or nullptr: d_t = phi(q_t) . z_t + eps of every token
+    // or nullptr: the state [S | z] entering every bwd_seg_chunks-th chunk, for the
+    // backward's segments ([bwd_nseg][bwd_heads][128 * dv + 128], dv == 128)
+    float *bwd_states = nullptr;
+    int bwd_seg_chunks = 0, bwd_nseg = 0, bwd_heads = 0;
     int H, T, dv;
     int nseg;             // sequence segments per head (1: the whole sequence in one CTA)
     int seg_chunks;       // chunks per segment (nseg > 1)
@@ -137,6 +141,7 @@ struct BackwardArgs {
     float *dS0, *dz0;                           // [B,H,r,dv], [B,H,r]
     float *ws;                                  // backward_workspace_floats(B, H, T) floats
     const float *d_in = nullptr;                // [B,H,T] d_t from the forward, or nullptr (the z pass forms it)
+    const float *states_in = nullptr;           // the forward's states at the segment starts, or nullptr
     int H, T, r, dv;
     float eps;
     int *status;                                // device status word

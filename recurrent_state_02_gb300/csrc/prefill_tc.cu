@@ -526,6 +526,17 @@ prefill_body(const CUtensorMap &map_q, const CUtensorMap &map_k, const CUtensorM
             }
             if (has_p) tc_ld_16x32bx2_x8<8>(tmem + lane_base + L::kColP + pb * 64 + qq * 16, p);
             tc_wait_ld();
+            // on request, the state entering chunk c where a segment of the backward starts
+            if (has_s && args.bwd_states && ((c0 + c) % args.bwd_seg_chunks) == 0 &&
+                (c0 + c) / args.bwd_seg_chunks < args.bwd_nseg) {
+                float *dst = args.bwd_states + ((size_t)((c0 + c) / args.bwd_seg_chunks) * args.bwd_heads + bh) *
+                                                   (kR * 128 + kR);
+#pragma unroll
+                for (int j = 0; j < SC; j += 4)
+                    *reinterpret_cast<float4 *>(dst + (size_t)srow * 128 + slice * DVS + qq * SC + j) =
+                        make_float4(S[j], S[j + 1], S[j + 2], S[j + 3]);
+                if (slice == 0 && qq == 0) dst[kR * 128 + srow] = zr;
+            }
             // Sprev of chunk c (BF16) and z split into two BF16 parts.  With a gate
             // the state is decayed by the chunk's gate product Gamma_last before its
             // increment lands; a fast chunk (whole head) reads the decayed state:

@@ -213,7 +213,7 @@ def test_saved_denominator_entries_reject_bad_arguments(native):
         a = dict(q=FAKE, dtype=native.LA_DTYPE_BF16, T=64, d_out=FAKE, y=FAKE)
         a.update(kw)
         return L.la_prefill_chunked_save(a["q"], FAKE, FAKE, a["dtype"], None, None, None, 1, 1, a["T"], 128, 128, 64,
-                                         1e-6, a["y"], FAKE, FAKE, a["d_out"], None, 0, None)
+                                         1e-6, a["y"], FAKE, FAKE, a["d_out"], a.get("states"), None, 0, None)
 
     assert fwd(d_out=None) == native.LA_ERR_NULL
     assert fwd(q=None) == native.LA_ERR_NULL
@@ -221,19 +221,24 @@ def test_saved_denominator_entries_reject_bad_arguments(native):
     assert fwd(dtype=7) == native.LA_ERR_DTYPE
     assert fwd(d_out=FAKE + 2) == native.LA_ERR_ALIGN
     assert fwd(dtype=native.LA_DTYPE_FP32, d_out=FAKE + 2) == native.LA_ERR_ALIGN
+    assert fwd(states=FAKE + 4) == native.LA_ERR_ALIGN
 
     def bwd(**kw):
         a = dict(q=FAKE, d=FAKE, T=64, ws=FAKE, ws_bytes=1 << 20)
         a.update(kw)
         return L.la_prefill_backward_saved(a["q"], FAKE, FAKE, native.LA_DTYPE_BF16, None, None, None, 1, 1, a["T"],
-                                           128, 128, FAKE, FAKE, a["d"], None, None, FAKE, FAKE, FAKE, None, FAKE,
-                                           FAKE, a["ws"], a["ws_bytes"], None)
+                                           128, 128, FAKE, FAKE, a["d"], a.get("states"), None, None, FAKE, FAKE,
+                                           FAKE, None, FAKE, FAKE, a["ws"], a["ws_bytes"], None)
 
     assert bwd(d=None) == native.LA_ERR_NULL
     assert bwd(q=None) == native.LA_ERR_NULL
     assert bwd(T=0) == native.LA_ERR_SHAPE
     assert bwd(d=FAKE + 2) == native.LA_ERR_ALIGN
     assert bwd(ws=None) == native.LA_ERR_WORKSPACE
+    assert bwd(states=FAKE + 4) == native.LA_ERR_ALIGN
+    # without a device there are no SMs to fill, so no segments and nothing to keep
+    assert L.la_backward_states_bytes(4, 16, 4096) == 0
+    assert L.la_backward_states_bytes(0, 16, 4096) == 0
 
 
 def test_backward_rejects_bad_arguments(native):

@@ -10,6 +10,10 @@ la_prefill_backward_saved takes it instead of recomputing it.
   written out below in FP64 on the inputs the kernels read.  BF16 bar 1e-2
   elementwise relative (d is a sum of positive terms; the chunk kernel forms it
   from BF16 operands, with phi in BF16), FP32 bar 1e-5.
+- Where the backward splits the sequence into segments, the states the forward
+  keeps for it are the oracle's states at chunk boundaries (its scan over the
+  prefix), in increasing order, the first one S0, z0; bar 2e-2 of each state's
+  largest entry.
 """
 import numpy as np
 import pytest
@@ -73,7 +77,7 @@ def test_saved_denominator_chain(la, oracle_mod, dtype, B, H, T, r, dv, gated, w
     d = _inputs(dtype, B, H, T, r, dv, gated, with_state, seed=500 + T + dv)
     g = {n: (t.cuda() if t is not None else None) for n, t in d.items()}
     kw = dict(alpha=g["alpha"], S0=g["S0"], z0=g["z0"], eps=EPS)
-    y, S_T, z_T, dn = la.prefill_chunked_save(g["q"], g["k"], g["v"], **kw)
+    y, S_T, z_T, dn, states = la.prefill_chunked_save(g["q"], g["k"], g["v"], **kw)
     y0, S0_, z0_ = la.prefill_chunked(g["q"], g["k"], g["v"], **kw)
     assert la.last_device_status() == 0
     assert torch.equal(y, y0) and torch.equal(S_T, S0_) and torch.equal(z_T, z0_)
@@ -85,7 +89,9 @@ def test_saved_denominator_chain(la, oracle_mod, dtype, B, H, T, r, dv, gated, w
     print(f"[parity] saved d: elementwise relative {d_err:.3e}")
     assert d_err <= TOL_D[dtype], d_err
 
-    out_saved = la.prefill_backward(g["q"], g["k"], g["v"], y, g["dy"], d=dn, **kw)
+    if states is not None:
+        _check_states(oracle_mod, d, states.cpu().double().numpy())
+    out_saved = la.prefill_backward(g["q"], g["k"], g["v"], y, g["dy"], d=dn, states=states, **kw)
     out_plain = la.prefill_backward(g["q"], g["k"], g["v"], y, g["dy"], **kw)
     assert la.last_device_status() == 0
     args = [to_oracle(d[n]) for n in ("q", "k", "v")]
@@ -103,3 +109,32 @@ def test_saved_denominator_chain(la, oracle_mod, dtype, B, H, T, r, dv, gated, w
               f"against the recomputing backward {max_rel_err(a, b):.3e}")
         assert err <= TOL_GRAD[dtype], (name, err)
         assert max_rel_err(a, b) <= TOL_GRAD[dtype], name
+
+
+def _check_states(oracle_mod, d, flat):
+    B, H, T, r = d["q"].shape
+    dv = d["v"].shape[3]
+    per = B * H * (r * dv + r)
+    assert flat.size % per == 0
+    nseg = flat.size // per
+    assert nseg >= 2
+    st = flat.reshape(nseg, B, H, r * dv + r)
+    S = st[..., :r * dv].reshape(nseg, B, H, r, dv)
+    z = st[..., r * dv:]
+    S0 = d["S0"].double().numpy() if d["S0"] is not None else np.zeros((B, H, r, dv))
+    z0 = d["z0"].double().numpy() if d["z0"] is not None else np.zeros((B, H, r))
+    assert np.array_equal(S[0], S0) and np.array_equal(z[0], z0)
+    # the oracle's state after every chunk boundary t0 (its scan over tokens [0, t0))
+    cut = lambda t, t0: to_oracle(t[:, :, :t0].contiguous()) if t is not None else None
+    prefix = {}
+    for t0 in range(64, T, 64):
+        _, Sr, zr = oracle_mod.scan(cut(d["q"], t0), cut(d["k"], t0), cut(d["v"], t0), alpha=cut(d["alpha"], t0),
+                                    S0=to_oracle(d["S0"]), z0=to_oracle(d["z0"]), eps=EPS, threads=0)
+        prefix[t0] = (Sr, zr)
+    last = 0
+    for gseg in range(1, nseg):
+        errs = {t0: max(max_rel_err(S[gseg], Sr), max_rel_err(z[gseg], zr)) for t0, (Sr, zr) in prefix.items()}
+        t0 = min(errs, key=errs.get)
+        print(f"[parity] kept state {gseg}: token {t0}, relative {errs[t0]:.3e}")
+        assert errs[t0] <= 2e-2 and t0 > last, (gseg, t0, errs[t0])
+        last = t0
