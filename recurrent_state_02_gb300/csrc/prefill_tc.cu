@@ -173,8 +173,10 @@ static_assert(smem_bytes<true, 128>() <= 232448, "shared memory budget");
 // The kernel body for one CTA.  FAST (gated whole-head CTAs only): every chunk
 // of this CTA carries its gates as row weights (see cta_all_fast), so the body is
 // built without the explicit path.  PLAIN: [B, H, T, d] inputs and one segment
-// per head (no packed sequences, no scanned start states).
-template <bool GATED, int DVS, bool FAST, bool PLAIN>
+// per head (no packed sequences, no scanned start states).  SAVE: the stores a
+// training forward asks for (d_t, and the states entering the backward's
+// segments) are compiled in; the other bodies carry none of their code.
+template <bool GATED, int DVS, bool FAST, bool PLAIN, bool SAVE>
 __device__ __forceinline__ void
 prefill_body(const CUtensorMap &map_q, const CUtensorMap &map_k, const CUtensorMap &map_v, const PrefillTcArgs &args)
 {
@@ -527,7 +529,7 @@ prefill_body(const CUtensorMap &map_q, const CUtensorMap &map_k, const CUtensorM
             if (has_p) tc_ld_16x32bx2_x8<8>(tmem + lane_base + L::kColP + pb * 64 + qq * 16, p);
             tc_wait_ld();
             // on request, the state entering chunk c where a segment of the backward starts
-            if (has_s && args.bwd_states && ((c0 + c) % args.bwd_seg_chunks) == 0 &&
+            if (SAVE && has_s && args.bwd_states && ((c0 + c) % args.bwd_seg_chunks) == 0 &&
                 (c0 + c) / args.bwd_seg_chunks < args.bwd_nseg) {
                 float *dst = args.bwd_states + ((size_t)((c0 + c) / args.bwd_seg_chunks) * args.bwd_heads + bh) *
                                                    (kR * 128 + kR);
@@ -650,7 +652,7 @@ prefill_body(const CUtensorMap &map_q, const CUtensorMap &map_k, const CUtensorM
                 const int t = tb + ce * kC + prow;
                 // d_t on request (one lane per row): the denominator of y, divided
                 // by the row weight where the chunk carries one
-                if (args.d_out && slice == 0 && qq == 0 && lane < 16 && t < T)
+                if (SAVE && args.d_out && slice == 0 && qq == 0 && lane < 16 && t < T)
                     args.d_out[tok_row(t)] = (GATED && L::kHead) ? (dn + epsw) / wrow : dn + epsw;
                 if (t < T) {
                     uint4 *dst = reinterpret_cast<uint4 *>(args.y + tok_row(t) * args.dv + slice * DVS + ocol);
@@ -803,18 +805,18 @@ __device__ __forceinline__ bool cta_all_fast(const PrefillTcArgs &args)
     return __syncthreads_and(ok) != 0;
 }
 
-template <bool GATED, int DVS, bool PLAIN>
+template <bool GATED, int DVS, bool PLAIN, bool SAVE = false>
 __global__ void __launch_bounds__(kThreads, 1)
 prefill_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
                   const __grid_constant__ CUtensorMap map_v, const PrefillTcArgs args)
 {
     if constexpr (GATED && Cfg<GATED, DVS>::kHead) {
         if (cta_all_fast(args)) {
-            prefill_body<GATED, DVS, true, PLAIN>(map_q, map_k, map_v, args);
+            prefill_body<GATED, DVS, true, PLAIN, SAVE>(map_q, map_k, map_v, args);
             return;
         }
     }
-    prefill_body<GATED, DVS, false, PLAIN>(map_q, map_k, map_v, args);
+    prefill_body<GATED, DVS, false, PLAIN, SAVE>(map_q, map_k, map_v, args);
 }
 
 }  // namespace
@@ -825,17 +827,22 @@ cudaError_t launch_prefill_tc(const CUtensorMap &map_q, const CUtensorMap &map_k
     if (dvs != 64 && dvs != 128) return cudaErrorInvalidValue;
     const dim3 grid(a.dv / dvs, a.H, B * a.nseg);
     using KernFn = void (*)(const CUtensorMap, const CUtensorMap, const CUtensorMap, const PrefillTcArgs);
-    // plain: [B, H, T, d] inputs and one segment per head
-    const bool plain = a.cu_seqlens == nullptr && a.nseg == 1 && a.S_start == nullptr;
-    const int v = (gated ? 1 : 0) + (dvs == 128 ? 2 : 0) + (plain ? 4 : 0);
-    static const KernFn kerns[8] = {prefill_tc_kernel<false, 64, false>, prefill_tc_kernel<true, 64, false>,
-                                    prefill_tc_kernel<false, 128, false>, prefill_tc_kernel<true, 128, false>,
-                                    prefill_tc_kernel<false, 64, true>,  prefill_tc_kernel<true, 64, true>,
-                                    prefill_tc_kernel<false, 128, true>, prefill_tc_kernel<true, 128, true>};
+    // plain: [B, H, T, d] inputs and one segment per head; save: the general body
+    // with the training stores
+    const bool save = a.d_out != nullptr || a.bwd_states != nullptr;
+    const bool plain = !save && a.cu_seqlens == nullptr && a.nseg == 1 && a.S_start == nullptr;
+    const int v = (gated ? 1 : 0) + (dvs == 128 ? 2 : 0) + (save ? 8 : plain ? 4 : 0);
+    static const KernFn kerns[12] = {
+        prefill_tc_kernel<false, 64, false>,       prefill_tc_kernel<true, 64, false>,
+        prefill_tc_kernel<false, 128, false>,      prefill_tc_kernel<true, 128, false>,
+        prefill_tc_kernel<false, 64, true>,        prefill_tc_kernel<true, 64, true>,
+        prefill_tc_kernel<false, 128, true>,       prefill_tc_kernel<true, 128, true>,
+        prefill_tc_kernel<false, 64, false, true>, prefill_tc_kernel<true, 64, false, true>,
+        prefill_tc_kernel<false, 128, false, true>, prefill_tc_kernel<true, 128, false, true>};
     static const uint32_t bytes[4] = {smem_bytes<false, 64>(), smem_bytes<true, 64>(), smem_bytes<false, 128>(),
                                       smem_bytes<true, 128>()};
     // The attribute is set once per device (not during stream capture of later calls).
-    static OncePerDevice attr_set[8];
+    static OncePerDevice attr_set[12];
     const cudaError_t e = set_smem_once(kerns[v], bytes[v & 3], attr_set[v]);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
