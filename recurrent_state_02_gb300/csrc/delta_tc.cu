@@ -64,11 +64,19 @@ constexpr uint32_t kPL = 0;                      // Lt (FP32, 64 x LD): Lt[u][i]
 constexpr uint32_t kPT00 = kPL + kC * LD * 4;    // T00 (FP32, [u][j])
 constexpr uint32_t kPT11t = kPT00 + 32 * LDT * 4;   // T11 transposed (FP32, [u][i])
 constexpr uint32_t kPM = kPT11t + 32 * LDT * 4;  // M = (K1 K0^T) T00 (FP32, [u][j])
-constexpr uint32_t kPK = 0;                      // K again once the solve is done (two 64-feature blocks)
-constexpr uint32_t kPT = 2 * kTQ;                // T (BF16 image)
-constexpr uint32_t kPBeta = kPT + kTV;           // beta of the chunk
+// T (BF16 image) in the rows of Lt that only the substitution of T11 reads: it is
+// written once both substitutions are done (the products after them read Lt's
+// first 32 rows, T00, T11 and M only)
+constexpr uint32_t kPT = 9 * 1024;
+// K again once T is complete, its two 64-feature blocks in space that is free by
+// then: Lt's first rows, and T00 / T11
+constexpr uint32_t kPK0 = 0, kPK1 = 18 * 1024;
+constexpr uint32_t kPBeta = 2 * kTQ;             // beta of the chunk
 constexpr uint32_t kPSmall = kPBeta + kC * 4;
 static_assert(kPM + 32 * LDT * 4 <= 2 * kTQ, "L and the solve's blocks fit in the K, Q region");
+static_assert(kPT >= (uint32_t)(kPL + 32 * LD * 4 + 32 * 4 + 32 * 4) && kPT + kTV <= kPT00,
+              "T lies past what the products read of Lt and before T00");
+static_assert(kPK0 + kTV <= kPT && kPK1 >= kPT + kTV && kPK1 + kTV <= kPM, "K lies clear of T and M");
 // workspace per chunk: the A image, the T image, then -W = -T K as the images of
 // its two 64-feature blocks
 constexpr uint32_t kWsChunk = 4 * kTV;
@@ -133,7 +141,7 @@ __device__ __forceinline__ uint32_t tile_off(int row, int col)
 // A = (Q K^T) . M, T = (I + L)^{-1} diag(beta) and -W = -T K of one chunk: one
 // CTA of 128 threads per (b, h, chunk).  Writes the BF16 images of the A and T
 // tiles (8 KB each) and of -W (two 64-feature blocks, 8 KB each) to ws.
-__global__ void __launch_bounds__(kPThreads)
+__global__ void __launch_bounds__(kPThreads, 6)
 delta_t_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
                const DeltaTcArgs args, int nch)
 {
@@ -166,8 +174,6 @@ delta_t_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant_
         const int t = t0 + tid;
         bc[tid] = t < T ? (args.beta ? args.beta[(size_t)bh * T + t] : 1.f) : 0.f;
     }
-    for (int x = tid; x < (int)(kTV / 16); x += kPThreads)   // the block above the diagonal stays zero
-        reinterpret_cast<uint4 *>(base + kPT)[x] = make_uint4(0, 0, 0, 0);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -239,11 +245,11 @@ delta_t_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant_
         __syncthreads();
         // T00, T11 by forward substitution: lane j of warp 0 (1) owns column j of
         // the block; after step u, acc[u] is final and is subtracted from the rows below.
+        float acc[32];
         if (warp < 2) {
             const int bb = 32 * warp;
             const float *Lb = Lt + bb * LD + bb;
             const float bl = bc[bb + lane];
-            float acc[32];
 #pragma unroll
             for (int i = 0; i < 32; ++i) acc[i] = i == lane ? bl : 0.f;
 #pragma unroll
@@ -267,11 +273,21 @@ delta_t_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant_
                     *reinterpret_cast<float4 *>(T11t + lane * LDT + 4 * m) =
                         make_float4(acc[4 * m], acc[4 * m + 1], acc[4 * m + 2], acc[4 * m + 3]);
             }
-#pragma unroll
-            for (int u = 0; u < 32; ++u)
-                *reinterpret_cast<uint16_t *>(base + kPT + tile_off(bb + u, bb + lane)) = bf16_bits(acc[u]);
         }
         __syncthreads();
+        // both substitutions are done: T00 and T11 into the T image (over Lt's last
+        // rows), and zeros above the diagonal
+        if (warp < 2) {
+#pragma unroll
+            for (int u = 0; u < 32; ++u)
+                *reinterpret_cast<uint16_t *>(base + kPT + tile_off(32 * warp + u, 32 * warp + lane)) = bf16_bits(acc[u]);
+        } else {
+            const int i = tid - 64;   // 0..63: rows 0..31 of the image, two of its upper 16-byte chunks each
+#pragma unroll
+            for (int x = 0; x < 2; ++x)
+                *reinterpret_cast<uint4 *>(base + kPT + sw128_offset(i >> 1, 4 + 2 * (i & 1) + x)) =
+                    make_uint4(0, 0, 0, 0);
+        }
         // M = G10 T00 and then T10 = -T11 M: thread (warp, lane) computes rows
         // 4 rg .. 4 rg + 3 and columns 2 cp, 2 cp + 1, rg = 2 warp + lane / 16
         const int rg = 2 * warp + (lane >> 4), cp = lane & 15;
@@ -316,8 +332,8 @@ delta_t_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant_
         __syncthreads();
         if (tid == 0) {
             mbar_arrive_expect_tx(&sm->full[1], kTQ);
-            tma_load_3d(base + kPK, &map_k, &sm->full[1], 0, t0, bh);
-            tma_load_3d(base + kPK + kTV, &map_k, &sm->full[1], 64, t0, bh);
+            tma_load_3d(base + kPK0, &map_k, &sm->full[1], 0, t0, bh);
+            tma_load_3d(base + kPK1, &map_k, &sm->full[1], 64, t0, bh);
         }
         uint4 *dst = reinterpret_cast<uint4 *>(wsc + kTV);
         const uint4 *src = reinterpret_cast<const uint4 *>(base + kPT);
@@ -335,7 +351,7 @@ delta_t_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant_
                 if (wok && lane == 0) {
                     tc_fence_after();
                     const uint32_t tlo = desc_lo(smem_u32(base + kPT), 16);
-                    const uint32_t klo = desc_lo(smem_u32(base + kPK + b * kTV), kTV);
+                    const uint32_t klo = desc_lo(smem_u32(base + (b ? kPK1 : kPK0)), kTV);
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk) {
                         if (kk == 0) tc_mma_bf16_w<false>(tmem, tlo, kHi128, klo, kHi128, idW);
