@@ -247,3 +247,17 @@ def test_delta_chunked_full_size_sampled_heads(la, oracle_mod):
         y_ref, S_ref = _oracle(oracle_mod, one)
         assert_close(S[b:b + 1, h:h + 1], S_ref, TOL_TC, f"chunked delta S head {b},{h}")
         assert_close(y[b:b + 1, h:h + 1], y_ref, TOL_TC, f"chunked delta y head {b},{h}")
+
+
+def test_delta_chunked_long_sequence(la, oracle_mod):
+    """512 chunks (T = 32768) with a carried state: the chain's load stages,
+    [-W; Q] buffers, accumulator buffers and barrier phases each wrap around
+    hundreds of times; both heads against the oracle."""
+    d = _inputs(1, 2, 32768, 128, 128, torch.bfloat16, True, True, seed=94)
+    y, S = _run_tc(la, d)
+    assert np.isfinite(y).all() and np.isfinite(S).all()
+    for h in range(2):
+        one = {k: (v[:, h:h + 1].contiguous() if v is not None else None) for k, v in d.items()}
+        y_ref, S_ref = _oracle(oracle_mod, one)
+        assert_close(S[:, h:h + 1], S_ref, TOL_TC, f"chunked delta S head {h}")
+        assert_close(y[:, h:h + 1], y_ref, TOL_TC, f"chunked delta y head {h}")
