@@ -33,6 +33,8 @@ CASES = [
     (torch.bfloat16, 1, 2, 1000, 128, 64, False, False),
     (torch.bfloat16, 1, 2, 2500, 128, 128, True, False),   # few long sequences: sequence segments
     (torch.bfloat16, 1, 1, 65, 128, 128, True, True),      # ragged tail of one token
+    (torch.bfloat16, 2, 2, 700, 128, 64, True, True),      # gated 64-column slices
+    (torch.bfloat16, 1, 2, 3000, 128, 128, False, True),   # ungated whole heads, segments, kept states
     (torch.float32, 2, 2, 200, 64, 64, True, True),
 ]
 
