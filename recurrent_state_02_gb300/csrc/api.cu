@@ -51,6 +51,10 @@ EncodeTiledFn encode_fn()
 #ifndef LA_HEAD_CTA
 #define LA_HEAD_CTA 1
 #endif
+// Continuations of at most this many tokens take the decode-shaped token walk.
+#ifndef LA_DECODE_MAX_T
+#define LA_DECODE_MAX_T 16
+#endif
 constexpr int kMinSegChunks = 16;    // at least 1024 tokens per segment
 constexpr int kStateCtasPerSm = 2;   // resident state-pass CTAs per SM
 constexpr int kStateCtaSetup = 2;    // set-up and pipeline fill of a state CTA, in chunks
@@ -300,6 +304,14 @@ static la_status prefill_chunked_impl(const void *q, const void *k, const void *
         for (const void *p : ptrs4)
             if (p && !aligned(p, 4)) return LA_ERR_ALIGN;
     }
+    // A short continuation (a few tokens per request from a carried state) is a
+    // decode-shaped job: the state-resident token walk reads and writes the state
+    // once, where the chunk kernel's set-up for a single partial chunk would
+    // dominate.  It computes the same recurrence in FP32 (phi in FP32 from the
+    // inputs; no BF16 operands).
+    if (T <= LA_DECODE_MAX_T && T <= 16 && dv == 128 && (!S0 || aligned(S0, 16)))
+        return from_cuda(la::launch_decode_multi(q, k, v, true, alpha, S0, z0, S_out, z_out, B, H, T, eps, y, d_out,
+                                                 st));
     const SegPlan plan = seg_plan(B, H, T, dv);
     const size_t need = seg_workspace_bytes(plan, B, H, dv);
     if (need) {

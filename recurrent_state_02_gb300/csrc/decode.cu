@@ -37,6 +37,30 @@ __device__ __forceinline__ void store_elem(void *p, size_t i, float x)
     else reinterpret_cast<float *>(p)[i] = x;
 }
 
+// Four consecutive elements (8-byte aligned for BF16, 16-byte for FP32): a raw load,
+// widened to floats when used.
+template <bool BF16> struct Quad;
+template <> struct Quad<true> {
+    using raw = uint2;
+    static __device__ __forceinline__ uint2 load(const void *p, size_t i)
+    {
+        return *reinterpret_cast<const uint2 *>(reinterpret_cast<const __nv_bfloat16 *>(p) + i);
+    }
+    static __device__ __forceinline__ float4 widen(uint2 w)
+    {
+        return make_float4(__uint_as_float(w.x << 16), __uint_as_float(w.x & 0xFFFF0000u), __uint_as_float(w.y << 16),
+                           __uint_as_float(w.y & 0xFFFF0000u));
+    }
+};
+template <> struct Quad<false> {
+    using raw = float4;
+    static __device__ __forceinline__ float4 load(const void *p, size_t i)
+    {
+        return *reinterpret_cast<const float4 *>(reinterpret_cast<const float *>(p) + i);
+    }
+    static __device__ __forceinline__ float4 widen(float4 w) { return w; }
+};
+
 __device__ __forceinline__ float4 ld_stream(const float4 *p)
 {
     float4 v;
@@ -121,6 +145,118 @@ decode128_kernel(const void *__restrict__ q, const void *__restrict__ k, const v
     }
 }
 
+// A short continuation, T <= kMultiMaxT tokens per (b, h) from a carried state,
+// r = dv = 128: the layout of decode128_kernel, with the state kept in registers
+// from the first token to the last, so that it is read and written once for all
+// T.  Every token's phi(q), phi(k), v and gate are read into shared memory up
+// front, in flight together with the state; each token then costs one block
+// barrier (the numerator's per-warp parts are double-buffered).  S0 and z0 are
+// read whole before anything is written, so they may alias S_out and z_out.
+// d_out (or nullptr) receives the denominators.
+constexpr int kMultiMaxT = 16;
+template <bool BF16>
+__global__ void __launch_bounds__(256, 2)
+decode128_multi_kernel(const void *__restrict__ q, const void *__restrict__ k, const void *__restrict__ v,
+                       const float *__restrict__ alpha, const float *S0, const float *z0, float *S_out,
+                       float *z_out, int T, float eps, void *__restrict__ y, float *__restrict__ d_out)
+{
+    constexpr int R = 128, DV = 128;
+    __shared__ float qf[kMultiMaxT][R], kf[kMultiMaxT][R];
+    __shared__ float4 vs[kMultiMaxT][DV / 4];
+    __shared__ float al[kMultiMaxT];
+    __shared__ float4 num_part[2][8][32];
+    __shared__ float den_part[2][4];
+    const int bh = blockIdx.x;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const size_t row0 = (size_t)warp * 16 * (DV / 4) + lane;   // this thread's first float4 of S
+
+    float4 s[16];
+    if (S0) {
+        const float4 *src = reinterpret_cast<const float4 *>(S0 + (size_t)bh * R * DV) + row0;
+#pragma unroll
+        for (int i = 0; i < 16; ++i) s[i] = ld_stream(src + i * (DV / 4));
+    } else {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) s[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    float zr = (tid < R && z0) ? z0[(size_t)bh * R + tid] : 0.f;
+    // the T tokens of this head are contiguous rows: 4 elements per load, all of a
+    // thread's loads issued before any is used
+    const size_t tok0 = (size_t)bh * T;
+    constexpr int kLoads = kMultiMaxT * R / 4 / 256;   // per thread and tensor
+    const int nvec = T * R / 4;
+    using Raw = typename Quad<BF16>::raw;   // the loads stay raw until they are stored
+    Raw rq[kLoads], rk[kLoads], rv[kLoads];
+#pragma unroll
+    for (int it = 0; it < kLoads; ++it) {
+        const int e = tid + it * 256;
+        if (e < nvec) {
+            rq[it] = Quad<BF16>::load(q, tok0 * R + 4 * (size_t)e);
+            rk[it] = Quad<BF16>::load(k, tok0 * R + 4 * (size_t)e);
+            rv[it] = Quad<BF16>::load(v, tok0 * DV + 4 * (size_t)e);
+        }
+    }
+    const float a_t = (tid < T && alpha) ? alpha[tok0 + tid] : 1.f;
+#pragma unroll
+    for (int it = 0; it < kLoads; ++it) {
+        const int e = tid + it * 256;
+        if (e < nvec) {
+            const float4 fq = Quad<BF16>::widen(rq[it]), fk = Quad<BF16>::widen(rk[it]);
+            reinterpret_cast<float4 *>(&qf[0][0])[e] =
+                make_float4(phi_exact(fq.x), phi_exact(fq.y), phi_exact(fq.z), phi_exact(fq.w));
+            reinterpret_cast<float4 *>(&kf[0][0])[e] =
+                make_float4(phi_exact(fk.x), phi_exact(fk.y), phi_exact(fk.z), phi_exact(fk.w));
+            reinterpret_cast<float4 *>(&vs[0][0])[e] = Quad<BF16>::widen(rv[it]);
+        }
+    }
+    if (tid < T) al[tid] = a_t;
+    __syncthreads();
+
+    for (int t = 0; t < T; ++t) {
+        const int pb = t & 1;
+        const float a = al[t];
+        const float4 vv = vs[t][lane];
+        if (tid < R) {
+            zr = fmaf(a, zr, kf[t][tid]);
+            float part = qf[t][tid] * zr;
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) part += __shfl_xor_sync(0xffffffffu, part, off);
+            if (lane == 0) den_part[pb][warp] = part;
+        }
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            const int row = warp * 16 + i;
+            const float kr = kf[t][row], qr = qf[t][row];
+            s[i].x = fmaf(a, s[i].x, kr * vv.x);
+            s[i].y = fmaf(a, s[i].y, kr * vv.y);
+            s[i].z = fmaf(a, s[i].z, kr * vv.z);
+            s[i].w = fmaf(a, s[i].w, kr * vv.w);
+            acc.x = fmaf(qr, s[i].x, acc.x);
+            acc.y = fmaf(qr, s[i].y, acc.y);
+            acc.z = fmaf(qr, s[i].z, acc.z);
+            acc.w = fmaf(qr, s[i].w, acc.w);
+        }
+        num_part[pb][warp][lane] = acc;
+        // one barrier per token: the parts of token t - 1 (the other buffer) were
+        // read before any thread passed this barrier's previous phase
+        __syncthreads();
+        if (tid < DV) {
+            const float *np = reinterpret_cast<const float *>(num_part[pb]);
+            float n = 0.f;
+#pragma unroll
+            for (int w = 0; w < 8; ++w) n += np[w * DV + tid];
+            const float den = den_part[pb][0] + den_part[pb][1] + den_part[pb][2] + den_part[pb][3] + eps;
+            store_elem<BF16>(y, (tok0 + t) * DV + tid, n / den);
+            if (d_out && tid == 0) d_out[tok0 + t] = den;
+        }
+    }
+    float4 *dst = reinterpret_cast<float4 *>(S_out + (size_t)bh * R * DV) + row0;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) st_stream(dst + i * (DV / 4), s[i]);
+    if (tid < R) z_out[(size_t)bh * R + tid] = zr;
+}
+
 // Any r, dv <= 256: thread j owns column j (and feature j for z), rows in order.
 template <bool BF16>
 __global__ void __launch_bounds__(256)
@@ -194,6 +330,21 @@ cudaError_t launch_decode(const void *q, const void *k, const void *v, bool bf16
         if (bf16) decode_generic_kernel<true><<<(unsigned)nbh, 256, 0, stream>>>(q, k, v, alpha, S, z, r, dv, eps, y);
         else decode_generic_kernel<false><<<(unsigned)nbh, 256, 0, stream>>>(q, k, v, alpha, S, z, r, dv, eps, y);
     }
+    return cudaGetLastError();
+}
+
+cudaError_t launch_decode_multi(const void *q, const void *k, const void *v, bool bf16, const float *alpha,
+                                const float *S0, const float *z0, float *S_out, float *z_out, int B, int H, int T,
+                                float eps, void *y, float *d_out, cudaStream_t stream)
+{
+    const long long nbh = (long long)B * H;
+    if (nbh < 1 || nbh > 0x7fffffffLL || T < 1 || T > kMultiMaxT) return cudaErrorInvalidValue;
+    if (bf16)
+        decode128_multi_kernel<true><<<(unsigned)nbh, 256, 0, stream>>>(q, k, v, alpha, S0, z0, S_out, z_out, T, eps,
+                                                                         y, d_out);
+    else
+        decode128_multi_kernel<false><<<(unsigned)nbh, 256, 0, stream>>>(q, k, v, alpha, S0, z0, S_out, z_out, T,
+                                                                          eps, y, d_out);
     return cudaGetLastError();
 }
 

@@ -124,6 +124,11 @@ cudaError_t launch_prefill_f32(const float *q, const float *k, const float *v, c
 cudaError_t launch_decode(const void *q, const void *k, const void *v, bool bf16, const float *alpha,
                           float *S, float *z, int B, int H, int r, int dv, float eps, void *y,
                           bool fast128, cudaStream_t stream);
+// T tokens per (b, h) (r = dv = 128) from S0, z0 (nullptr: zero) into S_out, z_out
+// (may alias), y [B,H,T,dv]; d_out (or nullptr) [B,H,T].
+cudaError_t launch_decode_multi(const void *q, const void *k, const void *v, bool bf16, const float *alpha,
+                                const float *S0, const float *z0, float *S_out, float *z_out, int B, int H, int T,
+                                float eps, void *y, float *d_out, cudaStream_t stream);
 
 // Delta-rule memory, token recurrence in FP32 (CUDA cores): r in {32, 64, 128, 256},
 // dv a multiple of 32; q, k, v, y 16-byte aligned; bf16 selects the q/k/v/y type.

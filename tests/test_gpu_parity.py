@@ -385,3 +385,41 @@ def test_prefill_varlen_bad_lengths(la, oracle_mod):
                           S0=to_oracle(S0[5:6]), z0=to_oracle(z0[5:6]), eps=1e-6)
     got = (y.float().cpu()[lo:hi].permute(1, 0, 2)[None].numpy(), S.cpu()[5:6].numpy(), z.cpu()[5:6].numpy())
     _check(got, ref, 2e-2, "varlen next to a bad sequence")
+
+
+# ------------------------------------------------------ short continuations
+# A BF16 call of at most 16 tokens at r = dv = 128 takes the decode-shaped token
+# walk (the state stays in registers for the whole run; FP32 arithmetic).
+SHORT_CASES = [
+    # B, H, T, gated, with_state
+    (3, 5, 1, False, True),
+    (2, 3, 2, True, True),
+    (4, 2, 7, True, False),
+    (2, 4, 16, False, False),
+    (1, 6, 16, True, True),
+]
+
+
+@pytest.mark.parametrize("B,H,T,gated,with_state", SHORT_CASES,
+                         ids=[f"B{c[0]}H{c[1]}T{c[2]}-g{int(c[3])}-s{int(c[4])}" for c in SHORT_CASES])
+def test_prefill_short_continuation(la, oracle_mod, B, H, T, gated, with_state):
+    inp = _inputs(torch.bfloat16, B, H, T, 128, 128, gated=gated, with_state=with_state, seed=600 + T)
+    _check(_gpu_prefill(la, inp), _oracle_prefill(oracle_mod, inp), 2e-2, f"short T={T}")
+
+
+def test_prefill_short_continuation_in_place_chain(la, oracle_mod):
+    """Prefill 100 tokens, then three continuations of 1, 5 and 16 tokens in place
+    (S0 = S_out), against one oracle pass over all 122 tokens."""
+    inp = _inputs(torch.bfloat16, 2, 3, 122, 128, 128, gated=True, with_state=True, seed=77)
+    ref = _oracle_prefill(oracle_mod, inp)
+    d = {k: (v.cuda() if v is not None else None) for k, v in inp.items()}
+    S, z = d["S0"].clone(), d["z0"].clone()
+    ys = []
+    for a, b in ((0, 100), (100, 101), (101, 106), (106, 122)):
+        part = {n: (d[n][:, :, a:b].contiguous() if d[n] is not None else None) for n in ("q", "k", "v", "alpha")}
+        y, _, _ = la.prefill_chunked(part["q"], part["k"], part["v"], alpha=part["alpha"], S0=S, z0=z,
+                                     S_out=S, z_out=z)
+        ys.append(y)
+    assert la.last_device_status() == 0
+    got = (torch.cat(ys, dim=2).float().cpu().numpy(), S.cpu().numpy(), z.cpu().numpy())
+    _check(got, ref, 2e-2, "prefill then short continuations")

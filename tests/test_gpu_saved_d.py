@@ -34,6 +34,7 @@ CASES = [
     (torch.bfloat16, 1, 2, 2500, 128, 128, True, False),   # few long sequences: sequence segments
     (torch.bfloat16, 1, 1, 65, 128, 128, True, True),      # ragged tail of one token
     (torch.bfloat16, 2, 2, 700, 128, 64, True, True),      # gated 64-column slices
+    (torch.bfloat16, 2, 3, 9, 128, 128, True, True),       # a short continuation (the token walk)
     (torch.bfloat16, 1, 2, 3000, 128, 128, False, True),   # ungated whole heads, segments, kept states
     (torch.float32, 2, 2, 200, 64, 64, True, True),
 ]
