@@ -66,6 +66,18 @@ def decode_bytes(B, H, r, dv, elem=2):
     return B * H * (2 * 4 * (r * dv + r) + elem * (2 * r + 2 * dv))
 
 
+def varlen_bytes(B, H, total_T, r, dv, elem=2):
+    """A packed batch from zero states: q, k, v read and y written (elem bytes) per
+    token-head, and each sequence's final S and z written (FP32)."""
+    return total_T * H * elem * (2 * r + 2 * dv) + B * H * 4 * (r * dv + r)
+
+
+def short_bytes(B, H, T, r, dv, gated, elem=2):
+    """A short continuation from a carried state: S and z read and written once
+    (FP32), and per token q, k, v read and y written (elem bytes) and the gate (FP32)."""
+    return B * H * (2 * 4 * (r * dv + r) + T * (elem * (2 * r + 2 * dv) + (4 if gated else 0)))
+
+
 def delta_flops(B, H, T, r, dv):
     """Algorithmic FLOPs of one delta-rule launch: per token and head, the read
     S^T k, the rank-1 write and the read S^T q, 2 r dv each."""
@@ -512,6 +524,41 @@ def run_ours(args, rank, world, local_rank):
                   "frac_of_hbm_peak": dec_gbs / peak, "launch_us": dec_launch * 1e6,
                   "algorithmic_bytes_per_launch": dbytes, "tokens_per_s": dw.B * world / dec_launch,
                   "traffic": profile_traffic("decode128_kernel<true>", "B256 H16", kernel_sources("decode.cu"))}
+        del dd, ydec, gd
+
+        # a short continuation (8 tokens per request from the carried state, gated):
+        # la_prefill_chunked in place, which takes the state-resident token walk
+        cw = W.SHORT
+        cin = {k: (v.to(dev) if v is not None else None)
+               for k, v in W.prefill_inputs(cw, with_state=True, seed=cw.seed + 1000 * rank).items()}
+        ycont = torch.empty((cw.B, cw.H, cw.T, cw.dv), device=dev, dtype=torch.bfloat16)
+
+        def k_cont():
+            _native.check(L.la_prefill_chunked(P(cin["q"]), P(cin["k"]), P(cin["v"]), _native.LA_DTYPE_BF16,
+                                               P(cin["alpha"]), P(cin["S0"]), P(cin["z0"]), cw.B, cw.H, cw.T, cw.r,
+                                               cw.dv, cw.chunk, cw.eps, P(ycont), P(cin["S0"]), P(cin["z0"]), None, 0,
+                                               sh), "la_prefill_chunked (short)")
+
+        with torch.cuda.stream(stream):
+            k_cont()
+        gc = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gc, stream=stream):
+            k_cont()
+        c_s = timed([gc] * N_ROT, args.steps, args.warmup)
+        c_s, = reduce_max([c_s], dev, dist)
+        assert _native.lib().la_last_device_status(sh) == 0
+        c_launch = c_s / args.steps
+        cbytes = short_bytes(cw.B, cw.H, cw.T, cw.r, cw.dv, cw.gated)
+        c_gbs = cbytes / c_launch / 1e9
+        decode["short_continuation"] = {
+            "workload": cw.name, "entry": "la_prefill_chunked (T <= 16: the state-resident token walk)",
+            "launch_us": c_launch * 1e6, "tokens_per_s": cw.B * cw.T * world / c_launch,
+            "token_heads_per_s": cw.B * cw.H * cw.T * world / c_launch,
+            "roofline": {"bound": "hbm", "achieved": c_gbs, "peak": peak, "unit": "GB/s", "frac": c_gbs / peak,
+                         "peak_kind": peak_kind, "algorithmic_bytes_per_launch": cbytes,
+                         "traffic": profile_traffic("decode128_multi_kernel<true>", "B256 H16 T8",
+                                                    kernel_sources("decode.cu"))}}
+        del cin, ycont, gc
 
     # the gated (B2 H16 T16384, alpha = sigmoid(N(3,1))) and long (B1 H32 T65536,
     # sigma = 2) prefill workloads, each on its own inputs from a zero state: the
@@ -569,6 +616,48 @@ def run_ours(args, rank, world, local_rank):
 
     gated_prefill = prefill_workload(W.GATED, 2, "prefill_tc_kernel<true, 128>") if want("gated") else None
     long_prefill = prefill_workload(W.LONG, 1, "prefill_tc_kernel<false, 128>") if want("long") else None
+
+    varlen = None
+    if want("varlen"):
+        # packed serving batches (la_prefill_varlen from zero states; q, k, v of 497 MB
+        # and 1.1 GB, > L2): the whole call (the plan, state pass, scan and chunk
+        # kernel when sequences are split) replayed as a CUDA graph
+        varlen = {}
+        for vw in (W.VARLEN_LONG, W.VARLEN_LOGU):
+            vin = W.varlen_inputs(vw, device=dev, seed=vw.seed + 1000 * rank)
+            nvb = len(vw.lens)
+            yv = torch.empty((vw.T, vw.H, vw.dv), device=dev, dtype=torch.bfloat16)
+            Sv = torch.empty((nvb, vw.H, vw.r, vw.dv), device=dev, dtype=torch.float32)
+            zv = torch.empty((nvb, vw.H, vw.r), device=dev, dtype=torch.float32)
+            nvws = int(L.la_prefill_varlen_workspace_bytes(nvb, vw.H, vw.T, vw.r, vw.dv))
+            vws = torch.empty(max(nvws, 256), device=dev, dtype=torch.uint8)
+
+            def k_varlen():
+                _native.check(L.la_prefill_varlen(P(vin["q"]), P(vin["k"]), P(vin["v"]), _native.LA_DTYPE_BF16, None,
+                                                  None, None, P(vin["cu_seqlens"]), nvb, vw.H, vw.T, vw.r, vw.dv,
+                                                  vw.chunk, vw.eps, P(yv), P(Sv), P(zv), P(vws) if nvws else None,
+                                                  nvws, sh), "la_prefill_varlen")
+
+            with torch.cuda.stream(stream):
+                k_varlen()
+            gv = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(gv, stream=stream):
+                k_varlen()
+            v_s = timed([gv] * N_ROT, args.steps, args.warmup)
+            v_s, = reduce_max([v_s], dev, dist)
+            assert _native.lib().la_last_device_status(sh) == 0
+            v_call = v_s / args.steps
+            vbytes = varlen_bytes(nvb, vw.H, vw.T, vw.r, vw.dv)
+            v_gbs = vbytes / v_call / 1e9
+            varlen[vw.name] = {
+                "call_us": v_call * 1e6, "tokens_per_s": vw.T * world / v_call,
+                "token_heads_per_s": vw.T * vw.H * world / v_call, "sequences": nvb, "tokens": vw.T,
+                "longest": max(vw.lens), "launches_per_call": 4 if nvws else 1,
+                "roofline": {"bound": "hbm", "achieved": v_gbs, "peak": peak, "unit": "GB/s", "frac": v_gbs / peak,
+                             "peak_kind": peak_kind, "algorithmic_bytes_per_launch": vbytes,
+                             "timed": "the whole call"}}
+            del vin, yv, Sv, zv, vws, gv
+        torch.cuda.empty_cache()
 
     if want("delta"):
         # delta-rule memory on its own workload (B=4, H=16, T=4096, r = dv = 128, BF16;
@@ -786,6 +875,7 @@ def run_ours(args, rank, world, local_rank):
                            "parallelism": f"replicas x{world} (independent batches, no collective)",
                            "launch": "CUDA graph per step"},
                 "roofline": roofline, "decode": decode, "gated_prefill": gated_prefill, "long_prefill": long_prefill,
+                "varlen": varlen,
                 "delta_rule": delta, "backward": backward, "cpu_baseline": cpu,
                 "e2e": e2e,
                 "gpu_launches": launches_per_step * args.steps, "clocks": clocks}
@@ -802,7 +892,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--only", default="",
                     help="comma-separated subset of the extra workloads to run beside the step: "
-                         "decode,gated,long,delta,backward,e2e (default: all)")
+                         "decode,gated,long,varlen,delta,backward,e2e (default: all)")
     ap.add_argument("--clock-warmup-seconds", type=float, default=0.6,
                     help="untimed load before timing so that clock samples see the GPU busy (0 under a profiler)")
     args = ap.parse_args()

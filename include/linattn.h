@@ -127,6 +127,15 @@ la_status la_prefill_chunked(const void *q, const void *k, const void *v, la_dty
                              void *workspace, size_t workspace_bytes, la_stream_t stream);
 
 /*
+ * la_prefill_varlen_workspace_bytes -- device scratch that la_prefill_varlen needs
+ * for a batch of B sequences, H heads and total_T tokens on the current device (0:
+ * the sequences are never split into segments).  It depends on the sizes and the
+ * device's SM count only, not on the lengths, which stay on the device.  Returns 0
+ * for sizes la_prefill_varlen rejects.
+ */
+size_t la_prefill_varlen_workspace_bytes(int B, int H, int total_T, int r, int dv);
+
+/*
  * la_prefill_varlen -- la_prefill_chunked for a batch of sequences of different
  * lengths packed one after another, e.g. the prompts of a serving batch, each
  * prefilled in large blocks and continuing from its own state ([LA]
@@ -144,16 +153,29 @@ la_status la_prefill_chunked(const void *q, const void *k, const void *v, la_dty
  *              The host cannot read it; a kernel finding a sequence outside
  *              [0, total_T] or of negative length skips it and records LA_ERR_SHAPE
  *              (read it with la_last_device_status).
+ *   workspace  device scratch of la_prefill_varlen_workspace_bytes(B, H, total_T, r, dv)
+ *              bytes, 256-byte aligned, owned by the caller and not read by the
+ *              caller afterwards; may be NULL when that is 0.  Calls that may
+ *              overlap in time need their own.
+ * Long sequences are split into segments, as la_prefill_chunked splits a long T
+ * ([LA] "门控递推为什么能做并行 scan？": a run of tokens composes into one affine map
+ * of the state): a plan kernel reads the lengths and picks the segment length from
+ * the batch's own chunk count, so that a long prompt among short ones no longer
+ * holds up the batch; a state pass over the segments that end before a sequence's
+ * last one and a scan give every segment its start state.  When no sequence is
+ * long enough, or any sequence's bounds are invalid, nothing is split.
  * Requires BF16, r == 128, dv in {64, 128}, chunk >= 1 (computed in chunks of 64
- * tokens, as la_prefill_chunked); q, k, v, y, S_out 16-byte aligned.  total_T may be 0.  The sequences are not split into segments (no
- * workspace).  Rows of y outside every sequence are not written.
+ * tokens, as la_prefill_chunked); q, k, v, y, S_out 16-byte aligned.  total_T may be 0.
+ * Rows of y outside every sequence are not written.
  * Errors: LA_ERR_NULL, LA_ERR_SHAPE, LA_ERR_DTYPE, LA_ERR_ALIGN, LA_ERR_UNSUPPORTED
- *         (FP32 or other sizes), LA_ERR_CUDA.
+ *         (FP32 or other sizes), LA_ERR_WORKSPACE (workspace missing or too small),
+ *         LA_ERR_CUDA.
  */
 la_status la_prefill_varlen(const void *q, const void *k, const void *v, la_dtype dtype,
                             const float *alpha, const float *S0, const float *z0, const int *cu_seqlens,
                             int B, int H, int total_T, int r, int dv, int chunk, float eps,
-                            void *y, float *S_out, float *z_out, la_stream_t stream);
+                            void *y, float *S_out, float *z_out,
+                            void *workspace, size_t workspace_bytes, la_stream_t stream);
 
 /*
  * la_prefill_chunked_noalloc -- la_prefill_chunked without caller scratch: the

@@ -148,12 +148,22 @@ def _prefill(q, k, v, alpha, S0, z0, chunk, eps, y, S_out, z_out, workspace, d_o
     return y, S_out, z_out
 
 
+def varlen_workspace_bytes(B, H, total_T, r, dv, device=None) -> int:
+    """Scratch bytes of prefill_varlen for these sizes on `device` (default: the
+    current device); it depends on the device's SM count, not on the lengths."""
+    if device is None:
+        return int(_native.lib().la_prefill_varlen_workspace_bytes(B, H, total_T, r, dv))
+    with _device_guard(torch.device(device)):
+        return int(_native.lib().la_prefill_varlen_workspace_bytes(B, H, total_T, r, dv))
+
+
 def prefill_varlen(q, k, v, cu_seqlens, alpha=None, S0=None, z0=None, chunk=64, eps=1e-6, y=None, S_out=None,
-                   z_out=None):
+                   z_out=None, workspace=None):
     """Packed sequences of different lengths: q, k [total_T, H, r], v [total_T, H, dv]
     (bf16, token-major); cu_seqlens int32 [B+1] on the device (sequence b is tokens
     cu_seqlens[b] .. cu_seqlens[b+1]-1); alpha [total_T, H] fp32 or None; S0
-    [B,H,r,dv], z0 [B,H,r] fp32 or None.  Returns (y [total_T, H, dv], S_T, z_T)."""
+    [B,H,r,dv], z0 [B,H,r] fp32 or None; workspace uint8 of varlen_workspace_bytes
+    (allocated here when None).  Returns (y [total_T, H, dv], S_T, z_T)."""
     if q.dtype not in _DTYPES:
         raise ValueError(f"unsupported dtype {q.dtype}")
     total_T, H, r = q.shape
@@ -178,10 +188,15 @@ def prefill_varlen(q, k, v, cu_seqlens, alpha=None, S0=None, z0=None, chunk=64, 
     _require(y, "y", (total_T, H, dv), q.dtype, dev)
     _require(S_out, "S_out", (B, H, r, dv), torch.float32, dev)
     _require(z_out, "z_out", (B, H, r), torch.float32, dev)
+    need = varlen_workspace_bytes(B, H, total_T, r, dv, device=dev)
+    if need and workspace is None:
+        workspace = torch.empty(need, device=dev, dtype=torch.uint8)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     with _device_guard(dev):
         st = _native.lib().la_prefill_varlen(
             _ptr(q), _ptr(k), _ptr(v), _DTYPES[q.dtype], _ptr(alpha), _ptr(S0), _ptr(z0), _ptr(cu_seqlens), B, H,
-            total_T, r, dv, chunk, float(eps), _ptr(y), _ptr(S_out), _ptr(z_out), _stream(dev))
+            total_T, r, dv, chunk, float(eps), _ptr(y), _ptr(S_out), _ptr(z_out), _ptr(workspace), ws_bytes,
+            _stream(dev))
     _native.check(st, "la_prefill_varlen")
     return y, S_out, z_out
 

@@ -21,8 +21,9 @@ SIGNATURES = {
     "la_prefill_workspace_bytes": (_sz, [_i, _i, _i, _i, _i, _i]),
     "la_prefill_chunked": (_i, [_vp, _vp, _vp, _i, _fp, _fp, _fp, _i, _i, _i, _i, _i, _i, _f, _vp, _fp, _fp,
                                 _vp, _sz, _vp]),
+    "la_prefill_varlen_workspace_bytes": (_sz, [_i, _i, _i, _i, _i]),
     "la_prefill_varlen": (_i, [_vp, _vp, _vp, _i, _fp, _fp, _fp, _vp, _i, _i, _i, _i, _i, _i, _f, _vp, _fp, _fp,
-                               _vp]),
+                               _vp, _sz, _vp]),
     "la_prefill_chunked_noalloc": (_i, [_vp, _vp, _vp, _i, _fp, _fp, _fp, _i, _i, _i, _i, _i, _i, _f, _vp, _fp,
                                         _fp, _vp]),
     "la_decode_step": (_i, [_vp, _vp, _vp, _i, _fp, _fp, _fp, _i, _i, _i, _i, _f, _vp, _vp]),

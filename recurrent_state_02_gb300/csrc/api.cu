@@ -166,6 +166,58 @@ size_t seg_workspace_bytes(const SegPlan &p, int B, int H, int dv)
     return seg_workspace_bytes(p.nsub, p.nseg, B, H, dv);
 }
 
+// Segments of a packed batch (la_prefill_varlen).  The host knows B, H and the
+// total only; the device plan splits each sequence into segments of L >= min_seg
+// chunks once it has read the lengths, so min_seg bounds the boundaries by
+// total_T / (64 min_seg).  min_seg is a quarter of an SM's share of the largest
+// possible batch of CTA-chunks, which keeps (boundaries x CTAs per segment) below
+// 4 SMs' worth, and so the workspace, whatever the total.  Workspace (256-byte
+// aligned parts): seg_len int[2], seq_info int4[B], items int2[B + max_bds], bds
+// int2[max_bds], A and dS of the state pass's parts, and 2 max_bds start-state
+// slots (a split sequence has at most twice as many segments as boundaries).
+struct VarlenPlan {
+    int dvs = 64, units = 0, min_seg = 0, max_bds = 0, sub_per_seg = 1;
+    size_t off_info = 0, off_items = 0, off_bds = 0, off_A = 0, off_dS = 0, off_S = 0, bytes = 0;
+};
+
+VarlenPlan varlen_plan(int B, int H, int total_T, int dv)
+{
+    VarlenPlan p;
+    const long long sms = sm_count();
+    p.dvs = head_width(B, H, dv, sms);
+    p.units = H * (dv / p.dvs);
+    if (sms <= 0 || total_T <= 0 || B < 1) return p;
+    const long long work = ((long long)(total_T + 63) / 64 + B) * p.units;   // CTA-chunks at most
+    long long L = (work + 4 * sms - 1) / (4 * sms);
+    if (L < kMinSegChunks) L = kMinSegChunks;
+    const long long nb = (long long)total_T / (64 * L);
+    if (nb < 1 || B + nb > 65535) return p;   // grid rows of the chunk kernel
+    // parts of the state pass over the nb full segments, as for the [B, H, T, d] layout
+    const long long slots = kStateCtasPerSm * sms;
+    long long best_cost = -1;
+    int best_n = 1;
+    for (int n = 1; n <= L && nb * n <= 65535 && nb * p.units * n <= 2 * slots; ++n) {
+        const long long waves = (nb * p.units * n + slots - 1) / slots;
+        const long long cost = waves * ((L + n - 1) / n + kStateCtaSetup);
+        if (best_cost < 0 || cost < best_cost) {
+            best_cost = cost;
+            best_n = n;
+        }
+    }
+    p.min_seg = (int)L;
+    p.max_bds = (int)nb;
+    p.sub_per_seg = best_n;
+    const size_t state = 128 * (size_t)dv + 128, nparts = (size_t)nb * best_n;
+    p.off_info = 256;
+    p.off_items = p.off_info + round_up(16 * (size_t)B, 256);
+    p.off_bds = p.off_items + round_up(8 * ((size_t)B + nb), 256);
+    p.off_A = p.off_bds + round_up(8 * (size_t)nb, 256);
+    p.off_dS = p.off_A + round_up(4 * nparts * H, 256);
+    p.off_S = p.off_dS + round_up(4 * nparts * H * state, 256);
+    p.bytes = p.off_S + 4 * 2 * (size_t)nb * H * state;
+    return p;
+}
+
 // Scratch of la_prefill_chunked_noalloc: a fixed buffer in the library's device
 // image, for callers that cannot pass device memory of their own.  It holds the
 // largest workspace a plan asks for (kMaxPlanWorkspace).
@@ -411,10 +463,17 @@ size_t la_backward_states_bytes(int B, int H, int T)
     return p.nseg > 1 ? sizeof(float) * (size_t)p.nseg * B * H * (128 * 128 + 128) : 0;
 }
 
+size_t la_prefill_varlen_workspace_bytes(int B, int H, int total_T, int r, int dv)
+{
+    if (B < 1 || H < 1 || total_T < 1 || r != 128 || (dv != 64 && dv != 128)) return 0;
+    if ((long long)B * H > 0x7fffffffLL || (long long)total_T * H > 0x7fffffffLL) return 0;
+    return varlen_plan(B, H, total_T, dv).bytes;
+}
+
 la_status la_prefill_varlen(const void *q, const void *k, const void *v, la_dtype dtype, const float *alpha,
                             const float *S0, const float *z0, const int *cu_seqlens, int B, int H, int total_T,
                             int r, int dv, int chunk, float eps, void *y, float *S_out, float *z_out,
-                            la_stream_t stream)
+                            void *workspace, size_t workspace_bytes, la_stream_t stream)
 {
     if (!cu_seqlens || !S_out || !z_out) return LA_ERR_NULL;
     if (total_T > 0 && (!q || !k || !v || !y)) return LA_ERR_NULL;
@@ -430,8 +489,14 @@ la_status la_prefill_varlen(const void *q, const void *k, const void *v, la_dtyp
         for (const void *p : ptrs4)
             if (p && !aligned(p, 4)) return LA_ERR_ALIGN;
     }
+    const VarlenPlan plan = varlen_plan(B, H, total_T, dv);
+    if (plan.bytes) {
+        if (!workspace || workspace_bytes < plan.bytes) return LA_ERR_WORKSPACE;
+        if (!aligned(workspace, 256)) return LA_ERR_ALIGN;
+    }
     int *status = status_word();
     if (!status) return LA_ERR_CUDA;
+    const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     // token-major views [total_T, H, d]; with no tokens at all no tile is ever
     // loaded, and any aligned address serves as the maps' base
     const void *qb = total_T ? q : S_out, *kb = total_T ? k : S_out, *vb = total_T ? v : S_out;
@@ -457,9 +522,47 @@ la_status la_prefill_varlen(const void *q, const void *k, const void *v, la_dtyp
     a.seg_chunks = 0;
     a.S_start = nullptr;
     a.cu_seqlens = cu_seqlens;
-    const int dvs = head_width(B, H, dv, sm_count());
-    return from_cuda(
-        la::launch_prefill_tc(mq, mk, mv, a, B, alpha != nullptr, dvs, reinterpret_cast<cudaStream_t>(stream)));
+    if (!plan.bytes)
+        return from_cuda(la::launch_prefill_tc(mq, mk, mv, a, B, alpha != nullptr, plan.dvs, st));
+    // the plan (segment length and tables) on the device, the state pass over the
+    // segments that end at a boundary, the scan of each split sequence, then every
+    // segment in parallel
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    int *seg_len = reinterpret_cast<int *>(ws);
+    int4 *seq_info = reinterpret_cast<int4 *>(ws + plan.off_info);
+    int2 *items = reinterpret_cast<int2 *>(ws + plan.off_items);
+    int2 *bds = reinterpret_cast<int2 *>(ws + plan.off_bds);
+    float *A = reinterpret_cast<float *>(ws + plan.off_A);
+    float *dS = reinterpret_cast<float *>(ws + plan.off_dS);
+    float *S_start = reinterpret_cast<float *>(ws + plan.off_S);
+    cudaError_t e = la::launch_varlen_plan(cu_seqlens, B, total_T, plan.min_seg, plan.units, sm_count(),
+                                           plan.max_bds, plan.sub_per_seg, seg_len, seq_info, items, bds, st);
+    la::StateTcArgs sa;
+    sa.alpha = alpha;
+    sa.dS = dS;
+    sa.A = A;
+    sa.H = H;
+    sa.T = total_T;
+    sa.dv = dv;
+    sa.nsub = 0;
+    sa.sub_per_seg = plan.sub_per_seg;
+    sa.sub_chunks = 0;
+    sa.seg_chunks = 0;
+    sa.cu_seqlens = cu_seqlens;
+    sa.bds = bds;
+    sa.seg_len = seg_len;
+    sa.status = status;
+    sa.wait_limit_ns = la::kWaitLimitNs;
+    if (e == cudaSuccess)
+        e = la::launch_state_tc(mk, mv, sa, B, alpha != nullptr, plan.dvs, st, false,
+                                plan.max_bds * plan.sub_per_seg);
+    if (e == cudaSuccess) e = la::launch_varlen_scan(S0, z0, A, dS, S_start, seq_info, B, H, dv, plan.sub_per_seg, st);
+    if (e != cudaSuccess) return from_cuda(e);
+    a.items = items;
+    a.seq_info = seq_info;
+    a.seg_len = seg_len;
+    a.S_start = S_start;
+    return from_cuda(la::launch_prefill_tc(mq, mk, mv, a, B, alpha != nullptr, plan.dvs, st, B + plan.max_bds));
 }
 
 la_status la_prefill_chunked_noalloc(const void *q, const void *k, const void *v, la_dtype dtype,

@@ -212,6 +212,7 @@ decode128_multi_kernel(const void *__restrict__ q, const void *__restrict__ k, c
     if (tid < T) al[tid] = a_t;
     __syncthreads();
 
+    const bool gated = alpha != nullptr;
     for (int t = 0; t < T; ++t) {
         const int pb = t & 1;
         const float a = al[t];
@@ -223,21 +224,27 @@ decode128_multi_kernel(const void *__restrict__ q, const void *__restrict__ k, c
             for (int off = 16; off > 0; off >>= 1) part += __shfl_xor_sync(0xffffffffu, part, off);
             if (lane == 0) den_part[pb][warp] = part;
         }
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        // two columns per instruction (packed FP32 pairs, each lane rounded as
+        // its scalar fmaf / multiply would be)
+        const float2 v01 = make_float2(vv.x, vv.y), v23 = make_float2(vv.z, vv.w), a2 = make_float2(a, a);
+        float2 acc01 = make_float2(0.f, 0.f), acc23 = make_float2(0.f, 0.f);
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
             const int row = warp * 16 + i;
-            const float kr = kf[t][row], qr = qf[t][row];
-            s[i].x = fmaf(a, s[i].x, kr * vv.x);
-            s[i].y = fmaf(a, s[i].y, kr * vv.y);
-            s[i].z = fmaf(a, s[i].z, kr * vv.z);
-            s[i].w = fmaf(a, s[i].w, kr * vv.w);
-            acc.x = fmaf(qr, s[i].x, acc.x);
-            acc.y = fmaf(qr, s[i].y, acc.y);
-            acc.z = fmaf(qr, s[i].z, acc.z);
-            acc.w = fmaf(qr, s[i].w, acc.w);
+            const float2 kr = make_float2(kf[t][row], kf[t][row]), qr = make_float2(qf[t][row], qf[t][row]);
+            float2 s01 = make_float2(s[i].x, s[i].y), s23 = make_float2(s[i].z, s[i].w);
+            if (gated) {
+                s01 = __ffma2_rn(a2, s01, __fmul2_rn(kr, v01));
+                s23 = __ffma2_rn(a2, s23, __fmul2_rn(kr, v23));
+            } else {
+                s01 = __ffma2_rn(kr, v01, s01);
+                s23 = __ffma2_rn(kr, v23, s23);
+            }
+            acc01 = __ffma2_rn(qr, s01, acc01);
+            acc23 = __ffma2_rn(qr, s23, acc23);
+            s[i] = make_float4(s01.x, s01.y, s23.x, s23.y);
         }
-        num_part[pb][warp][lane] = acc;
+        num_part[pb][warp][lane] = make_float4(acc01.x, acc01.y, acc23.x, acc23.y);
         // one barrier per token: the parts of token t - 1 (the other buffer) were
         // read before any thread passed this barrier's previous phase
         __syncthreads();

@@ -67,6 +67,15 @@ struct PrefillTcArgs {
     // cu_seqlens[b+1]-1 of q, k [T, H, 128], v, y [T, H, dv], alpha [T, H] (T the
     // total); the tensor maps are token-major views.  nullptr: [B, H, T, d] layout.
     const int *cu_seqlens;
+    // Packed sequences split into segments (the varlen plan's tables; else nullptr):
+    // items[blockIdx.z] = (b, g), segment g of sequence b (b < 0: no work; the
+    // plan writes the longest segments first), and seq_info[b] = (segments, first
+    // S_start slot, first boundary, 0).  A
+    // sequence of more than one segment starts every segment from S_start[slot + g]
+    // ([slot][H][128*dv + 128]); one of a single segment reads S0 itself.
+    const int2 *items = nullptr;
+    const int4 *seq_info = nullptr;
+    const int *seg_len = nullptr;   // with items: chunks per segment (in place of seg_chunks)
     float eps;
     int *status;          // device status word
     unsigned long long wait_limit_ns;
@@ -76,9 +85,10 @@ struct PrefillTcArgs {
 // columns per CTA, 64 (the slices of a head form a cluster) or 128 (one CTA per
 // head and segment).  Tensor maps: q, k over [B*H, T, 128]; v over [B*H, T, dv]
 // (BF16, 128-byte swizzle, boxes of 64 x 64).
+// grid_z (0: B * nseg) rows of CTAs; the varlen plan's item count when a.items is set.
 cudaError_t launch_prefill_tc(const CUtensorMap &map_q, const CUtensorMap &map_k,
                               const CUtensorMap &map_v, const PrefillTcArgs &a, int B, bool gated, int dvs,
-                              cudaStream_t stream);
+                              cudaStream_t stream, int grid_z = 0);
 
 // State pass of the sequence-segmented BF16 prefill (r == 128, dv a multiple of
 // dvs, chunk 64): for every sub-segment of a head's sequence, the state it would
@@ -95,6 +105,13 @@ struct StateTcArgs {
     int seg_first = 0;    // segment of the first part (the reversed pass covers segments 1 .. nseg-1)
     const float *d = nullptr;    // reversed pass: d_t and dd_t [B*H*T] of the backward
     const float *dd = nullptr;
+    // Packed sequences (token-major maps, alpha [T, H]): bds[k] = (b, g) for the
+    // varlen plan's boundary k, the full segment g of sequence b that ends there
+    // (b < 0: none); part j of it is CTA row k * sub_per_seg + j, and its outputs
+    // are row (k * sub_per_seg + j) * H + h of A and dS.
+    const int *cu_seqlens = nullptr;
+    const int2 *bds = nullptr;
+    const int *seg_len = nullptr;   // with bds: chunks per segment and per part (in place of seg_chunks, sub_chunks)
     int *status;          // device status word
     unsigned long long wait_limit_ns;
 };
@@ -103,8 +120,26 @@ struct StateTcArgs {
 // k over [B*H, T, 128] and v over [B*H, T, dv] as for launch_prefill_tc.
 // rev: the backward's reversed pass (dvs 128, seg_first 1): k is the map of q,
 // v the map of dy, and d, dd are given; the part maps carry [G | g].
+// grid_z (0: B * nsub) rows of CTAs; boundaries * sub_per_seg when a.bds is set.
 cudaError_t launch_state_tc(const CUtensorMap &map_k, const CUtensorMap &map_v, const StateTcArgs &a, int B,
-                            bool gated, int dvs, cudaStream_t stream, bool rev = false);
+                            bool gated, int dvs, cudaStream_t stream, bool rev = false, int grid_z = 0);
+
+// The varlen plan: from cu_seqlens [B + 1] (device), the segment length L >=
+// min_seg_chunks (from the batch's chunks, units CTAs per segment, sms SMs), and
+// sequence b of c_b chunks takes max(1, ceil(c_b / L)) segments; with bounds
+// outside [0, total_T] anywhere, or more than max_bds boundaries, one segment
+// each.  Writes seg_len [2] (L, chunks per part of sub_per_seg), seq_info [B],
+// items [B + max_bds] (longest segments first) and bds [max_bds] (see
+// PrefillTcArgs and StateTcArgs; unused entries b = -1).  One CTA.
+cudaError_t launch_varlen_plan(const int *cu_seqlens, int B, int total_T, int min_seg_chunks, int units, int sms,
+                               int max_bds, int sub_per_seg, int *seg_len, int4 *seq_info, int2 *items, int2 *bds,
+                               cudaStream_t stream);
+
+// The varlen scan: for every sequence of more than one segment and head h,
+// S_start[slot + 0] = S0[b], z0[b] (zero if null), then S_start[slot + g] the
+// state after the maps of boundary (first + g - 1)'s sub_per_seg parts, in order.
+cudaError_t launch_varlen_scan(const float *S0, const float *z0, const float *A, const float *dS, float *S_start,
+                               const int4 *seq_info, int B, int H, int dv, int sub_per_seg, cudaStream_t stream);
 
 // S_start[g][bh] (S then z) for g < nseg: S0/z0 (zero if null) carried through the
 // sub-segment maps S -> A S + dS in order.  rev: the maps of the reversed pass,

@@ -170,13 +170,34 @@ static_assert(smem_bytes<true, 64>() <= 232448, "shared memory budget");
 static_assert(smem_bytes<false, 128>() <= 232448, "shared memory budget");
 static_assert(smem_bytes<true, 128>() <= 232448, "shared memory budget");
 
+// This CTA's sequence b and segment g of it, the sequence's segment count, the
+// chunks per segment, and the S_start slot its start state is read from (-1: S0
+// itself).  Segments come
+// from the varlen plan's item table, or grid.z enumerates (b, segment) of the
+// [B, H, T, d] layout with args.nseg segments per sequence.
+struct CtaUnit {
+    int b, seg, nseg, len, slot;
+};
+template <bool ITEMS>
+__device__ __forceinline__ CtaUnit cta_unit(const PrefillTcArgs &args)
+{
+    if (ITEMS) {
+        const int2 it = args.items[blockIdx.z];
+        const int4 si = args.seq_info[it.x];
+        return CtaUnit{it.x, it.y, si.x, args.seg_len[0], si.x > 1 ? si.y + it.y : -1};
+    }
+    const int B = gridDim.z / args.nseg, b = blockIdx.z / args.nseg, seg = blockIdx.z % args.nseg;
+    return CtaUnit{b, seg, args.nseg, args.seg_chunks, args.S_start ? seg * B + b : -1};
+}
+
 // The kernel body for one CTA.  FAST (gated whole-head CTAs only): every chunk
 // of this CTA carries its gates as row weights (see cta_all_fast), so the body is
 // built without the explicit path.  PLAIN: [B, H, T, d] inputs and one segment
 // per head (no packed sequences, no scanned start states).  SAVE: the stores a
 // training forward asks for (d_t, and the states entering the backward's
-// segments) are compiled in; the other bodies carry none of their code.
-template <bool GATED, int DVS, bool FAST, bool PLAIN, bool SAVE>
+// segments) are compiled in; the other bodies carry none of their code.  ITEMS:
+// the CTA's sequence and segment come from the varlen plan's item table.
+template <bool GATED, int DVS, bool FAST, bool PLAIN, bool SAVE, bool ITEMS>
 __device__ __forceinline__ void
 prefill_body(const CUtensorMap &map_q, const CUtensorMap &map_k, const CUtensorMap &map_v, const PrefillTcArgs &args)
 {
@@ -191,10 +212,9 @@ prefill_body(const CUtensorMap &map_q, const CUtensorMap &map_k, const CUtensorM
     Ctx cx{&sm->abort_flag, args.wait_limit_ns, args.status};
 
     const int slice = blockIdx.x;
-    // grid.z enumerates (b, sequence segment); one segment unless the caller
-    // split the sequence (then every segment starts from a scanned state)
     const int h = blockIdx.y;
-    const int b = PLAIN ? (int)blockIdx.z : blockIdx.z / args.nseg, seg = PLAIN ? 0 : blockIdx.z % args.nseg;
+    const CtaUnit u = PLAIN ? CtaUnit{(int)blockIdx.z, 0, 1, 0, -1} : cta_unit<ITEMS>(args);
+    const int b = u.b, seg = u.seg;
     const int bh = b * args.H + h;
     // Packed sequences of different lengths (cu_seqlens; no segments) or the
     // [B, H, T, d] layout.  A sequence whose bounds are inconsistent with the
@@ -218,14 +238,14 @@ prefill_body(const CUtensorMap &map_q, const CUtensorMap &map_k, const CUtensorM
     auto tma_c1 = [&](int t0) { return varlen ? h : t0; };
     auto tma_c2 = [&](int t0) { return varlen ? seq0 + t0 : bh; };
     const int nch_all = (T + kC - 1) / kC;
-    const int c0 = seg * args.seg_chunks;                                     // first chunk of the segment
-    const int nch = (!PLAIN && args.nseg > 1) ? min(args.seg_chunks, nch_all - c0) : nch_all;   // its chunk count
+    const int c0 = seg * u.len;                                               // first chunk of the segment
+    const int nch = (!PLAIN && u.nseg > 1) ? min(u.len, nch_all - c0) : nch_all;   // its chunk count
     const int tb = c0 * kC;                                                   // its first token
-    const bool last_seg = PLAIN || seg == args.nseg - 1;
+    const bool last_seg = PLAIN || seg == u.nseg - 1;
     // start state of this head: S0/z0, or the scanned state of the segment
     const size_t state_len = (size_t)kR * args.dv + kR;
-    const bool scanned = !PLAIN && args.S_start != nullptr;
-    const float *S_init = scanned ? args.S_start + ((size_t)seg * (gridDim.z / args.nseg) * args.H + bh) * state_len
+    const bool scanned = u.slot >= 0;
+    const float *S_init = scanned ? args.S_start + ((size_t)u.slot * args.H + h) * state_len
                                   : (args.S0 ? args.S0 + (size_t)bh * kR * args.dv : nullptr);
     const float *z_init_src = scanned ? S_init + (size_t)kR * args.dv : (args.z0 ? args.z0 + (size_t)bh * kR : nullptr);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -774,9 +794,11 @@ prefill_body(const CUtensorMap &map_q, const CUtensorMap &map_k, const CUtensorM
 // above e^{kFastGateLog + 4}, a margin over the producer's own test (gate_products),
 // whose sums run in another order.  All threads take part; the result is the
 // same for every thread.
+template <bool PLAIN, bool ITEMS>
 __device__ __forceinline__ bool cta_all_fast(const PrefillTcArgs &args)
 {
-    const int h = blockIdx.y, b = blockIdx.z / args.nseg, seg = blockIdx.z % args.nseg;
+    const CtaUnit u = PLAIN ? CtaUnit{(int)blockIdx.z, 0, 1, 0, -1} : cta_unit<ITEMS>(args);
+    const int h = blockIdx.y, b = u.b, seg = u.seg;
     const int bh = b * args.H + h;
     const bool varlen = args.cu_seqlens != nullptr;
     int seq0 = 0, T = args.T;
@@ -788,8 +810,8 @@ __device__ __forceinline__ bool cta_all_fast(const PrefillTcArgs &args)
         T = seq1 - seq0;
     }
     const int nch_all = ok ? (T + kC - 1) / kC : 0;
-    const int c0 = seg * args.seg_chunks;
-    const int nch = args.nseg > 1 ? min(args.seg_chunks, nch_all - c0) : nch_all;
+    const int c0 = seg * u.len;
+    const int nch = u.nseg > 1 ? min(u.len, nch_all - c0) : nch_all;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     for (int c = warp; ok && c < nch; c += kThreads / 32) {
         const int t0 = (c0 + c) * kC + 2 * lane;
@@ -805,44 +827,54 @@ __device__ __forceinline__ bool cta_all_fast(const PrefillTcArgs &args)
     return __syncthreads_and(ok) != 0;
 }
 
-template <bool GATED, int DVS, bool PLAIN, bool SAVE = false>
+template <bool GATED, int DVS, bool PLAIN, bool SAVE = false, bool ITEMS = false>
 __global__ void __launch_bounds__(kThreads, 1)
 prefill_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
                   const __grid_constant__ CUtensorMap map_v, const PrefillTcArgs args)
 {
+    // a row of the varlen plan's item table beyond its items: no work (every CTA
+    // of a cluster has the same row)
+    if (ITEMS && args.items[blockIdx.z].x < 0) return;
     if constexpr (GATED && Cfg<GATED, DVS>::kHead) {
-        if (cta_all_fast(args)) {
-            prefill_body<GATED, DVS, true, PLAIN, SAVE>(map_q, map_k, map_v, args);
+        if (cta_all_fast<PLAIN, ITEMS>(args)) {
+            prefill_body<GATED, DVS, true, PLAIN, SAVE, ITEMS>(map_q, map_k, map_v, args);
             return;
         }
     }
-    prefill_body<GATED, DVS, false, PLAIN, SAVE>(map_q, map_k, map_v, args);
+    prefill_body<GATED, DVS, false, PLAIN, SAVE, ITEMS>(map_q, map_k, map_v, args);
 }
 
 }  // namespace
 
 cudaError_t launch_prefill_tc(const CUtensorMap &map_q, const CUtensorMap &map_k, const CUtensorMap &map_v,
-                              const PrefillTcArgs &a, int B, bool gated, int dvs, cudaStream_t stream)
+                              const PrefillTcArgs &a, int B, bool gated, int dvs, cudaStream_t stream,
+                              int grid_z)
 {
     if (dvs != 64 && dvs != 128) return cudaErrorInvalidValue;
-    const dim3 grid(a.dv / dvs, a.H, B * a.nseg);
+    if (a.items && (grid_z < 1 || !a.seq_info || !a.seg_len || !a.cu_seqlens || !a.S_start))
+        return cudaErrorInvalidValue;
+    const dim3 grid(a.dv / dvs, a.H, a.items ? grid_z : B * a.nseg);
     using KernFn = void (*)(const CUtensorMap, const CUtensorMap, const CUtensorMap, const PrefillTcArgs);
     // plain: [B, H, T, d] inputs and one segment per head; save: the general body
     // with the training stores
     const bool save = a.d_out != nullptr || a.bwd_states != nullptr;
-    const bool plain = !save && a.cu_seqlens == nullptr && a.nseg == 1 && a.S_start == nullptr;
-    const int v = (gated ? 1 : 0) + (dvs == 128 ? 2 : 0) + (save ? 8 : plain ? 4 : 0);
-    static const KernFn kerns[12] = {
+    const bool plain = !save && a.cu_seqlens == nullptr && a.nseg == 1 && a.S_start == nullptr && !a.items;
+    // items: the varlen plan's segments (never with the training stores)
+    if (a.items && save) return cudaErrorInvalidValue;
+    const int v = (gated ? 1 : 0) + (dvs == 128 ? 2 : 0) + (save ? 8 : a.items ? 12 : plain ? 4 : 0);
+    static const KernFn kerns[16] = {
         prefill_tc_kernel<false, 64, false>,       prefill_tc_kernel<true, 64, false>,
         prefill_tc_kernel<false, 128, false>,      prefill_tc_kernel<true, 128, false>,
         prefill_tc_kernel<false, 64, true>,        prefill_tc_kernel<true, 64, true>,
         prefill_tc_kernel<false, 128, true>,       prefill_tc_kernel<true, 128, true>,
         prefill_tc_kernel<false, 64, false, true>, prefill_tc_kernel<true, 64, false, true>,
-        prefill_tc_kernel<false, 128, false, true>, prefill_tc_kernel<true, 128, false, true>};
+        prefill_tc_kernel<false, 128, false, true>, prefill_tc_kernel<true, 128, false, true>,
+        prefill_tc_kernel<false, 64, false, false, true>, prefill_tc_kernel<true, 64, false, false, true>,
+        prefill_tc_kernel<false, 128, false, false, true>, prefill_tc_kernel<true, 128, false, false, true>};
     static const uint32_t bytes[4] = {smem_bytes<false, 64>(), smem_bytes<true, 64>(), smem_bytes<false, 128>(),
                                       smem_bytes<true, 128>()};
     // The attribute is set once per device (not during stream capture of later calls).
-    static OncePerDevice attr_set[12];
+    static OncePerDevice attr_set[16];
     const cudaError_t e = set_smem_once(kerns[v], bytes[v & 3], attr_set[v]);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};

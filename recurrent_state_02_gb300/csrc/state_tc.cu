@@ -106,15 +106,39 @@ state_tc_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant
     RevRing *rr = reinterpret_cast<RevRing *>(base + L::kOffRev);      // REV or gated
     Ctx cx{&sm->abort_flag, args.wait_limit_ns, args.status};
 
-    // grid: (dv slice, h, b * nsub + m); sub-segment m is part j of output segment g
+    // grid: (dv slice, h, b * nsub + m); sub-segment m is part j of output segment g.
+    // Packed sequences: (dv slice, h, k * sub_per_seg + j), part j of the segment
+    // that ends at the varlen plan's boundary k.
     const int slice = blockIdx.x, h = blockIdx.y;
-    const int b = blockIdx.z / args.nsub, m = blockIdx.z % args.nsub;
-    const int BH = (gridDim.z / args.nsub) * args.H;
+    const bool varlen = args.bds != nullptr;
+    int b, g, j, seq0 = 0, T = args.T, seg_chunks = args.seg_chunks, sub_chunks = args.sub_chunks;
+    size_t orow;   // row of this part's outputs in A and dS
+    if (varlen) {
+        const int2 e = args.bds[blockIdx.z / args.sub_per_seg];
+        if (e.x < 0) return;   // beyond the plan's boundaries: no work
+        b = e.x;
+        g = e.y;
+        j = blockIdx.z % args.sub_per_seg;
+        seq0 = args.cu_seqlens[b];
+        T = args.cu_seqlens[b + 1] - seq0;
+        seg_chunks = args.seg_len[0];
+        sub_chunks = args.seg_len[1];
+        orow = (size_t)blockIdx.z * args.H + h;
+    } else {
+        b = blockIdx.z / args.nsub;
+        const int m = blockIdx.z % args.nsub;
+        g = m / args.sub_per_seg + args.seg_first;
+        j = m % args.sub_per_seg;
+        orow = (size_t)m * ((gridDim.z / args.nsub) * args.H) + b * args.H + h;
+    }
     const int bh = b * args.H + h;
-    const int T = args.T;
-    const int g = m / args.sub_per_seg + args.seg_first, j = m % args.sub_per_seg;
-    const int cs = g * args.seg_chunks + j * args.sub_chunks;                 // first chunk
-    const int nch = max(0, min(min(cs + args.sub_chunks, (g + 1) * args.seg_chunks), (args.T + kC - 1) / kC) - cs);
+    // the last two TMA coordinates of a box starting at token t0, and the row of
+    // token t's gate
+    auto tma_c1 = [&](int t0) { return varlen ? h : t0; };
+    auto tma_c2 = [&](int t0) { return varlen ? seq0 + t0 : bh; };
+    auto gate_row = [&](int t) -> size_t { return varlen ? (size_t)(seq0 + t) * args.H + h : (size_t)bh * T + t; };
+    const int cs = g * seg_chunks + j * sub_chunks;                           // first chunk
+    const int nch = max(0, min(min(cs + sub_chunks, (g + 1) * seg_chunks), (T + kC - 1) / kC) - cs);
     const int tb = cs * kC;                                                   // first token
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     // first token of the c-th chunk processed: from the part's end in forward time,
@@ -183,9 +207,8 @@ state_tc_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant
             const int t0 = chunk_t0(c);
             float a0 = 1.f, a1 = 1.f;
             if (GATED) {
-                const float *ap = args.alpha + (size_t)bh * T;
-                if (t0 + 2 * lane < T) a0 = ap[t0 + 2 * lane];
-                if (t0 + 2 * lane + 1 < T) a1 = ap[t0 + 2 * lane + 1];
+                if (t0 + 2 * lane < T) a0 = args.alpha[gate_row(t0 + 2 * lane)];
+                if (t0 + 2 * lane + 1 < T) a1 = args.alpha[gate_row(t0 + 2 * lane + 1)];
             }
             float2 dv2 = make_float2(1.f, 1.f), dd2 = make_float2(0.f, 0.f);
             if (REV) {
@@ -201,19 +224,20 @@ state_tc_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant
             uint8_t *st = stage_ptr(s);
             if (lane == 0) {
                 mbar_arrive_expect_tx(&sm->full[s], kTileK + L::kTileV);
-                tma_load_3d(st + L::kOffK, &map_k, &sm->full[s], 0, t0, bh);
-                tma_load_3d(st + L::kOffK + kTileK / 2, &map_k, &sm->full[s], 64, t0, bh);
+                const int cy = tma_c1(t0), cz = tma_c2(t0);
+                tma_load_3d(st + L::kOffK, &map_k, &sm->full[s], 0, cy, cz);
+                tma_load_3d(st + L::kOffK + kTileK / 2, &map_k, &sm->full[s], 64, cy, cz);
 #pragma unroll
                 for (int vb = 0; vb < DVS / 64; ++vb)
-                    tma_load_3d(st + L::kOffV + vb * kBlkV, &map_v, &sm->full[s], slice * DVS + vb * 64, t0, bh);
+                    tma_load_3d(st + L::kOffV + vb * kBlkV, &map_v, &sm->full[s], slice * DVS + vb * 64, cy, cz);
                 if (c + NST < nch) {   // warm L2 for the load that reuses this stage
-                    const int tp = chunk_t0(c + NST);
+                    const int tp = chunk_t0(c + NST), yp = tma_c1(tp), zp = tma_c2(tp);
                     if (slice == 0) {
-                        tma_prefetch_l2_3d(&map_k, 0, tp, bh);
-                        tma_prefetch_l2_3d(&map_k, 64, tp, bh);
+                        tma_prefetch_l2_3d(&map_k, 0, yp, zp);
+                        tma_prefetch_l2_3d(&map_k, 64, yp, zp);
                     }
 #pragma unroll
-                    for (int vb = 0; vb < DVS / 64; ++vb) tma_prefetch_l2_3d(&map_v, slice * DVS + vb * 64, tp, bh);
+                    for (int vb = 0; vb < DVS / 64; ++vb) tma_prefetch_l2_3d(&map_v, slice * DVS + vb * 64, yp, zp);
                 }
             }
             if (GATED) {
@@ -238,7 +262,7 @@ state_tc_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant
         }
         // the part's gate product (1 without a gate or chunks)
         if (lane == 0 && slice == 0 && !aborted(cx))
-            args.A[(size_t)m * BH + bh] = (GATED && issued == nch) ? (cut ? 0.f : expf(off)) : 1.f;
+            args.A[orow] = (GATED && issued == nch) ? (cut ? 0.f : expf(off)) : 1.f;
         __syncwarp();
     } else if (warp == kWarpMma) {
         // ------------------------------------------------------------ MMA
@@ -290,7 +314,7 @@ state_tc_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant
             if (ok) {
                 tc_fence_after();
                 const size_t state_len = (size_t)kR * args.dv + kR;
-                float *out = args.dS + ((size_t)m * BH + bh) * state_len;
+                float *out = args.dS + orow * state_len;
                 float *dst = out + (size_t)srow * args.dv + slice * DVS;
                 float sh[32], zz;
                 tc_ld_32x32b_x1(tmem + lane_base + DVS, zz);
@@ -404,13 +428,228 @@ __global__ void seg_scan_kernel(const float *S0, const float *z0, const float *A
     }
 }
 
+// Exclusive prefix sum over the 1024 threads of a block (v >= 0); total in *sum.
+__device__ __forceinline__ int block_excl_scan(int v, int *warp_sums, int *sum)
+{
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    int x = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+    }
+    if (lane == 31) warp_sums[warp] = x;
+    __syncthreads();
+    if (warp == 0) {
+        int w = warp_sums[lane];
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, w, o);
+            if (lane >= o) w += y;
+        }
+        warp_sums[lane] = w;   // inclusive over warps
+        if (lane == 31) *sum = w;
+    }
+    __syncthreads();
+    const int before = (warp ? warp_sums[warp - 1] : 0) + x - v;
+    __syncthreads();   // warp_sums and *sum are reused by the next call
+    return before;
+}
+
+// Bucket of an item of c chunks in the longest-first order: c itself below 64,
+// then 8 buckets per octave; larger items get smaller keys.
+constexpr int kOrderBuckets = 64 + 8 * 26;
+__device__ __forceinline__ int order_key(int c)
+{
+    int idx = c;
+    if (c >= 64) {
+        const int oct = 31 - __clz(c);   // >= 6
+        idx = 64 + 8 * (oct - 6) + ((c >> (oct - 3)) & 7);
+    }
+    return kOrderBuckets - 1 - idx;
+}
+
+// Segments of a packed batch.  Sequence b (tokens cu[b] .. cu[b+1]-1, c_b chunks)
+// takes ceil(c_b / L) segments of L chunks.  L is the larger of L_min and an SM's
+// share of the batch's CTA-chunks (units CTAs per segment on sms SMs), so that
+// only a sequence that would hold up the batch is split.  With L >= L_min the
+// boundaries of valid disjoint sequences stay within floor(total_T / (64 L_min))
+// = max_bds; if any sequence's bounds lie outside [0, total_T] (the chunk kernel
+// records it) or the count exceeds max_bds regardless, no sequence is split.
+// The boundaries and the start-state slots of the split sequences are numbered
+// in sequence order; the items (every segment of every sequence) are written
+// longest first, so that the chunk kernel's CTAs start in that order and the
+// short ones fill in at the end (within a bucket of order_key, in no set order).
+// seg_len receives L and the chunks of each of a segment's sub_per_seg parts.
+__global__ void __launch_bounds__(1024)
+varlen_plan_kernel(const int *__restrict__ cu, int B, int total_T, int L_min, int units, int sms, int max_bds,
+                   int sub_per_seg, int *__restrict__ seg_len, int4 *__restrict__ seq_info, int2 *__restrict__ items,
+                   int2 *__restrict__ bds)
+{
+    __shared__ int warp_sums[32];
+    __shared__ int tot[2];
+    __shared__ unsigned long long acc[2];
+    __shared__ int bucket[kOrderBuckets];
+    auto chunks = [&](int b, bool &bad) {
+        const int s0 = cu[b], s1 = cu[b + 1];
+        if (s0 < 0 || s1 < s0 || s1 > total_T) {
+            bad = true;
+            return 0;
+        }
+        return (s1 - s0 + kC - 1) / kC;
+    };
+    if (threadIdx.x == 0) acc[0] = acc[1] = 0;
+    for (int i = threadIdx.x; i < kOrderBuckets; i += blockDim.x) bucket[i] = 0;
+    __syncthreads();
+    // pass 1: the batch's chunks, and whether every sequence is valid
+    unsigned long long sum = 0;
+    bool bad = false;
+    for (int b = threadIdx.x; b < B; b += blockDim.x) sum += chunks(b, bad);
+    atomicAdd(&acc[0], sum);
+    const bool any_bad = __syncthreads_or(bad) != 0;
+    const unsigned long long share = (acc[0] * (unsigned long long)units + sms - 1) / (unsigned long long)sms;
+    const int L = (int)max((unsigned long long)L_min, min(share, (unsigned long long)0x3fffffff));
+    // pass 2: the boundaries this L takes
+    unsigned long long count = 0;
+    for (int b = threadIdx.x; b < B; b += blockDim.x) {
+        bool dummy = false;
+        const int c = chunks(b, dummy);
+        count += c > L ? (c + L - 1) / L - 1 : 0;
+    }
+    atomicAdd(&acc[1], count);
+    __syncthreads();
+    const bool split = !any_bad && acc[1] <= (unsigned long long)max_bds;
+    if (threadIdx.x == 0) {
+        seg_len[0] = L;
+        seg_len[1] = (L + sub_per_seg - 1) / sub_per_seg;
+    }
+    // the segments of sequence b: nseg, and the chunks of the last one (the others have L)
+    auto segments = [&](int b, int &last) {
+        bool dummy = false;
+        const int c = chunks(b, dummy);
+        if (!split || c <= L) {
+            last = c;
+            return 1;
+        }
+        const int n = (c + L - 1) / L;
+        last = c - (n - 1) * L;
+        return n;
+    };
+    // pass 3: how many items fall in each bucket of the order
+    for (int b = threadIdx.x; b < B; b += blockDim.x) {
+        int last;
+        const int n = segments(b, last);
+        if (n > 1) atomicAdd(&bucket[order_key(L)], n - 1);
+        atomicAdd(&bucket[order_key(last)], 1);
+    }
+    __syncthreads();
+    // exclusive prefix over the buckets: their first rows in the item table
+    {
+        const int v = threadIdx.x < kOrderBuckets ? bucket[threadIdx.x] : 0;
+        const int first = block_excl_scan(v, warp_sums, &tot[0]);
+        if (threadIdx.x < kOrderBuckets) bucket[threadIdx.x] = first;
+        __syncthreads();
+    }
+    // pass 4: prefix sums of boundaries and slots, tile by tile, and each item's row
+    int carry_bd = 0, carry_slot = 0;
+    for (int b0 = 0; b0 < B; b0 += blockDim.x) {
+        const int b = b0 + threadIdx.x;
+        int last = 0;
+        const int nseg = b < B ? segments(b, last) : 1;
+        const int nbd = nseg - 1, nslot = nseg > 1 ? nseg : 0;
+        const int bd0 = carry_bd + block_excl_scan(nbd, warp_sums, &tot[0]);
+        const int tile_bd = tot[0];
+        const int slot0 = carry_slot + block_excl_scan(nslot, warp_sums, &tot[1]);
+        const int tile_slot = tot[1];
+        if (b < B) {
+            seq_info[b] = make_int4(nseg, nseg > 1 ? slot0 : -1, bd0, 0);
+            for (int g = 0; g < nseg; ++g)
+                items[atomicAdd(&bucket[order_key(g + 1 < nseg ? L : last)], 1)] = make_int2(b, g);
+            for (int g = 0; g + 1 < nseg; ++g) bds[bd0 + g] = make_int2(b, g);
+        }
+        carry_bd += tile_bd;
+        carry_slot += tile_slot;
+        __syncthreads();   // tot is rewritten by the next tile
+    }
+    // pass 5: the rows past the plan's items and boundaries do nothing
+    for (int i = B + carry_bd + threadIdx.x; i < B + max_bds; i += blockDim.x) items[i] = make_int2(-1, 0);
+    for (int k = carry_bd + threadIdx.x; k < max_bds; k += blockDim.x) bds[k] = make_int2(-1, 0);
+}
+
+// The start state of every segment of every split sequence: slot 0 holds S0, z0;
+// slot g the state after the maps of the parts that end at boundary first + g - 1
+// (S -> A S + dS, in order).  One thread per 4 consecutive state elements of a
+// head; a thread issues the loads of up to 8 parts before it applies them.
+__global__ void varlen_scan_kernel(const float *S0, const float *z0, const float *A, const float *dS, float *S_start,
+                                   const int4 *__restrict__ seq_info, int H, int dv, int sub_per_seg)
+{
+    const int b = blockIdx.x / H, h = blockIdx.x % H, bh = blockIdx.x;
+    const int4 si = seq_info[b];
+    if (si.x <= 1) return;
+    const int e = 4 * (blockIdx.y * blockDim.x + threadIdx.x);
+    const int s_len = kR * dv;
+    const int state_len = s_len + kR;
+    if (e >= state_len) return;
+    const float *src0 = e < s_len ? (S0 ? S0 + (size_t)bh * s_len + e : nullptr)
+                                  : (z0 ? z0 + (size_t)bh * kR + (e - s_len) : nullptr);
+    float4 s = src0 ? make_float4(src0[0], src0[1], src0[2], src0[3]) : make_float4(0.f, 0.f, 0.f, 0.f);
+    *reinterpret_cast<float4 *>(S_start + ((size_t)si.y * H + h) * state_len + e) = s;
+    const int nparts = (si.x - 1) * sub_per_seg;
+    const size_t part0 = (size_t)si.z * sub_per_seg;
+    for (int i0 = 0; i0 < nparts; i0 += 8) {
+        float4 d[8];
+        float a[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const size_t row = (part0 + i0 + i) * H + h;
+            d[i] = i0 + i < nparts ? *reinterpret_cast<const float4 *>(dS + row * state_len + e)
+                                   : make_float4(0.f, 0.f, 0.f, 0.f);
+            a[i] = i0 + i < nparts ? A[row] : 1.f;
+        }
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            if (i0 + i >= nparts) break;
+            s.x = fmaf(a[i], s.x, d[i].x);
+            s.y = fmaf(a[i], s.y, d[i].y);
+            s.z = fmaf(a[i], s.z, d[i].z);
+            s.w = fmaf(a[i], s.w, d[i].w);
+            if ((i0 + i + 1) % sub_per_seg == 0) {
+                const int g = (i0 + i + 1) / sub_per_seg;
+                *reinterpret_cast<float4 *>(S_start + ((size_t)(si.y + g) * H + h) * state_len + e) = s;
+            }
+        }
+    }
+}
+
 }  // namespace
 
+cudaError_t launch_varlen_plan(const int *cu_seqlens, int B, int total_T, int min_seg_chunks, int units, int sms,
+                               int max_bds, int sub_per_seg, int *seg_len, int4 *seq_info, int2 *items, int2 *bds,
+                               cudaStream_t stream)
+{
+    if (B < 1 || min_seg_chunks < 1 || units < 1 || sms < 1 || max_bds < 0 || total_T < 0 || sub_per_seg < 1)
+        return cudaErrorInvalidValue;
+    varlen_plan_kernel<<<1, 1024, 0, stream>>>(cu_seqlens, B, total_T, min_seg_chunks, units, sms, max_bds,
+                                                sub_per_seg, seg_len, seq_info, items, bds);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_varlen_scan(const float *S0, const float *z0, const float *A, const float *dS, float *S_start,
+                               const int4 *seq_info, int B, int H, int dv, int sub_per_seg, cudaStream_t stream)
+{
+    if (B < 1 || H < 1 || sub_per_seg < 1 || (long long)B * H > 0x7fffffffLL) return cudaErrorInvalidValue;
+    const int state_len = kR * dv + kR;
+    const dim3 grid(B * H, (state_len / 4 + 255) / 256);
+    varlen_scan_kernel<<<grid, 256, 0, stream>>>(S0, z0, A, dS, S_start, seq_info, H, dv, sub_per_seg);
+    return cudaGetLastError();
+}
+
 cudaError_t launch_state_tc(const CUtensorMap &map_k, const CUtensorMap &map_v, const StateTcArgs &a, int B,
-                            bool gated, int dvs, cudaStream_t stream, bool rev)
+                            bool gated, int dvs, cudaStream_t stream, bool rev, int grid_z)
 {
     if ((dvs != 64 && dvs != 128) || (rev && (dvs != 128 || !a.d || !a.dd))) return cudaErrorInvalidValue;
-    const dim3 grid(a.dv / dvs, a.H, B * a.nsub);
+    if (a.bds && (rev || grid_z < 1 || !a.cu_seqlens || !a.seg_len || a.sub_per_seg < 1)) return cudaErrorInvalidValue;
+    const dim3 grid(a.dv / dvs, a.H, a.bds ? grid_z : B * a.nsub);
     using KernFn = void (*)(const CUtensorMap, const CUtensorMap, const StateTcArgs);
     const int v = rev ? 4 + (gated ? 1 : 0) : (gated ? 1 : 0) + (dvs == 128 ? 2 : 0);
     static const KernFn kerns[6] = {state_tc_kernel<false, 64, false>,  state_tc_kernel<true, 64, false>,

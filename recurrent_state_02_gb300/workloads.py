@@ -34,6 +34,7 @@ class Workload:
     seed: int = 0
     decode: bool = False        # one token per request on a pre-existing state
     draw_fp64: bool = False     # draw in FP64 before rounding to ``dtype``
+    lens: tuple = ()            # packed sequences: the length of each (B of them, T in total)
 
     @property
     def token_heads(self) -> int:
@@ -59,6 +60,27 @@ WORKLOADS = {"tiny": TINY, "ungated": UNGATED, "gated": GATED, "decode": DECODE,
 DELTA = Workload("delta rule B4 H16 T4096 d128 bf16, unit q and k, beta=sigmoid(N(0,1))", B=4, H=16, T=4096,
                  seed=5)
 
+# A short continuation: 8 tokens per request on a carried state (the decode
+# requests' state distribution), gated; the state (256 MiB) exceeds L2.
+def _loguniform_lens(n, lo, hi, seed):
+    g = torch.Generator().manual_seed(seed)
+    u = torch.rand(n, generator=g, dtype=torch.float64)
+    return tuple(int(x) for x in torch.exp(u * (torch.log(torch.tensor(float(hi))) - torch.log(torch.tensor(float(lo))))
+                                             + torch.log(torch.tensor(float(lo)))))
+
+
+# Packed serving batches (la_prefill_varlen, token-major, from zero states, no gate):
+# one long prompt among short ones, and prompt lengths spread log-uniformly.
+_LONG_MIX = (16384,) + (512,) * 47
+VARLEN_LONG = Workload("varlen one prompt of 16384 + 47 of 512 tokens H16 d128 bf16", B=len(_LONG_MIX), H=16,
+                       T=sum(_LONG_MIX), lens=_LONG_MIX, seed=7)
+_LOGU_MIX = _loguniform_lens(48, 128, 8192, seed=8)
+VARLEN_LOGU = Workload("varlen 48 prompts of log-uniform 128..8192 tokens H16 d128 bf16", B=48, H=16,
+                       T=sum(_LOGU_MIX), lens=_LOGU_MIX, seed=8)
+
+SHORT = Workload("short continuation B256 H16 T8 d128 bf16 alpha=sigmoid(N(3,1)), fp32 state", B=256, H=16, T=8,
+                 gated=True, seed=6)
+
 
 def prefill_inputs(w: Workload, device="cpu", with_state: bool = False, seed: int | None = None):
     """q, k [B,H,T,r], v [B,H,T,dv] in ``w.dtype``; alpha [B,H,T] FP32 or None;
@@ -83,6 +105,20 @@ def prefill_inputs(w: Workload, device="cpu", with_state: bool = False, seed: in
     out = dict(q=q, k=k, v=v, alpha=alpha, S0=S0, z0=z0)
     if device != "cpu":
         out = {n: (t.to(device) if t is not None else None) for n, t in out.items()}
+    return out
+
+
+def varlen_inputs(w: Workload, device="cpu", seed: int | None = None):
+    """Packed sequences of lengths ``w.lens``: q, k [T, H, r], v [T, H, dv] in
+    ``w.dtype`` (token-major, T = sum of the lengths), drawn as ``prefill_inputs``
+    draws one sequence of T tokens; cu_seqlens int32 [B + 1]."""
+    one = prefill_inputs(w.with_(B=1, T=sum(w.lens)), seed=seed)
+    tok = lambda x: x[0].permute(1, 0, 2).contiguous()
+    cu = torch.zeros(len(w.lens) + 1, dtype=torch.int32)
+    cu[1:] = torch.cumsum(torch.tensor(w.lens, dtype=torch.int64), 0).to(torch.int32)
+    out = dict(q=tok(one["q"]), k=tok(one["k"]), v=tok(one["v"]), cu_seqlens=cu)
+    if device != "cpu":
+        out = {n: t.to(device) for n, t in out.items()}
     return out
 
 

@@ -129,11 +129,12 @@ def test_workloads_follow_the_recipe():
 
 def _varlen(native, **kw):
     a = dict(q=FAKE, k=FAKE, v=FAKE, dtype=native.LA_DTYPE_BF16, alpha=None, S0=None, z0=None, cu=FAKE, B=2, H=1,
-             T=100, r=128, dv=128, chunk=64, eps=1e-6, y=FAKE, S_out=FAKE, z_out=FAKE, stream=None)
+             T=100, r=128, dv=128, chunk=64, eps=1e-6, y=FAKE, S_out=FAKE, z_out=FAKE, ws=None, ws_bytes=0,
+             stream=None)
     a.update(kw)
     return native.lib().la_prefill_varlen(a["q"], a["k"], a["v"], a["dtype"], a["alpha"], a["S0"], a["z0"], a["cu"],
                                           a["B"], a["H"], a["T"], a["r"], a["dv"], a["chunk"], a["eps"], a["y"],
-                                          a["S_out"], a["z_out"], a["stream"])
+                                          a["S_out"], a["z_out"], a["ws"], a["ws_bytes"], a["stream"])
 
 
 def test_varlen_rejects_bad_arguments(native):
@@ -147,6 +148,16 @@ def test_varlen_rejects_bad_arguments(native):
     assert _varlen(native, dv=96) == native.LA_ERR_UNSUPPORTED
     assert _varlen(native, q=FAKE + 8) == native.LA_ERR_ALIGN
     assert _varlen(native, cu=FAKE + 2) == native.LA_ERR_ALIGN
+
+
+def test_varlen_workspace_bytes(native):
+    L = native.lib()
+    # sizes la_prefill_varlen rejects need nothing
+    for args in ((0, 16, 4096, 128, 128), (4, 0, 4096, 128, 128), (4, 16, 0, 128, 128), (4, 16, 4096, 64, 128),
+                 (4, 16, 4096, 128, 96)):
+        assert L.la_prefill_varlen_workspace_bytes(*args) == 0
+    # the plan follows the current device's SM count (none here): no segments
+    assert L.la_prefill_varlen_workspace_bytes(48, 16, 40448, 128, 128) == 0
 
 
 def test_delta_rejects_bad_arguments(native):

@@ -112,7 +112,7 @@ def test_every_wrapper_calls_with_the_tensors_device_current(rec, monkeypatch):
     la.prefill_chunked(q, k, v)   # outputs allocated by the wrapper
     la.last_device_status(DEV)
     _check(rec, "la_state_init", "la_prefill_chunked", "la_prefill_workspace_bytes", "la_prefill_chunked_noalloc",
-           "la_decode_step", "la_prefill_varlen", "la_delta_rule", "la_delta_rule_chunked", "la_prefill_backward", "la_last_device_status")
+           "la_decode_step", "la_prefill_varlen_workspace_bytes", "la_prefill_varlen", "la_delta_rule", "la_delta_rule_chunked", "la_prefill_backward", "la_last_device_status")
 
 
 def test_tensors_on_another_device_are_refused(rec):

@@ -1,0 +1,202 @@
+"""Packed sequences split into segments: la_prefill_varlen on batches where some
+sequences are long enough for the plan kernel to cut them into segments (a state
+pass and a scan give each segment its start state: "门控递推为什么能做并行 scan？" of
+[LA], a run of tokens is one affine map of the state).
+
+Every sequence is held to the oracle run over that sequence alone, from its own
+S0, z0 (BF16 bar 2e-2, as the other prefill tests).  The plan's segment length
+and the segment count of each sequence are read back from the head of the
+workspace (the length at byte 0, the per-sequence int4 records from byte 256:
+segments, first start-state slot, first boundary; the item table of (sequence,
+segment) pairs after them, from the next 256-byte boundary), so each test also
+checks that the split it is about took place and that the chunk kernel's CTAs
+start with the longest segments.
+"""
+import numpy as np
+import pytest
+import torch
+
+from conftest import assert_close, to_oracle
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def la():
+    from recurrent_state_02_gb300 import build
+    build.build()
+    import recurrent_state_02_gb300 as la_mod
+    assert torch.cuda.is_available()
+    return la_mod
+
+
+def _packed(lens, H, dv, gated, seed, zero_gates=()):
+    """q, k, v [total, H, d] BF16 and alpha [total, H] FP32 (token-major), cu_seqlens,
+    S0 [B, H, 128, dv] ~ N(0, 0.01), z0 [B, H, 128] ~ U(1, 11).  zero_gates: absolute
+    token rows whose gate is set to 0 (every head)."""
+    from recurrent_state_02_gb300 import workloads as W
+    cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    total = int(cu[-1])
+    base = W.prefill_inputs(W.Workload("varlen", B=1, H=H, T=total, dv=dv, dtype=torch.bfloat16, gated=gated,
+                                       seed=seed))
+    tok = lambda x: x[0].permute(1, 0, 2).contiguous()
+    alpha = base["alpha"][0].permute(1, 0).contiguous() if gated else None
+    if alpha is not None:
+        for t in zero_gates:
+            alpha[t] = 0.0
+    g = torch.Generator().manual_seed(seed + 1)
+    B = len(lens)
+    S0 = (torch.randn(B, H, 128, dv, generator=g) * 0.1).float()
+    z0 = (torch.rand(B, H, 128, generator=g) * 10 + 1).float()
+    return dict(q=tok(base["q"]), k=tok(base["k"]), v=tok(base["v"]), alpha=alpha, cu=cu, S0=S0, z0=z0)
+
+
+def _run(la, d, in_place=False):
+    B = len(d["cu"]) - 1
+    total, H, _ = d["q"].shape
+    dv = d["v"].shape[2]
+    need = la.varlen_workspace_bytes(B, H, total, 128, dv)
+    ws = torch.zeros(max(need, 256), device="cuda", dtype=torch.uint8)
+    g = {n: (d[n].cuda() if d[n] is not None else None) for n in ("q", "k", "v", "alpha", "S0", "z0")}
+    kw = dict(S_out=g["S0"], z_out=g["z0"]) if in_place else {}
+    y, S, z = la.prefill_varlen(g["q"], g["k"], g["v"], torch.from_numpy(d["cu"]).cuda(), alpha=g["alpha"],
+                                S0=g["S0"], z0=g["z0"], workspace=ws if need else None, **kw)
+    status = la.last_device_status()
+    plan = None
+    if need:
+        w = ws.cpu()
+        L = int(w[:4].view(torch.int32)[0])
+        info = w[256:256 + 16 * B].view(torch.int32).view(B, 4).numpy()
+        off = 256 + (16 * B + 255) // 256 * 256
+        n_items = B + int(np.sum(info[:, 0] - 1))
+        items = w[off:off + 8 * n_items].view(torch.int32).view(n_items, 2).numpy()
+        plan = (L, info, items)
+    return (y.float().cpu(), S.cpu(), z.cpu()), status, plan
+
+
+def _order_key(c):
+    """Larger items first: c itself below 64, then 8 buckets per octave."""
+    if c < 64:
+        return -c
+    o = c.bit_length() - 1
+    return -(64 + 8 * (o - 6) + ((c >> (o - 3)) & 7))
+
+
+def _check_plan(plan, lens, expect_split=True, invalid=()):
+    assert plan is not None, "no workspace: the plan does not segment at these sizes"
+    L, info, items = plan
+    assert L >= 16
+    # a sequence with bad bounds counts as empty
+    chunks = [0 if b in invalid else (n + 63) // 64 for b, n in enumerate(lens)]
+    want = [(c + L - 1) // L if (expect_split and c > L) else 1 for c in chunks]
+    assert list(info[:, 0]) == want, (L, list(info[:, 0]), want)
+    if expect_split:
+        assert max(want) > 1, "no sequence was split"
+        # boundaries and start-state slots are numbered in sequence order
+        bd = np.concatenate([[0], np.cumsum([n - 1 for n in want])])[:-1]
+        assert list(info[:, 2]) == list(bd)
+        slots = np.concatenate([[0], np.cumsum([n if n > 1 else 0 for n in want])])[:-1]
+        assert [int(info[b, 1]) for b in range(len(lens)) if want[b] > 1] == \
+            [int(slots[b]) for b in range(len(lens)) if want[b] > 1]
+    # every segment once, longest first
+    pairs = sorted(map(tuple, items.tolist()))
+    assert pairs == sorted((b, g) for b in range(len(lens)) for g in range(want[b]))
+    seg_chunks = lambda b, g: L if g + 1 < want[b] else chunks[b] - (want[b] - 1) * L
+    keys = [_order_key(seg_chunks(b, g)) for b, g in items.tolist()]
+    assert keys == sorted(keys)
+    return L
+
+
+def _check_seqs(oracle_mod, d, got, skip=()):
+    y, S, z = got
+    cu = d["cu"]
+    for b in range(len(cu) - 1):
+        if b in skip:
+            continue
+        lo, hi = int(cu[b]), int(cu[b + 1])
+        if hi == lo:   # an empty sequence hands its state on unchanged
+            assert torch.equal(S[b], d["S0"][b]) and torch.equal(z[b], d["z0"][b])
+            continue
+        sl = lambda x: x[lo:hi].permute(1, 0, 2)[None].contiguous()
+        ref = oracle_mod.scan(to_oracle(sl(d["q"])), to_oracle(sl(d["k"])), to_oracle(sl(d["v"])),
+                              alpha=to_oracle(d["alpha"][lo:hi].permute(1, 0)[None].contiguous())
+                              if d["alpha"] is not None else None,
+                              S0=to_oracle(d["S0"][b:b + 1]), z0=to_oracle(d["z0"][b:b + 1]), eps=1e-6)
+        g = (y[lo:hi].permute(1, 0, 2)[None].numpy(), S[b:b + 1].numpy(), z[b:b + 1].numpy())
+        for name, a, r in zip(("y", "S", "z"), g, ref):
+            assert_close(a, r, 2e-2, f"varlen seq {b} (T={hi - lo}) {name}")
+
+
+# long sequences among short and empty ones; the long ones span several 16-chunk
+# segments, with ragged ends
+MIXED = [5000, 0, 100, 2100, 64, 1, 3000, 17]
+
+
+@pytest.mark.parametrize("gated", [False, True])
+def test_varlen_segments_mixed(la, oracle_mod, gated):
+    d = _packed(MIXED, 2, 128, gated, seed=70 + gated)
+    got, status, plan = _run(la, d)
+    assert status == 0
+    _check_plan(plan, MIXED)
+    _check_seqs(oracle_mod, d, got)
+
+
+def test_varlen_segments_zero_gates(la, oracle_mod):
+    """Zero gates inside the long sequences: on the first token of a segment, on the
+    last one, and mid-segment; the maps of the parts before them must vanish."""
+    lens = [4200, 33, 2500]
+    d = _packed(lens, 2, 128, True, seed=73,
+                zero_gates=(1024, 2047, 3000, 4200 + 33 + 1500))
+    got, status, plan = _run(la, d)
+    assert status == 0
+    _check_plan(plan, lens)
+    _check_seqs(oracle_mod, d, got)
+
+
+def test_varlen_segments_in_place(la, oracle_mod):
+    """S0 and z0 are also S_out and z_out: the first segment of a split sequence must
+    not read a state that its last segment has already written."""
+    lens = [3100, 70, 0, 2600]
+    d = _packed(lens, 3, 128, True, seed=74)
+    got, status, plan = _run(la, d, in_place=True)
+    assert status == 0
+    _check_plan(plan, lens)
+    _check_seqs(oracle_mod, d, got)
+
+
+def test_varlen_segments_dv64(la, oracle_mod):
+    lens = [2900, 5, 1200, 640]
+    d = _packed(lens, 2, 64, True, seed=75)
+    got, status, plan = _run(la, d)
+    assert status == 0
+    _check_plan(plan, lens)
+    _check_seqs(oracle_mod, d, got)
+
+
+def test_varlen_segments_many_sequences(la, oracle_mod):
+    """More sequences than the plan kernel's 1024 threads: its prefix sums carry
+    across tiles.  Three long sequences, one in each tile and one at the end."""
+    rng = np.random.default_rng(76)
+    lens = [int(x) for x in rng.integers(0, 40, 1500)]
+    for i in (5, 1100, 1499):
+        lens[i] = 2300
+    d = _packed(lens, 1, 128, False, seed=76)
+    got, status, plan = _run(la, d)
+    assert status == 0
+    _check_plan(plan, lens)
+    _check_seqs(oracle_mod, d, got)
+
+
+def test_varlen_bad_lengths_disable_segments(la, oracle_mod):
+    """The last sequence runs past the total: nothing is split, the error is
+    recorded, and the other sequences (long ones included) are still exact."""
+    lens = [3000, 100, 2000, 500]
+    d = _packed(lens, 2, 128, False, seed=77)
+    d["cu"] = d["cu"].copy()
+    d["cu"][-1] += 5
+    got, status, plan = _run(la, d)
+    from recurrent_state_02_gb300 import _native
+    assert status == _native.LA_ERR_SHAPE
+    assert la.last_device_status() == 0
+    _check_plan(plan, lens, expect_split=False, invalid=(3,))
+    _check_seqs(oracle_mod, d, got, skip=(3,))
