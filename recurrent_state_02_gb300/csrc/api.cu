@@ -171,13 +171,16 @@ size_t seg_workspace_bytes(const SegPlan &p, int B, int H, int dv)
 // chunks once it has read the lengths, so min_seg bounds the boundaries by
 // total_T / (64 min_seg).  min_seg is a quarter of an SM's share of the largest
 // possible batch of CTA-chunks, which keeps (boundaries x CTAs per segment) below
-// 4 SMs' worth, and so the workspace, whatever the total.  Workspace (256-byte
-// aligned parts): seg_len int[2], seq_info int4[B], items int2[B + max_bds], bds
-// int2[max_bds], A and dS of the state pass's parts, and 2 max_bds start-state
-// slots (a split sequence has at most twice as many segments as boundaries).
+// 4 SMs' worth, and so the workspace, whatever the total.  The state pass gets
+// part_rows >= max_bds rows of CTAs; the plan shares about one wave of them
+// (part_target) among the boundaries it makes (more parts would shorten the
+// pass but lengthen the scan, which composes them one after another).  Workspace (256-byte aligned parts): seg_len int[3],
+// seq_info int4[B], items int2[B + max_bds], bds int2[part_rows], split_seqs
+// int[max_bds], A and dS of part_rows parts, and 2 max_bds start-state slots (a
+// split sequence has at most twice as many segments as boundaries).
 struct VarlenPlan {
-    int dvs = 64, units = 0, min_seg = 0, max_bds = 0, sub_per_seg = 1;
-    size_t off_info = 0, off_items = 0, off_bds = 0, off_A = 0, off_dS = 0, off_S = 0, bytes = 0;
+    int dvs = 64, units = 0, min_seg = 0, max_bds = 0, part_rows = 0, part_target = 0;
+    size_t off_info = 0, off_items = 0, off_bds = 0, off_split = 0, off_A = 0, off_dS = 0, off_S = 0, bytes = 0;
 };
 
 VarlenPlan varlen_plan(int B, int H, int total_T, int dv)
@@ -192,28 +195,21 @@ VarlenPlan varlen_plan(int B, int H, int total_T, int dv)
     if (L < kMinSegChunks) L = kMinSegChunks;
     const long long nb = (long long)total_T / (64 * L);
     if (nb < 1 || B + nb > 65535) return p;   // grid rows of the chunk kernel
-    // parts of the state pass over the nb full segments, as for the [B, H, T, d] layout
-    const long long slots = kStateCtasPerSm * sms;
-    long long best_cost = -1;
-    int best_n = 1;
-    for (int n = 1; n <= L && nb * n <= 65535 && nb * p.units * n <= 2 * slots; ++n) {
-        const long long waves = (nb * p.units * n + slots - 1) / slots;
-        const long long cost = waves * ((L + n - 1) / n + kStateCtaSetup);
-        if (best_cost < 0 || cost < best_cost) {
-            best_cost = cost;
-            best_n = n;
-        }
-    }
+    const long long wave = (kStateCtasPerSm * sms + p.units - 1) / p.units;
+    long long rows = wave < nb ? nb : wave;
+    if (rows > 65535) rows = 65535;
     p.min_seg = (int)L;
     p.max_bds = (int)nb;
-    p.sub_per_seg = best_n;
-    const size_t state = 128 * (size_t)dv + 128, nparts = (size_t)nb * best_n;
+    p.part_rows = (int)rows;
+    p.part_target = (int)(wave < rows ? wave : rows);
+    const size_t state = 128 * (size_t)dv + 128;
     p.off_info = 256;
     p.off_items = p.off_info + round_up(16 * (size_t)B, 256);
     p.off_bds = p.off_items + round_up(8 * ((size_t)B + nb), 256);
-    p.off_A = p.off_bds + round_up(8 * (size_t)nb, 256);
-    p.off_dS = p.off_A + round_up(4 * nparts * H, 256);
-    p.off_S = p.off_dS + round_up(4 * nparts * H * state, 256);
+    p.off_split = p.off_bds + round_up(8 * (size_t)rows, 256);
+    p.off_A = p.off_split + round_up(4 * (size_t)nb, 256);
+    p.off_dS = p.off_A + round_up(4 * (size_t)rows * H, 256);
+    p.off_S = p.off_dS + round_up(4 * (size_t)rows * H * state, 256);
     p.bytes = p.off_S + 4 * 2 * (size_t)nb * H * state;
     return p;
 }
@@ -532,11 +528,13 @@ la_status la_prefill_varlen(const void *q, const void *k, const void *v, la_dtyp
     int4 *seq_info = reinterpret_cast<int4 *>(ws + plan.off_info);
     int2 *items = reinterpret_cast<int2 *>(ws + plan.off_items);
     int2 *bds = reinterpret_cast<int2 *>(ws + plan.off_bds);
+    int *split_seqs = reinterpret_cast<int *>(ws + plan.off_split);
     float *A = reinterpret_cast<float *>(ws + plan.off_A);
     float *dS = reinterpret_cast<float *>(ws + plan.off_dS);
     float *S_start = reinterpret_cast<float *>(ws + plan.off_S);
     cudaError_t e = la::launch_varlen_plan(cu_seqlens, B, total_T, plan.min_seg, plan.units, sm_count(),
-                                           plan.max_bds, plan.sub_per_seg, seg_len, seq_info, items, bds, st);
+                                           plan.max_bds, plan.part_rows, plan.part_target, seg_len, seq_info, items,
+                                           bds, split_seqs, st);
     la::StateTcArgs sa;
     sa.alpha = alpha;
     sa.dS = dS;
@@ -545,7 +543,7 @@ la_status la_prefill_varlen(const void *q, const void *k, const void *v, la_dtyp
     sa.T = total_T;
     sa.dv = dv;
     sa.nsub = 0;
-    sa.sub_per_seg = plan.sub_per_seg;
+    sa.sub_per_seg = 1;   // the plan's parts per segment are in seg_len
     sa.sub_chunks = 0;
     sa.seg_chunks = 0;
     sa.cu_seqlens = cu_seqlens;
@@ -554,9 +552,9 @@ la_status la_prefill_varlen(const void *q, const void *k, const void *v, la_dtyp
     sa.status = status;
     sa.wait_limit_ns = la::kWaitLimitNs;
     if (e == cudaSuccess)
-        e = la::launch_state_tc(mk, mv, sa, B, alpha != nullptr, plan.dvs, st, false,
-                                plan.max_bds * plan.sub_per_seg);
-    if (e == cudaSuccess) e = la::launch_varlen_scan(S0, z0, A, dS, S_start, seq_info, B, H, dv, plan.sub_per_seg, st);
+        e = la::launch_state_tc(mk, mv, sa, B, alpha != nullptr, plan.dvs, st, false, plan.part_rows);
+    if (e == cudaSuccess)
+        e = la::launch_varlen_scan(S0, z0, A, dS, S_start, seq_info, split_seqs, seg_len, plan.max_bds, H, dv, st);
     if (e != cudaSuccess) return from_cuda(e);
     a.items = items;
     a.seq_info = seq_info;

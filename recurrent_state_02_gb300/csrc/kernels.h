@@ -107,11 +107,11 @@ struct StateTcArgs {
     const float *dd = nullptr;
     // Packed sequences (token-major maps, alpha [T, H]): bds[k] = (b, g) for the
     // varlen plan's boundary k, the full segment g of sequence b that ends there
-    // (b < 0: none); part j of it is CTA row k * sub_per_seg + j, and its outputs
-    // are row (k * sub_per_seg + j) * H + h of A and dS.
+    // (b < 0: none); part j of it is CTA row k * sub + j (sub = seg_len[2]), and
+    // its outputs are row (k * sub + j) * H + h of A and dS.
     const int *cu_seqlens = nullptr;
     const int2 *bds = nullptr;
-    const int *seg_len = nullptr;   // with bds: chunks per segment and per part (in place of seg_chunks, sub_chunks)
+    const int *seg_len = nullptr;   // with bds: chunks per segment, per part, parts per segment
     int *status;          // device status word
     unsigned long long wait_limit_ns;
 };
@@ -128,18 +128,21 @@ cudaError_t launch_state_tc(const CUtensorMap &map_k, const CUtensorMap &map_v, 
 // min_seg_chunks (from the batch's chunks, units CTAs per segment, sms SMs), and
 // sequence b of c_b chunks takes max(1, ceil(c_b / L)) segments; with bounds
 // outside [0, total_T] anywhere, or more than max_bds boundaries, one segment
-// each.  Writes seg_len [2] (L, chunks per part of sub_per_seg), seq_info [B],
-// items [B + max_bds] (longest segments first) and bds [max_bds] (see
-// PrefillTcArgs and StateTcArgs; unused entries b = -1).  One CTA.
+// each.  Writes seg_len [3] (L, chunks per part, parts per boundary's segment, so
+// that the boundaries fill about part_target of the part_rows >= max_bds rows),
+// seq_info [B], items
+// [B + max_bds] (longest segments first), bds [part_rows] and split_seqs
+// [max_bds] (see PrefillTcArgs and StateTcArgs; unused entries -1).  One CTA.
 cudaError_t launch_varlen_plan(const int *cu_seqlens, int B, int total_T, int min_seg_chunks, int units, int sms,
-                               int max_bds, int sub_per_seg, int *seg_len, int4 *seq_info, int2 *items, int2 *bds,
-                               cudaStream_t stream);
+                               int max_bds, int part_rows, int part_target, int *seg_len, int4 *seq_info,
+                               int2 *items, int2 *bds, int *split_seqs, cudaStream_t stream);
 
-// The varlen scan: for every sequence of more than one segment and head h,
-// S_start[slot + 0] = S0[b], z0[b] (zero if null), then S_start[slot + g] the
-// state after the maps of boundary (first + g - 1)'s sub_per_seg parts, in order.
+// The varlen scan: for every split sequence (split_seqs, max_bds entries) and head
+// h, S_start[slot + 0] = S0[b], z0[b] (zero if null), then S_start[slot + g] the
+// state after the maps of boundary (first + g - 1)'s parts, in order.
 cudaError_t launch_varlen_scan(const float *S0, const float *z0, const float *A, const float *dS, float *S_start,
-                               const int4 *seq_info, int B, int H, int dv, int sub_per_seg, cudaStream_t stream);
+                               const int4 *seq_info, const int *split_seqs, const int *seg_len, int max_bds, int H,
+                               int dv, cudaStream_t stream);
 
 // S_start[g][bh] (S then z) for g < nseg: S0/z0 (zero if null) carried through the
 // sub-segment maps S -> A S + dS in order.  rev: the maps of the reversed pass,

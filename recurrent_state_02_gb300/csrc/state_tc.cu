@@ -107,18 +107,19 @@ state_tc_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant
     Ctx cx{&sm->abort_flag, args.wait_limit_ns, args.status};
 
     // grid: (dv slice, h, b * nsub + m); sub-segment m is part j of output segment g.
-    // Packed sequences: (dv slice, h, k * sub_per_seg + j), part j of the segment
-    // that ends at the varlen plan's boundary k.
+    // Packed sequences: (dv slice, h, k * sub + j), part j of the segment that
+    // ends at the varlen plan's boundary k (sub parts per boundary, from the plan).
     const int slice = blockIdx.x, h = blockIdx.y;
     const bool varlen = args.bds != nullptr;
     int b, g, j, seq0 = 0, T = args.T, seg_chunks = args.seg_chunks, sub_chunks = args.sub_chunks;
     size_t orow;   // row of this part's outputs in A and dS
     if (varlen) {
-        const int2 e = args.bds[blockIdx.z / args.sub_per_seg];
+        const int sub = args.seg_len[2];
+        const int2 e = args.bds[blockIdx.z / sub];
         if (e.x < 0) return;   // beyond the plan's boundaries: no work
         b = e.x;
         g = e.y;
-        j = blockIdx.z % args.sub_per_seg;
+        j = blockIdx.z % sub;
         seq0 = args.cu_seqlens[b];
         T = args.cu_seqlens[b + 1] - seq0;
         seg_chunks = args.seg_len[0];
@@ -480,31 +481,44 @@ __device__ __forceinline__ int order_key(int c)
 // in sequence order; the items (every segment of every sequence) are written
 // longest first, so that the chunk kernel's CTAs start in that order and the
 // short ones fill in at the end (within a bucket of order_key, in no set order).
-// seg_len receives L and the chunks of each of a segment's sub_per_seg parts.
-__global__ void __launch_bounds__(1024)
+// The state pass has part_rows rows of CTAs: each boundary's segment is cut into
+// sub parts (of at least about 4 chunks) so that the boundaries fill part_target
+// of them (one wave of state CTAs), or one part each beyond that.
+// seg_len receives L, the chunks per part and sub; split_seqs the split
+// sequences (in no set order, then -1 up to max_bds).
+constexpr int kPlanCache = 4096;   // chunk counts of the first sequences, in shared memory
+__global__ void __launch_bounds__(1024, 1)
 varlen_plan_kernel(const int *__restrict__ cu, int B, int total_T, int L_min, int units, int sms, int max_bds,
-                   int sub_per_seg, int *__restrict__ seg_len, int4 *__restrict__ seq_info, int2 *__restrict__ items,
-                   int2 *__restrict__ bds)
+                   int part_rows, int part_target, int *__restrict__ seg_len, int4 *__restrict__ seq_info, int2 *__restrict__ items,
+                   int2 *__restrict__ bds, int *__restrict__ split_seqs)
 {
     __shared__ int warp_sums[32];
     __shared__ int tot[2];
     __shared__ unsigned long long acc[2];
     __shared__ int bucket[kOrderBuckets];
-    auto chunks = [&](int b, bool &bad) {
+    __shared__ int cached[kPlanCache];
+    __shared__ int n_split;
+    // chunks of sequence b (-1 when its bounds are bad)
+    auto read_chunks = [&](int b) {
         const int s0 = cu[b], s1 = cu[b + 1];
-        if (s0 < 0 || s1 < s0 || s1 > total_T) {
-            bad = true;
-            return 0;
-        }
-        return (s1 - s0 + kC - 1) / kC;
+        return (s0 < 0 || s1 < s0 || s1 > total_T) ? -1 : (s1 - s0 + kC - 1) / kC;
     };
-    if (threadIdx.x == 0) acc[0] = acc[1] = 0;
+    auto chunks = [&](int b) { return max(0, b < kPlanCache ? cached[b] : read_chunks(b)); };
+    if (threadIdx.x == 0) {
+        acc[0] = acc[1] = 0;
+        n_split = 0;
+    }
     for (int i = threadIdx.x; i < kOrderBuckets; i += blockDim.x) bucket[i] = 0;
     __syncthreads();
     // pass 1: the batch's chunks, and whether every sequence is valid
     unsigned long long sum = 0;
     bool bad = false;
-    for (int b = threadIdx.x; b < B; b += blockDim.x) sum += chunks(b, bad);
+    for (int b = threadIdx.x; b < B; b += blockDim.x) {
+        const int c = read_chunks(b);
+        if (b < kPlanCache) cached[b] = c;
+        bad = bad || c < 0;
+        sum += max(c, 0);
+    }
     atomicAdd(&acc[0], sum);
     const bool any_bad = __syncthreads_or(bad) != 0;
     const unsigned long long share = (acc[0] * (unsigned long long)units + sms - 1) / (unsigned long long)sms;
@@ -512,35 +526,25 @@ varlen_plan_kernel(const int *__restrict__ cu, int B, int total_T, int L_min, in
     // pass 2: the boundaries this L takes
     unsigned long long count = 0;
     for (int b = threadIdx.x; b < B; b += blockDim.x) {
-        bool dummy = false;
-        const int c = chunks(b, dummy);
+        const int c = chunks(b);
         count += c > L ? (c + L - 1) / L - 1 : 0;
     }
     atomicAdd(&acc[1], count);
     __syncthreads();
     const bool split = !any_bad && acc[1] <= (unsigned long long)max_bds;
-    if (threadIdx.x == 0) {
-        seg_len[0] = L;
-        seg_len[1] = (L + sub_per_seg - 1) / sub_per_seg;
-    }
-    // the segments of sequence b: nseg, and the chunks of the last one (the others have L)
-    auto segments = [&](int b, int &last) {
-        bool dummy = false;
-        const int c = chunks(b, dummy);
-        if (!split || c <= L) {
-            last = c;
-            return 1;
-        }
+    const int n_bd = split ? (int)acc[1] : 0;
+    // the segments of sequence b (x), and the chunks of the last one (y; the others have L)
+    auto segments = [&](int b) {
+        const int c = chunks(b);
+        if (!split || c <= L) return make_int2(1, c);
         const int n = (c + L - 1) / L;
-        last = c - (n - 1) * L;
-        return n;
+        return make_int2(n, c - (n - 1) * L);
     };
     // pass 3: how many items fall in each bucket of the order
     for (int b = threadIdx.x; b < B; b += blockDim.x) {
-        int last;
-        const int n = segments(b, last);
-        if (n > 1) atomicAdd(&bucket[order_key(L)], n - 1);
-        atomicAdd(&bucket[order_key(last)], 1);
+        const int2 sg = segments(b);
+        if (sg.x > 1) atomicAdd(&bucket[order_key(L)], sg.x - 1);
+        atomicAdd(&bucket[order_key(sg.y)], 1);
     }
     __syncthreads();
     // exclusive prefix over the buckets: their first rows in the item table
@@ -554,8 +558,8 @@ varlen_plan_kernel(const int *__restrict__ cu, int B, int total_T, int L_min, in
     int carry_bd = 0, carry_slot = 0;
     for (int b0 = 0; b0 < B; b0 += blockDim.x) {
         const int b = b0 + threadIdx.x;
-        int last = 0;
-        const int nseg = b < B ? segments(b, last) : 1;
+        const int2 sg = b < B ? segments(b) : make_int2(1, 0);
+        const int nseg = sg.x, last = sg.y;
         const int nbd = nseg - 1, nslot = nseg > 1 ? nseg : 0;
         const int bd0 = carry_bd + block_excl_scan(nbd, warp_sums, &tot[0]);
         const int tile_bd = tot[0];
@@ -566,56 +570,91 @@ varlen_plan_kernel(const int *__restrict__ cu, int B, int total_T, int L_min, in
             for (int g = 0; g < nseg; ++g)
                 items[atomicAdd(&bucket[order_key(g + 1 < nseg ? L : last)], 1)] = make_int2(b, g);
             for (int g = 0; g + 1 < nseg; ++g) bds[bd0 + g] = make_int2(b, g);
+            if (nseg > 1) split_seqs[atomicAdd(&n_split, 1)] = b;
         }
         carry_bd += tile_bd;
         carry_slot += tile_slot;
         __syncthreads();   // tot is rewritten by the next tile
     }
-    // pass 5: the rows past the plan's items and boundaries do nothing
+    // the parts of a boundary's segment: as many as the rows allow, of >= ~4 chunks
+    if (threadIdx.x == 0) {
+        int sub = n_bd ? min(part_rows, part_target) / n_bd : 1;
+        sub = max(1, min(sub, (L + 3) / 4));
+        const int sub_chunks = (L + sub - 1) / sub;
+        seg_len[0] = L;
+        seg_len[1] = sub_chunks;
+        seg_len[2] = (L + sub_chunks - 1) / sub_chunks;
+    }
+    // pass 5: the rows past the plan's items, boundaries and split sequences do nothing
     for (int i = B + carry_bd + threadIdx.x; i < B + max_bds; i += blockDim.x) items[i] = make_int2(-1, 0);
-    for (int k = carry_bd + threadIdx.x; k < max_bds; k += blockDim.x) bds[k] = make_int2(-1, 0);
+    for (int k = carry_bd + threadIdx.x; k < part_rows; k += blockDim.x) bds[k] = make_int2(-1, 0);
+    for (int i = n_split + threadIdx.x; i < max_bds; i += blockDim.x) split_seqs[i] = -1;
 }
 
 // The start state of every segment of every split sequence: slot 0 holds S0, z0;
 // slot g the state after the maps of the parts that end at boundary first + g - 1
-// (S -> A S + dS, in order).  One thread per 4 consecutive state elements of a
-// head; a thread issues the loads of up to 8 parts before it applies them.
-__global__ void varlen_scan_kernel(const float *S0, const float *z0, const float *A, const float *dS, float *S_start,
-                                   const int4 *__restrict__ seq_info, int H, int dv, int sub_per_seg)
+// (S -> A S + dS, in order; sub parts per boundary).  A block takes one head of
+// one split sequence and 512 consecutive float4 of its state; each thread holds
+// 2 of them and has the loads of 8 parts in flight at a time.
+constexpr int kScanVec = 2, kScanParts = 8;
+__global__ void __launch_bounds__(256)
+varlen_scan_kernel(const float *S0, const float *z0, const float *__restrict__ A, const float *__restrict__ dS,
+                   float *__restrict__ S_start,
+                   const int4 *__restrict__ seq_info, const int *__restrict__ split_seqs,
+                   const int *__restrict__ seg_len, int H, int dv)
 {
-    const int b = blockIdx.x / H, h = blockIdx.x % H, bh = blockIdx.x;
+    const int b = split_seqs[blockIdx.x / H], h = blockIdx.x % H;
+    if (b < 0) return;
     const int4 si = seq_info[b];
-    if (si.x <= 1) return;
-    const int e = 4 * (blockIdx.y * blockDim.x + threadIdx.x);
+    const int sub = seg_len[2];
+    const int bh = b * H + h;
     const int s_len = kR * dv;
     const int state_len = s_len + kR;
-    if (e >= state_len) return;
-    const float *src0 = e < s_len ? (S0 ? S0 + (size_t)bh * s_len + e : nullptr)
-                                  : (z0 ? z0 + (size_t)bh * kR + (e - s_len) : nullptr);
-    float4 s = src0 ? make_float4(src0[0], src0[1], src0[2], src0[3]) : make_float4(0.f, 0.f, 0.f, 0.f);
-    *reinterpret_cast<float4 *>(S_start + ((size_t)si.y * H + h) * state_len + e) = s;
-    const int nparts = (si.x - 1) * sub_per_seg;
-    const size_t part0 = (size_t)si.z * sub_per_seg;
-    for (int i0 = 0; i0 < nparts; i0 += 8) {
-        float4 d[8];
-        float a[8];
+    int e[kScanVec];
+    float4 s[kScanVec];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            const size_t row = (part0 + i0 + i) * H + h;
-            d[i] = i0 + i < nparts ? *reinterpret_cast<const float4 *>(dS + row * state_len + e)
-                                   : make_float4(0.f, 0.f, 0.f, 0.f);
-            a[i] = i0 + i < nparts ? A[row] : 1.f;
+    for (int q = 0; q < kScanVec; ++q) {
+        e[q] = 4 * ((blockIdx.y * kScanVec + q) * blockDim.x + threadIdx.x);
+        s[q] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (e[q] < state_len) {
+            // S0 and z0 are 4-byte aligned; the workspace parts are 16-byte aligned
+            const float *src0 = e[q] < s_len ? (S0 ? S0 + (size_t)bh * s_len + e[q] : nullptr)
+                                             : (z0 ? z0 + (size_t)bh * kR + (e[q] - s_len) : nullptr);
+            if (src0) s[q] = make_float4(src0[0], src0[1], src0[2], src0[3]);
+            *reinterpret_cast<float4 *>(S_start + ((size_t)si.y * H + h) * state_len + e[q]) = s[q];
+        }
+    }
+    const int nparts = (si.x - 1) * sub;
+    const size_t part0 = (size_t)si.z * sub;
+    for (int p0 = 0; p0 < nparts; p0 += kScanParts) {
+        float4 d[kScanParts][kScanVec];
+        float a[kScanParts];
+#pragma unroll
+        for (int i = 0; i < kScanParts; ++i) {
+            const size_t row = (part0 + p0 + i) * H + h;
+            const bool ok = p0 + i < nparts;
+            a[i] = ok ? A[row] : 1.f;
+#pragma unroll
+            for (int q = 0; q < kScanVec; ++q)
+                d[i][q] = (ok && e[q] < state_len) ? *reinterpret_cast<const float4 *>(dS + row * state_len + e[q])
+                                                   : make_float4(0.f, 0.f, 0.f, 0.f);
         }
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            if (i0 + i >= nparts) break;
-            s.x = fmaf(a[i], s.x, d[i].x);
-            s.y = fmaf(a[i], s.y, d[i].y);
-            s.z = fmaf(a[i], s.z, d[i].z);
-            s.w = fmaf(a[i], s.w, d[i].w);
-            if ((i0 + i + 1) % sub_per_seg == 0) {
-                const int g = (i0 + i + 1) / sub_per_seg;
-                *reinterpret_cast<float4 *>(S_start + ((size_t)(si.y + g) * H + h) * state_len + e) = s;
+        for (int i = 0; i < kScanParts; ++i) {
+            if (p0 + i >= nparts) break;
+#pragma unroll
+            for (int q = 0; q < kScanVec; ++q) {
+                s[q].x = fmaf(a[i], s[q].x, d[i][q].x);
+                s[q].y = fmaf(a[i], s[q].y, d[i][q].y);
+                s[q].z = fmaf(a[i], s[q].z, d[i][q].z);
+                s[q].w = fmaf(a[i], s[q].w, d[i][q].w);
+            }
+            if ((p0 + i + 1) % sub == 0) {
+                const int g = (p0 + i + 1) / sub;
+#pragma unroll
+                for (int q = 0; q < kScanVec; ++q)
+                    if (e[q] < state_len)
+                        *reinterpret_cast<float4 *>(S_start + ((size_t)(si.y + g) * H + h) * state_len + e[q]) = s[q];
             }
         }
     }
@@ -624,23 +663,25 @@ __global__ void varlen_scan_kernel(const float *S0, const float *z0, const float
 }  // namespace
 
 cudaError_t launch_varlen_plan(const int *cu_seqlens, int B, int total_T, int min_seg_chunks, int units, int sms,
-                               int max_bds, int sub_per_seg, int *seg_len, int4 *seq_info, int2 *items, int2 *bds,
-                               cudaStream_t stream)
+                               int max_bds, int part_rows, int part_target, int *seg_len, int4 *seq_info, int2 *items,
+                               int2 *bds, int *split_seqs, cudaStream_t stream)
 {
-    if (B < 1 || min_seg_chunks < 1 || units < 1 || sms < 1 || max_bds < 0 || total_T < 0 || sub_per_seg < 1)
+    if (B < 1 || min_seg_chunks < 1 || units < 1 || sms < 1 || max_bds < 1 || total_T < 0 || part_rows < max_bds ||
+        part_target < 1)
         return cudaErrorInvalidValue;
     varlen_plan_kernel<<<1, 1024, 0, stream>>>(cu_seqlens, B, total_T, min_seg_chunks, units, sms, max_bds,
-                                                sub_per_seg, seg_len, seq_info, items, bds);
+                                                part_rows, part_target, seg_len, seq_info, items, bds, split_seqs);
     return cudaGetLastError();
 }
 
 cudaError_t launch_varlen_scan(const float *S0, const float *z0, const float *A, const float *dS, float *S_start,
-                               const int4 *seq_info, int B, int H, int dv, int sub_per_seg, cudaStream_t stream)
+                               const int4 *seq_info, const int *split_seqs, const int *seg_len, int max_bds, int H,
+                               int dv, cudaStream_t stream)
 {
-    if (B < 1 || H < 1 || sub_per_seg < 1 || (long long)B * H > 0x7fffffffLL) return cudaErrorInvalidValue;
-    const int state_len = kR * dv + kR;
-    const dim3 grid(B * H, (state_len / 4 + 255) / 256);
-    varlen_scan_kernel<<<grid, 256, 0, stream>>>(S0, z0, A, dS, S_start, seq_info, H, dv, sub_per_seg);
+    if (max_bds < 1 || H < 1 || (long long)max_bds * H > 0x7fffffffLL) return cudaErrorInvalidValue;
+    const int n4 = (kR * dv + kR) / 4;
+    const dim3 grid(max_bds * H, (n4 + 256 * kScanVec - 1) / (256 * kScanVec));
+    varlen_scan_kernel<<<grid, 256, 0, stream>>>(S0, z0, A, dS, S_start, seq_info, split_seqs, seg_len, H, dv);
     return cudaGetLastError();
 }
 
@@ -648,7 +689,7 @@ cudaError_t launch_state_tc(const CUtensorMap &map_k, const CUtensorMap &map_v, 
                             bool gated, int dvs, cudaStream_t stream, bool rev, int grid_z)
 {
     if ((dvs != 64 && dvs != 128) || (rev && (dvs != 128 || !a.d || !a.dd))) return cudaErrorInvalidValue;
-    if (a.bds && (rev || grid_z < 1 || !a.cu_seqlens || !a.seg_len || a.sub_per_seg < 1)) return cudaErrorInvalidValue;
+    if (a.bds && (rev || grid_z < 1 || !a.cu_seqlens || !a.seg_len)) return cudaErrorInvalidValue;
     const dim3 grid(a.dv / dvs, a.H, a.bds ? grid_z : B * a.nsub);
     using KernFn = void (*)(const CUtensorMap, const CUtensorMap, const StateTcArgs);
     const int v = rev ? 4 + (gated ? 1 : 0) : (gated ? 1 : 0) + (dvs == 128 ? 2 : 0);
