@@ -457,6 +457,15 @@ __device__ __forceinline__ int block_excl_scan(int v, int *warp_sums, int *sum)
     return before;
 }
 
+// Sum over a warp, then one shared atomic per warp (1024 threads adding to one
+// word one by one would serialise).
+__device__ __forceinline__ void block_add(unsigned long long v, unsigned long long *dst)
+{
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    if ((threadIdx.x & 31) == 0 && v) atomicAdd(dst, v);
+}
+
 // Bucket of an item of c chunks in the longest-first order: c itself below 64,
 // then 8 buckets per octave; larger items get smaller keys.
 constexpr int kOrderBuckets = 64 + 8 * 26;
@@ -519,7 +528,7 @@ varlen_plan_kernel(const int *__restrict__ cu, int B, int total_T, int L_min, in
         bad = bad || c < 0;
         sum += max(c, 0);
     }
-    atomicAdd(&acc[0], sum);
+    block_add(sum, &acc[0]);
     const bool any_bad = __syncthreads_or(bad) != 0;
     const unsigned long long share = (acc[0] * (unsigned long long)units + sms - 1) / (unsigned long long)sms;
     const int L = (int)max((unsigned long long)L_min, min(share, (unsigned long long)0x3fffffff));
@@ -529,7 +538,7 @@ varlen_plan_kernel(const int *__restrict__ cu, int B, int total_T, int L_min, in
         const int c = chunks(b);
         count += c > L ? (c + L - 1) / L - 1 : 0;
     }
-    atomicAdd(&acc[1], count);
+    block_add(count, &acc[1]);
     __syncthreads();
     const bool split = !any_bad && acc[1] <= (unsigned long long)max_bds;
     const int n_bd = split ? (int)acc[1] : 0;
