@@ -289,7 +289,8 @@ delta_t_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant_
                     make_uint4(0, 0, 0, 0);
         }
         // M = G10 T00 and then T10 = -T11 M: thread (warp, lane) computes rows
-        // 4 rg .. 4 rg + 3 and columns 2 cp, 2 cp + 1, rg = 2 warp + lane / 16
+        // 4 rg .. 4 rg + 3 and columns 2 cp, 2 cp + 1, rg = 2 warp + lane / 16 (the
+        // two columns as one packed FP32 pair, each rounded as fmaf would)
         const int rg = 2 * warp + (lane >> 4), cp = lane & 15;
         {
             float2 m4[4] = {};
@@ -299,10 +300,7 @@ delta_t_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant_
                 const float4 g = *reinterpret_cast<const float4 *>(Lt + u * LD + 32 + 4 * rg);
                 const float gv[4] = {g.x, g.y, g.z, g.w};
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    m4[e].x = fmaf(gv[e], tj.x, m4[e].x);
-                    m4[e].y = fmaf(gv[e], tj.y, m4[e].y);
-                }
+                for (int e = 0; e < 4; ++e) m4[e] = __ffma2_rn(make_float2(gv[e], gv[e]), tj, m4[e]);
             }
 #pragma unroll
             for (int e = 0; e < 4; ++e) *reinterpret_cast<float2 *>(Mf + (4 * rg + e) * LDT + 2 * cp) = m4[e];
@@ -316,10 +314,7 @@ delta_t_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant_
                 const float4 a = *reinterpret_cast<const float4 *>(T11t + u * LDT + 4 * rg);
                 const float av[4] = {a.x, a.y, a.z, a.w};
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    o4[e].x = fmaf(av[e], mj.x, o4[e].x);
-                    o4[e].y = fmaf(av[e], mj.y, o4[e].y);
-                }
+                for (int e = 0; e < 4; ++e) o4[e] = __ffma2_rn(make_float2(av[e], av[e]), mj, o4[e]);
             }
 #pragma unroll
             for (int e = 0; e < 4; ++e)
