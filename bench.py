@@ -655,7 +655,9 @@ def run_ours(args, rank, world, local_rank):
                 "longest": max(vw.lens), "launches_per_call": 4 if nvws else 1,
                 "roofline": {"bound": "hbm", "achieved": v_gbs, "peak": peak, "unit": "GB/s", "frac": v_gbs / peak,
                              "peak_kind": peak_kind, "algorithmic_bytes_per_launch": vbytes,
-                             "timed": "the whole call"}}
+                             "timed": "the whole call", "kernel": "prefill_tc_kernel<false, 128> items",
+                             "traffic": profile_traffic("prefill_tc_kernel<false, 128> items",
+                                                        f"B{nvb} H{vw.H} T{vw.T}", kernel_sources("prefill_tc.cu"))}}
             del vin, yv, Sv, zv, vws, gv
         torch.cuda.empty_cache()
 
