@@ -551,7 +551,7 @@ def run_ours(args, rank, world, local_rank):
         cbytes = short_bytes(cw.B, cw.H, cw.T, cw.r, cw.dv, cw.gated)
         c_gbs = cbytes / c_launch / 1e9
         decode["short_continuation"] = {
-            "workload": cw.name, "entry": "la_prefill_chunked (T <= 16: the state-resident token walk)",
+            "workload": cw.name, "entry": "la_prefill_chunked (T <= 32: the state-resident token walk)",
             "launch_us": c_launch * 1e6, "tokens_per_s": cw.B * cw.T * world / c_launch,
             "token_heads_per_s": cw.B * cw.H * cw.T * world / c_launch,
             "roofline": {"bound": "hbm", "achieved": c_gbs, "peak": peak, "unit": "GB/s", "frac": c_gbs / peak,

@@ -53,7 +53,7 @@ EncodeTiledFn encode_fn()
 #endif
 // Continuations of at most this many tokens take the decode-shaped token walk.
 #ifndef LA_DECODE_MAX_T
-#define LA_DECODE_MAX_T 16
+#define LA_DECODE_MAX_T 32
 #endif
 constexpr int kMinSegChunks = 16;    // at least 1024 tokens per segment
 constexpr int kStateCtasPerSm = 2;   // resident state-pass CTAs per SM
@@ -357,7 +357,7 @@ static la_status prefill_chunked_impl(const void *q, const void *k, const void *
     // once, where the chunk kernel's set-up for a single partial chunk would
     // dominate.  It computes the same recurrence in FP32 (phi in FP32 from the
     // inputs; no BF16 operands).
-    if (T <= LA_DECODE_MAX_T && T <= 16 && dv == 128 && (!S0 || aligned(S0, 16)))
+    if (T <= LA_DECODE_MAX_T && T <= 32 && dv == 128 && (!S0 || aligned(S0, 16)))
         return from_cuda(la::launch_decode_multi(q, k, v, true, alpha, S0, z0, S_out, z_out, B, H, T, eps, y, d_out,
                                                  st));
     const SegPlan plan = seg_plan(B, H, T, dv);

@@ -153,16 +153,23 @@ decode128_kernel(const void *__restrict__ q, const void *__restrict__ k, const v
 // barrier (the numerator's per-warp parts are double-buffered).  S0 and z0 are
 // read whole before anything is written, so they may alias S_out and z_out.
 // d_out (or nullptr) receives the denominators.
-constexpr int kMultiMaxT = 16;
-template <bool BF16>
+// The tokens' phi(q), phi(k) (FP32) and v live in 48 KB of dynamic shared memory
+// laid out for 32 tokens whatever T (fixed offsets; registers already hold the
+// kernel to 2 CTAs per SM); they are loaded in halves of 16 tokens, so that the raw
+// loads held in registers stay those of 16.
+constexpr int kMultiMaxT = 32, kMultiHalf = 16;
+constexpr uint32_t kMultiTokenBytes = 128 * 4 * 3;
+template <bool BF16, int HALVES>
 __global__ void __launch_bounds__(256, 2)
 decode128_multi_kernel(const void *__restrict__ q, const void *__restrict__ k, const void *__restrict__ v,
                        const float *__restrict__ alpha, const float *S0, const float *z0, float *S_out,
                        float *z_out, int T, float eps, void *__restrict__ y, float *__restrict__ d_out)
 {
     constexpr int R = 128, DV = 128;
-    __shared__ float qf[kMultiMaxT][R], kf[kMultiMaxT][R];
-    __shared__ float4 vs[kMultiMaxT][DV / 4];
+    extern __shared__ float4 multi_smem[];
+    float(*qf)[R] = reinterpret_cast<float(*)[R]>(multi_smem);
+    float(*kf)[R] = reinterpret_cast<float(*)[R]>(multi_smem + kMultiMaxT * (R / 4));
+    float4(*vs)[DV / 4] = reinterpret_cast<float4(*)[DV / 4]>(multi_smem + 2 * kMultiMaxT * (R / 4));
     __shared__ float al[kMultiMaxT];
     __shared__ float4 num_part[2][8][32];
     __shared__ float den_part[2][4];
@@ -181,32 +188,36 @@ decode128_multi_kernel(const void *__restrict__ q, const void *__restrict__ k, c
     }
     float zr = (tid < R && z0) ? z0[(size_t)bh * R + tid] : 0.f;
     // the T tokens of this head are contiguous rows: 4 elements per load, all of a
-    // thread's loads issued before any is used
+    // thread's loads of a half issued before any is used
     const size_t tok0 = (size_t)bh * T;
-    constexpr int kLoads = kMultiMaxT * R / 4 / 256;   // per thread and tensor
-    const int nvec = T * R / 4;
+    constexpr int kLoads = kMultiHalf * R / 4 / 256;   // per thread, tensor and half
     using Raw = typename Quad<BF16>::raw;   // the loads stay raw until they are stored
-    Raw rq[kLoads], rk[kLoads], rv[kLoads];
-#pragma unroll
-    for (int it = 0; it < kLoads; ++it) {
-        const int e = tid + it * 256;
-        if (e < nvec) {
-            rq[it] = Quad<BF16>::load(q, tok0 * R + 4 * (size_t)e);
-            rk[it] = Quad<BF16>::load(k, tok0 * R + 4 * (size_t)e);
-            rv[it] = Quad<BF16>::load(v, tok0 * DV + 4 * (size_t)e);
-        }
-    }
     const float a_t = (tid < T && alpha) ? alpha[tok0 + tid] : 1.f;
 #pragma unroll
-    for (int it = 0; it < kLoads; ++it) {
-        const int e = tid + it * 256;
-        if (e < nvec) {
-            const float4 fq = Quad<BF16>::widen(rq[it]), fk = Quad<BF16>::widen(rk[it]);
-            reinterpret_cast<float4 *>(&qf[0][0])[e] =
-                make_float4(phi_exact(fq.x), phi_exact(fq.y), phi_exact(fq.z), phi_exact(fq.w));
-            reinterpret_cast<float4 *>(&kf[0][0])[e] =
-                make_float4(phi_exact(fk.x), phi_exact(fk.y), phi_exact(fk.z), phi_exact(fk.w));
-            reinterpret_cast<float4 *>(&vs[0][0])[e] = Quad<BF16>::widen(rv[it]);
+    for (int hv = 0; hv < HALVES; ++hv) {
+        const int h0 = hv * kMultiHalf;
+        const int nvec = min(kMultiHalf, T - h0) * R / 4, v0 = h0 * R / 4;
+        Raw rq[kLoads], rk[kLoads], rv[kLoads];
+#pragma unroll
+        for (int it = 0; it < kLoads; ++it) {
+            const int e = tid + it * 256;
+            if (e < nvec) {
+                rq[it] = Quad<BF16>::load(q, tok0 * R + 4 * (size_t)(v0 + e));
+                rk[it] = Quad<BF16>::load(k, tok0 * R + 4 * (size_t)(v0 + e));
+                rv[it] = Quad<BF16>::load(v, tok0 * DV + 4 * (size_t)(v0 + e));
+            }
+        }
+#pragma unroll
+        for (int it = 0; it < kLoads; ++it) {
+            const int e = tid + it * 256;
+            if (e < nvec) {
+                const float4 fq = Quad<BF16>::widen(rq[it]), fk = Quad<BF16>::widen(rk[it]);
+                reinterpret_cast<float4 *>(&qf[0][0])[v0 + e] =
+                    make_float4(phi_exact(fq.x), phi_exact(fq.y), phi_exact(fq.z), phi_exact(fq.w));
+                reinterpret_cast<float4 *>(&kf[0][0])[v0 + e] =
+                    make_float4(phi_exact(fk.x), phi_exact(fk.y), phi_exact(fk.z), phi_exact(fk.w));
+                reinterpret_cast<float4 *>(&vs[0][0])[v0 + e] = Quad<BF16>::widen(rv[it]);
+            }
         }
     }
     if (tid < T) al[tid] = a_t;
@@ -346,12 +357,19 @@ cudaError_t launch_decode_multi(const void *q, const void *k, const void *v, boo
 {
     const long long nbh = (long long)B * H;
     if (nbh < 1 || nbh > 0x7fffffffLL || T < 1 || T > kMultiMaxT) return cudaErrorInvalidValue;
-    if (bf16)
-        decode128_multi_kernel<true><<<(unsigned)nbh, 256, 0, stream>>>(q, k, v, alpha, S0, z0, S_out, z_out, T, eps,
-                                                                         y, d_out);
-    else
-        decode128_multi_kernel<false><<<(unsigned)nbh, 256, 0, stream>>>(q, k, v, alpha, S0, z0, S_out, z_out, T,
-                                                                          eps, y, d_out);
+    // the limit is raised once (the first call on a device must not be inside a
+    // stream capture)
+    // one half of 16 tokens or two
+    using Kern = void (*)(const void *, const void *, const void *, const float *, const float *, const float *,
+                          float *, float *, int, float, void *, float *);
+    static const Kern kerns[4] = {decode128_multi_kernel<false, 1>, decode128_multi_kernel<false, 2>,
+                                  decode128_multi_kernel<true, 1>, decode128_multi_kernel<true, 2>};
+    static OncePerDevice attr_set[4];
+    const int ki = (bf16 ? 2 : 0) + (T > kMultiHalf ? 1 : 0);
+    const uint32_t bytes = kMultiMaxT * kMultiTokenBytes;
+    const cudaError_t e = set_smem_once(kerns[ki], bytes, attr_set[ki]);
+    if (e != cudaSuccess) return e;
+    kerns[ki]<<<(unsigned)nbh, 256, bytes, stream>>>(q, k, v, alpha, S0, z0, S_out, z_out, T, eps, y, d_out);
     return cudaGetLastError();
 }
 

@@ -388,8 +388,9 @@ def test_prefill_varlen_bad_lengths(la, oracle_mod):
 
 
 # ------------------------------------------------------ short continuations
-# A BF16 call of at most 16 tokens at r = dv = 128 takes the decode-shaped token
-# walk (the state stays in registers for the whole run; FP32 arithmetic).
+# A BF16 call of at most 32 tokens at r = dv = 128 takes the decode-shaped token
+# walk (the state stays in registers for the whole run; FP32 arithmetic; the
+# tokens are staged in halves of 16).
 SHORT_CASES = [
     # B, H, T, gated, with_state
     (3, 5, 1, False, True),
@@ -397,6 +398,11 @@ SHORT_CASES = [
     (4, 2, 7, True, False),
     (2, 4, 16, False, False),
     (1, 6, 16, True, True),
+    (2, 3, 17, True, True),     # one token into the second half
+    (3, 2, 24, False, True),
+    (2, 2, 32, True, False),    # the most the walk takes
+    (1, 3, 32, False, True),
+    (2, 2, 33, True, True),     # one more: the chunk kernel
 ]
 
 
@@ -408,14 +414,14 @@ def test_prefill_short_continuation(la, oracle_mod, B, H, T, gated, with_state):
 
 
 def test_prefill_short_continuation_in_place_chain(la, oracle_mod):
-    """Prefill 100 tokens, then three continuations of 1, 5 and 16 tokens in place
-    (S0 = S_out), against one oracle pass over all 122 tokens."""
-    inp = _inputs(torch.bfloat16, 2, 3, 122, 128, 128, gated=True, with_state=True, seed=77)
+    """Prefill 100 tokens, then continuations of 1, 5, 16 and 29 tokens in place
+    (S0 = S_out), against one oracle pass over all 151 tokens."""
+    inp = _inputs(torch.bfloat16, 2, 3, 151, 128, 128, gated=True, with_state=True, seed=77)
     ref = _oracle_prefill(oracle_mod, inp)
     d = {k: (v.cuda() if v is not None else None) for k, v in inp.items()}
     S, z = d["S0"].clone(), d["z0"].clone()
     ys = []
-    for a, b in ((0, 100), (100, 101), (101, 106), (106, 122)):
+    for a, b in ((0, 100), (100, 101), (101, 106), (106, 122), (122, 151)):
         part = {n: (d[n][:, :, a:b].contiguous() if d[n] is not None else None) for n in ("q", "k", "v", "alpha")}
         y, _, _ = la.prefill_chunked(part["q"], part["k"], part["v"], alpha=part["alpha"], S0=S, z0=z,
                                      S_out=S, z_out=z)
