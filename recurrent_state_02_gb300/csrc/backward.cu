@@ -744,15 +744,85 @@ cudaError_t launch_rec(const RecArgs &a, int B, int L, cudaStream_t stream)
     }
 }
 
+// A second stream and four events per host thread and device, for the state
+// passes that run beside the main chain of the backward (so that calls from
+// several host threads never share them, and a stream capture on one thread never
+// takes in another's work).  Made on the first call on a device, which must not
+// be inside a stream capture; nullptr if they cannot be made (everything then
+// runs on the caller's stream).
+struct SideLane {
+    cudaStream_t stream = nullptr;
+    cudaEvent_t ev[4] = {};
+    bool failed = false;
+};
+
+SideLane *side_lane()
+{
+    thread_local SideLane lanes[kMaxDevices];
+    const int dev = current_device_index();
+    if (dev < 0) return nullptr;
+    SideLane &l = lanes[dev];
+    if (!l.stream && !l.failed) {
+        bool ok = cudaStreamCreateWithFlags(&l.stream, cudaStreamNonBlocking) == cudaSuccess;
+        for (int i = 0; ok && i < 4; ++i) ok = cudaEventCreateWithFlags(&l.ev[i], cudaEventDisableTiming) == cudaSuccess;
+        if (!ok) {
+            for (cudaEvent_t &ev : l.ev)
+                if (ev) cudaEventDestroy(ev), ev = nullptr;
+            if (l.stream) cudaStreamDestroy(l.stream);
+            l.stream = nullptr;
+            l.failed = true;
+            cudaGetLastError();   // the failure is not the caller's: clear it
+        }
+    }
+    return l.stream ? &l : nullptr;
+}
+
 template <typename Tin>
 cudaError_t launch_bwd_t(const BackwardArgs &a, int B, cudaStream_t stream)
 {
     const int BH = B * a.H;
     const size_t n = (size_t)BH * a.T;
     float *d = a.ws, *dd = d + n, *tok_sum = dd + n, *fin = tok_sum + n;
+    cudaError_t e;
+    // With the tensor-core sweeps over sequence segments, the state passes and
+    // their scans go on a side stream: the forward pass (k, v only) beside the z
+    // pass and d_t; the reversed pass (which needs d_t) beside the dq sweep.
+    const bool segmented = sizeof(Tin) == 2 && a.maps && a.nseg > 1;
+    SideLane *side = segmented ? side_lane() : nullptr;
+    const cudaStream_t ss = side ? side->stream : stream;
+    if (side) {   // the side work comes after everything the caller enqueued before
+        if ((e = cudaEventRecord(side->ev[0], stream)) != cudaSuccess) return e;
+        if ((e = cudaStreamWaitEvent(ss, side->ev[0], 0)) != cudaSuccess) return e;
+    }
+    const size_t state = (size_t)128 * 128 + 128;
+    const size_t a_floats = ((size_t)a.nsub * BH * 4 + 255) / 256 * 64;
+    const size_t pass_floats = a_floats + (size_t)a.nsub * BH * state + (size_t)a.nseg * BH * state;
+    StateTcArgs sa;
+    const float *Sf = a.states_in;
+    if (segmented) {
+        // the states entering each segment: the prefill's state pass and scan in
+        // forward time (for dq), and (below) their reversed form over (phi(q), dn,
+        // dd) from dS_T, dz_T (for dk and dv); each pass's workspace is A
+        // [nsub][BH] (256-byte aligned), the parts' maps [nsub][BH][state], the
+        // segment states [nseg][BH][state]
+        sa.alpha = a.alpha; sa.H = a.H; sa.T = a.T; sa.dv = 128;
+        sa.nsub = a.nsub; sa.sub_per_seg = a.sub_per_seg; sa.sub_chunks = a.sub_chunks;
+        sa.seg_chunks = a.seg_chunks; sa.status = a.status; sa.wait_limit_ns = a.limit_ns;
+        // forward: segments 0 .. nseg-2 over (phi(k), v), unless the forward kept them
+        if (!Sf) {
+            float *pf = a.seg_ws;
+            sa.A = pf; sa.dS = pf + a_floats; sa.seg_first = 0;
+            if ((e = launch_state_tc(a.maps[1], a.maps[2], sa, B, a.alpha != nullptr, 128, ss)) != cudaSuccess) return e;
+            float *sf = pf + a_floats + (size_t)a.nsub * BH * state;
+            if ((e = launch_seg_scan(a.S0, a.z0, sa.A, sa.dS, sf, BH, 128, a.nsub, a.sub_per_seg, a.nseg, ss)) !=
+                cudaSuccess)
+                return e;
+            Sf = sf;
+            if (side && (e = cudaEventRecord(side->ev[3], ss)) != cudaSuccess) return e;
+        }
+    }
     // d accumulates the feature sums; tok_sum and fin accumulate dalpha terms
-    cudaError_t e = cudaMemsetAsync(a.ws, 0, sizeof(float) * (3 * n + BH), stream);
-    if (e != cudaSuccess) return e;
+    if ((e = cudaMemsetAsync(a.ws, 0, sizeof(float) * (3 * n + BH), stream)) != cudaSuccess) return e;
     if (!a.d_in) {
         // z_t per segment of kZLen tokens: maps, scan, products
         const int nzs = (a.T + kZLen - 1) / kZLen;
@@ -785,42 +855,30 @@ cudaError_t launch_bwd_t(const BackwardArgs &a, int B, cudaStream_t stream)
             t.tok_sum = a.alpha ? tok_sum : nullptr; t.fin = a.alpha ? fin : nullptr;
             t.dS0 = a.dS0; t.dz0 = a.dz0;
             t.H = a.H; t.T = a.T; t.status = a.status; t.limit_ns = a.limit_ns;
-            if (a.nseg > 1) {
-                // the states entering each segment: the prefill's state pass and scan in
-                // forward time (for dq), and their reversed form over (phi(q), dn, dd)
-                // from dS_T, dz_T (for dk and dv); each pass's workspace is A [nsub][BH]
-                // (256-byte aligned), the parts' maps [nsub][BH][state], the segment
-                // states [nseg][BH][state]
-                const size_t state = (size_t)128 * 128 + 128;
-                const size_t a_floats = ((size_t)a.nsub * BH * 4 + 255) / 256 * 64;
-                const size_t pass_floats = a_floats + (size_t)a.nsub * BH * state + (size_t)a.nseg * BH * state;
-                float *pf = a.seg_ws, *pr = a.seg_ws + pass_floats;
-                StateTcArgs sa;
-                sa.alpha = a.alpha; sa.H = a.H; sa.T = a.T; sa.dv = 128;
-                sa.nsub = a.nsub; sa.sub_per_seg = a.sub_per_seg; sa.sub_chunks = a.sub_chunks;
-                sa.seg_chunks = a.seg_chunks; sa.status = a.status; sa.wait_limit_ns = a.limit_ns;
-                const bool gated = a.alpha != nullptr;
-                // forward: segments 0 .. nseg-2 over (phi(k), v), unless the forward kept them
-                const float *Sf = a.states_in;
-                if (!Sf) {
-                    sa.A = pf; sa.dS = pf + a_floats; sa.seg_first = 0;
-                    if ((e = launch_state_tc(a.maps[1], a.maps[2], sa, B, gated, 128, stream)) != cudaSuccess) return e;
-                    float *sf = pf + a_floats + (size_t)a.nsub * BH * state;
-                    if ((e = launch_seg_scan(a.S0, a.z0, sa.A, sa.dS, sf, BH, 128, a.nsub, a.sub_per_seg, a.nseg,
-                                             stream)) != cudaSuccess)
-                        return e;
-                    Sf = sf;
+            if (segmented) {
+                // reversed: segments 1 .. nseg-1 over (phi(q), dy / d, dd), once d_t is done
+                if (side) {
+                    if ((e = cudaEventRecord(side->ev[1], stream)) != cudaSuccess) return e;
+                    if ((e = cudaStreamWaitEvent(ss, side->ev[1], 0)) != cudaSuccess) return e;
                 }
-                // reversed: segments 1 .. nseg-1 over (phi(q), dy / d, dd)
+                float *pr = a.seg_ws + pass_floats;
                 sa.A = pr; sa.dS = pr + a_floats; sa.seg_first = 1; sa.d = d; sa.dd = dd;
-                if ((e = launch_state_tc(a.maps[0], a.maps[3], sa, B, gated, 128, stream, true)) != cudaSuccess) return e;
+                if ((e = launch_state_tc(a.maps[0], a.maps[3], sa, B, a.alpha != nullptr, 128, ss, true)) != cudaSuccess)
+                    return e;
                 float *Sr = pr + a_floats + (size_t)a.nsub * BH * state;
-                if ((e = launch_seg_scan(a.dS_T, a.dz_T, sa.A, sa.dS, Sr, BH, 128, a.nsub, a.sub_per_seg, a.nseg, stream,
+                if ((e = launch_seg_scan(a.dS_T, a.dz_T, sa.A, sa.dS, Sr, BH, 128, a.nsub, a.sub_per_seg, a.nseg, ss,
                                          true)) != cudaSuccess)
                     return e;
+                if (side && (e = cudaEventRecord(side->ev[2], ss)) != cudaSuccess) return e;
                 t.nseg = a.nseg; t.seg_chunks = a.seg_chunks; t.seg_state_f = Sf; t.seg_state_r = Sr;
+                // dq once the forward states are there; dk and dv once the reversed ones are
+                if (side && !a.states_in && (e = cudaStreamWaitEvent(stream, side->ev[3], 0)) != cudaSuccess) return e;
+                if ((e = launch_bwd_tc(a.maps, t, B, a.alpha != nullptr, stream, 0, 1)) != cudaSuccess) return e;
+                if (side && (e = cudaStreamWaitEvent(stream, side->ev[2], 0)) != cudaSuccess) return e;
+                if ((e = launch_bwd_tc(a.maps, t, B, a.alpha != nullptr, stream, 1, 3)) != cudaSuccess) return e;
+            } else if ((e = launch_bwd_tc(a.maps, t, B, a.alpha != nullptr, stream)) != cudaSuccess) {
+                return e;
             }
-            if ((e = launch_bwd_tc(a.maps, t, B, a.alpha != nullptr, stream)) != cudaSuccess) return e;
             if (a.alpha && a.dalpha) {
                 bwd_dalpha_kernel<<<BH, kDaThreads, 0, stream>>>(tok_sum, fin, a.alpha, a.T, a.dalpha);
                 if ((e = cudaGetLastError()) != cudaSuccess) return e;

@@ -635,7 +635,8 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
 
 }  // namespace
 
-cudaError_t launch_bwd_tc(const CUtensorMap *maps, const BwdTcArgs &a, int B, bool gated, cudaStream_t stream)
+cudaError_t launch_bwd_tc(const CUtensorMap *maps, const BwdTcArgs &a, int B, bool gated, cudaStream_t stream,
+                          int first_mode, int end_mode)
 {
     using KernFn = void (*)(const CUtensorMap, const CUtensorMap, const CUtensorMap, const CUtensorMap, const BwdTcArgs);
     static const KernFn kerns[2][3] = {{bwd_tc_kernel<kModeDq, false>, bwd_tc_kernel<kModeDk, false>,
@@ -644,7 +645,8 @@ cudaError_t launch_bwd_tc(const CUtensorMap *maps, const BwdTcArgs &a, int B, bo
                                         bwd_tc_kernel<kModeDv, true>}};
     static const uint32_t bytes[3] = {smem_bytes<kModeDq>(), smem_bytes<kModeDk>(), smem_bytes<kModeDv>()};
     static OncePerDevice attr_set[2][3];
-    for (int m = 0; m < 3; ++m) {
+    if (first_mode < 0 || end_mode > 3 || first_mode >= end_mode) return cudaErrorInvalidValue;
+    for (int m = first_mode; m < end_mode; ++m) {
         cudaError_t e = set_smem_once(kerns[gated][m], bytes[m], attr_set[gated][m]);
         if (e != cudaSuccess) return e;
         kerns[gated][m]<<<dim3(a.nseg, a.H, B), kThreads, bytes[m], stream>>>(maps[0], maps[1], maps[2], maps[3], a);

@@ -220,7 +220,9 @@ struct BwdTcArgs {
     int *status;
     unsigned long long limit_ns;
 };
-cudaError_t launch_bwd_tc(const CUtensorMap *maps, const BwdTcArgs &a, int B, bool gated, cudaStream_t stream);
+// Sweeps first_mode .. end_mode - 1 (0 dq, 1 dk, 2 dv), in that order.
+cudaError_t launch_bwd_tc(const CUtensorMap *maps, const BwdTcArgs &a, int B, bool gated, cudaStream_t stream,
+                          int first_mode = 0, int end_mode = 3);
 cudaError_t launch_backward(const BackwardArgs &a, int B, bool bf16, cudaStream_t stream);
 
 cudaError_t launch_state_init(float *S, float *z, long long n_S, long long n_z, cudaStream_t stream);
