@@ -258,7 +258,11 @@ size_t la_backward_workspace_bytes(int B, int H, int T);
  * for few long sequences over sequence segments whose entering states a forward
  * and a reversed state pass compute ([LA] "门控递推为什么能做并行 scan？"); the
  * other shapes and FP32 run them as gated rank-1 recurrences in FP32 on the CUDA
- * cores.  Requires r, dv in {32, 64, 128}, T >= 1, 16-byte aligned
+ * cores.  With segments, the state passes run on a second stream of the library's
+ * (one per host thread and device, ordered against `stream` by events), beside
+ * the z pass and the dq sweep; the call's work is still complete, in order, on
+ * `stream`.  The first call on a device from a host thread creates that stream
+ * and must not be made inside a stream capture.  Requires r, dv in {32, 64, 128}, T >= 1, 16-byte aligned
  * token arrays (q, k, v, y, dy, dq, dk, dv_out), 4-byte aligned FP32 arrays
  * (dS_T 8-byte aligned).
  * Errors: LA_ERR_NULL, LA_ERR_SHAPE, LA_ERR_DTYPE, LA_ERR_ALIGN, LA_ERR_UNSUPPORTED,
