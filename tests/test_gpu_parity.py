@@ -62,6 +62,24 @@ def test_state_init(la):
     assert not S.any() and not z.any()
 
 
+def test_state_init_unaligned(la):
+    """S and z that start 4 and 12 bytes past a 16-byte boundary, with lengths that
+    are not multiples of 4: the single-float head and tail around the 16-byte
+    stores, and nothing outside the arrays touched."""
+    B, H, r, dv = 2, 3, 7, 5
+    nS, nz = B * H * r * dv, B * H * r
+    bufS = torch.randn(nS + 8, device="cuda")
+    bufz = torch.randn(nz + 8, device="cuda")
+    S = bufS[1:1 + nS].view(B, H, r, dv)
+    z = bufz[3:3 + nz].view(B, H, r)
+    before_S, before_z = bufS.clone(), bufz.clone()
+    la.state_init(B, H, r, dv, S=S, z=z)
+    torch.cuda.synchronize()
+    assert not S.any() and not z.any()
+    assert torch.equal(bufS[:1], before_S[:1]) and torch.equal(bufS[1 + nS:], before_S[1 + nS:])
+    assert torch.equal(bufz[:3], before_z[:3]) and torch.equal(bufz[3 + nz:], before_z[3 + nz:])
+
+
 # ------------------------------------------------------------- FP32 prefill
 
 def test_tiny_workload_fp32(la, oracle_mod):
