@@ -431,6 +431,22 @@ def test_prefill_short_continuation(la, oracle_mod, B, H, T, gated, with_state):
     _check(_gpu_prefill(la, inp), _oracle_prefill(oracle_mod, inp), 2e-2, f"short T={T}")
 
 
+@pytest.mark.parametrize("T,gated", [(8, False), (32, True)])
+def test_prefill_short_continuation_unaligned_state(la, oracle_mod, T, gated):
+    """A carried S0 that is 4-byte aligned only: the call takes the chunk kernel
+    instead of the token walk (which reads S0 as float4) and still matches."""
+    inp = _inputs(torch.bfloat16, 2, 3, T, 128, 128, gated=gated, with_state=True, seed=640 + T)
+    d = {k: (v.cuda() if v is not None else None) for k, v in inp.items()}
+    n = d["S0"].numel()
+    buf = torch.empty(n + 4, device="cuda", dtype=torch.float32)
+    S0 = buf[1:1 + n].view_as(d["S0"])
+    S0.copy_(d["S0"])
+    y, S, z = la.prefill_chunked(d["q"], d["k"], d["v"], alpha=d["alpha"], S0=S0, z0=d["z0"])
+    assert la.last_device_status() == 0
+    _check((y.float().cpu().numpy(), S.cpu().numpy(), z.cpu().numpy()), _oracle_prefill(oracle_mod, inp), 2e-2,
+           f"short T={T} from a 4-byte aligned state")
+
+
 def test_prefill_short_continuation_in_place_chain(la, oracle_mod):
     """Prefill 100 tokens, then continuations of 1, 5, 16 and 29 tokens in place
     (S0 = S_out), against one oracle pass over all 151 tokens."""

@@ -200,3 +200,17 @@ def test_varlen_bad_lengths_disable_segments(la, oracle_mod):
     assert la.last_device_status() == 0
     _check_plan(plan, lens, expect_split=False, invalid=(3,))
     _check_seqs(oracle_mod, d, got, skip=(3,))
+
+
+def test_varlen_segments_exact_and_single_token_tails(la, oracle_mod):
+    """Every sequence split: one ends exactly on a segment boundary (2048 tokens,
+    two segments of 16 chunks), one leaves a last segment of a single token, and
+    one a last segment of a single chunk."""
+    lens = [2048, 2049, 1088, 3000]
+    d = _packed(lens, 2, 128, True, seed=78)
+    got, status, plan = _run(la, d)
+    assert status == 0
+    L = _check_plan(plan, lens)
+    assert L == 16   # a batch this small keeps the minimum segment length
+    _check_seqs(oracle_mod, d, got)
+
