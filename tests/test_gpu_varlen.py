@@ -214,3 +214,17 @@ def test_varlen_segments_exact_and_single_token_tails(la, oracle_mod):
     assert L == 16   # a batch this small keeps the minimum segment length
     _check_seqs(oracle_mod, d, got)
 
+
+def test_varlen_segments_beyond_the_plan_cache(la, oracle_mod):
+    """5000 sequences: the plan keeps the chunk counts of the first 4096 in shared
+    memory and reads the others again; long sequences on both sides of that mark."""
+    rng = np.random.default_rng(79)
+    lens = [int(x) for x in rng.integers(0, 12, 5000)]
+    for i in (100, 4095, 4096, 4999):
+        lens[i] = 2200
+    d = _packed(lens, 1, 128, False, seed=79)
+    got, status, plan = _run(la, d)
+    assert status == 0
+    _check_plan(plan, lens)
+    _check_seqs(oracle_mod, d, got)
+
