@@ -45,9 +45,6 @@ constexpr int kBCols = 32;       // columns per CTA
 
 enum Mode { kFwdDq = 0, kRevDk = 1, kRevDv = 2 };
 
-__device__ __forceinline__ float to_f32(float x) { return x; }
-__device__ __forceinline__ float to_f32(__nv_bfloat16 x) { return __bfloat162float(x); }
-
 // phi and its derivative with the hardware exponential: for the arguments
 // x <= 0 where it is used, the relative error is about 2.4e-7 + 6e-8 |x| (the
 // rounding of x log2 e and of the base-2 exponential), far inside the

@@ -108,9 +108,6 @@ constexpr uint32_t smem_bytes() { return BCfg<MODE>::kOffSmall + sizeof(BSmall) 
 static_assert(smem_bytes<kModeDq>() <= 232448 && smem_bytes<kModeDk>() <= 232448 && smem_bytes<kModeDv>() <= 232448,
               "shared memory budget");
 
-__device__ __forceinline__ float phi_f(float x) { return x > 0.f ? x + 1.f : __expf(x); }
-__device__ __forceinline__ float dphi_f(float x) { return x > 0.f ? 1.f : __expf(x); }
-
 // One sweep (MODE) of one head (blockIdx.y, blockIdx.z), or of segment blockIdx.x of it.
 template <int MODE, bool GATED>
 __device__ __forceinline__ void
