@@ -760,6 +760,7 @@ SideLane *side_lane()
     if (dev < 0) return nullptr;
     SideLane &l = lanes[dev];
     if (!l.stream && !l.failed) {
+        const cudaError_t pending = cudaPeekAtLastError();   // not ours to clear
         bool ok = cudaStreamCreateWithFlags(&l.stream, cudaStreamNonBlocking) == cudaSuccess;
         for (int i = 0; ok && i < 4; ++i) ok = cudaEventCreateWithFlags(&l.ev[i], cudaEventDisableTiming) == cudaSuccess;
         if (!ok) {
@@ -768,7 +769,7 @@ SideLane *side_lane()
             if (l.stream) cudaStreamDestroy(l.stream);
             l.stream = nullptr;
             l.failed = true;
-            cudaGetLastError();   // the failure is not the caller's: clear it
+            if (pending == cudaSuccess) cudaGetLastError();   // clear the error of the failed creation only
         }
     }
     return l.stream ? &l : nullptr;
