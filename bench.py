@@ -652,7 +652,7 @@ def run_ours(args, rank, world, local_rank):
             varlen[vw.name] = {
                 "call_us": v_call * 1e6, "tokens_per_s": vw.T * world / v_call,
                 "token_heads_per_s": vw.T * vw.H * world / v_call, "sequences": nvb, "tokens": vw.T,
-                "longest": max(vw.lens), "launches_per_call": 4 if nvws else 1,
+                "longest": max(vw.lens), "launches_per_call": 5 if nvws else 1,   # walk, plan, state pass, scan, chunk kernel
                 "roofline": {"bound": "hbm", "achieved": v_gbs, "peak": peak, "unit": "GB/s", "frac": v_gbs / peak,
                              "peak_kind": peak_kind, "algorithmic_bytes_per_launch": vbytes,
                              "timed": "the whole call", "kernel": "prefill_tc_kernel<false, 128> items",

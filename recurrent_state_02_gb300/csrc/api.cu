@@ -183,27 +183,30 @@ struct VarlenPlan {
     size_t off_info = 0, off_items = 0, off_bds = 0, off_split = 0, off_A = 0, off_dS = 0, off_S = 0, bytes = 0;
 };
 
-VarlenPlan varlen_plan(int B, int H, int total_T, int dv)
+// walk: short sequences go to the token walk, which needs the plan's tables even
+// when no sequence can be split.
+VarlenPlan varlen_plan(int B, int H, int total_T, int dv, bool walk)
 {
     VarlenPlan p;
     const long long sms = sm_count();
     p.dvs = head_width(B, H, dv, sms);
     p.units = H * (dv / p.dvs);
-    if (sms <= 0 || total_T <= 0 || B < 1) return p;
+    if (sms <= 0 || total_T < 0 || B < 1 || B > 65535) return p;
     const long long work = ((long long)(total_T + 63) / 64 + B) * p.units;   // CTA-chunks at most
     long long L = (work + 4 * sms - 1) / (4 * sms);
     if (L < kMinSegChunks) L = kMinSegChunks;
-    const long long nb = (long long)total_T / (64 * L);
-    if (nb < 1 || B + nb > 65535) return p;   // grid rows of the chunk kernel
+    long long nb = (long long)total_T / (64 * L);
+    if (B + nb > 65535) nb = 0;   // grid rows of the chunk kernel
+    if (nb < 1 && !walk) return p;
     const long long wave = (kStateCtasPerSm * sms + p.units - 1) / p.units;
-    long long rows = wave < nb ? nb : wave;
+    long long rows = nb < 1 ? 0 : wave < nb ? nb : wave;
     if (rows > 65535) rows = 65535;
     p.min_seg = (int)L;
     p.max_bds = (int)nb;
     p.part_rows = (int)rows;
     p.part_target = (int)(wave < rows ? wave : rows);
     const size_t state = 128 * (size_t)dv + 128;
-    p.off_info = 256;
+    p.off_info = 256;   // after seg_len
     p.off_items = p.off_info + round_up(16 * (size_t)B, 256);
     p.off_bds = p.off_items + round_up(8 * ((size_t)B + nb), 256);
     p.off_split = p.off_bds + round_up(8 * (size_t)rows, 256);
@@ -459,11 +462,15 @@ size_t la_backward_states_bytes(int B, int H, int T)
     return p.nseg > 1 ? sizeof(float) * (size_t)p.nseg * B * H * (128 * 128 + 128) : 0;
 }
 
+// The most tokens of a packed sequence the token walk takes (-1: none).
+int varlen_walk_max() { return LA_DECODE_MAX_T < 1 ? -1 : LA_DECODE_MAX_T < 32 ? LA_DECODE_MAX_T : 32; }
+
 size_t la_prefill_varlen_workspace_bytes(int B, int H, int total_T, int r, int dv)
 {
     if (B < 1 || H < 1 || total_T < 1 || r != 128 || (dv != 64 && dv != 128)) return 0;
     if ((long long)B * H > 0x7fffffffLL || (long long)total_T * H > 0x7fffffffLL) return 0;
-    return varlen_plan(B, H, total_T, dv).bytes;
+    // sized for the walk (the call takes it when S0 allows)
+    return varlen_plan(B, H, total_T, dv, dv == 128 && varlen_walk_max() >= 0).bytes;
 }
 
 la_status la_prefill_varlen(const void *q, const void *k, const void *v, la_dtype dtype, const float *alpha,
@@ -485,7 +492,10 @@ la_status la_prefill_varlen(const void *q, const void *k, const void *v, la_dtyp
         for (const void *p : ptrs4)
             if (p && !aligned(p, 4)) return LA_ERR_ALIGN;
     }
-    const VarlenPlan plan = varlen_plan(B, H, total_T, dv);
+    // sequences of at most 32 tokens (a short continuation each) take the token walk,
+    // which reads S0 as float4
+    const int walk_max = (dv == 128 && (!S0 || aligned(S0, 16))) ? varlen_walk_max() : -1;
+    const VarlenPlan plan = varlen_plan(B, H, total_T, dv, walk_max >= 0);
     if (plan.bytes) {
         if (!workspace || workspace_bytes < plan.bytes) return LA_ERR_WORKSPACE;
         if (!aligned(workspace, 256)) return LA_ERR_ALIGN;
@@ -520,9 +530,14 @@ la_status la_prefill_varlen(const void *q, const void *k, const void *v, la_dtyp
     a.cu_seqlens = cu_seqlens;
     if (!plan.bytes)
         return from_cuda(la::launch_prefill_tc(mq, mk, mv, a, B, alpha != nullptr, plan.dvs, st));
-    // the plan (segment length and tables) on the device, the state pass over the
-    // segments that end at a boundary, the scan of each split sequence, then every
-    // segment in parallel
+    // the walk over the short sequences, the plan (segment length and tables) on the
+    // device, the state pass over the segments that end at a boundary, the scan of
+    // each split sequence, then every other segment in parallel
+    if (walk_max >= 0) {
+        const cudaError_t ew = la::launch_decode_multi_packed(q, k, v, true, alpha, S0, z0, S_out, z_out, cu_seqlens,
+                                                              B, H, total_T, eps, y, st);
+        if (ew != cudaSuccess) return from_cuda(ew);
+    }
     uint8_t *ws = static_cast<uint8_t *>(workspace);
     int *seg_len = reinterpret_cast<int *>(ws);
     int4 *seq_info = reinterpret_cast<int4 *>(ws + plan.off_info);
@@ -533,8 +548,8 @@ la_status la_prefill_varlen(const void *q, const void *k, const void *v, la_dtyp
     float *dS = reinterpret_cast<float *>(ws + plan.off_dS);
     float *S_start = reinterpret_cast<float *>(ws + plan.off_S);
     cudaError_t e = la::launch_varlen_plan(cu_seqlens, B, total_T, plan.min_seg, plan.units, sm_count(),
-                                           plan.max_bds, plan.part_rows, plan.part_target, seg_len, seq_info, items,
-                                           bds, split_seqs, st);
+                                           plan.max_bds, plan.part_rows, plan.part_target, walk_max, seg_len,
+                                           seq_info, items, bds, split_seqs, st);
     la::StateTcArgs sa;
     sa.alpha = alpha;
     sa.dS = dS;
@@ -551,15 +566,15 @@ la_status la_prefill_varlen(const void *q, const void *k, const void *v, la_dtyp
     sa.seg_len = seg_len;
     sa.status = status;
     sa.wait_limit_ns = la::kWaitLimitNs;
-    if (e == cudaSuccess)
+    if (e == cudaSuccess && plan.max_bds > 0)
         e = la::launch_state_tc(mk, mv, sa, B, alpha != nullptr, plan.dvs, st, false, plan.part_rows);
-    if (e == cudaSuccess)
+    if (e == cudaSuccess && plan.max_bds > 0)
         e = la::launch_varlen_scan(S0, z0, A, dS, S_start, seq_info, split_seqs, seg_len, plan.max_bds, H, dv, st);
     if (e != cudaSuccess) return from_cuda(e);
     a.items = items;
     a.seq_info = seq_info;
     a.seg_len = seg_len;
-    a.S_start = S_start;
+    a.S_start = S_start;   // read only for split sequences (none when max_bds is 0)
     return from_cuda(la::launch_prefill_tc(mq, mk, mv, a, B, alpha != nullptr, plan.dvs, st, B + plan.max_bds));
 }
 

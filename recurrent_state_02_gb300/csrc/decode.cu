@@ -159,11 +159,16 @@ decode128_kernel(const void *__restrict__ q, const void *__restrict__ k, const v
 // loads held in registers stay those of 16.
 constexpr int kMultiMaxT = 32, kMultiHalf = 16;
 constexpr uint32_t kMultiTokenBytes = 128 * 4 * 3;
-template <bool BF16, int HALVES>
+// PACKED: sequences packed token-major ([total_T, H, d], alpha [total_T, H]);
+// CTA (b, h) walks sequence b if its bounds are valid and it has at most
+// kMultiMaxT tokens (T is then ignored), and otherwise leaves it to the chunk
+// kernel.
+template <bool BF16, int HALVES, bool PACKED = false>
 __global__ void __launch_bounds__(256, 2)
 decode128_multi_kernel(const void *__restrict__ q, const void *__restrict__ k, const void *__restrict__ v,
                        const float *__restrict__ alpha, const float *S0, const float *z0, float *S_out,
-                       float *z_out, int T, float eps, void *__restrict__ y, float *__restrict__ d_out)
+                       float *z_out, int T, float eps, void *__restrict__ y, float *__restrict__ d_out,
+                       const int *__restrict__ cu_seqlens = nullptr, int H = 1)
 {
     constexpr int R = 128, DV = 128;
     extern __shared__ float4 multi_smem[];
@@ -176,6 +181,17 @@ decode128_multi_kernel(const void *__restrict__ q, const void *__restrict__ k, c
     const int bh = blockIdx.x;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const size_t row0 = (size_t)warp * 16 * (DV / 4) + lane;   // this thread's first float4 of S
+    int seq0 = 0;
+    if (PACKED) {
+        const int b = bh / H;
+        seq0 = cu_seqlens[b];
+        const int seq1 = cu_seqlens[b + 1];
+        if (seq0 < 0 || seq1 < seq0 || seq1 > T || seq1 - seq0 > kMultiMaxT) return;   // not this kernel's
+        T = seq1 - seq0;
+    }
+    // row of token t of this head in q, k, v, y (rows of 128) and alpha
+    const size_t tok0 = (size_t)bh * T;
+    auto row = [&](int t) -> size_t { return PACKED ? (size_t)(seq0 + t) * H + bh % H : tok0 + t; };
 
     float4 s[16];
     if (S0) {
@@ -187,12 +203,11 @@ decode128_multi_kernel(const void *__restrict__ q, const void *__restrict__ k, c
         for (int i = 0; i < 16; ++i) s[i] = make_float4(0.f, 0.f, 0.f, 0.f);
     }
     float zr = (tid < R && z0) ? z0[(size_t)bh * R + tid] : 0.f;
-    // the T tokens of this head are contiguous rows: 4 elements per load, all of a
-    // thread's loads of a half issued before any is used
-    const size_t tok0 = (size_t)bh * T;
+    // 4 elements per load (32 loads a token row), all of a thread's loads of a
+    // half issued before any is used
     constexpr int kLoads = kMultiHalf * R / 4 / 256;   // per thread, tensor and half
     using Raw = typename Quad<BF16>::raw;   // the loads stay raw until they are stored
-    const float a_t = (tid < T && alpha) ? alpha[tok0 + tid] : 1.f;
+    const float a_t = (tid < T && alpha) ? alpha[row(tid)] : 1.f;
 #pragma unroll
     for (int hv = 0; hv < HALVES; ++hv) {
         const int h0 = hv * kMultiHalf;
@@ -202,9 +217,10 @@ decode128_multi_kernel(const void *__restrict__ q, const void *__restrict__ k, c
         for (int it = 0; it < kLoads; ++it) {
             const int e = tid + it * 256;
             if (e < nvec) {
-                rq[it] = Quad<BF16>::load(q, tok0 * R + 4 * (size_t)(v0 + e));
-                rk[it] = Quad<BF16>::load(k, tok0 * R + 4 * (size_t)(v0 + e));
-                rv[it] = Quad<BF16>::load(v, tok0 * DV + 4 * (size_t)(v0 + e));
+                const size_t off = row((v0 + e) / (R / 4)) * R + 4 * (size_t)((v0 + e) % (R / 4));
+                rq[it] = Quad<BF16>::load(q, off);
+                rk[it] = Quad<BF16>::load(k, off);
+                rv[it] = Quad<BF16>::load(v, off);   // DV == R
             }
         }
 #pragma unroll
@@ -265,8 +281,8 @@ decode128_multi_kernel(const void *__restrict__ q, const void *__restrict__ k, c
 #pragma unroll
             for (int w = 0; w < 8; ++w) n += np[w * DV + tid];
             const float den = den_part[pb][0] + den_part[pb][1] + den_part[pb][2] + den_part[pb][3] + eps;
-            store_elem<BF16>(y, (tok0 + t) * DV + tid, n / den);
-            if (d_out && tid == 0) d_out[tok0 + t] = den;
+            store_elem<BF16>(y, row(t) * DV + tid, n / den);
+            if (d_out && tid == 0) d_out[row(t)] = den;
         }
     }
     float4 *dst = reinterpret_cast<float4 *>(S_out + (size_t)bh * R * DV) + row0;
@@ -361,7 +377,7 @@ cudaError_t launch_decode_multi(const void *q, const void *k, const void *v, boo
     // stream capture)
     // one half of 16 tokens or two
     using Kern = void (*)(const void *, const void *, const void *, const float *, const float *, const float *,
-                          float *, float *, int, float, void *, float *);
+                          float *, float *, int, float, void *, float *, const int *, int);
     static const Kern kerns[4] = {decode128_multi_kernel<false, 1>, decode128_multi_kernel<false, 2>,
                                   decode128_multi_kernel<true, 1>, decode128_multi_kernel<true, 2>};
     static OncePerDevice attr_set[4];
@@ -369,7 +385,28 @@ cudaError_t launch_decode_multi(const void *q, const void *k, const void *v, boo
     const uint32_t bytes = kMultiMaxT * kMultiTokenBytes;
     const cudaError_t e = set_smem_once(kerns[ki], bytes, attr_set[ki]);
     if (e != cudaSuccess) return e;
-    kerns[ki]<<<(unsigned)nbh, 256, bytes, stream>>>(q, k, v, alpha, S0, z0, S_out, z_out, T, eps, y, d_out);
+    kerns[ki]<<<(unsigned)nbh, 256, bytes, stream>>>(q, k, v, alpha, S0, z0, S_out, z_out, T, eps, y, d_out, nullptr,
+                                                      1);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_decode_multi_packed(const void *q, const void *k, const void *v, bool bf16, const float *alpha,
+                                       const float *S0, const float *z0, float *S_out, float *z_out,
+                                       const int *cu_seqlens, int B, int H, int total_T, float eps, void *y,
+                                       cudaStream_t stream)
+{
+    const long long nbh = (long long)B * H;
+    if (nbh < 1 || nbh > 0x7fffffffLL || total_T < 0 || !cu_seqlens) return cudaErrorInvalidValue;
+    using Kern = void (*)(const void *, const void *, const void *, const float *, const float *, const float *,
+                          float *, float *, int, float, void *, float *, const int *, int);
+    static const Kern kerns[2] = {decode128_multi_kernel<false, 2, true>, decode128_multi_kernel<true, 2, true>};
+    static OncePerDevice attr_set[2];
+    const int ki = bf16 ? 1 : 0;
+    const uint32_t bytes = kMultiMaxT * kMultiTokenBytes;
+    const cudaError_t e = set_smem_once(kerns[ki], bytes, attr_set[ki]);
+    if (e != cudaSuccess) return e;
+    kerns[ki]<<<(unsigned)nbh, 256, bytes, stream>>>(q, k, v, alpha, S0, z0, S_out, z_out, total_T, eps, y, nullptr,
+                                                      cu_seqlens, H);
     return cudaGetLastError();
 }
 

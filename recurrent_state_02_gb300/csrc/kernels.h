@@ -128,14 +128,15 @@ cudaError_t launch_state_tc(const CUtensorMap &map_k, const CUtensorMap &map_v, 
 // min_seg_chunks (from the batch's chunks, units CTAs per segment, sms SMs), and
 // sequence b of c_b chunks takes max(1, ceil(c_b / L)) segments; with bounds
 // outside [0, total_T] anywhere, or more than max_bds boundaries, one segment
-// each.  Writes seg_len [3] (L, chunks per part, parts per boundary's segment, so
-// that the boundaries fill about part_target of the part_rows >= max_bds rows),
-// seq_info [B], items
-// [B + max_bds] (longest segments first), bds [part_rows] and split_seqs
-// [max_bds] (see PrefillTcArgs and StateTcArgs; unused entries -1).  One CTA.
+// each; a valid sequence of at most walk_max tokens (-1: none) takes no segment
+// (the token walk handles it).  Writes seg_len [3] (L, chunks per part, parts per
+// boundary's segment, so that the boundaries fill about part_target of the
+// part_rows >= max_bds rows), seq_info [B], items [B + max_bds] (longest segments
+// first), bds [part_rows] and split_seqs [max_bds] (see PrefillTcArgs and
+// StateTcArgs; unused entries -1).  One CTA.
 cudaError_t launch_varlen_plan(const int *cu_seqlens, int B, int total_T, int min_seg_chunks, int units, int sms,
-                               int max_bds, int part_rows, int part_target, int *seg_len, int4 *seq_info,
-                               int2 *items, int2 *bds, int *split_seqs, cudaStream_t stream);
+                               int max_bds, int part_rows, int part_target, int walk_max, int *seg_len,
+                               int4 *seq_info, int2 *items, int2 *bds, int *split_seqs, cudaStream_t stream);
 
 // The varlen scan: for every split sequence (split_seqs, max_bds entries) and head
 // h, S_start[slot + 0] = S0[b], z0[b] (zero if null), then S_start[slot + g] the
@@ -164,6 +165,13 @@ cudaError_t launch_decode(const void *q, const void *k, const void *v, bool bf16
                           bool fast128, cudaStream_t stream);
 // T tokens per (b, h) (r = dv = 128) from S0, z0 (nullptr: zero) into S_out, z_out
 // (may alias), y [B,H,T,dv]; d_out (or nullptr) [B,H,T].
+// The same walk over packed sequences (token-major, cu_seqlens [B + 1]): sequence
+// b's H heads are walked when its bounds lie in [0, total_T] and it has at most
+// 32 tokens (none of them: S0, z0 copied); the others are left untouched.
+cudaError_t launch_decode_multi_packed(const void *q, const void *k, const void *v, bool bf16, const float *alpha,
+                                       const float *S0, const float *z0, float *S_out, float *z_out,
+                                       const int *cu_seqlens, int B, int H, int total_T, float eps, void *y,
+                                       cudaStream_t stream);
 cudaError_t launch_decode_multi(const void *q, const void *k, const void *v, bool bf16, const float *alpha,
                                 const float *S0, const float *z0, float *S_out, float *z_out, int B, int H, int T,
                                 float eps, void *y, float *d_out, cudaStream_t stream);

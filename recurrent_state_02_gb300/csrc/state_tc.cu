@@ -494,11 +494,12 @@ __device__ __forceinline__ int order_key(int c)
 // sub parts (of at least about 4 chunks) so that the boundaries fill part_target
 // of them (one wave of state CTAs), or one part each beyond that.
 // seg_len receives L, the chunks per part and sub; split_seqs the split
-// sequences (in no set order, then -1 up to max_bds).
+// sequences (in no set order, then -1 up to max_bds).  A valid sequence of at most
+// walk_max tokens (-1: none) is left to the token walk: no item, no segment.
 constexpr int kPlanCache = 4096;   // chunk counts of the first sequences, in shared memory
 __global__ void __launch_bounds__(1024, 1)
 varlen_plan_kernel(const int *__restrict__ cu, int B, int total_T, int L_min, int units, int sms, int max_bds,
-                   int part_rows, int part_target, int *__restrict__ seg_len, int4 *__restrict__ seq_info, int2 *__restrict__ items,
+                   int part_rows, int part_target, int walk_max, int *__restrict__ seg_len, int4 *__restrict__ seq_info, int2 *__restrict__ items,
                    int2 *__restrict__ bds, int *__restrict__ split_seqs)
 {
     __shared__ int warp_sums[32];
@@ -507,12 +508,14 @@ varlen_plan_kernel(const int *__restrict__ cu, int B, int total_T, int L_min, in
     __shared__ int bucket[kOrderBuckets];
     __shared__ int cached[kPlanCache];
     __shared__ int n_split;
-    // chunks of sequence b (-1 when its bounds are bad)
+    // chunks of sequence b (-1 when its bounds are bad, -2 when the walk takes it)
     auto read_chunks = [&](int b) {
         const int s0 = cu[b], s1 = cu[b + 1];
-        return (s0 < 0 || s1 < s0 || s1 > total_T) ? -1 : (s1 - s0 + kC - 1) / kC;
+        if (s0 < 0 || s1 < s0 || s1 > total_T) return -1;
+        return s1 - s0 <= walk_max ? -2 : (s1 - s0 + kC - 1) / kC;
     };
-    auto chunks = [&](int b) { return max(0, b < kPlanCache ? cached[b] : read_chunks(b)); };
+    auto code = [&](int b) { return b < kPlanCache ? cached[b] : read_chunks(b); };
+    auto chunks = [&](int b) { return max(0, code(b)); };
     if (threadIdx.x == 0) {
         acc[0] = acc[1] = 0;
         n_split = 0;
@@ -525,7 +528,7 @@ varlen_plan_kernel(const int *__restrict__ cu, int B, int total_T, int L_min, in
     for (int b = threadIdx.x; b < B; b += blockDim.x) {
         const int c = read_chunks(b);
         if (b < kPlanCache) cached[b] = c;
-        bad = bad || c < 0;
+        bad = bad || c == -1;
         sum += max(c, 0);
     }
     block_add(sum, &acc[0]);
@@ -542,8 +545,10 @@ varlen_plan_kernel(const int *__restrict__ cu, int B, int total_T, int L_min, in
     __syncthreads();
     const bool split = !any_bad && acc[1] <= (unsigned long long)max_bds;
     const int n_bd = split ? (int)acc[1] : 0;
-    // the segments of sequence b (x), and the chunks of the last one (y; the others have L)
+    // the segments of sequence b (x; 0: the walk's), and the chunks of the last one
+    // (y; the others have L)
     auto segments = [&](int b) {
+        if (code(b) == -2) return make_int2(0, 0);
         const int c = chunks(b);
         if (!split || c <= L) return make_int2(1, c);
         const int n = (c + L - 1) / L;
@@ -553,7 +558,7 @@ varlen_plan_kernel(const int *__restrict__ cu, int B, int total_T, int L_min, in
     for (int b = threadIdx.x; b < B; b += blockDim.x) {
         const int2 sg = segments(b);
         if (sg.x > 1) atomicAdd(&bucket[order_key(L)], sg.x - 1);
-        atomicAdd(&bucket[order_key(sg.y)], 1);
+        if (sg.x > 0) atomicAdd(&bucket[order_key(sg.y)], 1);
     }
     __syncthreads();
     // exclusive prefix over the buckets: their first rows in the item table
@@ -563,13 +568,14 @@ varlen_plan_kernel(const int *__restrict__ cu, int B, int total_T, int L_min, in
         if (threadIdx.x < kOrderBuckets) bucket[threadIdx.x] = first;
         __syncthreads();
     }
+    const int n_items = tot[0];   // read before the scans below reuse tot
     // pass 4: prefix sums of boundaries and slots, tile by tile, and each item's row
     int carry_bd = 0, carry_slot = 0;
     for (int b0 = 0; b0 < B; b0 += blockDim.x) {
         const int b = b0 + threadIdx.x;
         const int2 sg = b < B ? segments(b) : make_int2(1, 0);
         const int nseg = sg.x, last = sg.y;
-        const int nbd = nseg - 1, nslot = nseg > 1 ? nseg : 0;
+        const int nbd = max(0, nseg - 1), nslot = nseg > 1 ? nseg : 0;
         const int bd0 = carry_bd + block_excl_scan(nbd, warp_sums, &tot[0]);
         const int tile_bd = tot[0];
         const int slot0 = carry_slot + block_excl_scan(nslot, warp_sums, &tot[1]);
@@ -595,7 +601,7 @@ varlen_plan_kernel(const int *__restrict__ cu, int B, int total_T, int L_min, in
         seg_len[2] = (L + sub_chunks - 1) / sub_chunks;
     }
     // pass 5: the rows past the plan's items, boundaries and split sequences do nothing
-    for (int i = B + carry_bd + threadIdx.x; i < B + max_bds; i += blockDim.x) items[i] = make_int2(-1, 0);
+    for (int i = n_items + threadIdx.x; i < B + max_bds; i += blockDim.x) items[i] = make_int2(-1, 0);
     for (int k = carry_bd + threadIdx.x; k < part_rows; k += blockDim.x) bds[k] = make_int2(-1, 0);
     for (int i = n_split + threadIdx.x; i < max_bds; i += blockDim.x) split_seqs[i] = -1;
 }
@@ -672,14 +678,15 @@ varlen_scan_kernel(const float *S0, const float *z0, const float *__restrict__ A
 }  // namespace
 
 cudaError_t launch_varlen_plan(const int *cu_seqlens, int B, int total_T, int min_seg_chunks, int units, int sms,
-                               int max_bds, int part_rows, int part_target, int *seg_len, int4 *seq_info, int2 *items,
-                               int2 *bds, int *split_seqs, cudaStream_t stream)
+                               int max_bds, int part_rows, int part_target, int walk_max, int *seg_len,
+                               int4 *seq_info, int2 *items, int2 *bds, int *split_seqs, cudaStream_t stream)
 {
-    if (B < 1 || min_seg_chunks < 1 || units < 1 || sms < 1 || max_bds < 1 || total_T < 0 || part_rows < max_bds ||
-        part_target < 1)
+    if (B < 1 || min_seg_chunks < 1 || units < 1 || sms < 1 || max_bds < 0 || total_T < 0 || part_rows < max_bds ||
+        (max_bds > 0 && part_target < 1) || walk_max < -1)
         return cudaErrorInvalidValue;
     varlen_plan_kernel<<<1, 1024, 0, stream>>>(cu_seqlens, B, total_T, min_seg_chunks, units, sms, max_bds,
-                                                part_rows, part_target, seg_len, seq_info, items, bds, split_seqs);
+                                                part_rows, part_target, walk_max, seg_len, seq_info, items, bds,
+                                                split_seqs);
     return cudaGetLastError();
 }
 

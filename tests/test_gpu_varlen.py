@@ -10,7 +10,8 @@ workspace (the length at byte 0, the per-sequence int4 records from byte 256:
 segments, first start-state slot, first boundary; the item table of (sequence,
 segment) pairs after them, from the next 256-byte boundary), so each test also
 checks that the split it is about took place and that the chunk kernel's CTAs
-start with the longest segments.
+start with the longest segments.  Sequences of at most 32 tokens (empty ones
+included) take the token walk instead: no segment, no item.
 """
 import numpy as np
 import pytest
@@ -68,9 +69,9 @@ def _run(la, d, in_place=False):
         L = int(w[:4].view(torch.int32)[0])
         info = w[256:256 + 16 * B].view(torch.int32).view(B, 4).numpy()
         off = 256 + (16 * B + 255) // 256 * 256
-        n_items = B + int(np.sum(info[:, 0] - 1))
+        n_items = int(np.sum(info[:, 0]))
         items = w[off:off + 8 * n_items].view(torch.int32).view(n_items, 2).numpy()
-        plan = (L, info, items)
+        plan = (L, info, items, dv)
     return (y.float().cpu(), S.cpu(), z.cpu()), status, plan
 
 
@@ -82,18 +83,23 @@ def _order_key(c):
     return -(64 + 8 * (o - 6) + ((c >> (o - 3)) & 7))
 
 
+WALK_MAX = 32   # a valid sequence of at most this many tokens takes the token walk (dv = 128)
+
+
 def _check_plan(plan, lens, expect_split=True, invalid=()):
     assert plan is not None, "no workspace: the plan does not segment at these sizes"
-    L, info, items = plan
+    L, info, items, dv = plan
+    walk_max = WALK_MAX if dv == 128 else -1
     assert L >= 16
-    # a sequence with bad bounds counts as empty
+    # a sequence with bad bounds counts as empty; a short valid one takes no segment
     chunks = [0 if b in invalid else (n + 63) // 64 for b, n in enumerate(lens)]
-    want = [(c + L - 1) // L if (expect_split and c > L) else 1 for c in chunks]
+    walked = [b not in invalid and n <= walk_max for b, n in enumerate(lens)]
+    want = [0 if walked[b] else (c + L - 1) // L if (expect_split and c > L) else 1 for b, c in enumerate(chunks)]
     assert list(info[:, 0]) == want, (L, list(info[:, 0]), want)
     if expect_split:
         assert max(want) > 1, "no sequence was split"
         # boundaries and start-state slots are numbered in sequence order
-        bd = np.concatenate([[0], np.cumsum([n - 1 for n in want])])[:-1]
+        bd = np.concatenate([[0], np.cumsum([max(0, n - 1) for n in want])])[:-1]
         assert list(info[:, 2]) == list(bd)
         slots = np.concatenate([[0], np.cumsum([n if n > 1 else 0 for n in want])])[:-1]
         assert [int(info[b, 1]) for b in range(len(lens)) if want[b] > 1] == \
@@ -227,4 +233,40 @@ def test_varlen_segments_beyond_the_plan_cache(la, oracle_mod):
     assert status == 0
     _check_plan(plan, lens)
     _check_seqs(oracle_mod, d, got)
+
+
+def _ragged_short_lens(seed):
+    rng = np.random.default_rng(seed)
+    lens = [int(x) for x in rng.integers(0, 33, 300)]   # 0 .. 32 tokens, empty ones included
+    lens[7], lens[150] = 1500, 33                        # a long prompt, and one token past the walk
+    return lens
+
+
+def test_varlen_ragged_short_continuations(la, oracle_mod):
+    """300 requests of 0 to 32 new tokens each from its own state, gated, in place
+    (the token walk), beside one long prompt and one of 33 tokens (the chunk kernel)."""
+    lens = _ragged_short_lens(80)
+    d = _packed(lens, 2, 128, True, seed=80)
+    got, status, plan = _run(la, d, in_place=True)
+    assert status == 0
+    _check_plan(plan, lens)
+    _check_seqs(oracle_mod, d, got)
+
+
+def test_varlen_ragged_short_unaligned_state(la, oracle_mod):
+    """The same batch with S0 only 4-byte aligned: the walk (which reads S0 as
+    float4) is not used, and every sequence takes the chunk kernel."""
+    lens = _ragged_short_lens(81)
+    d = _packed(lens, 2, 128, False, seed=81)
+    B, H = len(lens), 2
+    total = int(d["cu"][-1])
+    g = {n: d[n].cuda() for n in ("q", "k", "v")}
+    n = d["S0"].numel()
+    buf = torch.empty(n + 4, device="cuda", dtype=torch.float32)
+    S0 = buf[1:1 + n].view_as(d["S0"])
+    S0.copy_(d["S0"].cuda())
+    y, S, z = la.prefill_varlen(g["q"], g["k"], g["v"], torch.from_numpy(d["cu"]).cuda(), S0=S0, z0=d["z0"].cuda())
+    assert la.last_device_status() == 0
+    assert y.shape == (total, H, 128) and S.shape == (B, H, 128, 128)
+    _check_seqs(oracle_mod, d, (y.float().cpu(), S.cpu(), z.cpu()))
 
