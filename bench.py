@@ -619,11 +619,13 @@ def run_ours(args, rank, world, local_rank):
 
     varlen = None
     if want("varlen"):
-        # packed serving batches (la_prefill_varlen from zero states; q, k, v of 497 MB
-        # and 1.1 GB, > L2): the whole call (the plan, state pass, scan and chunk
-        # kernel when sequences are split) replayed as a CUDA graph
+        # packed serving batches through la_prefill_varlen: two prompt mixes from zero
+        # states (q, k, v of 497 MB and 1.1 GB, > L2), and ragged short continuations
+        # from 256 x 16 carried states in place (270 MB of state, > L2): the whole
+        # call (the token walk, the plan, state pass, scan and chunk kernel)
+        # replayed as a CUDA graph
         varlen = {}
-        for vw in (W.VARLEN_LONG, W.VARLEN_LOGU):
+        for vw in (W.VARLEN_LONG, W.VARLEN_LOGU, W.VARLEN_SHORT):
             vin = W.varlen_inputs(vw, device=dev, seed=vw.seed + 1000 * rank)
             nvb = len(vw.lens)
             yv = torch.empty((vw.T, vw.H, vw.dv), device=dev, dtype=torch.bfloat16)
@@ -632,11 +634,16 @@ def run_ours(args, rank, world, local_rank):
             nvws = int(L.la_prefill_varlen_workspace_bytes(nvb, vw.H, vw.T, vw.r, vw.dv))
             vws = torch.empty(max(nvws, 256), device=dev, dtype=torch.uint8)
 
+            # carried states are updated in place (S0 = S_out), as a serving step would
+            if "S0" in vin:
+                Sv, zv = vin["S0"], vin["z0"]
+            opt = lambda n: P(vin[n]) if n in vin else None
+
             def k_varlen():
-                _native.check(L.la_prefill_varlen(P(vin["q"]), P(vin["k"]), P(vin["v"]), _native.LA_DTYPE_BF16, None,
-                                                  None, None, P(vin["cu_seqlens"]), nvb, vw.H, vw.T, vw.r, vw.dv,
-                                                  vw.chunk, vw.eps, P(yv), P(Sv), P(zv), P(vws) if nvws else None,
-                                                  nvws, sh), "la_prefill_varlen")
+                _native.check(L.la_prefill_varlen(P(vin["q"]), P(vin["k"]), P(vin["v"]), _native.LA_DTYPE_BF16,
+                                                  opt("alpha"), opt("S0"), opt("z0"), P(vin["cu_seqlens"]), nvb, vw.H,
+                                                  vw.T, vw.r, vw.dv, vw.chunk, vw.eps, P(yv), P(Sv), P(zv),
+                                                  P(vws) if nvws else None, nvws, sh), "la_prefill_varlen")
 
             with torch.cuda.stream(stream):
                 k_varlen()
@@ -647,7 +654,11 @@ def run_ours(args, rank, world, local_rank):
             v_s, = reduce_max([v_s], dev, dist)
             assert _native.lib().la_last_device_status(sh) == 0
             v_call = v_s / args.steps
-            vbytes = varlen_bytes(nvb, vw.H, vw.T, vw.r, vw.dv)
+            # the dominant kernel: the token walk for the short continuations, else the chunk kernel
+            vkern, vsrc = (("decode128_multi_kernel<true, 2, packed>", "decode.cu") if vw is W.VARLEN_SHORT
+                           else ("prefill_tc_kernel<false, 128> items", "prefill_tc.cu"))
+            vbytes = varlen_bytes(nvb, vw.H, vw.T, vw.r, vw.dv) + (
+                nvb * vw.H * 4 * (vw.r * vw.dv + vw.r) if "S0" in vin else 0) + (vw.T * vw.H * 4 if vw.gated else 0)
             v_gbs = vbytes / v_call / 1e9
             varlen[vw.name] = {
                 "call_us": v_call * 1e6, "tokens_per_s": vw.T * world / v_call,
@@ -655,9 +666,8 @@ def run_ours(args, rank, world, local_rank):
                 "longest": max(vw.lens), "launches_per_call": 5 if nvws else 1,   # walk, plan, state pass, scan, chunk kernel
                 "roofline": {"bound": "hbm", "achieved": v_gbs, "peak": peak, "unit": "GB/s", "frac": v_gbs / peak,
                              "peak_kind": peak_kind, "algorithmic_bytes_per_launch": vbytes,
-                             "timed": "the whole call", "kernel": "prefill_tc_kernel<false, 128> items",
-                             "traffic": profile_traffic("prefill_tc_kernel<false, 128> items",
-                                                        f"B{nvb} H{vw.H} T{vw.T}", kernel_sources("prefill_tc.cu"))}}
+                             "timed": "the whole call", "kernel": vkern,
+                             "traffic": profile_traffic(vkern, f"B{nvb} H{vw.H} T{vw.T}", kernel_sources(vsrc))}}
             del vin, yv, Sv, zv, vws, gv
         torch.cuda.empty_cache()
 

@@ -75,8 +75,14 @@ _LONG_MIX = (16384,) + (512,) * 47
 VARLEN_LONG = Workload("varlen one prompt of 16384 + 47 of 512 tokens H16 d128 bf16", B=len(_LONG_MIX), H=16,
                        T=sum(_LONG_MIX), lens=_LONG_MIX, seed=7)
 _LOGU_MIX = _loguniform_lens(48, 128, 8192, seed=8)
+_SHORT_MIX = tuple(int(x) for x in torch.randint(1, 33, (256,), generator=torch.Generator().manual_seed(9)))
 VARLEN_LOGU = Workload("varlen 48 prompts of log-uniform 128..8192 tokens H16 d128 bf16", B=48, H=16,
                        T=sum(_LOGU_MIX), lens=_LOGU_MIX, seed=8)
+# Ragged short continuations: 256 requests of 1..32 new tokens each (uniform,
+# seeded), gated, each from its own carried state (the decode requests' state
+# distribution), in place.
+VARLEN_SHORT = Workload("varlen 256 short continuations of 1..32 tokens H16 d128 bf16 gated, fp32 states", B=256,
+                        H=16, T=sum(_SHORT_MIX), lens=_SHORT_MIX, gated=True, decode=True, seed=9)
 
 SHORT = Workload("short continuation B256 H16 T8 d128 bf16 alpha=sigmoid(N(3,1)), fp32 state", B=256, H=16, T=8,
                  gated=True, seed=6)
@@ -111,12 +117,21 @@ def prefill_inputs(w: Workload, device="cpu", with_state: bool = False, seed: in
 def varlen_inputs(w: Workload, device="cpu", seed: int | None = None):
     """Packed sequences of lengths ``w.lens``: q, k [T, H, r], v [T, H, dv] in
     ``w.dtype`` (token-major, T = sum of the lengths), drawn as ``prefill_inputs``
-    draws one sequence of T tokens; cu_seqlens int32 [B + 1]."""
+    draws one sequence of T tokens; cu_seqlens int32 [B + 1]; with a gate, alpha
+    [T, H] FP32; with ``w.decode`` (carried states), S0 [B,H,r,dv] ~ N(0,1)*0.1 and
+    z0 [B,H,r] ~ U(1,100), FP32."""
     one = prefill_inputs(w.with_(B=1, T=sum(w.lens)), seed=seed)
     tok = lambda x: x[0].permute(1, 0, 2).contiguous()
     cu = torch.zeros(len(w.lens) + 1, dtype=torch.int32)
     cu[1:] = torch.cumsum(torch.tensor(w.lens, dtype=torch.int64), 0).to(torch.int32)
     out = dict(q=tok(one["q"]), k=tok(one["k"]), v=tok(one["v"]), cu_seqlens=cu)
+    if w.gated:
+        out["alpha"] = one["alpha"][0].permute(1, 0).contiguous()
+    if w.decode:
+        g = torch.Generator().manual_seed((w.seed if seed is None else seed) + 1)
+        B = len(w.lens)
+        out["S0"] = torch.randn((B, w.H, w.r, w.dv), generator=g, dtype=torch.float32) * 0.1
+        out["z0"] = torch.rand((B, w.H, w.r), generator=g, dtype=torch.float32) * 99.0 + 1.0
     if device != "cpu":
         out = {n: t.to(device) for n, t in out.items()}
     return out
