@@ -166,7 +166,10 @@ size_t la_prefill_varlen_workspace_bytes(int B, int H, int total_T, int r, int d
  * long enough, or any sequence's bounds are invalid, nothing is split.  At dv = 128
  * with S0 16-byte aligned (or NULL), a sequence of at most 32 tokens (a short
  * continuation of one request, empty ones included) is walked token by token with
- * its state in registers (the walk of la_prefill_chunked), beside the others.
+ * its state in registers (the walk of la_prefill_chunked), beside the others, on a
+ * second stream of the library's (one per host thread and device, ordered against
+ * `stream` by events): the first such call on a device from a host thread creates
+ * it and must not be made inside a stream capture.
  * Requires BF16, r == 128, dv in {64, 128}, chunk >= 1 (computed in chunks of 64
  * tokens, as la_prefill_chunked); q, k, v, y, S_out 16-byte aligned.  total_T may be 0.
  * Rows of y outside every sequence are not written.

@@ -3,6 +3,7 @@
 #include "../../include/linattn.h"
 #include "delta_tc.h"
 #include "kernels.h"
+#include "side_lane.h"
 
 #include <atomic>
 #include <cstdint>
@@ -533,9 +534,18 @@ la_status la_prefill_varlen(const void *q, const void *k, const void *v, la_dtyp
     // the walk over the short sequences, the plan (segment length and tables) on the
     // device, the state pass over the segments that end at a boundary, the scan of
     // each split sequence, then every other segment in parallel
+    // The walk touches only the short sequences and the chain below only the others,
+    // so the walk runs on a side stream beside the chain (ordered by events: after
+    // what the caller enqueued before, and before what it enqueues after).
+    la::SideLane *side = walk_max >= 0 ? la::side_lane() : nullptr;
     if (walk_max >= 0) {
-        const cudaError_t ew = la::launch_decode_multi_packed(q, k, v, true, alpha, S0, z0, S_out, z_out, cu_seqlens,
-                                                              B, H, total_T, eps, y, st);
+        const cudaStream_t ws_ = side ? side->stream : st;
+        cudaError_t ew = cudaSuccess;
+        if (side && (ew = cudaEventRecord(side->ev[0], st)) == cudaSuccess) ew = cudaStreamWaitEvent(ws_, side->ev[0], 0);
+        if (ew == cudaSuccess)
+            ew = la::launch_decode_multi_packed(q, k, v, true, alpha, S0, z0, S_out, z_out, cu_seqlens, B, H, total_T,
+                                                eps, y, ws_);
+        if (ew == cudaSuccess && side) ew = cudaEventRecord(side->ev[1], ws_);
         if (ew != cudaSuccess) return from_cuda(ew);
     }
     uint8_t *ws = static_cast<uint8_t *>(workspace);
@@ -575,7 +585,9 @@ la_status la_prefill_varlen(const void *q, const void *k, const void *v, la_dtyp
     a.seq_info = seq_info;
     a.seg_len = seg_len;
     a.S_start = S_start;   // read only for split sequences (none when max_bds is 0)
-    return from_cuda(la::launch_prefill_tc(mq, mk, mv, a, B, alpha != nullptr, plan.dvs, st, B + plan.max_bds));
+    e = la::launch_prefill_tc(mq, mk, mv, a, B, alpha != nullptr, plan.dvs, st, B + plan.max_bds);
+    if (e == cudaSuccess && side) e = cudaStreamWaitEvent(st, side->ev[1], 0);   // join the walk
+    return from_cuda(e);
 }
 
 la_status la_prefill_chunked_noalloc(const void *q, const void *k, const void *v, la_dtype dtype,

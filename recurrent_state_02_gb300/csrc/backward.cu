@@ -31,6 +31,7 @@
 // converts a landed block once to FP32, already transformed (phi, dy / d_t).
 // Finally a pass of one CTA per head turns the per-token terms into dalpha.
 
+#include "side_lane.h"
 #include "tc_common.cuh"
 
 #include <cuda_bf16.h>
@@ -739,40 +740,6 @@ cudaError_t launch_rec(const RecArgs &a, int B, int L, cudaStream_t stream)
     case 128: return go(rec_kernel<Tin, Mode, 128>, sizeof(RecSmem<Tin, 128>));
     default: return cudaErrorInvalidValue;
     }
-}
-
-// A second stream and four events per host thread and device, for the state
-// passes that run beside the main chain of the backward (so that calls from
-// several host threads never share them, and a stream capture on one thread never
-// takes in another's work).  Made on the first call on a device, which must not
-// be inside a stream capture; nullptr if they cannot be made (everything then
-// runs on the caller's stream).
-struct SideLane {
-    cudaStream_t stream = nullptr;
-    cudaEvent_t ev[4] = {};
-    bool failed = false;
-};
-
-SideLane *side_lane()
-{
-    thread_local SideLane lanes[kMaxDevices];
-    const int dev = current_device_index();
-    if (dev < 0) return nullptr;
-    SideLane &l = lanes[dev];
-    if (!l.stream && !l.failed) {
-        const cudaError_t pending = cudaPeekAtLastError();   // not ours to clear
-        bool ok = cudaStreamCreateWithFlags(&l.stream, cudaStreamNonBlocking) == cudaSuccess;
-        for (int i = 0; ok && i < 4; ++i) ok = cudaEventCreateWithFlags(&l.ev[i], cudaEventDisableTiming) == cudaSuccess;
-        if (!ok) {
-            for (cudaEvent_t &ev : l.ev)
-                if (ev) cudaEventDestroy(ev), ev = nullptr;
-            if (l.stream) cudaStreamDestroy(l.stream);
-            l.stream = nullptr;
-            l.failed = true;
-            if (pending == cudaSuccess) cudaGetLastError();   // clear the error of the failed creation only
-        }
-    }
-    return l.stream ? &l : nullptr;
 }
 
 template <typename Tin>
