@@ -175,10 +175,12 @@ size_t seg_workspace_bytes(const SegPlan &p, int B, int H, int dv)
 // 4 SMs' worth, and so the workspace, whatever the total.  The state pass gets
 // part_rows >= max_bds rows of CTAs; the plan shares about one wave of them
 // (part_target) among the boundaries it makes (more parts would shorten the
-// pass but lengthen the scan, which composes them one after another).  Workspace (256-byte aligned parts): seg_len int[3],
-// seq_info int4[B], items int2[B + max_bds], bds int2[part_rows], split_seqs
-// int[max_bds], A and dS of part_rows parts, and 2 max_bds start-state slots (a
-// split sequence has at most twice as many segments as boundaries).
+// pass but lengthen the scan, which composes them one after another).  With the
+// token walk for short sequences the plan is made even when no sequence can be
+// split (max_bds 0: its tables only).  Workspace (256-byte aligned parts):
+// seg_len int[3], seq_info int4[B], items int2[B + max_bds], bds int2[part_rows],
+// split_seqs int[max_bds], A and dS of part_rows parts, and 2 max_bds start-state
+// slots (a split sequence has at most twice as many segments as boundaries).
 struct VarlenPlan {
     int dvs = 64, units = 0, min_seg = 0, max_bds = 0, part_rows = 0, part_target = 0;
     size_t off_info = 0, off_items = 0, off_bds = 0, off_split = 0, off_A = 0, off_dS = 0, off_S = 0, bytes = 0;
