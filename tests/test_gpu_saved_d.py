@@ -35,6 +35,7 @@ CASES = [
     (torch.bfloat16, 1, 1, 65, 128, 128, True, True),      # ragged tail of one token
     (torch.bfloat16, 2, 2, 700, 128, 64, True, True),      # gated 64-column slices
     (torch.bfloat16, 2, 3, 9, 128, 128, True, True),       # a short continuation (the token walk)
+    (torch.bfloat16, 2, 2, 25, 128, 128, True, True),      # the walk over two halves of 16 tokens
     (torch.bfloat16, 1, 2, 3000, 128, 128, False, True),   # ungated whole heads, segments, kept states
     (torch.float32, 2, 2, 200, 64, 64, True, True),
 ]

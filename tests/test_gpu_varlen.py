@@ -244,9 +244,12 @@ def _ragged_short_lens(seed):
 
 def test_varlen_ragged_short_continuations(la, oracle_mod):
     """300 requests of 0 to 32 new tokens each from its own state, gated, in place
-    (the token walk), beside one long prompt and one of 33 tokens (the chunk kernel)."""
+    (the token walk), beside one long prompt and one of 33 tokens (the chunk kernel);
+    a few gates are exactly 0 (a reset inside a request)."""
     lens = _ragged_short_lens(80)
-    d = _packed(lens, 2, 128, True, seed=80)
+    cu = np.concatenate([[0], np.cumsum(lens)])
+    zeros = [int(cu[b]) + lens[b] // 2 for b in (3, 40, 200) if lens[b] > 0] + [int(cu[7]) + 700]
+    d = _packed(lens, 2, 128, True, seed=80, zero_gates=zeros)
     got, status, plan = _run(la, d, in_place=True)
     assert status == 0
     _check_plan(plan, lens)
