@@ -128,10 +128,11 @@ la_status la_prefill_chunked(const void *q, const void *k, const void *v, la_dty
 
 /*
  * la_prefill_varlen_workspace_bytes -- device scratch that la_prefill_varlen needs
- * for a batch of B sequences, H heads and total_T tokens on the current device (0:
- * the sequences are never split into segments).  It depends on the sizes and the
- * device's SM count only, not on the lengths, which stay on the device.  Returns 0
- * for sizes la_prefill_varlen rejects.
+ * for a batch of B sequences, H heads and total_T tokens (total_T >= 0) on the
+ * current device: the plan's tables and, when sequences can be split, their
+ * segment states (0: the call needs none, dv = 64 with nothing to split).  It
+ * depends on the sizes and the device's SM count only, not on the lengths, which
+ * stay on the device.  Returns 0 for sizes la_prefill_varlen rejects.
  */
 size_t la_prefill_varlen_workspace_bytes(int B, int H, int total_T, int r, int dv);
 

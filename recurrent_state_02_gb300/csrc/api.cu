@@ -470,9 +470,10 @@ int varlen_walk_max() { return LA_DECODE_MAX_T < 1 ? -1 : LA_DECODE_MAX_T < 32 ?
 
 size_t la_prefill_varlen_workspace_bytes(int B, int H, int total_T, int r, int dv)
 {
-    if (B < 1 || H < 1 || total_T < 1 || r != 128 || (dv != 64 && dv != 128)) return 0;
+    if (B < 1 || H < 1 || total_T < 0 || r != 128 || (dv != 64 && dv != 128)) return 0;
     if ((long long)B * H > 0x7fffffffLL || (long long)total_T * H > 0x7fffffffLL) return 0;
-    // sized for the walk (the call takes it when S0 allows)
+    // sized for the walk (which runs even when there are no tokens at all: the
+    // states are handed on) (the call takes it when S0 allows)
     return varlen_plan(B, H, total_T, dv, dv == 128 && varlen_walk_max() >= 0).bytes;
 }
 

@@ -153,7 +153,7 @@ def test_varlen_rejects_bad_arguments(native):
 def test_varlen_workspace_bytes(native):
     L = native.lib()
     # sizes la_prefill_varlen rejects need nothing
-    for args in ((0, 16, 4096, 128, 128), (4, 0, 4096, 128, 128), (4, 16, 0, 128, 128), (4, 16, 4096, 64, 128),
+    for args in ((0, 16, 4096, 128, 128), (4, 0, 4096, 128, 128), (4, 16, -1, 128, 128), (4, 16, 4096, 64, 128),
                  (4, 16, 4096, 128, 96)):
         assert L.la_prefill_varlen_workspace_bytes(*args) == 0
     # the plan follows the current device's SM count (none here): no segments

@@ -273,3 +273,21 @@ def test_varlen_ragged_short_unaligned_state(la, oracle_mod):
     assert y.shape == (total, H, 128) and S.shape == (B, H, 128, 128)
     _check_seqs(oracle_mod, d, (y.float().cpu(), S.cpu(), z.cpu()))
 
+
+@pytest.mark.parametrize("in_place", [False, True])
+def test_varlen_no_tokens(la, in_place):
+    """A packed batch of three empty requests (no tokens at all): every state is
+    handed on unchanged, bit for bit (the walk copies it), in place or not."""
+    B, H = 3, 2
+    g = torch.Generator().manual_seed(82)
+    S0 = (torch.randn(B, H, 128, 128, generator=g) * 0.1).cuda()
+    z0 = (torch.rand(B, H, 128, generator=g) * 10 + 1).cuda()
+    S0c, z0c = S0.clone(), z0.clone()
+    q = torch.empty(0, H, 128, device="cuda", dtype=torch.bfloat16)
+    cu = torch.zeros(B + 1, device="cuda", dtype=torch.int32)
+    kw = dict(S_out=S0, z_out=z0) if in_place else {}
+    y, S, z = la.prefill_varlen(q, q, q, cu, S0=S0, z0=z0, **kw)
+    assert la.last_device_status() == 0
+    assert y.shape == (0, H, 128)
+    assert torch.equal(S.cpu(), S0c.cpu()) and torch.equal(z.cpu(), z0c.cpu())
+
